@@ -1,0 +1,168 @@
+/*
+ * dr.h — C-ABI of libdr: the generalised gated delta-rule recurrence on one
+ * GB300 (sm_103a).
+ *
+ * The operation (Kalman Delta Networks notes, section 1, unified recurrence and
+ * the table under it; Kaczmarz Linear Attention notes, section 1.1 and Eq. (3)):
+ *
+ *     S~_t = D_t S_{t-1}
+ *     e_t  = v_t - S~_t^T k_t
+ *     S_t  = S~_t + w_t e_t^T
+ *     o_t  = S_t^T q_t                       (read after the write)
+ *
+ * S_t is a dk x dv fp32 matrix per (batch, head).  D_t = alpha_t I for GDN, KLA
+ * and PGDN, diag(alpha_t) for Diagonal KDN; alpha = exp(log_alpha).  The write
+ * vector w_t per variant:
+ *
+ *   DR_GDN   w = eta k                        (KLA notes section 1.1)
+ *   DR_KLA   w = eta k / (||k||^2 + eps)      (KLA notes Eq. (3), Algorithm 1)
+ *   DR_PGDN  A_t = alphaP A_{t-1} + betaP (k*k);  r = ln max(A_t, log_floor) - mu;
+ *            B = exp(-ln(x) r / (1 + |r|));  w = eta (B * k)
+ *                                             (Preconditioned DeltaNet notes Eq. (9))
+ *   DR_KDN   p^ = alpha^2 p_{t-1} + omega;  kappa = p^ k / (r + sum p^ k^2);  w = kappa;
+ *            p_t = p^ / (1 + (info_scale / r) k*k p^)
+ *                                             (KDN notes Eqs. (23)-(30), (60)-(65))
+ *
+ * q and k are L2-normalised first when the corresponding flag is set
+ * (q / max(||q||, 1e-30)); KLA reads out with the normalised query (KLA notes
+ * Eq. (3)).  "k" above is then the normalised key everywhere.
+ *
+ * Layouts (row-major, innermost index last):
+ *   q, k     [B, T, H, dk]      v, out [B, T, H, dv]     (decode: T absent)
+ *   log_alpha [B, T, H]  (KDN: [B, T, H, dk])
+ *   eta, alphaP, betaP, r [B, T, H];  omega [B, T, H, dk];  mu [H]
+ *   state    [B, H, dk, dv] fp32;  aux (PGDN A / KDN p) [B, H, dk] fp32
+ * q/k/v/out are fp32 (DR_FP32) or bf16 (DR_BF16); every gate and state is fp32.
+ *
+ * Ownership: the caller owns every buffer; all pointers are device pointers
+ * unless stated otherwise.  The library allocates no device memory and never
+ * synchronises except in dr_get_device_status().  Calls are asynchronous on
+ * `stream` and may be captured in a CUDA graph.
+ *
+ * Errors: argument problems return a negative dr_status before anything is
+ * launched.  A launch failure returns DR_ERR_CUDA.  Problems found on the
+ * device (non-finite values when check_finite is set, a bounded wait that ran
+ * out) set a sticky device status word that dr_get_device_status() returns.
+ * Nothing traps.
+ */
+#ifndef DR_H
+#define DR_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *dr_stream_t;
+
+typedef enum { DR_GDN = 0, DR_KLA = 1, DR_PGDN = 2, DR_KDN = 3 } dr_variant;
+
+typedef enum { DR_FP32 = 0, DR_BF16 = 1 } dr_dtype;
+
+typedef enum {
+  DR_OK = 0,
+  DR_ERR_NULL = -1,        /* a required pointer is NULL                         */
+  DR_ERR_SHAPE = -2,       /* unsupported size (see each call)                   */
+  DR_ERR_DTYPE = -3,       /* dtype not DR_FP32 / DR_BF16                        */
+  DR_ERR_ALIGN = -4,       /* a pointer is not 16-byte aligned                   */
+  DR_ERR_WORKSPACE = -5,   /* workspace missing or too small                     */
+  DR_ERR_CUDA = -6,        /* a CUDA call or launch failed                       */
+  DR_ERR_TIMEOUT = -7,     /* a bounded device-side wait gave up                 */
+  DR_ERR_NONFINITE = -8,   /* check_finite found NaN/Inf in an output            */
+  DR_ERR_UNSUPPORTED = -9, /* variant / option combination not implemented       */
+  DR_ERR_ARG = -10         /* a scalar argument is out of range                  */
+} dr_status;
+
+/* Gate parameters shared by both calls.  Unused fields may be NULL / ignored.
+ * Initialise with dr_params_init() and set what the variant needs. */
+typedef struct dr_params {
+  int dtype;               /* dr_dtype of q, k, v and out                             */
+  int q_l2norm;            /* 1: normalise q before reading out                       */
+  int k_l2norm;            /* 1: normalise k before the residual and the write        */
+  const float *eta;        /* GDN/KLA eta, PGDN beta: [B,T,H] (decode [B,H])          */
+  const float *alphaP;     /* PGDN statistic decay  [B,T,H] (decode [B,H])            */
+  const float *betaP;      /* PGDN statistic gain   [B,T,H] (decode [B,H])            */
+  const float *mu;         /* PGDN per-head centre  [H]                               */
+  float x;                 /* PGDN bound, B in [1/x, x]; default 1.5                  */
+  float log_floor;         /* PGDN guard: ln max(A, log_floor); default 1e-12         */
+  const float *omega;      /* KDN process noise     [B,T,H,dk] (decode [B,H,dk])      */
+  const float *r;          /* KDN observation noise [B,T,H] (decode [B,H]), > 0       */
+  float info_scale;        /* KDN information scaling mu; default 1 (strict update)   */
+  const float *aux_init;   /* dr_chunk_fwd: PGDN A_0 / KDN p_0 [B,H,dk]; NULL => 0 / 1 */
+  float *aux_final;        /* dr_chunk_fwd: final A / p [B,H,dk]; NULL => not written */
+  void *workspace;         /* caller-owned scratch (see dr_chunk_fwd_workspace_bytes) */
+  size_t workspace_bytes;
+  int check_finite;        /* 1: scan outputs/states for NaN/Inf -> DR_ERR_NONFINITE  */
+} dr_params;
+
+/* Fill *p with the defaults above (dtype DR_BF16, x 1.5, log_floor 1e-12,
+ * info_scale 1, everything else 0/NULL). */
+void dr_params_init(dr_params *p);
+
+/*
+ * Chunkwise-parallel forward over a whole sequence (prefill / training forward).
+ *
+ * Computes exactly the recurrence above for t = 1..T from init_state, chunk by
+ * chunk: within a chunk the tokens' mutual dependence is the unit
+ * lower-triangular system [I + L] E = V - (Gamma.K) S_0 with
+ * L_ij = sum_c k_ic w_jc exp(g_ic - g_jc) (j < i), solved on chip, then
+ * O = (Gamma.Q) S_0 + P E and S_out = diag(gamma_C) S_0 + (exp(g_C - g_j).W)^T E
+ * (KLA notes section 2.5, Eqs. (7)-(9), generalised to a write matrix W as in
+ * the Preconditioned DeltaNet notes, section 2.6).  The result is the same as
+ * the tokenwise recurrence up to rounding for any chunk size.
+ *
+ * q, k, v, out     device, dtype gp->dtype, layouts above, 16-byte aligned.
+ * log_alpha        device fp32 [B,T,H] (KDN: [B,T,H,dk]).
+ * gp               host pointer; its device pointers must match the variant.
+ * variant          dr_variant.  eps: KLA stabiliser (>= 0).
+ * init_state       device fp32 [B,H,dk,dv] or NULL (zero state).
+ * final_state      device fp32 [B,H,dk,dv] or NULL (not written).
+ * Sizes: B, H, T >= 1; dk, dv in {64, 128}; chunk in {16, 32, 64, 128}.  T need
+ * not be a multiple of chunk.
+ * Returns DR_OK or a negative dr_status.
+ */
+int dr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                 const dr_params *gp, int variant, float eps,
+                 const float *init_state, void *out, float *final_state,
+                 int B, int T, int H, int dk, int dv, int chunk, dr_stream_t stream);
+
+/*
+ * One tokenwise step for every (batch, head) (decode).  Reads the state once
+ * and writes it once, in place; o = S_t^T q = alpha S^T q + (w^T q) e is formed
+ * from the same read (KLA notes Algorithm 1; PDN notes section 2.5; KDN notes
+ * section 2.2, predict -> gain -> update -> read).
+ *
+ * q, k [B,H,dk]; v, out [B,H,dv] (dtype gp->dtype); log_alpha [B,H] (KDN
+ * [B,H,dk]); gate arrays without the T axis.  state [B,H,dk,dv] fp32 in/out.
+ * aux_state [B,H,dk] fp32 in/out: PGDN A or KDN p (required for those
+ * variants, ignored otherwise).  gp->aux_init/aux_final are ignored.
+ * Sizes: B, H >= 1; dk, dv in {64, 128}.
+ */
+int dr_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,
+                   const dr_params *gp, int variant, float eps,
+                   float *state, float *aux_state, void *out,
+                   int B, int H, int dk, int dv, dr_stream_t stream);
+
+/* Scratch bytes dr_chunk_fwd needs for these sizes (0: no workspace needed). */
+size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H, int dk, int dv,
+                                    int chunk);
+
+/* Synchronises `stream`, returns and clears the sticky device status
+ * (DR_OK, DR_ERR_NONFINITE or DR_ERR_TIMEOUT), or DR_ERR_CUDA. */
+int dr_get_device_status(dr_stream_t stream);
+
+/* Static, NUL-terminated description of a dr_status value. */
+const char *dr_status_string(int status);
+
+/* Name of the kernel path dr_chunk_fwd takes for these arguments
+ * ("tc" tensor-core, "simt" fp32 CUDA cores); static string. */
+const char *dr_chunk_fwd_path(int variant, int dtype, int dk, int dv, int chunk);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DR_H */

@@ -1,0 +1,202 @@
+// decode.cu — one tokenwise step of the recurrence for every (batch, head).
+//
+// Bandwidth-bound: per (b, h) the fp32 state (dk x dv) is read once and written
+// once, everything else is O(dk + dv).  One CTA of 256 threads owns a
+// (b, h, column slice) and holds its slice of S in registers between the read
+// and the write:
+//
+//   1. issue the 128-bit streaming loads of S (they fly while 2-3 run);
+//   2. load q, k, v and the gates; L2-normalise; form the decay d and the write
+//      vector w for the variant (KLA notes Algorithm 1; PDN notes section 2.5,
+//      two states A and S; KDN notes section 2.2, predict -> gain -> update);
+//   3. one pass over S gives both S~^T k and S~^T q (S~ = D S), reduced over
+//      rows with registers + shared memory;
+//   4. e = v - S~^T k;  o = S~^T q + (w^T q) e  (= S_t^T q, read after write);
+//   5. S <- S~ + w e^T, streamed back with 128-bit stores.
+#include "dr_common.cuh"
+
+namespace dr {
+
+namespace {
+
+constexpr int kDecodeThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ float ld_in(const void* p, long i) {
+  return to_f<T>(static_cast<const T*>(p)[i]);
+}
+
+// Block-wide sum of one value per thread (all threads must call).
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kDecodeThreads / 32; ++i) s += red[i];
+  return s;
+}
+
+// DK rows x DVS columns of S per CTA.
+template <int DK, int DVS, typename Tin>
+__global__ void __launch_bounds__(kDecodeThreads) decode_kernel(FwdArgs a) {
+  constexpr int NCG = DVS / 4;            // float4 column groups
+  constexpr int RPW = 32 / NCG;           // rows covered by one warp-wide access
+  constexpr int NROWG = 8 * RPW;          // row groups across the CTA
+  constexpr int NM = DK / NROWG;          // float4 per thread
+  static_assert(NM * NROWG == DK, "tiling");
+
+  __shared__ float s_k[DK], s_q[DK], s_w[DK], s_d[DK];
+  __shared__ float s_v[DVS], s_e[DVS];
+  __shared__ float s_red[kDecodeThreads / 32];
+  __shared__ float4 s_pk[NROWG][NCG], s_pq[NROWG][NCG];
+
+  const int nslice = a.dv / DVS;
+  const int slice = blockIdx.x % nslice;
+  const int bh = blockIdx.x / nslice;
+  const int h = bh % a.H;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cg = lane % NCG, rsub = lane / NCG;
+  const int col0 = slice * DVS + 4 * cg;
+
+  // 1. state slice into registers (streaming: read once)
+  float4* S4 = reinterpret_cast<float4*>(a.S);
+  const long srow0 = (long)bh * DK;
+  float4 s[NM];
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+    const int r = warp * RPW + rsub + NROWG * m;
+    s[m] = __ldcs(S4 + (((srow0 + r) * a.dv + col0) >> 2));
+  }
+
+  // 2. token inputs and gates
+  const long tok = (long)bh;                    // decode layout [B, H, d]
+  float kc = 0.f, qc = 0.f;
+  if (tid < DK) {
+    kc = ld_in<Tin>(a.k, tok * DK + tid);
+    qc = ld_in<Tin>(a.q, tok * DK + tid);
+  }
+  if (tid < DVS) s_v[tid] = ld_in<Tin>(a.v, tok * a.dv + slice * DVS + tid);
+  const float kk = block_sum(kc * kc, s_red);
+  const float qq = block_sum(qc * qc, s_red);
+  if (a.k_l2norm) kc = kc / fmaxf(sqrtf(kk), 1e-30f);
+  if (a.q_l2norm) qc = qc / fmaxf(sqrtf(qq), 1e-30f);
+  const float kk_eff = a.k_l2norm ? block_sum(kc * kc, s_red) : kk;
+
+  float w = 0.f, d = 0.f;
+  if (a.variant == DR_KDN) {
+    float p_hat = 0.f, alpha = 0.f;
+    if (tid < DK) {
+      alpha = expf(a.log_alpha[tok * DK + tid]);
+      p_hat = alpha * alpha * a.aux[tok * DK + tid] + a.omega[tok * DK + tid];
+    }
+    const float z = block_sum(tid < DK ? p_hat * kc * kc : 0.f, s_red);
+    if (tid < DK) {
+      const float rr = a.r[tok];
+      w = p_hat * kc / (rr + z);
+      d = alpha;
+      if (slice == 0) {
+        const float u = (a.info_scale / rr) * kc * kc;
+        a.aux[tok * DK + tid] = p_hat / (1.f + u * p_hat);
+      }
+    }
+  } else if (tid < DK) {
+    d = expf(a.log_alpha[tok]);
+    const float eta = a.eta[tok];
+    if (a.variant == DR_GDN) {
+      w = eta * kc;
+    } else if (a.variant == DR_KLA) {
+      w = eta / (kk_eff + a.eps) * kc;
+    } else {  // DR_PGDN
+      const float A = a.alphaP[tok] * a.aux[tok * DK + tid] + a.betaP[tok] * kc * kc;
+      const float rr = logf(fmaxf(A, a.log_floor)) - a.mu[h];
+      const float sq = rr / (1.f + fabsf(rr));
+      w = eta * expf(-a.ln_x * sq) * kc;
+      if (slice == 0) a.aux[tok * DK + tid] = A;
+    }
+  }
+  if (tid < DK) {
+    s_k[tid] = kc;
+    s_q[tid] = qc;
+    s_w[tid] = w;
+    s_d[tid] = d;
+  }
+  const float wq = block_sum(tid < DK ? w * qc : 0.f, s_red);  // includes a __syncthreads
+
+  // 3. S~^T k and S~^T q partials over this thread's rows
+  float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+    const int r = warp * RPW + rsub + NROWG * m;
+    const float dk_ = s_d[r] * s_k[r], dq_ = s_d[r] * s_q[r];
+    pk.x += s[m].x * dk_; pk.y += s[m].y * dk_; pk.z += s[m].z * dk_; pk.w += s[m].w * dk_;
+    pq.x += s[m].x * dq_; pq.y += s[m].y * dq_; pq.z += s[m].z * dq_; pq.w += s[m].w * dq_;
+  }
+  s_pk[warp * RPW + rsub][cg] = pk;
+  s_pq[warp * RPW + rsub][cg] = pq;
+  __syncthreads();
+
+  // 4. residual and output for this slice's columns
+  if (tid < DVS) {
+    const float* fk = reinterpret_cast<const float*>(&s_pk[0][0]);
+    const float* fq = reinterpret_cast<const float*>(&s_pq[0][0]);
+    float sk = 0.f, sq = 0.f;
+#pragma unroll
+    for (int g = 0; g < NROWG; ++g) {
+      sk += fk[g * DVS + tid];
+      sq += fq[g * DVS + tid];
+    }
+    const float e = s_v[tid] - sk;
+    const float o = sq + wq * e;
+    s_e[tid] = e;
+    static_cast<Tin*>(a.out)[tok * a.dv + slice * DVS + tid] = from_f<Tin>(o);
+    if (a.check_finite && !finite_f(o)) set_status(DR_ERR_NONFINITE);
+  }
+  __syncthreads();
+
+  // 5. S <- D S + w e^T
+  const float4 e4 = make_float4(s_e[4 * cg], s_e[4 * cg + 1], s_e[4 * cg + 2], s_e[4 * cg + 3]);
+  bool bad = false;
+#pragma unroll
+  for (int m = 0; m < NM; ++m) {
+    const int r = warp * RPW + rsub + NROWG * m;
+    const float dr_ = s_d[r], wr = s_w[r];
+    float4 n;
+    n.x = dr_ * s[m].x + wr * e4.x;
+    n.y = dr_ * s[m].y + wr * e4.y;
+    n.z = dr_ * s[m].z + wr * e4.z;
+    n.w = dr_ * s[m].w + wr * e4.w;
+    if (a.check_finite) bad |= !(finite_f(n.x) && finite_f(n.y) && finite_f(n.z) && finite_f(n.w));
+    __stcs(S4 + (((srow0 + r) * a.dv + col0) >> 2), n);
+  }
+  if (bad) set_status(DR_ERR_NONFINITE);
+}
+
+}  // namespace
+
+// Dispatch on (dtype, dk, slice width).  Variants with an aux state (PGDN, KDN)
+// keep one CTA per (b, h) so the in-place aux update is written by the CTA that
+// read it; GDN/KLA split dv = 128 into two slices for more CTAs.
+cudaError_t launch_decode(const FwdArgs& a, int dtype, cudaStream_t st) {
+  const bool split = (a.dv == 128) && (a.variant == DR_GDN || a.variant == DR_KLA);
+  const int dvs = split ? 64 : a.dv;
+  const int grid = a.B * a.H * (a.dv / dvs);
+#define DR_DEC(DK_, DVS_, T_)                                                  \
+  if (a.dk == DK_ && dvs == DVS_) {                                            \
+    decode_kernel<DK_, DVS_, T_><<<grid, kDecodeThreads, 0, st>>>(a);          \
+    return cudaGetLastError();                                                 \
+  }
+  if (dtype == DR_BF16) {
+    DR_DEC(64, 64, __nv_bfloat16) DR_DEC(128, 64, __nv_bfloat16)
+    DR_DEC(64, 128, __nv_bfloat16) DR_DEC(128, 128, __nv_bfloat16)
+  } else {
+    DR_DEC(64, 64, float) DR_DEC(128, 64, float)
+    DR_DEC(64, 128, float) DR_DEC(128, 128, float)
+  }
+#undef DR_DEC
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dr

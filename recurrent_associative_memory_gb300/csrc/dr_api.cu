@@ -1,0 +1,182 @@
+// dr_api.cu — the extern "C" entry points of libdr: argument checks, path
+// selection and launches.  No device memory is allocated here; the only
+// library-owned device storage is the sticky status word below.
+#include <math.h>
+#include <stdint.h>
+
+#include "dr_common.cuh"
+
+namespace dr {
+
+__device__ int g_status = 0;
+
+cudaError_t launch_decode(const FwdArgs& a, int dtype, cudaStream_t st);
+cudaError_t launch_chunk_simt(const FwdArgs& a, int dtype, cudaStream_t st);
+cudaError_t launch_chunk_tc(const FwdArgs& a, cudaStream_t st);
+bool chunk_tc_supported(int variant, int dtype, int dk, int dv, int chunk);
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dim_ok(int d) { return d == 64 || d == 128; }
+
+// Pointers the variant needs, shared by the forward and the decode step.
+int check_gates(const dr_params* gp, int variant) {
+  switch (variant) {
+    case DR_GDN:
+    case DR_KLA:
+      if (!gp->eta) return DR_ERR_NULL;
+      return DR_OK;
+    case DR_PGDN:
+      if (!gp->eta || !gp->alphaP || !gp->betaP || !gp->mu) return DR_ERR_NULL;
+      if (!(gp->x > 1.f) || !(gp->log_floor > 0.f)) return DR_ERR_ARG;
+      return DR_OK;
+    case DR_KDN:
+      if (!gp->omega || !gp->r) return DR_ERR_NULL;
+      if (!(gp->info_scale >= 0.f)) return DR_ERR_ARG;
+      return DR_OK;
+    default:
+      return DR_ERR_UNSUPPORTED;
+  }
+}
+
+FwdArgs make_args(const void* q, const void* k, const void* v, const float* log_alpha,
+                  const dr_params* gp, int variant, float eps, int B, int T, int H, int dk,
+                  int dv, int chunk) {
+  FwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.log_alpha = log_alpha;
+  a.eta = gp->eta;
+  a.alphaP = gp->alphaP;
+  a.betaP = gp->betaP;
+  a.mu = gp->mu;
+  a.omega = gp->omega;
+  a.r = gp->r;
+  a.B = B;
+  a.T = T;
+  a.H = H;
+  a.dk = dk;
+  a.dv = dv;
+  a.chunk = chunk;
+  a.variant = variant;
+  a.q_l2norm = gp->q_l2norm ? 1 : 0;
+  a.k_l2norm = gp->k_l2norm ? 1 : 0;
+  a.check_finite = gp->check_finite ? 1 : 0;
+  a.eps = eps;
+  a.ln_x = variant == DR_PGDN ? logf(gp->x) : 0.f;
+  a.log_floor = gp->log_floor;
+  a.info_scale = gp->info_scale;
+  return a;
+}
+
+}  // namespace
+}  // namespace dr
+
+using namespace dr;
+
+extern "C" {
+
+void dr_params_init(dr_params* p) {
+  if (!p) return;
+  *p = dr_params{};
+  p->dtype = DR_BF16;
+  p->x = 1.5f;
+  p->log_floor = 1e-12f;
+  p->info_scale = 1.f;
+}
+
+const char* dr_status_string(int s) {
+  switch (s) {
+    case DR_OK: return "ok";
+    case DR_ERR_NULL: return "a required pointer is NULL";
+    case DR_ERR_SHAPE: return "unsupported size (B,T,H >= 1; dk,dv in {64,128}; chunk in {16,32,64,128})";
+    case DR_ERR_DTYPE: return "dtype must be DR_FP32 or DR_BF16";
+    case DR_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
+    case DR_ERR_WORKSPACE: return "workspace missing or too small";
+    case DR_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case DR_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+    case DR_ERR_NONFINITE: return "non-finite value in an output or state";
+    case DR_ERR_UNSUPPORTED: return "variant or option combination not supported";
+    case DR_ERR_ARG: return "a scalar argument is out of range";
+    default: return "unknown status";
+  }
+}
+
+size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H, int dk, int dv,
+                                    int chunk) {
+  (void)variant; (void)dtype; (void)B; (void)T; (void)H; (void)dk; (void)dv; (void)chunk;
+  return 0;  // every forward path keeps its intermediates on chip
+}
+
+const char* dr_chunk_fwd_path(int variant, int dtype, int dk, int dv, int chunk) {
+  return chunk_tc_supported(variant, dtype, dk, dv, chunk) ? "tc" : "simt";
+}
+
+int dr_chunk_fwd(const void* q, const void* k, const void* v, const float* log_alpha,
+                 const dr_params* gp, int variant, float eps, const float* init_state,
+                 void* out, float* final_state, int B, int T, int H, int dk, int dv, int chunk,
+                 dr_stream_t stream) {
+  if (!gp || !q || !k || !v || !log_alpha || !out) return DR_ERR_NULL;
+  if (gp->dtype != DR_FP32 && gp->dtype != DR_BF16) return DR_ERR_DTYPE;
+  if (B < 1 || T < 1 || H < 1 || !dim_ok(dk) || !dim_ok(dv)) return DR_ERR_SHAPE;
+  if (chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128) return DR_ERR_SHAPE;
+  if ((long long)B * T * H * (dk > dv ? dk : dv) >= (1LL << 40)) return DR_ERR_SHAPE;
+  if (!(eps >= 0.f)) return DR_ERR_ARG;
+  int st = check_gates(gp, variant);
+  if (st != DR_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      !aligned16(init_state) || !aligned16(final_state) || !aligned16(log_alpha))
+    return DR_ERR_ALIGN;
+
+  FwdArgs a = make_args(q, k, v, log_alpha, gp, variant, eps, B, T, H, dk, dv, chunk);
+  a.S0 = init_state;
+  a.S = final_state;
+  a.aux0 = gp->aux_init;
+  a.aux = gp->aux_final;
+  a.out = out;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err = chunk_tc_supported(variant, gp->dtype, dk, dv, chunk)
+                        ? launch_chunk_tc(a, s)
+                        : launch_chunk_simt(a, gp->dtype, s);
+  return err == cudaSuccess ? DR_OK : DR_ERR_CUDA;
+}
+
+int dr_decode_step(const void* q, const void* k, const void* v, const float* log_alpha,
+                   const dr_params* gp, int variant, float eps, float* state, float* aux_state,
+                   void* out, int B, int H, int dk, int dv, dr_stream_t stream) {
+  if (!gp || !q || !k || !v || !log_alpha || !state || !out) return DR_ERR_NULL;
+  if (gp->dtype != DR_FP32 && gp->dtype != DR_BF16) return DR_ERR_DTYPE;
+  if (B < 1 || H < 1 || !dim_ok(dk) || !dim_ok(dv)) return DR_ERR_SHAPE;
+  if (!(eps >= 0.f)) return DR_ERR_ARG;
+  int st = check_gates(gp, variant);
+  if (st != DR_OK) return st;
+  if ((variant == DR_PGDN || variant == DR_KDN) && !aux_state) return DR_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      !aligned16(state) || !aligned16(aux_state))
+    return DR_ERR_ALIGN;
+  FwdArgs a = make_args(q, k, v, log_alpha, gp, variant, eps, B, 1, H, dk, dv, 0);
+  a.S = state;
+  a.aux = aux_state;
+  a.out = out;
+  cudaError_t err = launch_decode(a, gp->dtype, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? DR_OK : DR_ERR_CUDA;
+}
+
+int dr_get_device_status(dr_stream_t stream) {
+  int h = 0;
+  const int zero = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyFromSymbolAsync(&h, g_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return DR_ERR_CUDA;
+  if (cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) !=
+      cudaSuccess)
+    return DR_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DR_ERR_CUDA;
+  return h;
+}
+
+}  // extern "C"

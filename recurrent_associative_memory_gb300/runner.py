@@ -1,0 +1,65 @@
+"""Call the library on a workload's tensors: output allocation + marshalling.
+
+``chunk_fwd`` and ``decode_step`` take the dict produced by ``workloads``
+(already on the GPU), allocate the outputs with torch and call
+``dr.dr_chunk_fwd`` / ``dr.dr_decode_step``.  They do no arithmetic of their
+own.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import dr
+
+GATE_KEYS = ("log_alpha", "eta", "alphaP", "betaP", "mu", "omega", "r")
+
+
+def to_device(inp: dict, device="cuda") -> dict:
+    """Copy every tensor of an input dict to ``device`` (contiguous)."""
+    return {k: (v.to(device).contiguous() if torch.is_tensor(v) else v) for k, v in inp.items()}
+
+
+def params_for(inp: dict, aux_init=None, aux_final=None, check_finite=False) -> dr.DrParams:
+    dtype = dr.DR_BF16 if inp["q"].dtype == torch.bfloat16 else dr.DR_FP32
+    return dr.make_params(dtype=dtype, q_l2norm=inp.get("q_l2norm", False),
+                          k_l2norm=inp.get("k_l2norm", False), eta=inp.get("eta"),
+                          alphaP=inp.get("alphaP"), betaP=inp.get("betaP"), mu=inp.get("mu"),
+                          x=inp.get("x", 1.5), log_floor=inp.get("log_floor", 1e-12),
+                          omega=inp.get("omega"), r=inp.get("r"),
+                          info_scale=inp.get("info_scale", 1.0), aux_init=aux_init,
+                          aux_final=aux_final, check_finite=check_finite)
+
+
+def chunk_fwd(inp: dict, *, init_state=None, aux_init=None, chunk=None, want_final=True,
+              check_finite=False, stream=None, out=None, final_state=None, aux_final=None):
+    """Run dr_chunk_fwd on a device input dict; returns (out, final_state, aux_final)."""
+    q, k, v = inp["q"], inp["k"], inp["v"]
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    variant = dr.VARIANT_IDS[inp["variant"]]
+    if out is None:
+        out = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
+    if want_final and final_state is None:
+        final_state = torch.empty(B, H, dk, dv, dtype=torch.float32, device=q.device)
+    if want_final and aux_final is None and inp["variant"] in ("pgdn", "kdn"):
+        aux_final = torch.empty(B, H, dk, dtype=torch.float32, device=q.device)
+    p = params_for(inp, aux_init=aux_init, aux_final=aux_final, check_finite=check_finite)
+    st = dr.dr_chunk_fwd(q, k, v, inp["log_alpha"], p, variant, inp.get("eps", 1e-6), init_state,
+                         out, final_state, B, T, H, dk, dv, chunk or inp.get("chunk", 64), stream)
+    dr.check(st, "dr_chunk_fwd")
+    return out, final_state, aux_final
+
+
+def decode_step(inp: dict, state, aux_state=None, out=None, stream=None, check_finite=False):
+    """One dr_decode_step on [B, H, d] device inputs; state/aux updated in place."""
+    q, k, v = inp["q"], inp["k"], inp["v"]
+    B, H, dk = k.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty(B, H, dv, dtype=q.dtype, device=q.device)
+    p = params_for(inp, check_finite=check_finite)
+    st = dr.dr_decode_step(q, k, v, inp["log_alpha"], p, dr.VARIANT_IDS[inp["variant"]],
+                           inp.get("eps", 1e-6), state, aux_state, out, B, H, dk, dv, stream)
+    dr.check(st, "dr_decode_step")
+    return out

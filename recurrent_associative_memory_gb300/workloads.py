@@ -159,7 +159,9 @@ def generate_decode_step(wl: Workload, step: int, variant: str | None = None):
     gen = torch.Generator().manual_seed(wl.seed + step)
     q, k, v = _draw_qkv(gen, wl, wl.B, 1)
     gates = _draw_gates(gen, wl, variant, wl.B, 1)
-    out = dict(q=q[:, 0], k=k[:, 0], v=v[:, 0], variant=variant)
+    out = dict(q=q[:, 0], k=k[:, 0], v=v[:, 0], variant=variant, q_l2norm=wl.q_l2norm,
+               k_l2norm=wl.k_l2norm, eps=wl.eps, x=wl.x, log_floor=wl.log_floor,
+               info_scale=wl.info_scale)
     for name, t in gates.items():
         out[name] = t if name == "mu" else t[:, 0]
     return out

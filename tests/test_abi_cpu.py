@@ -1,0 +1,131 @@
+"""Host-side checks of the C-ABI library (no GPU needed, no kernel launched).
+
+* libdr.so exports every function include/dr.h declares;
+* the ctypes mirror of dr_params has the C compiler's layout;
+* argument validation rejects bad calls before anything reaches CUDA.  Every
+  call here fails validation, so no fake pointer is ever dereferenced.
+"""
+
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dr.h")
+LIB = os.path.join(ROOT, "recurrent_associative_memory_gb300", "libdr.so")
+
+
+@pytest.fixture(scope="module")
+def dr():
+    if not os.path.exists(LIB):
+        from recurrent_associative_memory_gb300 import build
+        build.build()
+    from recurrent_associative_memory_gb300 import dr as mod
+    return mod
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dr_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("dr_chunk_fwd", "dr_decode_step", "dr_chunk_fwd_workspace_bytes",
+              "dr_get_device_status", "dr_status_string", "dr_params_init"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(dr):
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (dr_[a-z0-9_]+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    lib = ctypes.CDLL(LIB)
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_params_struct_layout_matches_c(dr):
+    fields = [f for f, _ in dr.DrParams._fields_]
+    src = "#include <stdio.h>\n#include <stddef.h>\n#include \"dr.h\"\nint main(void){\n"
+    src += 'printf("%zu\\n", sizeof(dr_params));\n'
+    for f in fields:
+        src += f'printf("%zu\\n", offsetof(dr_params, {f}));\n'
+    src += "return 0;}\n"
+    with tempfile.TemporaryDirectory() as td:
+        c = os.path.join(td, "layout.c")
+        exe = os.path.join(td, "layout")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-std=c99", "-I", os.path.dirname(HEADER), c, "-o", exe], check=True)
+        vals = [int(x) for x in subprocess.run([exe], capture_output=True, text=True,
+                                               check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(dr.DrParams)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(dr.DrParams, f).offset == off, f
+
+
+def test_params_defaults(dr):
+    p = dr.dr_params_init()
+    assert p.dtype == dr.DR_BF16 and p.x == pytest.approx(1.5) and p.info_scale == 1.0
+    assert p.log_floor == pytest.approx(1e-12) and not p.eta and not p.check_finite
+
+
+def test_status_strings(dr):
+    for code in dr.STATUS:
+        s = dr.dr_status_string(code)
+        assert isinstance(s, str) and s
+    assert dr.dr_status_string(12345) == "unknown status"
+    assert dr.dr_chunk_fwd_workspace_bytes(1, 1, 8, 2048, 8, 128, 128, 64) == 0
+    assert dr.dr_chunk_fwd_path(dr.DR_KLA, dr.DR_FP32, 64, 64, 64) == "simt"
+
+
+A = 1 << 20          # a 16-byte aligned address that is never dereferenced
+MIS = A + 4          # misaligned
+
+
+def fwd(dr, variant=1, q=A, k=A, v=A, la=A, out=A, init=None, fin=None, B=1, T=8, H=1, dk=64,
+        dv=64, chunk=64, eps=1e-6, **pk):
+    p = dr.make_params(**{"dtype": dr.DR_FP32, "eta": A, **pk})
+    return dr.dr_chunk_fwd(q, k, v, la, p, variant, eps, init, out, fin, B, T, H, dk, dv, chunk,
+                           stream=0)
+
+
+def test_chunk_fwd_rejects_bad_arguments(dr):
+    assert fwd(dr, q=None) == dr.DR_ERR_NULL
+    assert fwd(dr, out=None) == dr.DR_ERR_NULL
+    assert fwd(dr, eta=None) == dr.DR_ERR_NULL
+    assert fwd(dr, variant=2) == dr.DR_ERR_NULL                # PGDN without alphaP/betaP/mu
+    assert fwd(dr, variant=3) == dr.DR_ERR_NULL                # KDN without omega/r
+    assert fwd(dr, variant=7) == dr.DR_ERR_UNSUPPORTED
+    assert fwd(dr, dtype=5) == dr.DR_ERR_DTYPE
+    assert fwd(dr, dk=96) == dr.DR_ERR_SHAPE
+    assert fwd(dr, dv=32) == dr.DR_ERR_SHAPE
+    assert fwd(dr, T=0) == dr.DR_ERR_SHAPE
+    assert fwd(dr, B=0) == dr.DR_ERR_SHAPE
+    assert fwd(dr, chunk=48) == dr.DR_ERR_SHAPE
+    assert fwd(dr, eps=-1.0) == dr.DR_ERR_ARG
+    assert fwd(dr, variant=2, alphaP=A, betaP=A, mu=A, x=1.0) == dr.DR_ERR_ARG
+    assert fwd(dr, variant=3, omega=A, r=A, info_scale=-1.0) == dr.DR_ERR_ARG
+    assert fwd(dr, q=MIS) == dr.DR_ERR_ALIGN
+    assert fwd(dr, fin=MIS) == dr.DR_ERR_ALIGN
+    assert fwd(dr, init=MIS) == dr.DR_ERR_ALIGN
+
+
+def test_decode_rejects_bad_arguments(dr):
+    def dec(variant=1, state=A, aux=None, dk=64, **pk):
+        p = dr.make_params(**{"dtype": dr.DR_FP32, "eta": A, **pk})
+        return dr.dr_decode_step(A, A, A, A, p, variant, 1e-6, state, aux, A, 1, 1, dk, 64,
+                                 stream=0)
+    assert dec(state=None) == dr.DR_ERR_NULL
+    assert dec(variant=2, alphaP=A, betaP=A, mu=A) == dr.DR_ERR_NULL   # aux state required
+    assert dec(variant=3, omega=A, r=A) == dr.DR_ERR_NULL
+    assert dec(dk=32) == dr.DR_ERR_SHAPE
+    assert dec(state=MIS) == dr.DR_ERR_ALIGN
+    assert dec(dtype=2) == dr.DR_ERR_DTYPE
