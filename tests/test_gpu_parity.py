@@ -213,3 +213,24 @@ def test_check_finite_reports_nonfinite(rt):
     inp["v"][0, 5, 0, 3] = 0.0
     runner.chunk_fwd(runner.to_device(inp), check_finite=True)
     assert dr.dr_get_device_status() == 0
+
+
+# ------------------------------------------------------------ tensor-core path specifics
+
+@pytest.mark.parametrize("variant", ["gdn", "kla", "pgdn"])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 333])
+def test_tc_path_ragged_with_state(rt, variant, T):
+    """bf16, dk = dv = 128, chunk 64 runs on the tcgen05 kernel: ragged tails,
+    nonzero initial state and aux state."""
+    dr, runner = rt
+    assert dr.dr_chunk_fwd_path(dr.VARIANT_IDS[variant], dr.DR_BF16, 128, 128, 64) == "tc"
+    inp = small_inputs(variant, "bf16", B=2, T=T, H=3, seed=100 + T)
+    S0, aux0 = random_state(inp, seed=T)
+    check_fwd(rt, inp, S0, aux0)
+
+
+def test_tc_path_unnormalised_gdn_strong_keys(rt):
+    """GDN on raw keys with energy spread ~10x (the unstable corner of the
+    workload family): the state grows large but stays finite."""
+    inp = small_inputs("gdn", "bf16", B=1, T=512, H=4, seed=77)
+    check_fwd(rt, inp)
