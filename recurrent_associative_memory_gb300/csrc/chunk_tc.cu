@@ -36,7 +36,7 @@ namespace {
 using namespace umma;
 
 constexpr int kTcThreads = 256;
-constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint64_t kWaitLimit = 2000000000ull;   // 2 s per bounded wait
 
 // shared-memory map (bytes from a 1024-aligned base).  The raw bf16 input tiles
 // are never modified: every per-token scale is folded into an operand computed
@@ -52,7 +52,8 @@ constexpr uint32_t oE = oP + 16384;             // E hi | E lo | uE hi | uE lo  
 constexpr uint32_t oW = oE + 32768;             // PGDN write keys [64][128]       16 KB
 constexpr uint32_t oVec = oW + 16384;           // per-token vectors + scratch      8 KB
 constexpr uint32_t kSmemBytes = oVec + 8192 + 1024;   // + alignment slack
-constexpr int LDL = 65;                         // fp32 L/T row stride (aliases oE)
+constexpr int LDL = 68;                         // fp32 L/T row stride (aliases oE)
+constexpr int LDX = 36;                         // fp32 scratch row stride (after L/T in oE)
 
 // tensor-memory columns
 constexpr uint32_t cGram = 0;    // M=128 x 64
@@ -69,10 +70,10 @@ constexpr uint32_t ID_N64 = idesc_bf16(64, 64, 0, 1);
 constexpr uint32_t ID_ENEG = idesc_bf16(64, 64, 0, 1, 1);
 constexpr uint32_t ID_DS = idesc_bf16(128, 64, 1, 1);
 
+// two floats -> packed bf16x2 (round to nearest even), one conversion instruction
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-  return a | (b << 16);
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // 8 consecutive bf16 (one 16-byte chunk) -> float
@@ -90,16 +91,74 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
                     pack_bf16(f[6], f[7]));
 }
 
-// hi = bf16(x), lo = bf16(x - hi), 8 values
+// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi), 8 values, packed conversions
 __device__ __forceinline__ void split8(const float (&x)[8], uint4& hi, uint4& lo) {
-  float hv[8], lv[8];
+  uint32_t h[4], l[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    hv[i] = __bfloat162float(__float2bfloat16_rn(x[i]));
-    lv[i] = x[i] - hv[i];
+  for (int i = 0; i < 4; ++i) {
+    h[i] = pack_bf16(x[2 * i], x[2 * i + 1]);
+    const float r0 = x[2 * i] - __uint_as_float(h[i] << 16);
+    const float r1 = x[2 * i + 1] - __uint_as_float(h[i] & 0xFFFF0000u);
+    l[i] = pack_bf16(r0, r1);
   }
-  hi = pack8(hv);
-  lo = pack8(lv);
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// ---- warp-level tensor-core products for the 16/32-row blocks of the triangular
+// inverse (below tcgen05's minimum M).  m16n8k8 TF32 with each operand split into
+// two TF32 terms (a = a_hi + a_lo) and three products, which keeps fp32 accuracy.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32"
+      " {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// D (16 x 8 tile, fp32 fragment) += A[m0.., k0..k0+K) * B[k0.., n0..] over K in steps of 8.
+// A, B are fp32 row-major in shared memory with leading dimensions lda, ldb.
+template <int KSTEPS>
+__device__ __forceinline__ void tile_mm3(float (&d)[4], const float* A, int lda, const float* B,
+                                         int ldb, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int ks = 0; ks < KSTEPS; ++ks) {
+    const float* a = A + 8 * ks;
+    const float* bb = B + 8 * ks * ldb;
+    const float af[4] = {a[g * lda + t], a[(g + 8) * lda + t], a[g * lda + t + 4],
+                         a[(g + 8) * lda + t + 4]};
+    const float bf[2] = {bb[t * ldb + g], bb[(t + 4) * ldb + g]};
+    uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      ah[i] = to_tf32(af[i]);
+      al[i] = to_tf32(af[i] - __uint_as_float(ah[i]));
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      bh[i] = to_tf32(bf[i]);
+      bl[i] = to_tf32(bf[i] - __uint_as_float(bh[i]));
+    }
+    mma_tf32(d, al, bh);
+    mma_tf32(d, ah, bl);
+    mma_tf32(d, ah, bh);
+  }
+}
+
+// store a 16 x 8 fp32 fragment (scaled by s) at C[m0.., n0..]
+__device__ __forceinline__ void tile_store(float* C, int ldc, const float (&d)[4], float s, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  C[g * ldc + 2 * t] = s * d[0];
+  C[g * ldc + 2 * t + 1] = s * d[1];
+  C[(g + 8) * ldc + 2 * t] = s * d[2];
+  C[(g + 8) * ldc + 2 * t + 1] = s * d[3];
 }
 
 __device__ __forceinline__ void ld32cols(uint32_t taddr, float (&v)[32]) {
@@ -147,9 +206,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float* vbP = vaP + 64;
   float* vkk = vbP + 64;
   float* vqq = vkk + 64;
-  float* vmisc = vqq + 64;  // [0] = gamma_C
-  float* Xtmp = vg + 1024;  // 768 floats of inversion scratch
+  float* vF = vqq + 64;     // e^{g_e(J) - g_j}: decay from token j to the end of its 16-block
+  float* vmisc = vF + 64;   // [0] = gamma_C
   float* LT = reinterpret_cast<float*>(sm + oE);     // L, inverted in place into T (fp32)
+  float* XS = LT + 64 * LDL;                         // 32 x LDX fp32 scratch for the inverse
 
   if (tid == 0) {
     mbar_init(&bar_kq[0], 1);
@@ -215,10 +275,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   fence_proxy_async();
   __syncthreads();
 
+  // gates of the next chunk, prefetched into registers one chunk ahead (thread i < 64 = token i)
+  float nla = 0.f, neta = 0.f, naP = 1.f, nbP = 0.f;
+  auto prefetch_gates = [&](int c) {
+    const int i = tid, t = c * 64 + i;
+    if (i < 64 && t < a.T) {
+      const long ti = ((long)b * a.T + t) * a.H + h;
+      nla = a.log_alpha[ti];
+      neta = a.eta[ti];
+      if (kPgdn) {
+        naP = a.alphaP[ti];
+        nbP = a.betaP[ti];
+      }
+    } else {
+      nla = 0.f; neta = 0.f; naP = 1.f; nbP = 0.f;
+    }
+  };
+  prefetch_gates(0);
+
   uint32_t mma_phase = 0;
   bool bad = false;
+  volatile int* abort_flag = &s_abort;
   auto wait_mma = [&]() {
-    if (!mbar_wait(&bar_mma, mma_phase, kWaitLimit)) s_abort = 1;
+    if (!*abort_flag && !mbar_wait(&bar_mma, mma_phase, kWaitLimit)) *abort_flag = 1;
     mma_phase ^= 1;
     tc_fence_after();
   };
@@ -237,15 +316,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---------------- 1. gates, norms, write coefficients
     if (tid < 64) {
       const int i = tid;
-      const bool real = i < Cc;
-      const long ti = real ? ((long)b * a.T + t0 + i) * a.H + h : 0;
-      vla[i] = real ? a.log_alpha[ti] : 0.f;
-      veta[i] = real ? a.eta[ti] : 0.f;
+      vla[i] = nla;
+      veta[i] = neta;
       if (kPgdn) {
-        vaP[i] = real ? a.alphaP[ti] : 1.f;
-        vbP[i] = real ? a.betaP[ti] : 0.f;
+        vaP[i] = naP;
+        vbP[i] = nbP;
       }
     }
+    if (c + 1 < NC) prefetch_gates(c + 1);
     {  // squared norms of k and q rows: 4 threads per row, 32 elements each
       const int i = tid >> 2, part = tid & 3, kb = part >> 1, c0 = (part & 1) * 32;
       float kk = 0.f, qq = 0.f;
@@ -298,6 +376,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       vks[i] = eg * cr;
       vqs[i] = eg * qn;
       vu[i] = __expf(gC - gi) * coef;
+      vF[i] = __expf(vg[i | 15] - gi);
       if (i == 0) vmisc[0] = __expf(gC);
     }
     __syncthreads();
@@ -306,15 +385,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (tid < 128) {
         const int ch = tid, kb = ch >> 6, col = ch & 63;
         float A = carryA;
-        for (int i = 0; i < 64; ++i) {
-          const float kv = __bfloat162float(
-              *reinterpret_cast<const __nv_bfloat16*>(KQ + kb * 16384 + sw128_offset(i, col))) * vcr[i];
-          A = vaP[i] * A + vbP[i] * kv * kv;
-          const float rr = __logf(fmaxf(A, a.log_floor)) - mu_h;
-          const float sq = rr / (1.f + fabsf(rr));
-          const float w = veta[i] * __expf(-a.ln_x * sq) * kv;
-          *reinterpret_cast<__nv_bfloat16*>(Wt + kb * 8192 + sw128_offset(i, col)) =
-              __float2bfloat16_rn(w);
+        for (int i0 = 0; i0 < 64; i0 += 8) {
+          float kv[8], Av[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            kv[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                        KQ + kb * 16384 + sw128_offset(i0 + e, col))) * vcr[i0 + e];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            A = vaP[i0 + e] * A + vbP[i0 + e] * kv[e] * kv[e];
+            Av[e] = A;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float rr = __logf(fmaxf(Av[e], a.log_floor)) - mu_h;
+            const float sq = __fdividef(rr, 1.f + fabsf(rr));
+            const float w = veta[i0 + e] * __expf(-a.ln_x * sq) * kv[e];
+            *reinterpret_cast<__nv_bfloat16*>(Wt + kb * 8192 + sw128_offset(i0 + e, col)) =
+                __float2bfloat16_rn(w);
+          }
         }
         carryA = A;
       }
@@ -339,39 +428,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     wait_mma();
 
     // ---------------- 3. Gram readout: L (fp32, in the E area) and P (bf16 hi/lo)
-    if (warp < 4) {
-      const int row = tid;  // lane of the M=128 accumulator
-      float gv[64];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        float t16[16];
-        tmem_ld16(tmem + lane_off + cGram + 16 * m, t16);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) gv[16 * m + e] = t16[e];
-      }
+    // warp (quad, chalf) reads rows 32 quad.. and columns 32 chalf..; decay factors:
+    // same 16-block: e^{g_i - g_j} directly; earlier block J: e^{g_i - g_e(J)} e^{g_e(J) - g_j}.
+    {
+      const int row = quad * 32 + lane;          // lane of the M=128 accumulator
+      const int i = row & 63, I = i >> 4;
+      float gv[32];
+      ld32cols(tmem + lane_off + cGram + chalf * 32, gv);
       tmem_ld_wait();
-      if (row < 64) {
-        const int i = row;
-        const float gi = vg[i], ci = vcr[i];
+      const float gi = vg[i];
+      const float rs = (row < 64) ? vcr[i] : vqn[i];
+      float fb[2];
 #pragma unroll
-        for (int j = 0; j < 64; ++j)
-          LT[i * LDL + j] = (j < i) ? gv[j] * ci * va[j] * __expf(gi - vg[j]) : 0.f;
+      for (int jb = 0; jb < 2; ++jb) {
+        const int J = chalf * 2 + jb;
+        fb[jb] = (J < I) ? __expf(gi - vg[16 * J + 15]) : 0.f;
+      }
+      float x[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int j = chalf * 32 + e, J = j >> 4;
+        const float ed = __expf(fminf(gi - vg[j], 0.f));          // same 16-block
+        const float f = (J < I) ? fb[e >> 4] * vF[j] : ((J == I && j <= i) ? ed : 0.f);
+        x[e] = gv[e] * rs * va[j] * f;
+      }
+      if (row < 64) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int j = chalf * 32 + e;
+          LT[i * LDL + j] = (j < i) ? x[e] : 0.f;
+        }
       } else {
-        const int i = row - 64;
-        const float gi = vg[i], qi = vqn[i];
         uint8_t* Pt = sm + oP;
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          float x[8];
+        for (int m = 0; m < 4; ++m) {
+          float y[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = 8 * m + e;
-            x[e] = (j <= i) ? gv[j] * qi * va[j] * __expf(gi - vg[j]) : 0.f;
-          }
+          for (int e = 0; e < 8; ++e) y[e] = x[8 * m + e];
           uint4 hi, lo;
-          split8(x, hi, lo);
-          *reinterpret_cast<uint4*>(Pt + sw128_offset(i, 8 * m)) = hi;
-          *reinterpret_cast<uint4*>(Pt + 8192 + sw128_offset(i, 8 * m)) = lo;
+          split8(y, hi, lo);
+          *reinterpret_cast<uint4*>(Pt + sw128_offset(i, chalf * 32 + 8 * m)) = hi;
+          *reinterpret_cast<uint4*>(Pt + 8192 + sw128_offset(i, chalf * 32 + 8 * m)) = lo;
         }
       }
     }
@@ -399,24 +496,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     __syncthreads();
-    for (int I = 1; I < 4; ++I) {  // row block I: X_J = sum_{K=J}^{I-1} L_IK T_KJ, then T_IJ = -T_II X_J
-      for (int e = tid; e < I * 256; e += kTcThreads) {
-        const int J = e >> 8, ii = (e >> 4) & 15, jj = e & 15;
-        const int gi = 16 * I + ii, gj = 16 * J + jj;
-        float s = 0.f;
-        for (int l = 16 * J; l < 16 * I; ++l) s += LT[gi * LDL + l] * LT[l * LDL + gj];
-        Xtmp[e] = s;
-      }
-      __syncthreads();
-      for (int e = tid; e < I * 256; e += kTcThreads) {
-        const int J = e >> 8, ii = (e >> 4) & 15, jj = e & 15;
-        const int gi = 16 * I + ii, gj = 16 * J + jj;
-        float s = 0.f;
-        for (int ll = 0; ll <= ii; ++ll) s += LT[gi * LDL + 16 * I + ll] * Xtmp[J * 256 + ll * 16 + jj];
-        LT[gi * LDL + gj] = -s;
-      }
-      __syncthreads();
+    // level 1: T_10 = -T_11 (L_10 T_00) and T_32 = -T_33 (L_32 T_22); warp w < 4 owns
+    // (block w >> 1, 8-column tile w & 1).  Level 2: rows 32-63 x cols 0-31,
+    // T_C = -T_B (L_C T_A), one 16 x 8 output tile per warp.  (TF32 x3 products.)
+    if (warp < 4) {
+      const int blk = warp >> 1, nt = warp & 1;
+      const int r0 = 32 * blk + 16, c0 = 32 * blk;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      tile_mm3<2>(d, LT + r0 * LDL + c0, LDL, LT + c0 * LDL + c0 + 8 * nt, LDL, lane);
+      tile_store(XS + 16 * blk * LDX + 8 * nt, LDX, d, 1.f, lane);
     }
+    __syncthreads();
+    if (warp < 4) {
+      const int blk = warp >> 1, nt = warp & 1;
+      const int r0 = 32 * blk + 16, c0 = 32 * blk;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      tile_mm3<2>(d, LT + r0 * LDL + r0, LDL, XS + 16 * blk * LDX + 8 * nt, LDX, lane);
+      tile_store(LT + r0 * LDL + c0 + 8 * nt, LDL, d, -1.f, lane);
+    }
+    __syncthreads();
+    {
+      const int mt = warp >> 2, nt = warp & 3;       // 2 x 4 tiles of 16 x 8
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      tile_mm3<4>(d, LT + (32 + 16 * mt) * LDL, LDL, LT + 8 * nt, LDL, lane);   // X = L_C T_A
+      tile_store(XS + 16 * mt * LDX + 8 * nt, LDX, d, 1.f, lane);
+    }
+    __syncthreads();
+    {
+      const int mt = warp >> 2, nt = warp & 3;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      if (mt == 0)   // T_B is lower triangular: rows 32-47 only need columns 32-47
+        tile_mm3<2>(d, LT + 32 * LDL + 32, LDL, XS + 8 * nt, LDX, lane);
+      else
+        tile_mm3<4>(d, LT + 48 * LDL + 32, LDL, XS + 8 * nt, LDX, lane);
+      __syncthreads();   // every read of L_C (in X) is done; overwrite it with T_C
+      tile_store(LT + (32 + 16 * mt) * LDL + 8 * nt, LDL, d, -1.f, lane);
+    }
+    __syncthreads();
     {  // T and Ts = T diag(ks) -> bf16 hi/lo, K-major [64 rows][64]
       const int i = tid >> 2, c0 = (tid & 3) * 16;
       uint8_t* Tt = sm + oT;
@@ -443,7 +559,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
 
     // ---------------- 5. MMA 2: W' = Ts K (N = 128),  U' = T V (N = 64); hi + lo along K
-    if (!mbar_wait(&bar_v, c & 1, kWaitLimit)) s_abort = 1;
+    if (!*abort_flag && !mbar_wait(&bar_v, c & 1, kWaitLimit)) *abort_flag = 1;
     if (tid == 0) {
       tc_fence_after();
       const uint32_t tb = smem_u32(sm + oT), kq = smem_u32(KQ), vt = smem_u32(sm + oV);
@@ -612,8 +728,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     set_status(DR_ERR_TIMEOUT);
     // let any TMA still in flight land before the CTA exits
     if (tid == 0) {
-      mbar_wait(&bar_kq[0], 0, 1024);
-      mbar_wait(&bar_v, 0, 1024);
+      mbar_wait(&bar_kq[0], 0, kWaitLimit / 4);
+      mbar_wait(&bar_v, 0, kWaitLimit / 4);
     }
   }
   if (bad) set_status(DR_ERR_NONFINITE);
