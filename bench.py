@@ -61,6 +61,37 @@ def parse():
     return p.parse_args()
 
 
+KERNEL_SOURCES = {
+    "chunk_tc": ["chunk_tc.cu", "umma.cuh", "dr_common.cuh"],
+    "chunk_simt": ["chunk_simt.cu", "dr_common.cuh"],
+    "decode": ["decode.cu", "dr_common.cuh"],
+}
+
+
+def source_hash(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "recurrent_associative_memory_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel, workload, variant=None):
+    """DRAM bytes per launch from the ncu capture recorded in profiles/traffic.json,
+    or None when there is none or the kernel source changed since the capture."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(kernel)
+    except Exception:
+        return None
+    if not rec or rec.get("source_sha256") != source_hash(kernel):
+        return None
+    if rec.get("workload") != workload or (variant and rec.get("variant") != variant):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -342,8 +373,10 @@ def main():
     dom = max(variants, key=lambda v: var_stats[v]["ms"])
     byt = fwd_bytes(wl, dom)
     ach = byt / (var_stats[dom]["ms"] / 1e3) / 1e9
+    kname = "chunk_tc" if var_stats[dom]["path"] == "tc" else "chunk_simt"
     roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
-            "frac": ach / pk["hbm_gbs"], "traffic": None, "kernel": f"chunk fwd ({dom})",
+            "frac": ach / pk["hbm_gbs"], "traffic": measured_traffic(kname, wl.name, dom),
+            "kernel": f"{kname} ({dom})",
             "algorithmic_bytes_per_launch": byt, "peak_source": pk["src"]}
 
     result = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -379,6 +412,7 @@ def main():
         result["decode"] = {"workload": dwl.name, "B": dwl.B, "H": dwl.H, "d": dwl.dk,
                             "ms_per_step": ms, "gbs": gbs, "frac": gbs / pk["hbm_gbs"],
                             "algorithmic_bytes_per_step": db, "steps": args.decode_steps,
+                            "traffic": measured_traffic("decode", dwl.name),
                             "tokens_per_s": dwl.B / (ms / 1e3), "launches": args.decode_steps}
 
     # ---- end to end through the public API with pinned host buffers

@@ -128,6 +128,7 @@ template <int KSTEPS>
 __device__ __forceinline__ void tile_mm3(float (&d)[4], const float* A, int lda, const float* B,
                                          int ldb, int lane) {
   const int g = lane >> 2, t = lane & 3;
+  float dc[4] = {0.f, 0.f, 0.f, 0.f};   // correction terms, an independent accumulation chain
 #pragma unroll
   for (int ks = 0; ks < KSTEPS; ++ks) {
     const float* a = A + 8 * ks;
@@ -146,10 +147,12 @@ __device__ __forceinline__ void tile_mm3(float (&d)[4], const float* A, int lda,
       bh[i] = to_tf32(bf[i]);
       bl[i] = to_tf32(bf[i] - __uint_as_float(bh[i]));
     }
-    mma_tf32(d, al, bh);
-    mma_tf32(d, ah, bl);
+    mma_tf32(dc, al, bh);
+    mma_tf32(dc, ah, bl);
     mma_tf32(d, ah, bh);
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] += dc[i];
 }
 
 // store a 16 x 8 fp32 fragment (scaled by s) at C[m0.., n0..]
