@@ -14,6 +14,8 @@ cudaError_t launch_decode(const FwdArgs& a, int dtype, cudaStream_t st);
 cudaError_t launch_chunk_simt(const FwdArgs& a, int dtype, cudaStream_t st);
 cudaError_t launch_chunk_tc(const FwdArgs& a, cudaStream_t st);
 bool chunk_tc_supported(int variant, int dtype, int dk, int dv, int chunk);
+cudaError_t launch_chunk_tc_ws(const FwdArgs& a, cudaStream_t st);
+bool chunk_tc_ws_supported(int variant, int dtype, int dk, int dv, int chunk);
 
 namespace {
 
@@ -138,9 +140,13 @@ int dr_chunk_fwd(const void* q, const void* k, const void* v, const float* log_a
   a.aux = gp->aux_final;
   a.out = out;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t err = chunk_tc_supported(variant, gp->dtype, dk, dv, chunk)
-                        ? launch_chunk_tc(a, s)
-                        : launch_chunk_simt(a, gp->dtype, s);
+  cudaError_t err;
+  if (chunk_tc_ws_supported(variant, gp->dtype, dk, dv, chunk))
+    err = launch_chunk_tc_ws(a, s);          // GDN / KLA: warp-specialised tensor-core kernel
+  else if (chunk_tc_supported(variant, gp->dtype, dk, dv, chunk))
+    err = launch_chunk_tc(a, s);             // PGDN: phase-sequential tensor-core kernel
+  else
+    err = launch_chunk_simt(a, gp->dtype, s);
   return err == cudaSuccess ? DR_OK : DR_ERR_CUDA;
 }
 
