@@ -39,9 +39,12 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return s;
 }
 
-// DK rows x DVS columns of S per CTA.
+// DK rows x DVS columns of S per CTA.  Slices of up to 128 x 64 keep 32 state
+// values per thread, so four CTAs share an SM (more state bytes in flight);
+// full 128 x 128 slices keep 64 and run two per SM.
 template <int DK, int DVS, typename Tin>
-__global__ void __launch_bounds__(kDecodeThreads) decode_kernel(FwdArgs a) {
+__global__ void __launch_bounds__(kDecodeThreads, (DK * DVS <= 8192) ? 4 : 2)
+    decode_kernel(FwdArgs a) {
   constexpr int NCG = DVS / 4;            // float4 column groups
   constexpr int RPW = 32 / NCG;           // rows covered by one warp-wide access
   constexpr int NROWG = 8 * RPW;          // row groups across the CTA
