@@ -4,17 +4,17 @@
 // Same chunk algebra as chunk_tc.cu (KLA notes section 2.5, Eqs. (7)-(9), with a
 // general write matrix as in the PDN notes section 2.6), reorganised so that
 // the chunk-local preparation of chunk c+1 runs concurrently with the state
-// carry of chunk c.  One CTA per (b, h, 64-column half of dv); 17 warps:
+// carry of chunk c.  One CTA per (b, h, 64-column half of dv); 13 warps:
 //
-//   chain  (warps 0-7)   state carry of chunk c: E = U' - W' S readout as bf16
+//   chain  (warps 0-3)   state carry of chunk c: E = U' - W' S readout as bf16
 //                        hi/lo tiles, then S <- gamma_C S + dS and the output
 //                        o = e^g qn . QS + PE.  The fp32 state slice (128 x 64)
 //                        lives in these warps' registers.
-//   prep   (warps 8-15)  chunk c+1: gates, norms and write coefficients; the
+//   prep   (warps 4-11)  chunk c+1: gates, norms and write coefficients; the
 //                        Gram readout into L (fp32) and P (bf16 hi/lo); the
 //                        block inverse T = (I + L)^-1; T and T diag(e^g c) as
 //                        bf16 hi/lo tiles; W' readout.
-//   issue  (warp 16)     one lane issues every TMA load and tcgen05 MMA in the
+//   issue  (warp 12)     one lane issues every TMA load and tcgen05 MMA in the
 //                        order M2(c), G(c+1), M3(c), M4(c):
 //                          G   Gram [K; Q] K^T                      (M=128)
 //                          M2  W' = (T diag(e^g c)) K,  U' = T V    (M=64)
@@ -36,7 +36,7 @@ namespace {
 using namespace umma;
 using namespace tc;
 
-constexpr int kWsThreads = 17 * 32;
+constexpr int kWsThreads = 13 * 32;
 constexpr uint64_t kWsWait = 2000000000ull;   // 2 s per bounded wait
 
 // shared-memory map (bytes from a 1024-aligned base)
@@ -140,36 +140,39 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     return ok;
   };
 
-  if (warp < 8) {
+  if (warp < 4) {
     // =====================================================================================
-    // chain group: warps 0-7.  Thread = row r of the state slice (quadrant = warp & 3),
-    // warpgroup = 32-column half of the 64 columns.
-    const int quad = warp & 3, chalf = warp >> 2;
-    const int srow = quad * 32 + lane;
+    // chain group: warps 0-3.  Thread = row r of the state slice (TMEM lane r), all 64 columns.
+    const int quad = warp;
+    const int srow = tid;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const bool leader = (tid == 0);
-    float S[32];
+    float S[64];
     auto store_state_tiles = [&]() {
       uint8_t* sS = sm + wS;
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
+      for (int m = 0; m < 8; ++m) {
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = S[8 * m + e];
         uint4 hi, lo;
         split8(x, hi, lo);
-        *reinterpret_cast<uint4*>(sS + sw128_offset(srow, chalf * 32 + 8 * m)) = hi;
-        *reinterpret_cast<uint4*>(sS + 16384 + sw128_offset(srow, chalf * 32 + 8 * m)) = lo;
+        *reinterpret_cast<uint4*>(sS + sw128_offset(srow, 8 * m)) = hi;
+        *reinterpret_cast<uint4*>(sS + 16384 + sw128_offset(srow, 8 * m)) = lo;
       }
     };
     {
-      const long base = ((long)bh * 128 + srow) * a.dv + half * 64 + chalf * 32;
+      const long base = ((long)bh * 128 + srow) * a.dv + half * 64;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) S[j] = a.S0 ? a.S0[base + j] : 0.f;
+      for (int j = 0; j < 64; j += 4) {
+        const float4 v = a.S0 ? *reinterpret_cast<const float4*>(a.S0 + base + j)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
+      }
       store_state_tiles();
     }
     fence_proxy_async();
-    named_bar(1, 256);
+    named_bar(1, 128);
     if (leader) mbar_arrive(&bars[B_SREADY]);   // S tiles of chunk 0
     bool bad = false;
 
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       const float* vqs = vslot + slot * 192;
       const float* vu = vqs + 64;
       const int t0 = c * 64, Cc = min(64, a.T - t0);
-      if (!group_wait(0, 1, 256, &bars[B_M3], c & 1, leader)) break;
+      if (!group_wait(0, 1, 128, &bars[B_M3], c & 1, leader)) break;
       tc_fence_after();
       // E (M=64 layout: rows on lanes 0-15 of each quadrant) -> E and u.E hi/lo tiles
       {
@@ -186,44 +189,44 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         const float u = vu[i & 63];
         uint8_t* Et = sm + wE;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
+        for (int hf = 0; hf < 4; ++hf) {
           float ev[16];
-          tmem_ld16(tmem + lane_off + tE0 + slot * 64 + chalf * 32 + 16 * hf, ev);
+          tmem_ld16(tmem + lane_off + tE0 + slot * 64 + 16 * hf, ev);
           tmem_ld_wait();
           if (lane < 16) {
 #pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            float x[8], y[8];
+            for (int m = 0; m < 2; ++m) {
+              float x[8], y[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              x[e] = ev[8 * m + e];
-              y[e] = u * x[e];
+              for (int e = 0; e < 8; ++e) {
+                x[e] = ev[8 * m + e];
+                y[e] = u * x[e];
+              }
+              const uint32_t off = sw128_offset(i, 16 * hf + 8 * m);
+              uint4 hi, lo;
+              split8(x, hi, lo);
+              *reinterpret_cast<uint4*>(Et + off) = hi;
+              *reinterpret_cast<uint4*>(Et + 8192 + off) = lo;
+              split8(y, hi, lo);
+              *reinterpret_cast<uint4*>(Et + 16384 + off) = hi;
+              *reinterpret_cast<uint4*>(Et + 24576 + off) = lo;
             }
-            const uint32_t off = sw128_offset(i, chalf * 32 + 16 * hf + 8 * m);
-            uint4 hi, lo;
-            split8(x, hi, lo);
-            *reinterpret_cast<uint4*>(Et + off) = hi;
-            *reinterpret_cast<uint4*>(Et + 8192 + off) = lo;
-            split8(y, hi, lo);
-            *reinterpret_cast<uint4*>(Et + 16384 + off) = hi;
-            *reinterpret_cast<uint4*>(Et + 24576 + off) = lo;
-          }
           }
         }
       }
       tc_fence_before();
       fence_proxy_async();
-      named_bar(1, 256);
+      named_bar(1, 128);
       if (leader) mbar_arrive(&bars[B_EREADY]);
-      if (!group_wait(0, 1, 256, &bars[B_M4], c & 1, leader)) break;
+      if (!group_wait(0, 1, 128, &bars[B_M4], c & 1, leader)) break;
       tc_fence_after();
       // epilogue: S <- gamma_C S + dS ; o = qs QS + PE
       {
         const float gC = vqs[128];
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
+        for (int hf = 0; hf < 4; ++hf) {
           float ds[16];
-          tmem_ld16(tmem + lane_off + tDS + chalf * 32 + 16 * hf, ds);
+          tmem_ld16(tmem + lane_off + tDS + 16 * hf, ds);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 16; ++e) S[16 * hf + e] = gC * S[16 * hf + e] + ds[e];
@@ -232,12 +235,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         const int i = quad * 16 + lane;
         const float qs = vqs[i & 63];
         __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out) +
-                            (((long)b * a.T + t0 + (i & 63)) * a.H + h) * a.dv + half * 64 + chalf * 32;
+                            (((long)b * a.T + t0 + (i & 63)) * a.H + h) * a.dv + half * 64;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
+        for (int hf = 0; hf < 4; ++hf) {
           float qv[16], pe[16];
-          tmem_ld16(tmem + lane_off + tQS + chalf * 32 + 16 * hf, qv);
-          tmem_ld16(tmem + lane_off + tPE + chalf * 32 + 16 * hf, pe);
+          tmem_ld16(tmem + lane_off + tQS + 16 * hf, qv);
+          tmem_ld16(tmem + lane_off + tPE + 16 * hf, pe);
           tmem_ld_wait();
           if (lane < 16 && i < Cc) {
 #pragma unroll
@@ -255,26 +258,26 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       }
       tc_fence_before();
       fence_proxy_async();
-      named_bar(1, 256);
+      named_bar(1, 128);
       if (leader) {
         mbar_arrive(&bars[B_SREADY]);            // S tiles of chunk c+1
         mbar_arrive(&bars[B_VF0 + slot]);        // vector slot free again
       }
     }
     if (!s_abort && a.S) {
-      const long base = ((long)bh * 128 + srow) * a.dv + half * 64 + chalf * 32;
+      const long base = ((long)bh * 128 + srow) * a.dv + half * 64;
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) {
+      for (int j = 0; j < 64; j += 4) {
         *reinterpret_cast<float4*>(a.S + base + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
         if (a.check_finite)
           bad |= !(finite_f(S[j]) && finite_f(S[j + 1]) && finite_f(S[j + 2]) && finite_f(S[j + 3]));
       }
     }
     if (bad) set_status(DR_ERR_NONFINITE);
-  } else if (warp < 16) {
+  } else if (warp < 12) {
     // =====================================================================================
-    // prep group: warps 8-15
-    const int ptid = tid - 256, pwarp = warp - 8;
+    // prep group: warps 4-11
+    const int ptid = tid - 128, pwarp = warp - 4;
     const int quad = warp & 3, pchalf = pwarp >> 2;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const bool leader = (ptid == 0);
@@ -539,7 +542,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     }
   } else if (lane == 0) {
     // =====================================================================================
-    // issue lane (warp 16): TMA and tcgen05 MMAs
+    // issue lane (warp 12): TMA and tcgen05 MMAs
     auto wait = [&](int id, uint32_t parity) -> bool {
       if (s_abort) return false;
       if (!mbar_wait(&bars[id], parity, kWsWait)) {
@@ -654,7 +657,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     mbar_wait(&bars[B_M4], (NC - 1) & 1, kWsWait / 4);
   }
 
-  if (warp == 16) __syncwarp();   // lanes 1-31 of the issue warp wait for lane 0
+  if (warp == 12) __syncwarp();   // lanes 1-31 of the issue warp wait for lane 0
   tc_fence_before();
   __syncthreads();
   if (s_abort && tid == 0) set_status(DR_ERR_TIMEOUT);
