@@ -62,8 +62,9 @@ def parse():
 
 
 KERNEL_SOURCES = {
-    "chunk_tc": ["chunk_tc.cu", "umma.cuh", "dr_common.cuh"],
-    "chunk_simt": ["chunk_simt.cu", "dr_common.cuh"],
+    "chunk_tc_ws": ["chunk_tc_ws.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh"],
+    "chunk_tc": ["chunk_tc.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh"],
+    "chunk_simt": ["chunk_simt.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh"],
     "decode": ["decode.cu", "dr_common.cuh"],
 }
 
@@ -373,7 +374,7 @@ def main():
     dom = max(variants, key=lambda v: var_stats[v]["ms"])
     byt = fwd_bytes(wl, dom)
     ach = byt / (var_stats[dom]["ms"] / 1e3) / 1e9
-    kname = "chunk_tc" if var_stats[dom]["path"] == "tc" else "chunk_simt"
+    kname = "chunk_" + var_stats[dom]["path"]
     roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": ach / pk["hbm_gbs"], "traffic": measured_traffic(kname, wl.name, dom),
             "kernel": f"{kname} ({dom})",

@@ -157,8 +157,11 @@ int dr_get_device_status(dr_stream_t stream);
 /* Static, NUL-terminated description of a dr_status value. */
 const char *dr_status_string(int status);
 
-/* Name of the kernel path dr_chunk_fwd takes for these arguments
- * ("tc" tensor-core, "simt" fp32 CUDA cores); static string. */
+/* Name of the kernel path dr_chunk_fwd takes for these arguments; static string.
+ * "tc_ws"  warp-specialised tcgen05 kernel (GDN, KLA; bf16, dk = dv = 128, chunk 64)
+ * "tc"     phase-sequential tcgen05 kernel (PGDN; same shapes)
+ * "simt"   fp32 CUDA-core kernel (everything else: fp32 mode, KDN, dk or dv 64,
+ *          other chunk sizes). */
 const char *dr_chunk_fwd_path(int variant, int dtype, int dk, int dv, int chunk);
 
 #ifdef __cplusplus

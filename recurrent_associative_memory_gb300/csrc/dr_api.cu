@@ -114,6 +114,7 @@ size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H,
 }
 
 const char* dr_chunk_fwd_path(int variant, int dtype, int dk, int dv, int chunk) {
+  if (chunk_tc_ws_supported(variant, dtype, dk, dv, chunk)) return "tc_ws";
   return chunk_tc_supported(variant, dtype, dk, dv, chunk) ? "tc" : "simt";
 }
 
