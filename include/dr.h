@@ -93,8 +93,8 @@ typedef struct dr_params {
   float info_scale;        /* KDN information scaling mu; default 1 (strict update)   */
   const float *aux_init;   /* dr_chunk_fwd: PGDN A_0 / KDN p_0 [B,H,dk]; NULL => 0 / 1 */
   float *aux_final;        /* dr_chunk_fwd: final A / p [B,H,dk]; NULL => not written */
-  void *workspace;         /* caller-owned scratch (see dr_chunk_fwd_workspace_bytes) */
-  size_t workspace_bytes;
+  void *workspace;         /* dr_chunk_fwd: caller-owned device scratch, 256-byte     */
+  size_t workspace_bytes;  /* aligned, or NULL (see dr_chunk_fwd_workspace_bytes)     */
   int check_finite;        /* 1: scan outputs/states for NaN/Inf -> DR_ERR_NONFINITE  */
 } dr_params;
 
@@ -122,6 +122,15 @@ void dr_params_init(dr_params *p);
  * final_state      device fp32 [B,H,dk,dv] or NULL (not written).
  * Sizes: B, H, T >= 1; dk, dv in {64, 128}; chunk in {16, 32, 64, 128}.  T need
  * not be a multiple of chunk.
+ * gp->workspace    optional.  Where dr_chunk_fwd_workspace_bytes() is non-zero
+ *                  and a workspace of at least that size is given, the
+ *                  chunk-local work (Grams, gates, triangular inverse, W') of
+ *                  all chunks runs first, in parallel, and leaves one record per
+ *                  chunk there; the carry over chunks then reads them.  Its
+ *                  contents are undefined afterwards.  NULL: the single-kernel
+ *                  path runs (same results up to rounding order).  A workspace
+ *                  that is too small returns DR_ERR_WORKSPACE, a misaligned one
+ *                  DR_ERR_ALIGN.  Two calls in flight must not share one.
  * Returns DR_OK or a negative dr_status.
  */
 int dr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
@@ -146,7 +155,9 @@ int dr_decode_step(const void *q, const void *k, const void *v, const float *log
                    float *state, float *aux_state, void *out,
                    int B, int H, int dk, int dv, dr_stream_t stream);
 
-/* Scratch bytes dr_chunk_fwd needs for these sizes (0: no workspace needed). */
+/* Bytes of the optional dr_chunk_fwd workspace for these sizes: B H ceil(T/64)
+ * records of 66560 bytes on the two-phase path (GDN/KLA, bf16, dk = dv = 128,
+ * chunk 64), 0 where no path uses one. */
 size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H, int dk, int dv,
                                     int chunk);
 
@@ -158,7 +169,10 @@ int dr_get_device_status(dr_stream_t stream);
 const char *dr_status_string(int status);
 
 /* Name of the kernel path dr_chunk_fwd takes for these arguments; static string.
- * "tc_ws"  warp-specialised tcgen05 kernel (GDN, KLA; bf16, dk = dv = 128, chunk 64)
+ * "tc_split" two-phase tcgen05 path (GDN, KLA; bf16, dk = dv = 128, chunk 64) when
+ *          the workspace of dr_chunk_fwd_workspace_bytes() is supplied; without a
+ *          workspace the same shapes take
+ * "tc_ws"  the warp-specialised single-kernel tcgen05 path
  * "tc"     phase-sequential tcgen05 kernel (PGDN; same shapes)
  * "simt"   fp32 CUDA-core kernel (everything else: fp32 mode, KDN, dk or dv 64,
  *          other chunk sizes). */

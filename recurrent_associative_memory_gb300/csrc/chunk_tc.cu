@@ -21,9 +21,11 @@
 // Decay ratios come from log differences (KDN notes section 6, numerics).
 // Precision: the raw bf16 K, Q, V tiles are used as MMA operands unchanged
 // (they are exact), and every per-token scale is folded into an operand that
-// is computed on chip anyway.  Those computed operands -- T, T diag(e^g c), P,
-// E, u.E and S -- are fed as two bf16 terms (x = hi + lo, error ~2^-16); only
-// W' is a single bf16 term.  All bounded waits give up with DR_ERR_TIMEOUT.
+// is computed on chip anyway.  Those computed operands -- T, T diag(e^g c), W',
+// P, E, u.E and S -- are fed as two bf16 terms (x = hi + lo, error ~2^-16; the
+// lo x lo product is dropped).  W' needs its lo term for raw (unnormalised)
+// keys, where E = U' - W' S cancels heavily.  All bounded waits give up with
+// DR_ERR_TIMEOUT.
 #include <cuda.h>
 
 #include "dr_common.cuh"
@@ -46,7 +48,7 @@ constexpr uint32_t oKQ = 0;                     // 2 stages x [K rows 0-63 | Q r
 constexpr uint32_t kKQBytes = 32768;
 constexpr uint32_t oV = 2 * kKQBytes;           // V tile [64 tokens][64 cols]      8 KB
 constexpr uint32_t oT = oV + 8192;              // T hi | T lo | Ts hi | Ts lo    32 KB
-constexpr uint32_t oWp = oT + 32768;            // W' bf16 [64][128]               16 KB
+constexpr uint32_t oWp = oT + 32768;            // W' hi bf16 [64][128] (lo: E tiles) 16 KB
 constexpr uint32_t oS = oWp + 16384;            // S hi | S lo  [128][64]          32 KB
 constexpr uint32_t oP = oS + 32768;             // P hi | P lo  [64][64]           16 KB
 constexpr uint32_t oE = oP + 16384;             // E hi | E lo | uE hi | uE lo     32 KB
@@ -478,7 +480,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     if (tid == 0 && c + 1 < NC) issue_v(c + 1);   // V tile is free again
 
-    // ---------------- 6. W' (M=64 layout: row 16 quad + lane, lanes < 16) -> bf16 tile
+    // ---------------- 6. W' (M=64 layout: row 16 quad + lane, lanes < 16) -> bf16 hi/lo tiles
     {
       float w[64];
 #pragma unroll
@@ -492,30 +494,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane < 16) {
         const int i = quad * 16 + lane;
         uint8_t* Wp = sm + oWp + chalf * 8192;
+        uint8_t* Wl = sm + oE + chalf * 8192;   // lo term borrows the (free) E tiles
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
           float x[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = w[8 * m + e];
-          *reinterpret_cast<uint4*>(Wp + sw128_offset(i, 8 * m)) = pack8(x);
+          uint4 hi, lo;
+          split8(x, hi, lo);
+          *reinterpret_cast<uint4*>(Wp + sw128_offset(i, 8 * m)) = hi;
+          *reinterpret_cast<uint4*>(Wl + sw128_offset(i, 8 * m)) = lo;
         }
       }
     }
     fence_proxy_async();
     __syncthreads();
 
-    // ---------------- 7. MMA 3: E = U' - W' (S_hi + S_lo),  QS = Q (S_hi + S_lo)
+    // ---------------- 7. MMA 3: E = U' - (W'_hi S_hi + W'_hi S_lo + W'_lo S_hi),  QS = Q (S_hi + S_lo)
     if (tid == 0) {
       tc_fence_after();
       const uint32_t kq = smem_u32(KQ), sb = smem_u32(sm + oS), wp = smem_u32(sm + oWp);
+      const uint32_t wl = smem_u32(sm + oE);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint64_t dsh = desc_sw128(sb + ks * 2048, 16384, 1024);
         const uint64_t dsl = desc_sw128(sb + 16384 + ks * 2048, 16384, 1024);
         const uint64_t dw = desc_sw128(wp + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
         const uint64_t dq = desc_sw128(kq + (ks >> 2) * 16384 + 8192 + (ks & 3) * 32, 16, 1024);
+        const uint64_t dwl = desc_sw128(wl + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
         mma_bf16(tmem + cE, dw, dsh, ID_ENEG, true);
         mma_bf16(tmem + cE, dw, dsl, ID_ENEG, true);
+        mma_bf16(tmem + cE, dwl, dsh, ID_ENEG, true);
         mma_bf16(tmem + cQS, dq, dsh, ID_N64, ks > 0);
         mma_bf16(tmem + cQS, dq, dsl, ID_N64, true);
       }

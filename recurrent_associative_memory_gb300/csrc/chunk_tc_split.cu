@@ -1,0 +1,881 @@
+// chunk_tc_split.cu — two-phase tcgen05 chunkwise forward for GDN and KLA
+// (scalar decay, w = coefficient x raw key), bf16 q/k/v/out, dk = dv = 128, chunk 64.
+//
+// The chunk algebra is that of chunk_tc_ws.cu (KLA notes section 2.5, Eqs. (7)-(9),
+// with the write matrix of the PDN notes section 2.6).  Everything in it that
+// does not involve the state is independent across chunks (the chunkwise form
+// exists for exactly that reason), so it is split off into a first kernel that
+// runs on every SM at once, and the sequential carry over chunks becomes a
+// second kernel whose critical path holds only the state-dependent products:
+//
+//   chunk_prep   one task per (b, h, chunk), 2 CTAs per SM, persistent.
+//                Gram [K; Q] K^T on tcgen05; gates, norms and write coefficients;
+//                L and P = lower((Q W^T) . e^{g_i - g_j}); T = (I + L)^-1 by
+//                16x16 forward substitution and TF32x3 recursive doubling;
+//                W' = T diag(e^g c) K on tcgen05.  Writes one record per chunk
+//                to the workspace: T, W' and P as bf16 hi/lo pairs, and the row
+//                vectors e^g qn, e^{g_C - g} c, gamma_C.  (W' needs its lo term:
+//                with raw GDN keys E = U' - W' S cancels heavily, and a single
+//                bf16 W' costs ~1e-2 of the state.)
+//   chunk_carry  one CTA per (b, h, 64-column half of dv), 4 state warps + 1
+//                issue warp.  Per chunk:  U' = T V,  E = U' - W' S,
+//                dS = K^T (u . E),  S <- gamma_C S + dS,  o = e^g qn . Q S + P E.
+//                The record and the K, Q, V tiles arrive by bulk / tensor copies
+//                issued as soon as the previous chunk's MMAs free each buffer.
+//
+// The records are intermediates of the method, not algorithmic traffic; the
+// workspace is caller-owned (dr_chunk_fwd_workspace_bytes).  Every wait is
+// bounded in wall-clock time; a timeout sets DR_ERR_TIMEOUT and the CTA drains
+// its copies in flight before it frees TMEM and exits.
+#include "dr_common.cuh"
+#include "tc_common.cuh"
+
+namespace dr {
+
+namespace {
+
+using namespace umma;
+using namespace tc;
+
+constexpr uint64_t kWait = 2000000000ull;   // 2 s per bounded wait
+constexpr int LDL = 68;                     // fp32 L/T row stride
+constexpr int LDX = 36;                     // fp32 scratch row stride
+
+// ---- per-chunk record in the workspace (bytes); 128B-swizzled tile images
+constexpr uint32_t rT = 0;          // T hi | T lo       (64 x 64 bf16 each)
+constexpr uint32_t rWp = 16384;     // W' hi k-blocks 0 | 1, then W' lo k-blocks 0 | 1
+constexpr uint32_t rP = 49152;      // P hi | P lo
+constexpr uint32_t rVec = 65536;    // fp32 [0,64) e^g qn ; [64,128) e^{g_C-g} c ; [128] gamma_C
+constexpr uint32_t kRec = 66560;
+
+// ================================================================= chunk_prep
+constexpr int kPrepThreads = 9 * 32;        // warps 0-7 prep, warp 8 issue
+constexpr uint32_t pKQ = 0;                 // 2 stages x [K kb0 | Q kb0 | K kb1 | Q kb1], 32 KB each
+constexpr uint32_t pT = 65536;              // T hi | T lo | Ts hi | Ts lo (L/T fp32 aliases it)
+constexpr uint32_t pVec = pT + 32768;       // vectors, 4 KB
+constexpr uint32_t kPrepSmem = pVec + 4096 + 1024;
+constexpr uint32_t tG0 = 0;                 // 2 Gram slots, M=128 x 64
+constexpr uint32_t tPWp = 128;              // W', M=64 x 128
+constexpr uint32_t kPrepTmem = 256;
+
+constexpr uint32_t I_GRAM = idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t I_WP = idesc_bf16(64, 128, 0, 1);
+constexpr uint32_t I_N64 = idesc_bf16(64, 64, 0, 1);
+constexpr uint32_t I_NEG = idesc_bf16(64, 64, 0, 1, 1);
+constexpr uint32_t I_DS = idesc_bf16(128, 64, 1, 1);
+
+enum { P_KQ0, P_KQ1, P_G0, P_G1, P_W, P_GFREE0, P_GFREE1, P_TREADY, P_WFREE, P_COUNT };
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+template <int VARIANT>
+__global__ void __launch_bounds__(kPrepThreads, 2)
+    chunk_prep_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      FwdArgs a, uint8_t* __restrict__ ws) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t bars[P_COUNT];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int s_abort;
+  __shared__ volatile int s_ok;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NC = (a.T + 63) / 64;
+  const int ntask = a.B * a.H * NC;
+  // tasks of this CTA: blockIdx.x + k gridDim.x
+  auto task_of = [&](int k) { return blockIdx.x + k * gridDim.x; };
+  const int nmine = (blockIdx.x < ntask) ? (ntask - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+  float* vg = reinterpret_cast<float*>(sm + pVec);   // cumulative log-decay
+  float* va = vg + 64;      // coefficient of the raw key row in w
+  float* vcr = va + 64;     // key normalisation
+  float* vqn = vcr + 64;    // query normalisation
+  float* vks = vqn + 64;    // e^{g_j} c_j
+  float* vF = vks + 64;     // e^{g_e(J) - g_j}
+  float* vkk = vF + 64;
+  float* vqq = vkk + 64;
+  float* vla = vqq + 64;
+  float* veta = vla + 64;
+  float* LT = reinterpret_cast<float*>(sm + pT);
+  float* XS = LT + 64 * LDL;
+
+  if (tid == 0) {
+    for (int i = 0; i < P_COUNT; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+    s_abort = 0;
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+  }
+  if (warp == 0) tmem_alloc(&tmem_base_s, kPrepTmem);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  if (warp < 8) {
+    // ===================================================================== prep warps
+    const int ptid = tid, pwarp = warp;
+    const int quad = warp & 3, pchalf = pwarp >> 2;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const bool leader = (ptid == 0);
+    auto group_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (leader) {
+        bool ok = !s_abort && mbar_wait(bar, parity, kWait);
+        if (!ok) s_abort = 1;
+        s_ok = ok ? 1 : 0;
+      }
+      named_bar(1, 256);
+      const bool ok = s_ok != 0;
+      named_bar(1, 256);
+      return ok;
+    };
+
+    float nla = 0.f, neta = 0.f;   // gates of the next task (thread ptid < 64 = token)
+    auto prefetch_gates = [&](int k) {
+      const int t = task_of(k), bh = t / NC, c = t % NC;
+      const int i = ptid, tok = c * 64 + i;
+      if (i < 64 && tok < a.T) {
+        const long ti = ((long)(bh / a.H) * a.T + tok) * a.H + (bh % a.H);
+        nla = a.log_alpha[ti];
+        neta = a.eta[ti];
+      } else {
+        nla = 0.f;
+        neta = 0.f;
+      }
+    };
+    if (nmine > 0) prefetch_gates(0);
+
+    for (int k = 0; k < nmine; ++k) {
+      const int t = task_of(k);
+      uint8_t* rec = ws + (size_t)t * kRec;   // tasks are numbered (b h) major, chunk minor
+      const int st = k & 1;
+      const uint8_t* KQ = sm + pKQ + st * 32768;
+
+      // ---- gates: decay, norms, write coefficients, the carry's row vectors
+      if (!group_wait(&bars[P_KQ0 + st], (k >> 1) & 1)) break;
+      if (ptid < 64) {
+        vla[ptid] = nla;
+        veta[ptid] = neta;
+      }
+      if (k + 1 < nmine) prefetch_gates(k + 1);
+      {
+        const int i = ptid >> 2, part = ptid & 3, kb = part >> 1, c0 = (part & 1) * 32;
+        float kk = 0.f, qq = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          float fk[8], fq[8];
+          unpack8(*reinterpret_cast<const uint4*>(KQ + kb * 16384 + sw128_offset(i, c0 + 8 * m)), fk);
+          unpack8(*reinterpret_cast<const uint4*>(KQ + kb * 16384 + sw128_offset(64 + i, c0 + 8 * m)), fq);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            kk += fk[e] * fk[e];
+            qq += fq[e] * fq[e];
+          }
+        }
+        kk += __shfl_xor_sync(0xffffffffu, kk, 1);
+        kk += __shfl_xor_sync(0xffffffffu, kk, 2);
+        qq += __shfl_xor_sync(0xffffffffu, qq, 1);
+        qq += __shfl_xor_sync(0xffffffffu, qq, 2);
+        if (part == 0) {
+          vkk[i] = kk;
+          vqq[i] = qq;
+        }
+      }
+      named_bar(1, 256);
+      if (pwarp == 0) {
+        const float x0 = vla[2 * lane], x1 = vla[2 * lane + 1];
+        float s = x0 + x1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, s, o);
+          if (lane >= o) s += y;
+        }
+        vg[2 * lane] = s - x1;
+        vg[2 * lane + 1] = s;
+      }
+      named_bar(1, 256);
+      if (ptid < 64) {
+        const int i = ptid;
+        const float gi = vg[i], gC = vg[63];
+        const float kk = vkk[i], qq = vqq[i];
+        const float cr = a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f;
+        const float qn = a.q_l2norm ? 1.f / fmaxf(sqrtf(qq), 1e-30f) : 1.f;
+        float beta = veta[i];
+        if (VARIANT == DR_KLA) beta = beta / (kk * cr * cr + a.eps);
+        const float coef = beta * cr;
+        va[i] = coef;
+        vcr[i] = cr;
+        vqn[i] = qn;
+        const float eg = __expf(gi);
+        vks[i] = eg * cr;
+        vF[i] = __expf(vg[i | 15] - gi);
+        float* rv = reinterpret_cast<float*>(rec + rVec);
+        rv[i] = eg * qn;
+        rv[64 + i] = __expf(gC - gi) * coef;
+        if (i == 0) rv[128] = __expf(gC);
+      }
+      named_bar(1, 256);
+
+      // ---- Gram readout -> L (fp32, smem) and P (bf16 hi/lo, record)
+      if (!group_wait(&bars[P_G0 + st], (k >> 1) & 1)) break;
+      tc_fence_after();
+      {
+        const int row = quad * 32 + lane;
+        const int i = row & 63, I = i >> 4;
+        float gv[32];
+        ld32cols(tmem + lane_off + tG0 + st * 64 + pchalf * 32, gv);
+        tmem_ld_wait();
+        const float gi = vg[i];
+        const float rs = (row < 64) ? vcr[i] : vqn[i];
+        float fb[2];
+#pragma unroll
+        for (int jb = 0; jb < 2; ++jb) {
+          const int J = pchalf * 2 + jb;
+          fb[jb] = (J < I) ? __expf(gi - vg[16 * J + 15]) : 0.f;
+        }
+        float x[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int j = pchalf * 32 + e, J = j >> 4;
+          const float ed = __expf(fminf(gi - vg[j], 0.f));
+          const float f = (J < I) ? fb[e >> 4] * vF[j] : ((J == I && j <= i) ? ed : 0.f);
+          x[e] = gv[e] * rs * va[j] * f;
+        }
+        if (row < 64) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const int j = pchalf * 32 + e;
+            *reinterpret_cast<float4*>(LT + i * LDL + j) =
+                make_float4(j < i ? x[e] : 0.f, j + 1 < i ? x[e + 1] : 0.f,
+                            j + 2 < i ? x[e + 2] : 0.f, j + 3 < i ? x[e + 3] : 0.f);
+          }
+        } else {
+          uint8_t* Pg = rec + rP;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = x[8 * m + e];
+            uint4 hi, lo;
+            split8(y, hi, lo);
+            *reinterpret_cast<uint4*>(Pg + sw128_offset(i, pchalf * 32 + 8 * m)) = hi;
+            *reinterpret_cast<uint4*>(Pg + 8192 + sw128_offset(i, pchalf * 32 + 8 * m)) = lo;
+          }
+        }
+      }
+      tc_fence_before();
+      named_bar(1, 256);
+      if (leader) mbar_arrive(&bars[P_GFREE0 + st]);
+      // ---- T = (I + L)^-1 in place: diagonal 16x16 blocks (threads 0-63, one column each)
+      {
+        const int j = ptid & 15, I = (ptid >> 4) & 3, r0 = 16 * I;
+        float tt[16];
+#pragma unroll
+        for (int l = 0; l < 16; ++l) tt[l] = (l == j) ? 1.f : 0.f;
+        if (ptid < 64) {
+#pragma unroll
+          for (int i = 1; i < 16; ++i) {
+            float s = 0.f;
+#pragma unroll
+            for (int l = 0; l < i; ++l) s += LT[(r0 + i) * LDL + r0 + l] * tt[l];
+            if (i > j) tt[i] = -s;
+          }
+        }
+        named_bar(1, 256);
+        if (ptid < 64) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) LT[(r0 + i) * LDL + r0 + j] = tt[i];
+        }
+      }
+      named_bar(1, 256);
+      // level 1: T_10, T_32 ; level 2: the 32 x 32 lower-left block (TF32x3 mma.sync)
+      if (pwarp < 4) {
+        const int blk = pwarp >> 1, nt = pwarp & 1;
+        const int r0 = 32 * blk + 16, c0 = 32 * blk;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mm3<2>(d, LT + r0 * LDL + c0, LDL, LT + c0 * LDL + c0 + 8 * nt, LDL, lane);
+        tile_store(XS + 16 * blk * LDX + 8 * nt, LDX, d, 1.f, lane);
+      }
+      named_bar(1, 256);
+      if (pwarp < 4) {
+        const int blk = pwarp >> 1, nt = pwarp & 1;
+        const int r0 = 32 * blk + 16, c0 = 32 * blk;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mm3<2>(d, LT + r0 * LDL + r0, LDL, XS + 16 * blk * LDX + 8 * nt, LDX, lane);
+        tile_store(LT + r0 * LDL + c0 + 8 * nt, LDL, d, -1.f, lane);
+      }
+      named_bar(1, 256);
+      {
+        const int mt = pwarp >> 2, nt = pwarp & 3;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mm3<4>(d, LT + (32 + 16 * mt) * LDL, LDL, LT + 8 * nt, LDL, lane);
+        tile_store(XS + 16 * mt * LDX + 8 * nt, LDX, d, 1.f, lane);
+      }
+      named_bar(1, 256);
+      {
+        const int mt = pwarp >> 2, nt = pwarp & 3;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        if (mt == 0)
+          tile_mm3<2>(d, LT + 32 * LDL + 32, LDL, XS + 8 * nt, LDX, lane);
+        else
+          tile_mm3<4>(d, LT + 48 * LDL + 32, LDL, XS + 8 * nt, LDX, lane);
+        tile_store(LT + (32 + 16 * mt) * LDL + 8 * nt, LDL, d, -1.f, lane);
+      }
+      named_bar(1, 256);
+      // ---- T (record) and Ts = T diag(ks) (smem, for W'); the tiles alias L/T, so read first
+      {
+        const int i = ptid >> 2, c0 = (ptid & 3) * 16;
+        float tv[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int j = c0 + e;
+          tv[e] = (j <= i) ? LT[i * LDL + j] : 0.f;
+        }
+        named_bar(1, 256);
+        uint8_t* Tt = sm + pT;
+        uint8_t* Tg = rec + rT;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          float x[8], y[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            x[e] = tv[8 * m + e];
+            y[e] = x[e] * vks[c0 + 8 * m + e];
+          }
+          const uint32_t off = sw128_offset(i, c0 + 8 * m);
+          uint4 hi, lo;
+          split8(x, hi, lo);
+          *reinterpret_cast<uint4*>(Tg + off) = hi;
+          *reinterpret_cast<uint4*>(Tg + 8192 + off) = lo;
+          split8(y, hi, lo);
+          *reinterpret_cast<uint4*>(Tt + 16384 + off) = hi;
+          *reinterpret_cast<uint4*>(Tt + 24576 + off) = lo;
+        }
+      }
+      fence_proxy_async();
+      named_bar(1, 256);
+      if (leader) mbar_arrive(&bars[P_TREADY]);
+      // ---- W' readout -> record
+      if (!group_wait(&bars[P_W], k & 1)) break;
+      tc_fence_after();
+      {
+        const int i = quad * 16 + lane;
+        uint8_t* Wg = rec + rWp + pchalf * 8192;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          float w[16];
+          tmem_ld16(tmem + lane_off + tPWp + pchalf * 64 + 16 * m, w);
+          tmem_ld_wait();
+          if (lane < 16) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              float x[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) x[e] = w[8 * hh + e];
+              uint4 hi, lo;
+              split8(x, hi, lo);
+              *reinterpret_cast<uint4*>(Wg + sw128_offset(i, 16 * m + 8 * hh)) = hi;
+              *reinterpret_cast<uint4*>(Wg + 16384 + sw128_offset(i, 16 * m + 8 * hh)) = lo;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      named_bar(1, 256);
+      if (leader) mbar_arrive(&bars[P_WFREE]);
+    }
+  } else if (lane == 0) {
+    // ===================================================================== issue lane
+    auto wait = [&](int id, uint32_t parity) -> bool {
+      if (s_abort) return false;
+      if (!mbar_wait(&bars[id], parity, kWait)) {
+        s_abort = 1;
+        return false;
+      }
+      return true;
+    };
+    int kq_issued = 0;   // KQ loads issued so far (task k uses stage k & 1)
+    auto issue_kq = [&](int k) {
+      const int t = task_of(k), bh = t / NC, c = t % NC;
+      const int b = bh / a.H, h = bh % a.H, st = k & 1;
+      uint8_t* base = sm + pKQ + st * 32768;
+      mbar_expect_tx(&bars[P_KQ0 + st], 32768);
+      tma_load_4d(base, &tmK, &bars[P_KQ0 + st], 0, h, c * 64, b);
+      tma_load_4d(base + 16384, &tmK, &bars[P_KQ0 + st], 64, h, c * 64, b);
+      tma_load_4d(base + 8192, &tmQ, &bars[P_KQ0 + st], 0, h, c * 64, b);
+      tma_load_4d(base + 16384 + 8192, &tmQ, &bars[P_KQ0 + st], 64, h, c * 64, b);
+      kq_issued = k + 1;
+    };
+    auto gram = [&](int k) {
+      const uint32_t kq = smem_u32(sm + pKQ + (k & 1) * 32768);
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t d = desc_sw128(kq + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+        mma_bf16(tmem + tG0 + (k & 1) * 64, d, d, I_GRAM, ks > 0);
+      }
+      mma_commit(&bars[P_G0 + (k & 1)]);
+    };
+    bool ok = true;
+    if (nmine > 0) issue_kq(0);
+    if (nmine > 1) issue_kq(1);
+    if (nmine > 0 && (ok = wait(P_KQ0, 0))) gram(0);
+    int w_done = 0;   // W' MMAs committed
+    for (int k = 0; ok && k < nmine; ++k) {
+      const int st = k & 1;
+      // Gram of the next task into the other slot once its readout (task k-1) is done
+      if (k + 1 < nmine) {
+        if (!(ok = wait(P_KQ0 + (st ^ 1), ((k + 1) >> 1) & 1))) break;
+        if (k >= 1 && !(ok = wait(P_GFREE0 + (st ^ 1), ((k - 1) >> 1) & 1))) break;
+        gram(k + 1);
+      }
+      // W'(k) = Ts K once the tiles are ready and W'(k-1) has been read out
+      if (!(ok = wait(P_TREADY, k & 1))) break;
+      if (k >= 1 && !(ok = wait(P_WFREE, (k - 1) & 1))) break;
+      tc_fence_after();
+      {
+        const uint32_t tb = smem_u32(sm + pT), kq = smem_u32(sm + pKQ + st * 32768);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t dts = desc_sw128(tb + 16384 + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
+          const uint64_t dk = desc_sw128(kq + (ks & 3) * 2048, 16384, 1024);
+          mma_bf16(tmem + tPWp, dts, dk, I_WP, ks > 0);
+        }
+        mma_commit(&bars[P_W]);
+        w_done = k + 1;
+      }
+      // stage st is free once W'(k) (its last reader) is done
+      if (k + 2 < nmine) {
+        if (!(ok = wait(P_W, k & 1))) break;
+        issue_kq(k + 2);
+      }
+    }
+    if (!ok) set_status(DR_ERR_TIMEOUT);
+    // drain: the last W' MMA and every KQ load issued
+    if (w_done > 0) mbar_wait(&bars[P_W], (w_done - 1) & 1, kWait / 4);
+    for (int k = (kq_issued > 2 ? kq_issued - 2 : 0); k < kq_issued; ++k)
+      mbar_wait(&bars[P_KQ0 + (k & 1)], (k >> 1) & 1, kWait / 4);
+  }
+
+  if (warp == 8) __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (s_abort && tid == 0) set_status(DR_ERR_TIMEOUT);
+  if (warp == 0) tmem_dealloc(tmem, kPrepTmem);
+}
+
+// ================================================================= chunk_carry
+constexpr int kCarryThreads = 5 * 32;       // warps 0-3 state, warp 4 issue
+constexpr uint32_t cT = 0;                  // T hi | T lo              16 KB
+constexpr uint32_t cV = 16384;              // V [64 tok][64 col]       8 KB
+constexpr uint32_t cWp = 24576;             // W' hi kb0|kb1, lo kb0|kb1  32 KB
+constexpr uint32_t cQ = 57344;              // Q kb0 | kb1              16 KB
+constexpr uint32_t cK = 73728;              // K kb0 | kb1              16 KB
+constexpr uint32_t cP = 90112;              // P hi | P lo              16 KB
+constexpr uint32_t cS = 106496;             // S hi | S lo [128][64]    32 KB
+constexpr uint32_t cE = 139264;             // E hi | E lo | uE hi | uE lo   32 KB
+constexpr uint32_t cVec = 172032;           // 2 slots x 1 KB record vectors
+constexpr uint32_t kCarrySmem = cVec + 2048 + 1024;
+constexpr uint32_t tU0 = 0;                 // 2 slots M=64 x 64: U', then E
+constexpr uint32_t tQS = 128;               // M=64 x 64
+constexpr uint32_t tPE = 192;               // M=64 x 64
+constexpr uint32_t tDS = 256;               // M=128 x 64
+constexpr uint32_t kCarryTmem = 512;
+
+enum {
+  C_TV, C_WQ, C_KP,                         // copies landed
+  C_M2, C_E, C_QS, C_DS, C_PE,              // MMAs complete
+  C_SREADY, C_EREADY, C_OUTDONE,            // state-group hand-offs
+  C_COUNT
+};
+
+__global__ void __launch_bounds__(kCarryThreads, 1)
+    chunk_carry_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, FwdArgs a,
+                       const uint8_t* __restrict__ ws) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t bars[C_COUNT];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int s_abort;
+  __shared__ volatile int s_ok;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int half = blockIdx.x & 1;
+  const int bh = blockIdx.x >> 1;
+  const int b = bh / a.H, h = bh % a.H;
+  const int NC = (a.T + 63) / 64;
+  const uint8_t* recs = ws + (size_t)bh * NC * kRec;
+
+  if (tid == 0) {
+    for (int i = 0; i < C_COUNT; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+    s_abort = 0;
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 0) tmem_alloc(&tmem_base_s, kCarryTmem);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  if (warp < 4) {
+    // ===================================================================== state warps
+    // thread = row r of the state slice (TMEM lane r), all 64 columns
+    const int quad = warp, srow = tid;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const bool leader = (tid == 0);
+    auto group_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (leader) {
+        bool ok = !s_abort && mbar_wait(bar, parity, kWait);
+        if (!ok) s_abort = 1;
+        s_ok = ok ? 1 : 0;
+      }
+      named_bar(1, 128);
+      const bool ok = s_ok != 0;
+      named_bar(1, 128);
+      return ok;
+    };
+    float S[64];
+    auto store_state_tiles = [&]() {
+      uint8_t* sS = sm + cS;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = S[8 * m + e];
+        uint4 hi, lo;
+        split8(x, hi, lo);
+        *reinterpret_cast<uint4*>(sS + sw128_offset(srow, 8 * m)) = hi;
+        *reinterpret_cast<uint4*>(sS + 16384 + sw128_offset(srow, 8 * m)) = lo;
+      }
+    };
+    {
+      const long base = ((long)bh * 128 + srow) * a.dv + half * 64;
+#pragma unroll
+      for (int j = 0; j < 64; j += 4) {
+        const float4 v = a.S0 ? *reinterpret_cast<const float4*>(a.S0 + base + j)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
+      }
+      store_state_tiles();
+    }
+    fence_proxy_async();
+    named_bar(1, 128);
+    if (leader) mbar_arrive(&bars[C_SREADY]);   // S tiles of chunk 0
+    bool bad = false;
+    bool ok = group_wait(&bars[C_TV], 0);       // vectors of chunk 0
+
+    for (int c = 0; ok && c < NC; ++c) {
+      const int slot = c & 1;
+      const float* vqs = reinterpret_cast<const float*>(sm + cVec + slot * 1024);
+      const float* vu = vqs + 64;
+      const int t0 = c * 64, Cc = min(64, a.T - t0);
+      const int i = quad * 16 + lane;           // token row held by lanes 0-15 (M=64 layout)
+      // ---- E -> E and u.E hi/lo tiles
+      if (!(ok = group_wait(&bars[C_E], c & 1))) break;
+      tc_fence_after();
+      {
+        const float u = vu[i & 63];
+        uint8_t* Et = sm + cE;
+        float ev[64];
+#pragma unroll
+        for (int hf = 0; hf < 4; ++hf) {
+          float t16[16];
+          tmem_ld16(tmem + lane_off + tU0 + slot * 64 + 16 * hf, t16);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ev[16 * hf + e] = t16[e];
+        }
+        tmem_ld_wait();
+        if (lane < 16) {
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            float x[8], y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              x[e] = ev[8 * m + e];
+              y[e] = u * x[e];
+            }
+            const uint32_t off = sw128_offset(i, 8 * m);
+            uint4 hi, lo;
+            split8(x, hi, lo);
+            *reinterpret_cast<uint4*>(Et + off) = hi;
+            *reinterpret_cast<uint4*>(Et + 8192 + off) = lo;
+            split8(y, hi, lo);
+            *reinterpret_cast<uint4*>(Et + 16384 + off) = hi;
+            *reinterpret_cast<uint4*>(Et + 24576 + off) = lo;
+          }
+        }
+      }
+      tc_fence_before();
+      fence_proxy_async();
+      named_bar(1, 128);
+      if (leader) mbar_arrive(&bars[C_EREADY]);
+      // ---- S <- gamma_C S + dS, then the S tiles of chunk c+1
+      if (!(ok = group_wait(&bars[C_DS], c & 1))) break;
+      tc_fence_after();
+      {
+        const float gC = vqs[128];
+        float ds[64];
+#pragma unroll
+        for (int hf = 0; hf < 4; ++hf) {
+          float t16[16];
+          tmem_ld16(tmem + lane_off + tDS + 16 * hf, t16);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ds[16 * hf + e] = t16[e];
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 64; ++e) S[e] = gC * S[e] + ds[e];
+        store_state_tiles();
+      }
+      tc_fence_before();
+      fence_proxy_async();
+      named_bar(1, 128);
+      if (leader) mbar_arrive(&bars[C_SREADY]);
+      // ---- o = e^g qn . QS + PE  (off the carry's critical path)
+      if (!(ok = group_wait(&bars[C_QS], c & 1))) break;
+      if (!(ok = group_wait(&bars[C_PE], c & 1))) break;
+      tc_fence_after();
+      {
+        const float qs = vqs[i & 63];
+        __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out) +
+                            (((long)b * a.T + t0 + (i & 63)) * a.H + h) * a.dv + half * 64;
+#pragma unroll
+        for (int hf = 0; hf < 4; ++hf) {
+          float qv[16], pe[16];
+          tmem_ld16(tmem + lane_off + tQS + 16 * hf, qv);
+          tmem_ld16(tmem + lane_off + tPE + 16 * hf, pe);
+          tmem_ld_wait();
+          if (lane < 16 && i < Cc) {
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              float x[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                x[e] = qs * qv[8 * m + e] + pe[8 * m + e];
+                if (a.check_finite) bad |= !finite_f(x[e]);
+              }
+              *reinterpret_cast<uint4*>(op + 16 * hf + 8 * m) = pack8(x);
+            }
+          }
+        }
+      }
+      // the vectors of chunk c+1 must have landed before the issue lane may
+      // reuse this slot (it reloads it only after OUTDONE(c))
+      if (c + 1 < NC && !(ok = group_wait(&bars[C_TV], (c + 1) & 1))) break;
+      tc_fence_before();
+      named_bar(1, 128);
+      if (leader) mbar_arrive(&bars[C_OUTDONE]);
+    }
+    if (ok && !s_abort && a.S) {
+      const long base = ((long)bh * 128 + srow) * a.dv + half * 64;
+#pragma unroll
+      for (int j = 0; j < 64; j += 4) {
+        *reinterpret_cast<float4*>(a.S + base + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        if (a.check_finite)
+          bad |= !(finite_f(S[j]) && finite_f(S[j + 1]) && finite_f(S[j + 2]) && finite_f(S[j + 3]));
+      }
+    }
+    if (bad) set_status(DR_ERR_NONFINITE);
+  } else if (warp == 4 && lane == 0) {
+    // ===================================================================== issue lane
+    auto wait = [&](int id, uint32_t parity) -> bool {
+      if (s_abort) return false;
+      if (!mbar_wait(&bars[id], parity, kWait)) {
+        s_abort = 1;
+        return false;
+      }
+      return true;
+    };
+    int n_tv = 0, n_wq = 0, n_kp = 0;   // copies issued per buffer group
+    auto load_tv = [&](int c) {
+      const uint8_t* rec = recs + (size_t)c * kRec;
+      mbar_expect_tx(&bars[C_TV], 16384 + 1024 + 8192);
+      bulk_load(sm + cT, rec + rT, 16384, &bars[C_TV]);
+      bulk_load(sm + cVec + (c & 1) * 1024, rec + rVec, 1024, &bars[C_TV]);
+      tma_load_4d(sm + cV, &tmV, &bars[C_TV], half * 64, h, c * 64, b);
+      n_tv = c + 1;
+    };
+    auto load_wq = [&](int c) {
+      const uint8_t* rec = recs + (size_t)c * kRec;
+      mbar_expect_tx(&bars[C_WQ], 32768 + 16384);
+      bulk_load(sm + cWp, rec + rWp, 32768, &bars[C_WQ]);
+      tma_load_4d(sm + cQ, &tmQ, &bars[C_WQ], 0, h, c * 64, b);
+      tma_load_4d(sm + cQ + 8192, &tmQ, &bars[C_WQ], 64, h, c * 64, b);
+      n_wq = c + 1;
+    };
+    auto load_kp = [&](int c) {
+      const uint8_t* rec = recs + (size_t)c * kRec;
+      mbar_expect_tx(&bars[C_KP], 16384 + 16384);
+      bulk_load(sm + cP, rec + rP, 16384, &bars[C_KP]);
+      tma_load_4d(sm + cK, &tmK, &bars[C_KP], 0, h, c * 64, b);
+      tma_load_4d(sm + cK + 8192, &tmK, &bars[C_KP], 64, h, c * 64, b);
+      n_kp = c + 1;
+    };
+    load_tv(0);
+    load_wq(0);
+    load_kp(0);
+    bool ok = true;
+    int n_pe = 0;   // PE commits issued
+    for (int c = 0; ok && c < NC; ++c) {
+      const int slot = c & 1;
+      const uint32_t uacc = tmem + tU0 + slot * 64;
+      // M2(c): U' = T_hi V + T_lo V
+      if (!(ok = wait(C_TV, c & 1))) break;
+      tc_fence_after();
+      {
+        const uint32_t tb = smem_u32(sm + cT), vt = smem_u32(sm + cV);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t dt = desc_sw128(tb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
+          const uint64_t dv = desc_sw128(vt + (ks & 3) * 2048, 8192, 1024);
+          mma_bf16(uacc, dt, dv, I_N64, ks > 0);
+        }
+        mma_commit(&bars[C_M2]);
+      }
+      // E(c) = U' - (W'_hi S_hi + W'_hi S_lo + W'_lo S_hi)
+      if (!(ok = wait(C_SREADY, c & 1) && wait(C_WQ, c & 1))) break;
+      tc_fence_after();
+      const uint32_t sb = smem_u32(sm + cS);
+      {
+        const uint32_t wp = smem_u32(sm + cWp);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t dsh = desc_sw128(sb + ks * 2048, 16384, 1024);
+          const uint64_t dsl = desc_sw128(sb + 16384 + ks * 2048, 16384, 1024);
+          const uint64_t dw = desc_sw128(wp + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
+          const uint64_t dwl = desc_sw128(wp + 16384 + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
+          mma_bf16(uacc, dw, dsh, I_NEG, true);
+          mma_bf16(uacc, dw, dsl, I_NEG, true);
+          mma_bf16(uacc, dwl, dsh, I_NEG, true);
+        }
+        mma_commit(&bars[C_E]);
+      }
+      // QS(c) = Q (S_hi + S_lo) once the output of chunk c-1 has read tQS
+      if (c >= 1 && !(ok = wait(C_OUTDONE, (c - 1) & 1))) break;
+      tc_fence_after();
+      {
+        const uint32_t qb = smem_u32(sm + cQ);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t dsh = desc_sw128(sb + ks * 2048, 16384, 1024);
+          const uint64_t dsl = desc_sw128(sb + 16384 + ks * 2048, 16384, 1024);
+          const uint64_t dq = desc_sw128(qb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
+          mma_bf16(tmem + tQS, dq, dsh, I_N64, ks > 0);
+          mma_bf16(tmem + tQS, dq, dsl, I_N64, true);
+        }
+        mma_commit(&bars[C_QS]);
+      }
+      // refill T/V/vectors (M2(c) done; vector slot c+1 was freed by OUTDONE(c-1))
+      if (c + 1 < NC) {
+        if (!(ok = wait(C_M2, c & 1))) break;
+        load_tv(c + 1);
+      }
+      // refill W'/Q (their last reader QS(c) is done)
+      if (c + 1 < NC) {
+        if (!(ok = wait(C_QS, c & 1))) break;
+        load_wq(c + 1);
+      }
+      // M4(c): dS = K^T (uE_hi + uE_lo) ; PE = P_hi E_hi + P_lo E_hi + P_hi E_lo
+      if (!(ok = wait(C_EREADY, c & 1) && wait(C_KP, c & 1))) break;
+      tc_fence_after();
+      {
+        const uint32_t pb = smem_u32(sm + cP), eb = smem_u32(sm + cE), kb = smem_u32(sm + cK);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t uh = desc_sw128(eb + 16384 + ks * 2048, 8192, 1024);
+          const uint64_t ul = desc_sw128(eb + 24576 + ks * 2048, 8192, 1024);
+          const uint64_t dk = desc_sw128(kb + ks * 2048, 8192, 1024);
+          mma_bf16(tmem + tDS, dk, uh, I_DS, ks > 0);
+          mma_bf16(tmem + tDS, dk, ul, I_DS, true);
+        }
+        mma_commit(&bars[C_DS]);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t ph = desc_sw128(pb + ks * 32, 16, 1024);
+          const uint64_t pl = desc_sw128(pb + 8192 + ks * 32, 16, 1024);
+          const uint64_t eh = desc_sw128(eb + ks * 2048, 8192, 1024);
+          const uint64_t el = desc_sw128(eb + 8192 + ks * 2048, 8192, 1024);
+          mma_bf16(tmem + tPE, ph, eh, I_N64, ks > 0);
+          mma_bf16(tmem + tPE, pl, eh, I_N64, true);
+          mma_bf16(tmem + tPE, ph, el, I_N64, true);
+        }
+        mma_commit(&bars[C_PE]);
+        n_pe = c + 1;
+      }
+      // refill K/P (their last reader PE(c) is done)
+      if (c + 1 < NC) {
+        if (!(ok = wait(C_PE, c & 1))) break;
+        load_kp(c + 1);
+      }
+    }
+    if (!ok) set_status(DR_ERR_TIMEOUT);
+    // drain: the last MMAs and every copy issued, so nothing lands after exit
+    if (n_pe > 0) mbar_wait(&bars[C_PE], (n_pe - 1) & 1, kWait / 4);
+    if (n_tv > 0) mbar_wait(&bars[C_TV], (n_tv - 1) & 1, kWait / 4);
+    if (n_wq > 0) mbar_wait(&bars[C_WQ], (n_wq - 1) & 1, kWait / 4);
+    if (n_kp > 0) mbar_wait(&bars[C_KP], (n_kp - 1) & 1, kWait / 4);
+  }
+
+  if (warp == 4) __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (s_abort && tid == 0) set_status(DR_ERR_TIMEOUT);
+  if (warp == 0) tmem_dealloc(tmem, kCarryTmem);
+}
+
+int sm_count() {
+  static int count[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!count[dev]) cudaDeviceGetAttribute(&count[dev], cudaDevAttrMultiProcessorCount, dev);
+  return count[dev];
+}
+
+}  // namespace
+
+bool chunk_tc_split_supported(int variant, int dtype, int dk, int dv, int chunk) {
+  return (variant == DR_GDN || variant == DR_KLA) && dtype == DR_BF16 && dk == 128 &&
+         dv == 128 && chunk == 64;
+}
+
+size_t chunk_tc_split_workspace_bytes(int B, int T, int H) {
+  return (size_t)B * H * ((T + 63) / 64) * kRec;
+}
+
+cudaError_t launch_chunk_tc_split(const FwdArgs& a, void* workspace, cudaStream_t st) {
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, a.q, a.B, a.T, a.H, 128) || !make_map(&mk, a.k, a.B, a.T, a.H, 128) ||
+      !make_map(&mv, a.v, a.B, a.T, a.H, 128))
+    return cudaErrorInvalidValue;
+  const int nsm = sm_count();
+  if (nsm <= 0) return cudaErrorInvalidValue;
+  const long ntask = (long)a.B * a.H * ((a.T + 63) / 64);
+  const int pgrid = (int)(ntask < 2L * nsm ? ntask : 2L * nsm);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e;
+#define DR_PREP(V_)                                                                        \
+  if (a.variant == V_) {                                                                   \
+    e = cudaFuncSetAttribute(chunk_prep_kernel<V_>,                                        \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem); \
+    if (e != cudaSuccess) return e;                                                        \
+    chunk_prep_kernel<V_><<<pgrid, kPrepThreads, kPrepSmem, st>>>(mq, mk, a, ws);          \
+  }
+  DR_PREP(DR_GDN) else DR_PREP(DR_KLA) else return cudaErrorInvalidValue;
+#undef DR_PREP
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(chunk_carry_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kCarrySmem);
+  if (e != cudaSuccess) return e;
+  chunk_carry_kernel<<<a.B * a.H * 2, kCarryThreads, kCarrySmem, st>>>(mq, mk, mv, a, ws);
+  return cudaGetLastError();
+}
+
+}  // namespace dr

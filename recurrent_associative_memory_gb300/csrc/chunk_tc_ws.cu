@@ -44,7 +44,7 @@ constexpr uint32_t wKQ = 0;                 // 2 stages x 32 KB: [K rows 0-63 | 
 constexpr uint32_t wV = 65536;              // V tile [64][64]                          8 KB
 constexpr uint32_t wT = wV + 8192;          // T hi | T lo | Ts hi | Ts lo             32 KB
                                             //   (L/T fp32 and scratch alias it during the inverse)
-constexpr uint32_t wWp = wT + 32768;        // W' [64][128] bf16                       16 KB
+constexpr uint32_t wWp = wT + 32768;        // W' hi [64][128] bf16 (lo: E tiles)      16 KB
 constexpr uint32_t wS = wWp + 16384;        // S hi | S lo [128][64]                   32 KB
 constexpr uint32_t wP = wS + 32768;         // 2 slots x (P hi | P lo)                 32 KB
 constexpr uint32_t wE = wP + 32768;         // E hi | E lo | uE hi | uE lo             32 KB
@@ -511,27 +511,33 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       if (leader) mbar_arrive(&bars[B_TREADY]);
       // ---- gates of the next chunk while M2(c) runs
       if (c + 1 < NC && !gates(c + 1)) break;
-      // ---- W' readout (after M2(c); the W' tile is free once M3(c-1) is done)
+      // ---- W' readout as a bf16 hi/lo pair (after M2(c)).  The hi tile is free once
+      //      M3(c-1) is done; the lo tile borrows the E tiles, free once M4(c-1) is done
+      //      (the carry rewrites them only after M3(c), the lo tile's one reader).
       if (!group_wait(1, 2, 256, &bars[B_M2], c & 1, leader)) break;
       if (c >= 1 && !group_wait(1, 2, 256, &bars[B_M3], (c - 1) & 1, leader)) break;
+      if (c >= 1 && !group_wait(1, 2, 256, &bars[B_M4], (c - 1) & 1, leader)) break;
       tc_fence_after();
       {
         const int i = quad * 16 + lane;
         uint8_t* Wp = sm + wWp + pchalf * 8192;
+        uint8_t* Wl = sm + wE + pchalf * 8192;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
           float w[16];
           tmem_ld16(tmem + lane_off + tWp + pchalf * 64 + 16 * m, w);
           tmem_ld_wait();
           if (lane < 16) {
-            float x[8], y[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              x[e] = w[e];
-              y[e] = w[8 + e];
+            for (int hh = 0; hh < 2; ++hh) {
+              float x[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) x[e] = w[8 * hh + e];
+              uint4 hi, lo;
+              split8(x, hi, lo);
+              *reinterpret_cast<uint4*>(Wp + sw128_offset(i, 16 * m + 8 * hh)) = hi;
+              *reinterpret_cast<uint4*>(Wl + sw128_offset(i, 16 * m + 8 * hh)) = lo;
             }
-            *reinterpret_cast<uint4*>(Wp + sw128_offset(i, 16 * m)) = pack8(x);
-            *reinterpret_cast<uint4*>(Wp + sw128_offset(i, 16 * m + 8)) = pack8(y);
           }
         }
       }
@@ -606,21 +612,23 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         if (!(ok = wait(B_M2, c & 1))) break;      // V tile free again
         issue_v(c + 1);
       }
-      // M3(c): QS = Q (S_hi + S_lo),  E = U' - W' (S_hi + S_lo)
+      // M3(c): QS = Q (S_hi + S_lo),  E = U' - (W'_hi S_hi + W'_hi S_lo + W'_lo S_hi)
       if (!(ok = wait(B_PREP, c & 1) && wait(B_SREADY, c & 1))) break;
       tc_fence_after();
       {
-        const uint32_t sb = smem_u32(sm + wS), wp = smem_u32(sm + wWp);
+        const uint32_t sb = smem_u32(sm + wS), wp = smem_u32(sm + wWp), wl = smem_u32(sm + wE);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint64_t dsh = desc_sw128(sb + ks * 2048, 16384, 1024);
           const uint64_t dsl = desc_sw128(sb + 16384 + ks * 2048, 16384, 1024);
           const uint64_t dq = desc_sw128(kq + (ks >> 2) * 16384 + 8192 + (ks & 3) * 32, 16, 1024);
           const uint64_t dw = desc_sw128(wp + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
+          const uint64_t dwl = desc_sw128(wl + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
           mma_bf16(tmem + tQS, dq, dsh, I_N64, ks > 0);
           mma_bf16(tmem + tQS, dq, dsl, I_N64, true);
           mma_bf16(tmem + tE0 + slot * 64, dw, dsh, I_NEG, true);
           mma_bf16(tmem + tE0 + slot * 64, dw, dsl, I_NEG, true);
+          mma_bf16(tmem + tE0 + slot * 64, dwl, dsh, I_NEG, true);
         }
         mma_commit(&bars[B_M3]);
       }

@@ -31,13 +31,29 @@ def params_for(inp: dict, aux_init=None, aux_final=None, check_finite=False) -> 
                           aux_final=aux_final, check_finite=check_finite)
 
 
+def workspace_for(inp: dict, chunk=None):
+    """Device scratch for dr_chunk_fwd on these inputs (None where no path uses one)."""
+    q, k, v = inp["q"], inp["k"], inp["v"]
+    B, T, H, dk = k.shape
+    dtype = dr.DR_BF16 if q.dtype == torch.bfloat16 else dr.DR_FP32
+    n = dr.dr_chunk_fwd_workspace_bytes(dr.VARIANT_IDS[inp["variant"]], dtype, B, T, H, dk,
+                                        v.shape[-1], chunk or inp.get("chunk", 64))
+    return torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+
+
 def chunk_fwd(inp: dict, *, init_state=None, aux_init=None, chunk=None, want_final=True,
-              check_finite=False, stream=None, out=None, final_state=None, aux_final=None):
-    """Run dr_chunk_fwd on a device input dict; returns (out, final_state, aux_final)."""
+              check_finite=False, stream=None, out=None, final_state=None, aux_final=None,
+              workspace="auto"):
+    """Run dr_chunk_fwd on a device input dict; returns (out, final_state, aux_final).
+
+    ``workspace``: "auto" allocates the scratch the fastest path wants, None runs
+    without one, or a uint8 device tensor to reuse."""
     q, k, v = inp["q"], inp["k"], inp["v"]
     B, T, H, dk = k.shape
     dv = v.shape[-1]
     variant = dr.VARIANT_IDS[inp["variant"]]
+    if isinstance(workspace, str):
+        workspace = workspace_for(inp, chunk)
     if out is None:
         out = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
     if want_final and final_state is None:
@@ -45,6 +61,8 @@ def chunk_fwd(inp: dict, *, init_state=None, aux_init=None, chunk=None, want_fin
     if want_final and aux_final is None and inp["variant"] in ("pgdn", "kdn"):
         aux_final = torch.empty(B, H, dk, dtype=torch.float32, device=q.device)
     p = params_for(inp, aux_init=aux_init, aux_final=aux_final, check_finite=check_finite)
+    if workspace is not None:
+        p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
     st = dr.dr_chunk_fwd(q, k, v, inp["log_alpha"], p, variant, inp.get("eps", 1e-6), init_state,
                          out, final_state, B, T, H, dk, dv, chunk or inp.get("chunk", 64), stream)
     dr.check(st, "dr_chunk_fwd")

@@ -82,7 +82,15 @@ def test_status_strings(dr):
         s = dr.dr_status_string(code)
         assert isinstance(s, str) and s
     assert dr.dr_status_string(12345) == "unknown status"
-    assert dr.dr_chunk_fwd_workspace_bytes(1, 1, 8, 2048, 8, 128, 128, 64) == 0
+    # the two-phase GDN/KLA path: one 66560-byte record per (b, h, 64-token chunk)
+    assert dr.dr_chunk_fwd_workspace_bytes(1, 1, 8, 2048, 8, 128, 128, 64) == 8 * 8 * 32 * 66560
+    assert dr.dr_chunk_fwd_workspace_bytes(0, 1, 2, 65, 3, 128, 128, 64) == 2 * 3 * 2 * 66560
+    for args in [(1, 0, 8, 2048, 8, 128, 128, 64), (1, 1, 8, 2048, 8, 64, 128, 64),
+                 (1, 1, 8, 2048, 8, 128, 128, 32), (2, 1, 8, 2048, 8, 128, 128, 64),
+                 (3, 1, 8, 2048, 8, 128, 128, 64)]:
+        assert dr.dr_chunk_fwd_workspace_bytes(*args) == 0, args
+    assert dr.dr_chunk_fwd_path(dr.DR_KLA, dr.DR_BF16, 128, 128, 64) == "tc_split"
+    assert dr.dr_chunk_fwd_path(dr.DR_PGDN, dr.DR_BF16, 128, 128, 64) == "tc"
     assert dr.dr_chunk_fwd_path(dr.DR_KLA, dr.DR_FP32, 64, 64, 64) == "simt"
 
 
@@ -129,3 +137,12 @@ def test_decode_rejects_bad_arguments(dr):
     assert dec(dk=32) == dr.DR_ERR_SHAPE
     assert dec(state=MIS) == dr.DR_ERR_ALIGN
     assert dec(dtype=2) == dr.DR_ERR_DTYPE
+
+
+def test_chunk_fwd_workspace_checks(dr):
+    """A workspace that is too small or misaligned is refused before any launch."""
+    need = dr.dr_chunk_fwd_workspace_bytes(dr.DR_KLA, dr.DR_BF16, 1, 8, 1, 128, 128, 64)
+    assert need == 66560
+    base = dict(dtype=dr.DR_BF16, dk=128, dv=128)
+    assert fwd(dr, workspace=A, workspace_bytes=need - 16, **base) == dr.DR_ERR_WORKSPACE
+    assert fwd(dr, workspace=A + 16, workspace_bytes=need, **base) == dr.DR_ERR_ALIGN

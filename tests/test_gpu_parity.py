@@ -43,12 +43,13 @@ def random_state(inp, seed=3):
     return S0, aux0
 
 
-def check_fwd(rt, inp, S0=None, aux0=None, pairs=None, chunk=None):
+def check_fwd(rt, inp, S0=None, aux0=None, pairs=None, chunk=None, workspace="auto"):
     dr, runner = rt
     dev = runner.to_device(inp)
     S0d = None if S0 is None else S0.cuda()
     aux0d = None if aux0 is None else aux0.cuda()
-    out, S, aux = runner.chunk_fwd(dev, init_state=S0d, aux_init=aux0d, chunk=chunk)
+    out, S, aux = runner.chunk_fwd(dev, init_state=S0d, aux_init=aux0d, chunk=chunk,
+                                   workspace=workspace)
     torch.cuda.synchronize()
     assert dr.dr_get_device_status() == 0
     o_ref, S_ref, aux_ref = run_oracle(inp, S0, aux0, pairs)
@@ -220,14 +221,60 @@ def test_check_finite_reports_nonfinite(rt):
 @pytest.mark.parametrize("variant", ["gdn", "kla", "pgdn"])
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 333])
 def test_tc_path_ragged_with_state(rt, variant, T):
-    """bf16, dk = dv = 128, chunk 64 runs on the tcgen05 kernel: ragged tails,
-    nonzero initial state and aux state."""
+    """bf16, dk = dv = 128, chunk 64 runs on the tcgen05 kernels (GDN/KLA: the
+    two-phase path with a workspace): ragged tails, nonzero initial and aux state."""
     dr, runner = rt
-    want = "tc" if variant == "pgdn" else "tc_ws"
+    want = "tc" if variant == "pgdn" else "tc_split"
     assert dr.dr_chunk_fwd_path(dr.VARIANT_IDS[variant], dr.DR_BF16, 128, 128, 64) == want
     inp = small_inputs(variant, "bf16", B=2, T=T, H=3, seed=100 + T)
     S0, aux0 = random_state(inp, seed=T)
     check_fwd(rt, inp, S0, aux0)
+
+
+@pytest.mark.parametrize("variant", ["gdn", "kla"])
+@pytest.mark.parametrize("T", [1, 65, 333])
+def test_tc_single_kernel_path_without_workspace(rt, variant, T):
+    """Without a workspace GDN/KLA take the warp-specialised single-kernel path."""
+    inp = small_inputs(variant, "bf16", B=2, T=T, H=3, seed=200 + T)
+    S0, _ = random_state(inp, seed=T)
+    check_fwd(rt, inp, S0, workspace=None)
+
+
+@pytest.mark.parametrize("workspace", ["auto", None])
+@pytest.mark.parametrize("variant", ["gdn", "kla"])
+def test_tc_raw_key_cancellation(rt, variant, workspace):
+    """Raw GDN keys with |k|^2 ~ 128 make E = U' - W' S cancel heavily: the
+    inputs on which a single-bf16 W' gave a 9.8e-3 state error (a CPU emulation
+    of the chunk algebra reproduces it; the hi/lo W' brings it to ~2e-5)."""
+    inp = small_inputs(variant, "bf16", B=2, T=65, H=3, seed=265)
+    S0, _ = random_state(inp, seed=65)
+    check_fwd(rt, inp, S0, workspace=workspace)
+
+
+def test_tc_pgdn_raw_keys(rt):
+    """PGDN on the phase-sequential tensor-core kernel with un-normalised keys."""
+    inp = small_inputs("pgdn", "bf16", B=2, T=130, H=2, seed=266, k_l2norm=False)
+    S0, aux0 = random_state(inp, seed=66)
+    check_fwd(rt, inp, S0, aux0)
+
+
+def test_tc_split_path_many_tasks(rt):
+    """More chunk tasks than two per SM, so every prep CTA loops over several
+    (b, h, chunk) records and both K/Q stages are reused."""
+    inp = small_inputs("kla", "bf16", B=6, T=2048 + 17, H=8, seed=91)
+    check_fwd(rt, inp, pairs=[(0, 0), (5, 7), (3, 2)])
+
+
+def test_tc_split_workspace_reuse_matches_fresh(rt):
+    """A reused (dirty) workspace gives the same bits as a fresh one."""
+    dr, runner = rt
+    dev = runner.to_device(small_inputs("gdn", "bf16", B=2, T=300, H=4, seed=5))
+    ws = runner.workspace_for(dev)
+    ws.fill_(0xA5)
+    o1, s1, _ = runner.chunk_fwd(dev, workspace=ws)
+    o2, s2, _ = runner.chunk_fwd(dev, workspace=runner.workspace_for(dev))
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
 
 
 def test_tc_path_unnormalised_gdn_strong_keys(rt):
