@@ -161,6 +161,37 @@ int dr_decode_step(const void *q, const void *k, const void *v, const float *log
 size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H, int dk, int dv,
                                     int chunk);
 
+/*
+ * Same forward as dr_chunk_fwd on the two-phase tensor-core path (GDN, KLA;
+ * bf16, dk = dv = 128, chunk 64), for callers that cannot allocate device
+ * memory: code that runs where cudaMalloc is off limits (a host framework that
+ * owns every byte of device memory through its own allocator, a real-time loop
+ * that must not take cudaMalloc's implicit device synchronisation, a plug-in
+ * handed only its input and output buffers).  The paper has no counterpart:
+ * this is an interface convenience, not part of the method.
+ *
+ * The per-chunk records live in one library-owned device array of
+ * DR_NOALLOC_SCRATCH_BYTES, created with the library's CUDA module on every
+ * device that loads it and held until the process exits.  The caller still
+ * passes every input and output; gp->workspace is ignored.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind (nothing in it has to start at zero).  Calls that overlap on the
+ *     GPU -- two streams, or two host threads -- race on it: serialise them.
+ * Returns DR_ERR_UNSUPPORTED for other variants, dtypes or shapes (dr_chunk_fwd
+ * needs no workspace for those), DR_ERR_WORKSPACE when the records
+ * (dr_chunk_fwd_workspace_bytes) would exceed DR_NOALLOC_SCRATCH_BYTES, i.e.
+ * B H ceil(T/64) > 1008, otherwise whatever dr_chunk_fwd returns.
+ */
+#define DR_NOALLOC_SCRATCH_BYTES (64u << 20)
+int dr_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *log_alpha,
+                         const dr_params *gp, int variant, float eps,
+                         const float *init_state, void *out, float *final_state,
+                         int B, int T, int H, int dk, int dv, int chunk, dr_stream_t stream);
+
 /* Synchronises `stream`, returns and clears the sticky device status
  * (DR_OK, DR_ERR_NONFINITE or DR_ERR_TIMEOUT), or DR_ERR_CUDA. */
 int dr_get_device_status(dr_stream_t stream);

@@ -67,6 +67,11 @@ _lib.dr_status_string.argtypes = [c_int]
 _lib.dr_status_string.restype = c_char_p
 _lib.dr_chunk_fwd_path.argtypes = [c_int] * 5
 _lib.dr_chunk_fwd_path.restype = c_char_p
+_lib.dr_chunk_fwd_noalloc.argtypes = _lib.dr_chunk_fwd.argtypes
+_lib.dr_chunk_fwd_noalloc.restype = c_int
+
+# size of the library-owned scratch behind dr_chunk_fwd_noalloc (include/dr.h)
+DR_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class DrError(RuntimeError):
@@ -150,3 +155,12 @@ def dr_status_string(status: int) -> str:
 
 def dr_chunk_fwd_path(variant, dtype, dk, dv, chunk) -> str:
     return _lib.dr_chunk_fwd_path(variant, dtype, dk, dv, chunk).decode()
+
+
+def dr_chunk_fwd_noalloc(q, k, v, log_alpha, params: DrParams, variant: int, eps: float,
+                         init_state, out, final_state, B: int, T: int, H: int, dk: int, dv: int,
+                         chunk: int, stream=None) -> int:
+    return _lib.dr_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                                     ctypes.byref(params), int(variant), float(eps),
+                                     _ptr(init_state), _ptr(out), _ptr(final_state), B, T, H, dk,
+                                     dv, chunk, _stream(stream))

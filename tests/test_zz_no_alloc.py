@@ -1,0 +1,65 @@
+"""dr_chunk_fwd_noalloc: the two-phase forward on the library's own scratch.
+
+Some callers cannot allocate device memory (a framework whose allocator owns
+all of it, a real-time loop that cannot take cudaMalloc's synchronisation, a
+plug-in given only its input and output buffers), so they cannot supply the
+workspace dr_chunk_fwd wants for its fastest path.  This entry point keeps the
+per-chunk records in a fixed library-owned device array instead.
+
+The GPU test calls it through the C ABI twice in a row, on different inputs, so
+the second call runs over the first call's leftover records, and compares each
+result with dr_chunk_fwd on a caller-allocated workspace within the parity
+tolerance.  The host test covers the refusals that happen before any CUDA call.
+This file is collected last on purpose.
+"""
+
+import pytest
+import torch
+
+from parity_util import TOL, np64, rel_err
+from recurrent_associative_memory_gb300 import workloads as W
+
+A = 1 << 20   # a 16-byte aligned address that is never dereferenced (refused calls only)
+
+
+def test_noalloc_refusals_on_host():
+    from recurrent_associative_memory_gb300 import dr
+
+    def call(B=1, T=64, H=1, dk=128, dv=128, chunk=64, dtype=None, variant=None):
+        p = dr.make_params(dtype=dr.DR_BF16 if dtype is None else dtype, eta=A)
+        return dr.dr_chunk_fwd_noalloc(A, A, A, A, p, dr.DR_KLA if variant is None else variant,
+                                       1e-6, None, A, None, B, T, H, dk, dv, chunk, stream=0)
+
+    max_records = dr.DR_NOALLOC_SCRATCH_BYTES // 66560
+    assert max_records == 1008
+    assert call(T=64 * (max_records + 1)) == dr.DR_ERR_WORKSPACE
+    assert call(B=2, T=64 * 64, H=8) == dr.DR_ERR_WORKSPACE          # 2*8*64 = 1024 records
+    assert call(dk=64) == dr.DR_ERR_UNSUPPORTED
+    assert call(chunk=32) == dr.DR_ERR_UNSUPPORTED
+    assert call(dtype=dr.DR_FP32) == dr.DR_ERR_UNSUPPORTED
+    assert call(variant=dr.DR_KDN) == dr.DR_ERR_UNSUPPORTED
+    assert call(T=0) == dr.DR_ERR_SHAPE
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_chunk_fwd_on_two_calls():
+    from recurrent_associative_memory_gb300 import dr, runner
+
+    cases = [("kla", 2, 333, 3, 31), ("gdn", 1, 64 * 40 + 9, 8, 32)]   # 36 then 328 records
+    g = torch.Generator().manual_seed(30)
+    for variant, B, T, H, seed in cases:
+        wl = W.small("gdn_kla_bf16", B=B, T=T, H=H, seed=seed)
+        dev = runner.to_device(W.generate(wl, variant))
+        S0 = (0.3 * torch.randn(B, H, 128, 128, generator=g)).cuda()
+        ref_out, ref_S, _ = runner.chunk_fwd(dev, init_state=S0)   # dr_chunk_fwd + own workspace
+        out = torch.empty_like(ref_out)
+        S = torch.empty_like(ref_S)
+        st = dr.dr_chunk_fwd_noalloc(dev["q"], dev["k"], dev["v"], dev["log_alpha"],
+                                     runner.params_for(dev), dr.VARIANT_IDS[variant],
+                                     dev.get("eps", 1e-6), S0, out, S, B, T, H, 128, 128, 64)
+        dr.check(st, "dr_chunk_fwd_noalloc")
+        torch.cuda.synchronize()
+        assert dr.dr_get_device_status() == 0
+        eo = rel_err(np64(out), np64(ref_out))
+        es = rel_err(np64(S), np64(ref_S))
+        assert eo <= TOL["bf16"] and es <= TOL["bf16"], (variant, eo, es)
