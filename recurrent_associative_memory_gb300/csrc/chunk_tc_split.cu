@@ -43,7 +43,7 @@ constexpr int LDX = 36;                     // fp32 scratch row stride
 
 // ---- per-chunk record in the workspace (bytes); 128B-swizzled tile images
 constexpr uint32_t rT = 0;          // T hi | T lo       (64 x 64 bf16 each)
-constexpr uint32_t rWp = 16384;     // W' hi k-blocks 0 | 1, then W' lo k-blocks 0 | 1
+constexpr uint32_t rWp = 16384;     // W'^T hi [128 dk][64 tok], then W'^T lo
 constexpr uint32_t rP = 49152;      // P hi | P lo
 constexpr uint32_t rVec = 65536;    // fp32 [0,64) e^g qn ; [64,128) e^{g_C-g} c ; [128] gamma_C
 constexpr uint32_t kRec = 66560;
@@ -55,13 +55,13 @@ constexpr uint32_t pT = 65536;              // T hi | T lo | Ts hi | Ts lo (L/T 
 constexpr uint32_t pVec = pT + 32768;       // vectors, 4 KB
 constexpr uint32_t kPrepSmem = pVec + 4096 + 1024;
 constexpr uint32_t tG0 = 0;                 // 2 Gram slots, M=128 x 64
-constexpr uint32_t tPWp = 128;              // W', M=64 x 128
+constexpr uint32_t tPWt = 128;              // W'^T = K^T Ts^T, M=128 x 64
 constexpr uint32_t kPrepTmem = 256;
 
 constexpr uint32_t I_GRAM = idesc_bf16(128, 64, 0, 0);
-constexpr uint32_t I_WP = idesc_bf16(64, 128, 0, 1);
+constexpr uint32_t I_WT = idesc_bf16(128, 64, 1, 0);     // A = K (MN-major), B = Ts (K-major)
 constexpr uint32_t I_N64 = idesc_bf16(64, 64, 0, 1);
-constexpr uint32_t I_NEG = idesc_bf16(64, 64, 0, 1, 1);
+constexpr uint32_t I_NEGT = idesc_bf16(64, 64, 1, 1, 1);    // A = W'^T (MN-major), negated
 constexpr uint32_t I_DS = idesc_bf16(128, 64, 1, 1);
 
 enum { P_KQ0, P_KQ1, P_G0, P_G1, P_W, P_GFREE0, P_GFREE1, P_TREADY, P_WFREE, P_COUNT };
@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   float* vqq = vkk + 64;
   float* vla = vqq + 64;
   float* veta = vla + 64;
+  float* vcf = veta + 64;   // c_j e^{g_e(J) - g_j}: column factor of the off-diagonal blocks
   float* LT = reinterpret_cast<float*>(sm + pT);
   float* XS = LT + 64 * LDL;
 
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       const int t = task_of(k);
       uint8_t* rec = ws + (size_t)t * kRec;   // tasks are numbered (b h) major, chunk minor
       const int st = k & 1;
-      const uint8_t* KQ = sm + pKQ + st * 32768;
+      uint8_t* KQ = sm + pKQ + st * 32768;
 
       // ---- gates: decay, norms, write coefficients, the carry's row vectors
       if (!group_wait(&bars[P_KQ0 + st], (k >> 1) & 1)) break;
@@ -212,6 +213,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         const float eg = __expf(gi);
         vks[i] = eg * cr;
         vF[i] = __expf(vg[i | 15] - gi);
+        vcf[i] = coef * vF[i];
         float* rv = reinterpret_cast<float*>(rec + rVec);
         rv[i] = eg * qn;
         rv[64 + i] = __expf(gC - gi) * coef;
@@ -219,7 +221,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       }
       named_bar(1, 256);
 
-      // ---- Gram readout -> L (fp32, smem) and P (bf16 hi/lo, record)
+      // ---- Gram readout -> L (fp32, smem) and P (bf16 hi/lo, staged in the Q half of
+      //      the K/Q stage, which the Gram was the last to read, then one bulk copy)
+      if (leader) bulk_wait_read<0>();   // the previous task's W' copy has left the T region
       if (!group_wait(&bars[P_G0 + st], (k >> 1) & 1)) break;
       tc_fence_after();
       {
@@ -230,19 +234,27 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         tmem_ld_wait();
         const float gi = vg[i];
         const float rs = (row < 64) ? vcr[i] : vqn[i];
-        float fb[2];
+        // block (I, J) of 16 x 16: J < I factors through the end of sub-chunk J
+        // (row factor e^{g_i - g_e(J)} <= 1, column factor c_j e^{g_e(J) - g_j} <= 1);
+        // J = I takes e^{g_i - g_j} directly on and below the diagonal; J > I is 0
+        float x[32];
 #pragma unroll
         for (int jb = 0; jb < 2; ++jb) {
           const int J = pchalf * 2 + jb;
-          fb[jb] = (J < I) ? __expf(gi - vg[16 * J + 15]) : 0.f;
-        }
-        float x[32];
+          if (J < I) {
+            const float rf = rs * __expf(gi - vg[16 * J + 15]);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int j = pchalf * 32 + e, J = j >> 4;
-          const float ed = __expf(fminf(gi - vg[j], 0.f));
-          const float f = (J < I) ? fb[e >> 4] * vF[j] : ((J == I && j <= i) ? ed : 0.f);
-          x[e] = gv[e] * rs * va[j] * f;
+            for (int e = 0; e < 16; ++e) x[16 * jb + e] = gv[16 * jb + e] * rf * vcf[16 * J + e];
+          } else if (J == I) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int j = 16 * J + e;
+              x[16 * jb + e] = (j <= i) ? gv[16 * jb + e] * rs * va[j] * __expf(gi - vg[j]) : 0.f;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[16 * jb + e] = 0.f;
+          }
         }
         if (row < 64) {
 #pragma unroll
@@ -253,7 +265,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
                             j + 2 < i ? x[e + 2] : 0.f, j + 3 < i ? x[e + 3] : 0.f);
           }
         } else {
-          uint8_t* Pg = rec + rP;
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
             float y[8];
@@ -261,14 +272,20 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
             for (int e = 0; e < 8; ++e) y[e] = x[8 * m + e];
             uint4 hi, lo;
             split8(y, hi, lo);
-            *reinterpret_cast<uint4*>(Pg + sw128_offset(i, pchalf * 32 + 8 * m)) = hi;
-            *reinterpret_cast<uint4*>(Pg + 8192 + sw128_offset(i, pchalf * 32 + 8 * m)) = lo;
+            *reinterpret_cast<uint4*>(KQ + 8192 + sw128_offset(i, pchalf * 32 + 8 * m)) = hi;
+            *reinterpret_cast<uint4*>(KQ + 24576 + sw128_offset(i, pchalf * 32 + 8 * m)) = lo;
           }
         }
       }
       tc_fence_before();
+      fence_proxy_async();
       named_bar(1, 256);
-      if (leader) mbar_arrive(&bars[P_GFREE0 + st]);
+      if (leader) {
+        mbar_arrive(&bars[P_GFREE0 + st]);
+        bulk_store(rec + rP, KQ + 8192, 8192);
+        bulk_store(rec + rP + 8192, KQ + 24576, 8192);
+        bulk_commit();
+      }
       // ---- T = (I + L)^-1 in place: diagonal 16x16 blocks (threads 0-63, one column each)
       {
         const int j = ptid & 15, I = (ptid >> 4) & 3, r0 = 16 * I;
@@ -336,7 +353,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         }
         named_bar(1, 256);
         uint8_t* Tt = sm + pT;
-        uint8_t* Tg = rec + rT;
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
           float x[8], y[8];
@@ -348,8 +364,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
           const uint32_t off = sw128_offset(i, c0 + 8 * m);
           uint4 hi, lo;
           split8(x, hi, lo);
-          *reinterpret_cast<uint4*>(Tg + off) = hi;
-          *reinterpret_cast<uint4*>(Tg + 8192 + off) = lo;
+          *reinterpret_cast<uint4*>(Tt + off) = hi;
+          *reinterpret_cast<uint4*>(Tt + 8192 + off) = lo;
           split8(y, hi, lo);
           *reinterpret_cast<uint4*>(Tt + 16384 + off) = hi;
           *reinterpret_cast<uint4*>(Tt + 24576 + off) = lo;
@@ -357,36 +373,44 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       }
       fence_proxy_async();
       named_bar(1, 256);
-      if (leader) mbar_arrive(&bars[P_TREADY]);
-      // ---- W' readout -> record
+      if (leader) {
+        bulk_store(rec + rT, sm + pT, 16384);
+        bulk_commit();
+        bulk_wait_read<1>();   // P has left the K/Q stage, which W'(k) then frees for a reload
+        mbar_arrive(&bars[P_TREADY]);
+      }
+      // ---- W'^T readout (row = dk index = TMEM lane, 32 tokens per thread), staged
+      //      over T / Ts (both read by now), then one bulk copy into the record
+      if (leader) bulk_wait_read<0>();
       if (!group_wait(&bars[P_W], k & 1)) break;
       tc_fence_after();
       {
-        const int i = quad * 16 + lane;
-        uint8_t* Wg = rec + rWp + pchalf * 8192;
+        const int r = quad * 32 + lane;
+        uint8_t* Wg = sm + pT;
+        float w[32];
+        ld32cols(tmem + lane_off + tPWt + pchalf * 32, w);
+        tmem_ld_wait();
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-          float w[16];
-          tmem_ld16(tmem + lane_off + tPWp + pchalf * 64 + 16 * m, w);
-          tmem_ld_wait();
-          if (lane < 16) {
+          float x[8];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              float x[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) x[e] = w[8 * hh + e];
-              uint4 hi, lo;
-              split8(x, hi, lo);
-              *reinterpret_cast<uint4*>(Wg + sw128_offset(i, 16 * m + 8 * hh)) = hi;
-              *reinterpret_cast<uint4*>(Wg + 16384 + sw128_offset(i, 16 * m + 8 * hh)) = lo;
-            }
-          }
+          for (int e = 0; e < 8; ++e) x[e] = w[8 * m + e];
+          uint4 hi, lo;
+          split8(x, hi, lo);
+          *reinterpret_cast<uint4*>(Wg + sw128_offset(r, pchalf * 32 + 8 * m)) = hi;
+          *reinterpret_cast<uint4*>(Wg + 16384 + sw128_offset(r, pchalf * 32 + 8 * m)) = lo;
         }
       }
       tc_fence_before();
+      fence_proxy_async();
       named_bar(1, 256);
-      if (leader) mbar_arrive(&bars[P_WFREE]);
+      if (leader) {
+        mbar_arrive(&bars[P_WFREE]);
+        bulk_store(rec + rWp, sm + pT, 32768);
+        bulk_commit();
+      }
     }
+    if (leader) bulk_wait_all();   // every record byte is in global memory before exit
   } else if (lane == 0) {
     // ===================================================================== issue lane
     auto wait = [&](int id, uint32_t parity) -> bool {
@@ -442,7 +466,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         for (int ks = 0; ks < 8; ++ks) {
           const uint64_t dts = desc_sw128(tb + 16384 + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
           const uint64_t dk = desc_sw128(kq + (ks & 3) * 2048, 16384, 1024);
-          mma_bf16(tmem + tPWp, dts, dk, I_WP, ks > 0);
+          mma_bf16(tmem + tPWt, dk, dts, I_WT, ks > 0);
         }
         mma_commit(&bars[P_W]);
         w_done = k + 1;
@@ -468,17 +492,25 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 }
 
 // ================================================================= chunk_carry
-constexpr int kCarryThreads = 5 * 32;       // warps 0-3 state, warp 4 issue
+// Roles (15 warps):
+//   state  warps 0-7   thread = one state row (TMEM lane) x 32 of the CTA's 64
+//                      columns: E readout -> E, u.E tiles; S <- gamma_C S + dS.
+//                      Its leader issues the two MMAs on the carry's critical
+//                      path itself, E(c+1) and dS(c), so no hand-off sits there.
+//   output warps 9-12  o = e^g qn . QS + PE for every row of the chunk.
+//   issue  warp 8      copies (record, K, Q, V) and the off-path MMAs U' = T V,
+//                      QS = Q S, PE = P E.
+// The row vectors (e^g qn, u, gamma_C) are read from the record in global
+// memory, one chunk ahead, so no shared buffer of them needs recycling.
+constexpr int kCarryThreads = 13 * 32;
 constexpr uint32_t cT = 0;                  // T hi | T lo              16 KB
 constexpr uint32_t cV = 16384;              // V [64 tok][64 col]       8 KB
-constexpr uint32_t cWp = 24576;             // W' hi kb0|kb1, lo kb0|kb1  32 KB
-constexpr uint32_t cQ = 57344;              // Q kb0 | kb1              16 KB
-constexpr uint32_t cK = 73728;              // K kb0 | kb1              16 KB
-constexpr uint32_t cP = 90112;              // P hi | P lo              16 KB
-constexpr uint32_t cS = 106496;             // S hi | S lo [128][64]    32 KB
-constexpr uint32_t cE = 139264;             // E hi | E lo | uE hi | uE lo   32 KB
-constexpr uint32_t cVec = 172032;           // 2 slots x 1 KB record vectors
-constexpr uint32_t kCarrySmem = cVec + 2048 + 1024;
+constexpr uint32_t cW = 24576;              // 2 slots x W' [hi kb0|kb1, lo kb0|kb1]   64 KB
+constexpr uint32_t cQ = 90112;              // Q kb0 | kb1              16 KB
+constexpr uint32_t cKP = 106496;            // K kb0 | K kb1 | P hi | P lo   32 KB
+constexpr uint32_t cS = 139264;             // S hi | S lo [128][64]    32 KB
+constexpr uint32_t cE = 172032;             // E hi | E lo | uE hi | uE lo   32 KB
+constexpr uint32_t kCarrySmem = cE + 32768 + 1024;
 constexpr uint32_t tU0 = 0;                 // 2 slots M=64 x 64: U', then E
 constexpr uint32_t tQS = 128;               // M=64 x 64
 constexpr uint32_t tPE = 192;               // M=64 x 64
@@ -486,9 +518,9 @@ constexpr uint32_t tDS = 256;               // M=128 x 64
 constexpr uint32_t kCarryTmem = 512;
 
 enum {
-  C_TV, C_WQ, C_KP,                         // copies landed
+  C_TV, C_W0, C_W1, C_Q, C_KP,              // copies landed
   C_M2, C_E, C_QS, C_DS, C_PE,              // MMAs complete
-  C_SREADY, C_EREADY, C_OUTDONE,            // state-group hand-offs
+  C_SREADY, C_EREADY, C_OUTDONE,            // group hand-offs to the issue lane
   C_COUNT
 };
 
@@ -502,7 +534,6 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
   __shared__ uint64_t bars[C_COUNT];
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int s_abort;
-  __shared__ volatile int s_ok;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int half = blockIdx.x & 1;
@@ -525,166 +556,256 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
 
-  if (warp < 4) {
+  // Every thread of a group waits itself (bounded), then one named barrier makes
+  // the outcome uniform: a timeout anywhere sets s_abort, which all read after it.
+  auto group_wait2 = [&](int bar_id, int nthreads, uint64_t* b1, uint32_t p1, uint64_t* b2,
+                         uint32_t p2) -> bool {
+    if (!s_abort) {
+      bool ok = mbar_wait(b1, p1, kWait);
+      if (ok && b2) ok = mbar_wait(b2, p2, kWait);
+      if (!ok) s_abort = 1;
+    }
+    named_bar(bar_id, nthreads);
+    return !s_abort;
+  };
+
+  if (warp < 8) {
     // ===================================================================== state warps
-    // thread = row r of the state slice (TMEM lane r), all 64 columns
-    const int quad = warp, srow = tid;
+    const int quad = warp & 3, hc = warp >> 2;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const bool leader = (tid == 0);
-    auto group_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      if (leader) {
-        bool ok = !s_abort && mbar_wait(bar, parity, kWait);
-        if (!ok) s_abort = 1;
-        s_ok = ok ? 1 : 0;
-      }
-      named_bar(1, 128);
-      const bool ok = s_ok != 0;
-      named_bar(1, 128);
-      return ok;
-    };
-    float S[64];
+    const int srow = quad * 32 + lane;          // state row (dk index) = TMEM lane
+    const int erow = quad * 16 + (lane & 15);   // token row of E (M=64 layout)
+    const int ecol = 32 * hc + ((lane < 16) ? 0 : 16);
+    float S[32];
     auto store_state_tiles = [&]() {
       uint8_t* sS = sm + cS;
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
+      for (int m = 0; m < 4; ++m) {
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = S[8 * m + e];
         uint4 hi, lo;
         split8(x, hi, lo);
-        *reinterpret_cast<uint4*>(sS + sw128_offset(srow, 8 * m)) = hi;
-        *reinterpret_cast<uint4*>(sS + 16384 + sw128_offset(srow, 8 * m)) = lo;
+        *reinterpret_cast<uint4*>(sS + sw128_offset(srow, 32 * hc + 8 * m)) = hi;
+        *reinterpret_cast<uint4*>(sS + 16384 + sw128_offset(srow, 32 * hc + 8 * m)) = lo;
       }
     };
-    {
-      const long base = ((long)bh * 128 + srow) * a.dv + half * 64;
+    // E(c) = U' - (W'_hi S_hi + W'_hi S_lo + W'_lo S_hi), issued by the leader
+    auto issue_e = [&](int c) {
+      tc_fence_after();
+      const uint32_t sb = smem_u32(sm + cS), wp = smem_u32(sm + cW + (c & 1) * 32768);
+      const uint32_t uacc = tmem + tU0 + (c & 1) * 64;
 #pragma unroll
-      for (int j = 0; j < 64; j += 4) {
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t dsh = desc_sw128(sb + ks * 2048, 16384, 1024);
+        const uint64_t dsl = desc_sw128(sb + 16384 + ks * 2048, 16384, 1024);
+        const uint64_t dw = desc_sw128(wp + ks * 2048, 16384, 1024);
+        const uint64_t dwl = desc_sw128(wp + 16384 + ks * 2048, 16384, 1024);
+        mma_bf16(uacc, dw, dsh, I_NEGT, true);
+        mma_bf16(uacc, dw, dsl, I_NEGT, true);
+        mma_bf16(uacc, dwl, dsh, I_NEGT, true);
+      }
+      mma_commit(&bars[C_E]);
+    };
+    {
+      const long base = ((long)bh * 128 + srow) * a.dv + half * 64 + 32 * hc;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
         const float4 v = a.S0 ? *reinterpret_cast<const float4*>(a.S0 + base + j)
                               : make_float4(0.f, 0.f, 0.f, 0.f);
         S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
       }
       store_state_tiles();
     }
+    tc_fence_before();
     fence_proxy_async();
-    named_bar(1, 128);
-    if (leader) mbar_arrive(&bars[C_SREADY]);   // S tiles of chunk 0
+    named_bar(1, 256);
+    bool ok = true;
+    if (leader) {
+      ok = mbar_wait(&bars[C_M2], 0, kWait) && mbar_wait(&bars[C_W0], 0, kWait);
+      if (ok) {
+        issue_e(0);
+        mbar_arrive(&bars[C_SREADY]);   // S tiles of chunk 0 (for QS(0))
+      } else {
+        s_abort = 1;
+      }
+    }
+    // row vectors of chunk 0: u (this thread's E row) and gamma_C
+    float u_cur = reinterpret_cast<const float*>(recs + rVec)[64 + erow];
+    float g_cur = reinterpret_cast<const float*>(recs + rVec)[128];
     bool bad = false;
-    bool ok = group_wait(&bars[C_TV], 0);       // vectors of chunk 0
 
-    for (int c = 0; ok && c < NC; ++c) {
+    for (int c = 0; c < NC; ++c) {
       const int slot = c & 1;
-      const float* vqs = reinterpret_cast<const float*>(sm + cVec + slot * 1024);
-      const float* vu = vqs + 64;
-      const int t0 = c * 64, Cc = min(64, a.T - t0);
-      const int i = quad * 16 + lane;           // token row held by lanes 0-15 (M=64 layout)
-      // ---- E -> E and u.E hi/lo tiles
-      if (!(ok = group_wait(&bars[C_E], c & 1))) break;
+      float u_nxt = 0.f, g_nxt = 0.f;
+      if (c + 1 < NC) {   // one chunk ahead; consumed next iteration
+        const float* rv = reinterpret_cast<const float*>(recs + (size_t)(c + 1) * kRec + rVec);
+        u_nxt = rv[64 + erow];
+        g_nxt = rv[128];
+      }
+      // ---- E -> E and u.E hi/lo tiles (lanes 16-31 take columns 16-31 of the row)
+      if (!(ok = group_wait2(1, 256, &bars[C_E], c & 1, nullptr, 0))) break;
       tc_fence_after();
       {
-        const float u = vu[i & 63];
-        uint8_t* Et = sm + cE;
-        float ev[64];
+        float ev[32], x[16];
+        float t16[16];
+        tmem_ld16(tmem + lane_off + tU0 + slot * 64 + 32 * hc, t16);
 #pragma unroll
-        for (int hf = 0; hf < 4; ++hf) {
-          float t16[16];
-          tmem_ld16(tmem + lane_off + tU0 + slot * 64 + 16 * hf, t16);
+        for (int e = 0; e < 16; ++e) ev[e] = t16[e];
+        tmem_ld16(tmem + lane_off + tU0 + slot * 64 + 32 * hc + 16, t16);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) ev[16 * hf + e] = t16[e];
-        }
+        for (int e = 0; e < 16; ++e) ev[16 + e] = t16[e];
         tmem_ld_wait();
-        if (lane < 16) {
 #pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            float x[8], y[8];
+        for (int e = 0; e < 16; ++e) {
+          const float y = __shfl_sync(0xffffffffu, ev[16 + e], lane & 15);
+          x[e] = (lane < 16) ? ev[e] : y;
+        }
+        uint8_t* Et = sm + cE;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              x[e] = ev[8 * m + e];
-              y[e] = u * x[e];
-            }
-            const uint32_t off = sw128_offset(i, 8 * m);
-            uint4 hi, lo;
-            split8(x, hi, lo);
-            *reinterpret_cast<uint4*>(Et + off) = hi;
-            *reinterpret_cast<uint4*>(Et + 8192 + off) = lo;
-            split8(y, hi, lo);
-            *reinterpret_cast<uint4*>(Et + 16384 + off) = hi;
-            *reinterpret_cast<uint4*>(Et + 24576 + off) = lo;
+        for (int m = 0; m < 2; ++m) {
+          float p[8], q8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            p[e] = x[8 * m + e];
+            q8[e] = u_cur * p[e];
           }
+          const uint32_t off = sw128_offset(erow, ecol + 8 * m);
+          uint4 hi, lo;
+          split8(p, hi, lo);
+          *reinterpret_cast<uint4*>(Et + off) = hi;
+          *reinterpret_cast<uint4*>(Et + 8192 + off) = lo;
+          split8(q8, hi, lo);
+          *reinterpret_cast<uint4*>(Et + 16384 + off) = hi;
+          *reinterpret_cast<uint4*>(Et + 24576 + off) = lo;
         }
       }
       tc_fence_before();
       fence_proxy_async();
-      named_bar(1, 128);
-      if (leader) mbar_arrive(&bars[C_EREADY]);
-      // ---- S <- gamma_C S + dS, then the S tiles of chunk c+1
-      if (!(ok = group_wait(&bars[C_DS], c & 1))) break;
+      named_bar(1, 256);
+      // ---- leader: dS(c) = K^T (uE_hi + uE_lo)
+      if (leader) {
+        if (!s_abort && mbar_wait(&bars[C_KP], c & 1, kWait)) {
+          tc_fence_after();
+          const uint32_t kb = smem_u32(sm + cKP), eb = smem_u32(sm + cE);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t uh = desc_sw128(eb + 16384 + ks * 2048, 8192, 1024);
+            const uint64_t ul = desc_sw128(eb + 24576 + ks * 2048, 8192, 1024);
+            const uint64_t dk = desc_sw128(kb + ks * 2048, 8192, 1024);
+            mma_bf16(tmem + tDS, dk, uh, I_DS, ks > 0);
+            mma_bf16(tmem + tDS, dk, ul, I_DS, true);
+          }
+          mma_commit(&bars[C_DS]);
+          mbar_arrive(&bars[C_EREADY]);
+        } else {
+          s_abort = 1;
+        }
+      }
+      // ---- S <- gamma_C S + dS (QS(c) must be done reading the old S tiles)
+      if (!(ok = group_wait2(1, 256, &bars[C_DS], c & 1, &bars[C_QS], c & 1))) break;
       tc_fence_after();
       {
-        const float gC = vqs[128];
-        float ds[64];
+        float ds[32];
+        float t16[16];
+        tmem_ld16(tmem + lane_off + tDS + 32 * hc, t16);
 #pragma unroll
-        for (int hf = 0; hf < 4; ++hf) {
-          float t16[16];
-          tmem_ld16(tmem + lane_off + tDS + 16 * hf, t16);
+        for (int e = 0; e < 16; ++e) ds[e] = t16[e];
+        tmem_ld16(tmem + lane_off + tDS + 32 * hc + 16, t16);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) ds[16 * hf + e] = t16[e];
-        }
+        for (int e = 0; e < 16; ++e) ds[16 + e] = t16[e];
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 64; ++e) S[e] = gC * S[e] + ds[e];
+        for (int e = 0; e < 32; ++e) S[e] = g_cur * S[e] + ds[e];
         store_state_tiles();
       }
       tc_fence_before();
       fence_proxy_async();
-      named_bar(1, 128);
-      if (leader) mbar_arrive(&bars[C_SREADY]);
-      // ---- o = e^g qn . QS + PE  (off the carry's critical path)
-      if (!(ok = group_wait(&bars[C_QS], c & 1))) break;
-      if (!(ok = group_wait(&bars[C_PE], c & 1))) break;
-      tc_fence_after();
-      {
-        const float qs = vqs[i & 63];
-        __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out) +
-                            (((long)b * a.T + t0 + (i & 63)) * a.H + h) * a.dv + half * 64;
-#pragma unroll
-        for (int hf = 0; hf < 4; ++hf) {
-          float qv[16], pe[16];
-          tmem_ld16(tmem + lane_off + tQS + 16 * hf, qv);
-          tmem_ld16(tmem + lane_off + tPE + 16 * hf, pe);
-          tmem_ld_wait();
-          if (lane < 16 && i < Cc) {
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-              float x[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                x[e] = qs * qv[8 * m + e] + pe[8 * m + e];
-                if (a.check_finite) bad |= !finite_f(x[e]);
-              }
-              *reinterpret_cast<uint4*>(op + 16 * hf + 8 * m) = pack8(x);
-            }
-          }
+      named_bar(1, 256);
+      // ---- leader: E(c+1) as soon as S(c+1), W'(c+1) and U'(c+1) are in place
+      if (leader) {
+        if (c + 1 < NC) {
+          if (!s_abort && mbar_wait(&bars[C_M2], (c + 1) & 1, kWait) &&
+              mbar_wait(&bars[C_W0 + ((c + 1) & 1)], ((c + 1) >> 1) & 1, kWait))
+            issue_e(c + 1);
+          else
+            s_abort = 1;
         }
+        mbar_arrive(&bars[C_SREADY]);
       }
-      // the vectors of chunk c+1 must have landed before the issue lane may
-      // reuse this slot (it reloads it only after OUTDONE(c))
-      if (c + 1 < NC && !(ok = group_wait(&bars[C_TV], (c + 1) & 1))) break;
-      tc_fence_before();
-      named_bar(1, 128);
-      if (leader) mbar_arrive(&bars[C_OUTDONE]);
+      u_cur = u_nxt;
+      g_cur = g_nxt;
     }
-    if (ok && !s_abort && a.S) {
-      const long base = ((long)bh * 128 + srow) * a.dv + half * 64;
+    if (!s_abort && a.S) {
+      const long base = ((long)bh * 128 + srow) * a.dv + half * 64 + 32 * hc;
 #pragma unroll
-      for (int j = 0; j < 64; j += 4) {
+      for (int j = 0; j < 32; j += 4) {
         *reinterpret_cast<float4*>(a.S + base + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
         if (a.check_finite)
           bad |= !(finite_f(S[j]) && finite_f(S[j + 1]) && finite_f(S[j + 2]) && finite_f(S[j + 3]));
       }
     }
     if (bad) set_status(DR_ERR_NONFINITE);
-  } else if (warp == 4 && lane == 0) {
+  } else if (warp >= 9) {
+    // ===================================================================== output warps
+    const int quad = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const bool oleader = (warp == 9 && lane == 0);
+    const int i = quad * 16 + (lane & 15);
+    bool bad = false;
+    float qs_cur = reinterpret_cast<const float*>(recs + rVec)[i];
+    for (int c = 0; c < NC; ++c) {
+      float qs_nxt = 0.f;
+      if (c + 1 < NC) qs_nxt = reinterpret_cast<const float*>(recs + (size_t)(c + 1) * kRec + rVec)[i];
+      const int t0 = c * 64, Cc = min(64, a.T - t0);
+      if (!group_wait2(2, 128, &bars[C_QS], c & 1, &bars[C_PE], c & 1)) break;
+      tc_fence_after();
+      __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out) +
+                          (((long)b * a.T + t0 + i) * a.H + h) * a.dv + half * 64;
+#pragma unroll
+      for (int hcol = 0; hcol < 2; ++hcol) {
+        float o[32];
+        {
+          float qv[16], pe[16];
+          tmem_ld16(tmem + lane_off + tQS + 32 * hcol, qv);
+          tmem_ld16(tmem + lane_off + tPE + 32 * hcol, pe);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = qs_cur * qv[e] + pe[e];
+          tmem_ld16(tmem + lane_off + tQS + 32 * hcol + 16, qv);
+          tmem_ld16(tmem + lane_off + tPE + 32 * hcol + 16, pe);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[16 + e] = qs_cur * qv[e] + pe[e];
+        }
+        float x[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float y = __shfl_sync(0xffffffffu, o[16 + e], lane & 15);
+          x[e] = (lane < 16) ? o[e] : y;
+        }
+        if (i < Cc) {
+          const int col = 32 * hcol + ((lane < 16) ? 0 : 16);
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            float y8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              y8[e] = x[8 * m + e];
+              if (a.check_finite) bad |= !finite_f(y8[e]);
+            }
+            *reinterpret_cast<uint4*>(op + col + 8 * m) = pack8(y8);
+          }
+        }
+      }
+      tc_fence_before();
+      named_bar(2, 128);
+      if (oleader) mbar_arrive(&bars[C_OUTDONE]);
+      qs_cur = qs_nxt;
+    }
+    if (bad) set_status(DR_ERR_NONFINITE);
+  } else if (lane == 0) {
     // ===================================================================== issue lane
     auto wait = [&](int id, uint32_t parity) -> bool {
       if (s_abort) return false;
@@ -694,75 +815,67 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       }
       return true;
     };
-    int n_tv = 0, n_wq = 0, n_kp = 0;   // copies issued per buffer group
+    int n_tv = 0, n_w = 0, n_q = 0, n_kp = 0;   // copies issued per buffer group
     auto load_tv = [&](int c) {
       const uint8_t* rec = recs + (size_t)c * kRec;
-      mbar_expect_tx(&bars[C_TV], 16384 + 1024 + 8192);
+      mbar_expect_tx(&bars[C_TV], 16384 + 8192);
       bulk_load(sm + cT, rec + rT, 16384, &bars[C_TV]);
-      bulk_load(sm + cVec + (c & 1) * 1024, rec + rVec, 1024, &bars[C_TV]);
       tma_load_4d(sm + cV, &tmV, &bars[C_TV], half * 64, h, c * 64, b);
       n_tv = c + 1;
     };
-    auto load_wq = [&](int c) {
-      const uint8_t* rec = recs + (size_t)c * kRec;
-      mbar_expect_tx(&bars[C_WQ], 32768 + 16384);
-      bulk_load(sm + cWp, rec + rWp, 32768, &bars[C_WQ]);
-      tma_load_4d(sm + cQ, &tmQ, &bars[C_WQ], 0, h, c * 64, b);
-      tma_load_4d(sm + cQ + 8192, &tmQ, &bars[C_WQ], 64, h, c * 64, b);
-      n_wq = c + 1;
+    auto load_w = [&](int c) {   // slot c & 1
+      uint64_t* bar = &bars[C_W0 + (c & 1)];
+      mbar_expect_tx(bar, 32768);
+      bulk_load(sm + cW + (c & 1) * 32768, recs + (size_t)c * kRec + rWp, 32768, bar);
+      n_w = c + 1;
+    };
+    auto load_q = [&](int c) {
+      mbar_expect_tx(&bars[C_Q], 16384);
+      tma_load_4d(sm + cQ, &tmQ, &bars[C_Q], 0, h, c * 64, b);
+      tma_load_4d(sm + cQ + 8192, &tmQ, &bars[C_Q], 64, h, c * 64, b);
+      n_q = c + 1;
     };
     auto load_kp = [&](int c) {
-      const uint8_t* rec = recs + (size_t)c * kRec;
       mbar_expect_tx(&bars[C_KP], 16384 + 16384);
-      bulk_load(sm + cP, rec + rP, 16384, &bars[C_KP]);
-      tma_load_4d(sm + cK, &tmK, &bars[C_KP], 0, h, c * 64, b);
-      tma_load_4d(sm + cK + 8192, &tmK, &bars[C_KP], 64, h, c * 64, b);
+      bulk_load(sm + cKP + 16384, recs + (size_t)c * kRec + rP, 16384, &bars[C_KP]);
+      tma_load_4d(sm + cKP, &tmK, &bars[C_KP], 0, h, c * 64, b);
+      tma_load_4d(sm + cKP + 8192, &tmK, &bars[C_KP], 64, h, c * 64, b);
       n_kp = c + 1;
     };
+    auto m2 = [&](int c) {   // U' = T_hi V + T_lo V into slot c & 1
+      tc_fence_after();
+      const uint32_t tb = smem_u32(sm + cT), vt = smem_u32(sm + cV);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t dt = desc_sw128(tb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
+        const uint64_t dv = desc_sw128(vt + (ks & 3) * 2048, 8192, 1024);
+        mma_bf16(tmem + tU0 + (c & 1) * 64, dt, dv, I_N64, ks > 0);
+      }
+      mma_commit(&bars[C_M2]);
+    };
     load_tv(0);
-    load_wq(0);
+    load_w(0);
+    if (NC > 1) load_w(1);
+    load_q(0);
     load_kp(0);
-    bool ok = true;
-    int n_pe = 0;   // PE commits issued
+    bool ok = wait(C_TV, 0);
+    if (ok) m2(0);
+    int n_pe = 0, n_m2 = ok ? 1 : 0;
+    if (ok && NC > 1 && (ok = wait(C_M2, 0))) load_tv(1);
+    // Pipe order per chunk: E(c) [state leader], QS(c), U'(c+1), dS(c) [state
+    // leader], PE(c).  U'(c+1) runs while the state warps read E(c) out, so only
+    // PE(c) sits between dS(c) and E(c+1), inside the S update.  Each refill
+    // follows the last read of its buffer and precedes, in this thread's order,
+    // the MMA whose completion could start the buffer's next phase, so no waiter
+    // can fall two phases behind.
     for (int c = 0; ok && c < NC; ++c) {
-      const int slot = c & 1;
-      const uint32_t uacc = tmem + tU0 + slot * 64;
-      // M2(c): U' = T_hi V + T_lo V
-      if (!(ok = wait(C_TV, c & 1))) break;
-      tc_fence_after();
-      {
-        const uint32_t tb = smem_u32(sm + cT), vt = smem_u32(sm + cV);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t dt = desc_sw128(tb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
-          const uint64_t dv = desc_sw128(vt + (ks & 3) * 2048, 8192, 1024);
-          mma_bf16(uacc, dt, dv, I_N64, ks > 0);
-        }
-        mma_commit(&bars[C_M2]);
-      }
-      // E(c) = U' - (W'_hi S_hi + W'_hi S_lo + W'_lo S_hi)
-      if (!(ok = wait(C_SREADY, c & 1) && wait(C_WQ, c & 1))) break;
-      tc_fence_after();
-      const uint32_t sb = smem_u32(sm + cS);
-      {
-        const uint32_t wp = smem_u32(sm + cWp);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t dsh = desc_sw128(sb + ks * 2048, 16384, 1024);
-          const uint64_t dsl = desc_sw128(sb + 16384 + ks * 2048, 16384, 1024);
-          const uint64_t dw = desc_sw128(wp + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
-          const uint64_t dwl = desc_sw128(wp + 16384 + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
-          mma_bf16(uacc, dw, dsh, I_NEG, true);
-          mma_bf16(uacc, dw, dsl, I_NEG, true);
-          mma_bf16(uacc, dwl, dsh, I_NEG, true);
-        }
-        mma_commit(&bars[C_E]);
-      }
-      // QS(c) = Q (S_hi + S_lo) once the output of chunk c-1 has read tQS
+      // QS(c) = Q (S_hi + S_lo): S(c) tiles ready, tQS read by the output of c-1
+      if (!(ok = wait(C_SREADY, c & 1))) break;
       if (c >= 1 && !(ok = wait(C_OUTDONE, (c - 1) & 1))) break;
+      if (!(ok = wait(C_Q, c & 1))) break;
       tc_fence_after();
       {
-        const uint32_t qb = smem_u32(sm + cQ);
+        const uint32_t sb = smem_u32(sm + cS), qb = smem_u32(sm + cQ);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint64_t dsh = desc_sw128(sb + ks * 2048, 16384, 1024);
@@ -773,30 +886,17 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
         }
         mma_commit(&bars[C_QS]);
       }
-      // refill T/V/vectors (M2(c) done; vector slot c+1 was freed by OUTDONE(c-1))
+      // U'(c+1) into the other slot (its E(c-1) was read out before EREADY(c-1))
       if (c + 1 < NC) {
-        if (!(ok = wait(C_M2, c & 1))) break;
-        load_tv(c + 1);
+        if (!(ok = wait(C_TV, (c + 1) & 1))) break;
+        m2(c + 1);
+        n_m2 = c + 2;
       }
-      // refill W'/Q (their last reader QS(c) is done)
-      if (c + 1 < NC) {
-        if (!(ok = wait(C_QS, c & 1))) break;
-        load_wq(c + 1);
-      }
-      // M4(c): dS = K^T (uE_hi + uE_lo) ; PE = P_hi E_hi + P_lo E_hi + P_hi E_lo
+      // PE(c) = P_hi E_hi + P_lo E_hi + P_hi E_lo once the E tiles are written
       if (!(ok = wait(C_EREADY, c & 1) && wait(C_KP, c & 1))) break;
       tc_fence_after();
       {
-        const uint32_t pb = smem_u32(sm + cP), eb = smem_u32(sm + cE), kb = smem_u32(sm + cK);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t uh = desc_sw128(eb + 16384 + ks * 2048, 8192, 1024);
-          const uint64_t ul = desc_sw128(eb + 24576 + ks * 2048, 8192, 1024);
-          const uint64_t dk = desc_sw128(kb + ks * 2048, 8192, 1024);
-          mma_bf16(tmem + tDS, dk, uh, I_DS, ks > 0);
-          mma_bf16(tmem + tDS, dk, ul, I_DS, true);
-        }
-        mma_commit(&bars[C_DS]);
+        const uint32_t pb = smem_u32(sm + cKP) + 16384, eb = smem_u32(sm + cE);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           const uint64_t ph = desc_sw128(pb + ks * 32, 16, 1024);
@@ -810,21 +910,33 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
         mma_commit(&bars[C_PE]);
         n_pe = c + 1;
       }
-      // refill K/P (their last reader PE(c) is done)
-      if (c + 1 < NC) {
-        if (!(ok = wait(C_PE, c & 1))) break;
-        load_kp(c + 1);
+      // W' slot c & 1 for chunk c+2: E(c), its reader, finished before EREADY(c)
+      if (c + 2 < NC) load_w(c + 2);
+      // T/V of chunk c+2 once U'(c+1) has read them
+      if (c + 2 < NC) {
+        if (!(ok = wait(C_M2, (c + 1) & 1))) break;
+        load_tv(c + 2);
       }
+      // Q of chunk c+1 once QS(c) has read it
+      if (!(ok = wait(C_QS, c & 1))) break;
+      if (c + 1 < NC) load_q(c + 1);
+      // K/P of chunk c+1 once dS(c) and PE(c) have read them; dS(c+1) waits on
+      // this very load, so DS cannot run a phase ahead of this wait
+      if (!(ok = wait(C_DS, c & 1) && wait(C_PE, c & 1))) break;
+      if (c + 1 < NC) load_kp(c + 1);
     }
     if (!ok) set_status(DR_ERR_TIMEOUT);
     // drain: the last MMAs and every copy issued, so nothing lands after exit
     if (n_pe > 0) mbar_wait(&bars[C_PE], (n_pe - 1) & 1, kWait / 4);
+    if (n_m2 > 0) mbar_wait(&bars[C_M2], (n_m2 - 1) & 1, kWait / 4);
     if (n_tv > 0) mbar_wait(&bars[C_TV], (n_tv - 1) & 1, kWait / 4);
-    if (n_wq > 0) mbar_wait(&bars[C_WQ], (n_wq - 1) & 1, kWait / 4);
+    if (n_q > 0) mbar_wait(&bars[C_Q], (n_q - 1) & 1, kWait / 4);
     if (n_kp > 0) mbar_wait(&bars[C_KP], (n_kp - 1) & 1, kWait / 4);
+    for (int k = (n_w > 2 ? n_w - 2 : 0); k < n_w; ++k)
+      mbar_wait(&bars[C_W0 + (k & 1)], (k >> 1) & 1, kWait / 4);
   }
 
-  if (warp == 4) __syncwarp();
+  if (warp == 8) __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (s_abort && tid == 0) set_status(DR_ERR_TIMEOUT);
