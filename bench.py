@@ -89,7 +89,8 @@ def measured_traffic(kernel, workload, variant=None):
         return None
     if not rec or rec.get("source_sha256") != source_hash(kernel):
         return None
-    if rec.get("workload") != workload or (variant and rec.get("variant") != variant):
+    variants = rec.get("variants", [rec.get("variant")])
+    if rec.get("workload") != workload or (variant and variant not in variants):
         return None
     return rec.get("dram_bytes_per_launch")
 
