@@ -47,6 +47,14 @@ constexpr uint32_t rWp = 16384;     // W'^T hi [128 dk][64 tok], then W'^T lo
 constexpr uint32_t rP = 49152;      // P hi | P lo
 constexpr uint32_t rVec = 65536;    // fp32 [0,64) e^g qn ; [64,128) e^{g_C-g} c ; [128] gamma_C
 constexpr uint32_t kRec = 66560;
+// PGDN records add the explicit write keys and the statistic's chunk map
+constexpr uint32_t rW = 66560;      // W hi [64 tok][128] (2 k-blocks), then W lo      32 KB
+constexpr uint32_t rAux = 99328;    // fp32 [0] prod alphaP, [1,129) chunk offset of A,
+                                    //      [256,384) A at the chunk start
+constexpr uint32_t kRecP = 101376;
+
+template <int VARIANT>
+__host__ __device__ constexpr uint32_t rec_bytes() { return VARIANT == DR_PGDN ? kRecP : kRec; }
 
 // ================================================================= chunk_prep
 constexpr int kPrepThreads = 9 * 32;        // warps 0-7 prep, warp 8 issue
@@ -64,7 +72,7 @@ constexpr uint32_t I_N64 = idesc_bf16(64, 64, 0, 1);
 constexpr uint32_t I_NEGT = idesc_bf16(64, 64, 1, 1, 1);    // A = W'^T (MN-major), negated
 constexpr uint32_t I_DS = idesc_bf16(128, 64, 1, 1);
 
-enum { P_KQ0, P_KQ1, P_G0, P_G1, P_W, P_GFREE0, P_GFREE1, P_TREADY, P_WFREE, P_COUNT };
+enum { P_KQ0, P_KQ1, P_G0, P_G1, P_W, P_GFREE0, P_GFREE1, P_TREADY, P_WFREE, P_WREADY, P_COUNT };
 
 __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -100,6 +108,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   float* vla = vqq + 64;
   float* veta = vla + 64;
   float* vcf = veta + 64;   // c_j e^{g_e(J) - g_j}: column factor of the off-diagonal blocks
+  float* vaP = vcf + 64;    // PGDN statistic decay / gain per token
+  float* vbP = vaP + 64;
+  constexpr bool kPgdn = (VARIANT == DR_PGDN);
+  constexpr uint32_t kRecV = rec_bytes<VARIANT>();
+  const float mu_h_unused = 0.f;
+  (void)mu_h_unused;
   float* LT = reinterpret_cast<float*>(sm + pT);
   float* XS = LT + 64 * LDL;
 
@@ -134,7 +148,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       return ok;
     };
 
-    float nla = 0.f, neta = 0.f;   // gates of the next task (thread ptid < 64 = token)
+    float nla = 0.f, neta = 0.f, naP = 1.f, nbP = 0.f;   // gates of the next task (ptid < 64 = token)
     auto prefetch_gates = [&](int k) {
       const int t = task_of(k), bh = t / NC, c = t % NC;
       const int i = ptid, tok = c * 64 + i;
@@ -142,16 +156,22 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         const long ti = ((long)(bh / a.H) * a.T + tok) * a.H + (bh % a.H);
         nla = a.log_alpha[ti];
         neta = a.eta[ti];
+        if (kPgdn) {
+          naP = a.alphaP[ti];
+          nbP = a.betaP[ti];
+        }
       } else {
         nla = 0.f;
         neta = 0.f;
+        naP = 1.f;
+        nbP = 0.f;
       }
     };
     if (nmine > 0) prefetch_gates(0);
 
     for (int k = 0; k < nmine; ++k) {
       const int t = task_of(k);
-      uint8_t* rec = ws + (size_t)t * kRec;   // tasks are numbered (b h) major, chunk minor
+      uint8_t* rec = ws + (size_t)t * kRecV;   // tasks are numbered (b h) major, chunk minor
       const int st = k & 1;
       uint8_t* KQ = sm + pKQ + st * 32768;
 
@@ -160,6 +180,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       if (ptid < 64) {
         vla[ptid] = nla;
         veta[ptid] = neta;
+        if (kPgdn) {
+          vaP[ptid] = naP;
+          vbP[ptid] = nbP;
+        }
       }
       if (k + 1 < nmine) prefetch_gates(k + 1);
       {
@@ -206,7 +230,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         const float qn = a.q_l2norm ? 1.f / fmaxf(sqrtf(qq), 1e-30f) : 1.f;
         float beta = veta[i];
         if (VARIANT == DR_KLA) beta = beta / (kk * cr * cr + a.eps);
-        const float coef = beta * cr;
+        const float coef = kPgdn ? 1.f : beta * cr;   // PGDN: w is explicit (below)
         va[i] = coef;
         vcr[i] = cr;
         vqn[i] = qn;
@@ -219,7 +243,50 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         rv[64 + i] = __expf(gC - gi) * coef;
         if (i == 0) rv[128] = __expf(gC);
       }
+      if (kPgdn && leader) bulk_wait_read<0>();   // the previous W'^T copy has left the T region
       named_bar(1, 256);
+      if (kPgdn) {
+        // statistic scan from the chunk-start value (prefix of the chunk maps), the
+        // bounded map B(A) and the write keys w = eta B(A) . k^ (PDN notes Eq. (9)),
+        // as bf16 hi/lo [64 tokens][128] tiles in the T region: the Gram's B operand
+        // and the carry's dS operand (one bulk copy into the record)
+        if (ptid < 128) {
+          const int ch = ptid, kb = ch >> 6, col = ch & 63;
+          const float mu_h = a.mu[(t / NC) % a.H];
+          float A = reinterpret_cast<const float*>(rec + rAux)[256 + ch];
+          uint8_t* Wt = sm + pT;
+          for (int i0 = 0; i0 < 64; i0 += 8) {
+            float kv[8], Av[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              kv[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                          KQ + kb * 16384 + sw128_offset(i0 + e, col))) * vcr[i0 + e];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              A = vaP[i0 + e] * A + vbP[i0 + e] * kv[e] * kv[e];
+              Av[e] = A;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float rr = __logf(fmaxf(Av[e], a.log_floor)) - mu_h;
+              const float sq = __fdividef(rr, 1.f + fabsf(rr));
+              const float w = veta[i0 + e] * __expf(-a.ln_x * sq) * kv[e];
+              const __nv_bfloat16 wh = __float2bfloat16_rn(w);
+              const __nv_bfloat16 wl = __float2bfloat16_rn(w - __bfloat162float(wh));
+              const uint32_t off = kb * 8192 + sw128_offset(i0 + e, col);
+              *reinterpret_cast<__nv_bfloat16*>(Wt + off) = wh;
+              *reinterpret_cast<__nv_bfloat16*>(Wt + 16384 + off) = wl;
+            }
+          }
+        }
+        fence_proxy_async();
+        named_bar(1, 256);
+        if (leader) {
+          bulk_store(rec + rW, sm + pT, 32768);
+          bulk_commit();
+          mbar_arrive(&bars[P_WREADY]);
+        }
+      }
 
       // ---- Gram readout -> L (fp32, smem) and P (bf16 hi/lo, staged in the Q half of
       //      the K/Q stage, which the Gram was the last to read, then one bulk copy)
@@ -433,25 +500,38 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       tma_load_4d(base + 16384 + 8192, &tmQ, &bars[P_KQ0 + st], 64, h, c * 64, b);
       kq_issued = k + 1;
     };
+    // Gram [K; Q] W^T into slot k & 1: W = K itself (GDN/KLA, A and B share one
+    // descriptor), or the PGDN write keys (bf16 hi/lo) the prep warps left in the T region
     auto gram = [&](int k) {
       const uint32_t kq = smem_u32(sm + pKQ + (k & 1) * 32768);
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint64_t d = desc_sw128(kq + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-        mma_bf16(tmem + tG0 + (k & 1) * 64, d, d, I_GRAM, ks > 0);
+        if (kPgdn) {
+          const uint32_t wb = smem_u32(sm + pT) + (ks >> 2) * 8192 + (ks & 3) * 32;
+          mma_bf16(tmem + tG0 + (k & 1) * 64, d, desc_sw128(wb, 16, 1024), I_GRAM, ks > 0);
+          mma_bf16(tmem + tG0 + (k & 1) * 64, d, desc_sw128(wb + 16384, 16, 1024), I_GRAM, true);
+        } else {
+          mma_bf16(tmem + tG0 + (k & 1) * 64, d, d, I_GRAM, ks > 0);
+        }
       }
       mma_commit(&bars[P_G0 + (k & 1)]);
     };
     bool ok = true;
     if (nmine > 0) issue_kq(0);
     if (nmine > 1) issue_kq(1);
-    if (nmine > 0 && (ok = wait(P_KQ0, 0))) gram(0);
+    if (!kPgdn && nmine > 0 && (ok = wait(P_KQ0, 0))) gram(0);
     int w_done = 0;   // W' MMAs committed
     for (int k = 0; ok && k < nmine; ++k) {
       const int st = k & 1;
-      // Gram of the next task into the other slot once its readout (task k-1) is done
-      if (k + 1 < nmine) {
+      if (kPgdn) {
+        // PGDN: the Gram needs this task's write keys, so it follows WREADY(k)
+        // (the slot's previous readout, task k-2, finished before WREADY(k-1))
+        if (!(ok = wait(P_WREADY, k & 1) && wait(P_KQ0 + st, (k >> 1) & 1))) break;
+        gram(k);
+      } else if (k + 1 < nmine) {
+        // Gram of the next task into the other slot once its readout (task k-1) is done
         if (!(ok = wait(P_KQ0 + (st ^ 1), ((k + 1) >> 1) & 1))) break;
         if (k >= 1 && !(ok = wait(P_GFREE0 + (st ^ 1), ((k - 1) >> 1) & 1))) break;
         gram(k + 1);
@@ -491,6 +571,97 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   if (warp == 0) tmem_dealloc(tmem, kPrepTmem);
 }
 
+// ================================================================= pgdn_stat
+// The PGDN key statistic A_t = alphaP_t A_{t-1} + betaP_t (k^_t . k^_t) (PDN notes
+// Eq. (9), first line) is linear in A, so over one chunk it is the affine map
+// A -> a_c A + b_c with a_c = prod alphaP and b_c the chunk's own accumulation
+// from 0 (the chunked form of the PDN notes section 2.6).
+//   pgdn_map_kernel   one warp per (b, h, chunk), lane = 4 channels, the key norm
+//                     by a warp reduction; eight tokens' loads in flight at once.
+//   pgdn_scan_kernel  one thread per (b, h, channel) composes the maps in chunk
+//                     order and leaves A at every chunk start in the chunk's
+//                     record (and the final A).
+constexpr int kMapWarps = 8;
+
+__global__ void __launch_bounds__(kMapWarps * 32) pgdn_map_kernel(FwdArgs a, uint8_t* __restrict__ ws) {
+  const int NC = (a.T + 63) / 64;
+  const long task = (long)blockIdx.x * kMapWarps + (threadIdx.x >> 5);
+  if (task >= (long)a.B * a.H * NC) return;   // whole warps leave together
+  const int lane = threadIdx.x & 31;
+  const int bh = (int)(task / NC), c = (int)(task % NC), b = bh / a.H, h = bh % a.H;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, prod = 1.f;
+  const int t_end = min(64, a.T - c * 64);
+  for (int i0 = 0; i0 < t_end; i0 += 8) {
+    uint2 raw[8];
+    float aP[8], bP[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const bool real = i0 + e < t_end;
+      const long ti = ((long)b * a.T + c * 64 + (real ? i0 + e : 0)) * a.H + h;
+      raw[e] = real ? *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(a.k) +
+                                                      ti * 128 + 4 * lane)
+                    : make_uint2(0u, 0u);
+      aP[e] = real ? a.alphaP[ti] : 1.f;
+      bP[e] = real ? a.betaP[ti] : 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const __nv_bfloat162 k01 = *reinterpret_cast<const __nv_bfloat162*>(&raw[e].x);
+      const __nv_bfloat162 k23 = *reinterpret_cast<const __nv_bfloat162*>(&raw[e].y);
+      const float kv[4] = {__low2float(k01), __high2float(k01), __low2float(k23), __high2float(k23)};
+      const float kk = warp_sum(kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3]);
+      const float cr = a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float kh = kv[q] * cr;
+        acc[q] = aP[e] * acc[q] + bP[e] * kh * kh;
+      }
+      prod *= aP[e];
+    }
+  }
+  float* aux = reinterpret_cast<float*>(ws + (size_t)task * kRecP + rAux);
+  if (lane == 0) aux[0] = prod;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) aux[1 + 4 * lane + e] = acc[e];
+}
+
+__global__ void __launch_bounds__(128) pgdn_scan_kernel(FwdArgs a, uint8_t* __restrict__ ws) {
+  const int bh = blockIdx.x, ch = threadIdx.x;
+  const int NC = (a.T + 63) / 64;
+  uint8_t* recs = ws + (size_t)bh * NC * kRecP;
+  float A = a.aux0 ? a.aux0[(long)bh * 128 + ch] : 0.f;
+  constexpr int D = 8;   // maps loaded ahead of their use
+  float am[D], bm[D];
+#pragma unroll
+  for (int d = 0; d < D; ++d) {
+    const float* m = reinterpret_cast<const float*>(recs + (size_t)min(d, NC - 1) * kRecP + rAux);
+    am[d] = m[0];
+    bm[d] = m[1 + ch];
+  }
+  for (int c0 = 0; c0 < NC; c0 += D) {
+    float an[D], bn[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) {   // next block of maps, in flight during this block
+      const float* m = reinterpret_cast<const float*>(recs + (size_t)min(c0 + D + d, NC - 1) * kRecP + rAux);
+      an[d] = m[0];
+      bn[d] = m[1 + ch];
+    }
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      if (c0 + d < NC) {
+        reinterpret_cast<float*>(recs + (size_t)(c0 + d) * kRecP + rAux)[256 + ch] = A;
+        A = am[d] * A + bm[d];
+      }
+    }
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      am[d] = an[d];
+      bm[d] = bn[d];
+    }
+  }
+  if (a.aux) a.aux[(long)bh * 128 + ch] = A;
+}
+
 // ================================================================= chunk_carry
 // Roles (15 warps):
 //   state  warps 0-7   thread = one state row (TMEM lane) x 32 of the CTA's 64
@@ -507,10 +678,18 @@ constexpr uint32_t cT = 0;                  // T hi | T lo              16 KB
 constexpr uint32_t cV = 16384;              // V [64 tok][64 col]       8 KB
 constexpr uint32_t cW = 24576;              // 2 slots x W' [hi kb0|kb1, lo kb0|kb1]   64 KB
 constexpr uint32_t cQ = 90112;              // Q kb0 | kb1              16 KB
-constexpr uint32_t cKP = 106496;            // K kb0 | K kb1 | P hi | P lo   32 KB
-constexpr uint32_t cS = 139264;             // S hi | S lo [128][64]    32 KB
-constexpr uint32_t cE = 172032;             // E hi | E lo | uE hi | uE lo   32 KB
-constexpr uint32_t kCarrySmem = cE + 32768 + 1024;
+constexpr uint32_t cKP = 106496;            // dS operand + P: GDN/KLA [K kb0 | K kb1 | P hi | P lo]
+                                            // 32 KB; PGDN [W hi | W lo | P hi | P lo] 48 KB
+// then S hi | S lo [128][64] (32 KB) and E hi | E lo | uE hi | uE lo (32 KB)
+template <bool PG>
+struct CarryMap {
+  static constexpr uint32_t kKP = PG ? 49152 : 32768;
+  static constexpr uint32_t P = PG ? 32768 : 16384;     // P inside the K/P buffer
+  static constexpr uint32_t S = cKP + kKP;
+  static constexpr uint32_t E = S + 32768;
+  static constexpr uint32_t bytes = E + 32768 + 1024;
+  static constexpr uint32_t rec = PG ? kRecP : kRec;
+};
 constexpr uint32_t tU0 = 0;                 // 2 slots M=64 x 64: U', then E
 constexpr uint32_t tQS = 128;               // M=64 x 64
 constexpr uint32_t tPE = 192;               // M=64 x 64
@@ -524,6 +703,7 @@ enum {
   C_COUNT
 };
 
+template <bool PG>
 __global__ void __launch_bounds__(kCarryThreads, 1)
     chunk_carry_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, FwdArgs a,
@@ -540,7 +720,9 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
   const int bh = blockIdx.x >> 1;
   const int b = bh / a.H, h = bh % a.H;
   const int NC = (a.T + 63) / 64;
-  const uint8_t* recs = ws + (size_t)bh * NC * kRec;
+  using CM = CarryMap<PG>;
+  constexpr uint32_t cS = CM::S, cE = CM::E, kRecV = CM::rec;
+  const uint8_t* recs = ws + (size_t)bh * NC * kRecV;
 
   if (tid == 0) {
     for (int i = 0; i < C_COUNT; ++i) mbar_init(&bars[i], 1);
@@ -640,7 +822,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       const int slot = c & 1;
       float u_nxt = 0.f, g_nxt = 0.f;
       if (c + 1 < NC) {   // one chunk ahead; consumed next iteration
-        const float* rv = reinterpret_cast<const float*>(recs + (size_t)(c + 1) * kRec + rVec);
+        const float* rv = reinterpret_cast<const float*>(recs + (size_t)(c + 1) * kRecV + rVec);
         u_nxt = rv[64 + erow];
         g_nxt = rv[128];
       }
@@ -696,6 +878,10 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
             const uint64_t dk = desc_sw128(kb + ks * 2048, 8192, 1024);
             mma_bf16(tmem + tDS, dk, uh, I_DS, ks > 0);
             mma_bf16(tmem + tDS, dk, ul, I_DS, true);
+            if (PG) {   // PGDN: dS = (W_hi + W_lo)^T (u.E); u = e^{g_C - g_j}
+              const uint64_t dkl = desc_sw128(kb + 16384 + ks * 2048, 8192, 1024);
+              mma_bf16(tmem + tDS, dkl, uh, I_DS, true);
+            }
           }
           mma_commit(&bars[C_DS]);
           mbar_arrive(&bars[C_EREADY]);
@@ -757,7 +943,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
     float qs_cur = reinterpret_cast<const float*>(recs + rVec)[i];
     for (int c = 0; c < NC; ++c) {
       float qs_nxt = 0.f;
-      if (c + 1 < NC) qs_nxt = reinterpret_cast<const float*>(recs + (size_t)(c + 1) * kRec + rVec)[i];
+      if (c + 1 < NC) qs_nxt = reinterpret_cast<const float*>(recs + (size_t)(c + 1) * kRecV + rVec)[i];
       const int t0 = c * 64, Cc = min(64, a.T - t0);
       if (!group_wait2(2, 128, &bars[C_QS], c & 1, &bars[C_PE], c & 1)) break;
       tc_fence_after();
@@ -817,7 +1003,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
     };
     int n_tv = 0, n_w = 0, n_q = 0, n_kp = 0;   // copies issued per buffer group
     auto load_tv = [&](int c) {
-      const uint8_t* rec = recs + (size_t)c * kRec;
+      const uint8_t* rec = recs + (size_t)c * kRecV;
       mbar_expect_tx(&bars[C_TV], 16384 + 8192);
       bulk_load(sm + cT, rec + rT, 16384, &bars[C_TV]);
       tma_load_4d(sm + cV, &tmV, &bars[C_TV], half * 64, h, c * 64, b);
@@ -826,7 +1012,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
     auto load_w = [&](int c) {   // slot c & 1
       uint64_t* bar = &bars[C_W0 + (c & 1)];
       mbar_expect_tx(bar, 32768);
-      bulk_load(sm + cW + (c & 1) * 32768, recs + (size_t)c * kRec + rWp, 32768, bar);
+      bulk_load(sm + cW + (c & 1) * 32768, recs + (size_t)c * kRecV + rWp, 32768, bar);
       n_w = c + 1;
     };
     auto load_q = [&](int c) {
@@ -835,11 +1021,16 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       tma_load_4d(sm + cQ + 8192, &tmQ, &bars[C_Q], 64, h, c * 64, b);
       n_q = c + 1;
     };
-    auto load_kp = [&](int c) {
-      mbar_expect_tx(&bars[C_KP], 16384 + 16384);
-      bulk_load(sm + cKP + 16384, recs + (size_t)c * kRec + rP, 16384, &bars[C_KP]);
-      tma_load_4d(sm + cKP, &tmK, &bars[C_KP], 0, h, c * 64, b);
-      tma_load_4d(sm + cKP + 8192, &tmK, &bars[C_KP], 64, h, c * 64, b);
+    auto load_kp = [&](int c) {   // the dS operand (K, or the PGDN write keys) and P
+      const uint8_t* rec = recs + (size_t)c * kRecV;
+      mbar_expect_tx(&bars[C_KP], CM::kKP);
+      bulk_load(sm + cKP + CM::P, rec + rP, 16384, &bars[C_KP]);
+      if (PG) {
+        bulk_load(sm + cKP, rec + rW, 32768, &bars[C_KP]);
+      } else {
+        tma_load_4d(sm + cKP, &tmK, &bars[C_KP], 0, h, c * 64, b);
+        tma_load_4d(sm + cKP + 8192, &tmK, &bars[C_KP], 64, h, c * 64, b);
+      }
       n_kp = c + 1;
     };
     auto m2 = [&](int c) {   // U' = T_hi V + T_lo V into slot c & 1
@@ -896,7 +1087,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       if (!(ok = wait(C_EREADY, c & 1) && wait(C_KP, c & 1))) break;
       tc_fence_after();
       {
-        const uint32_t pb = smem_u32(sm + cKP) + 16384, eb = smem_u32(sm + cE);
+        const uint32_t pb = smem_u32(sm + cKP) + CM::P, eb = smem_u32(sm + cE);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           const uint64_t ph = desc_sw128(pb + ks * 32, 16, 1024);
@@ -954,12 +1145,12 @@ int sm_count() {
 }  // namespace
 
 bool chunk_tc_split_supported(int variant, int dtype, int dk, int dv, int chunk) {
-  return (variant == DR_GDN || variant == DR_KLA) && dtype == DR_BF16 && dk == 128 &&
-         dv == 128 && chunk == 64;
+  return (variant == DR_GDN || variant == DR_KLA || variant == DR_PGDN) && dtype == DR_BF16 &&
+         dk == 128 && dv == 128 && chunk == 64;
 }
 
-size_t chunk_tc_split_workspace_bytes(int B, int T, int H) {
-  return (size_t)B * H * ((T + 63) / 64) * kRec;
+size_t chunk_tc_split_workspace_bytes(int variant, int B, int T, int H) {
+  return (size_t)B * H * ((T + 63) / 64) * (variant == DR_PGDN ? kRecP : kRec);
 }
 
 cudaError_t launch_chunk_tc_split(const FwdArgs& a, void* workspace, cudaStream_t st) {
@@ -973,6 +1164,11 @@ cudaError_t launch_chunk_tc_split(const FwdArgs& a, void* workspace, cudaStream_
   const int pgrid = (int)(ntask < 2L * nsm ? ntask : 2L * nsm);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaError_t e;
+  if (a.variant == DR_PGDN) {   // chunk-start values of the key statistic first
+    pgdn_map_kernel<<<(int)((ntask + kMapWarps - 1) / kMapWarps), kMapWarps * 32, 0, st>>>(a, ws);
+    pgdn_scan_kernel<<<a.B * a.H, 128, 0, st>>>(a, ws);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
 #define DR_PREP(V_)                                                                        \
   if (a.variant == V_) {                                                                   \
     e = cudaFuncSetAttribute(chunk_prep_kernel<V_>,                                        \
@@ -980,13 +1176,20 @@ cudaError_t launch_chunk_tc_split(const FwdArgs& a, void* workspace, cudaStream_
     if (e != cudaSuccess) return e;                                                        \
     chunk_prep_kernel<V_><<<pgrid, kPrepThreads, kPrepSmem, st>>>(mq, mk, a, ws);          \
   }
-  DR_PREP(DR_GDN) else DR_PREP(DR_KLA) else return cudaErrorInvalidValue;
+  DR_PREP(DR_GDN) else DR_PREP(DR_KLA) else DR_PREP(DR_PGDN) else return cudaErrorInvalidValue;
 #undef DR_PREP
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(chunk_carry_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kCarrySmem);
-  if (e != cudaSuccess) return e;
-  chunk_carry_kernel<<<a.B * a.H * 2, kCarryThreads, kCarrySmem, st>>>(mq, mk, mv, a, ws);
+#define DR_CARRY(PG_)                                                                      \
+  {                                                                                        \
+    e = cudaFuncSetAttribute(chunk_carry_kernel<PG_>,                                      \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,                  \
+                             (int)CarryMap<PG_>::bytes);                                   \
+    if (e != cudaSuccess) return e;                                                        \
+    chunk_carry_kernel<PG_><<<a.B * a.H * 2, kCarryThreads, CarryMap<PG_>::bytes, st>>>(   \
+        mq, mk, mv, a, ws);                                                                \
+  }
+  if (a.variant == DR_PGDN) DR_CARRY(true) else DR_CARRY(false)
+#undef DR_CARRY
   return cudaGetLastError();
 }
 

@@ -18,7 +18,7 @@ cudaError_t launch_chunk_tc_ws(const FwdArgs& a, cudaStream_t st);
 bool chunk_tc_ws_supported(int variant, int dtype, int dk, int dv, int chunk);
 cudaError_t launch_chunk_tc_split(const FwdArgs& a, void* workspace, cudaStream_t st);
 bool chunk_tc_split_supported(int variant, int dtype, int dk, int dv, int chunk);
-size_t chunk_tc_split_workspace_bytes(int B, int T, int H);
+size_t chunk_tc_split_workspace_bytes(int variant, int B, int T, int H);
 
 namespace {
 
@@ -115,7 +115,7 @@ size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H,
   if (B < 1 || T < 1 || H < 1) return 0;
   // only the two-phase tensor-core path uses a workspace: one record per chunk
   if (chunk_tc_split_supported(variant, dtype, dk, dv, chunk))
-    return chunk_tc_split_workspace_bytes(B, T, H);
+    return chunk_tc_split_workspace_bytes(variant, B, T, H);
   return 0;
 }
 
@@ -150,13 +150,13 @@ int dr_chunk_fwd(const void* q, const void* k, const void* v, const float* log_a
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err;
   const size_t need = chunk_tc_split_supported(variant, gp->dtype, dk, dv, chunk)
-                          ? chunk_tc_split_workspace_bytes(B, T, H)
+                          ? chunk_tc_split_workspace_bytes(variant, B, T, H)
                           : 0;
   const bool split = need > 0 && gp->workspace != nullptr;
   if (split && gp->workspace_bytes < need) return DR_ERR_WORKSPACE;
   if (split && (reinterpret_cast<uintptr_t>(gp->workspace) & 255u)) return DR_ERR_ALIGN;
   if (split)
-    err = launch_chunk_tc_split(a, gp->workspace, s);   // GDN / KLA: prep on every SM, then the carry
+    err = launch_chunk_tc_split(a, gp->workspace, s);   // GDN / KLA / PGDN: prep on every SM, then the carry
   else if (chunk_tc_ws_supported(variant, gp->dtype, dk, dv, chunk))
     err = launch_chunk_tc_ws(a, s);          // GDN / KLA: warp-specialised tensor-core kernel
   else if (chunk_tc_supported(variant, gp->dtype, dk, dv, chunk))

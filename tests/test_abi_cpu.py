@@ -85,12 +85,13 @@ def test_status_strings(dr):
     # the two-phase GDN/KLA path: one 66560-byte record per (b, h, 64-token chunk)
     assert dr.dr_chunk_fwd_workspace_bytes(1, 1, 8, 2048, 8, 128, 128, 64) == 8 * 8 * 32 * 66560
     assert dr.dr_chunk_fwd_workspace_bytes(0, 1, 2, 65, 3, 128, 128, 64) == 2 * 3 * 2 * 66560
+    # PGDN records also carry the write keys and the statistic's chunk map
+    assert dr.dr_chunk_fwd_workspace_bytes(2, 1, 4, 4096, 16, 128, 128, 64) == 4 * 16 * 64 * 101376
     for args in [(1, 0, 8, 2048, 8, 128, 128, 64), (1, 1, 8, 2048, 8, 64, 128, 64),
-                 (1, 1, 8, 2048, 8, 128, 128, 32), (2, 1, 8, 2048, 8, 128, 128, 64),
-                 (3, 1, 8, 2048, 8, 128, 128, 64)]:
+                 (1, 1, 8, 2048, 8, 128, 128, 32), (3, 1, 8, 2048, 8, 128, 128, 64)]:
         assert dr.dr_chunk_fwd_workspace_bytes(*args) == 0, args
     assert dr.dr_chunk_fwd_path(dr.DR_KLA, dr.DR_BF16, 128, 128, 64) == "tc_split"
-    assert dr.dr_chunk_fwd_path(dr.DR_PGDN, dr.DR_BF16, 128, 128, 64) == "tc"
+    assert dr.dr_chunk_fwd_path(dr.DR_PGDN, dr.DR_BF16, 128, 128, 64) == "tc_split"
     assert dr.dr_chunk_fwd_path(dr.DR_KLA, dr.DR_FP32, 64, 64, 64) == "simt"
 
 

@@ -224,20 +224,28 @@ def test_tc_path_ragged_with_state(rt, variant, T):
     """bf16, dk = dv = 128, chunk 64 runs on the tcgen05 kernels (GDN/KLA: the
     two-phase path with a workspace): ragged tails, nonzero initial and aux state."""
     dr, runner = rt
-    want = "tc" if variant == "pgdn" else "tc_split"
-    assert dr.dr_chunk_fwd_path(dr.VARIANT_IDS[variant], dr.DR_BF16, 128, 128, 64) == want
+    assert dr.dr_chunk_fwd_path(dr.VARIANT_IDS[variant], dr.DR_BF16, 128, 128, 64) == "tc_split"
     inp = small_inputs(variant, "bf16", B=2, T=T, H=3, seed=100 + T)
     S0, aux0 = random_state(inp, seed=T)
     check_fwd(rt, inp, S0, aux0)
 
 
-@pytest.mark.parametrize("variant", ["gdn", "kla"])
+@pytest.mark.parametrize("variant", ["gdn", "kla", "pgdn"])
 @pytest.mark.parametrize("T", [1, 65, 333])
 def test_tc_single_kernel_path_without_workspace(rt, variant, T):
-    """Without a workspace GDN/KLA take the warp-specialised single-kernel path."""
+    """Without a workspace GDN/KLA take the warp-specialised single-kernel path,
+    PGDN the phase-sequential one."""
     inp = small_inputs(variant, "bf16", B=2, T=T, H=3, seed=200 + T)
-    S0, _ = random_state(inp, seed=T)
-    check_fwd(rt, inp, S0, workspace=None)
+    S0, aux0 = random_state(inp, seed=T)
+    check_fwd(rt, inp, S0, aux0, workspace=None)
+
+
+def test_tc_split_pgdn_many_chunks_with_aux(rt):
+    """PGDN on the two-phase path over many chunks: the key statistic's chunk maps
+    are scanned across 40 chunks from a nonzero initial statistic."""
+    inp = small_inputs("pgdn", "bf16", B=2, T=64 * 40 + 5, H=4, seed=93)
+    S0, aux0 = random_state(inp, seed=94)
+    check_fwd(rt, inp, S0, aux0, pairs=[(0, 0), (1, 3), (0, 2)])
 
 
 @pytest.mark.parametrize("workspace", ["auto", None])
@@ -251,11 +259,12 @@ def test_tc_raw_key_cancellation(rt, variant, workspace):
     check_fwd(rt, inp, S0, workspace=workspace)
 
 
-def test_tc_pgdn_raw_keys(rt):
-    """PGDN on the phase-sequential tensor-core kernel with un-normalised keys."""
+@pytest.mark.parametrize("workspace", ["auto", None])
+def test_tc_pgdn_raw_keys(rt, workspace):
+    """PGDN with un-normalised keys, on both tensor-core paths."""
     inp = small_inputs("pgdn", "bf16", B=2, T=130, H=2, seed=266, k_l2norm=False)
     S0, aux0 = random_state(inp, seed=66)
-    check_fwd(rt, inp, S0, aux0)
+    check_fwd(rt, inp, S0, aux0, workspace=workspace)
 
 
 def test_tc_split_path_many_tasks(rt):
