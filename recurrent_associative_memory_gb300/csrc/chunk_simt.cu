@@ -64,9 +64,28 @@ __device__ __forceinline__ long tok_index(const FwdArgs& a, int b, int t, int h)
   return ((long)b * a.T + t) * a.H + h;
 }
 
+// read-only global loads (ld.global.nc), so the compiler may keep many in flight
 template <typename Tin>
-__device__ __forceinline__ float ldg_in(const void* p, long i) {
-  return to_f<Tin>(static_cast<const Tin*>(p)[i]);
+__device__ __forceinline__ float ldg_in(const void* p, long i);
+template <>
+__device__ __forceinline__ float ldg_in<float>(const void* p, long i) {
+  return __ldg(static_cast<const float*>(p) + i);
+}
+template <>
+__device__ __forceinline__ float ldg_in<__nv_bfloat16>(const void* p, long i) {
+  const unsigned short u = __ldg(static_cast<const unsigned short*>(p) + i);
+  return __uint_as_float(static_cast<uint32_t>(u) << 16);
+}
+
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 zero-fills the destination
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
 // index of the (I, J) pair, J < I, among the 6 strictly lower sub-chunk pairs
@@ -133,6 +152,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a) {
     const int Cc = min(CM, a.T - t0);
     __syncthreads();
 
+    if (kdn) {   // per-channel log-decay and process noise, row-major [i][c], copied
+                 // asynchronously (16-byte pieces, zero-filled past the end) under the loads below
+      constexpr int kPieces = CM * DK / 4;   // 16-byte pieces per array
+#pragma unroll
+      for (int r = 0; r < kPieces / kThreads; ++r) {
+        const int e4 = tid + r * kThreads, i = (4 * e4) / DK, c = (4 * e4) % DK;
+        const bool real = i < Cc;
+        const long ti = (real ? tok_index(a, b, t0 + i, h) : tok_index(a, b, 0, h)) * DK + c;
+        cp_async16(sX + 4 * e4, a.log_alpha + ti, real ? 16 : 0);
+        cp_async16(sW + 4 * e4, a.omega + ti, real ? 16 : 0);
+      }
+    }
+
     // ---- 1. per-token scalars (rows Cc..CM-1 are padding: zero inputs, no decay)
     if (tid < CM) {
       const int i = tid;
@@ -143,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a) {
         sb1[i] = real ? a.eta[ti] : 0.f;
       } else {
         sb1[i] = real ? a.r[ti] : 1.f;
+        sb2[i] = a.info_scale / sb1[i];   // information scale over r, used by the variance scan
       }
       if (pgdn) {
         sb2[i] = real ? a.alphaP[ti] : 1.f;
@@ -189,20 +222,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a) {
         if (sub == 0 && real && a.variant == DR_KLA) sb1[i] = sb1[i] / (kk * kn * kn + a.eps);
       }
     }
-    for (int e = tid; e < CM * NV; e += kThreads) {
-      const int i = e / NV, n = e % NV;
-      sV[e] = (i < Cc) ? ldg_in<Tin>(a.v, tok_index(a, b, t0 + i, h) * a.dv + tile * NV + n) : 0.f;
-    }
-    if (kdn) {   // per-channel log-decay and process noise, row-major [i][c]
-#pragma unroll 4
-      for (int e = tid; e < CM * DK; e += kThreads) {
-        const int i = e / DK, c = e % DK;
-        const bool real = i < Cc;
-        const long ti = real ? tok_index(a, b, t0 + i, h) * DK + c : 0;
-        sX[e] = real ? a.log_alpha[ti] : 0.f;
-        sW[e] = real ? a.omega[ti] : 0.f;
+    {
+      float vv[CM * NV / kThreads];
+#pragma unroll
+      for (int r = 0; r < CM * NV / kThreads; ++r) {   // all loads in flight, then the stores
+        const int e = tid + r * kThreads, i = e / NV, n = e % NV;
+        vv[r] = (i < Cc) ? ldg_in<Tin>(a.v, tok_index(a, b, t0 + i, h) * a.dv + tile * NV + n) : 0.f;
       }
+#pragma unroll
+      for (int r = 0; r < CM * NV / kThreads; ++r) sV[tid + r * kThreads] = vv[r];
     }
+    if (kdn) cp_async_wait_all();
     __syncthreads();
 
     // ---- 3. cumulative decay and write vectors
@@ -259,9 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a) {
             const float al = expf(la);
             const float a2 = al * al;
             const float kv = sKt[c * CS + i];
-            const float u = (a.info_scale / sb1[i]) * kv * kv;
+            const float u = sb2[i] * kv * kv;
             const float n1 = a2 * n + sW[i * DK + c] * d;
-            sW[i * DK + c] = n1 / d;                // p^_i
+            sW[i * DK + c] = __fdividef(n1, d);     // p^_i
             d = d + u * n1;
             n = n1;
             g += la;
@@ -282,12 +312,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a) {
           z += sW[i * DK + c] * kv * kv;
         }
         z = warp_sum(z);
-        if (lane == 0) sz[i] = z;
+        if (lane == 0) sz[i] = 1.f / (sb1[i] + z);   // gain denominator, inverted once per row
       }
       __syncthreads();
       for (int e = tid; e < CM * DK; e += kThreads) {
         const int i = e / DK, c = e % DK;
-        const float w = sW[e] * sKt[c * CS + i] / (sb1[i] + sz[i]);
+        const float w = sW[e] * sKt[c * CS + i] * sz[i];
         sW[e] = w;
         sWt[c * CS + i] = w;
       }

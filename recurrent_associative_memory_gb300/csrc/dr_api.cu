@@ -140,6 +140,7 @@ int dr_chunk_fwd(const void* q, const void* k, const void* v, const float* log_a
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
       !aligned16(init_state) || !aligned16(final_state) || !aligned16(log_alpha))
     return DR_ERR_ALIGN;
+  if (variant == DR_KDN && !aligned16(gp->omega)) return DR_ERR_ALIGN;   // copied in 16-byte pieces
 
   FwdArgs a = make_args(q, k, v, log_alpha, gp, variant, eps, B, T, H, dk, dv, chunk);
   a.S0 = init_state;

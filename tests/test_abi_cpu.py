@@ -125,6 +125,7 @@ def test_chunk_fwd_rejects_bad_arguments(dr):
     assert fwd(dr, q=MIS) == dr.DR_ERR_ALIGN
     assert fwd(dr, fin=MIS) == dr.DR_ERR_ALIGN
     assert fwd(dr, init=MIS) == dr.DR_ERR_ALIGN
+    assert fwd(dr, variant=3, omega=MIS, r=A) == dr.DR_ERR_ALIGN
 
 
 def test_decode_rejects_bad_arguments(dr):
