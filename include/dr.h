@@ -156,15 +156,17 @@ int dr_decode_step(const void *q, const void *k, const void *v, const float *log
                    int B, int H, int dk, int dv, dr_stream_t stream);
 
 /* Bytes of the optional dr_chunk_fwd workspace for these sizes: B H ceil(T/64)
- * records on the two-phase path (bf16, dk = dv = 128, chunk 64) of 66560 bytes
- * (GDN, KLA) or 101376 bytes (PGDN: also the write keys and the key statistic's
- * chunk map), 0 where no path uses one. */
+ * records on the two-phase paths (dk = dv = 128, chunk 64) of 66560 bytes (GDN,
+ * KLA; bf16), 101376 bytes (PGDN, bf16: also the write keys and the key
+ * statistic's chunk map) or 135168 bytes (Diagonal KDN, bf16 or fp32: fp32
+ * operands and the variance chunk map), 0 where no path uses one. */
 size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H, int dk, int dv,
                                     int chunk);
 
 /*
- * Same forward as dr_chunk_fwd on the two-phase tensor-core path (GDN, KLA,
- * PGDN; bf16, dk = dv = 128, chunk 64), for callers that cannot allocate device
+ * Same forward as dr_chunk_fwd on its two-phase paths (GDN, KLA, PGDN in bf16
+ * and Diagonal KDN in bf16 or fp32; dk = dv = 128, chunk 64), for callers that
+ * cannot allocate device
  * memory: code that runs where cudaMalloc is off limits (a host framework that
  * owns every byte of device memory through its own allocator, a real-time loop
  * that must not take cudaMalloc's implicit device synchronisation, a plug-in
@@ -185,8 +187,8 @@ size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H,
  * Returns DR_ERR_UNSUPPORTED for other variants, dtypes or shapes (dr_chunk_fwd
  * needs no workspace for those), DR_ERR_WORKSPACE when the records
  * (dr_chunk_fwd_workspace_bytes) would exceed DR_NOALLOC_SCRATCH_BYTES, i.e.
- * B H ceil(T/64) > 1008 (GDN, KLA) or > 661 (PGDN), otherwise whatever
- * dr_chunk_fwd returns.
+ * B H ceil(T/64) > 1008 (GDN, KLA), > 661 (PGDN) or > 496 (KDN), otherwise
+ * whatever dr_chunk_fwd returns.
  */
 #define DR_NOALLOC_SCRATCH_BYTES (64u << 20)
 int dr_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *log_alpha,
@@ -207,6 +209,8 @@ const char *dr_status_string(int status);
  *          without a workspace the same shapes take
  * "tc_ws"  the warp-specialised single-kernel tcgen05 path (GDN, KLA), or
  * "tc"     the phase-sequential tcgen05 kernel (PGDN)
+ * "simt_split" two-phase fp32 CUDA-core path (Diagonal KDN, bf16 or fp32,
+ *          dk = dv = 128, chunk 64) when the workspace is supplied
  * "simt"   fp32 CUDA-core kernel (everything else: fp32 mode, KDN, dk or dv 64,
  *          other chunk sizes). */
 const char *dr_chunk_fwd_path(int variant, int dtype, int dk, int dv, int chunk);

@@ -91,8 +91,24 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // index of the (I, J) pair, J < I, among the 6 strictly lower sub-chunk pairs
 __device__ __forceinline__ int pair_index(int I, int J) { return I * (I - 1) / 2 + J; }
 
-template <int DK, typename Tin>
-__global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a) {
+// ---- per-chunk record of the two-phase Diagonal KDN path (fp32, bytes; dk = dv = 128)
+constexpr uint32_t rkT = 0;          // T = (I + L)^-1, row-major [64][64]
+constexpr uint32_t rkP = 16384;      // P^T [64 j][64 i]
+constexpr uint32_t rkK = 32768;      // (Gamma.K)^T [128 c][64 i]
+constexpr uint32_t rkQ = 65536;      // (Gamma.Q)^T [128 c][64 i]
+constexpr uint32_t rkW = 98304;      // (exp(g_C - g_j).w_j) [64 j][128 c]
+constexpr uint32_t rkG = 131072;     // gamma_C [128]
+constexpr uint32_t rkMap = 131584;   // variance chunk map, 4 floats per channel
+constexpr uint32_t rkP0 = 133632;    // variance p at the chunk start [128]
+constexpr uint32_t kRecK = 135168;
+constexpr uint32_t kRecKTiles = rkMap;   // bytes the carry copies per chunk
+
+// PREP = false: the fused forward, one CTA per (b, h, 32 columns), chunks in order.
+// PREP = true (Diagonal KDN, dk = 128): one task per (b, h, chunk), all chunks in
+// parallel, the variance state at the chunk start read from the record; the
+// chunk's carry operands are written to the record instead of being used.
+template <int DK, typename Tin, bool PREP>
+__global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint8_t* __restrict__ ws) {
   using SM = SimtSmem<DK>;
   constexpr int TPR = DK / 8;                // threads per token row in the load pass
   constexpr int RPP = kThreads / TPR;        // rows per load pass
@@ -118,9 +134,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a) {
   float* sOne = sgC + DK;         // [DK] ones (neutral factor vector)
 
   const int ntile = a.dv / NV;
-  const int tile = blockIdx.x % ntile;
-  const int bh = blockIdx.x / ntile;
-  const int b = bh / a.H, h = bh % a.H;
+  const int NCk = (a.T + CM - 1) / CM;
+  const int tile = PREP ? 0 : (int)(blockIdx.x % ntile);
+  int bh = PREP ? 0 : (int)(blockIdx.x / ntile);
+  int b = bh / a.H, h = bh % a.H;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool kdn = (a.variant == DR_KDN);
   const bool pgdn = (a.variant == DR_PGDN);
@@ -132,9 +149,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a) {
   float* fDb = fDa + NSM * DK;            // [NSM][DK] exp(g_m(I) - g_e(I))
   float* fGb = fDb + NSM * DK;            // [NSM][DK] exp(g_b(I))  (b(0): chunk start)
 
-  for (int e = tid; e < DK * NV; e += kThreads) {
-    const int c = e / NV, n = e % NV;
-    sS[e] = a.S0 ? a.S0[((long)bh * DK + c) * a.dv + tile * NV + n] : 0.f;
+  if (!PREP) {
+    for (int e = tid; e < DK * NV; e += kThreads) {
+      const int c = e / NV, n = e % NV;
+      sS[e] = a.S0 ? a.S0[((long)bh * DK + c) * a.dv + tile * NV + n] : 0.f;
+    }
   }
   if (tid < DK) sOne[tid] = 1.f;
   // per-channel carried gain state (PGDN A / KDN p), held by the thread that
@@ -148,7 +167,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a) {
   const float mu_h = pgdn ? a.mu[h] : 0.f;
   bool bad = false;
 
-  for (int t0 = 0; t0 < a.T; t0 += CM) {
+  const long kIters = PREP ? (long)a.B * a.H * NCk : NCk;
+  for (long it = PREP ? blockIdx.x : 0; it < kIters; it += PREP ? gridDim.x : 1) {
+    int t0 = (int)it * CM;
+    uint8_t* rec = nullptr;
+    if (PREP) {   // task (b h, chunk); the variance at the chunk start comes from the scan
+      bh = (int)(it / NCk);
+      b = bh / a.H;
+      h = bh % a.H;
+      t0 = (int)(it % NCk) * CM;
+      rec = ws + (size_t)it * kRecK;
+      if (tid < DK) carry = reinterpret_cast<const float*>(rec + rkP0)[tid];
+    }
     const int Cc = min(CM, a.T - t0);
     __syncthreads();
 
@@ -222,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a) {
         if (sub == 0 && real && a.variant == DR_KLA) sb1[i] = sb1[i] / (kk * kn * kn + a.eps);
       }
     }
-    {
+    if (!PREP) {
       float vv[CM * NV / kThreads];
 #pragma unroll
       for (int r = 0; r < CM * NV / kThreads; ++r) {   // all loads in flight, then the stores
@@ -481,6 +511,31 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a) {
       tile_store(sLT + (32 + 16 * mt) * LDL + 8 * nt, LDL, d, -1.f, lane);
     }
     __syncthreads();
+    if (PREP) {   // the carry's operands -> the record (float4 stores, coalesced)
+      float4* rT = reinterpret_cast<float4*>(rec + rkT);
+      float4* rP = reinterpret_cast<float4*>(rec + rkP);
+      float4* rK = reinterpret_cast<float4*>(rec + rkK);
+      float4* rQ = reinterpret_cast<float4*>(rec + rkQ);
+      float4* rW = reinterpret_cast<float4*>(rec + rkW);
+#pragma unroll
+      for (int r = 0; r < CM * CM / 4 / kThreads; ++r) {
+        const int e = tid + r * kThreads, row = e >> 4, c4 = (e & 15) * 4;
+        const float4 tv = *reinterpret_cast<const float4*>(sLT + row * LDL + c4);
+        rT[e] = make_float4(c4 <= row ? tv.x : 0.f, c4 + 1 <= row ? tv.y : 0.f,
+                            c4 + 2 <= row ? tv.z : 0.f, c4 + 3 <= row ? tv.w : 0.f);
+        rP[e] = *reinterpret_cast<const float4*>(sPt + row * CS + c4);
+      }
+#pragma unroll
+      for (int r = 0; r < DK * CM / 4 / kThreads; ++r) {
+        const int e = tid + r * kThreads, row = e >> 4, c4 = (e & 15) * 4;
+        rK[e] = *reinterpret_cast<const float4*>(sKt + row * CS + c4);
+        rQ[e] = *reinterpret_cast<const float4*>(sQt + row * CS + c4);
+        rW[e] = *reinterpret_cast<const float4*>(sW + 4 * e);
+      }
+      if (tid < DK / 4)
+        reinterpret_cast<float4*>(rec + rkG)[tid] = *reinterpret_cast<const float4*>(sgC + 4 * tid);
+      continue;
+    }
     for (int e = tid; e < CM * CM; e += kThreads) {   // T^T (upper triangle of T is zero)
       const int i = e >> 6, j = e & 63;
       sTt[j * CS + i] = (j <= i) ? sLT[i * LDL + j] : 0.f;
@@ -597,6 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a) {
   __syncthreads();
 
   // final state and aux
+  if (PREP) return;
   if (a.S) {
     for (int e = tid; e < DK * NV; e += kThreads) {
       const int c = e / NV, n = e % NV;
@@ -610,6 +666,304 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a) {
   if (bad) set_status(DR_ERR_NONFINITE);
 }
 
+// ================================================================= two-phase Diagonal KDN
+// The per-channel variance recurrence p^ = a^2 p + w, p = p^ / (1 + u p^) is a
+// Moebius map of p, i.e. the linear map (n, d) <- [[a^2, w], [u a^2, 1 + u w]] (n, d)
+// in homogeneous coordinates p = n / d (KDN notes section 6); a chunk is the
+// product of its tokens' matrices.
+//   kdn_map_kernel   one warp per (b, h, chunk), lane = 4 channels (key norm by a
+//                    warp reduction); the product is rescaled by a power of two
+//                    every 8 tokens (p is scale-free).
+//   kdn_scan_kernel  one thread per (b, h, channel) applies the maps in chunk
+//                    order and leaves p at every chunk start in the record.
+// Then chunk_simt_kernel<PREP> does every chunk's local work in parallel and
+// kdn_carry_kernel walks the chunks with 64 state columns per CTA.
+constexpr int kKdnMapWarps = 8;   // 4 chunk tasks per block, two warps (token halves) each
+
+__global__ void __launch_bounds__(kKdnMapWarps * 32, 2) kdn_map_kernel(FwdArgs a, uint8_t* __restrict__ ws,
+                                                                         int bf16_in) {
+  __shared__ float4 part[kKdnMapWarps / 2][128];   // second half's product, per channel
+  const int NC = (a.T + CM - 1) / CM;
+  const long ntask = (long)a.B * a.H * NC;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slot = warp >> 1, halfw = warp & 1;   // task slot in the block, token half
+  const long task = (long)blockIdx.x * (kKdnMapWarps / 2) + slot;
+  const bool live = task < ntask;
+  const int bh = live ? (int)(task / NC) : 0, c = live ? (int)(task % NC) : 0;
+  const int b = bh / a.H, h = bh % a.H;
+  float m[4][4];   // per channel [m00, m01, m10, m11]
+#pragma unroll
+  for (int q = 0; q < 4; ++q) { m[q][0] = 1.f; m[q][1] = 0.f; m[q][2] = 0.f; m[q][3] = 1.f; }
+  const int t_lo = halfw * 32, t_hi = live ? min(t_lo + 32, a.T - c * CM) : 0;
+  for (int i0 = t_lo; i0 < t_hi; i0 += 4) {
+    float kv[4][4], la[4][4], om[4][4], ir[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {   // four tokens' loads in flight at once
+      const bool real = i0 + e < t_hi;
+      const long ti = ((long)b * a.T + c * CM + (real ? i0 + e : 0)) * a.H + h;
+      if (bf16_in) {
+        const uint2 raw = real ? *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(a.k) +
+                                                                 ti * 128 + 4 * lane)
+                               : make_uint2(0u, 0u);
+        kv[e][0] = __uint_as_float(raw.x << 16);
+        kv[e][1] = __uint_as_float(raw.x & 0xffff0000u);
+        kv[e][2] = __uint_as_float(raw.y << 16);
+        kv[e][3] = __uint_as_float(raw.y & 0xffff0000u);
+      } else {
+        const float4 f = real ? *reinterpret_cast<const float4*>(static_cast<const float*>(a.k) +
+                                                                 ti * 128 + 4 * lane)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        kv[e][0] = f.x; kv[e][1] = f.y; kv[e][2] = f.z; kv[e][3] = f.w;
+      }
+      const float4 l4 = real ? *reinterpret_cast<const float4*>(a.log_alpha + ti * 128 + 4 * lane)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 o4 = real ? *reinterpret_cast<const float4*>(a.omega + ti * 128 + 4 * lane)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+      la[e][0] = l4.x; la[e][1] = l4.y; la[e][2] = l4.z; la[e][3] = l4.w;
+      om[e][0] = o4.x; om[e][1] = o4.y; om[e][2] = o4.z; om[e][3] = o4.w;
+      ir[e] = real ? a.info_scale / a.r[ti] : 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float kk = warp_sum(kv[e][0] * kv[e][0] + kv[e][1] * kv[e][1] + kv[e][2] * kv[e][2] +
+                                kv[e][3] * kv[e][3]);
+      const float cr = a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float al = __expf(la[e][q]), a2 = al * al, w = om[e][q];
+        const float kh = kv[e][q] * cr, u = ir[e] * kh * kh;
+        // M <- [[a2, w], [u a2, 1 + u w]] M
+        const float n0 = a2 * m[q][0] + w * m[q][2], n1 = a2 * m[q][1] + w * m[q][3];
+        const float d0 = u * n0 + m[q][2], d1 = u * n1 + m[q][3];
+        m[q][0] = n0; m[q][1] = n1; m[q][2] = d0; m[q][3] = d1;
+      }
+    }
+    if (((i0 - t_lo) & 7) == 4 || i0 + 4 >= t_hi) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {   // exact power-of-two rescale
+        int ex;
+        frexpf(fmaxf(fmaxf(fabsf(m[q][0]), fabsf(m[q][1])), fmaxf(fabsf(m[q][2]), fabsf(m[q][3]))), &ex);
+#pragma unroll
+        for (int z = 0; z < 4; ++z) m[q][z] = ldexpf(m[q][z], -ex);
+      }
+    }
+  }
+  if (halfw == 1) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) part[slot][4 * lane + q] = make_float4(m[q][0], m[q][1], m[q][2], m[q][3]);
+  }
+  __syncthreads();
+  if (halfw == 0 && live) {   // M = M_second M_first
+    float4* out = reinterpret_cast<float4*>(ws + (size_t)task * kRecK + rkMap);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 s2 = part[slot][4 * lane + q];
+      out[4 * lane + q] = make_float4(s2.x * m[q][0] + s2.y * m[q][2], s2.x * m[q][1] + s2.y * m[q][3],
+                                      s2.z * m[q][0] + s2.w * m[q][2], s2.z * m[q][1] + s2.w * m[q][3]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(128) kdn_scan_kernel(FwdArgs a, uint8_t* __restrict__ ws) {
+  const int bh = blockIdx.x, ch = threadIdx.x;
+  const int NC = (a.T + CM - 1) / CM;
+  uint8_t* recs = ws + (size_t)bh * NC * kRecK;
+  float n = a.aux0 ? a.aux0[(long)bh * 128 + ch] : 1.f, d = 1.f;
+  float4 mc = reinterpret_cast<const float4*>(recs + rkMap)[ch];
+  for (int c = 0; c < NC; ++c) {
+    const float4 mn = reinterpret_cast<const float4*>(recs + (size_t)min(c + 1, NC - 1) * kRecK + rkMap)[ch];
+    reinterpret_cast<float*>(recs + (size_t)c * kRecK + rkP0)[ch] = n / d;
+    const float n2 = mc.x * n + mc.y * d, d2 = mc.z * n + mc.w * d;
+    int ex;
+    frexpf(fmaxf(fabsf(n2), fabsf(d2)), &ex);
+    n = ldexpf(n2, -ex);
+    d = ldexpf(d2, -ex);
+    mc = mn;
+  }
+  if (a.aux) a.aux[(long)bh * 128 + ch] = n / d;
+}
+
+// The carry of the two-phase Diagonal KDN path: one CTA per (b, h, 64 columns).
+// Per chunk it copies the record's operands (cp.async) and forms
+//   R = V - (Gamma.K) S,  E = T R,  O = (Gamma.Q) S + P E,
+//   S <- diag(gamma_C) S + (exp(g_C - g_j).w_j)^T E     (fp32, CUDA cores).
+constexpr int kKcNV = 64;
+constexpr uint32_t kKcSmem = kRecKTiles + (128 * kKcNV + CM * kKcNV) * 4;
+
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads, 1) kdn_carry_kernel(FwdArgs a, const uint8_t* __restrict__ ws) {
+  extern __shared__ __align__(16) float smk[];
+  const float* kT = smk;                                    // [64][64]
+  const float* kPt = smk + rkP / 4;                         // [64 j][64 i]
+  const float* kKt = smk + rkK / 4;                         // [128 c][64 i]
+  const float* kQt = smk + rkQ / 4;                         // [128 c][64 i]
+  const float* kW = smk + rkW / 4;                          // [64 j][128 c]
+  const float* kG = smk + rkG / 4;                          // [128]
+  float* sS = smk + kRecKTiles / 4;                         // [128][64]
+  float* sV = sS + 128 * kKcNV;                             // [64][64]: V, R, E
+  const int tid = threadIdx.x;
+  const int tile = blockIdx.x & 1, bh = blockIdx.x >> 1, b = bh / a.H, h = bh % a.H;
+  const int NC = (a.T + CM - 1) / CM;
+  const uint8_t* recs = ws + (size_t)bh * NC * kRecK;
+  bool bad = false;
+  for (int e = tid; e < 128 * kKcNV / 4; e += kThreads) {
+    const int c = e >> 4, n4 = (e & 15) * 4;
+    reinterpret_cast<float4*>(sS)[e] =
+        a.S0 ? *reinterpret_cast<const float4*>(a.S0 + ((long)bh * 128 + c) * a.dv + tile * kKcNV + n4)
+             : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const int ti = tid >> 4, tn = tid & 15;   // rows 4 ti.., columns 4 tn..
+  for (int c = 0; c < NC; ++c) {
+    const int t0 = c * CM, Cc = min(CM, a.T - t0);
+    __syncthreads();
+    {
+      const uint8_t* rec = recs + (size_t)c * kRecK;
+      for (int e = tid; e < (int)(kRecKTiles / 16); e += kThreads)
+        cp_async16(smk + 4 * e, rec + 16 * e, 16);
+      float vv[CM * kKcNV / kThreads];
+#pragma unroll
+      for (int r = 0; r < CM * kKcNV / kThreads; ++r) {
+        const int e = tid + r * kThreads, i = e >> 6, n = e & 63;
+        vv[r] = (i < Cc) ? ldg_in<Tin>(a.v, tok_index(a, b, t0 + i, h) * a.dv + tile * kKcNV + n) : 0.f;
+      }
+#pragma unroll
+      for (int r = 0; r < CM * kKcNV / kThreads; ++r) sV[tid + r * kThreads] = vv[r];
+      cp_async_wait_all();
+    }
+    __syncthreads();
+    float acc[4][4];
+    // R = V - (Gamma.K) S
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+    for (int cc = 0; cc < 128; ++cc) {
+      const float4 k4 = *reinterpret_cast<const float4*>(kKt + cc * 64 + 4 * ti);
+      const float4 s4 = *reinterpret_cast<const float4*>(sS + cc * kKcNV + 4 * tn);
+      const float kx[4] = {k4.x, k4.y, k4.z, k4.w}, sx[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) acc[x][y] += kx[x] * sx[y];
+    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      float4* vp = reinterpret_cast<float4*>(sV + (4 * ti + x) * kKcNV + 4 * tn);
+      float4 v4 = *vp;
+      v4.x -= acc[x][0]; v4.y -= acc[x][1]; v4.z -= acc[x][2]; v4.w -= acc[x][3];
+      *vp = v4;
+    }
+    __syncthreads();
+    // E = T R (T lower triangular), written over R once every thread has read it
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+    for (int j = 0; j < 4 * ti + 4; ++j) {
+      const float4 r4 = *reinterpret_cast<const float4*>(sV + j * kKcNV + 4 * tn);
+      const float rx[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const float t = kT[(4 * ti + x) * 64 + j];
+#pragma unroll
+        for (int y = 0; y < 4; ++y) acc[x][y] += t * rx[y];
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+      *reinterpret_cast<float4*>(sV + (4 * ti + x) * kKcNV + 4 * tn) =
+          make_float4(acc[x][0], acc[x][1], acc[x][2], acc[x][3]);
+    __syncthreads();
+    // O = (Gamma.Q) S + P E -> global
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+    for (int cc = 0; cc < 128; ++cc) {
+      const float4 q4 = *reinterpret_cast<const float4*>(kQt + cc * 64 + 4 * ti);
+      const float4 s4 = *reinterpret_cast<const float4*>(sS + cc * kKcNV + 4 * tn);
+      const float qx[4] = {q4.x, q4.y, q4.z, q4.w}, sx[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) acc[x][y] += qx[x] * sx[y];
+    }
+    for (int j = 0; j < 4 * ti + 4; ++j) {
+      const float4 p4 = *reinterpret_cast<const float4*>(kPt + j * 64 + 4 * ti);
+      const float4 e4 = *reinterpret_cast<const float4*>(sV + j * kKcNV + 4 * tn);
+      const float px[4] = {p4.x, p4.y, p4.z, p4.w}, ex[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) acc[x][y] += px[x] * ex[y];
+    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int i = 4 * ti + x;
+      if (i < Cc) {
+        Tin* op = static_cast<Tin*>(a.out) + tok_index(a, b, t0 + i, h) * a.dv + tile * kKcNV + 4 * tn;
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          op[y] = from_f<Tin>(acc[x][y]);
+          if (a.check_finite) bad |= !finite_f(acc[x][y]);
+        }
+      }
+    }
+    // S <- diag(gamma_C) S + Wbar^T E  (thread: 4 channels x 8 columns); S is read
+    // above by every thread, so the update waits for all of them
+    __syncthreads();
+    {
+      const int cg = tid >> 3, vg = tid & 7;
+      float s8[4][8];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int ch = 4 * cg + x;
+        const float gcf = kG[ch];
+        const float4 o0 = *reinterpret_cast<const float4*>(sS + ch * kKcNV + 8 * vg);
+        const float4 o1 = *reinterpret_cast<const float4*>(sS + ch * kKcNV + 8 * vg + 4);
+        s8[x][0] = gcf * o0.x; s8[x][1] = gcf * o0.y; s8[x][2] = gcf * o0.z; s8[x][3] = gcf * o0.w;
+        s8[x][4] = gcf * o1.x; s8[x][5] = gcf * o1.y; s8[x][6] = gcf * o1.z; s8[x][7] = gcf * o1.w;
+      }
+      for (int j = 0; j < CM; ++j) {
+        const float4 w4 = *reinterpret_cast<const float4*>(kW + j * 128 + 4 * cg);
+        const float4 e0 = *reinterpret_cast<const float4*>(sV + j * kKcNV + 8 * vg);
+        const float4 e1 = *reinterpret_cast<const float4*>(sV + j * kKcNV + 8 * vg + 4);
+        const float wx[4] = {w4.x, w4.y, w4.z, w4.w};
+        const float ex[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+#pragma unroll
+          for (int y = 0; y < 8; ++y) s8[x][y] += wx[x] * ex[y];
+      }
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        float* sp = sS + (4 * cg + x) * kKcNV + 8 * vg;
+        *reinterpret_cast<float4*>(sp) = make_float4(s8[x][0], s8[x][1], s8[x][2], s8[x][3]);
+        *reinterpret_cast<float4*>(sp + 4) = make_float4(s8[x][4], s8[x][5], s8[x][6], s8[x][7]);
+      }
+    }
+  }
+  __syncthreads();
+  if (a.S) {
+    for (int e = tid; e < 128 * kKcNV / 4; e += kThreads) {
+      const int c = e >> 4, n4 = (e & 15) * 4;
+      const float4 v = reinterpret_cast<const float4*>(sS)[e];
+      *reinterpret_cast<float4*>(a.S + ((long)bh * 128 + c) * a.dv + tile * kKcNV + n4) = v;
+      if (a.check_finite) bad |= !(finite_f(v.x) && finite_f(v.y) && finite_f(v.z) && finite_f(v.w));
+    }
+  }
+  if (bad) set_status(DR_ERR_NONFINITE);
+}
+
+int simt_sm_count() {
+  static int count[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!count[dev]) cudaDeviceGetAttribute(&count[dev], cudaDevAttrMultiProcessorCount, dev);
+  return count[dev];
+}
+
 }  // namespace
 
 size_t simt_smem_bytes(int dk) {
@@ -621,11 +975,11 @@ cudaError_t launch_chunk_simt(const FwdArgs& a, int dtype, cudaStream_t st) {
   const size_t smem = simt_smem_bytes(a.dk);
 #define DR_SIMT(DK_, T_)                                                                   \
   if (a.dk == DK_) {                                                                       \
-    cudaError_t err = cudaFuncSetAttribute(chunk_simt_kernel<DK_, T_>,                     \
+    cudaError_t err = cudaFuncSetAttribute(chunk_simt_kernel<DK_, T_, false>,              \
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,    \
                                            (int)smem);                                     \
     if (err != cudaSuccess) return err;                                                    \
-    chunk_simt_kernel<DK_, T_><<<grid, kThreads, smem, st>>>(a);                           \
+    chunk_simt_kernel<DK_, T_, false><<<grid, kThreads, smem, st>>>(a, nullptr);           \
     return cudaGetLastError();                                                             \
   }
   if (dtype == DR_BF16) {
@@ -635,6 +989,47 @@ cudaError_t launch_chunk_simt(const FwdArgs& a, int dtype, cudaStream_t st) {
   }
 #undef DR_SIMT
   return cudaErrorInvalidValue;
+}
+
+}  // namespace dr
+
+namespace dr {
+
+bool kdn_split_supported(int variant, int dtype, int dk, int dv, int chunk) {
+  return variant == DR_KDN && (dtype == DR_BF16 || dtype == DR_FP32) && dk == 128 && dv == 128 &&
+         chunk == 64;
+}
+
+size_t kdn_split_workspace_bytes(int B, int T, int H) {
+  return (size_t)B * H * ((T + CM - 1) / CM) * kRecK;
+}
+
+cudaError_t launch_kdn_split(const FwdArgs& a, int dtype, void* workspace, cudaStream_t st) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const long ntask = (long)a.B * a.H * ((a.T + CM - 1) / CM);
+  const int nsm = simt_sm_count();
+  if (nsm <= 0) return cudaErrorInvalidValue;
+  kdn_map_kernel<<<(int)((ntask + kKdnMapWarps / 2 - 1) / (kKdnMapWarps / 2)), kKdnMapWarps * 32, 0,
+                   st>>>(a, ws, dtype == DR_BF16 ? 1 : 0);
+  kdn_scan_kernel<<<a.B * a.H, 128, 0, st>>>(a, ws);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const size_t psmem = simt_smem_bytes(128);
+  const int pgrid = (int)(ntask < nsm ? ntask : nsm);
+#define DR_KDN2(T_)                                                                        \
+  {                                                                                        \
+    err = cudaFuncSetAttribute(chunk_simt_kernel<128, T_, true>,                           \
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);   \
+    if (err != cudaSuccess) return err;                                                    \
+    chunk_simt_kernel<128, T_, true><<<pgrid, kThreads, psmem, st>>>(a, ws);              \
+    err = cudaFuncSetAttribute(kdn_carry_kernel<T_>,                                       \
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kKcSmem); \
+    if (err != cudaSuccess) return err;                                                    \
+    kdn_carry_kernel<T_><<<a.B * a.H * 2, kThreads, kKcSmem, st>>>(a, ws);                 \
+  }
+  if (dtype == DR_BF16) DR_KDN2(__nv_bfloat16) else DR_KDN2(float)
+#undef DR_KDN2
+  return cudaGetLastError();
 }
 
 }  // namespace dr

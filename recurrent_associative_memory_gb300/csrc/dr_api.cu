@@ -19,6 +19,9 @@ bool chunk_tc_ws_supported(int variant, int dtype, int dk, int dv, int chunk);
 cudaError_t launch_chunk_tc_split(const FwdArgs& a, void* workspace, cudaStream_t st);
 bool chunk_tc_split_supported(int variant, int dtype, int dk, int dv, int chunk);
 size_t chunk_tc_split_workspace_bytes(int variant, int B, int T, int H);
+cudaError_t launch_kdn_split(const FwdArgs& a, int dtype, void* workspace, cudaStream_t st);
+bool kdn_split_supported(int variant, int dtype, int dk, int dv, int chunk);
+size_t kdn_split_workspace_bytes(int B, int T, int H);
 
 namespace {
 
@@ -116,11 +119,13 @@ size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H,
   // only the two-phase tensor-core path uses a workspace: one record per chunk
   if (chunk_tc_split_supported(variant, dtype, dk, dv, chunk))
     return chunk_tc_split_workspace_bytes(variant, B, T, H);
+  if (kdn_split_supported(variant, dtype, dk, dv, chunk)) return kdn_split_workspace_bytes(B, T, H);
   return 0;
 }
 
 const char* dr_chunk_fwd_path(int variant, int dtype, int dk, int dv, int chunk) {
   if (chunk_tc_split_supported(variant, dtype, dk, dv, chunk)) return "tc_split";
+  if (kdn_split_supported(variant, dtype, dk, dv, chunk)) return "simt_split";
   if (chunk_tc_ws_supported(variant, dtype, dk, dv, chunk)) return "tc_ws";
   return chunk_tc_supported(variant, dtype, dk, dv, chunk) ? "tc" : "simt";
 }
@@ -150,13 +155,16 @@ int dr_chunk_fwd(const void* q, const void* k, const void* v, const float* log_a
   a.out = out;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err;
+  const bool kdn_split = kdn_split_supported(variant, gp->dtype, dk, dv, chunk);
   const size_t need = chunk_tc_split_supported(variant, gp->dtype, dk, dv, chunk)
                           ? chunk_tc_split_workspace_bytes(variant, B, T, H)
-                          : 0;
+                          : (kdn_split ? kdn_split_workspace_bytes(B, T, H) : 0);
   const bool split = need > 0 && gp->workspace != nullptr;
   if (split && gp->workspace_bytes < need) return DR_ERR_WORKSPACE;
   if (split && (reinterpret_cast<uintptr_t>(gp->workspace) & 255u)) return DR_ERR_ALIGN;
-  if (split)
+  if (split && kdn_split)
+    err = launch_kdn_split(a, gp->dtype, gp->workspace, s);   // Diagonal KDN: CUDA-core two phases
+  else if (split)
     err = launch_chunk_tc_split(a, gp->workspace, s);   // GDN / KLA / PGDN: prep on every SM, then the carry
   else if (chunk_tc_ws_supported(variant, gp->dtype, dk, dv, chunk))
     err = launch_chunk_tc_ws(a, s);          // GDN / KLA: warp-specialised tensor-core kernel

@@ -291,3 +291,20 @@ def test_tc_path_unnormalised_gdn_strong_keys(rt):
     workload family): the state grows large but stays finite."""
     inp = small_inputs("gdn", "bf16", B=1, T=512, H=4, seed=77)
     check_fwd(rt, inp)
+
+
+# ------------------------------------------------------------ Diagonal KDN paths
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("workspace", ["auto", None])
+def test_kdn_two_phase_and_fused_paths(rt, dtype, workspace):
+    """Diagonal KDN with a workspace runs the two-phase CUDA-core path (variance
+    chunk maps + scan, parallel chunk prep, 64-column carry); without one the
+    fused kernel.  Ragged tail, nonzero initial state and variance."""
+    dr, runner = rt
+    if workspace == "auto":
+        assert dr.dr_chunk_fwd_path(dr.DR_KDN, dr.DR_BF16 if dtype == "bf16" else dr.DR_FP32,
+                                    128, 128, 64) == "simt_split"
+    inp = small_inputs("kdn", dtype, B=2, T=64 * 5 + 13, H=3, seed=301)
+    S0, aux0 = random_state(inp, seed=302)
+    check_fwd(rt, inp, S0, aux0, workspace=workspace)

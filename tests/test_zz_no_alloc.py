@@ -37,7 +37,7 @@ def test_noalloc_refusals_on_host():
     assert call(dk=64) == dr.DR_ERR_UNSUPPORTED
     assert call(chunk=32) == dr.DR_ERR_UNSUPPORTED
     assert call(dtype=dr.DR_FP32) == dr.DR_ERR_UNSUPPORTED
-    assert call(variant=dr.DR_KDN) == dr.DR_ERR_UNSUPPORTED
+    assert call(variant=dr.DR_KDN, dk=64, dv=64) == dr.DR_ERR_UNSUPPORTED
     assert call(T=0) == dr.DR_ERR_SHAPE
 
 
