@@ -101,7 +101,6 @@ constexpr uint32_t rkG = 131072;     // gamma_C [128]
 constexpr uint32_t rkMap = 131584;   // variance chunk map, 4 floats per channel
 constexpr uint32_t rkP0 = 133632;    // variance p at the chunk start [128]
 constexpr uint32_t kRecK = 135168;
-constexpr uint32_t kRecKTiles = rkMap;   // bytes the carry copies per chunk
 
 // PREP = false: the fused forward, one CTA per (b, h, 32 columns), chunks in order.
 // PREP = true (Diagonal KDN, dk = 128): one task per (b, h, chunk), all chunks in
@@ -511,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       tile_store(sLT + (32 + 16 * mt) * LDL + 8 * nt, LDL, d, -1.f, lane);
     }
     __syncthreads();
-    if (PREP) {   // the carry's operands -> the record (float4 stores, coalesced)
+    if constexpr (PREP) {   // the carry's operands -> the record (float4 stores, coalesced)
       float4* rT = reinterpret_cast<float4*>(rec + rkT);
       float4* rP = reinterpret_cast<float4*>(rec + rkP);
       float4* rK = reinterpret_cast<float4*>(rec + rkK);
@@ -784,59 +783,119 @@ __global__ void __launch_bounds__(128) kdn_scan_kernel(FwdArgs a, uint8_t* __res
 }
 
 // The carry of the two-phase Diagonal KDN path: one CTA per (b, h, 64 columns).
-// Per chunk it copies the record's operands (cp.async) and forms
-//   R = V - (Gamma.K) S,  E = T R,  O = (Gamma.Q) S + P E,
+// Per chunk, from the record (cp.async):
+//   R = V - (Gamma.K) S  and  Q S  in one pass over S,  E = T R,  O = (Gamma.Q) S + P E,
 //   S <- diag(gamma_C) S + (exp(g_C - g_j).w_j)^T E     (fp32, CUDA cores).
+// (Gamma.K)^T of chunk c+1 is copied into a second buffer during chunk c's state
+// update; the other operands of chunk c are copied while R is computed.
 constexpr int kKcNV = 64;
-constexpr uint32_t kKcSmem = kRecKTiles + (128 * kKcNV + CM * kKcNV) * 4;
+// shared layout (bytes): K^T x 2 | T | P^T | Q^T | Wbar | gamma | S | V/R/E
+constexpr uint32_t kcK = 0;                 // 2 x 32 KB
+constexpr uint32_t kcT = 65536;             // 16 KB
+constexpr uint32_t kcP = kcT + 16384;       // 16 KB
+constexpr uint32_t kcQ = kcP + 16384;       // 32 KB
+constexpr uint32_t kcW = kcQ + 32768;       // 32 KB
+constexpr uint32_t kcG = kcW + 32768;       // 512 B
+constexpr uint32_t kcS = kcG + 512;         // 32 KB
+constexpr uint32_t kcV = kcS + 32768;       // 16 KB
+constexpr uint32_t kKcSmem = kcV + 16384;
+
 
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads, 1) kdn_carry_kernel(FwdArgs a, const uint8_t* __restrict__ ws) {
   extern __shared__ __align__(16) float smk[];
-  const float* kT = smk;                                    // [64][64]
-  const float* kPt = smk + rkP / 4;                         // [64 j][64 i]
-  const float* kKt = smk + rkK / 4;                         // [128 c][64 i]
-  const float* kQt = smk + rkQ / 4;                         // [128 c][64 i]
-  const float* kW = smk + rkW / 4;                          // [64 j][128 c]
-  const float* kG = smk + rkG / 4;                          // [128]
-  float* sS = smk + kRecKTiles / 4;                         // [128][64]
-  float* sV = sS + 128 * kKcNV;                             // [64][64]: V, R, E
+  __shared__ uint64_t bars[3];   // (Gamma.K)^T buffers 0 / 1, the rest of the record
+  __shared__ volatile int s_abort;
+  uint8_t* smb = reinterpret_cast<uint8_t*>(smk);
+  const float* kT = reinterpret_cast<const float*>(smb + kcT);   // [64][64]
+  const float* kPt = reinterpret_cast<const float*>(smb + kcP);  // [64 j][64 i]
+  const float* kQt = reinterpret_cast<const float*>(smb + kcQ);  // [128 c][64 i]
+  const float* kW = reinterpret_cast<const float*>(smb + kcW);   // [64 j][128 c]
+  const float* kG = reinterpret_cast<const float*>(smb + kcG);   // [128]
+  float* sS = reinterpret_cast<float*>(smb + kcS);               // [128][64]
+  float* sV = reinterpret_cast<float*>(smb + kcV);               // [64][64]: V, R, E
   const int tid = threadIdx.x;
   const int tile = blockIdx.x & 1, bh = blockIdx.x >> 1, b = bh / a.H, h = bh % a.H;
   const int NC = (a.T + CM - 1) / CM;
   const uint8_t* recs = ws + (size_t)bh * NC * kRecK;
   bool bad = false;
+  // record pieces arrive by bulk copies (one thread issues, every thread waits,
+  // bounded in time; a wait that gives up marks the CTA aborted)
+  if (tid == 0) {
+    for (int q = 0; q < 3; ++q) umma::mbar_init(&bars[q], 1);
+    umma::fence_mbar_init();
+    s_abort = 0;
+  }
+  __syncthreads();
+  int n_issued[3] = {0, 0, 0};   // copies issued per barrier (thread 0)
+  auto load_k = [&](int c) {
+    uint64_t* bar = &bars[c & 1];
+    ++n_issued[c & 1];
+    umma::mbar_expect_tx(bar, 32768);
+    umma::bulk_load(smb + kcK + (c & 1) * 32768, recs + (size_t)c * kRecK + rkK, 32768, bar);
+  };
+  auto wait_bar = [&](int q, uint32_t parity) {
+    if (!s_abort && !umma::mbar_wait(&bars[q], parity, 2000000000ull)) s_abort = 1;
+  };
   for (int e = tid; e < 128 * kKcNV / 4; e += kThreads) {
     const int c = e >> 4, n4 = (e & 15) * 4;
     reinterpret_cast<float4*>(sS)[e] =
         a.S0 ? *reinterpret_cast<const float4*>(a.S0 + ((long)bh * 128 + c) * a.dv + tile * kKcNV + n4)
              : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  if (tid == 0) load_k(0);
   const int ti = tid >> 4, tn = tid & 15;   // rows 4 ti.., columns 4 tn..
   for (int c = 0; c < NC; ++c) {
     const int t0 = c * CM, Cc = min(CM, a.T - t0);
-    __syncthreads();
+    const float* kKt = reinterpret_cast<const float*>(smb + kcK + (c & 1) * 32768);
+    __syncthreads();   // previous chunk done with T, P, Q, W, V
     {
       const uint8_t* rec = recs + (size_t)c * kRecK;
-      for (int e = tid; e < (int)(kRecKTiles / 16); e += kThreads)
-        cp_async16(smk + 4 * e, rec + 16 * e, 16);
-      float vv[CM * kKcNV / kThreads];
+      if (tid == 0) {
+        ++n_issued[2];
+        umma::mbar_expect_tx(&bars[2], 32768 + 32768 * 2 + 512);
+        umma::bulk_load(smb + kcT, rec + rkT, 32768, &bars[2]);             // T, P^T
+        umma::bulk_load(smb + kcQ, rec + rkQ, 32768 * 2 + 512, &bars[2]);   // Q^T, Wbar, gamma
+      }
+      // V tile [64 tokens][64 columns] with 16-byte loads
+      constexpr int kPer = (int)sizeof(Tin) == 2 ? 8 : 4;   // elements per 16 bytes
+      constexpr int kVec = CM * kKcNV / kPer / kThreads;
+      uint4 raw[kVec];
 #pragma unroll
-      for (int r = 0; r < CM * kKcNV / kThreads; ++r) {
-        const int e = tid + r * kThreads, i = e >> 6, n = e & 63;
-        vv[r] = (i < Cc) ? ldg_in<Tin>(a.v, tok_index(a, b, t0 + i, h) * a.dv + tile * kKcNV + n) : 0.f;
+      for (int r = 0; r < kVec; ++r) {
+        const int e = tid + r * kThreads, i = e / (kKcNV / kPer), n0 = (e % (kKcNV / kPer)) * kPer;
+        raw[r] = (i < Cc) ? __ldg(reinterpret_cast<const uint4*>(static_cast<const Tin*>(a.v) +
+                                  tok_index(a, b, t0 + i, h) * a.dv + tile * kKcNV + n0))
+                          : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int r = 0; r < CM * kKcNV / kThreads; ++r) sV[tid + r * kThreads] = vv[r];
-      cp_async_wait_all();
+      for (int r = 0; r < kVec; ++r) {
+        const int e = tid + r * kThreads, i = e / (kKcNV / kPer), n0 = (e % (kKcNV / kPer)) * kPer;
+        float* dst = sV + i * kKcNV + n0;
+        if (kPer == 8) {
+          const uint32_t w[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            dst[2 * q] = __uint_as_float(w[q] << 16);
+            dst[2 * q + 1] = __uint_as_float(w[q] & 0xffff0000u);
+          }
+        } else {
+          *reinterpret_cast<uint4*>(dst) = raw[r];
+        }
+      }
+      wait_bar(c & 1, (c >> 1) & 1);   // this chunk's (Gamma.K)^T; the rest may still fly
     }
     __syncthreads();
-    float acc[4][4];
-    // R = V - (Gamma.K) S
+    if (s_abort) break;
+    float acc[4][4], aq[4][4];
+    // R = V - (Gamma.K) S  and the (Gamma.Q) S part of O, one pass over S; the Q
+    // tile is read only after it lands, so the pass waits for it half-way in:
+    // first (Gamma.K) S alone over all channels, then (Gamma.Q) S.
 #pragma unroll
     for (int x = 0; x < 4; ++x)
 #pragma unroll
       for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+#pragma unroll 8
     for (int cc = 0; cc < 128; ++cc) {
       const float4 k4 = *reinterpret_cast<const float4*>(kKt + cc * 64 + 4 * ti);
       const float4 s4 = *reinterpret_cast<const float4*>(sS + cc * kKcNV + 4 * tn);
@@ -853,12 +912,32 @@ __global__ void __launch_bounds__(kThreads, 1) kdn_carry_kernel(FwdArgs a, const
       v4.x -= acc[x][0]; v4.y -= acc[x][1]; v4.z -= acc[x][2]; v4.w -= acc[x][3];
       *vp = v4;
     }
-    __syncthreads();
+    wait_bar(2, c & 1);
+    __syncthreads();   // R complete; T, P, Q, W, gamma landed
+    if (s_abort) break;
+    // (Gamma.K)^T of chunk c+1 into the other buffer, under the rest of this chunk
+    if (tid == 0 && c + 1 < NC) load_k(c + 1);
+    // (Gamma.Q) S
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int y = 0; y < 4; ++y) aq[x][y] = 0.f;
+#pragma unroll 8
+    for (int cc = 0; cc < 128; ++cc) {
+      const float4 q4 = *reinterpret_cast<const float4*>(kQt + cc * 64 + 4 * ti);
+      const float4 s4 = *reinterpret_cast<const float4*>(sS + cc * kKcNV + 4 * tn);
+      const float qx[4] = {q4.x, q4.y, q4.z, q4.w}, sx[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) aq[x][y] += qx[x] * sx[y];
+    }
     // E = T R (T lower triangular), written over R once every thread has read it
 #pragma unroll
     for (int x = 0; x < 4; ++x)
 #pragma unroll
       for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+#pragma unroll 4
     for (int j = 0; j < 4 * ti + 4; ++j) {
       const float4 r4 = *reinterpret_cast<const float4*>(sV + j * kKcNV + 4 * tn);
       const float rx[4] = {r4.x, r4.y, r4.z, r4.w};
@@ -876,19 +955,7 @@ __global__ void __launch_bounds__(kThreads, 1) kdn_carry_kernel(FwdArgs a, const
           make_float4(acc[x][0], acc[x][1], acc[x][2], acc[x][3]);
     __syncthreads();
     // O = (Gamma.Q) S + P E -> global
-#pragma unroll
-    for (int x = 0; x < 4; ++x)
-#pragma unroll
-      for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
-    for (int cc = 0; cc < 128; ++cc) {
-      const float4 q4 = *reinterpret_cast<const float4*>(kQt + cc * 64 + 4 * ti);
-      const float4 s4 = *reinterpret_cast<const float4*>(sS + cc * kKcNV + 4 * tn);
-      const float qx[4] = {q4.x, q4.y, q4.z, q4.w}, sx[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-      for (int x = 0; x < 4; ++x)
-#pragma unroll
-        for (int y = 0; y < 4; ++y) acc[x][y] += qx[x] * sx[y];
-    }
+#pragma unroll 4
     for (int j = 0; j < 4 * ti + 4; ++j) {
       const float4 p4 = *reinterpret_cast<const float4*>(kPt + j * 64 + 4 * ti);
       const float4 e4 = *reinterpret_cast<const float4*>(sV + j * kKcNV + 4 * tn);
@@ -896,7 +963,7 @@ __global__ void __launch_bounds__(kThreads, 1) kdn_carry_kernel(FwdArgs a, const
 #pragma unroll
       for (int x = 0; x < 4; ++x)
 #pragma unroll
-        for (int y = 0; y < 4; ++y) acc[x][y] += px[x] * ex[y];
+        for (int y = 0; y < 4; ++y) aq[x][y] += px[x] * ex[y];
     }
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
@@ -905,13 +972,13 @@ __global__ void __launch_bounds__(kThreads, 1) kdn_carry_kernel(FwdArgs a, const
         Tin* op = static_cast<Tin*>(a.out) + tok_index(a, b, t0 + i, h) * a.dv + tile * kKcNV + 4 * tn;
 #pragma unroll
         for (int y = 0; y < 4; ++y) {
-          op[y] = from_f<Tin>(acc[x][y]);
-          if (a.check_finite) bad |= !finite_f(acc[x][y]);
+          op[y] = from_f<Tin>(aq[x][y]);
+          if (a.check_finite) bad |= !finite_f(aq[x][y]);
         }
       }
     }
-    // S <- diag(gamma_C) S + Wbar^T E  (thread: 4 channels x 8 columns); S is read
-    // above by every thread, so the update waits for all of them
+    // S <- diag(gamma_C) S + Wbar^T E  (thread: 4 channels x 8 columns); S was read
+    // above by every thread (R and Q S), so the update waits for all of them
     __syncthreads();
     {
       const int cg = tid >> 3, vg = tid & 7;
@@ -925,6 +992,7 @@ __global__ void __launch_bounds__(kThreads, 1) kdn_carry_kernel(FwdArgs a, const
         s8[x][0] = gcf * o0.x; s8[x][1] = gcf * o0.y; s8[x][2] = gcf * o0.z; s8[x][3] = gcf * o0.w;
         s8[x][4] = gcf * o1.x; s8[x][5] = gcf * o1.y; s8[x][6] = gcf * o1.z; s8[x][7] = gcf * o1.w;
       }
+#pragma unroll 8
       for (int j = 0; j < CM; ++j) {
         const float4 w4 = *reinterpret_cast<const float4*>(kW + j * 128 + 4 * cg);
         const float4 e0 = *reinterpret_cast<const float4*>(sV + j * kKcNV + 8 * vg);
@@ -945,6 +1013,14 @@ __global__ void __launch_bounds__(kThreads, 1) kdn_carry_kernel(FwdArgs a, const
     }
   }
   __syncthreads();
+  if (s_abort) {   // drain the copies this CTA may still have in flight, then report
+    if (tid == 0) {
+      for (int q = 0; q < 3; ++q)
+        if (n_issued[q] > 0) umma::mbar_wait(&bars[q], (n_issued[q] - 1) & 1, 500000000ull);
+      set_status(DR_ERR_TIMEOUT);
+    }
+    return;
+  }
   if (a.S) {
     for (int e = tid; e < 128 * kKcNV / 4; e += kThreads) {
       const int c = e >> 4, n4 = (e & 15) * 4;
