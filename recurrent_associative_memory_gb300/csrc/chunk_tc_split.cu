@@ -97,18 +97,17 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   auto task_of = [&](int k) { return blockIdx.x + k * gridDim.x; };
   const int nmine = (blockIdx.x < ntask) ? (ntask - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
-  float* vg = reinterpret_cast<float*>(sm + pVec);   // cumulative log-decay
+  float* vC = reinterpret_cast<float*>(sm + pVec);   // [4 I][64 j] c_j e^{g_m(I) - g_j}
+  float* vg = vC + 256;     // cumulative log-decay
   float* va = vg + 64;      // coefficient of the raw key row in w
   float* vcr = va + 64;     // key normalisation
   float* vqn = vcr + 64;    // query normalisation
   float* vks = vqn + 64;    // e^{g_j} c_j
-  float* vF = vks + 64;     // e^{g_e(J) - g_j}
-  float* vkk = vF + 64;
+  float* vkk = vks + 64;
   float* vqq = vkk + 64;
   float* vla = vqq + 64;
   float* veta = vla + 64;
-  float* vcf = veta + 64;   // c_j e^{g_e(J) - g_j}: column factor of the off-diagonal blocks
-  float* vaP = vcf + 64;    // PGDN statistic decay / gain per token
+  float* vaP = veta + 64;   // PGDN statistic decay / gain per token
   float* vbP = vaP + 64;
   constexpr bool kPgdn = (VARIANT == DR_PGDN);
   constexpr uint32_t kRecV = rec_bytes<VARIANT>();
@@ -236,8 +235,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         vqn[i] = qn;
         const float eg = __expf(gi);
         vks[i] = eg * cr;
-        vF[i] = __expf(vg[i | 15] - gi);
-        vcf[i] = coef * vF[i];
         float* rv = reinterpret_cast<float*>(rec + rVec);
         rv[i] = eg * qn;
         rv[64 + i] = __expf(gC - gi) * coef;
@@ -289,7 +286,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       }
 
       // ---- Gram readout -> L (fp32, smem) and P (bf16 hi/lo, staged in the Q half of
-      //      the K/Q stage, which the Gram was the last to read, then one bulk copy)
+      //      the K/Q stage, which the Gram was the last to read, then one bulk copy).
+      //      Each 16-row block I takes its sub-chunk's middle token m(I) as the
+      //      reference: L_ij = G_ij [rs_i e^{g_i - g_m(I)}] [c_j e^{g_m(I) - g_j}] for
+      //      j <= i, where the column factor is <= 1 below block I and bounded by the
+      //      decay over 8 tokens inside it; above the diagonal the select drops it.
+      {
+        const int I = ptid >> 6, j = ptid & 63;
+        vC[ptid] = va[j] * __expf(vg[16 * I + 7] - vg[j]);
+      }
       if (leader) bulk_wait_read<0>();   // the previous task's W' copy has left the T region
       if (!group_wait(&bars[P_G0 + st], (k >> 1) & 1)) break;
       tc_fence_after();
@@ -299,29 +304,17 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         float gv[32];
         ld32cols(tmem + lane_off + tG0 + st * 64 + pchalf * 32, gv);
         tmem_ld_wait();
-        const float gi = vg[i];
-        const float rs = (row < 64) ? vcr[i] : vqn[i];
-        // block (I, J) of 16 x 16: J < I factors through the end of sub-chunk J
-        // (row factor e^{g_i - g_e(J)} <= 1, column factor c_j e^{g_e(J) - g_j} <= 1);
-        // J = I takes e^{g_i - g_j} directly on and below the diagonal; J > I is 0
+        const float rf = ((row < 64) ? vcr[i] : vqn[i]) * __expf(vg[i] - vg[16 * I + 7]);
+        const float* C = vC + I * 64 + pchalf * 32;
         float x[32];
 #pragma unroll
-        for (int jb = 0; jb < 2; ++jb) {
-          const int J = pchalf * 2 + jb;
-          if (J < I) {
-            const float rf = rs * __expf(gi - vg[16 * J + 15]);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) x[16 * jb + e] = gv[16 * jb + e] * rf * vcf[16 * J + e];
-          } else if (J == I) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int j = 16 * J + e;
-              x[16 * jb + e] = (j <= i) ? gv[16 * jb + e] * rs * va[j] * __expf(gi - vg[j]) : 0.f;
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) x[16 * jb + e] = 0.f;
-          }
+        for (int e = 0; e < 32; e += 4) {
+          const float4 c4 = *reinterpret_cast<const float4*>(C + e);
+          const int j = pchalf * 32 + e;
+          x[e] = (j <= i) ? gv[e] * rf * c4.x : 0.f;
+          x[e + 1] = (j + 1 <= i) ? gv[e + 1] * rf * c4.y : 0.f;
+          x[e + 2] = (j + 2 <= i) ? gv[e + 2] * rf * c4.z : 0.f;
+          x[e + 3] = (j + 3 <= i) ? gv[e + 3] * rf * c4.w : 0.f;
         }
         if (row < 64) {
 #pragma unroll
