@@ -108,8 +108,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float* vbP = vaP + 64;
   float* vkk = vbP + 64;
   float* vqq = vkk + 64;
-  float* vF = vqq + 64;     // e^{g_e(J) - g_j}: decay from token j to the end of its 16-block
-  float* vmisc = vF + 64;   // [0] = gamma_C
+  float* vmisc = vqq + 64;  // [0] = gamma_C
+  float* vC = vmisc + 128;  // [4 I][64 j] c_j e^{g_m(I) - g_j}: readout column factors
   float* LT = reinterpret_cast<float*>(sm + oE);     // L, inverted in place into T (fp32)
   float* XS = LT + 64 * LDL;                         // 32 x LDX fp32 scratch for the inverse
 
@@ -278,8 +278,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       vks[i] = eg * cr;
       vqs[i] = eg * qn;
       vu[i] = __expf(gC - gi) * coef;
-      vF[i] = __expf(vg[i | 15] - gi);
       if (i == 0) vmisc[0] = __expf(gC);
+    }
+    __syncthreads();
+    {
+      const int I = tid >> 6, j = tid & 63;
+      vC[tid] = va[j] * __expf(vg[16 * I + 7] - vg[j]);
     }
     __syncthreads();
     if (kPgdn) {  // statistic scan per channel -> write keys (K-major [64 tokens][128], 2 x 8 KB)
@@ -330,29 +334,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     wait_mma();
 
     // ---------------- 3. Gram readout: L (fp32, in the E area) and P (bf16 hi/lo)
-    // warp (quad, chalf) reads rows 32 quad.. and columns 32 chalf..; decay factors:
-    // same 16-block: e^{g_i - g_j} directly; earlier block J: e^{g_i - g_e(J)} e^{g_e(J) - g_j}.
+    // warp (quad, chalf) reads rows 32 quad.. and columns 32 chalf..
     {
       const int row = quad * 32 + lane;          // lane of the M=128 accumulator
       const int i = row & 63, I = i >> 4;
       float gv[32];
       ld32cols(tmem + lane_off + cGram + chalf * 32, gv);
       tmem_ld_wait();
-      const float gi = vg[i];
-      const float rs = (row < 64) ? vcr[i] : vqn[i];
-      float fb[2];
-#pragma unroll
-      for (int jb = 0; jb < 2; ++jb) {
-        const int J = chalf * 2 + jb;
-        fb[jb] = (J < I) ? __expf(gi - vg[16 * J + 15]) : 0.f;
-      }
+      // one reference token per 16-row block: G_ij [rs_i e^{g_i - g_m(I)}] [c_j e^{g_m(I) - g_j}]
+      const float rf = ((row < 64) ? vcr[i] : vqn[i]) * __expf(vg[i] - vg[16 * I + 7]);
+      const float* C = vC + I * 64 + chalf * 32;
       float x[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int j = chalf * 32 + e, J = j >> 4;
-        const float ed = __expf(fminf(gi - vg[j], 0.f));          // same 16-block
-        const float f = (J < I) ? fb[e >> 4] * vF[j] : ((J == I && j <= i) ? ed : 0.f);
-        x[e] = gv[e] * rs * va[j] * f;
+      for (int e = 0; e < 32; e += 4) {
+        const float4 c4 = *reinterpret_cast<const float4*>(C + e);
+        const int j = chalf * 32 + e;
+        x[e] = (j <= i) ? gv[e] * rf * c4.x : 0.f;
+        x[e + 1] = (j + 1 <= i) ? gv[e + 1] * rf * c4.y : 0.f;
+        x[e + 2] = (j + 2 <= i) ? gv[e + 2] * rf * c4.z : 0.f;
+        x[e + 3] = (j + 3 <= i) ? gv[e + 3] * rf * c4.w : 0.f;
       }
       if (row < 64) {
 #pragma unroll

@@ -49,7 +49,7 @@ constexpr uint32_t wS = wWp + 16384;        // S hi | S lo [128][64]            
 constexpr uint32_t wP = wS + 32768;         // 2 slots x (P hi | P lo)                 32 KB
 constexpr uint32_t wE = wP + 32768;         // E hi | E lo | uE hi | uE lo             32 KB
 constexpr uint32_t wVec = wE + 32768;       // vectors                                   4 KB
-constexpr uint32_t kWsSmem = wVec + 4096 + 1024;
+constexpr uint32_t kWsSmem = wVec + 5120 + 1024;   // vectors + readout column factors
 constexpr int LDL = 68;                     // fp32 L/T row stride
 constexpr int LDX = 36;                     // fp32 scratch row stride
 
@@ -103,12 +103,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   float* vcr = va + 64;     // key normalisation
   float* vqn = vcr + 64;    // query normalisation
   float* vks = vqn + 64;    // e^{g_j} c_j
-  float* vF = vks + 64;     // e^{g_e(J) - g_j}
-  float* vkk = vF + 64;
+  float* vkk = vks + 64;
   float* vqq = vkk + 64;
   float* vla = vqq + 64;
   float* veta = vla + 64;
   float* vslot = veta + 64;   // 2 slots x [vqs 64 | vu 64 | gamma_C 1 (+pad)] = 2 x 192 floats
+  float* vC = vslot + 384;    // [4 I][64 j] c_j e^{g_m(I) - g_j}: readout column factors
   float* LT = reinterpret_cast<float*>(sm + wT);
   float* XS = LT + 64 * LDL;
 
@@ -358,12 +358,15 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         vqn[i] = qn;
         const float eg = __expf(gi);
         vks[i] = eg * cr;
-        vF[i] = __expf(vg[i | 15] - gi);
         vqs[i] = eg * qn;
         vu[i] = __expf(gC - gi) * coef;
         if (i == 0) vqs[128] = __expf(gC);
       }
       named_bar(2, 256);
+      {   // column factors of the readout (read after the next group wait)
+        const int I = ptid >> 6, j = ptid & 63;
+        vC[ptid] = va[j] * __expf(vg[16 * I + 7] - vg[j]);
+      }
       return true;
     };
 
@@ -381,21 +384,18 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         float gv[32];
         ld32cols(tmem + lane_off + tGram + pchalf * 32, gv);
         tmem_ld_wait();
-        const float gi = vg[i];
-        const float rs = (row < 64) ? vcr[i] : vqn[i];
-        float fb[2];
-#pragma unroll
-        for (int jb = 0; jb < 2; ++jb) {
-          const int J = pchalf * 2 + jb;
-          fb[jb] = (J < I) ? __expf(gi - vg[16 * J + 15]) : 0.f;
-        }
+        // one reference token per 16-row block: L_ij = G_ij [rs_i e^{g_i - g_m(I)}] [c_j e^{g_m(I) - g_j}]
+        const float rf = ((row < 64) ? vcr[i] : vqn[i]) * __expf(vg[i] - vg[16 * I + 7]);
+        const float* C = vC + I * 64 + pchalf * 32;
         float x[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int j = pchalf * 32 + e, J = j >> 4;
-          const float ed = __expf(fminf(gi - vg[j], 0.f));
-          const float f = (J < I) ? fb[e >> 4] * vF[j] : ((J == I && j <= i) ? ed : 0.f);
-          x[e] = gv[e] * rs * va[j] * f;
+        for (int e = 0; e < 32; e += 4) {
+          const float4 c4 = *reinterpret_cast<const float4*>(C + e);
+          const int j = pchalf * 32 + e;
+          x[e] = (j <= i) ? gv[e] * rf * c4.x : 0.f;
+          x[e + 1] = (j + 1 <= i) ? gv[e + 1] * rf * c4.y : 0.f;
+          x[e + 2] = (j + 2 <= i) ? gv[e + 2] * rf * c4.z : 0.f;
+          x[e + 3] = (j + 3 <= i) ? gv[e + 3] * rf * c4.w : 0.f;
         }
         if (row < 64) {
 #pragma unroll
