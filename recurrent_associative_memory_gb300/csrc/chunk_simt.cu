@@ -98,9 +98,15 @@ constexpr uint32_t rkK = 32768;      // (Gamma.K)^T [128 c][64 i]
 constexpr uint32_t rkQ = 65536;      // (Gamma.Q)^T [128 c][64 i]
 constexpr uint32_t rkW = 98304;      // (exp(g_C - g_j).w_j) [64 j][128 c]
 constexpr uint32_t rkG = 131072;     // gamma_C [128]
-constexpr uint32_t rkMap = 131584;   // variance chunk map, 4 floats per channel
-constexpr uint32_t rkP0 = 133632;    // variance p at the chunk start [128]
+constexpr uint32_t rkMap = 132096;   // variance chunk map, 4 floats per channel
+constexpr uint32_t rkP0 = 134144;    // variance p at the chunk start [128]
 constexpr uint32_t kRecK = 135168;
+// bf16 inputs: the record is read by the tensor-core carry instead, as bf16 hi/lo
+// 128-byte-swizzled tile images (same offsets as the GDN/KLA records for the
+// shared pieces): T [64][64], W'^T = ((Gamma.K)^T T^T) [128][64], P [64][64],
+// vectors (ones for the e^g qn and u slots, gamma_C per channel at float 128),
+// (Gamma.Q) and (exp(g_C - g_j).w_j) as [64 tok][128] in two 64-column blocks.
+constexpr uint32_t rbT = 0, rbWp = 16384, rbP = 49152, rbVec = 65536, rbQ = 66560, rbW = 99328;
 
 // PREP = false: the fused forward, one CTA per (b, h, 32 columns), chunks in order.
 // PREP = true (Diagonal KDN, dk = 128): one task per (b, h, chunk), all chunks in
@@ -510,6 +516,73 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       tile_store(sLT + (32 + 16 * mt) * LDL + 8 * nt, LDL, d, -1.f, lane);
     }
     __syncthreads();
+    if constexpr (PREP && sizeof(Tin) == 2) {   // tile images for the tensor-core carry
+      for (int e = tid; e < CM * CM; e += kThreads) {   // T^T, zero above the diagonal of T
+        const int i = e >> 6, j = e & 63;
+        sTt[j * CS + i] = (j <= i) ? sLT[i * LDL + j] : 0.f;
+      }
+      __syncthreads();
+      auto put = [&](uint32_t base, int row, int col, const float (&x)[8], uint32_t lo_off) {
+        uint4 hi, lo;
+        tc::split8(x, hi, lo);
+        const uint32_t off = umma::sw128_offset(row, col);
+        *reinterpret_cast<uint4*>(rec + base + off) = hi;
+        *reinterpret_cast<uint4*>(rec + base + lo_off + off) = lo;
+      };
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {   // T and P: [64 i][64 j]
+        const int e = tid + r * kThreads, i = e >> 3, g = e & 7;
+        float xt[8], xp[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          xt[q] = sTt[(8 * g + q) * CS + i];
+          xp[q] = sPt[(8 * g + q) * CS + i];
+        }
+        put(rbT, i, 8 * g, xt, 8192);
+        put(rbP, i, 8 * g, xp, 8192);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {   // (Gamma.Q) and Wbar: [64 tok][128] as two 64-column blocks
+        const int e = tid + r * kThreads, i = e >> 4, g = e & 15, kb = g >> 3, cg = g & 7;
+        float xq[8], xw[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          xq[q] = sQt[(8 * g + q) * CS + i];
+          xw[q] = sW[i * DK + 8 * g + q];
+        }
+        put(rbQ + kb * 8192, i, 8 * cg, xq, 16384);
+        put(rbW + kb * 8192, i, 8 * cg, xw, 16384);
+      }
+      {   // W'^T [c][i] = sum_{j <= i} (Gamma.K)^T[c][j] T[i][j]: 4 rows x 8 tokens per thread
+        const int c0 = (tid >> 3) * 4, i0 = (tid & 7) * 8;
+        float w[4][8];
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+#pragma unroll
+          for (int y = 0; y < 8; ++y) w[x][y] = 0.f;
+        for (int j = 0; j < i0 + 8; ++j) {
+          const float4 t0 = *reinterpret_cast<const float4*>(sTt + j * CS + i0);
+          const float4 t1 = *reinterpret_cast<const float4*>(sTt + j * CS + i0 + 4);
+          const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const float kv = sKt[(c0 + x) * CS + j];
+#pragma unroll
+            for (int y = 0; y < 8; ++y) w[x][y] += kv * tv[y];
+          }
+        }
+#pragma unroll
+        for (int x = 0; x < 4; ++x) put(rbWp, c0 + x, i0, w[x], 16384);
+      }
+      if (tid < CM) {
+        float* rv = reinterpret_cast<float*>(rec + rbVec);
+        rv[tid] = 1.f;          // e^g qn: folded into (Gamma.Q)
+        rv[64 + tid] = 1.f;     // u: folded into Wbar
+        rv[128 + tid] = sgC[tid];
+        rv[192 + tid] = sgC[64 + tid];
+      }
+      continue;
+    }
     if constexpr (PREP) {   // the carry's operands -> the record (float4 stores, coalesced)
       float4* rT = reinterpret_cast<float4*>(rec + rkT);
       float4* rP = reinterpret_cast<float4*>(rec + rkP);
@@ -1071,6 +1144,8 @@ cudaError_t launch_chunk_simt(const FwdArgs& a, int dtype, cudaStream_t st) {
 
 namespace dr {
 
+cudaError_t launch_carry_kdn_tc(const FwdArgs& a, void* workspace, cudaStream_t st);
+
 bool kdn_split_supported(int variant, int dtype, int dk, int dv, int chunk) {
   return variant == DR_KDN && (dtype == DR_BF16 || dtype == DR_FP32) && dk == 128 && dv == 128 &&
          chunk == 64;
@@ -1092,19 +1167,24 @@ cudaError_t launch_kdn_split(const FwdArgs& a, int dtype, void* workspace, cudaS
   if (err != cudaSuccess) return err;
   const size_t psmem = simt_smem_bytes(128);
   const int pgrid = (int)(ntask < nsm ? ntask : nsm);
-#define DR_KDN2(T_)                                                                        \
+#define DR_KDN_PREP(T_)                                                                    \
   {                                                                                        \
     err = cudaFuncSetAttribute(chunk_simt_kernel<128, T_, true>,                           \
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);   \
     if (err != cudaSuccess) return err;                                                    \
     chunk_simt_kernel<128, T_, true><<<pgrid, kThreads, psmem, st>>>(a, ws);              \
-    err = cudaFuncSetAttribute(kdn_carry_kernel<T_>,                                       \
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kKcSmem); \
-    if (err != cudaSuccess) return err;                                                    \
-    kdn_carry_kernel<T_><<<a.B * a.H * 2, kThreads, kKcSmem, st>>>(a, ws);                 \
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;                             \
   }
-  if (dtype == DR_BF16) DR_KDN2(__nv_bfloat16) else DR_KDN2(float)
-#undef DR_KDN2
+  if (dtype == DR_BF16) {   // bf16 records -> the tensor-core carry
+    DR_KDN_PREP(__nv_bfloat16)
+    return launch_carry_kdn_tc(a, ws, st);
+  }
+  DR_KDN_PREP(float)
+#undef DR_KDN_PREP
+  err = cudaFuncSetAttribute(kdn_carry_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kKcSmem);
+  if (err != cudaSuccess) return err;
+  kdn_carry_kernel<float><<<a.B * a.H * 2, kThreads, kKcSmem, st>>>(a, ws);
   return cudaGetLastError();
 }
 

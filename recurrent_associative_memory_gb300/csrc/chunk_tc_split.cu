@@ -662,6 +662,10 @@ __global__ void __launch_bounds__(128) pgdn_scan_kernel(FwdArgs a, uint8_t* __re
 //                      Its leader issues the two MMAs on the carry's critical
 //                      path itself, E(c+1) and dS(c), so no hand-off sits there.
 //   output warps 9-12  o = e^g qn . QS + PE for every row of the chunk.
+// MODE 0 (GDN, KLA): dS = K^T (u.E) with K by TMA.  MODE 1 (PGDN): dS from the
+// record's write keys.  MODE 2 (Diagonal KDN): Q S and dS take the record's
+// (Gamma.Q) and (exp(g_C - g_j).w_j) as bf16 hi/lo operands (per-channel decay
+// is folded into them), u = 1, and gamma_C is per state row.
 //   issue  warp 8      copies (record, K, Q, V) and the off-path MMAs U' = T V,
 //                      QS = Q S, PE = P E.
 // The row vectors (e^g qn, u, gamma_C) are read from the record in global
@@ -670,18 +674,26 @@ constexpr int kCarryThreads = 13 * 32;
 constexpr uint32_t cT = 0;                  // T hi | T lo              16 KB
 constexpr uint32_t cV = 16384;              // V [64 tok][64 col]       8 KB
 constexpr uint32_t cW = 24576;              // 2 slots x W' [hi kb0|kb1, lo kb0|kb1]   64 KB
-constexpr uint32_t cQ = 90112;              // Q kb0 | kb1              16 KB
-constexpr uint32_t cKP = 106496;            // dS operand + P: GDN/KLA [K kb0 | K kb1 | P hi | P lo]
-                                            // 32 KB; PGDN [W hi | W lo | P hi | P lo] 48 KB
-// then S hi | S lo [128][64] (32 KB) and E hi | E lo | uE hi | uE lo (32 KB)
-template <bool PG>
+constexpr uint32_t cQ = 90112;              // Q kb0 | kb1 (16 KB); KDN: Q~ hi | lo (32 KB)
+// then the dS operand + P: GDN/KLA [K kb0 | K kb1 | P hi | P lo] 32 KB; PGDN / KDN
+// [W hi | W lo | P hi | P lo] 48 KB; S hi | S lo [128][64] (32 KB); E hi | E lo |
+// uE hi | uE lo (32 KB; KDN, where u = 1: E hi | E lo, 16 KB)
+// KDN record (bf16 images; rT, rWp, rP, rVec as above, gamma_C per channel at
+// float 128 of rVec, ones elsewhere): (Gamma.Q) and Wbar as [64 tok][128] hi | lo
+constexpr uint32_t rQk = 66560;
+constexpr uint32_t rWk = 99328;
+constexpr uint32_t kRecKdn = 135168;        // also holds the variance chunk map and p0
+template <int MODE>
 struct CarryMap {
-  static constexpr uint32_t kKP = PG ? 49152 : 32768;
-  static constexpr uint32_t P = PG ? 32768 : 16384;     // P inside the K/P buffer
-  static constexpr uint32_t S = cKP + kKP;
+  static constexpr uint32_t kQ = MODE == 2 ? 32768 : 16384;
+  static constexpr uint32_t KP = cQ + kQ;
+  static constexpr uint32_t kKP = MODE == 0 ? 32768 : 49152;
+  static constexpr uint32_t P = MODE == 0 ? 16384 : 32768;     // P inside the K/P buffer
+  static constexpr uint32_t S = KP + kKP;
   static constexpr uint32_t E = S + 32768;
-  static constexpr uint32_t bytes = E + 32768 + 1024;
-  static constexpr uint32_t rec = PG ? kRecP : kRec;
+  static constexpr uint32_t bytes = E + (MODE == 2 ? 16384 : 32768) + 1024;
+  static constexpr uint32_t rec = MODE == 0 ? kRec : (MODE == 1 ? kRecP : kRecKdn);
+  static constexpr uint32_t rW_ = MODE == 1 ? rW : rWk;        // record dS operand
 };
 constexpr uint32_t tU0 = 0;                 // 2 slots M=64 x 64: U', then E
 constexpr uint32_t tQS = 128;               // M=64 x 64
@@ -696,7 +708,7 @@ enum {
   C_COUNT
 };
 
-template <bool PG>
+template <int MODE>
 __global__ void __launch_bounds__(kCarryThreads, 1)
     chunk_carry_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, FwdArgs a,
@@ -713,8 +725,9 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
   const int bh = blockIdx.x >> 1;
   const int b = bh / a.H, h = bh % a.H;
   const int NC = (a.T + 63) / 64;
-  using CM = CarryMap<PG>;
-  constexpr uint32_t cS = CM::S, cE = CM::E, kRecV = CM::rec;
+  using CM = CarryMap<MODE>;
+  constexpr uint32_t cS = CM::S, cE = CM::E, kRecV = CM::rec, cKP = CM::KP;
+  constexpr bool kKdn = (MODE == 2), kExplicitW = (MODE != 0);
   const uint8_t* recs = ws + (size_t)bh * NC * kRecV;
 
   if (tid == 0) {
@@ -808,7 +821,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
     }
     // row vectors of chunk 0: u (this thread's E row) and gamma_C
     float u_cur = reinterpret_cast<const float*>(recs + rVec)[64 + erow];
-    float g_cur = reinterpret_cast<const float*>(recs + rVec)[128];
+    float g_cur = reinterpret_cast<const float*>(recs + rVec)[kKdn ? 128 + srow : 128];
     bool bad = false;
 
     for (int c = 0; c < NC; ++c) {
@@ -817,7 +830,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       if (c + 1 < NC) {   // one chunk ahead; consumed next iteration
         const float* rv = reinterpret_cast<const float*>(recs + (size_t)(c + 1) * kRecV + rVec);
         u_nxt = rv[64 + erow];
-        g_nxt = rv[128];
+        g_nxt = rv[kKdn ? 128 + srow : 128];
       }
       // ---- E -> E and u.E hi/lo tiles (lanes 16-31 take columns 16-31 of the row)
       if (!(ok = group_wait2(1, 256, &bars[C_E], c & 1, nullptr, 0))) break;
@@ -851,9 +864,11 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
           split8(p, hi, lo);
           *reinterpret_cast<uint4*>(Et + off) = hi;
           *reinterpret_cast<uint4*>(Et + 8192 + off) = lo;
-          split8(q8, hi, lo);
-          *reinterpret_cast<uint4*>(Et + 16384 + off) = hi;
-          *reinterpret_cast<uint4*>(Et + 24576 + off) = lo;
+          if (!kKdn) {
+            split8(q8, hi, lo);
+            *reinterpret_cast<uint4*>(Et + 16384 + off) = hi;
+            *reinterpret_cast<uint4*>(Et + 24576 + off) = lo;
+          }
         }
       }
       tc_fence_before();
@@ -864,14 +879,15 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
         if (!s_abort && mbar_wait(&bars[C_KP], c & 1, kWait)) {
           tc_fence_after();
           const uint32_t kb = smem_u32(sm + cKP), eb = smem_u32(sm + cE);
+          const uint32_t ub = kKdn ? eb : eb + 16384;   // u.E (KDN: u = 1, the E tiles)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t uh = desc_sw128(eb + 16384 + ks * 2048, 8192, 1024);
-            const uint64_t ul = desc_sw128(eb + 24576 + ks * 2048, 8192, 1024);
+            const uint64_t uh = desc_sw128(ub + ks * 2048, 8192, 1024);
+            const uint64_t ul = desc_sw128(ub + 8192 + ks * 2048, 8192, 1024);
             const uint64_t dk = desc_sw128(kb + ks * 2048, 8192, 1024);
             mma_bf16(tmem + tDS, dk, uh, I_DS, ks > 0);
             mma_bf16(tmem + tDS, dk, ul, I_DS, true);
-            if (PG) {   // PGDN: dS = (W_hi + W_lo)^T (u.E); u = e^{g_C - g_j}
+            if (kExplicitW) {   // PGDN / KDN: dS = (W_hi + W_lo)^T (u.E)
               const uint64_t dkl = desc_sw128(kb + 16384 + ks * 2048, 8192, 1024);
               mma_bf16(tmem + tDS, dkl, uh, I_DS, true);
             }
@@ -1008,18 +1024,22 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       bulk_load(sm + cW + (c & 1) * 32768, recs + (size_t)c * kRecV + rWp, 32768, bar);
       n_w = c + 1;
     };
-    auto load_q = [&](int c) {
-      mbar_expect_tx(&bars[C_Q], 16384);
-      tma_load_4d(sm + cQ, &tmQ, &bars[C_Q], 0, h, c * 64, b);
-      tma_load_4d(sm + cQ + 8192, &tmQ, &bars[C_Q], 64, h, c * 64, b);
+    auto load_q = [&](int c) {   // KDN: the record's (Gamma.Q) hi | lo
+      mbar_expect_tx(&bars[C_Q], CM::kQ);
+      if (kKdn) {
+        bulk_load(sm + cQ, recs + (size_t)c * kRecV + rQk, 32768, &bars[C_Q]);
+      } else {
+        tma_load_4d(sm + cQ, &tmQ, &bars[C_Q], 0, h, c * 64, b);
+        tma_load_4d(sm + cQ + 8192, &tmQ, &bars[C_Q], 64, h, c * 64, b);
+      }
       n_q = c + 1;
     };
     auto load_kp = [&](int c) {   // the dS operand (K, or the PGDN write keys) and P
       const uint8_t* rec = recs + (size_t)c * kRecV;
       mbar_expect_tx(&bars[C_KP], CM::kKP);
       bulk_load(sm + cKP + CM::P, rec + rP, 16384, &bars[C_KP]);
-      if (PG) {
-        bulk_load(sm + cKP, rec + rW, 32768, &bars[C_KP]);
+      if (kExplicitW) {
+        bulk_load(sm + cKP, rec + CM::rW_, 32768, &bars[C_KP]);
       } else {
         tma_load_4d(sm + cKP, &tmK, &bars[C_KP], 0, h, c * 64, b);
         tma_load_4d(sm + cKP + 8192, &tmK, &bars[C_KP], 64, h, c * 64, b);
@@ -1067,6 +1087,10 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
           const uint64_t dq = desc_sw128(qb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
           mma_bf16(tmem + tQS, dq, dsh, I_N64, ks > 0);
           mma_bf16(tmem + tQS, dq, dsl, I_N64, true);
+          if (kKdn) {   // (Gamma.Q) is a computed operand: its lo term too
+            const uint64_t dql = desc_sw128(qb + 16384 + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
+            mma_bf16(tmem + tQS, dql, dsh, I_N64, true);
+          }
         }
         mma_commit(&bars[C_QS]);
       }
@@ -1172,16 +1196,29 @@ cudaError_t launch_chunk_tc_split(const FwdArgs& a, void* workspace, cudaStream_
   DR_PREP(DR_GDN) else DR_PREP(DR_KLA) else DR_PREP(DR_PGDN) else return cudaErrorInvalidValue;
 #undef DR_PREP
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-#define DR_CARRY(PG_)                                                                      \
+#define DR_CARRY(M_)                                                                       \
   {                                                                                        \
-    e = cudaFuncSetAttribute(chunk_carry_kernel<PG_>,                                      \
+    e = cudaFuncSetAttribute(chunk_carry_kernel<M_>,                                       \
                              cudaFuncAttributeMaxDynamicSharedMemorySize,                  \
-                             (int)CarryMap<PG_>::bytes);                                   \
+                             (int)CarryMap<M_>::bytes);                                    \
     if (e != cudaSuccess) return e;                                                        \
-    chunk_carry_kernel<PG_><<<a.B * a.H * 2, kCarryThreads, CarryMap<PG_>::bytes, st>>>(   \
+    chunk_carry_kernel<M_><<<a.B * a.H * 2, kCarryThreads, CarryMap<M_>::bytes, st>>>(     \
         mq, mk, mv, a, ws);                                                                \
   }
-  if (a.variant == DR_PGDN) DR_CARRY(true) else DR_CARRY(false)
+  if (a.variant == DR_PGDN) DR_CARRY(1) else DR_CARRY(0)
+  return cudaGetLastError();
+}
+
+// The tensor-core carry over Diagonal KDN records (bf16 inputs; records written by
+// the CUDA-core prep of chunk_simt.cu in the bf16 tile format above).
+cudaError_t launch_carry_kdn_tc(const FwdArgs& a, void* workspace, cudaStream_t st) {
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, a.q, a.B, a.T, a.H, 128) || !make_map(&mk, a.k, a.B, a.T, a.H, 128) ||
+      !make_map(&mv, a.v, a.B, a.T, a.H, 128))
+    return cudaErrorInvalidValue;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e;
+  DR_CARRY(2)
 #undef DR_CARRY
   return cudaGetLastError();
 }
