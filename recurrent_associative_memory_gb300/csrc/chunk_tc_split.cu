@@ -69,8 +69,11 @@ constexpr uint32_t kPrepTmem = 256;
 constexpr uint32_t I_GRAM = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t I_WT = idesc_bf16(128, 64, 1, 0);     // A = K (MN-major), B = Ts (K-major)
 constexpr uint32_t I_N64 = idesc_bf16(64, 64, 0, 1);
-constexpr uint32_t I_NEGT = idesc_bf16(64, 64, 1, 1, 1);    // A = W'^T (MN-major), negated
 constexpr uint32_t I_DS = idesc_bf16(128, 64, 1, 1);
+// N = 128 over a [hi | lo] pair of B tiles one 64-column group apart: one MMA
+// reads A once for both halves of the split operand (the two products land in
+// columns [0, 64) and [64, 128) and are added on readout)
+constexpr uint32_t I_DS2 = idesc_bf16(128, 128, 1, 1);
 
 enum { P_KQ0, P_KQ1, P_G0, P_G1, P_W, P_GFREE0, P_GFREE1, P_TREADY, P_WFREE, P_WREADY, P_COUNT };
 
@@ -656,18 +659,29 @@ __global__ void __launch_bounds__(128) pgdn_scan_kernel(FwdArgs a, uint8_t* __re
 }
 
 // ================================================================= chunk_carry
-// Roles (15 warps):
-//   state  warps 0-7   thread = one state row (TMEM lane) x 32 of the CTA's 64
-//                      columns: E readout -> E, u.E tiles; S <- gamma_C S + dS.
-//                      Its leader issues the two MMAs on the carry's critical
-//                      path itself, E(c+1) and dS(c), so no hand-off sits there.
+// Roles (13 warps):
+//   state  warps 0-7   thread = one TMEM lane x 32 of the CTA's 64 columns:
+//                      E readout -> E, u.E tiles; S <- gamma_C S + dS.  Its
+//                      leader issues the MMAs of the carry's critical path
+//                      itself (E(c), dS(c), then U'(c+1)), so no hand-off sits
+//                      on that path.
+//   issue  warp 8      copies (record, K, Q, V) and the off-path MMAs QS = Q S
+//                      and PE = P E.
 //   output warps 9-12  o = e^g qn . QS + PE for every row of the chunk.
+// MMA shapes.  One issuing thread sustains about one tcgen05.mma per 55-65
+// cycles, and the tensor pipe takes an M=128 x N=128 step in about 1.7x the
+// time of an M=64 x N=64 one, so the bf16 hi/lo splits are folded into few,
+// wide MMAs instead of one MMA per pair of parts:
+//   U', E   A = [T_hi ; T_lo], [W'_hi ; W'_lo] stacked along M (TMEM lanes
+//           64-127 hold the lo-part rows), B = [S_hi | S_lo] along N; the E
+//           readout adds the four quadrants (lanes i and 64 + i, columns j and
+//           64 + j), the lo x lo product included.
+//   dS      B = [uE_hi | uE_lo] (N = 128), the two column halves added.
+//   QS, PE  (M = 64) B = [S_hi | S_lo] and [E_hi | E_lo] (N = 128).
 // MODE 0 (GDN, KLA): dS = K^T (u.E) with K by TMA.  MODE 1 (PGDN): dS from the
 // record's write keys.  MODE 2 (Diagonal KDN): Q S and dS take the record's
 // (Gamma.Q) and (exp(g_C - g_j).w_j) as bf16 hi/lo operands (per-channel decay
 // is folded into them), u = 1, and gamma_C is per state row.
-//   issue  warp 8      copies (record, K, Q, V) and the off-path MMAs U' = T V,
-//                      QS = Q S, PE = P E.
 // The row vectors (e^g qn, u, gamma_C) are read from the record in global
 // memory, one chunk ahead, so no shared buffer of them needs recycling.
 constexpr int kCarryThreads = 13 * 32;
@@ -677,12 +691,14 @@ constexpr uint32_t cW = 24576;              // 2 slots x W' [hi kb0|kb1, lo kb0|
 constexpr uint32_t cQ = 90112;              // Q kb0 | kb1 (16 KB); KDN: Q~ hi | lo (32 KB)
 // then the dS operand + P: GDN/KLA [K kb0 | K kb1 | P hi | P lo] 32 KB; PGDN / KDN
 // [W hi | W lo | P hi | P lo] 48 KB; S hi | S lo [128][64] (32 KB); E hi | E lo |
-// uE hi | uE lo (32 KB; KDN, where u = 1: E hi | E lo, 16 KB)
+// uE hi | uE lo (32 KB; KDN, where u = 1: E hi | E lo, 16 KB).  The E readout
+// exchanges its lo-part rows through the W' slot that E has just consumed.
 // KDN record (bf16 images; rT, rWp, rP, rVec as above, gamma_C per channel at
 // float 128 of rVec, ones elsewhere): (Gamma.Q) and Wbar as [64 tok][128] hi | lo
 constexpr uint32_t rQk = 66560;
 constexpr uint32_t rWk = 99328;
 constexpr uint32_t kRecKdn = 135168;        // also holds the variance chunk map and p0
+constexpr int kXs = 68;                     // fp32 row stride of the E exchange buffer
 template <int MODE>
 struct CarryMap {
   static constexpr uint32_t kQ = MODE == 2 ? 32768 : 16384;
@@ -695,11 +711,15 @@ struct CarryMap {
   static constexpr uint32_t rec = MODE == 0 ? kRec : (MODE == 1 ? kRecP : kRecKdn);
   static constexpr uint32_t rW_ = MODE == 1 ? rW : rWk;        // record dS operand
 };
-constexpr uint32_t tU0 = 0;                 // 2 slots M=64 x 64: U', then E
-constexpr uint32_t tQS = 128;               // M=64 x 64
-constexpr uint32_t tPE = 192;               // M=64 x 64
-constexpr uint32_t tDS = 256;               // M=128 x 64
+constexpr uint32_t tE = 0;                  // M=128 x 128: U' then E, in four quadrants
+constexpr uint32_t tQS = 128;               // M=64 x 128: Q S_hi | Q S_lo
+constexpr uint32_t tPE = 256;               // M=64 x 128: (P_hi + P_lo) E_hi | P_hi E_lo
+constexpr uint32_t tDS = 384;               // M=128 x 128: K^T uE_hi (+ W_lo^T uE_hi) | K^T uE_lo
 constexpr uint32_t kCarryTmem = 512;
+constexpr uint32_t I_U2 = idesc_bf16(128, 64, 0, 1);         // [T_hi ; T_lo] V
+constexpr uint32_t I_E1 = idesc_bf16(128, 64, 1, 1, 1);      // -[W'_hi ; W'_lo] S_hi (or S_lo)
+constexpr uint32_t I_E2 = idesc_bf16(128, 128, 1, 1, 1);     // -[W'_hi ; W'_lo] [S_hi | S_lo]
+constexpr uint32_t I_Q2 = idesc_bf16(64, 128, 0, 1);         // Q [S_hi | S_lo], P_hi [E_hi | E_lo]
 
 enum {
   C_TV, C_W0, C_W1, C_Q, C_KP,              // copies landed
@@ -763,9 +783,13 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const bool leader = (tid == 0);
     const int srow = quad * 32 + lane;          // state row (dk index) = TMEM lane
-    const int erow = quad * 16 + (lane & 15);   // token row of E (M=64 layout)
-    const int ecol = 32 * hc + ((lane < 16) ? 0 : 16);
+    // E readout: lanes 0-63 hold the hi-part rows of E, lanes 64-127 the lo-part
+    // rows; partners (same row, same 32 columns) split the columns between them
+    const int erow = 32 * (quad & 1) + lane;
+    const int keep = quad >> 1, send = 1 - keep;
     float S[32];
+    uint64_t* last_bar = nullptr;               // leader: its last MMA commit
+    uint32_t last_par = 0;
     auto store_state_tiles = [&]() {
       uint8_t* sS = sm + cS;
 #pragma unroll
@@ -779,23 +803,41 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
         *reinterpret_cast<uint4*>(sS + 16384 + sw128_offset(srow, 32 * hc + 8 * m)) = lo;
       }
     };
-    // E(c) = U' - (W'_hi S_hi + W'_hi S_lo + W'_lo S_hi), issued by the leader
+    // U'(c) = [T_hi ; T_lo] V into the E accumulator (columns 0-63)
+    auto issue_u = [&](int c) {
+      tc_fence_after();
+      const uint64_t dt0 = desc_sw128(smem_u32(sm + cT), 16, 1024);
+      const uint64_t dv0 = desc_sw128(smem_u32(sm + cV), 8192, 1024);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + tE, dt0 + ks * (32 >> 4), dv0 + ks * (2048 >> 4), I_U2, ks > 0);
+      mma_commit(&bars[C_M2]);
+      last_bar = &bars[C_M2];
+      last_par = c & 1;
+    };
+    // E(c) = U' - [W'_hi ; W'_lo] [S_hi | S_lo].  Descriptors advance by the
+    // k-step's 2048 bytes in their start-address field (address >> 4; every
+    // operand lies inside shared memory, so the field cannot carry over).  The
+    // first k-step starts the S_lo columns (64-127) instead of accumulating.
     auto issue_e = [&](int c) {
       tc_fence_after();
-      const uint32_t sb = smem_u32(sm + cS), wp = smem_u32(sm + cW + (c & 1) * 32768);
-      const uint32_t uacc = tmem + tU0 + (c & 1) * 64;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t dsh = desc_sw128(sb + ks * 2048, 16384, 1024);
-        const uint64_t dsl = desc_sw128(sb + 16384 + ks * 2048, 16384, 1024);
-        const uint64_t dw = desc_sw128(wp + ks * 2048, 16384, 1024);
-        const uint64_t dwl = desc_sw128(wp + 16384 + ks * 2048, 16384, 1024);
-        mma_bf16(uacc, dw, dsh, I_NEGT, true);
-        mma_bf16(uacc, dw, dsl, I_NEGT, true);
-        mma_bf16(uacc, dwl, dsh, I_NEGT, true);
-      }
+      const uint64_t dsh0 = desc_sw128(smem_u32(sm + cS), 16384, 1024);
+      const uint64_t dw0 = desc_sw128(smem_u32(sm + cW + (c & 1) * 32768), 16384, 1024);
+      mma_bf16(tmem + tE, dw0, dsh0, I_E1, true);
+      mma_bf16(tmem + tE + 64, dw0, dsh0 + (16384 >> 4), I_E1, false);
+#pragma unroll 1
+      for (int ks = 1; ks < 8; ++ks)
+        mma_bf16(tmem + tE, dw0 + ks * (2048 >> 4), dsh0 + ks * (2048 >> 4), I_E2, true);
       mma_commit(&bars[C_E]);
+      last_bar = &bars[C_E];
+      last_par = c & 1;
     };
+    if (leader) {
+      if (mbar_wait(&bars[C_TV], 0, kWait))
+        issue_u(0);
+      else
+        s_abort = 1;
+    }
     {
       const long base = ((long)bh * 128 + srow) * a.dv + half * 64 + 32 * hc;
 #pragma unroll
@@ -811,8 +853,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
     named_bar(1, 256);
     bool ok = true;
     if (leader) {
-      ok = mbar_wait(&bars[C_M2], 0, kWait) && mbar_wait(&bars[C_W0], 0, kWait);
-      if (ok) {
+      if (!s_abort && mbar_wait(&bars[C_W0], 0, kWait)) {
         issue_e(0);
         mbar_arrive(&bars[C_SREADY]);   // S tiles of chunk 0 (for QS(0))
       } else {
@@ -832,23 +873,40 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
         u_nxt = rv[64 + erow];
         g_nxt = rv[kKdn ? 128 + srow : 128];
       }
-      // ---- E -> E and u.E hi/lo tiles (lanes 16-31 take columns 16-31 of the row)
-      if (!(ok = group_wait2(1, 256, &bars[C_E], c & 1, nullptr, 0))) break;
+      // ---- E -> E and u.E hi/lo tiles, once E(c) is done and PE(c-1) has read
+      // the previous E tiles
+      if (!(ok = group_wait2(1, 256, &bars[C_E], c & 1, c >= 1 ? &bars[C_PE] : nullptr, (c - 1) & 1)))
+        break;
       tc_fence_after();
       {
-        float ev[32], x[16];
-        float t16[16];
-        tmem_ld16(tmem + lane_off + tU0 + slot * 64 + 32 * hc, t16);
+        float* X = reinterpret_cast<float*>(sm + cW + slot * 32768);   // W'(c) is consumed
+        const uint32_t e0 = tmem + lane_off + tE + 32 * hc;
+        float kv[16], t16[16];
+        {   // the partner's 16 columns: column halves added, handed over in X
+          float s16[16];
+          tmem_ld16(e0 + 16 * send, s16);
+          tmem_ld16(e0 + 64 + 16 * send, t16);
+          tmem_ld_wait();
+          float* xr = X + erow * kXs + 32 * hc + 16 * send;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) ev[e] = t16[e];
-        tmem_ld16(tmem + lane_off + tU0 + slot * 64 + 32 * hc + 16, t16);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) ev[16 + e] = t16[e];
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(xr + e) =
+                make_float4(s16[e] + t16[e], s16[e + 1] + t16[e + 1], s16[e + 2] + t16[e + 2],
+                            s16[e + 3] + t16[e + 3]);
+        }
+        tmem_ld16(e0 + 16 * keep, kv);
+        tmem_ld16(e0 + 64 + 16 * keep, t16);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float y = __shfl_sync(0xffffffffu, ev[16 + e], lane & 15);
-          x[e] = (lane < 16) ? ev[e] : y;
+        for (int e = 0; e < 16; ++e) kv[e] += t16[e];
+        named_bar(1, 256);
+        {
+          const float* xk = X + erow * kXs + 32 * hc + 16 * keep;
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) {
+            const float4 p = *reinterpret_cast<const float4*>(xk + e);
+            kv[e] += p.x; kv[e + 1] += p.y; kv[e + 2] += p.z; kv[e + 3] += p.w;
+          }
         }
         uint8_t* Et = sm + cE;
 #pragma unroll
@@ -856,10 +914,10 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
           float p[8], q8[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            p[e] = x[8 * m + e];
+            p[e] = kv[8 * m + e];
             q8[e] = u_cur * p[e];
           }
-          const uint32_t off = sw128_offset(erow, ecol + 8 * m);
+          const uint32_t off = sw128_offset(erow, 32 * hc + 16 * keep + 8 * m);
           uint4 hi, lo;
           split8(p, hi, lo);
           *reinterpret_cast<uint4*>(Et + off) = hi;
@@ -874,26 +932,29 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       tc_fence_before();
       fence_proxy_async();
       named_bar(1, 256);
-      // ---- leader: dS(c) = K^T (uE_hi + uE_lo)
+      // ---- leader: dS(c) = K^T [uE_hi | uE_lo], then U'(c+1) into the E accumulator
       if (leader) {
         if (!s_abort && mbar_wait(&bars[C_KP], c & 1, kWait)) {
           tc_fence_after();
           const uint32_t kb = smem_u32(sm + cKP), eb = smem_u32(sm + cE);
           const uint32_t ub = kKdn ? eb : eb + 16384;   // u.E (KDN: u = 1, the E tiles)
+          const uint64_t du0 = desc_sw128(ub, 8192, 1024), dk0 = desc_sw128(kb, 8192, 1024);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t uh = desc_sw128(ub + ks * 2048, 8192, 1024);
-            const uint64_t ul = desc_sw128(ub + 8192 + ks * 2048, 8192, 1024);
-            const uint64_t dk = desc_sw128(kb + ks * 2048, 8192, 1024);
-            mma_bf16(tmem + tDS, dk, uh, I_DS, ks > 0);
-            mma_bf16(tmem + tDS, dk, ul, I_DS, true);
-            if (kExplicitW) {   // PGDN / KDN: dS = (W_hi + W_lo)^T (u.E)
-              const uint64_t dkl = desc_sw128(kb + 16384 + ks * 2048, 8192, 1024);
-              mma_bf16(tmem + tDS, dkl, uh, I_DS, true);
-            }
+            mma_bf16(tmem + tDS, dk0 + ks * (2048 >> 4), du0 + ks * (2048 >> 4), I_DS2, ks > 0);
+            if (kExplicitW)   // PGDN / KDN: dS = (W_hi + W_lo)^T (u.E)
+              mma_bf16(tmem + tDS, dk0 + ((16384 + ks * 2048) >> 4), du0 + ks * (2048 >> 4), I_DS, true);
           }
           mma_commit(&bars[C_DS]);
+          last_bar = &bars[C_DS];
+          last_par = c & 1;
           mbar_arrive(&bars[C_EREADY]);
+          if (c + 1 < NC) {
+            if (mbar_wait(&bars[C_TV], (c + 1) & 1, kWait))
+              issue_u(c + 1);
+            else
+              s_abort = 1;
+          }
         } else {
           s_abort = 1;
         }
@@ -902,27 +963,26 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       if (!(ok = group_wait2(1, 256, &bars[C_DS], c & 1, &bars[C_QS], c & 1))) break;
       tc_fence_after();
       {
-        float ds[32];
-        float t16[16];
-        tmem_ld16(tmem + lane_off + tDS + 32 * hc, t16);
+        float t16[16], l16[16];
+        const uint32_t dcol0 = tmem + lane_off + tDS + 32 * hc;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) ds[e] = t16[e];
-        tmem_ld16(tmem + lane_off + tDS + 32 * hc + 16, t16);
+        for (int part = 0; part < 2; ++part) {
+          tmem_ld16(dcol0 + 16 * part, t16);
+          tmem_ld16(dcol0 + 64 + 16 * part, l16);
+          tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) ds[16 + e] = t16[e];
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) S[e] = g_cur * S[e] + ds[e];
+          for (int e = 0; e < 16; ++e) S[16 * part + e] = g_cur * S[16 * part + e] + (t16[e] + l16[e]);
+        }
         store_state_tiles();
       }
       tc_fence_before();
       fence_proxy_async();
       named_bar(1, 256);
-      // ---- leader: E(c+1) as soon as S(c+1), W'(c+1) and U'(c+1) are in place
+      // ---- leader: E(c+1) once S(c+1) and W'(c+1) are in place (U'(c+1) precedes
+      // it in this thread's MMA order)
       if (leader) {
         if (c + 1 < NC) {
-          if (!s_abort && mbar_wait(&bars[C_M2], (c + 1) & 1, kWait) &&
-              mbar_wait(&bars[C_W0 + ((c + 1) & 1)], ((c + 1) >> 1) & 1, kWait))
+          if (!s_abort && mbar_wait(&bars[C_W0 + ((c + 1) & 1)], ((c + 1) >> 1) & 1, kWait))
             issue_e(c + 1);
           else
             s_abort = 1;
@@ -932,6 +992,8 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       u_cur = u_nxt;
       g_cur = g_nxt;
     }
+    // the leader's MMAs complete before TMEM is freed (its commits track all of them)
+    if (leader && last_bar) mbar_wait(last_bar, last_par, kWait / 4);
     if (!s_abort && a.S) {
       const long base = ((long)bh * 128 + srow) * a.dv + half * 64 + 32 * hc;
 #pragma unroll
@@ -947,7 +1009,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
     const int quad = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const bool oleader = (warp == 9 && lane == 0);
-    const int i = quad * 16 + (lane & 15);
+    const int i = quad * 16 + (lane & 15);       // token row (M=64 layout: lanes 0-15)
     bool bad = false;
     float qs_cur = reinterpret_cast<const float*>(recs + rVec)[i];
     for (int c = 0; c < NC; ++c) {
@@ -960,25 +1022,29 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
                           (((long)b * a.T + t0 + i) * a.H + h) * a.dv + half * 64;
 #pragma unroll
       for (int hcol = 0; hcol < 2; ++hcol) {
-        float o[32];
-        {
-          float qv[16], pe[16];
-          tmem_ld16(tmem + lane_off + tQS + 32 * hcol, qv);
-          tmem_ld16(tmem + lane_off + tPE + 32 * hcol, pe);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = qs_cur * qv[e] + pe[e];
-          tmem_ld16(tmem + lane_off + tQS + 32 * hcol + 16, qv);
-          tmem_ld16(tmem + lane_off + tPE + 32 * hcol + 16, pe);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) o[16 + e] = qs_cur * qv[e] + pe[e];
-        }
+        const uint32_t q0 = tmem + lane_off + tQS + 32 * hcol, p0 = tmem + lane_off + tPE + 32 * hcol;
         float x[16];
+        {   // columns 16-31 of the 32: lanes 16-31 take them from lanes 0-15
+          float qa[16], qb[16], pa[16], pb[16];
+          tmem_ld16(q0 + 16, qa);
+          tmem_ld16(q0 + 80, qb);
+          tmem_ld16(p0 + 16, pa);
+          tmem_ld16(p0 + 80, pb);
+          tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float y = __shfl_sync(0xffffffffu, o[16 + e], lane & 15);
-          x[e] = (lane < 16) ? o[e] : y;
+          for (int e = 0; e < 16; ++e)
+            x[e] = __shfl_sync(0xffffffffu, qs_cur * (qa[e] + qb[e]) + (pa[e] + pb[e]), lane & 15);
+        }
+        {   // columns 0-15
+          float qa[16], qb[16], pa[16], pb[16];
+          tmem_ld16(q0, qa);
+          tmem_ld16(q0 + 64, qb);
+          tmem_ld16(p0, pa);
+          tmem_ld16(p0 + 64, pb);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            x[e] = (lane < 16) ? qs_cur * (qa[e] + qb[e]) + (pa[e] + pb[e]) : x[e];
         }
         if (i < Cc) {
           const int col = 32 * hcol + ((lane < 16) ? 0 : 16);
@@ -1011,6 +1077,8 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       return true;
     };
     int n_tv = 0, n_w = 0, n_q = 0, n_kp = 0;   // copies issued per buffer group
+    uint64_t* last_bar = nullptr;               // this thread's last MMA commit
+    uint32_t last_par = 0;
     auto load_tv = [&](int c) {
       const uint8_t* rec = recs + (size_t)c * kRecV;
       mbar_expect_tx(&bars[C_TV], 16384 + 8192);
@@ -1046,79 +1114,58 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       }
       n_kp = c + 1;
     };
-    auto m2 = [&](int c) {   // U' = T_hi V + T_lo V into slot c & 1
-      tc_fence_after();
-      const uint32_t tb = smem_u32(sm + cT), vt = smem_u32(sm + cV);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t dt = desc_sw128(tb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
-        const uint64_t dv = desc_sw128(vt + (ks & 3) * 2048, 8192, 1024);
-        mma_bf16(tmem + tU0 + (c & 1) * 64, dt, dv, I_N64, ks > 0);
-      }
-      mma_commit(&bars[C_M2]);
-    };
     load_tv(0);
     load_w(0);
     if (NC > 1) load_w(1);
     load_q(0);
     load_kp(0);
-    bool ok = wait(C_TV, 0);
-    if (ok) m2(0);
-    int n_pe = 0, n_m2 = ok ? 1 : 0;
-    if (ok && NC > 1 && (ok = wait(C_M2, 0))) load_tv(1);
-    // Pipe order per chunk: E(c) [state leader], QS(c), U'(c+1), dS(c) [state
-    // leader], PE(c).  U'(c+1) runs while the state warps read E(c) out, so only
-    // PE(c) sits between dS(c) and E(c+1), inside the S update.  Each refill
-    // follows the last read of its buffer and precedes, in this thread's order,
-    // the MMA whose completion could start the buffer's next phase, so no waiter
-    // can fall two phases behind.
+    bool ok = true;
+    // T/V of chunk 1 once U'(0) has read chunk 0's
+    if (NC > 1 && (ok = wait(C_M2, 0))) load_tv(1);
+    // Pipe order per chunk: E(c) [state leader], QS(c) [here, while E(c) is read
+    // out], dS(c) and U'(c+1) [state leader], PE(c) [here, during the S update],
+    // E(c+1).  Each refill follows the last read of its buffer and precedes, in
+    // this thread's order, the MMA whose completion could start the buffer's
+    // next phase, so no waiter can fall two phases behind.
     for (int c = 0; ok && c < NC; ++c) {
-      // QS(c) = Q (S_hi + S_lo): S(c) tiles ready, tQS read by the output of c-1
+      // QS(c) = Q [S_hi | S_lo]: S(c) tiles ready, tQS read by the output of c-1
       if (!(ok = wait(C_SREADY, c & 1))) break;
       if (c >= 1 && !(ok = wait(C_OUTDONE, (c - 1) & 1))) break;
       if (!(ok = wait(C_Q, c & 1))) break;
       tc_fence_after();
       {
-        const uint32_t sb = smem_u32(sm + cS), qb = smem_u32(sm + cQ);
+        const uint64_t ds0 = desc_sw128(smem_u32(sm + cS), 16384, 1024);
+        const uint64_t dq0 = desc_sw128(smem_u32(sm + cQ), 16, 1024);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t dsh = desc_sw128(sb + ks * 2048, 16384, 1024);
-          const uint64_t dsl = desc_sw128(sb + 16384 + ks * 2048, 16384, 1024);
-          const uint64_t dq = desc_sw128(qb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
-          mma_bf16(tmem + tQS, dq, dsh, I_N64, ks > 0);
-          mma_bf16(tmem + tQS, dq, dsl, I_N64, true);
-          if (kKdn) {   // (Gamma.Q) is a computed operand: its lo term too
-            const uint64_t dql = desc_sw128(qb + 16384 + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
-            mma_bf16(tmem + tQS, dql, dsh, I_N64, true);
-          }
+          const uint64_t dq = dq0 + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4);
+          const uint64_t ds = ds0 + ks * (2048 >> 4);
+          mma_bf16(tmem + tQS, dq, ds, I_Q2, ks > 0);
+          if (kKdn)   // (Gamma.Q) is a computed operand: its lo term against S_hi
+            mma_bf16(tmem + tQS, dq + (16384 >> 4), ds, I_N64, true);
         }
         mma_commit(&bars[C_QS]);
+        last_bar = &bars[C_QS];
+        last_par = c & 1;
       }
-      // U'(c+1) into the other slot (its E(c-1) was read out before EREADY(c-1))
-      if (c + 1 < NC) {
-        if (!(ok = wait(C_TV, (c + 1) & 1))) break;
-        m2(c + 1);
-        n_m2 = c + 2;
-      }
-      // PE(c) = P_hi E_hi + P_lo E_hi + P_hi E_lo once the E tiles are written
+      // PE(c) = P_hi [E_hi | E_lo] + P_lo E_hi once the E tiles are written
       if (!(ok = wait(C_EREADY, c & 1) && wait(C_KP, c & 1))) break;
       tc_fence_after();
       {
-        const uint32_t pb = smem_u32(sm + cKP) + CM::P, eb = smem_u32(sm + cE);
+        const uint64_t dp0 = desc_sw128(smem_u32(sm + cKP) + CM::P, 16, 1024);
+        const uint64_t de0 = desc_sw128(smem_u32(sm + cE), 8192, 1024);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t ph = desc_sw128(pb + ks * 32, 16, 1024);
-          const uint64_t pl = desc_sw128(pb + 8192 + ks * 32, 16, 1024);
-          const uint64_t eh = desc_sw128(eb + ks * 2048, 8192, 1024);
-          const uint64_t el = desc_sw128(eb + 8192 + ks * 2048, 8192, 1024);
-          mma_bf16(tmem + tPE, ph, eh, I_N64, ks > 0);
-          mma_bf16(tmem + tPE, pl, eh, I_N64, true);
-          mma_bf16(tmem + tPE, ph, el, I_N64, true);
+          const uint64_t dp = dp0 + ks * (32 >> 4), de = de0 + ks * (2048 >> 4);
+          mma_bf16(tmem + tPE, dp, de, I_Q2, ks > 0);
+          mma_bf16(tmem + tPE, dp + (8192 >> 4), de, I_N64, true);
         }
         mma_commit(&bars[C_PE]);
-        n_pe = c + 1;
+        last_bar = &bars[C_PE];
+        last_par = c & 1;
       }
-      // W' slot c & 1 for chunk c+2: E(c), its reader, finished before EREADY(c)
+      // W' slot c & 1 for chunk c+2: E(c) and the exchange through the slot
+      // finished before EREADY(c)
       if (c + 2 < NC) load_w(c + 2);
       // T/V of chunk c+2 once U'(c+1) has read them
       if (c + 2 < NC) {
@@ -1134,9 +1181,8 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       if (c + 1 < NC) load_kp(c + 1);
     }
     if (!ok) set_status(DR_ERR_TIMEOUT);
-    // drain: the last MMAs and every copy issued, so nothing lands after exit
-    if (n_pe > 0) mbar_wait(&bars[C_PE], (n_pe - 1) & 1, kWait / 4);
-    if (n_m2 > 0) mbar_wait(&bars[C_M2], (n_m2 - 1) & 1, kWait / 4);
+    // drain: this thread's last MMAs and every copy issued, so nothing lands after exit
+    if (last_bar) mbar_wait(last_bar, last_par, kWait / 4);
     if (n_tv > 0) mbar_wait(&bars[C_TV], (n_tv - 1) & 1, kWait / 4);
     if (n_q > 0) mbar_wait(&bars[C_Q], (n_q - 1) & 1, kWait / 4);
     if (n_kp > 0) mbar_wait(&bars[C_KP], (n_kp - 1) & 1, kWait / 4);
