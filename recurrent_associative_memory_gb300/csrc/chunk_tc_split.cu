@@ -659,14 +659,17 @@ __global__ void __launch_bounds__(128) pgdn_scan_kernel(FwdArgs a, uint8_t* __re
 }
 
 // ================================================================= chunk_carry
-// Roles (13 warps):
+// Roles (14 warps):
 //   state  warps 0-7   thread = one TMEM lane x 32 of the CTA's 64 columns:
 //                      E readout -> E, u.E tiles; S <- gamma_C S + dS.  Its
-//                      leader issues the MMAs of the carry's critical path
-//                      itself (E(c), dS(c), then U'(c+1)), so no hand-off sits
-//                      on that path.
-//   issue  warp 8      copies (record, K, Q, V) and the off-path MMAs QS = Q S
-//                      and PE = P E.
+//                      leader issues the two MMAs of the carry's critical path
+//                      itself (E(c), dS(c)), so no hand-off sits on that path.
+//   issue  warp 8      copies (T, V, W', Q) and the off-path MMAs QS = Q S and
+//                      U'(c+1) = T V.
+//   PE     warp 13     the off-path MMA PE = P E (a second issuing thread: one
+//                      thread issues about one MMA per 60-70 cycles, so U' and
+//                      PE, both due while the state is updated, come from two),
+//                      and the K and P copies, which wait on dS and PE.
 //   output warps 9-12  o = e^g qn . QS + PE for every row of the chunk.
 // MMA shapes.  One issuing thread sustains about one tcgen05.mma per 55-65
 // cycles, and the tensor pipe takes an M=128 x N=128 step in about 1.7x the
@@ -684,7 +687,7 @@ __global__ void __launch_bounds__(128) pgdn_scan_kernel(FwdArgs a, uint8_t* __re
 // is folded into them), u = 1, and gamma_C is per state row.
 // The row vectors (e^g qn, u, gamma_C) are read from the record in global
 // memory, one chunk ahead, so no shared buffer of them needs recycling.
-constexpr int kCarryThreads = 13 * 32;
+constexpr int kCarryThreads = 14 * 32;
 constexpr uint32_t cT = 0;                  // T hi | T lo              16 KB
 constexpr uint32_t cV = 16384;              // V [64 tok][64 col]       8 KB
 constexpr uint32_t cW = 24576;              // 2 slots x W' [hi kb0|kb1, lo kb0|kb1]   64 KB
@@ -722,9 +725,9 @@ constexpr uint32_t I_E2 = idesc_bf16(128, 128, 1, 1, 1);     // -[W'_hi ; W'_lo]
 constexpr uint32_t I_Q2 = idesc_bf16(64, 128, 0, 1);         // Q [S_hi | S_lo], P_hi [E_hi | E_lo]
 
 enum {
-  C_TV, C_W0, C_W1, C_Q, C_KP,              // copies landed
+  C_TV, C_W0, C_W1, C_Q, C_K, C_P,          // copies landed
   C_M2, C_E, C_QS, C_DS, C_PE,              // MMAs complete
-  C_SREADY, C_EREADY, C_OUTDONE,            // group hand-offs to the issue lane
+  C_SREADY, C_EREADY, C_QSFREE, C_OUTDONE,  // group hand-offs to the issuing lanes
   C_COUNT
 };
 
@@ -803,18 +806,6 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
         *reinterpret_cast<uint4*>(sS + 16384 + sw128_offset(srow, 32 * hc + 8 * m)) = lo;
       }
     };
-    // U'(c) = [T_hi ; T_lo] V into the E accumulator (columns 0-63)
-    auto issue_u = [&](int c) {
-      tc_fence_after();
-      const uint64_t dt0 = desc_sw128(smem_u32(sm + cT), 16, 1024);
-      const uint64_t dv0 = desc_sw128(smem_u32(sm + cV), 8192, 1024);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + tE, dt0 + ks * (32 >> 4), dv0 + ks * (2048 >> 4), I_U2, ks > 0);
-      mma_commit(&bars[C_M2]);
-      last_bar = &bars[C_M2];
-      last_par = c & 1;
-    };
     // E(c) = U' - [W'_hi ; W'_lo] [S_hi | S_lo].  Descriptors advance by the
     // k-step's 2048 bytes in their start-address field (address >> 4; every
     // operand lies inside shared memory, so the field cannot carry over).  The
@@ -832,12 +823,6 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       last_bar = &bars[C_E];
       last_par = c & 1;
     };
-    if (leader) {
-      if (mbar_wait(&bars[C_TV], 0, kWait))
-        issue_u(0);
-      else
-        s_abort = 1;
-    }
     {
       const long base = ((long)bh * 128 + srow) * a.dv + half * 64 + 32 * hc;
 #pragma unroll
@@ -853,7 +838,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
     named_bar(1, 256);
     bool ok = true;
     if (leader) {
-      if (!s_abort && mbar_wait(&bars[C_W0], 0, kWait)) {
+      if (!s_abort && mbar_wait(&bars[C_M2], 0, kWait) && mbar_wait(&bars[C_W0], 0, kWait)) {
         issue_e(0);
         mbar_arrive(&bars[C_SREADY]);   // S tiles of chunk 0 (for QS(0))
       } else {
@@ -932,9 +917,9 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       tc_fence_before();
       fence_proxy_async();
       named_bar(1, 256);
-      // ---- leader: dS(c) = K^T [uE_hi | uE_lo], then U'(c+1) into the E accumulator
+      // ---- leader: dS(c) = K^T [uE_hi | uE_lo]
       if (leader) {
-        if (!s_abort && mbar_wait(&bars[C_KP], c & 1, kWait)) {
+        if (!s_abort && mbar_wait(&bars[C_K], c & 1, kWait)) {
           tc_fence_after();
           const uint32_t kb = smem_u32(sm + cKP), eb = smem_u32(sm + cE);
           const uint32_t ub = kKdn ? eb : eb + 16384;   // u.E (KDN: u = 1, the E tiles)
@@ -949,12 +934,6 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
           last_bar = &bars[C_DS];
           last_par = c & 1;
           mbar_arrive(&bars[C_EREADY]);
-          if (c + 1 < NC) {
-            if (mbar_wait(&bars[C_TV], (c + 1) & 1, kWait))
-              issue_u(c + 1);
-            else
-              s_abort = 1;
-          }
         } else {
           s_abort = 1;
         }
@@ -978,11 +957,11 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       tc_fence_before();
       fence_proxy_async();
       named_bar(1, 256);
-      // ---- leader: E(c+1) once S(c+1) and W'(c+1) are in place (U'(c+1) precedes
-      // it in this thread's MMA order)
+      // ---- leader: E(c+1) once S(c+1), U'(c+1) and W'(c+1) are in place
       if (leader) {
         if (c + 1 < NC) {
-          if (!s_abort && mbar_wait(&bars[C_W0 + ((c + 1) & 1)], ((c + 1) >> 1) & 1, kWait))
+          if (!s_abort && mbar_wait(&bars[C_M2], (c + 1) & 1, kWait) &&
+              mbar_wait(&bars[C_W0 + ((c + 1) & 1)], ((c + 1) >> 1) & 1, kWait))
             issue_e(c + 1);
           else
             s_abort = 1;
@@ -1004,7 +983,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       }
     }
     if (bad) set_status(DR_ERR_NONFINITE);
-  } else if (warp >= 9) {
+  } else if (warp >= 9 && warp <= 12) {
     // ===================================================================== output warps
     const int quad = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -1016,36 +995,47 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       float qs_nxt = 0.f;
       if (c + 1 < NC) qs_nxt = reinterpret_cast<const float*>(recs + (size_t)(c + 1) * kRecV + rVec)[i];
       const int t0 = c * 64, Cc = min(64, a.T - t0);
-      if (!group_wait2(2, 128, &bars[C_QS], c & 1, &bars[C_PE], c & 1)) break;
+      // e^g qn . Q S first: tQS is released as soon as it is read, so QS(c+1)
+      // need not wait for PE(c) and the stores of chunk c
+      float qv[2][16];
+      if (!group_wait2(2, 128, &bars[C_QS], c & 1, nullptr, 0)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int hcol = 0; hcol < 2; ++hcol) {
+        const uint32_t q0 = tmem + lane_off + tQS + 32 * hcol;
+        float qa[16], qb[16];
+        tmem_ld16(q0 + 16, qa);   // columns 16-31 of the 32: lanes 16-31 take them from lanes 0-15
+        tmem_ld16(q0 + 80, qb);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) qv[hcol][e] = __shfl_sync(0xffffffffu, qs_cur * (qa[e] + qb[e]), lane & 15);
+        tmem_ld16(q0, qa);        // columns 0-15
+        tmem_ld16(q0 + 64, qb);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) qv[hcol][e] = (lane < 16) ? qs_cur * (qa[e] + qb[e]) : qv[hcol][e];
+      }
+      tc_fence_before();
+      named_bar(2, 128);
+      if (oleader) mbar_arrive(&bars[C_QSFREE]);
+      if (!group_wait2(2, 128, &bars[C_PE], c & 1, nullptr, 0)) break;
       tc_fence_after();
       __nv_bfloat16* op = static_cast<__nv_bfloat16*>(a.out) +
                           (((long)b * a.T + t0 + i) * a.H + h) * a.dv + half * 64;
 #pragma unroll
       for (int hcol = 0; hcol < 2; ++hcol) {
-        const uint32_t q0 = tmem + lane_off + tQS + 32 * hcol, p0 = tmem + lane_off + tPE + 32 * hcol;
-        float x[16];
-        {   // columns 16-31 of the 32: lanes 16-31 take them from lanes 0-15
-          float qa[16], qb[16], pa[16], pb[16];
-          tmem_ld16(q0 + 16, qa);
-          tmem_ld16(q0 + 80, qb);
-          tmem_ld16(p0 + 16, pa);
-          tmem_ld16(p0 + 80, pb);
-          tmem_ld_wait();
+        const uint32_t p0 = tmem + lane_off + tPE + 32 * hcol;
+        float x[16], pa[16], pb[16];
+        tmem_ld16(p0 + 16, pa);
+        tmem_ld16(p0 + 80, pb);
+        tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            x[e] = __shfl_sync(0xffffffffu, qs_cur * (qa[e] + qb[e]) + (pa[e] + pb[e]), lane & 15);
-        }
-        {   // columns 0-15
-          float qa[16], qb[16], pa[16], pb[16];
-          tmem_ld16(q0, qa);
-          tmem_ld16(q0 + 64, qb);
-          tmem_ld16(p0, pa);
-          tmem_ld16(p0 + 64, pb);
-          tmem_ld_wait();
+        for (int e = 0; e < 16; ++e) x[e] = __shfl_sync(0xffffffffu, pa[e] + pb[e], lane & 15);
+        tmem_ld16(p0, pa);
+        tmem_ld16(p0 + 64, pb);
+        tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            x[e] = (lane < 16) ? qs_cur * (qa[e] + qb[e]) + (pa[e] + pb[e]) : x[e];
-        }
+        for (int e = 0; e < 16; ++e) x[e] = qv[hcol][e] + ((lane < 16) ? pa[e] + pb[e] : x[e]);
         if (i < Cc) {
           const int col = 32 * hcol + ((lane < 16) ? 0 : 16);
 #pragma unroll
@@ -1066,7 +1056,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       qs_cur = qs_nxt;
     }
     if (bad) set_status(DR_ERR_NONFINITE);
-  } else if (lane == 0) {
+  } else if (warp == 8 && lane == 0) {
     // ===================================================================== issue lane
     auto wait = [&](int id, uint32_t parity) -> bool {
       if (s_abort) return false;
@@ -1076,7 +1066,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       }
       return true;
     };
-    int n_tv = 0, n_w = 0, n_q = 0, n_kp = 0;   // copies issued per buffer group
+    int n_tv = 0, n_w = 0, n_q = 0;             // copies issued per buffer group
     uint64_t* last_bar = nullptr;               // this thread's last MMA commit
     uint32_t last_par = 0;
     auto load_tv = [&](int c) {
@@ -1102,35 +1092,35 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       }
       n_q = c + 1;
     };
-    auto load_kp = [&](int c) {   // the dS operand (K, or the PGDN write keys) and P
-      const uint8_t* rec = recs + (size_t)c * kRecV;
-      mbar_expect_tx(&bars[C_KP], CM::kKP);
-      bulk_load(sm + cKP + CM::P, rec + rP, 16384, &bars[C_KP]);
-      if (kExplicitW) {
-        bulk_load(sm + cKP, rec + CM::rW_, 32768, &bars[C_KP]);
-      } else {
-        tma_load_4d(sm + cKP, &tmK, &bars[C_KP], 0, h, c * 64, b);
-        tma_load_4d(sm + cKP + 8192, &tmK, &bars[C_KP], 64, h, c * 64, b);
-      }
-      n_kp = c + 1;
+    // U'(c) = [T_hi ; T_lo] V into the E accumulator (columns 0-63)
+    auto issue_u = [&](int c) {
+      tc_fence_after();
+      const uint64_t dt0 = desc_sw128(smem_u32(sm + cT), 16, 1024);
+      const uint64_t dv0 = desc_sw128(smem_u32(sm + cV), 8192, 1024);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + tE, dt0 + ks * (32 >> 4), dv0 + ks * (2048 >> 4), I_U2, ks > 0);
+      mma_commit(&bars[C_M2]);
+      last_bar = &bars[C_M2];
+      last_par = c & 1;
     };
     load_tv(0);
     load_w(0);
     if (NC > 1) load_w(1);
     load_q(0);
-    load_kp(0);
-    bool ok = true;
+    bool ok = wait(C_TV, 0);
+    if (ok) issue_u(0);
     // T/V of chunk 1 once U'(0) has read chunk 0's
-    if (NC > 1 && (ok = wait(C_M2, 0))) load_tv(1);
+    if (ok && NC > 1 && (ok = wait(C_M2, 0))) load_tv(1);
     // Pipe order per chunk: E(c) [state leader], QS(c) [here, while E(c) is read
-    // out], dS(c) and U'(c+1) [state leader], PE(c) [here, during the S update],
-    // E(c+1).  Each refill follows the last read of its buffer and precedes, in
-    // this thread's order, the MMA whose completion could start the buffer's
-    // next phase, so no waiter can fall two phases behind.
+    // out], dS(c) [state leader], U'(c+1) [here] and PE(c) [PE lane] while the
+    // state is updated, E(c+1).  Each refill follows the last read of its buffer
+    // and precedes, in this thread's order, the MMA whose completion could start
+    // the buffer's next phase, so no waiter can fall two phases behind.
     for (int c = 0; ok && c < NC; ++c) {
       // QS(c) = Q [S_hi | S_lo]: S(c) tiles ready, tQS read by the output of c-1
       if (!(ok = wait(C_SREADY, c & 1))) break;
-      if (c >= 1 && !(ok = wait(C_OUTDONE, (c - 1) & 1))) break;
+      if (c >= 1 && !(ok = wait(C_QSFREE, (c - 1) & 1))) break;
       if (!(ok = wait(C_Q, c & 1))) break;
       tc_fence_after();
       {
@@ -1148,49 +1138,97 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
         last_bar = &bars[C_QS];
         last_par = c & 1;
       }
-      // PE(c) = P_hi [E_hi | E_lo] + P_lo E_hi once the E tiles are written
-      if (!(ok = wait(C_EREADY, c & 1) && wait(C_KP, c & 1))) break;
-      tc_fence_after();
-      {
-        const uint64_t dp0 = desc_sw128(smem_u32(sm + cKP) + CM::P, 16, 1024);
-        const uint64_t de0 = desc_sw128(smem_u32(sm + cE), 8192, 1024);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t dp = dp0 + ks * (32 >> 4), de = de0 + ks * (2048 >> 4);
-          mma_bf16(tmem + tPE, dp, de, I_Q2, ks > 0);
-          mma_bf16(tmem + tPE, dp + (8192 >> 4), de, I_N64, true);
-        }
-        mma_commit(&bars[C_PE]);
-        last_bar = &bars[C_PE];
-        last_par = c & 1;
+      // U'(c+1) once E(c) has been read out of the accumulator (EREADY(c))
+      if (!(ok = wait(C_EREADY, c & 1))) break;
+      if (c + 1 < NC) {
+        if (!(ok = wait(C_TV, (c + 1) & 1))) break;
+        issue_u(c + 1);
       }
       // W' slot c & 1 for chunk c+2: E(c) and the exchange through the slot
       // finished before EREADY(c)
       if (c + 2 < NC) load_w(c + 2);
+      // Q of chunk c+1 once QS(c) has read it
+      if (!(ok = wait(C_QS, c & 1))) break;
+      if (c + 1 < NC) load_q(c + 1);
       // T/V of chunk c+2 once U'(c+1) has read them
       if (c + 2 < NC) {
         if (!(ok = wait(C_M2, (c + 1) & 1))) break;
         load_tv(c + 2);
       }
-      // Q of chunk c+1 once QS(c) has read it
-      if (!(ok = wait(C_QS, c & 1))) break;
-      if (c + 1 < NC) load_q(c + 1);
-      // K/P of chunk c+1 once dS(c) and PE(c) have read them; dS(c+1) waits on
-      // this very load, so DS cannot run a phase ahead of this wait
-      if (!(ok = wait(C_DS, c & 1) && wait(C_PE, c & 1))) break;
-      if (c + 1 < NC) load_kp(c + 1);
     }
     if (!ok) set_status(DR_ERR_TIMEOUT);
     // drain: this thread's last MMAs and every copy issued, so nothing lands after exit
     if (last_bar) mbar_wait(last_bar, last_par, kWait / 4);
     if (n_tv > 0) mbar_wait(&bars[C_TV], (n_tv - 1) & 1, kWait / 4);
     if (n_q > 0) mbar_wait(&bars[C_Q], (n_q - 1) & 1, kWait / 4);
-    if (n_kp > 0) mbar_wait(&bars[C_KP], (n_kp - 1) & 1, kWait / 4);
     for (int k = (n_w > 2 ? n_w - 2 : 0); k < n_w; ++k)
       mbar_wait(&bars[C_W0 + (k & 1)], (k >> 1) & 1, kWait / 4);
+  } else if (warp == 13 && lane == 0) {
+    // ===================================================================== PE lane
+    // also refills the K and P buffers, so the issue lane never waits on PE or dS
+    int n_pe = 0, n_k = 0, n_p = 0;
+    bool ok = true;
+    auto load_k = [&](int c) {    // the dS operand: K, or the record's write keys
+      mbar_expect_tx(&bars[C_K], kExplicitW ? 32768 : 16384);
+      if (kExplicitW) {
+        bulk_load(sm + cKP, recs + (size_t)c * kRecV + CM::rW_, 32768, &bars[C_K]);
+      } else {
+        tma_load_4d(sm + cKP, &tmK, &bars[C_K], 0, h, c * 64, b);
+        tma_load_4d(sm + cKP + 8192, &tmK, &bars[C_K], 64, h, c * 64, b);
+      }
+      n_k = c + 1;
+    };
+    auto load_p = [&](int c) {
+      mbar_expect_tx(&bars[C_P], 16384);
+      bulk_load(sm + cKP + CM::P, recs + (size_t)c * kRecV + rP, 16384, &bars[C_P]);
+      n_p = c + 1;
+    };
+    load_k(0);
+    load_p(0);
+    for (int c = 0; c < NC; ++c) {
+      // PE(c) = P_hi [E_hi | E_lo] + P_lo E_hi once the E tiles are written and
+      // the output of c-1 has read tPE
+      if (s_abort || !mbar_wait(&bars[C_EREADY], c & 1, kWait) || !mbar_wait(&bars[C_P], c & 1, kWait) ||
+          (c >= 1 && !mbar_wait(&bars[C_OUTDONE], (c - 1) & 1, kWait))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t dp0 = desc_sw128(smem_u32(sm + cKP) + CM::P, 16, 1024);
+      const uint64_t de0 = desc_sw128(smem_u32(sm + cE), 8192, 1024);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint64_t dp = dp0 + ks * (32 >> 4), de = de0 + ks * (2048 >> 4);
+        mma_bf16(tmem + tPE, dp, de, I_Q2, ks > 0);
+        mma_bf16(tmem + tPE, dp + (8192 >> 4), de, I_N64, true);
+      }
+      mma_commit(&bars[C_PE]);
+      n_pe = c + 1;
+      if (c + 1 < NC) {
+        // K of chunk c+1 once dS(c) has read it (dS(c+1) waits on this very
+        // load, so DS cannot run a phase ahead of this wait), P once PE(c) has
+        if (s_abort || !mbar_wait(&bars[C_DS], c & 1, kWait)) {
+          ok = false;
+          break;
+        }
+        load_k(c + 1);
+        if (!mbar_wait(&bars[C_PE], c & 1, kWait)) {
+          ok = false;
+          break;
+        }
+        load_p(c + 1);
+      }
+    }
+    if (!ok && !s_abort) {
+      s_abort = 1;
+      set_status(DR_ERR_TIMEOUT);
+    }
+    if (n_pe > 0) mbar_wait(&bars[C_PE], (n_pe - 1) & 1, kWait / 4);
+    if (n_k > 0) mbar_wait(&bars[C_K], (n_k - 1) & 1, kWait / 4);
+    if (n_p > 0) mbar_wait(&bars[C_P], (n_p - 1) & 1, kWait / 4);
   }
 
-  if (warp == 8) __syncwarp();
+  if (warp == 8 || warp == 13) __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (s_abort && tid == 0) set_status(DR_ERR_TIMEOUT);
