@@ -714,9 +714,9 @@ struct CarryMap {
   static constexpr uint32_t rec = MODE == 0 ? kRec : (MODE == 1 ? kRecP : kRecKdn);
   static constexpr uint32_t rW_ = MODE == 1 ? rW : rWk;        // record dS operand
 };
-constexpr uint32_t tE = 0;                  // M=128 x 128: U' then E, in four quadrants
-constexpr uint32_t tQS = 128;               // M=64 x 128: Q S_hi | Q S_lo
-constexpr uint32_t tPE = 256;               // M=64 x 128: (P_hi + P_lo) E_hi | P_hi E_lo
+constexpr uint32_t tE = 0;                  // 2 slots M=128 x 128: U' then E, in four quadrants
+constexpr uint32_t tO = 256;                // M=64 x 128: Q S_hi | Q S_lo, then (once read)
+                                            //   (P_hi + P_lo) E_hi | P_hi E_lo
 constexpr uint32_t tDS = 384;               // M=128 x 128: K^T uE_hi (+ W_lo^T uE_hi) | K^T uE_lo
 constexpr uint32_t kCarryTmem = 512;
 constexpr uint32_t I_U2 = idesc_bf16(128, 64, 0, 1);         // [T_hi ; T_lo] V
@@ -814,11 +814,12 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       tc_fence_after();
       const uint64_t dsh0 = desc_sw128(smem_u32(sm + cS), 16384, 1024);
       const uint64_t dw0 = desc_sw128(smem_u32(sm + cW + (c & 1) * 32768), 16384, 1024);
-      mma_bf16(tmem + tE, dw0, dsh0, I_E1, true);
-      mma_bf16(tmem + tE + 64, dw0, dsh0 + (16384 >> 4), I_E1, false);
+      const uint32_t acc = tmem + tE + (c & 1) * 128;
+      mma_bf16(acc, dw0, dsh0, I_E1, true);
+      mma_bf16(acc + 64, dw0, dsh0 + (16384 >> 4), I_E1, false);
 #pragma unroll 1
       for (int ks = 1; ks < 8; ++ks)
-        mma_bf16(tmem + tE, dw0 + ks * (2048 >> 4), dsh0 + ks * (2048 >> 4), I_E2, true);
+        mma_bf16(acc, dw0 + ks * (2048 >> 4), dsh0 + ks * (2048 >> 4), I_E2, true);
       mma_commit(&bars[C_E]);
       last_bar = &bars[C_E];
       last_par = c & 1;
@@ -865,7 +866,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       tc_fence_after();
       {
         float* X = reinterpret_cast<float*>(sm + cW + slot * 32768);   // W'(c) is consumed
-        const uint32_t e0 = tmem + lane_off + tE + 32 * hc;
+        const uint32_t e0 = tmem + lane_off + tE + slot * 128 + 32 * hc;
         float kv[16], t16[16];
         {   // the partner's 16 columns: column halves added, handed over in X
           float s16[16];
@@ -995,14 +996,14 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       float qs_nxt = 0.f;
       if (c + 1 < NC) qs_nxt = reinterpret_cast<const float*>(recs + (size_t)(c + 1) * kRecV + rVec)[i];
       const int t0 = c * 64, Cc = min(64, a.T - t0);
-      // e^g qn . Q S first: tQS is released as soon as it is read, so QS(c+1)
-      // need not wait for PE(c) and the stores of chunk c
+      // e^g qn . Q S first; the accumulator is released as soon as it is read,
+      // and PE(c) lands in it next
       float qv[2][16];
       if (!group_wait2(2, 128, &bars[C_QS], c & 1, nullptr, 0)) break;
       tc_fence_after();
 #pragma unroll
       for (int hcol = 0; hcol < 2; ++hcol) {
-        const uint32_t q0 = tmem + lane_off + tQS + 32 * hcol;
+        const uint32_t q0 = tmem + lane_off + tO + 32 * hcol;
         float qa[16], qb[16];
         tmem_ld16(q0 + 16, qa);   // columns 16-31 of the 32: lanes 16-31 take them from lanes 0-15
         tmem_ld16(q0 + 80, qb);
@@ -1024,7 +1025,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
                           (((long)b * a.T + t0 + i) * a.H + h) * a.dv + half * 64;
 #pragma unroll
       for (int hcol = 0; hcol < 2; ++hcol) {
-        const uint32_t p0 = tmem + lane_off + tPE + 32 * hcol;
+        const uint32_t p0 = tmem + lane_off + tO + 32 * hcol;
         float x[16], pa[16], pb[16];
         tmem_ld16(p0 + 16, pa);
         tmem_ld16(p0 + 80, pb);
@@ -1092,14 +1093,14 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       }
       n_q = c + 1;
     };
-    // U'(c) = [T_hi ; T_lo] V into the E accumulator (columns 0-63)
+    // U'(c) = [T_hi ; T_lo] V into E slot c & 1 (columns 0-63)
     auto issue_u = [&](int c) {
       tc_fence_after();
       const uint64_t dt0 = desc_sw128(smem_u32(sm + cT), 16, 1024);
       const uint64_t dv0 = desc_sw128(smem_u32(sm + cV), 8192, 1024);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + tE, dt0 + ks * (32 >> 4), dv0 + ks * (2048 >> 4), I_U2, ks > 0);
+        mma_bf16(tmem + tE + (c & 1) * 128, dt0 + ks * (32 >> 4), dv0 + ks * (2048 >> 4), I_U2, ks > 0);
       mma_commit(&bars[C_M2]);
       last_bar = &bars[C_M2];
       last_par = c & 1;
@@ -1112,15 +1113,15 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
     if (ok) issue_u(0);
     // T/V of chunk 1 once U'(0) has read chunk 0's
     if (ok && NC > 1 && (ok = wait(C_M2, 0))) load_tv(1);
-    // Pipe order per chunk: E(c) [state leader], QS(c) [here, while E(c) is read
-    // out], dS(c) [state leader], U'(c+1) [here] and PE(c) [PE lane] while the
-    // state is updated, E(c+1).  Each refill follows the last read of its buffer
+    // Pipe order per chunk: E(c) [state leader], QS(c) and U'(c+1) [here, while
+    // E(c) is read out], dS(c) [state leader], PE(c) [PE lane] while the state is
+    // updated, E(c+1).  Each refill follows the last read of its buffer
     // and precedes, in this thread's order, the MMA whose completion could start
     // the buffer's next phase, so no waiter can fall two phases behind.
     for (int c = 0; ok && c < NC; ++c) {
-      // QS(c) = Q [S_hi | S_lo]: S(c) tiles ready, tQS read by the output of c-1
+      // QS(c) = Q [S_hi | S_lo]: S(c) tiles ready, PE(c-1) read out of tO
       if (!(ok = wait(C_SREADY, c & 1))) break;
-      if (c >= 1 && !(ok = wait(C_QSFREE, (c - 1) & 1))) break;
+      if (c >= 1 && !(ok = wait(C_OUTDONE, (c - 1) & 1))) break;
       if (!(ok = wait(C_Q, c & 1))) break;
       tc_fence_after();
       {
@@ -1130,22 +1131,23 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
         for (int ks = 0; ks < 8; ++ks) {
           const uint64_t dq = dq0 + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4);
           const uint64_t ds = ds0 + ks * (2048 >> 4);
-          mma_bf16(tmem + tQS, dq, ds, I_Q2, ks > 0);
+          mma_bf16(tmem + tO, dq, ds, I_Q2, ks > 0);
           if (kKdn)   // (Gamma.Q) is a computed operand: its lo term against S_hi
-            mma_bf16(tmem + tQS, dq + (16384 >> 4), ds, I_N64, true);
+            mma_bf16(tmem + tO, dq + (16384 >> 4), ds, I_N64, true);
         }
         mma_commit(&bars[C_QS]);
         last_bar = &bars[C_QS];
         last_par = c & 1;
       }
-      // U'(c+1) once E(c) has been read out of the accumulator (EREADY(c))
-      if (!(ok = wait(C_EREADY, c & 1))) break;
+      // U'(c+1) into the other E slot (E(c-1) was read out of it before
+      // EREADY(c-1)), in the pipe behind QS(c) while E(c) is read out
       if (c + 1 < NC) {
         if (!(ok = wait(C_TV, (c + 1) & 1))) break;
         issue_u(c + 1);
       }
       // W' slot c & 1 for chunk c+2: E(c) and the exchange through the slot
       // finished before EREADY(c)
+      if (!(ok = wait(C_EREADY, c & 1))) break;
       if (c + 2 < NC) load_w(c + 2);
       // Q of chunk c+1 once QS(c) has read it
       if (!(ok = wait(C_QS, c & 1))) break;
@@ -1187,9 +1189,9 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
     load_p(0);
     for (int c = 0; c < NC; ++c) {
       // PE(c) = P_hi [E_hi | E_lo] + P_lo E_hi once the E tiles are written and
-      // the output of c-1 has read tPE
+      // the output warps have read QS(c) out of tO
       if (s_abort || !mbar_wait(&bars[C_EREADY], c & 1, kWait) || !mbar_wait(&bars[C_P], c & 1, kWait) ||
-          (c >= 1 && !mbar_wait(&bars[C_OUTDONE], (c - 1) & 1, kWait))) {
+          !mbar_wait(&bars[C_QSFREE], c & 1, kWait)) {
         ok = false;
         break;
       }
@@ -1199,8 +1201,8 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         const uint64_t dp = dp0 + ks * (32 >> 4), de = de0 + ks * (2048 >> 4);
-        mma_bf16(tmem + tPE, dp, de, I_Q2, ks > 0);
-        mma_bf16(tmem + tPE, dp + (8192 >> 4), de, I_N64, true);
+        mma_bf16(tmem + tO, dp, de, I_Q2, ks > 0);
+        mma_bf16(tmem + tO, dp + (8192 >> 4), de, I_N64, true);
       }
       mma_commit(&bars[C_PE]);
       n_pe = c + 1;
