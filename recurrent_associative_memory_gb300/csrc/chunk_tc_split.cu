@@ -63,11 +63,11 @@ constexpr uint32_t pT = 65536;              // T hi | T lo | Ts hi | Ts lo (L/T 
 constexpr uint32_t pVec = pT + 32768;       // vectors, 4 KB
 constexpr uint32_t kPrepSmem = pVec + 4096 + 1024;
 constexpr uint32_t tG0 = 0;                 // 2 Gram slots, M=128 x 64
-constexpr uint32_t tPWt = 128;              // W'^T = K^T Ts^T, M=128 x 64
+constexpr uint32_t tPWt = 128;              // W'^T = K^T [Ts_hi ; Ts_lo]^T, M=128 x 128 (halves added)
 constexpr uint32_t kPrepTmem = 256;
 
 constexpr uint32_t I_GRAM = idesc_bf16(128, 64, 0, 0);
-constexpr uint32_t I_WT = idesc_bf16(128, 64, 1, 0);     // A = K (MN-major), B = Ts (K-major)
+constexpr uint32_t I_WT = idesc_bf16(128, 128, 1, 0);    // A = K (MN-major), B = [Ts_hi ; Ts_lo] (K-major)
 constexpr uint32_t I_N64 = idesc_bf16(64, 64, 0, 1);
 constexpr uint32_t I_DS = idesc_bf16(128, 64, 1, 1);
 // N = 128 over a [hi | lo] pair of B tiles one 64-column group apart: one MMA
@@ -75,7 +75,7 @@ constexpr uint32_t I_DS = idesc_bf16(128, 64, 1, 1);
 // columns [0, 64) and [64, 128) and are added on readout)
 constexpr uint32_t I_DS2 = idesc_bf16(128, 128, 1, 1);
 
-enum { P_KQ0, P_KQ1, P_G0, P_G1, P_W, P_GFREE0, P_GFREE1, P_TREADY, P_WFREE, P_WREADY, P_COUNT };
+enum { P_KQ0, P_KQ1, P_G0, P_G1, P_W, P_GFREE0, P_GFREE1, P_TREADY, P_WFREE, P_WREADY, P_PREAD, P_COUNT };
 
 __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -439,20 +439,30 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       if (leader) {
         bulk_store(rec + rT, sm + pT, 16384);
         bulk_commit();
-        bulk_wait_read<1>();   // P has left the K/Q stage, which W'(k) then frees for a reload
         mbar_arrive(&bars[P_TREADY]);
       }
       // ---- W'^T readout (row = dk index = TMEM lane, 32 tokens per thread), staged
-      //      over T / Ts (both read by now), then one bulk copy into the record
+      //      over T / Ts (both read by now), then one bulk copy into the record.  The
+      //      P copy has left the K/Q stage too, so the stage may be reloaded (PREAD).
       if (leader) bulk_wait_read<0>();
       if (!group_wait(&bars[P_W], k & 1)) break;
+      if (leader) mbar_arrive(&bars[P_PREAD]);
       tc_fence_after();
       {
         const int r = quad * 32 + lane;
         uint8_t* Wg = sm + pT;
         float w[32];
-        ld32cols(tmem + lane_off + tPWt + pchalf * 32, w);
-        tmem_ld_wait();
+        {
+          float t16[16], u16[16];
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            tmem_ld16(tmem + lane_off + tPWt + pchalf * 32 + 16 * part, t16);
+            tmem_ld16(tmem + lane_off + tPWt + 64 + pchalf * 32 + 16 * part, u16);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w[16 * part + e] = t16[e] + u16[e];
+          }
+        }
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
           float x[8];
@@ -539,17 +549,19 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       {
         const uint32_t tb = smem_u32(sm + pT), kq = smem_u32(sm + pKQ + st * 32768);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t dts = desc_sw128(tb + 16384 + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024);
-          const uint64_t dk = desc_sw128(kq + (ks & 3) * 2048, 16384, 1024);
+        for (int ks = 0; ks < 4; ++ks) {   // B = [Ts_hi ; Ts_lo] stacked along N
+          const uint64_t dts = desc_sw128(tb + 16384 + ks * 32, 16, 1024);
+          const uint64_t dk = desc_sw128(kq + ks * 2048, 16384, 1024);
           mma_bf16(tmem + tPWt, dk, dts, I_WT, ks > 0);
         }
         mma_commit(&bars[P_W]);
         w_done = k + 1;
       }
-      // stage st is free once W'(k) (its last reader) is done
+      // stage st is free once W'(k) (its last MMA reader) is done and the P copy
+      // out of its Q half has been read (PREAD(k), arrived after the prep warps
+      // have seen W'(k) complete, so it cannot run a phase ahead of this wait)
       if (k + 2 < nmine) {
-        if (!(ok = wait(P_W, k & 1))) break;
+        if (!(ok = wait(P_W, k & 1) && wait(P_PREAD, k & 1))) break;
         issue_kq(k + 2);
       }
     }
