@@ -681,7 +681,8 @@ __global__ void __launch_bounds__(128) pgdn_scan_kernel(FwdArgs a, uint8_t* __re
 //   PE     warp 13     the off-path MMA PE = P E (a second issuing thread: one
 //                      thread issues about one MMA per 60-70 cycles, so U' and
 //                      PE, both due while the state is updated, come from two),
-//                      and the K and P copies, which wait on dS and PE.
+//                      and the P copies, which wait on PE (the state leader
+//                      refills K the moment dS has read it).
 //   output warps 9-12  o = e^g qn . QS + PE for every row of the chunk.
 // MMA shapes.  One issuing thread sustains about one tcgen05.mma per 55-65
 // cycles, and the tensor pipe takes an M=128 x N=128 step in about 1.7x the
@@ -805,6 +806,18 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
     float S[32];
     uint64_t* last_bar = nullptr;               // leader: its last MMA commit
     uint32_t last_par = 0;
+    int n_k = 0;                                // leader: K copies issued
+    auto load_k = [&](int c) {    // the dS operand: K, or the record's write keys
+      mbar_expect_tx(&bars[C_K], kExplicitW ? 32768 : 16384);
+      if (kExplicitW) {
+        bulk_load(sm + cKP, recs + (size_t)c * kRecV + CM::rW_, 32768, &bars[C_K]);
+      } else {
+        tma_load_4d(sm + cKP, &tmK, &bars[C_K], 0, h, c * 64, b);
+        tma_load_4d(sm + cKP + 8192, &tmK, &bars[C_K], 64, h, c * 64, b);
+      }
+      n_k = c + 1;
+    };
+    if (leader) load_k(0);
     auto store_state_tiles = [&]() {
       uint8_t* sS = sm + cS;
 #pragma unroll
@@ -880,21 +893,21 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
         float* X = reinterpret_cast<float*>(sm + cW + slot * 32768);   // W'(c) is consumed
         const uint32_t e0 = tmem + lane_off + tE + slot * 128 + 32 * hc;
         float kv[16], t16[16];
-        {   // the partner's 16 columns: column halves added, handed over in X
-          float s16[16];
+        {   // all four loads in flight, one wait; the partner's 16 columns (column
+            // halves added) are handed over in X
+          float s16[16], u16[16];
           tmem_ld16(e0 + 16 * send, s16);
-          tmem_ld16(e0 + 64 + 16 * send, t16);
+          tmem_ld16(e0 + 64 + 16 * send, u16);
+          tmem_ld16(e0 + 16 * keep, kv);
+          tmem_ld16(e0 + 64 + 16 * keep, t16);
           tmem_ld_wait();
           float* xr = X + erow * kXs + 32 * hc + 16 * send;
 #pragma unroll
           for (int e = 0; e < 16; e += 4)
             *reinterpret_cast<float4*>(xr + e) =
-                make_float4(s16[e] + t16[e], s16[e + 1] + t16[e + 1], s16[e + 2] + t16[e + 2],
-                            s16[e + 3] + t16[e + 3]);
+                make_float4(s16[e] + u16[e], s16[e + 1] + u16[e + 1], s16[e + 2] + u16[e + 2],
+                            s16[e + 3] + u16[e + 3]);
         }
-        tmem_ld16(e0 + 16 * keep, kv);
-        tmem_ld16(e0 + 64 + 16 * keep, t16);
-        tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 16; ++e) kv[e] += t16[e];
         named_bar(1, 256);
@@ -927,12 +940,17 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
           }
         }
       }
+      // the leader takes the waits for dS(c)'s and E(c+1)'s other operands off the
+      // chain: K(c) before the E-tile barrier, U'(c+1) and W'(c+1) during dS(c)
+      bool k_ok = true;
+      if (leader) k_ok = !s_abort && mbar_wait(&bars[C_K], c & 1, kWait);
       tc_fence_before();
       fence_proxy_async();
       named_bar(1, 256);
       // ---- leader: dS(c) = K^T [uE_hi | uE_lo]
+      bool e_ok = true;
       if (leader) {
-        if (!s_abort && mbar_wait(&bars[C_K], c & 1, kWait)) {
+        if (k_ok && !s_abort) {
           tc_fence_after();
           const uint32_t kb = smem_u32(sm + cKP), eb = smem_u32(sm + cE);
           const uint32_t ub = kKdn ? eb : eb + 16384;   // u.E (KDN: u = 1, the E tiles)
@@ -947,23 +965,30 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
           last_bar = &bars[C_DS];
           last_par = c & 1;
           mbar_arrive(&bars[C_EREADY]);
+          if (c + 1 < NC)
+            e_ok = mbar_wait(&bars[C_M2], (c + 1) & 1, kWait) &&
+                   mbar_wait(&bars[C_W0 + ((c + 1) & 1)], ((c + 1) >> 1) & 1, kWait);
         } else {
           s_abort = 1;
         }
       }
-      // ---- S <- gamma_C S + dS (QS(c) must be done reading the old S tiles)
+      // ---- S <- gamma_C S + dS (QS(c) must be done reading the old S tiles); the
+      // leader refills K for dS(c+1) the moment dS(c) has read it
       if (!(ok = group_wait2(1, 256, &bars[C_DS], c & 1, &bars[C_QS], c & 1))) break;
+      if (leader && c + 1 < NC) load_k(c + 1);
       tc_fence_after();
       {
-        float t16[16], l16[16];
+        float t16[16], l16[16], t16b[16], l16b[16];
         const uint32_t dcol0 = tmem + lane_off + tDS + 32 * hc;
+        tmem_ld16(dcol0, t16);   // all four loads in flight, one wait
+        tmem_ld16(dcol0 + 64, l16);
+        tmem_ld16(dcol0 + 16, t16b);
+        tmem_ld16(dcol0 + 80, l16b);
+        tmem_ld_wait();
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          tmem_ld16(dcol0 + 16 * part, t16);
-          tmem_ld16(dcol0 + 64 + 16 * part, l16);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 16; ++e) S[16 * part + e] = g_cur * S[16 * part + e] + (t16[e] + l16[e]);
+        for (int e = 0; e < 16; ++e) {
+          S[e] = g_cur * S[e] + (t16[e] + l16[e]);
+          S[16 + e] = g_cur * S[16 + e] + (t16b[e] + l16b[e]);
         }
         store_state_tiles();
       }
@@ -973,8 +998,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       // ---- leader: E(c+1) once S(c+1), U'(c+1) and W'(c+1) are in place
       if (leader) {
         if (c + 1 < NC) {
-          if (!s_abort && mbar_wait(&bars[C_M2], (c + 1) & 1, kWait) &&
-              mbar_wait(&bars[C_W0 + ((c + 1) & 1)], ((c + 1) >> 1) & 1, kWait))
+          if (!s_abort && e_ok)
             issue_e(c + 1);
           else
             s_abort = 1;
@@ -984,8 +1008,10 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       u_cur = u_nxt;
       g_cur = g_nxt;
     }
-    // the leader's MMAs complete before TMEM is freed (its commits track all of them)
+    // the leader's MMAs complete before TMEM is freed (its commits track all of them),
+    // and its K copies land before the CTA exits
     if (leader && last_bar) mbar_wait(last_bar, last_par, kWait / 4);
+    if (leader && n_k > 0) mbar_wait(&bars[C_K], (n_k - 1) & 1, kWait / 4);
     if (!s_abort && a.S) {
       const long base = ((long)bh * 128 + srow) * a.dv + half * 64 + 32 * hc;
 #pragma unroll
@@ -1179,25 +1205,14 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       mbar_wait(&bars[C_W0 + (k & 1)], (k >> 1) & 1, kWait / 4);
   } else if (warp == 13 && lane == 0) {
     // ===================================================================== PE lane
-    // also refills the K and P buffers, so the issue lane never waits on PE or dS
-    int n_pe = 0, n_k = 0, n_p = 0;
+    // also refills the P buffer, so the issue lane never waits on PE
+    int n_pe = 0, n_p = 0;
     bool ok = true;
-    auto load_k = [&](int c) {    // the dS operand: K, or the record's write keys
-      mbar_expect_tx(&bars[C_K], kExplicitW ? 32768 : 16384);
-      if (kExplicitW) {
-        bulk_load(sm + cKP, recs + (size_t)c * kRecV + CM::rW_, 32768, &bars[C_K]);
-      } else {
-        tma_load_4d(sm + cKP, &tmK, &bars[C_K], 0, h, c * 64, b);
-        tma_load_4d(sm + cKP + 8192, &tmK, &bars[C_K], 64, h, c * 64, b);
-      }
-      n_k = c + 1;
-    };
     auto load_p = [&](int c) {
       mbar_expect_tx(&bars[C_P], 16384);
       bulk_load(sm + cKP + CM::P, recs + (size_t)c * kRecV + rP, 16384, &bars[C_P]);
       n_p = c + 1;
     };
-    load_k(0);
     load_p(0);
     for (int c = 0; c < NC; ++c) {
       // PE(c) = P_hi [E_hi | E_lo] + P_lo E_hi once the E tiles are written and
@@ -1219,14 +1234,8 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       mma_commit(&bars[C_PE]);
       n_pe = c + 1;
       if (c + 1 < NC) {
-        // K of chunk c+1 once dS(c) has read it (dS(c+1) waits on this very
-        // load, so DS cannot run a phase ahead of this wait), P once PE(c) has
-        if (s_abort || !mbar_wait(&bars[C_DS], c & 1, kWait)) {
-          ok = false;
-          break;
-        }
-        load_k(c + 1);
-        if (!mbar_wait(&bars[C_PE], c & 1, kWait)) {
+        // P of chunk c+1 once PE(c) has read it
+        if (s_abort || !mbar_wait(&bars[C_PE], c & 1, kWait)) {
           ok = false;
           break;
         }
@@ -1238,7 +1247,6 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       set_status(DR_ERR_TIMEOUT);
     }
     if (n_pe > 0) mbar_wait(&bars[C_PE], (n_pe - 1) & 1, kWait / 4);
-    if (n_k > 0) mbar_wait(&bars[C_K], (n_k - 1) & 1, kWait / 4);
     if (n_p > 0) mbar_wait(&bars[C_P], (n_p - 1) & 1, kWait / 4);
   }
 
