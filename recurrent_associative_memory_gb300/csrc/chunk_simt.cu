@@ -217,6 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         sb3[i] = real ? a.betaP[ti] : 0.f;
       }
     }
+    if constexpr (PREP && sizeof(Tin) == 2) {
+      if (tid == 0) umma::bulk_wait_read<0>();   // the previous task's record copies
+    }
     __syncthreads();
 
     // ---- 2. loads of K, Q with fused L2 norms; thread (row i, sub) holds channels
@@ -317,14 +320,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         const int c = tid;
         float n = carry, d = 1.f, g = 0.f;
         for (int i0 = 0; i0 < CM; i0 += 8) {
+          const float4 k0 = *reinterpret_cast<const float4*>(sKt + c * CS + i0);
+          const float4 k1 = *reinterpret_cast<const float4*>(sKt + c * CS + i0 + 4);
+          const float kvs[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int i = i0 + e;
             const float la = sX[i * DK + c];
             const float al = expf(la);
             const float a2 = al * al;
-            const float kv = sKt[c * CS + i];
-            const float u = sb2[i] * kv * kv;
+            const float kk = kvs[e] * kvs[e];
+            const float u = sb2[i] * kk;
             const float n1 = a2 * n + sW[i * DK + c] * d;
             sW[i * DK + c] = __fdividef(n1, d);     // p^_i
             d = d + u * n1;
@@ -340,8 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         carry = n / d;
       }
       __syncthreads();
-      for (int i = warp; i < CM; i += kThreads / 32) {
+      for (int i = warp; i < CM; i += kThreads / 32) {   // z_i = sum_c p^_ic k_ic^2
         float z = 0.f;
+#pragma unroll 4
         for (int c = lane; c < DK; c += 32) {
           const float kv = sKt[c * CS + i];
           z += sW[i * DK + c] * kv * kv;
@@ -350,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         if (lane == 0) sz[i] = 1.f / (sb1[i] + z);   // gain denominator, inverted once per row
       }
       __syncthreads();
+#pragma unroll 4
       for (int e = tid; e < CM * DK; e += kThreads) {
         const int i = e / DK, c = e % DK;
         const float w = sW[e] * sKt[c * CS + i] * sz[i];
@@ -372,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       if (tid < DK) sgC[tid] = expf(sX[(CM - 1) * DK + tid]);
       // scale K, Q to their sub-chunk's previous boundary and W^T to its own end;
       // the row-major W becomes exp(g_C - g_j) . w_j for the state update
+#pragma unroll 4
       for (int e = tid; e < CM * DK; e += kThreads) {
         const int i = e / DK, c = e % DK, I = i >> 4;
         const float gi = sX[e];
@@ -442,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
 
     // ---- 5. operands of the carry: Gamma.K, Gamma.Q, exp(g_C - g_j).W, gamma_C
     if (kdn) {
+#pragma unroll 4
       for (int e = tid; e < CM * DK; e += kThreads) {
         const int i = e / DK, c = e % DK;
         const float gb = fGb[(i >> 4) * DK + c];
@@ -450,6 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       }
     } else {
       const float gC = sg[CM - 1];
+#pragma unroll 4
       for (int e = tid; e < CM * DK; e += kThreads) {
         const int i = e / DK, c = e % DK;
         const float gi = expf(sg[i]);
@@ -517,62 +528,106 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
     }
     __syncthreads();
     if constexpr (PREP && sizeof(Tin) == 2) {   // tile images for the tensor-core carry
+      // Each image is built in shared memory regions this task no longer needs and
+      // leaves with one bulk copy (thread 0): T and P over the L/T buffer, then
+      // W'^T there too, (Gamma.Q) over (Gamma.K)^T and Wbar over T^T.
       for (int e = tid; e < CM * CM; e += kThreads) {   // T^T, zero above the diagonal of T
         const int i = e >> 6, j = e & 63;
         sTt[j * CS + i] = (j <= i) ? sLT[i * LDL + j] : 0.f;
       }
       __syncthreads();
-      auto put = [&](uint32_t base, int row, int col, const float (&x)[8], uint32_t lo_off) {
+      uint8_t* stX = reinterpret_cast<uint8_t*>(sX);
+      auto put = [&](uint8_t* base, int row, int col, const float (&x)[8], uint32_t lo_off) {
         uint4 hi, lo;
         tc::split8(x, hi, lo);
         const uint32_t off = umma::sw128_offset(row, col);
-        *reinterpret_cast<uint4*>(rec + base + off) = hi;
-        *reinterpret_cast<uint4*>(rec + base + lo_off + off) = lo;
+        *reinterpret_cast<uint4*>(base + off) = hi;
+        *reinterpret_cast<uint4*>(base + lo_off + off) = lo;
       };
+      // T and P [64 i][64 j] from token-minor buffers: lanes take consecutive tokens
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {   // T and P: [64 i][64 j]
-        const int e = tid + r * kThreads, i = e >> 3, g = e & 7;
+      for (int r = 0; r < 2; ++r) {
+        const int e = tid + r * kThreads, i = e & 63, g = e >> 6;
         float xt[8], xp[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           xt[q] = sTt[(8 * g + q) * CS + i];
           xp[q] = sPt[(8 * g + q) * CS + i];
         }
-        put(rbT, i, 8 * g, xt, 8192);
-        put(rbP, i, 8 * g, xp, 8192);
+        put(stX, i, 8 * g, xt, 8192);
+        put(stX + 16384, i, 8 * g, xp, 8192);
       }
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {   // (Gamma.Q) and Wbar: [64 tok][128] as two 64-column blocks
-        const int e = tid + r * kThreads, i = e >> 4, g = e & 15, kb = g >> 3, cg = g & 7;
-        float xq[8], xw[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          xq[q] = sQt[(8 * g + q) * CS + i];
-          xw[q] = sW[i * DK + 8 * g + q];
-        }
-        put(rbQ + kb * 8192, i, 8 * cg, xq, 16384);
-        put(rbW + kb * 8192, i, 8 * cg, xw, 16384);
+      umma::fence_proxy_async();
+      __syncthreads();
+      if (tid == 0) {
+        umma::bulk_store(rec + rbT, stX, 16384);
+        umma::bulk_store(rec + rbP, stX + 16384, 16384);
+        umma::bulk_commit();
       }
-      {   // W'^T [c][i] = sum_{j <= i} (Gamma.K)^T[c][j] T[i][j]: 4 rows x 8 tokens per thread
-        const int c0 = (tid >> 3) * 4, i0 = (tid & 7) * 8;
-        float w[4][8];
+      // W'^T [c][i] = sum_{j <= i} (Gamma.K)^T[c][j] T[i][j].  Tokens in 16 blocks of 4;
+      // warp w takes blocks w and 15 - w, so every warp runs 17 steps of 4 j (T is
+      // lower triangular); lane l takes rows l + 32x.  (Gamma.K)^T is read 4 j at a
+      // time (16-byte loads, conflict-free across lanes), T^T rows are broadcast.
+      float w[2][4][4];
+#pragma unroll
+      for (int bsel = 0; bsel < 2; ++bsel) {
+        const int i0 = 4 * (bsel == 0 ? warp : 15 - warp);
 #pragma unroll
         for (int x = 0; x < 4; ++x)
 #pragma unroll
-          for (int y = 0; y < 8; ++y) w[x][y] = 0.f;
-        for (int j = 0; j < i0 + 8; ++j) {
-          const float4 t0 = *reinterpret_cast<const float4*>(sTt + j * CS + i0);
-          const float4 t1 = *reinterpret_cast<const float4*>(sTt + j * CS + i0 + 4);
-          const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+          for (int y = 0; y < 4; ++y) w[bsel][x][y] = 0.f;
+        for (int j = 0; j < i0 + 4; j += 4) {
+          float4 kv[4];
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const float kv = sKt[(c0 + x) * CS + j];
+          for (int x = 0; x < 4; ++x)
+            kv[x] = *reinterpret_cast<const float4*>(sKt + (lane + 32 * x) * CS + j);
 #pragma unroll
-            for (int y = 0; y < 8; ++y) w[x][y] += kv * tv[y];
+          for (int jj = 0; jj < 4; ++jj) {
+            const float4 t4 = *reinterpret_cast<const float4*>(sTt + (j + jj) * CS + i0);
+            const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const float k = jj == 0 ? kv[x].x : (jj == 1 ? kv[x].y : (jj == 2 ? kv[x].z : kv[x].w));
+#pragma unroll
+              for (int y = 0; y < 4; ++y) w[bsel][x][y] += k * tv[y];
+            }
           }
         }
+      }
+      if (tid == 0) umma::bulk_wait_read<0>();   // T, P have left the L/T buffer
+      __syncthreads();                           // (Gamma.K)^T and T^T are read too
+      uint8_t* stK = reinterpret_cast<uint8_t*>(sKt);
+      uint8_t* stT = reinterpret_cast<uint8_t*>(sTt);
 #pragma unroll
-        for (int x = 0; x < 4; ++x) put(rbWp, c0 + x, i0, w[x], 16384);
+      for (int bsel = 0; bsel < 2; ++bsel) {   // 4 tokens = half of a 16-byte chunk
+        const int i0 = 4 * (bsel == 0 ? warp : 15 - warp);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const float* v = w[bsel][x];
+          const uint32_t h0 = tc::pack_bf16(v[0], v[1]), h1 = tc::pack_bf16(v[2], v[3]);
+          const uint32_t l0 = tc::pack_bf16(v[0] - __uint_as_float(h0 << 16), v[1] - __uint_as_float(h0 & 0xFFFF0000u));
+          const uint32_t l1 = tc::pack_bf16(v[2] - __uint_as_float(h1 << 16), v[3] - __uint_as_float(h1 & 0xFFFF0000u));
+          const uint32_t off = umma::sw128_offset(lane + 32 * x, i0);
+          *reinterpret_cast<uint2*>(stX + off) = make_uint2(h0, h1);
+          *reinterpret_cast<uint2*>(stX + 16384 + off) = make_uint2(l0, l1);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {   // (Gamma.Q) and Wbar: [64 tok][128] as two 64-column blocks
+        {
+          const int e = tid + r * kThreads, i = e & 63, g = e >> 6, kb = g >> 3, cg = g & 7;
+          float xq[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) xq[q] = sQt[(8 * g + q) * CS + i];
+          put(stK + kb * 8192, i, 8 * cg, xq, 16384);
+        }
+        {   // Wbar is token-major: lanes take consecutive 8-channel groups of one row
+          const int e = tid + r * kThreads, i = e >> 4, g = e & 15, kb = g >> 3, cg = g & 7;
+          const float4 w0 = *reinterpret_cast<const float4*>(sW + i * DK + 8 * g);
+          const float4 w1 = *reinterpret_cast<const float4*>(sW + i * DK + 8 * g + 4);
+          const float xw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          put(stT + kb * 8192, i, 8 * cg, xw, 16384);
+        }
       }
       if (tid < CM) {
         float* rv = reinterpret_cast<float*>(rec + rbVec);
@@ -580,6 +635,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         rv[64 + tid] = 1.f;     // u: folded into Wbar
         rv[128 + tid] = sgC[tid];
         rv[192 + tid] = sgC[64 + tid];
+      }
+      umma::fence_proxy_async();
+      __syncthreads();
+      if (tid == 0) {
+        umma::bulk_store(rec + rbWp, stX, 32768);
+        umma::bulk_commit();
+        umma::bulk_store(rec + rbQ, stK, 32768);
+        umma::bulk_store(rec + rbW, stT, 32768);
+        umma::bulk_commit();
+        // the next task's gate copies overwrite the L/T buffer at once; the two
+        // token-minor buffers only at its key loads (waited there)
+        umma::bulk_wait_read<1>();
       }
       continue;
     }
@@ -724,6 +791,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
   __syncthreads();
 
   // final state and aux
+  if constexpr (PREP && sizeof(Tin) == 2) {
+    if (tid == 0) umma::bulk_wait_all();   // every record byte is in global memory before exit
+  }
   if (PREP) return;
   if (a.S) {
     for (int e = tid; e < DK * NV; e += kThreads) {
