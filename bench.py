@@ -228,6 +228,10 @@ def oracle_sample(name, n_heads, pool=None):
 
 # ---------------------------------------------------------------- distributed helpers
 
+# One process per GPU; the ranks run independent replicas (the forward shards over
+# (b, h) with no exchange), so the only collectives are the timing barrier and the
+# max of the ranks' times.  NCCL on GPUs; gloo when no GPU is present (CPU tests).
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -235,8 +239,11 @@ def dist_setup(args):
     if world > 1:
         import torch.distributed as dist
         import torch
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
     return world, rank, local
 
 
@@ -251,9 +258,16 @@ def max_over_ranks(x, world):
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tokens_per_s(world, steps, n_variants, B, T, seconds):
+    """Whole-job throughput: every rank runs the same workload, so the job moves
+    world x steps x variants x B x T tokens in the slowest rank's time."""
+    return world * steps * n_variants * B * T / seconds
 
 
 # ---------------------------------------------------------------- reference arm
@@ -371,8 +385,7 @@ def main():
                                     wl.dv, wl.chunk)
         return 2 if (path == "tc_split" and ws is not None) else 1
     launches = args.steps * sum(kernels_per_call(v) for v in variants)
-    tokens = world * args.steps * len(variants) * wl.B * wl.T
-    value = tokens / total_s
+    value = job_tokens_per_s(world, args.steps, len(variants), wl.B, wl.T, total_s)
 
     var_stats = {}
     for v in variants:
