@@ -15,8 +15,12 @@ The same JSON line carries:
                 measured HBM peak in MEASURED_PEAKS.json;
   decode        dr_decode_step at batch 256, H=16, d=128 (KLA): HBM GB/s of the
                 algorithmic bytes (state read + write, q/k/v/o, gates);
-  e2e           the same forward metric with pinned host buffers: H2D of the
-                step's inputs, both forwards, D2H of both outputs, all timed;
+  e2e           the same forward metric with pinned host buffers: every step
+                copies its inputs H2D, runs both forwards and copies both
+                outputs D2H, all inside the timed region; the copies run on
+                their own streams into double-buffered device tensors, so step
+                i+1's inputs arrive and step i-1's outputs leave while step i
+                computes;
   cpu_baseline  the fp64 oracle (numpy, tokenwise) on a bounded sample of the
                 workload (one batch row, all heads), on the host cores;
   clocks        nvidia-smi SM clocks and throttle reasons sampled during the
@@ -455,30 +459,52 @@ def main():
                    for v in variants for k in keys if k not in ("q", "k", "v"))
         d2h = sum(hout[v].numel() * hout[v].element_size() for v in variants)
 
-        def e2e_step():
-            for k in ("q", "k", "v"):
-                dev[variants[0]][k].copy_(hpin[variants[0]][k], non_blocking=True)
-            for v in variants:
-                for k in keys:
-                    if k not in ("q", "k", "v"):
-                        dev[v][k].copy_(hpin[v][k], non_blocking=True)
-                d = dict(dev[v])
-                for k in ("q", "k", "v"):
-                    d[k] = dev[variants[0]][k]
-                runner.chunk_fwd(d, out=outs[v], final_state=finals[v], aux_final=auxf[v],
-                                 stream=stream, workspace=ws)
-                hout[v].copy_(outs[v], non_blocking=True)
+        # two device buffer sets: set i & 1 takes step i's inputs and outputs
+        sets = [dev, {v: {k: (t.clone() if torch.is_tensor(t) else t) for k, t in dev[v].items()}
+                      for v in variants}]
+        osets = [outs, {v: torch.empty_like(outs[v]) for v in variants}]
+        h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+        ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("h2d", "fwd", "d2h")}
 
-        for _ in range(3):
-            e2e_step()
+        def e2e_step(i):
+            s_ = i & 1
+            d_in = sets[s_]
+            with torch.cuda.stream(h2d_s):
+                if i >= 2:
+                    h2d_s.wait_event(ev["fwd"][s_])     # step i-2 has read set s_
+                for k in ("q", "k", "v"):
+                    d_in[variants[0]][k].copy_(hpin[variants[0]][k], non_blocking=True)
+                for v in variants:
+                    for k in keys:
+                        if k not in ("q", "k", "v"):
+                            d_in[v][k].copy_(hpin[v][k], non_blocking=True)
+                ev["h2d"][s_].record(h2d_s)
+            stream.wait_event(ev["h2d"][s_])
+            if i >= 2:
+                stream.wait_event(ev["d2h"][s_])        # step i-2's outputs have left set s_
+            for v in variants:
+                d = dict(d_in[v])
+                for k in ("q", "k", "v"):
+                    d[k] = d_in[variants[0]][k]
+                runner.chunk_fwd(d, out=osets[s_][v], final_state=finals[v], aux_final=auxf[v],
+                                 stream=stream, workspace=ws)
+            ev["fwd"][s_].record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(ev["fwd"][s_])
+                for v in variants:
+                    hout[v].copy_(osets[s_][v], non_blocking=True)
+                ev["d2h"][s_].record(d2h_s)
+
+        for i in range(3):
+            e2e_step(i)
         torch.cuda.synchronize()
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         n = max(5, min(args.steps, 20))
-        e0.record(stream)
-        for _ in range(n):
-            e2e_step()
-        e1.record(stream)
+        e0.record(h2d_s)
+        for i in range(n):
+            e2e_step(i)
+        e1.record(d2h_s)                                # after the last step's D2H
         torch.cuda.synchronize()
         sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
         result["e2e"] = {"value": world * n * len(variants) * wl.B * wl.T / sec, "unit": "tokens/s",
