@@ -1,0 +1,63 @@
+"""Host-side pieces of the benchmark, on CPU: the algorithmic byte counts the
+roofline divides by (per head-token: q, k, v, o and the gates; plus the final
+state), the decode step's bytes, and the rule that a recorded DRAM traffic
+figure is only used for the kernel source it was captured on."""
+
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from recurrent_associative_memory_gb300 import workloads as W  # noqa: E402
+
+
+@pytest.mark.parametrize("variant,per_head_token", [("gdn", 1032), ("kla", 1032),
+                                                     ("pgdn", 1040), ("kdn", 2052)])
+def test_forward_bytes_per_head_token(variant, per_head_token):
+    name = {"gdn": "gdn_kla_bf16", "kla": "gdn_kla_bf16", "pgdn": "pgdn_bf16",
+            "kdn": "kdn_bf16"}[variant]
+    wl = W.WORKLOADS[name]
+    ht = wl.B * wl.T * wl.H
+    extra = wl.H * 4 if variant == "pgdn" else 0     # PGDN's per-head mu
+    assert bench.fwd_bytes(wl, variant, with_final=False) == ht * per_head_token + extra
+
+
+def test_bench_workload_bytes():
+    wl = W.WORKLOADS["gdn_kla_bf16"]
+    state = wl.B * wl.H * wl.dk * wl.dv * 4
+    assert bench.fwd_bytes(wl, "kla") == 8 * 2048 * 8 * 1032 + state == 139_460_608
+
+
+def test_decode_step_bytes():
+    wl = W.WORKLOADS["kla_decode_bf16"]
+    # per (b, h): fp32 state read + write, q, k, v, o in bf16, two fp32 gates
+    per_bh = 2 * 128 * 128 * 4 + 4 * 128 * 2 + 8
+    assert bench.decode_bytes(wl) == wl.B * wl.H * per_bh == 541_097_984
+
+
+def test_recorded_traffic_is_tied_to_the_kernel_source(tmp_path, monkeypatch):
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)["chunk_tc_split"]
+    fake_root = tmp_path
+    os.makedirs(fake_root / "profiles")
+    stale = dict(rec, source_sha256="0" * 64)
+    (fake_root / "profiles" / "traffic.json").write_text(json.dumps({"chunk_tc_split": stale}))
+    monkeypatch.setattr(bench, "ROOT", str(fake_root))
+    monkeypatch.setattr(bench, "source_hash", lambda kernel: "f" * 64)
+    assert bench.measured_traffic("chunk_tc_split", rec["workload"], "kla") is None
+    fresh = dict(rec, source_sha256="f" * 64)
+    (fake_root / "profiles" / "traffic.json").write_text(json.dumps({"chunk_tc_split": fresh}))
+    assert bench.measured_traffic("chunk_tc_split", rec["workload"], "kla") == rec["dram_bytes_per_launch"]
+    assert bench.measured_traffic("chunk_tc_split", "pgdn_bf16", "pgdn") is None   # other workload
+
+
+def test_default_arguments_are_one_gpu_and_short(monkeypatch):
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    args = bench.parse()
+    assert args.gpus == 1 and args.impl == "ours" and args.workload == "gdn_kla_bf16"
+    assert args.warmup >= 3 and 1 <= args.steps <= 200
