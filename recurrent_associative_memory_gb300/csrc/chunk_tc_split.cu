@@ -1,5 +1,7 @@
-// chunk_tc_split.cu — two-phase tcgen05 chunkwise forward for GDN and KLA
-// (scalar decay, w = coefficient x raw key), bf16 q/k/v/out, dk = dv = 128, chunk 64.
+// chunk_tc_split.cu — two-phase tcgen05 chunkwise forward: GDN and KLA (scalar
+// decay, w = coefficient x raw key) and PGDN (explicit write keys), bf16
+// q/k/v/out, dk = dv = 128, chunk 64; the carry also runs over Diagonal KDN
+// records written by the CUDA-core prep of chunk_simt.cu.
 //
 // The chunk algebra is that of chunk_tc_ws.cu (KLA notes section 2.5, Eqs. (7)-(9),
 // with the write matrix of the PDN notes section 2.6).  Everything in it that
@@ -9,17 +11,20 @@
 // second kernel whose critical path holds only the state-dependent products:
 //
 //   chunk_prep   one task per (b, h, chunk), 2 CTAs per SM, persistent.
-//                Gram [K; Q] K^T on tcgen05; gates, norms and write coefficients;
+//                Gram [K; Q] W^T on tcgen05; gates, norms and write coefficients;
 //                L and P = lower((Q W^T) . e^{g_i - g_j}); T = (I + L)^-1 by
 //                16x16 forward substitution and TF32x3 recursive doubling;
 //                W' = T diag(e^g c) K on tcgen05.  Writes one record per chunk
 //                to the workspace: T, W' and P as bf16 hi/lo pairs, and the row
-//                vectors e^g qn, e^{g_C - g} c, gamma_C.  (W' needs its lo term:
-//                with raw GDN keys E = U' - W' S cancels heavily, and a single
-//                bf16 W' costs ~1e-2 of the state.)
-//   chunk_carry  one CTA per (b, h, 64-column half of dv), 4 state warps + 1
-//                issue warp.  Per chunk:  U' = T V,  E = U' - W' S,
-//                dS = K^T (u . E),  S <- gamma_C S + dS,  o = e^g qn . Q S + P E.
+//                vectors e^g qn, e^{g_C - g} c, gamma_C (PGDN adds its write keys
+//                and the statistic's chunk map).  (W' needs its lo term: with raw
+//                GDN keys E = U' - W' S cancels heavily, and a single bf16 W'
+//                costs ~1e-2 of the state.)
+//   chunk_carry  one CTA per (b, h, 64-column half of dv): 8 state warps, an
+//                issue lane, a PE lane and 4 output warps.  Per chunk:
+//                U' = T V,  E = U' - W' S,  dS = K^T (u . E),
+//                S <- gamma_C S + dS,  o = e^g qn . Q S + P E, with the bf16
+//                hi/lo splits folded into few wide MMAs (see the carry section).
 //                The record and the K, Q, V tiles arrive by bulk / tensor copies
 //                issued as soon as the previous chunk's MMAs free each buffer.
 //
