@@ -25,6 +25,14 @@
 //           two growing factors stay below exp(decay over 8 tokens).
 // This path serves the fp32 mode (tolerance 1e-4), per-channel decay and the
 // shapes the tensor-core kernels do not take.
+//
+// Two-phase Diagonal KDN (dk = dv = 128, chunk 64, with a workspace): the
+// variance recurrence is a Moebius map per token, so kdn_map_kernel builds each
+// chunk's 2x2 product and kdn_scan_kernel composes them into p at every chunk
+// start; the same kernel in prep mode (PREP = true) then does every chunk's local
+// work in parallel and writes a per-chunk record -- bf16 hi/lo tile images for
+// the tcgen05 carry of chunk_tc_split.cu when the inputs are bf16, an fp32
+// record for kdn_carry_kernel (CUDA cores) when they are fp32.
 #include "dr_common.cuh"
 #include "tc_common.cuh"
 
