@@ -308,3 +308,23 @@ def test_kdn_two_phase_and_fused_paths(rt, dtype, workspace):
     inp = small_inputs("kdn", dtype, B=2, T=64 * 5 + 13, H=3, seed=301)
     S0, aux0 = random_state(inp, seed=302)
     check_fwd(rt, inp, S0, aux0, workspace=workspace)
+
+
+# ------------------------------------------------------------ seeded random shapes, two-phase paths
+
+@pytest.mark.parametrize("variant", ["gdn", "kla", "pgdn", "kdn"])
+def test_two_phase_random_shapes(rt, variant):
+    """Seeded draws of (B, T, H) on the two-phase paths (tcgen05 carry for every
+    variant in bf16), with a random initial state and aux state: odd head
+    counts, lengths that end anywhere inside a chunk, one to nine chunks."""
+    dr, _ = rt
+    vid = dr.VARIANT_IDS[variant]
+    assert dr.dr_chunk_fwd_path(vid, dr.DR_BF16, 128, 128, 64) in ("tc_split", "simt_split")
+    g = torch.Generator().manual_seed(900 + vid)
+    for case in range(3):
+        B = int(torch.randint(1, 3, (1,), generator=g))
+        H = int(torch.randint(1, 4, (1,), generator=g))
+        T = int(torch.randint(1, 9 * 64 + 1, (1,), generator=g))
+        inp = small_inputs(variant, "bf16", B=B, T=T, H=H, seed=1000 + 10 * vid + case)
+        S0, aux0 = random_state(inp, seed=2000 + 10 * vid + case)
+        check_fwd(rt, inp, S0, aux0)
