@@ -158,8 +158,9 @@ int dr_decode_step(const void *q, const void *k, const void *v, const float *log
 /* Bytes of the optional dr_chunk_fwd workspace for these sizes: B H ceil(T/64)
  * records on the two-phase paths (dk = dv = 128, chunk 64) of 66560 bytes (GDN,
  * KLA; bf16), 101376 bytes (PGDN, bf16: also the write keys and the key
- * statistic's chunk map) or 135168 bytes (Diagonal KDN, bf16 or fp32: fp32
- * operands and the variance chunk map), 0 where no path uses one. */
+ * statistic's chunk map) or 135168 bytes (Diagonal KDN, bf16 or fp32: the
+ * carry's operands -- bf16 hi/lo tile images for bf16 inputs, fp32 for fp32 --
+ * and the variance chunk map), 0 where no path uses one. */
 size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H, int dk, int dv,
                                     int chunk);
 
@@ -209,8 +210,11 @@ const char *dr_status_string(int status);
  *          without a workspace the same shapes take
  * "tc_ws"  the warp-specialised single-kernel tcgen05 path (GDN, KLA), or
  * "tc"     the phase-sequential tcgen05 kernel (PGDN)
- * "simt_split" two-phase fp32 CUDA-core path (Diagonal KDN, bf16 or fp32,
- *          dk = dv = 128, chunk 64) when the workspace is supplied
+ * "simt_split" two-phase Diagonal KDN path (bf16 or fp32, dk = dv = 128,
+ *          chunk 64) when the workspace is supplied: variance chunk maps and
+ *          scan, then every chunk's local work on fp32 CUDA cores, then the
+ *          state carry -- the tcgen05 carry for bf16 inputs, fp32 CUDA cores
+ *          for fp32
  * "simt"   fp32 CUDA-core kernel (everything else: fp32 mode, KDN, dk or dv 64,
  *          other chunk sizes). */
 const char *dr_chunk_fwd_path(int variant, int dtype, int dk, int dv, int chunk);
