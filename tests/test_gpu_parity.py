@@ -216,6 +216,19 @@ def test_check_finite_reports_nonfinite(rt):
     assert dr.dr_get_device_status() == 0
 
 
+@pytest.mark.parametrize("variant", ["kla", "pgdn", "kdn"])
+def test_check_finite_on_the_two_phase_paths(rt, variant):
+    """The tcgen05 carry's output and state checks (bf16, with a workspace)."""
+    dr, runner = rt
+    inp = small_inputs(variant, "bf16", B=1, T=150, H=2, seed=4)
+    inp["v"][0, 70, 1, 9] = float("nan")
+    runner.chunk_fwd(runner.to_device(inp), check_finite=True)
+    assert dr.dr_get_device_status() == dr.DR_ERR_NONFINITE
+    inp["v"][0, 70, 1, 9] = 0.0
+    runner.chunk_fwd(runner.to_device(inp), check_finite=True)
+    assert dr.dr_get_device_status() == 0
+
+
 # ------------------------------------------------------------ tensor-core path specifics
 
 @pytest.mark.parametrize("variant", ["gdn", "kla", "pgdn"])
