@@ -234,17 +234,25 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
     //         sub + TPR e, so the transposed stores hit distinct banks
     {
       const int sub = tid % TPR;
+      constexpr int kPasses = CM / RPP;
+      float kvp[kPasses][8], qvp[kPasses][8];   // every pass's loads in flight first
 #pragma unroll
-      for (int r0 = 0; r0 < CM; r0 += RPP) {
-        const int i = r0 + tid / TPR;
+      for (int pz = 0; pz < kPasses; ++pz) {
+        const int i = pz * RPP + tid / TPR;
         const bool real = i < Cc;
         const long base = real ? tok_index(a, b, t0 + i, h) * DK : 0;
-        float kv[8], qv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          kv[e] = real ? ldg_in<Tin>(a.k, base + sub + TPR * e) : 0.f;
-          qv[e] = real ? ldg_in<Tin>(a.q, base + sub + TPR * e) : 0.f;
+          kvp[pz][e] = real ? ldg_in<Tin>(a.k, base + sub + TPR * e) : 0.f;
+          qvp[pz][e] = real ? ldg_in<Tin>(a.q, base + sub + TPR * e) : 0.f;
         }
+      }
+#pragma unroll
+      for (int pz = 0; pz < kPasses; ++pz) {
+        const int i = pz * RPP + tid / TPR;
+        const bool real = i < Cc;
+        const float* kv = kvp[pz];
+        const float* qv = qvp[pz];
         float kk = 0.f, qq = 0.f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
