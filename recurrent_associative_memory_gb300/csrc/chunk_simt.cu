@@ -362,15 +362,30 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         carry = n / d;
       }
       __syncthreads();
-      for (int i = warp; i < CM; i += kThreads / 32) {   // z_i = sum_c p^_ic k_ic^2
-        float z = 0.f;
-#pragma unroll 4
+      {   // z_i = sum_c p^_ic k_ic^2: warp w takes rows w + 8 r, all partial sums first,
+          // then the eight reductions side by side
+        constexpr int kRows = CM / (kThreads / 32);
+        float z[kRows];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) z[r] = 0.f;
+#pragma unroll
         for (int c = lane; c < DK; c += 32) {
-          const float kv = sKt[c * CS + i];
-          z += sW[i * DK + c] * kv * kv;
+#pragma unroll
+          for (int r = 0; r < kRows; ++r) {
+            const int i = warp + r * (kThreads / 32);
+            const float kv = sKt[c * CS + i];
+            z[r] += sW[i * DK + c] * kv * kv;
+          }
         }
-        z = warp_sum(z);
-        if (lane == 0) sz[i] = 1.f / (sb1[i] + z);   // gain denominator, inverted once per row
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) z[r] = warp_sum(z[r]);
+        if (lane == 0) {
+#pragma unroll
+          for (int r = 0; r < kRows; ++r) {   // gain denominator, inverted once per row
+            const int i = warp + r * (kThreads / 32);
+            sz[i] = 1.f / (sb1[i] + z[r]);
+          }
+        }
       }
       __syncthreads();
 #pragma unroll 4
