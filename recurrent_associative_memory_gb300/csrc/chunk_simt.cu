@@ -388,12 +388,20 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         }
       }
       __syncthreads();
-#pragma unroll 4
-      for (int e = tid; e < CM * DK; e += kThreads) {
-        const int i = e / DK, c = e % DK;
-        const float w = sW[e] * sKt[c * CS + i] * sz[i];
-        sW[e] = w;
-        sWt[c * CS + i] = w;
+      // thread (channel c, tokens 4 i4 .. 4 i4 + 3): 16-byte accesses to the token-minor
+      // buffers, consecutive channels across lanes in the token-major one
+#pragma unroll 2
+      for (int e4 = tid; e4 < CM * DK / 4; e4 += kThreads) {
+        const int c = e4 % DK, i0 = 4 * (e4 / DK);
+        const float4 k4 = *reinterpret_cast<const float4*>(sKt + c * CS + i0);
+        const float kx[4] = {k4.x, k4.y, k4.z, k4.w};
+        float w[4];
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          w[y] = sW[(i0 + y) * DK + c] * kx[y] * sz[i0 + y];
+          sW[(i0 + y) * DK + c] = w[y];
+        }
+        *reinterpret_cast<float4*>(sWt + c * CS + i0) = make_float4(w[0], w[1], w[2], w[3]);
       }
       __syncthreads();
       // factor vectors from the per-channel g (g_{-1} = 0 at the chunk start)
@@ -411,17 +419,31 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       if (tid < DK) sgC[tid] = expf(sX[(CM - 1) * DK + tid]);
       // scale K, Q to their sub-chunk's previous boundary and W^T to its own end;
       // the row-major W becomes exp(g_C - g_j) . w_j for the state update
-#pragma unroll 4
-      for (int e = tid; e < CM * DK; e += kThreads) {
-        const int i = e / DK, c = e % DK, I = i >> 4;
-        const float gi = sX[e];
+      // (same thread mapping as the gains above: 4 tokens of one sub-chunk per thread)
+#pragma unroll 2
+      for (int e4 = tid; e4 < CM * DK / 4; e4 += kThreads) {
+        const int c = e4 % DK, i0 = 4 * (e4 / DK), I = i0 >> 4;
         const float gb = (I == 0) ? 0.f : sX[(16 * I - 1) * DK + c];
         const float ge = sX[(16 * I + 15) * DK + c];
-        const float fk = expf(gi - gb);
-        sKt[c * CS + i] *= fk;
-        sQt[c * CS + i] *= fk;
-        sWt[c * CS + i] *= expf(ge - gi);
-        sW[e] *= expf(sX[(CM - 1) * DK + c] - gi);
+        const float gC = sX[(CM - 1) * DK + c];
+        float4 k4 = *reinterpret_cast<const float4*>(sKt + c * CS + i0);
+        float4 q4 = *reinterpret_cast<const float4*>(sQt + c * CS + i0);
+        float4 w4 = *reinterpret_cast<const float4*>(sWt + c * CS + i0);
+        float* kx = reinterpret_cast<float*>(&k4);
+        float* qx = reinterpret_cast<float*>(&q4);
+        float* wx = reinterpret_cast<float*>(&w4);
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+          const float gi = sX[(i0 + y) * DK + c];
+          const float fk = expf(gi - gb);
+          kx[y] *= fk;
+          qx[y] *= fk;
+          wx[y] *= expf(ge - gi);
+          sW[(i0 + y) * DK + c] *= expf(gC - gi);
+        }
+        *reinterpret_cast<float4*>(sKt + c * CS + i0) = k4;
+        *reinterpret_cast<float4*>(sQt + c * CS + i0) = q4;
+        *reinterpret_cast<float4*>(sWt + c * CS + i0) = w4;
       }
       __syncthreads();
     }
