@@ -503,13 +503,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
     }
 
     // ---- 5. operands of the carry: Gamma.K, Gamma.Q, exp(g_C - g_j).W, gamma_C
-    if (kdn) {
-#pragma unroll 4
-      for (int e = tid; e < CM * DK; e += kThreads) {
-        const int i = e / DK, c = e % DK;
-        const float gb = fGb[(i >> 4) * DK + c];
-        sKt[c * CS + i] *= gb;
-        sQt[c * CS + i] *= gb;
+    if (kdn) {   // one channel x 4 tokens of a sub-chunk per thread (16-byte accesses)
+#pragma unroll 2
+      for (int e4 = tid; e4 < CM * DK / 4; e4 += kThreads) {
+        const int c = e4 % DK, i0 = 4 * (e4 / DK);
+        const float gb = fGb[(i0 >> 4) * DK + c];
+        float4 k4 = *reinterpret_cast<const float4*>(sKt + c * CS + i0);
+        float4 q4 = *reinterpret_cast<const float4*>(sQt + c * CS + i0);
+        k4.x *= gb; k4.y *= gb; k4.z *= gb; k4.w *= gb;
+        q4.x *= gb; q4.y *= gb; q4.z *= gb; q4.w *= gb;
+        *reinterpret_cast<float4*>(sKt + c * CS + i0) = k4;
+        *reinterpret_cast<float4*>(sQt + c * CS + i0) = q4;
       }
     } else {
       const float gC = sg[CM - 1];
