@@ -588,9 +588,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       // Each image is built in shared memory regions this task no longer needs and
       // leaves with one bulk copy (thread 0): T and P over the L/T buffer, then
       // W'^T there too, (Gamma.Q) over (Gamma.K)^T and Wbar over T^T.
-      for (int e = tid; e < CM * CM; e += kThreads) {   // T^T, zero above the diagonal of T
-        const int i = e >> 6, j = e & 63;
-        sTt[j * CS + i] = (j <= i) ? sLT[i * LDL + j] : 0.f;
+      // T^T, zero above the diagonal of T: thread (j, tokens 4 i4 .. 4 i4 + 3), one
+      // 16-byte store into the token-minor buffer
+      for (int e4 = tid; e4 < CM * CM / 4; e4 += kThreads) {
+        const int j = e4 & 63, i0 = 4 * (e4 >> 6);
+        float t[4];
+#pragma unroll
+        for (int y = 0; y < 4; ++y) t[y] = (j <= i0 + y) ? sLT[(i0 + y) * LDL + j] : 0.f;
+        *reinterpret_cast<float4*>(sTt + j * CS + i0) = make_float4(t[0], t[1], t[2], t[3]);
       }
       __syncthreads();
       uint8_t* stX = reinterpret_cast<uint8_t*>(sX);
