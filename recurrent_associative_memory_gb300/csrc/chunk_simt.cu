@@ -449,57 +449,82 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
     }
 
     // ---- 4. Gram: L (row-major, into the L/T buffer) and P^T; the per-channel g is dead
+    //      Warp-level TF32x3 tensor-core products (fp32-accurate, as in the inverse).
+    //      One unit = the 16 x 16 output of sub-chunk pair (I, J <= I) for K (-> L) or
+    //      Q (-> P) over all dk channels, as two 16 x 8 halves sharing the A operand;
+    //      the pair's per-channel factors scale the W operand before it is split.
+    //      Six independent accumulation chains per k-step (hi.hi, lo.hi, hi.lo for each
+    //      half) keep the tensor pipe busy.  20 units over 8 warps.
     {
-      const int ti = tid >> 4, tj = tid & 15;
-      const int I = ti >> 2, J = tj >> 2;
-      float ak[4][4], aq[4][4];
-#pragma unroll
-      for (int x = 0; x < 4; ++x)
-#pragma unroll
-        for (int y = 0; y < 4; ++y) ak[x][y] = aq[x][y] = 0.f;
-      if (tj <= ti) {
-        const float* Wsrc = explicit_w ? sWt : sKt;
+      const int g = lane >> 2, t = lane & 3;
+      const float* Wsrc = explicit_w ? sWt : sKt;
+      for (int u = warp; u < 20; u += kThreads / 32) {
+        const int pr = u >> 1, isq = u & 1;
+        int I = 0;
+        while ((I + 1) * (I + 2) / 2 <= pr) ++I;           // pair pr -> (I, J), J <= I
+        const int J = pr - I * (I + 1) / 2;
+        const float* Xt = isq ? sQt : sKt;
         const float* fk = (kdn && J == I) ? fDa + I * DK : sOne;
         const float* fw = kdn ? ((J < I) ? fOff + pair_index(I, J) * DK : fDb + I * DK) : sOne;
-        for (int c = 0; c < DK; ++c) {
-          const float4 k4 = *reinterpret_cast<const float4*>(sKt + c * CS + 4 * ti);
-          const float4 q4 = *reinterpret_cast<const float4*>(sQt + c * CS + 4 * ti);
-          const float4 w4 = *reinterpret_cast<const float4*>(Wsrc + c * CS + 4 * tj);
-          const float sk = fk[c], sw = fw[c];
-          const float kx[4] = {k4.x * sk, k4.y * sk, k4.z * sk, k4.w * sk};
-          const float qx[4] = {q4.x * sk, q4.y * sk, q4.z * sk, q4.w * sk};
-          const float wx[4] = {w4.x * sw, w4.y * sw, w4.z * sw, w4.w * sw};
+        const int ra = 16 * I + g, cb = 16 * J + g;
+        float d[2][4], dl[2][4], dr[2][4];
 #pragma unroll
-          for (int x = 0; x < 4; ++x)
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int y = 0; y < 4; ++y) {
-              ak[x][y] += kx[x] * wx[y];
-              aq[x][y] += qx[x] * wx[y];
-            }
-        }
-      }
-      __syncthreads();   // the KDN g in sX is read above; L overwrites it below
-      float lv[4][4], pv[4][4];
+          for (int x = 0; x < 4; ++x) d[h][x] = dl[h][x] = dr[h][x] = 0.f;
+#pragma unroll 2
+        for (int ks = 0; ks < DK / 8; ++ks) {
+          const int c0 = 8 * ks + t, c1 = c0 + 4;
+          const float af[4] = {Xt[c0 * CS + ra], Xt[c0 * CS + ra + 8], Xt[c1 * CS + ra],
+                               Xt[c1 * CS + ra + 8]};
+          const float f0 = fk[c0] * fw[c0], f1 = fk[c1] * fw[c1];
+          uint32_t ah[4], al[4];
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int i = 4 * ti + x;
-#pragma unroll
-        for (int y = 0; y < 4; ++y) {
-          const int j = 4 * tj + y;
-          float f = 1.f;
-          if (!kdn) {
-            f = expf(fminf(sg[i] - sg[j], 0.f));
-            if (!explicit_w) f *= sb1[j];
+          for (int x = 0; x < 4; ++x) {
+            ah[x] = tc::to_tf32(af[x]);
+            al[x] = tc::to_tf32(af[x] - __uint_as_float(ah[x]));
           }
-          lv[x][y] = (j < i) ? ak[x][y] * f : 0.f;
-          pv[x][y] = (j <= i) ? aq[x][y] * f : 0.f;
-        }
-        *reinterpret_cast<float4*>(sLT + i * LDL + 4 * tj) = make_float4(lv[x][0], lv[x][1], lv[x][2], lv[x][3]);
-      }
 #pragma unroll
-      for (int y = 0; y < 4; ++y)
-        *reinterpret_cast<float4*>(sPt + (4 * tj + y) * CS + 4 * ti) =
-            make_float4(pv[0][y], pv[1][y], pv[2][y], pv[3][y]);
+          for (int h = 0; h < 2; ++h) {
+            const float bf[2] = {Wsrc[c0 * CS + cb + 8 * h] * f0, Wsrc[c1 * CS + cb + 8 * h] * f1};
+            uint32_t bh[2], bl[2];
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+              bh[x] = tc::to_tf32(bf[x]);
+              bl[x] = tc::to_tf32(bf[x] - __uint_as_float(bh[x]));
+            }
+            tc::mma_tf32(dl[h], al, bh);
+            tc::mma_tf32(dr[h], ah, bl);
+            tc::mma_tf32(d[h], ah, bh);
+          }
+        }
+        // fragment element (row g or g + 8, column 2t or 2t + 1) -> L row-major / P^T
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const int i = 16 * I + g + 8 * (x >> 1), j = 16 * J + 8 * h + 2 * t + (x & 1);
+            float v = d[h][x] + (dl[h][x] + dr[h][x]);
+            if (!kdn) {
+              v *= expf(fminf(sg[i] - sg[j], 0.f));
+              if (!explicit_w) v *= sb1[j];
+            }
+            if (isq)
+              sPt[j * CS + i] = (j <= i) ? v : 0.f;
+            else
+              sLT[i * LDL + j] = (j < i) ? v : 0.f;
+          }
+      }
+      // L and P above the diagonal blocks are zero (the inverse's 32 x 32 step reads
+      // the upper block of T's top-left quarter)
+      for (int e = tid; e < 6 * 256; e += kThreads) {
+        const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+        const int I = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int J = blk < 3 ? 1 + blk : (blk < 5 ? blk - 1 : 3);
+        sPt[(16 * J + cc) * CS + 16 * I + r] = 0.f;
+        sLT[(16 * I + r) * LDL + 16 * J + cc] = 0.f;
+      }
+      __syncthreads();
     }
 
     // ---- 5. operands of the carry: Gamma.K, Gamma.Q, exp(g_C - g_j).W, gamma_C
