@@ -96,6 +96,21 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
+// m16n8k16 bf16 mma.sync, fp32 accumulate (the bf16-input Gram's split products)
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                               const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32"
+      " {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// (x0, x1) -> packed bf16x2 hi = bf16(x) and lo = bf16(x - hi)
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = tc::pack_bf16(x0, x1);
+  lo = tc::pack_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xFFFF0000u));
+}
+
 // index of the (I, J) pair, J < I, among the 6 strictly lower sub-chunk pairs
 __device__ __forceinline__ int pair_index(int I, int J) { return I * (I - 1) / 2 + J; }
 
@@ -472,30 +487,56 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int x = 0; x < 4; ++x) d[h][x] = dl[h][x] = dr[h][x] = 0.f;
+        if constexpr (sizeof(Tin) == 2) {
+          // bf16 inputs (5e-3 bar): m16n8k16 bf16 products of hi/lo splits (~2^-16
+          // relative per term), 16 channels per k-step
 #pragma unroll 2
-        for (int ks = 0; ks < DK / 8; ++ks) {
-          const int c0 = 8 * ks + t, c1 = c0 + 4;
-          const float af[4] = {Xt[c0 * CS + ra], Xt[c0 * CS + ra + 8], Xt[c1 * CS + ra],
-                               Xt[c1 * CS + ra + 8]};
-          const float f0 = fk[c0] * fw[c0], f1 = fk[c1] * fw[c1];
-          uint32_t ah[4], al[4];
+          for (int ks = 0; ks < DK / 16; ++ks) {
+            const int c0 = 16 * ks + 2 * t, c1 = c0 + 8;   // channels c0, c0+1, c1, c1+1
+            const float f00 = fk[c0] * fw[c0], f01 = fk[c0 + 1] * fw[c0 + 1];
+            const float f10 = fk[c1] * fw[c1], f11 = fk[c1 + 1] * fw[c1 + 1];
+            uint32_t ah[4], al[4];
+            split2(Xt[c0 * CS + ra], Xt[(c0 + 1) * CS + ra], ah[0], al[0]);
+            split2(Xt[c0 * CS + ra + 8], Xt[(c0 + 1) * CS + ra + 8], ah[1], al[1]);
+            split2(Xt[c1 * CS + ra], Xt[(c1 + 1) * CS + ra], ah[2], al[2]);
+            split2(Xt[c1 * CS + ra + 8], Xt[(c1 + 1) * CS + ra + 8], ah[3], al[3]);
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            ah[x] = tc::to_tf32(af[x]);
-            al[x] = tc::to_tf32(af[x] - __uint_as_float(ah[x]));
-          }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float bf[2] = {Wsrc[c0 * CS + cb + 8 * h] * f0, Wsrc[c1 * CS + cb + 8 * h] * f1};
-            uint32_t bh[2], bl[2];
-#pragma unroll
-            for (int x = 0; x < 2; ++x) {
-              bh[x] = tc::to_tf32(bf[x]);
-              bl[x] = tc::to_tf32(bf[x] - __uint_as_float(bh[x]));
+            for (int h = 0; h < 2; ++h) {
+              const int cc = cb + 8 * h;
+              uint32_t bh[2], bl[2];
+              split2(Wsrc[c0 * CS + cc] * f00, Wsrc[(c0 + 1) * CS + cc] * f01, bh[0], bl[0]);
+              split2(Wsrc[c1 * CS + cc] * f10, Wsrc[(c1 + 1) * CS + cc] * f11, bh[1], bl[1]);
+              mma_bf16_16816(dl[h], al, bh);
+              mma_bf16_16816(dr[h], ah, bl);
+              mma_bf16_16816(d[h], ah, bh);
             }
-            tc::mma_tf32(dl[h], al, bh);
-            tc::mma_tf32(dr[h], ah, bl);
-            tc::mma_tf32(d[h], ah, bh);
+          }
+        } else {
+  #pragma unroll 2
+          for (int ks = 0; ks < DK / 8; ++ks) {
+            const int c0 = 8 * ks + t, c1 = c0 + 4;
+            const float af[4] = {Xt[c0 * CS + ra], Xt[c0 * CS + ra + 8], Xt[c1 * CS + ra],
+                                 Xt[c1 * CS + ra + 8]};
+            const float f0 = fk[c0] * fw[c0], f1 = fk[c1] * fw[c1];
+            uint32_t ah[4], al[4];
+  #pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              ah[x] = tc::to_tf32(af[x]);
+              al[x] = tc::to_tf32(af[x] - __uint_as_float(ah[x]));
+            }
+  #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float bf[2] = {Wsrc[c0 * CS + cb + 8 * h] * f0, Wsrc[c1 * CS + cb + 8 * h] * f1};
+              uint32_t bh[2], bl[2];
+  #pragma unroll
+              for (int x = 0; x < 2; ++x) {
+                bh[x] = tc::to_tf32(bf[x]);
+                bl[x] = tc::to_tf32(bf[x] - __uint_as_float(bh[x]));
+              }
+              tc::mma_tf32(dl[h], al, bh);
+              tc::mma_tf32(dr[h], ah, bl);
+              tc::mma_tf32(d[h], ah, bh);
+            }
           }
         }
         // fragment element (row g or g + 8, column 2t or 2t + 1) -> L row-major / P^T
