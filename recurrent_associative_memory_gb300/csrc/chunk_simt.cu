@@ -692,53 +692,60 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         umma::bulk_store(rec + rbP, stX + 16384, 16384);
         umma::bulk_commit();
       }
-      // W'^T [c][i] = sum_{j <= i} (Gamma.K)^T[c][j] T[i][j].  Tokens in 16 blocks of 4;
-      // warp w takes blocks w and 15 - w, so every warp runs 17 steps of 4 j (T is
-      // lower triangular); lane l takes rows l + 32x.  (Gamma.K)^T is read 4 j at a
-      // time (16-byte loads, conflict-free across lanes), T^T rows are broadcast.
-      float w[2][4][4];
+      // W'^T [c][i] = sum_{j <= i} (Gamma.K)^T[c][j] T[i][j] on m16n8k16 bf16 products of
+      // hi/lo splits: warp w takes rows 16w .. 16w + 15 and every 8-token column tile,
+      // whose k-steps stop at its last token (T is lower triangular).  The fp32
+      // fragments stay in registers until the record image is written.
+      float wacc[8][4];
+      {
+        const int g = lane >> 2, t = lane & 3, r0 = 16 * warp + g;
+        uint32_t ah[4][4], al[4][4];   // A = (Gamma.K)^T fragments of the 4 k-steps
 #pragma unroll
-      for (int bsel = 0; bsel < 2; ++bsel) {
-        const int i0 = 4 * (bsel == 0 ? warp : 15 - warp);
+        for (int kk = 0; kk < 4; ++kk) {
+          const int c0 = 16 * kk + 2 * t, c1 = c0 + 8;
+          const float2 x0 = *reinterpret_cast<const float2*>(sKt + r0 * CS + c0);
+          const float2 x1 = *reinterpret_cast<const float2*>(sKt + (r0 + 8) * CS + c0);
+          const float2 x2 = *reinterpret_cast<const float2*>(sKt + r0 * CS + c1);
+          const float2 x3 = *reinterpret_cast<const float2*>(sKt + (r0 + 8) * CS + c1);
+          split2(x0.x, x0.y, ah[kk][0], al[kk][0]);
+          split2(x1.x, x1.y, ah[kk][1], al[kk][1]);
+          split2(x2.x, x2.y, ah[kk][2], al[kk][2]);
+          split2(x3.x, x3.y, ah[kk][3], al[kk][3]);
+        }
 #pragma unroll
-        for (int x = 0; x < 4; ++x)
+        for (int n = 0; n < 8; ++n) {
+          float dh[4] = {0.f, 0.f, 0.f, 0.f}, dl[4] = {0.f, 0.f, 0.f, 0.f}, dr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int y = 0; y < 4; ++y) w[bsel][x][y] = 0.f;
-        for (int j = 0; j < i0 + 4; j += 4) {
-          float4 kv[4];
-#pragma unroll
-          for (int x = 0; x < 4; ++x)
-            kv[x] = *reinterpret_cast<const float4*>(sKt + (lane + 32 * x) * CS + j);
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const float4 t4 = *reinterpret_cast<const float4*>(sTt + (j + jj) * CS + i0);
-            const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const float k = jj == 0 ? kv[x].x : (jj == 1 ? kv[x].y : (jj == 2 ? kv[x].z : kv[x].w));
-#pragma unroll
-              for (int y = 0; y < 4; ++y) w[bsel][x][y] += k * tv[y];
-            }
+          for (int kk = 0; kk <= n / 2; ++kk) {
+            const int j0 = 16 * kk + 2 * t, col = 8 * n + g;
+            uint32_t bh[2], bl[2];
+            split2(sTt[j0 * CS + col], sTt[(j0 + 1) * CS + col], bh[0], bl[0]);
+            split2(sTt[(j0 + 8) * CS + col], sTt[(j0 + 9) * CS + col], bh[1], bl[1]);
+            mma_bf16_16816(dl, al[kk], bh);
+            mma_bf16_16816(dr, ah[kk], bl);
+            mma_bf16_16816(dh, ah[kk], bh);
           }
+#pragma unroll
+          for (int x = 0; x < 4; ++x) wacc[n][x] = dh[x] + (dl[x] + dr[x]);
         }
       }
       if (tid == 0) umma::bulk_wait_read<0>();   // T, P have left the L/T buffer
       __syncthreads();                           // (Gamma.K)^T and T^T are read too
       uint8_t* stK = reinterpret_cast<uint8_t*>(sKt);
       uint8_t* stT = reinterpret_cast<uint8_t*>(sTt);
+      {   // W'^T fragments -> hi/lo image: element pairs (row c, tokens 2t, 2t + 1)
+        const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-      for (int bsel = 0; bsel < 2; ++bsel) {   // 4 tokens = half of a 16-byte chunk
-        const int i0 = 4 * (bsel == 0 ? warp : 15 - warp);
+        for (int n = 0; n < 8; ++n)
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const float* v = w[bsel][x];
-          const uint32_t h0 = tc::pack_bf16(v[0], v[1]), h1 = tc::pack_bf16(v[2], v[3]);
-          const uint32_t l0 = tc::pack_bf16(v[0] - __uint_as_float(h0 << 16), v[1] - __uint_as_float(h0 & 0xFFFF0000u));
-          const uint32_t l1 = tc::pack_bf16(v[2] - __uint_as_float(h1 << 16), v[3] - __uint_as_float(h1 & 0xFFFF0000u));
-          const uint32_t off = umma::sw128_offset(lane + 32 * x, i0);
-          *reinterpret_cast<uint2*>(stX + off) = make_uint2(h0, h1);
-          *reinterpret_cast<uint2*>(stX + 16384 + off) = make_uint2(l0, l1);
-        }
+          for (int hr = 0; hr < 2; ++hr) {
+            const int c = 16 * warp + g + 8 * hr, i = 8 * n + 2 * t;
+            uint32_t hi, lo;
+            split2(wacc[n][2 * hr], wacc[n][2 * hr + 1], hi, lo);
+            const uint32_t off = umma::sw128_offset(c, i);
+            *reinterpret_cast<uint32_t*>(stX + off) = hi;
+            *reinterpret_cast<uint32_t*>(stX + 16384 + off) = lo;
+          }
       }
 #pragma unroll
       for (int r = 0; r < 4; ++r) {   // (Gamma.Q) and Wbar: [64 tok][128] as two 64-column blocks
