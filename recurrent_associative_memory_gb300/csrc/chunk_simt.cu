@@ -377,29 +377,29 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         carry = n / d;
       }
       __syncthreads();
-      {   // z_i = sum_c p^_ic k_ic^2: warp w takes rows w + 8 r, all partial sums first,
-          // then the eight reductions side by side
+      {   // z_i = sum_c p^_ic k_ic^2: warp w takes rows 8w .. 8w + 7 (keys read as two
+          // 16-byte pieces per channel), all partial sums first, then the eight
+          // reductions side by side
         constexpr int kRows = CM / (kThreads / 32);
+        static_assert(kRows == 8, "eight rows per warp");
+        const int i0 = kRows * warp;
         float z[kRows];
 #pragma unroll
         for (int r = 0; r < kRows; ++r) z[r] = 0.f;
 #pragma unroll
         for (int c = lane; c < DK; c += 32) {
+          const float4 k0 = *reinterpret_cast<const float4*>(sKt + c * CS + i0);
+          const float4 k1 = *reinterpret_cast<const float4*>(sKt + c * CS + i0 + 4);
+          const float kv[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
 #pragma unroll
-          for (int r = 0; r < kRows; ++r) {
-            const int i = warp + r * (kThreads / 32);
-            const float kv = sKt[c * CS + i];
-            z[r] += sW[i * DK + c] * kv * kv;
-          }
+          for (int r = 0; r < kRows; ++r) z[r] += sW[(i0 + r) * DK + c] * kv[r] * kv[r];
         }
 #pragma unroll
         for (int r = 0; r < kRows; ++r) z[r] = warp_sum(z[r]);
         if (lane == 0) {
 #pragma unroll
-          for (int r = 0; r < kRows; ++r) {   // gain denominator, inverted once per row
-            const int i = warp + r * (kThreads / 32);
-            sz[i] = 1.f / (sb1[i] + z[r]);
-          }
+          for (int r = 0; r < kRows; ++r)   // gain denominator, inverted once per row
+            sz[i0 + r] = 1.f / (sb1[i0 + r] + z[r]);
         }
       }
       __syncthreads();
