@@ -26,13 +26,18 @@
 // This path serves the fp32 mode (tolerance 1e-4), per-channel decay and the
 // shapes the tensor-core kernels do not take.
 //
-// Two-phase Diagonal KDN (dk = dv = 128, chunk 64, with a workspace): the
-// variance recurrence is a Moebius map per token, so kdn_map_kernel builds each
-// chunk's 2x2 product and kdn_scan_kernel composes them into p at every chunk
-// start; the same kernel in prep mode (PREP = true) then does every chunk's local
-// work in parallel and writes a per-chunk record -- bf16 hi/lo tile images for
-// the tcgen05 carry of chunk_tc_split.cu when the inputs are bf16, an fp32
-// record for kdn_carry_kernel (CUDA cores) when they are fp32.
+// Two-phase Diagonal KDN (dk = dv = 128, chunk 64, with a workspace): the same
+// kernel in prep mode (PREP = true) does every chunk's local work in parallel and
+// writes a per-chunk record -- bf16 hi/lo tile images for the tcgen05 carry of
+// chunk_tc_split.cu when the inputs are bf16, an fp32 record for kdn_carry_kernel
+// (CUDA cores) when they are fp32.  Only the variance p at the chunk start is
+// sequential across chunks.  With many (b, h) rows the prep chains it itself:
+// tasks are taken in chunk-major ticket order and each one hands p at its end to
+// the next chunk of its row through the workspace (a release flag; the wait is
+// bounded), which costs each CTA only a one-off phase lag.  With few rows the
+// chain would serialise the CTAs, so kdn_map_kernel first builds each chunk's
+// variance map (a 2x2 Moebius product) and kdn_scan_kernel composes them into p
+// at every chunk start.
 #include "dr_common.cuh"
 #include "tc_common.cuh"
 
@@ -96,6 +101,31 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
+// GPU-scope release store / acquire load of a chain flag
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Waits until *flag != 0 or *abort != 0, at most limit_ns of global-timer time.
+// Returns false (and raises *abort, so every other waiter returns at once) when
+// the flag did not arrive.
+__device__ bool chain_wait(const uint32_t* flag, uint32_t* abort, uint64_t limit_ns) {
+  if (ld_acquire_gpu(flag)) return true;
+  const uint64_t t0 = umma::globaltimer_ns();
+  for (;;) {
+    if (ld_acquire_gpu(flag)) return true;
+    if (ld_acquire_gpu(abort) || umma::globaltimer_ns() - t0 > limit_ns) {
+      atomicExch(abort, 1u);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
 // m16n8k16 bf16 mma.sync, fp32 accumulate (the bf16-input Gram's split products)
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
                                                const uint32_t (&b)[2]) {
@@ -133,10 +163,19 @@ constexpr uint32_t rbT = 0, rbWp = 16384, rbP = 49152, rbVec = 65536, rbQ = 6656
 
 // PREP = false: the fused forward, one CTA per (b, h, 32 columns), chunks in order.
 // PREP = true (Diagonal KDN, dk = 128): one task per (b, h, chunk), all chunks in
-// parallel, the variance state at the chunk start read from the record; the
-// chunk's carry operands are written to the record instead of being used.
+// parallel; the chunk's carry operands are written to the record instead of being
+// used.  The variance at the chunk start is read from the record (written by
+// kdn_scan_kernel) when chain is null.  Otherwise chain holds one flag per record,
+// then the ticket counter and the abort word, all zero at launch: tasks are taken
+// by ticket in chunk-major order, a task waits for its flag, reads p from its
+// record and hands p at its end to the next chunk's record (then raises that
+// chunk's flag); the last chunk of a row writes p to aux.  A task only waits on
+// tickets claimed earlier by running CTAs, so the chain needs no co-residency.
+constexpr uint64_t kChainWaitNs = 2000000000ull;   // 2 s: a lost flag, not a slow one
+
 template <int DK, typename Tin, bool PREP>
-__global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint8_t* __restrict__ ws) {
+__global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint8_t* __restrict__ ws,
+                                                                 uint32_t* __restrict__ chain) {
   using SM = SimtSmem<DK>;
   constexpr int TPR = DK / 8;                // threads per token row in the load pass
   constexpr int RPP = kThreads / TPR;        // rows per load pass
@@ -196,19 +235,37 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
   bool bad = false;
 
   const long kIters = PREP ? (long)a.B * a.H * NCk : NCk;
-  for (long it = PREP ? blockIdx.x : 0; it < kIters; it += PREP ? gridDim.x : 1) {
+  const bool chained = PREP && chain != nullptr;
+  __shared__ long s_ticket;   // chained prep: the task after this one (claimed one ahead)
+  long it0 = PREP ? blockIdx.x : 0;
+  if (chained) {
+    if (tid == 0) s_ticket = atomicAdd(chain + kIters, 1u);
+    __syncthreads();
+    it0 = s_ticket;
+  }
+  for (long it = it0; it < kIters; it = chained ? s_ticket : it + (PREP ? gridDim.x : 1)) {
     int t0 = (int)it * CM;
+    int ci = 0;       // chunk of a prep task
+    long ri = 0;      // its record
     uint8_t* rec = nullptr;
-    if (PREP) {   // task (b h, chunk); the variance at the chunk start comes from the scan
-      bh = (int)(it / NCk);
+    if (PREP) {   // task (b h, chunk)
+      if (chained) {
+        ci = (int)(it / (a.B * a.H));
+        bh = (int)(it % (a.B * a.H));
+      } else {
+        bh = (int)(it / NCk);
+        ci = (int)(it % NCk);
+      }
       b = bh / a.H;
       h = bh % a.H;
-      t0 = (int)(it % NCk) * CM;
-      rec = ws + (size_t)it * kRecK;
-      if (tid < DK) carry = reinterpret_cast<const float*>(rec + rkP0)[tid];
+      t0 = ci * CM;
+      ri = (long)bh * NCk + ci;
+      rec = ws + (size_t)ri * kRecK;
+      if (!chained && tid < DK) carry = reinterpret_cast<const float*>(rec + rkP0)[tid];
     }
     const int Cc = min(CM, a.T - t0);
     __syncthreads();
+    if (chained && tid == 0) s_ticket = atomicAdd(chain + kIters, 1u);
 
     if (kdn) {   // per-channel log-decay and process noise, row-major [i][c], copied
                  // asynchronously (16-byte pieces, zero-filled past the end) under the loads below
@@ -302,7 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       for (int r = 0; r < CM * NV / kThreads; ++r) sV[tid + r * kThreads] = vv[r];
     }
     if (kdn) cp_async_wait_all();
+    if (chained && ci > 0 && tid == 0 && !chain_wait(chain + ri, chain + kIters + 1, kChainWaitNs))
+      set_status(DR_ERR_TIMEOUT);
     __syncthreads();
+    if (chained && tid < DK)   // p at the chunk start: the row's initial value, or the previous chunk's
+      carry = ci == 0 ? (a.aux0 ? a.aux0[(long)bh * DK + tid] : 1.f)
+                      : __ldcg(reinterpret_cast<const float*>(rec + rkP0) + tid);
 
     // ---- 3. cumulative decay and write vectors
     if (!kdn) {
@@ -375,8 +437,17 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
           d = ldexpf(d, -ex);
         }
         carry = n / d;
+        if (chained) {   // p at the chunk end -> the next chunk's record, or aux after the last
+          if (ci + 1 < NCk) {
+            __stcg(reinterpret_cast<float*>(rec + kRecK + rkP0) + c, carry);
+            __threadfence();
+          } else if (a.aux) {
+            a.aux[(long)bh * DK + c] = carry;
+          }
+        }
       }
       __syncthreads();
+      if (chained && tid == 0 && ci + 1 < NCk) st_release_gpu(chain + ri + 1, 1u);
       {   // z_i = sum_c p^_ic k_ic^2: warp w takes rows 8w .. 8w + 7 (keys read as two
           // 16-byte pieces per channel), all partial sums first, then the eight
           // reductions side by side
@@ -947,14 +1018,16 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
 // The per-channel variance recurrence p^ = a^2 p + w, p = p^ / (1 + u p^) is a
 // Moebius map of p, i.e. the linear map (n, d) <- [[a^2, w], [u a^2, 1 + u w]] (n, d)
 // in homogeneous coordinates p = n / d (KDN notes section 6); a chunk is the
-// product of its tokens' matrices.
+// product of its tokens' matrices.  With few (b, h) rows (4 B H < SM count) two
+// kernels give p at every chunk start before the prep:
 //   kdn_map_kernel   one warp per (b, h, chunk), lane = 4 channels (key norm by a
 //                    warp reduction); the product is rescaled by a power of two
 //                    every 8 tokens (p is scale-free).
 //   kdn_scan_kernel  one thread per (b, h, channel) applies the maps in chunk
 //                    order and leaves p at every chunk start in the record.
-// Then chunk_simt_kernel<PREP> does every chunk's local work in parallel and
-// kdn_carry_kernel walks the chunks with 64 state columns per CTA.
+// With more rows the prep chains p itself.  Then chunk_simt_kernel<PREP> does
+// every chunk's local work in parallel and kdn_carry_kernel (fp32) or the tcgen05
+// carry (bf16) walks the chunks.
 constexpr int kKdnMapWarps = 8;   // 4 chunk tasks per block, two warps (token halves) each
 
 __global__ void __launch_bounds__(kKdnMapWarps * 32, 2) kdn_map_kernel(FwdArgs a, uint8_t* __restrict__ ws,
@@ -1333,7 +1406,7 @@ cudaError_t launch_chunk_simt(const FwdArgs& a, int dtype, cudaStream_t st) {
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,    \
                                            (int)smem);                                     \
     if (err != cudaSuccess) return err;                                                    \
-    chunk_simt_kernel<DK_, T_, false><<<grid, kThreads, smem, st>>>(a, nullptr);           \
+    chunk_simt_kernel<DK_, T_, false><<<grid, kThreads, smem, st>>>(a, nullptr, nullptr);           \
     return cudaGetLastError();                                                             \
   }
   if (dtype == DR_BF16) {
@@ -1356,8 +1429,12 @@ bool kdn_split_supported(int variant, int dtype, int dk, int dv, int chunk) {
          chunk == 64;
 }
 
+// chained prep: one flag per record, the ticket counter and the abort word
+size_t kdn_chain_bytes(long ntask) { return ((size_t)(ntask + 2) * 4 + 255) / 256 * 256; }
+
 size_t kdn_split_workspace_bytes(int B, int T, int H) {
-  return (size_t)B * H * ((T + CM - 1) / CM) * kRecK;
+  const long ntask = (long)B * H * ((T + CM - 1) / CM);
+  return (size_t)ntask * kRecK + kdn_chain_bytes(ntask);
 }
 
 cudaError_t launch_kdn_split(const FwdArgs& a, int dtype, void* workspace, cudaStream_t st) {
@@ -1365,10 +1442,20 @@ cudaError_t launch_kdn_split(const FwdArgs& a, int dtype, void* workspace, cudaS
   const long ntask = (long)a.B * a.H * ((a.T + CM - 1) / CM);
   const int nsm = simt_sm_count();
   if (nsm <= 0) return cudaErrorInvalidValue;
-  kdn_map_kernel<<<(int)((ntask + kKdnMapWarps / 2 - 1) / (kKdnMapWarps / 2)), kKdnMapWarps * 32, 0,
-                   st>>>(a, ws, dtype == DR_BF16 ? 1 : 0);
-  kdn_scan_kernel<<<a.B * a.H, 128, 0, st>>>(a, ws);
-  cudaError_t err = cudaGetLastError();
+  // The chain keeps about nsm / (B H) chunks of one row in flight at once; a
+  // hand-over costs a fraction of a task, so up to four of them per wave only
+  // shift the CTAs in phase.  Fewer rows: map and scan kernels first.
+  const bool chained = 4L * a.B * a.H >= nsm;
+  uint32_t* chain = chained ? reinterpret_cast<uint32_t*>(ws + (size_t)ntask * kRecK) : nullptr;
+  cudaError_t err;
+  if (chained) {
+    err = cudaMemsetAsync(chain, 0, kdn_chain_bytes(ntask), st);
+  } else {
+    kdn_map_kernel<<<(int)((ntask + kKdnMapWarps / 2 - 1) / (kKdnMapWarps / 2)), kKdnMapWarps * 32, 0,
+                     st>>>(a, ws, dtype == DR_BF16 ? 1 : 0);
+    kdn_scan_kernel<<<a.B * a.H, 128, 0, st>>>(a, ws);
+    err = cudaGetLastError();
+  }
   if (err != cudaSuccess) return err;
   const size_t psmem = simt_smem_bytes(128);
   const int pgrid = (int)(ntask < nsm ? ntask : nsm);
@@ -1377,7 +1464,7 @@ cudaError_t launch_kdn_split(const FwdArgs& a, int dtype, void* workspace, cudaS
     err = cudaFuncSetAttribute(chunk_simt_kernel<128, T_, true>,                           \
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);   \
     if (err != cudaSuccess) return err;                                                    \
-    chunk_simt_kernel<128, T_, true><<<pgrid, kThreads, psmem, st>>>(a, ws);              \
+    chunk_simt_kernel<128, T_, true><<<pgrid, kThreads, psmem, st>>>(a, ws, chain);       \
     if ((err = cudaGetLastError()) != cudaSuccess) return err;                             \
   }
   if (dtype == DR_BF16) {   // bf16 records -> the tensor-core carry

@@ -87,9 +87,12 @@ def test_status_strings(dr):
     assert dr.dr_chunk_fwd_workspace_bytes(0, 1, 2, 65, 3, 128, 128, 64) == 2 * 3 * 2 * 66560
     # PGDN records also carry the write keys and the statistic's chunk map
     assert dr.dr_chunk_fwd_workspace_bytes(2, 1, 4, 4096, 16, 128, 128, 64) == 4 * 16 * 64 * 101376
-    # Diagonal KDN: fp32 operand records (either input dtype)
-    assert dr.dr_chunk_fwd_workspace_bytes(3, 1, 4, 8192, 16, 128, 128, 64) == 4 * 16 * 128 * 135168
-    assert dr.dr_chunk_fwd_workspace_bytes(3, 0, 1, 65, 1, 128, 128, 64) == 2 * 135168
+    # Diagonal KDN: fp32 operand records (either input dtype), then the flags of
+    # the variance chain (one per record, a ticket counter and an abort word,
+    # rounded up to 256 bytes)
+    assert dr.dr_chunk_fwd_workspace_bytes(3, 1, 4, 8192, 16, 128, 128, 64) == \
+        4 * 16 * 128 * 135168 + 33024
+    assert dr.dr_chunk_fwd_workspace_bytes(3, 0, 1, 65, 1, 128, 128, 64) == 2 * 135168 + 256
     for args in [(1, 0, 8, 2048, 8, 128, 128, 64), (1, 1, 8, 2048, 8, 64, 128, 64),
                  (1, 1, 8, 2048, 8, 128, 128, 32), (3, 1, 8, 2048, 8, 64, 64, 64),
                  (3, 1, 8, 2048, 8, 128, 128, 32)]:

@@ -311,9 +311,10 @@ def test_tc_path_unnormalised_gdn_strong_keys(rt):
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("workspace", ["auto", None])
 def test_kdn_two_phase_and_fused_paths(rt, dtype, workspace):
-    """Diagonal KDN with a workspace runs the two-phase CUDA-core path (variance
-    chunk maps + scan, parallel chunk prep, 64-column carry); without one the
-    fused kernel.  Ragged tail, nonzero initial state and variance."""
+    """Diagonal KDN with a workspace runs the two-phase path (with these few
+    rows: variance chunk maps + scan, parallel chunk prep, then the carry);
+    without one the fused kernel.  Ragged tail, nonzero initial state and
+    variance."""
     dr, runner = rt
     if workspace == "auto":
         assert dr.dr_chunk_fwd_path(dr.DR_KDN, dr.DR_BF16 if dtype == "bf16" else dr.DR_FP32,
@@ -321,6 +322,30 @@ def test_kdn_two_phase_and_fused_paths(rt, dtype, workspace):
     inp = small_inputs("kdn", dtype, B=2, T=64 * 5 + 13, H=3, seed=301)
     S0, aux0 = random_state(inp, seed=302)
     check_fwd(rt, inp, S0, aux0, workspace=workspace)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_kdn_chained_variance_many_rows(rt, dtype):
+    """With many (b, h) rows (four times the rows at least the SM count) the
+    prep hands the variance from chunk to chunk itself (chunk-major tickets,
+    flags in the workspace) instead of running the map and scan kernels.  Every
+    row checked, more tasks than CTAs, a ragged tail, nonzero initial state and
+    variance; a dirty workspace (stale flags and records) gives the same bits."""
+    dr, runner = rt
+    B, H = 2, 24
+    assert 4 * B * H >= torch.cuda.get_device_properties(0).multi_processor_count
+    inp = small_inputs("kdn", dtype, B=B, T=64 * 4 + 21, H=H, seed=311)
+    S0, aux0 = random_state(inp, seed=312)
+    check_fwd(rt, inp, S0, aux0)
+    dev = runner.to_device(inp)
+    S0d, aux0d = S0.cuda(), aux0.cuda()
+    ws = runner.workspace_for(dev)
+    ws.fill_(0xA5)
+    o1, s1, a1 = runner.chunk_fwd(dev, init_state=S0d, aux_init=aux0d, workspace=ws)
+    o2, s2, a2 = runner.chunk_fwd(dev, init_state=S0d, aux_init=aux0d, workspace=ws)
+    torch.cuda.synchronize()
+    assert dr.dr_get_device_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(s1, s2) and torch.equal(a1, a2)
 
 
 # ------------------------------------------------------------ seeded random shapes, two-phase paths
