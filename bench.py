@@ -384,10 +384,15 @@ def main():
     step_ms = [s.elapsed_time(e) for s, e in ev]
     total_s = max_over_ranks(sum(step_ms) / 1e3, world)
     dr.check(dr.dr_get_device_status(), "timed region")
-    def kernels_per_call(v):   # the two-phase path launches its prep and carry kernels
+    def kernels_per_call(v):   # the two-phase paths launch a prep and a carry kernel
         path = dr.dr_chunk_fwd_path(dr.VARIANT_IDS[v], 1 if wl.dtype == "bf16" else 0, wl.dk,
                                     wl.dv, wl.chunk)
-        return 2 if (path == "tc_split" and ws is not None) else 1
+        if ws is None or path not in ("tc_split", "simt_split"):
+            return 1
+        if path == "simt_split":   # few rows: variance map and scan kernels first
+            nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+            return 2 if 4 * wl.B * wl.H >= nsm else 4
+        return 4 if v == "pgdn" else 2   # PGDN: statistic map and scan kernels first
     launches = args.steps * sum(kernels_per_call(v) for v in variants)
     value = job_tokens_per_s(world, args.steps, len(variants), wl.B, wl.T, total_s)
 
