@@ -158,12 +158,12 @@ int dr_decode_step(const void *q, const void *k, const void *v, const float *log
 /* Bytes of the optional dr_chunk_fwd workspace for these sizes: B H ceil(T/64)
  * records on the two-phase paths (dk = dv = 128, chunk 64) of 66560 bytes (GDN,
  * KLA; bf16), 101376 bytes (PGDN, bf16: also the write keys and the key
- * statistic's chunk map) or 135168 bytes (Diagonal KDN, bf16 or fp32: the
- * carry's operands -- bf16 hi/lo tile images for bf16 inputs, fp32 for fp32 --
- * and the variance chunk map and chunk-start value), plus for Diagonal KDN
- * 4 (n + 2) bytes rounded up to 256 (n = B H ceil(T/64) records): the flags of
- * the variance chain between chunks, which the call clears itself; 0 where no
- * path uses one. */
+ * statistic's chunk map and chunk-start value) or 135168 bytes (Diagonal KDN,
+ * bf16 or fp32: the carry's operands -- bf16 hi/lo tile images for bf16
+ * inputs, fp32 for fp32 -- and the variance chunk map and chunk-start value),
+ * plus for Diagonal KDN 4 (n + 2) bytes rounded up to 256 (n = B H ceil(T/64)
+ * records): the flags of the variance chain between chunks, which the call
+ * clears itself; 0 where no path uses one. */
 size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H, int dk, int dv,
                                     int chunk);
 

@@ -101,30 +101,6 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-// GPU-scope release store / acquire load of a chain flag
-__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-// Waits until *flag != 0 or *abort != 0, at most limit_ns of global-timer time.
-// Returns false (and raises *abort, so every other waiter returns at once) when
-// the flag did not arrive.
-__device__ bool chain_wait(const uint32_t* flag, uint32_t* abort, uint64_t limit_ns) {
-  if (ld_acquire_gpu(flag)) return true;
-  const uint64_t t0 = umma::globaltimer_ns();
-  for (;;) {
-    if (ld_acquire_gpu(flag)) return true;
-    if (ld_acquire_gpu(abort) || umma::globaltimer_ns() - t0 > limit_ns) {
-      atomicExch(abort, 1u);
-      return false;
-    }
-    __nanosleep(64);
-  }
-}
 
 // m16n8k16 bf16 mma.sync, fp32 accumulate (the bf16-input Gram's split products)
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
@@ -1018,7 +994,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
 // The per-channel variance recurrence p^ = a^2 p + w, p = p^ / (1 + u p^) is a
 // Moebius map of p, i.e. the linear map (n, d) <- [[a^2, w], [u a^2, 1 + u w]] (n, d)
 // in homogeneous coordinates p = n / d (KDN notes section 6); a chunk is the
-// product of its tokens' matrices.  With few (b, h) rows (4 B H < SM count) two
+// product of its tokens' matrices.  With few (b, h) rows (3 B H < SM count) two
 // kernels give p at every chunk start before the prep:
 //   kdn_map_kernel   one warp per (b, h, chunk), lane = 4 channels (key norm by a
 //                    warp reduction); the product is rescaled by a power of two
@@ -1429,12 +1405,9 @@ bool kdn_split_supported(int variant, int dtype, int dk, int dv, int chunk) {
          chunk == 64;
 }
 
-// chained prep: one flag per record, the ticket counter and the abort word
-size_t kdn_chain_bytes(long ntask) { return ((size_t)(ntask + 2) * 4 + 255) / 256 * 256; }
-
 size_t kdn_split_workspace_bytes(int B, int T, int H) {
   const long ntask = (long)B * H * ((T + CM - 1) / CM);
-  return (size_t)ntask * kRecK + kdn_chain_bytes(ntask);
+  return (size_t)ntask * kRecK + chain_bytes(ntask);
 }
 
 cudaError_t launch_kdn_split(const FwdArgs& a, int dtype, void* workspace, cudaStream_t st) {
@@ -1442,14 +1415,15 @@ cudaError_t launch_kdn_split(const FwdArgs& a, int dtype, void* workspace, cudaS
   const long ntask = (long)a.B * a.H * ((a.T + CM - 1) / CM);
   const int nsm = simt_sm_count();
   if (nsm <= 0) return cudaErrorInvalidValue;
-  // The chain keeps about nsm / (B H) chunks of one row in flight at once; a
-  // hand-over costs a fraction of a task, so up to four of them per wave only
-  // shift the CTAs in phase.  Fewer rows: map and scan kernels first.
-  const bool chained = 4L * a.B * a.H >= nsm;
+  // A row's chunks form a chain of hand-overs (flag latency + the 4.7K-cycle
+  // variance scan, ~6K cycles each), which must stay well inside the prep's own
+  // time (NC B H / nsm tasks of ~44K cycles per CTA): NC 6K <= 0.4 NC B H 44K / nsm
+  // for 3 B H >= nsm.  Fewer rows: map and scan kernels first.
+  const bool chained = 3L * a.B * a.H >= nsm;
   uint32_t* chain = chained ? reinterpret_cast<uint32_t*>(ws + (size_t)ntask * kRecK) : nullptr;
   cudaError_t err;
   if (chained) {
-    err = cudaMemsetAsync(chain, 0, kdn_chain_bytes(ntask), st);
+    err = cudaMemsetAsync(chain, 0, chain_bytes(ntask), st);
   } else {
     kdn_map_kernel<<<(int)((ntask + kKdnMapWarps / 2 - 1) / (kKdnMapWarps / 2)), kKdnMapWarps * 32, 0,
                      st>>>(a, ws, dtype == DR_BF16 ? 1 : 0);
