@@ -70,7 +70,7 @@ KERNEL_SOURCES = {
     "chunk_tc_split": ["chunk_tc_split.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh"],
     "chunk_tc_ws": ["chunk_tc_ws.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh"],
     "chunk_tc": ["chunk_tc.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh"],
-    "chunk_simt": ["chunk_simt.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh"],
+    "chunk_simt": ["chunk_simt.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh", "chain.cuh"],
     "decode": ["decode.cu", "dr_common.cuh"],
 }
 

@@ -40,6 +40,7 @@
 // at every chunk start.
 #include "dr_common.cuh"
 #include "tc_common.cuh"
+#include "chain.cuh"
 
 namespace dr {
 

@@ -589,53 +589,88 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 // Eq. (9), first line) is linear in A, so over one chunk it is the affine map
 // A -> a_c A + b_c with a_c = prod alphaP and b_c the chunk's own accumulation
 // from 0 (the chunked form of the PDN notes section 2.6).
-//   pgdn_map_kernel   one warp per (b, h, chunk), lane = 4 channels, the key norm
-//                     by a warp reduction; eight tokens' loads in flight at once.
+//   pgdn_map_kernel   two warps per (b, h, chunk), four chunks per block: the
+//                     chunk's key tile arrives by TMA (two 64-channel boxes, 16 KB,
+//                     zero past the end), then a thread per token forms the key
+//                     norm and a thread per channel pair runs the affine map over
+//                     the chunk's 64 tokens out of shared memory.
 //   pgdn_scan_kernel  one thread per (b, h, channel) composes the maps in chunk
 //                     order and leaves A at every chunk start in the chunk's
 //                     record (and the final A).
-constexpr int kMapWarps = 8;
+constexpr int kMapTasks = 4;                            // chunk tasks per block
+constexpr uint32_t kMapSmem = kMapTasks * 16384 + 1024; // key tiles (+ 1 KB alignment)
 
-__global__ void __launch_bounds__(kMapWarps * 32) pgdn_map_kernel(FwdArgs a, uint8_t* __restrict__ ws) {
+__global__ void __launch_bounds__(kMapTasks * 64) pgdn_map_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                                   FwdArgs a, uint8_t* __restrict__ ws) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t bars[kMapTasks];
+  __shared__ float s_cr[kMapTasks][64], s_aP[kMapTasks][64], s_bP[kMapTasks][64];
+  const int tid = threadIdx.x, slot = tid >> 6, sub = tid & 63;
   const int NC = (a.T + 63) / 64;
-  const long task = (long)blockIdx.x * kMapWarps + (threadIdx.x >> 5);
-  if (task >= (long)a.B * a.H * NC) return;   // whole warps leave together
-  const int lane = threadIdx.x & 31;
-  const int bh = (int)(task / NC), c = (int)(task % NC), b = bh / a.H, h = bh % a.H;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f}, prod = 1.f;
-  const int t_end = min(64, a.T - c * 64);
-  for (int i0 = 0; i0 < t_end; i0 += 8) {
-    uint2 raw[8];
-    float aP[8], bP[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const bool real = i0 + e < t_end;
-      const long ti = ((long)b * a.T + c * 64 + (real ? i0 + e : 0)) * a.H + h;
-      raw[e] = real ? *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(a.k) +
-                                                      ti * 128 + 4 * lane)
-                    : make_uint2(0u, 0u);
-      aP[e] = real ? a.alphaP[ti] : 1.f;
-      bP[e] = real ? a.betaP[ti] : 0.f;
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const __nv_bfloat162 k01 = *reinterpret_cast<const __nv_bfloat162*>(&raw[e].x);
-      const __nv_bfloat162 k23 = *reinterpret_cast<const __nv_bfloat162*>(&raw[e].y);
-      const float kv[4] = {__low2float(k01), __high2float(k01), __low2float(k23), __high2float(k23)};
-      const float kk = warp_sum(kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3]);
-      const float cr = a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float kh = kv[q] * cr;
-        acc[q] = aP[e] * acc[q] + bP[e] * kh * kh;
-      }
-      prod *= aP[e];
+  const long ntask = (long)a.B * a.H * NC;
+  const long task = (long)blockIdx.x * kMapTasks + slot;
+  const bool live = task < ntask;
+  const int bh = live ? (int)(task / NC) : 0, c = live ? (int)(task % NC) : 0;
+  const int b = bh / a.H, h = bh % a.H;
+  uint8_t* tile = sm + slot * 16384;   // [64 tok][64 ch] bf16, channels 0-63 | 64-127
+  if (tid == 0) {
+    for (int q = 0; q < kMapTasks; ++q) mbar_init(&bars[q], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (live && sub == 0) {
+    mbar_expect_tx(&bars[slot], 16384);
+    tma_load_4d(tile, &tmK, &bars[slot], 0, h, c * 64, b);
+    tma_load_4d(tile + 8192, &tmK, &bars[slot], 64, h, c * 64, b);
+  }
+  {   // the statistic's gates of token sub, under the copy (identity past the end)
+    const int tok = c * 64 + sub;
+    const bool real = live && tok < a.T;
+    const long ti = ((long)b * a.T + tok) * a.H + h;
+    s_aP[slot][sub] = real ? a.alphaP[ti] : 1.f;
+    s_bP[slot][sub] = real ? a.betaP[ti] : 0.f;
+  }
+  bool ok = true;
+  if (live) {
+    ok = mbar_wait(&bars[slot], 0, kWait);
+    if (!ok) {   // report, and let the copy land before the block's memory is released
+      set_status(DR_ERR_TIMEOUT);
+      mbar_wait(&bars[slot], 0, kWait / 4);
     }
   }
-  float* aux = reinterpret_cast<float*>(ws + (size_t)task * kRecP + rAux);
-  if (lane == 0) aux[0] = prod;
+  if (live && ok) {   // key norm of token sub
+    float kk = 0.f;
 #pragma unroll
-  for (int e = 0; e < 4; ++e) aux[1 + 4 * lane + e] = acc[e];
+    for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4*>(tile + kb * 8192 + sw128_offset(sub, 8 * m)), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) kk += f[e] * f[e];
+      }
+    s_cr[slot][sub] = a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f;
+  }
+  __syncthreads();
+  if (!live || !ok) return;
+  // channels 2 sub, 2 sub + 1: A -> prod(alphaP) A + acc over the chunk (acc from 0)
+  const int kb = sub >> 5, col = 2 * (sub & 31);
+  float acc0 = 0.f, acc1 = 0.f, prod = 1.f;
+#pragma unroll 8
+  for (int i = 0; i < 64; ++i) {
+    const __nv_bfloat162 k2 = *reinterpret_cast<const __nv_bfloat162*>(tile + kb * 8192 + sw128_offset(i, col));
+    const float cr = s_cr[slot][i], aP = s_aP[slot][i], bP = s_bP[slot][i];
+    const float k0 = __low2float(k2) * cr, k1 = __high2float(k2) * cr;
+    acc0 = aP * acc0 + bP * k0 * k0;
+    acc1 = aP * acc1 + bP * k1 * k1;
+    prod *= aP;
+  }
+  float* aux = reinterpret_cast<float*>(ws + (size_t)task * kRecP + rAux);
+  if (sub == 0) aux[0] = prod;
+  aux[1 + 64 * kb + col] = acc0;
+  aux[2 + 64 * kb + col] = acc1;
 }
 
 __global__ void __launch_bounds__(128) pgdn_scan_kernel(FwdArgs a, uint8_t* __restrict__ ws) {
@@ -1293,7 +1328,9 @@ cudaError_t launch_chunk_tc_split(const FwdArgs& a, void* workspace, cudaStream_
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaError_t e;
   if (a.variant == DR_PGDN) {   // chunk-start values of the key statistic first
-    pgdn_map_kernel<<<(int)((ntask + kMapWarps - 1) / kMapWarps), kMapWarps * 32, 0, st>>>(a, ws);
+    e = cudaFuncSetAttribute(pgdn_map_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMapSmem);
+    if (e != cudaSuccess) return e;
+    pgdn_map_kernel<<<(int)((ntask + kMapTasks - 1) / kMapTasks), kMapTasks * 64, kMapSmem, st>>>(mk, a, ws);
     pgdn_scan_kernel<<<a.B * a.H, 128, 0, st>>>(a, ws);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
