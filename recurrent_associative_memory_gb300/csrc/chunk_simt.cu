@@ -101,6 +101,18 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_b
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
+// 4-byte variant (through L1); src_bytes = 0 zero-fills
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// waits for the committed groups but the newest (copies issued since stay in flight)
+__device__ __forceinline__ void cp_async_wait_but_newest() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
 
 
 // m16n8k16 bf16 mma.sync, fp32 accumulate (the bf16-input Gram's split products)
@@ -220,6 +232,52 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
     __syncthreads();
     it0 = s_ticket;
   }
+  // bf16 prep: the raw K and Q rows of a task (2 x 16 KB, row-major) and its
+  // observation noise are copied into shared memory the previous task no longer
+  // needs (the fp32 Q^T buffer once the Q image is built; the state buffer,
+  // unused in prep mode), and its process noise straight into W (dead once the
+  // Wbar image is built), so their latency hides behind the record copies.  Two
+  // groups: rows and r, then the process noise (waited with the log-decay).
+  constexpr bool kStage = PREP && sizeof(Tin) == 2;
+  auto prefetch_task = [&](long nit) {
+    int nbh, nci;
+    if (chained) {
+      nci = (int)(nit / (a.B * a.H));
+      nbh = (int)(nit % (a.B * a.H));
+    } else {
+      nbh = (int)(nit / NCk);
+      nci = (int)(nit % NCk);
+    }
+    const int nb = nbh / a.H, nh = nbh % a.H, nt0 = nci * CM, nCc = min(CM, a.T - nt0);
+    uint8_t* stg = reinterpret_cast<uint8_t*>(sQt);
+    constexpr int kPieces = 2 * CM * DK * 2 / 16;   // 16-byte pieces of K and Q
+#pragma unroll
+    for (int r = 0; r < kPieces / kThreads; ++r) {
+      const int e = tid + r * kThreads, which = e / (kPieces / 2), row = (e / (DK / 8)) % CM,
+                pc = e % (DK / 8);
+      const bool real = row < nCc;
+      const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(which ? a.q : a.k) +
+                                 (real ? tok_index(a, nb, nt0 + row, nh) * DK + pc * 8 : 0);
+      cp_async16(stg + which * (CM * DK * 2) + row * (DK * 2) + pc * 16, src, real ? 16 : 0);
+    }
+    if (tid < CM) {
+      const bool real = tid < nCc;
+      cp_async4(sS + tid, a.r + (real ? tok_index(a, nb, nt0 + tid, nh) : 0), real ? 4 : 0);
+    }
+    cp_async_commit();
+    constexpr int kGatePieces = CM * DK / 4;   // 16-byte pieces of omega
+#pragma unroll
+    for (int r = 0; r < kGatePieces / kThreads; ++r) {
+      const int e4 = tid + r * kThreads, i = (4 * e4) / DK, c = (4 * e4) % DK;
+      const bool real = i < nCc;
+      const long ti = (real ? tok_index(a, nb, nt0 + i, nh) : tok_index(a, nb, 0, nh)) * DK + c;
+      cp_async16(sW + 4 * e4, a.omega + ti, real ? 16 : 0);
+    }
+    cp_async_commit();
+  };
+  if constexpr (kStage) {
+    if (it0 < kIters) prefetch_task(it0);
+  }
   for (long it = it0; it < kIters; it = chained ? s_ticket : it + (PREP ? gridDim.x : 1)) {
     int t0 = (int)it * CM;
     int ci = 0;       // chunk of a prep task
@@ -241,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       if (!chained && tid < DK) carry = reinterpret_cast<const float*>(rec + rkP0)[tid];
     }
     const int Cc = min(CM, a.T - t0);
+    if constexpr (kStage) cp_async_wait_but_newest();   // this task's staged rows and r
     __syncthreads();
     if (chained && tid == 0) s_ticket = atomicAdd(chain + kIters, 1u);
 
@@ -253,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         const bool real = i < Cc;
         const long ti = (real ? tok_index(a, b, t0 + i, h) : tok_index(a, b, 0, h)) * DK + c;
         cp_async16(sX + 4 * e4, a.log_alpha + ti, real ? 16 : 0);
-        cp_async16(sW + 4 * e4, a.omega + ti, real ? 16 : 0);
+        if (!kStage) cp_async16(sW + 4 * e4, a.omega + ti, real ? 16 : 0);   // staged: already in flight
       }
     }
 
@@ -266,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         sg[i] = real ? a.log_alpha[ti] : 0.f;
         sb1[i] = real ? a.eta[ti] : 0.f;
       } else {
-        sb1[i] = real ? a.r[ti] : 1.f;
+        sb1[i] = real ? (kStage ? sS[i] : a.r[ti]) : 1.f;
         sb2[i] = a.info_scale / sb1[i];   // information scale over r, used by the variance scan
       }
       if (pgdn) {
@@ -285,15 +344,30 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       const int sub = tid % TPR;
       constexpr int kPasses = CM / RPP;
       float kvp[kPasses][8], qvp[kPasses][8];   // every pass's loads in flight first
+      if constexpr (kStage) {   // from the staged rows (zero past the end)
+        const unsigned short* stK = reinterpret_cast<const unsigned short*>(sQt);
+        const unsigned short* stQ = stK + CM * DK;
 #pragma unroll
-      for (int pz = 0; pz < kPasses; ++pz) {
-        const int i = pz * RPP + tid / TPR;
-        const bool real = i < Cc;
-        const long base = real ? tok_index(a, b, t0 + i, h) * DK : 0;
+        for (int pz = 0; pz < kPasses; ++pz) {
+          const int i = pz * RPP + tid / TPR;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          kvp[pz][e] = real ? ldg_in<Tin>(a.k, base + sub + TPR * e) : 0.f;
-          qvp[pz][e] = real ? ldg_in<Tin>(a.q, base + sub + TPR * e) : 0.f;
+          for (int e = 0; e < 8; ++e) {
+            kvp[pz][e] = __uint_as_float(static_cast<uint32_t>(stK[i * DK + sub + TPR * e]) << 16);
+            qvp[pz][e] = __uint_as_float(static_cast<uint32_t>(stQ[i * DK + sub + TPR * e]) << 16);
+          }
+        }
+        __syncthreads();   // the staging area is the Q^T buffer written below
+      } else {
+#pragma unroll
+        for (int pz = 0; pz < kPasses; ++pz) {
+          const int i = pz * RPP + tid / TPR;
+          const bool real = i < Cc;
+          const long base = real ? tok_index(a, b, t0 + i, h) * DK : 0;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            kvp[pz][e] = real ? ldg_in<Tin>(a.k, base + sub + TPR * e) : 0.f;
+            qvp[pz][e] = real ? ldg_in<Tin>(a.q, base + sub + TPR * e) : 0.f;
+          }
         }
       }
 #pragma unroll
@@ -821,6 +895,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       }
       umma::fence_proxy_async();
       __syncthreads();
+      {   // the next task's rows: the Q^T buffer is dead once the Q image is built
+        const long nit = chained ? s_ticket : it + gridDim.x;
+        if (nit < kIters) prefetch_task(nit);
+      }
       if (tid == 0) {
         umma::bulk_store(rec + rbWp, stX, 32768);
         umma::bulk_commit();
