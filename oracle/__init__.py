@@ -9,8 +9,8 @@ holds none of the method's arithmetic.
 
 Modules
 -------
-recurrence  Tokenwise recurrence (the plain definition) for GDN, KLA, PGDN and
-            Diagonal KDN, one token at a time, in float64.
+recurrence  Tokenwise recurrence (the plain definition) for GDN, KLA, PGDN,
+            Diagonal KDN, KDA and PKDA, one token at a time, in float64.
 chunkwise   A naive chunkwise-parallel restatement (triangular system per
             chunk), written independently of ``recurrence`` as a cross-check.
 ridge       Side oracles fixed by closed forms: exact ridge regression (ATQ),

@@ -133,11 +133,11 @@ def chunkwise(q, k, v, log_alpha, variant: str, chunk: int, *, eta=None,
 
     o = np.zeros((B, T, H, dv))
     S_fin = np.zeros((B, H, dk, dv))
-    aux_fin = None if variant in ("gdn", "kla") else np.zeros((B, H, dk))
+    aux_fin = None if variant in ("gdn", "kla", "kda") else np.zeros((B, H, dk))
     for b in range(B):
         for h in range(H):
             S = np.zeros((dk, dv)) if S0 is None else np.array(S0[b, h], dtype=np.float64)
-            if variant == "pgdn":
+            if variant in ("pgdn", "pkda"):
                 aux = np.zeros(dk) if aux0 is None else np.array(aux0[b, h], dtype=np.float64)
             elif variant == "kdn":
                 aux = np.ones(dk) if aux0 is None else np.array(aux0[b, h], dtype=np.float64)
@@ -148,11 +148,11 @@ def chunkwise(q, k, v, log_alpha, variant: str, chunk: int, *, eta=None,
                 g = np.cumsum(la, axis=0)
                 if not per_channel:
                     g = np.repeat(g[:, None], dk, axis=1)
-                if variant == "gdn":
+                if variant in ("gdn", "kda"):
                     w = eta[b, t0:t1, h][:, None] * kc
                 elif variant == "kla":
                     w = (eta[b, t0:t1, h] / (np.sum(kc * kc, axis=1) + eps))[:, None] * kc
-                elif variant == "pgdn":
+                elif variant in ("pgdn", "pkda"):
                     A = pgdn_stat_chunk(aux, kc * kc, np.log(alphaP[b, t0:t1, h]), betaP[b, t0:t1, h])
                     aux = A[-1]
                     w = eta[b, t0:t1, h][:, None] * pgdn_squash(A, mu[h], x, log_floor) * kc

@@ -12,19 +12,22 @@ every token to storing a map", the displayed equation and the table under it):
     o_t  = S_t^T q_t                    (read after the write)
 
 with S in R^{dk x dv}, D_t = alpha_t I (GDN, KLA, PGDN) or diag(alpha_t)
-(Diagonal KDN), and a per-variant write vector w_t:
+(KDA, PKDA, Diagonal KDN), and a per-variant write vector w_t:
 
     GDN   w = eta k                                 (KLA notes section 1.1)
+    KDA   w = eta k, D_t = diag(alpha_t)            (KDN notes section 1, table)
     KLA   w = eta k / (||k||^2 + eps)               (KLA notes Eq. (3), Alg. 1)
     PGDN  A_t = alphaP A_{t-1} + betaP (k*k)        (PDN notes Eq. (9))
           r = log max(A_t, floor) - mu ; s = r / (1 + |r|)
           B = exp(-log(x) s) ;  w = beta (B * k)
+    PKDA  the PGDN write key with D_t = diag(alpha_t)   (PDN notes section 2.5)
     KDN   p^ = alpha^2 * p_{t-1} + omega            (KDN notes Eq. (23))
           kappa = p^ * k / (r + sum(p^ k^2)) ; w = kappa
           p_t = p^ / (1 + (mu/r) k*k * p^)          (KDN notes Eqs. (60)-(65))
 
 Layouts follow the library: tokens are [B, T, H, d]; per-token scalars are
-[B, T, H]; per-channel gates (KDN log-alpha and omega) are [B, T, H, dk]; the
+[B, T, H]; per-channel gates (KDA, PKDA and KDN log-alpha, KDN omega) are
+[B, T, H, dk]; the
 state is [B, H, dk, dv].  Everything is computed in float64.
 """
 
@@ -32,7 +35,7 @@ from __future__ import annotations
 
 import numpy as np
 
-VARIANTS = ("gdn", "kla", "pgdn", "kdn")
+VARIANTS = ("gdn", "kla", "pgdn", "kdn", "kda", "pkda")
 
 
 def l2normalize(x: np.ndarray, floor: float = 1e-30) -> np.ndarray:
@@ -129,11 +132,11 @@ def tokenwise(q, k, v, log_alpha, variant: str, *, eta=None, eps: float = 1e-6,
 
     variant  one of VARIANTS.
     eta      [B,T,H]: GDN/KLA eta, PGDN beta.
-    alphaP, betaP [B,T,H]; mu [H]          PGDN statistic gates and centre.
+    alphaP, betaP [B,T,H]; mu [H]          PGDN / PKDA statistic gates and centre.
     omega [B,T,H,dk]; r [B,T,H]            KDN process / observation noise.
-    log_alpha [B,T,H] (scalar decay) or [B,T,H,dk] (KDN).
-    S0 [B,H,dk,dv] (None = 0); aux0 [B,H,dk]: PGDN A_0 (None = 0) or KDN p_0
-    (None = 1).
+    log_alpha [B,T,H] (scalar decay) or [B,T,H,dk] (KDA, PKDA, KDN).
+    S0 [B,H,dk,dv] (None = 0); aux0 [B,H,dk]: PGDN / PKDA A_0 (None = 0) or
+    KDN p_0 (None = 1).
     Returns (o [B,T,H,dv], S_T [B,H,dk,dv], aux_T [B,H,dk] or None); with
     ``return_trace`` also a dict of per-token write vectors and residuals.
     """
@@ -151,7 +154,7 @@ def tokenwise(q, k, v, log_alpha, variant: str, *, eta=None, eps: float = 1e-6,
 
     S = np.zeros((B, H, dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
     aux = None
-    if variant == "pgdn":
+    if variant in ("pgdn", "pkda"):
         aux = np.zeros((B, H, dk)) if aux0 is None else np.array(aux0, dtype=np.float64)
     elif variant == "kdn":
         aux = np.ones((B, H, dk)) if aux0 is None else np.array(aux0, dtype=np.float64)
@@ -161,11 +164,11 @@ def tokenwise(q, k, v, log_alpha, variant: str, *, eta=None, eps: float = 1e-6,
     for t in range(T):
         kt, qt, vt = k[:, t], q[:, t], v[:, t]
         alpha = np.exp(log_alpha[:, t])
-        if variant == "gdn":
+        if variant in ("gdn", "kda"):
             w = gdn_write(kt, eta[:, t])
         elif variant == "kla":
             w = kla_write(kt, eta[:, t], eps)
-        elif variant == "pgdn":
+        elif variant in ("pgdn", "pkda"):
             aux = pgdn_stat_update(aux, kt, alphaP[:, t], betaP[:, t])
             Bscale = pgdn_squash(aux, mu[None, :, None], x, log_floor)
             w = eta[:, t][..., None] * (Bscale * kt)

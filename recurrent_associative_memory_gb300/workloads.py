@@ -24,6 +24,12 @@ contexts up to 64K) with these distributions:
   as for PGDN; per-channel log alpha = -softplus(N(0,1)+2); omega =
   softplus(N(-3,1)) per channel; r = softplus(N(0,1)) per (b,t,h); p_0 = 1;
   information scale 1.
+* ``kda_bf16``         KDA (per-channel decay, w = eta k), bf16, B=4 H=16
+  T=8192 d=128 C=64; q,k,v as for PGDN; eta = sigmoid(N(0,1)); per-channel
+  log alpha = -softplus(N(0,1)+2).
+* ``pkda_bf16``        PKDA (the PGDN write key with per-channel decay), bf16,
+  B=4 H=16 T=4096 d=128 C=64; the PGDN gates, then per-channel log alpha as
+  for KDA.
 * ``kla_prefill_bf16`` KLA, bf16, B=1 H=16 T=65536 d=128, inputs as
   ``gdn_kla_bf16``.
 * ``kla_decode_bf16``  KLA decode steps at batch 256, H=16, d=128; fresh
@@ -74,6 +80,10 @@ WORKLOADS = {
                           k_l2norm=True, seed=1002),
     "kdn_bf16": Workload("kdn_bf16", ("kdn",), 4, 8192, 16, 128, 128, 64, "bf16",
                          k_l2norm=True, seed=1003),
+    "kda_bf16": Workload("kda_bf16", ("kda",), 4, 8192, 16, 128, 128, 64, "bf16",
+                         k_l2norm=True, seed=1005),
+    "pkda_bf16": Workload("pkda_bf16", ("pkda",), 4, 4096, 16, 128, 128, 64, "bf16",
+                          k_l2norm=True, seed=1006),
     "kla_prefill_bf16": Workload("kla_prefill_bf16", ("kla",), 1, 65536, 16, 128, 128, 64,
                                  "bf16", key_dist="lognormal_scaled", seed=1004),
     "kla_decode_bf16": Workload("kla_decode_bf16", ("kla",), 256, 1, 16, 128, 128, 64, "bf16",
@@ -122,6 +132,15 @@ def _draw_gates(gen, wl: Workload, variant: str, B, T):
         g["log_alpha"] = -_softplus(torch.randn(B, T, H, dk, generator=gen) + 2.0)
         g["omega"] = _softplus(torch.randn(B, T, H, dk, generator=gen) - 3.0)
         g["r"] = _softplus(torch.randn(B, T, H, generator=gen))
+    elif variant == "kda":
+        g["eta"] = torch.sigmoid(torch.randn(B, T, H, generator=gen))
+        g["log_alpha"] = -_softplus(torch.randn(B, T, H, dk, generator=gen) + 2.0)
+    elif variant == "pkda":
+        g["alphaP"] = torch.sigmoid(torch.randn(B, T, H, generator=gen) + 3.0)
+        g["betaP"] = torch.sigmoid(torch.randn(B, T, H, generator=gen))
+        g["mu"] = torch.exp(0.5 * torch.randn(H, generator=gen))
+        g["eta"] = torch.sigmoid(torch.randn(B, T, H, generator=gen))
+        g["log_alpha"] = -_softplus(torch.randn(B, T, H, dk, generator=gen) + 2.0)
     else:
         raise ValueError(variant)
     return g

@@ -69,13 +69,15 @@ def random_inputs(variant, B=2, T=37, H=2, dk=8, dv=6, seed=0, decay_shift=0.5):
              v=r.standard_normal((B, T, H, dv)))
     sig = lambda x: 1 / (1 + np.exp(-x))  # noqa: E731
     sp = lambda x: np.log1p(np.exp(x))  # noqa: E731
-    if variant in ("gdn", "kla", "pgdn"):
+    if variant in ("gdn", "kla", "pgdn", "kda", "pkda"):
         d["eta"] = sig(r.standard_normal((B, T, H)))
         d["log_alpha"] = -sp(r.standard_normal((B, T, H)) + decay_shift)
-    if variant == "pgdn":
+    if variant in ("pgdn", "pkda"):
         d["alphaP"] = sig(r.standard_normal((B, T, H)) + 3)
         d["betaP"] = sig(r.standard_normal((B, T, H)))
         d["mu"] = np.exp(0.5 * r.standard_normal(H))
+    if variant in ("kda", "pkda"):   # per-channel decay
+        d["log_alpha"] = -sp(r.standard_normal((B, T, H, dk)) + decay_shift)
     if variant == "kdn":
         d["log_alpha"] = -sp(r.standard_normal((B, T, H, dk)) + decay_shift)
         d["omega"] = sp(r.standard_normal((B, T, H, dk)) - 3)
@@ -313,6 +315,47 @@ def test_gdn_without_decay_is_deltanet_contraction():
         np.testing.assert_allclose(d["v"][0, t, 0] - S_t.T @ k[t], (1 - beta * k[t] @ k[t]) * e, atol=1e-11)
 
 
+# ------------------------------------------------------------------ KDA / PKDA reductions
+
+@pytest.mark.parametrize("pair", [("kda", "gdn"), ("pkda", "pgdn")])
+def test_per_channel_decay_uniform_across_channels_reduces(pair):
+    """KDA with alpha_t the same on every channel is Gated DeltaNet (KDN notes
+    section 1, table: D_t = diag(alpha_t) vs alpha_t I, same write beta k), and
+    PKDA so reduces to PGDN (PDN notes section 2.5, the unified form)."""
+    vec, sca = pair
+    d = random_inputs(vec, B=2, T=29, H=2, dk=5, dv=3, seed=21)
+    la = d["log_alpha"][..., 0]
+    d["log_alpha"] = np.repeat(la[..., None], 5, axis=-1)
+    s = dict(d, log_alpha=la)
+    r = rng(22)
+    S0 = r.standard_normal((2, 2, 5, 3))
+    aux0 = r.uniform(0, 2, (2, 2, 5)) if vec == "pkda" else None
+    for fn in (oracle.tokenwise, lambda *a, **k: oracle.chunkwise(*a, chunk=8, **k)):
+        o1, S1, a1 = call(fn, vec, d, S0=S0, aux0=aux0, q_l2norm=True)
+        o2, S2, a2 = call(fn, sca, s, S0=S0, aux0=aux0, q_l2norm=True)
+        np.testing.assert_allclose(o1, o2, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(S1, S2, rtol=1e-12, atol=1e-13)
+        if a1 is not None:
+            np.testing.assert_allclose(a1, a2, rtol=1e-13)
+
+
+@pytest.mark.parametrize("variant", ["kda", "pkda"])
+def test_per_channel_decay_scales_key_rows(variant):
+    """With nothing written (eta = 0) the memory only decays: S_t = D_t ... D_1 S_0
+    with D = diag(alpha) acting on the key index (KDN notes section 1), so the
+    read is o_t[v] = sum_i q_t[i] prod_{s <= t} alpha_s[i] S_0[i, v].  dk != dv,
+    so decaying the value index instead fails."""
+    d = random_inputs(variant, B=1, T=11, H=1, dk=4, dv=6, seed=23)
+    d["eta"] = np.zeros_like(d["eta"])
+    S0 = rng(24).standard_normal((1, 1, 4, 6))
+    cum = np.exp(np.cumsum(d["log_alpha"][0, :, 0], axis=0))          # [T, dk]
+    expect = np.einsum("ti,ti,iv->tv", d["q"][0, :, 0], cum, S0[0, 0])
+    for fn in (oracle.tokenwise, lambda *a, **k: oracle.chunkwise(*a, chunk=4, **k)):
+        o, S, _ = call(fn, variant, d, S0=S0)
+        np.testing.assert_allclose(o[0, :, 0], expect, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(S[0, 0], cum[-1][:, None] * S0[0, 0], rtol=1e-12, atol=1e-14)
+
+
 # ------------------------------------------------------------------ P8: tokenwise == chunkwise
 
 CASES = [  # (T, dk, dv, chunk)
@@ -327,8 +370,10 @@ def test_tokenwise_equals_chunkwise(variant, T, dk, dv, chunk):
     d = random_inputs(variant, B=1, T=T, H=2, dk=dk, dv=dv, seed=T * 31 + dk)
     r = rng(T)
     S0 = r.standard_normal((1, 2, dk, dv))
-    aux0 = {"pgdn": r.uniform(0, 2, (1, 2, dk)), "kdn": r.uniform(0.5, 1.5, (1, 2, dk))}.get(variant)
-    kw = dict(S0=S0, aux0=aux0, q_l2norm=True, k_l2norm=(variant in ("pgdn", "kdn")), eps=1e-6)
+    aux0 = {"pgdn": r.uniform(0, 2, (1, 2, dk)), "pkda": r.uniform(0, 2, (1, 2, dk)),
+            "kdn": r.uniform(0.5, 1.5, (1, 2, dk))}.get(variant)
+    kw = dict(S0=S0, aux0=aux0, q_l2norm=True, k_l2norm=(variant in ("pgdn", "pkda", "kdn")),
+              eps=1e-6)
     o1, S1, a1 = call(oracle.tokenwise, variant, d, **kw)
     o2, S2, a2 = call(oracle.chunkwise, variant, d, chunk=chunk, **kw)
     scale = max(1.0, np.abs(o1).max())
