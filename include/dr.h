@@ -11,8 +11,8 @@
  *     o_t  = S_t^T q_t                       (read after the write)
  *
  * S_t is a dk x dv fp32 matrix per (batch, head).  D_t = alpha_t I for GDN, KLA
- * and PGDN, diag(alpha_t) for Diagonal KDN; alpha = exp(log_alpha).  The write
- * vector w_t per variant:
+ * and PGDN, diag(alpha_t) (scaling the rows of S) for Diagonal KDN, KDA and
+ * PKDA; alpha = exp(log_alpha).  The write vector w_t per variant:
  *
  *   DR_GDN   w = eta k                        (KLA notes section 1.1)
  *   DR_KLA   w = eta k / (||k||^2 + eps)      (KLA notes Eq. (3), Algorithm 1)
@@ -22,6 +22,9 @@
  *   DR_KDN   p^ = alpha^2 p_{t-1} + omega;  kappa = p^ k / (r + sum p^ k^2);  w = kappa;
  *            p_t = p^ / (1 + (info_scale / r) k*k p^)
  *                                             (KDN notes Eqs. (23)-(30), (60)-(65))
+ *   DR_KDA   w = eta k with per-channel decay (KDN notes section 1, table)
+ *   DR_PKDA  the DR_PGDN write key with per-channel decay
+ *                                             (Preconditioned DeltaNet notes section 2.5)
  *
  * q and k are L2-normalised first when the corresponding flag is set
  * (q / max(||q||, 1e-30)); KLA reads out with the normalised query (KLA notes
@@ -29,9 +32,9 @@
  *
  * Layouts (row-major, innermost index last):
  *   q, k     [B, T, H, dk]      v, out [B, T, H, dv]     (decode: T absent)
- *   log_alpha [B, T, H]  (KDN: [B, T, H, dk])
+ *   log_alpha [B, T, H]  (KDN, KDA, PKDA: [B, T, H, dk])
  *   eta, alphaP, betaP, r [B, T, H];  omega [B, T, H, dk];  mu [H]
- *   state    [B, H, dk, dv] fp32;  aux (PGDN A / KDN p) [B, H, dk] fp32
+ *   state    [B, H, dk, dv] fp32;  aux (PGDN / PKDA A, KDN p) [B, H, dk] fp32
  * q/k/v/out are fp32 (DR_FP32) or bf16 (DR_BF16); every gate and state is fp32.
  *
  * Ownership: the caller owns every buffer; all pointers are device pointers
@@ -58,7 +61,7 @@ struct CUstream_st;
 /* Same type as cudaStream_t; NULL is the legacy default stream. */
 typedef struct CUstream_st *dr_stream_t;
 
-typedef enum { DR_GDN = 0, DR_KLA = 1, DR_PGDN = 2, DR_KDN = 3 } dr_variant;
+typedef enum { DR_GDN = 0, DR_KLA = 1, DR_PGDN = 2, DR_KDN = 3, DR_KDA = 4, DR_PKDA = 5 } dr_variant;
 
 typedef enum { DR_FP32 = 0, DR_BF16 = 1 } dr_dtype;
 
@@ -82,16 +85,16 @@ typedef struct dr_params {
   int dtype;               /* dr_dtype of q, k, v and out                             */
   int q_l2norm;            /* 1: normalise q before reading out                       */
   int k_l2norm;            /* 1: normalise k before the residual and the write        */
-  const float *eta;        /* GDN/KLA eta, PGDN beta: [B,T,H] (decode [B,H])          */
-  const float *alphaP;     /* PGDN statistic decay  [B,T,H] (decode [B,H])            */
-  const float *betaP;      /* PGDN statistic gain   [B,T,H] (decode [B,H])            */
-  const float *mu;         /* PGDN per-head centre  [H]                               */
+  const float *eta;        /* GDN/KLA/KDA eta, PGDN/PKDA beta: [B,T,H] (decode [B,H]) */
+  const float *alphaP;     /* PGDN/PKDA statistic decay [B,T,H] (decode [B,H])        */
+  const float *betaP;      /* PGDN/PKDA statistic gain  [B,T,H] (decode [B,H])        */
+  const float *mu;         /* PGDN/PKDA per-head centre [H]                           */
   float x;                 /* PGDN bound, B in [1/x, x]; default 1.5                  */
   float log_floor;         /* PGDN guard: ln max(A, log_floor); default 1e-12         */
   const float *omega;      /* KDN process noise     [B,T,H,dk] (decode [B,H,dk])      */
   const float *r;          /* KDN observation noise [B,T,H] (decode [B,H]), > 0       */
   float info_scale;        /* KDN information scaling mu; default 1 (strict update)   */
-  const float *aux_init;   /* dr_chunk_fwd: PGDN A_0 / KDN p_0 [B,H,dk]; NULL => 0 / 1 */
+  const float *aux_init;   /* dr_chunk_fwd: PGDN/PKDA A_0, KDN p_0 [B,H,dk]; NULL => 0, 1 */
   float *aux_final;        /* dr_chunk_fwd: final A / p [B,H,dk]; NULL => not written */
   void *workspace;         /* dr_chunk_fwd: caller-owned device scratch, 256-byte     */
   size_t workspace_bytes;  /* aligned, or NULL (see dr_chunk_fwd_workspace_bytes)     */

@@ -197,7 +197,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool kdn = (a.variant == DR_KDN);
   const bool pgdn = (a.variant == DR_PGDN);
-  const bool explicit_w = kdn || pgdn;       // W is not a per-row multiple of K
+  const bool kda = (a.variant == DR_KDA);
+  const bool pkda = (a.variant == DR_PKDA);
+  const bool perchan = kdn || kda || pkda;   // per-channel decay D = diag(alpha)
+  const bool pstat = pgdn || pkda;           // the PGDN key statistic and write key
+  // W is formed explicitly (not as a per-row multiple of K in the Gram's readout)
+  const bool explicit_w = perchan || pgdn;
 
   // KDN factor vectors inside sF
   float* fOff = sF;                       // [6][DK]   exp(g_b(I) - g_e(J)), J < I
@@ -217,10 +222,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
   const int my_c = pgdn ? tid - 32 : tid;
   float carry = 0.f;
   if (my_c >= 0 && my_c < DK) {
-    if (pgdn) carry = a.aux0 ? a.aux0[(long)bh * DK + my_c] : 0.f;
+    if (pstat) carry = a.aux0 ? a.aux0[(long)bh * DK + my_c] : 0.f;
     if (kdn) carry = a.aux0 ? a.aux0[(long)bh * DK + my_c] : 1.f;
   }
-  const float mu_h = pgdn ? a.mu[h] : 0.f;
+  const float mu_h = pstat ? a.mu[h] : 0.f;
   bool bad = false;
 
   const long kIters = PREP ? (long)a.B * a.H * NCk : NCk;
@@ -303,8 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
     __syncthreads();
     if (chained && tid == 0) s_ticket = atomicAdd(chain + kIters, 1u);
 
-    if (kdn) {   // per-channel log-decay and process noise, row-major [i][c], copied
-                 // asynchronously (16-byte pieces, zero-filled past the end) under the loads below
+    if (perchan) {   // per-channel log-decay (and KDN process noise), row-major [i][c],
+                     // copied asynchronously (16-byte pieces, zero past the end) under the loads
       constexpr int kPieces = CM * DK / 4;   // 16-byte pieces per array
 #pragma unroll
       for (int r = 0; r < kPieces / kThreads; ++r) {
@@ -312,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         const bool real = i < Cc;
         const long ti = (real ? tok_index(a, b, t0 + i, h) : tok_index(a, b, 0, h)) * DK + c;
         cp_async16(sX + 4 * e4, a.log_alpha + ti, real ? 16 : 0);
-        if (!kStage) cp_async16(sW + 4 * e4, a.omega + ti, real ? 16 : 0);   // staged: already in flight
+        if (kdn && !kStage) cp_async16(sW + 4 * e4, a.omega + ti, real ? 16 : 0);   // staged: in flight
       }
     }
 
@@ -322,13 +327,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       const bool real = i < Cc;
       const long ti = real ? tok_index(a, b, t0 + i, h) : 0;
       if (!kdn) {
-        sg[i] = real ? a.log_alpha[ti] : 0.f;
+        if (!perchan) sg[i] = real ? a.log_alpha[ti] : 0.f;
         sb1[i] = real ? a.eta[ti] : 0.f;
       } else {
         sb1[i] = real ? (kStage ? sS[i] : a.r[ti]) : 1.f;
         sb2[i] = a.info_scale / sb1[i];   // information scale over r, used by the variance scan
       }
-      if (pgdn) {
+      if (pstat) {
         sb2[i] = real ? a.alphaP[ti] : 1.f;
         sb3[i] = real ? a.betaP[ti] : 0.f;
       }
@@ -409,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
 #pragma unroll
       for (int r = 0; r < CM * NV / kThreads; ++r) sV[tid + r * kThreads] = vv[r];
     }
-    if (kdn) cp_async_wait_all();
+    if (perchan) cp_async_wait_all();
     if (chained && ci > 0 && tid == 0 && !chain_wait(chain + ri, chain + kIters + 1, kChainWaitNs))
       set_status(DR_ERR_TIMEOUT);
     __syncthreads();
@@ -418,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
                       : __ldcg(reinterpret_cast<const float*>(rec + rkP0) + tid);
 
     // ---- 3. cumulative decay and write vectors
-    if (!kdn) {
+    if (!perchan) {
       if (warp == 0) {  // inclusive scan of log-alpha over 64 tokens, 2 per lane
         const float x0 = sg[2 * lane], x1 = sg[2 * lane + 1];
         float s = x0 + x1;
@@ -456,8 +461,49 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         carry = A;
       }
       __syncthreads();
-    } else {
+    } else if (!kdn) {
+      // KDA / PKDA: channel c's cumulative log-decay (thread c), then the write
+      // vectors: eta k^ (KDA), or the PGDN statistic scan carried across chunks
+      // and w = eta B(A) . k^ (PKDA)
       if (tid < DK) {
+        const int c = tid;
+        float g = 0.f;
+        for (int i0 = 0; i0 < CM; i0 += 8) {
+          float la[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) la[e] = sX[(i0 + e) * DK + c];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            g += la[e];
+            sX[(i0 + e) * DK + c] = g;
+          }
+        }
+        float A = carry;
+        for (int i0 = 0; i0 < CM; i0 += 8) {
+          const float4 k0 = *reinterpret_cast<const float4*>(sKt + c * CS + i0);
+          const float4 k1 = *reinterpret_cast<const float4*>(sKt + c * CS + i0 + 4);
+          const float kv[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+          float w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float scale = 1.f;
+            if (pkda) {
+              A = sb2[i0 + e] * A + sb3[i0 + e] * kv[e] * kv[e];
+              const float rr = logf(fmaxf(A, a.log_floor)) - mu_h;
+              scale = expf(-a.ln_x * __fdividef(rr, 1.f + fabsf(rr)));
+            }
+            w[e] = sb1[i0 + e] * scale * kv[e];
+            sW[(i0 + e) * DK + c] = w[e];
+          }
+          *reinterpret_cast<float4*>(sWt + c * CS + i0) = make_float4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<float4*>(sWt + c * CS + i0 + 4) = make_float4(w[4], w[5], w[6], w[7]);
+        }
+        if (pkda) carry = A;
+      }
+      __syncthreads();
+    }
+    if (perchan) {
+      if (kdn && tid < DK) {
         // variance scan of channel c in homogeneous form: (n, d) <- M_t (n, d) with
         // M_t = [[a^2, w], [u a^2, 1 + u w]] (KDN notes section 6); p^_t = n_t / d_{t-1};
         // the pair is rescaled by a power of two (exact) every 8 tokens.
@@ -497,9 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
           }
         }
       }
-      __syncthreads();
+      if (kdn) __syncthreads();
       if (chained && tid == 0 && ci + 1 < NCk) st_release_gpu(chain + ri + 1, 1u);
-      {   // z_i = sum_c p^_ic k_ic^2: warp w takes rows 8w .. 8w + 7 (keys read as two
+      if (kdn) {   // z_i = sum_c p^_ic k_ic^2: warp w takes rows 8w .. 8w + 7 (keys read as two
           // 16-byte pieces per channel), all partial sums first, then the eight
           // reductions side by side
         constexpr int kRows = CM / (kThreads / 32);
@@ -524,11 +570,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
             sz[i0 + r] = 1.f / (sb1[i0 + r] + z[r]);
         }
       }
-      __syncthreads();
+      if (kdn) __syncthreads();
       // thread (channel c, tokens 4 i4 .. 4 i4 + 3): 16-byte accesses to the token-minor
       // buffers, consecutive channels across lanes in the token-major one
 #pragma unroll 2
-      for (int e4 = tid; e4 < CM * DK / 4; e4 += kThreads) {
+      for (int e4 = tid; kdn && e4 < CM * DK / 4; e4 += kThreads) {
         const int c = e4 % DK, i0 = 4 * (e4 / DK);
         const float4 k4 = *reinterpret_cast<const float4*>(sKt + c * CS + i0);
         const float kx[4] = {k4.x, k4.y, k4.z, k4.w};
@@ -601,8 +647,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         while ((I + 1) * (I + 2) / 2 <= pr) ++I;           // pair pr -> (I, J), J <= I
         const int J = pr - I * (I + 1) / 2;
         const float* Xt = isq ? sQt : sKt;
-        const float* fk = (kdn && J == I) ? fDa + I * DK : sOne;
-        const float* fw = kdn ? ((J < I) ? fOff + pair_index(I, J) * DK : fDb + I * DK) : sOne;
+        const float* fk = (perchan && J == I) ? fDa + I * DK : sOne;
+        const float* fw = perchan ? ((J < I) ? fOff + pair_index(I, J) * DK : fDb + I * DK) : sOne;
         const int ra = 16 * I + g, cb = 16 * J + g;
         float d[2][4], dl[2][4], dr[2][4];
 #pragma unroll
@@ -668,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
           for (int x = 0; x < 4; ++x) {
             const int i = 16 * I + g + 8 * (x >> 1), j = 16 * J + 8 * h + 2 * t + (x & 1);
             float v = d[h][x] + (dl[h][x] + dr[h][x]);
-            if (!kdn) {
+            if (!perchan) {
               v *= expf(fminf(sg[i] - sg[j], 0.f));
               if (!explicit_w) v *= sb1[j];
             }
@@ -691,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
     }
 
     // ---- 5. operands of the carry: Gamma.K, Gamma.Q, exp(g_C - g_j).W, gamma_C
-    if (kdn) {   // one channel x 4 tokens of a sub-chunk per thread (16-byte accesses)
+    if (perchan) {   // one channel x 4 tokens of a sub-chunk per thread (16-byte accesses)
 #pragma unroll 2
       for (int e4 = tid; e4 < CM * DK / 4; e4 += kThreads) {
         const int c = e4 % DK, i0 = 4 * (e4 / DK);
@@ -1028,7 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
           const int c = 4 * cb + x;
-          const float gcf = kdn ? sgC[c] : sgC[0];
+          const float gcf = perchan ? sgC[c] : sgC[0];
           const float4 old = *reinterpret_cast<const float4*>(sS + c * NV + 4 * tv);
           s4[x][0] = gcf * old.x; s4[x][1] = gcf * old.y; s4[x][2] = gcf * old.z; s4[x][3] = gcf * old.w;
         }
@@ -1064,7 +1110,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       if (a.check_finite) bad |= !finite_f(v);
     }
   }
-  if (a.aux && tile == 0 && (pgdn || kdn) && my_c >= 0 && my_c < DK)
+  if (a.aux && tile == 0 && (pstat || kdn) && my_c >= 0 && my_c < DK)
     a.aux[(long)bh * DK + my_c] = carry;
   if (bad) set_status(DR_ERR_NONFINITE);
 }

@@ -8,7 +8,8 @@
 //   1. issue the 128-bit streaming loads of S (they fly while 2-3 run);
 //   2. load q, k, v and the gates; L2-normalise; form the decay d and the write
 //      vector w for the variant (KLA notes Algorithm 1; PDN notes section 2.5,
-//      two states A and S; KDN notes section 2.2, predict -> gain -> update);
+//      two states A and S; KDN notes section 2.2, predict -> gain -> update;
+//      KDA / PKDA: the GDN / PGDN write under per-channel decay);
 //   3. one pass over S gives both S~^T k and S~^T q (S~ = D S), reduced over
 //      rows with registers + shared memory;
 //   4. e = v - S~^T k;  o = S~^T q + (w^T q) e  (= S_t^T q, read after write);
@@ -106,13 +107,14 @@ __global__ void __launch_bounds__(kDecodeThreads, (DK * DVS <= 8192) ? 4 : 2)
       }
     }
   } else if (tid < DK) {
-    d = expf(a.log_alpha[tok]);
+    const bool perchan = (a.variant == DR_KDA || a.variant == DR_PKDA);   // decay per row of S
+    d = expf(a.log_alpha[perchan ? tok * DK + tid : tok]);
     const float eta = a.eta[tok];
-    if (a.variant == DR_GDN) {
+    if (a.variant == DR_GDN || a.variant == DR_KDA) {
       w = eta * kc;
     } else if (a.variant == DR_KLA) {
       w = eta / (kk_eff + a.eps) * kc;
-    } else {  // DR_PGDN
+    } else {  // DR_PGDN, DR_PKDA
       const float A = a.alphaP[tok] * a.aux[tok * DK + tid] + a.betaP[tok] * kc * kc;
       const float rr = logf(fmaxf(A, a.log_floor)) - a.mu[h];
       const float sq = rr / (1.f + fabsf(rr));

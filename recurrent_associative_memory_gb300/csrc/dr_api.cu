@@ -34,9 +34,11 @@ int check_gates(const dr_params* gp, int variant) {
   switch (variant) {
     case DR_GDN:
     case DR_KLA:
+    case DR_KDA:
       if (!gp->eta) return DR_ERR_NULL;
       return DR_OK;
     case DR_PGDN:
+    case DR_PKDA:
       if (!gp->eta || !gp->alphaP || !gp->betaP || !gp->mu) return DR_ERR_NULL;
       if (!(gp->x > 1.f) || !(gp->log_floor > 0.f)) return DR_ERR_ARG;
       return DR_OK;
@@ -74,7 +76,7 @@ FwdArgs make_args(const void* q, const void* k, const void* v, const float* log_
   a.k_l2norm = gp->k_l2norm ? 1 : 0;
   a.check_finite = gp->check_finite ? 1 : 0;
   a.eps = eps;
-  a.ln_x = variant == DR_PGDN ? logf(gp->x) : 0.f;
+  a.ln_x = (variant == DR_PGDN || variant == DR_PKDA) ? logf(gp->x) : 0.f;
   a.log_floor = gp->log_floor;
   a.info_scale = gp->info_scale;
   return a;
@@ -146,6 +148,7 @@ int dr_chunk_fwd(const void* q, const void* k, const void* v, const float* log_a
       !aligned16(init_state) || !aligned16(final_state) || !aligned16(log_alpha))
     return DR_ERR_ALIGN;
   if (variant == DR_KDN && !aligned16(gp->omega)) return DR_ERR_ALIGN;   // copied in 16-byte pieces
+  // per-channel log-decay is copied in 16-byte pieces too (checked above)
 
   FwdArgs a = make_args(q, k, v, log_alpha, gp, variant, eps, B, T, H, dk, dv, chunk);
   a.S0 = init_state;
@@ -184,7 +187,7 @@ int dr_decode_step(const void* q, const void* k, const void* v, const float* log
   if (!(eps >= 0.f)) return DR_ERR_ARG;
   int st = check_gates(gp, variant);
   if (st != DR_OK) return st;
-  if ((variant == DR_PGDN || variant == DR_KDN) && !aux_state) return DR_ERR_NULL;
+  if ((variant == DR_PGDN || variant == DR_KDN || variant == DR_PKDA) && !aux_state) return DR_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
       !aligned16(state) || !aligned16(aux_state))
     return DR_ERR_ALIGN;

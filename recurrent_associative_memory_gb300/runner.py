@@ -58,7 +58,7 @@ def chunk_fwd(inp: dict, *, init_state=None, aux_init=None, chunk=None, want_fin
         out = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
     if want_final and final_state is None:
         final_state = torch.empty(B, H, dk, dv, dtype=torch.float32, device=q.device)
-    if want_final and aux_final is None and inp["variant"] in ("pgdn", "kdn"):
+    if want_final and aux_final is None and inp["variant"] in ("pgdn", "kdn", "pkda"):
         aux_final = torch.empty(B, H, dk, dtype=torch.float32, device=q.device)
     p = params_for(inp, aux_init=aux_init, aux_final=aux_final, check_finite=check_finite)
     if workspace is not None:

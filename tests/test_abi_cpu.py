@@ -101,6 +101,9 @@ def test_status_strings(dr):
     assert dr.dr_chunk_fwd_path(dr.DR_KLA, dr.DR_BF16, 128, 128, 64) == "tc_split"
     assert dr.dr_chunk_fwd_path(dr.DR_PGDN, dr.DR_BF16, 128, 128, 64) == "tc_split"
     assert dr.dr_chunk_fwd_path(dr.DR_KLA, dr.DR_FP32, 64, 64, 64) == "simt"
+    for vid in (dr.DR_KDA, dr.DR_PKDA):   # per-channel decay: the fused CUDA-core kernel
+        assert dr.dr_chunk_fwd_path(vid, dr.DR_BF16, 128, 128, 64) == "simt"
+        assert dr.dr_chunk_fwd_workspace_bytes(vid, 1, 4, 8192, 16, 128, 128, 64) == 0
 
 
 A = 1 << 20          # a 16-byte aligned address that is never dereferenced
@@ -120,6 +123,9 @@ def test_chunk_fwd_rejects_bad_arguments(dr):
     assert fwd(dr, eta=None) == dr.DR_ERR_NULL
     assert fwd(dr, variant=2) == dr.DR_ERR_NULL                # PGDN without alphaP/betaP/mu
     assert fwd(dr, variant=3) == dr.DR_ERR_NULL                # KDN without omega/r
+    assert fwd(dr, variant=4, eta=None) == dr.DR_ERR_NULL      # KDA without eta
+    assert fwd(dr, variant=5) == dr.DR_ERR_NULL                # PKDA without alphaP/betaP/mu
+    assert fwd(dr, variant=5, alphaP=A, betaP=A, mu=A, x=0.5) == dr.DR_ERR_ARG
     assert fwd(dr, variant=7) == dr.DR_ERR_UNSUPPORTED
     assert fwd(dr, dtype=5) == dr.DR_ERR_DTYPE
     assert fwd(dr, dk=96) == dr.DR_ERR_SHAPE
@@ -144,6 +150,7 @@ def test_decode_rejects_bad_arguments(dr):
     assert dec(state=None) == dr.DR_ERR_NULL
     assert dec(variant=2, alphaP=A, betaP=A, mu=A) == dr.DR_ERR_NULL   # aux state required
     assert dec(variant=3, omega=A, r=A) == dr.DR_ERR_NULL
+    assert dec(variant=5, alphaP=A, betaP=A, mu=A) == dr.DR_ERR_NULL   # PKDA: aux state required
     assert dec(dk=32) == dr.DR_ERR_SHAPE
     assert dec(state=MIS) == dr.DR_ERR_ALIGN
     assert dec(dtype=2) == dr.DR_ERR_DTYPE

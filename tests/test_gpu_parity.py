@@ -15,7 +15,8 @@ from recurrent_associative_memory_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-BASE = {"gdn": "gdn_kla_bf16", "kla": "gdn_kla_bf16", "pgdn": "pgdn_bf16", "kdn": "kdn_bf16"}
+BASE = {"gdn": "gdn_kla_bf16", "kla": "gdn_kla_bf16", "pgdn": "pgdn_bf16", "kdn": "kdn_bf16",
+        "kda": "kda_bf16", "pkda": "pkda_bf16"}
 
 
 @pytest.fixture(scope="module")
@@ -36,7 +37,7 @@ def random_state(inp, seed=3):
     dv = inp["v"].shape[-1]
     S0 = 0.3 * torch.randn(B, H, dk, dv, generator=g)
     aux0 = None
-    if inp["variant"] == "pgdn":
+    if inp["variant"] in ("pgdn", "pkda"):
         aux0 = torch.rand(B, H, dk, generator=g) * 2.0
     if inp["variant"] == "kdn":
         aux0 = 0.5 + torch.rand(B, H, dk, generator=g)
@@ -133,7 +134,7 @@ def test_kdn_information_scale_dk(rt):
 # ------------------------------------------------------------ decode step
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-@pytest.mark.parametrize("variant", ["gdn", "kla", "pgdn", "kdn"])
+@pytest.mark.parametrize("variant", ["gdn", "kla", "pgdn", "kdn", "kda", "pkda"])
 def test_decode_steps_match_oracle(rt, variant, dtype):
     dr, runner = rt
     inp = small_inputs(variant, dtype, B=3, T=12, H=2, seed=21)
@@ -346,6 +347,35 @@ def test_kdn_chained_variance_many_rows(rt, dtype):
     torch.cuda.synchronize()
     assert dr.dr_get_device_status() == 0
     assert torch.equal(o1, o2) and torch.equal(s1, s2) and torch.equal(a1, a2)
+
+
+# ------------------------------------------------------------ per-channel decay: KDA, PKDA
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("variant", ["kda", "pkda"])
+@pytest.mark.parametrize("T", [1, 63, 130])
+def test_per_channel_decay_variants(rt, variant, dtype, T):
+    """KDA (w = eta k, D = diag(alpha)) and PKDA (the PGDN write key under
+    per-channel decay) on the fused CUDA-core kernel: ragged lengths, nonzero
+    initial state and key statistic."""
+    inp = small_inputs(variant, dtype, B=2, T=T, H=3, seed=400 + T)
+    S0, aux0 = random_state(inp, seed=401 + T)
+    check_fwd(rt, inp, S0, aux0)
+
+
+@pytest.mark.parametrize("variant", ["kda", "pkda"])
+def test_per_channel_decay_head_dims_and_chunks(rt, variant):
+    for dk, dv, chunk in [(64, 128, 64), (128, 64, 32), (64, 64, 128)]:
+        inp = small_inputs(variant, "bf16", B=1, T=150, H=2, d=dk, dv=dv, chunk=chunk, seed=dk + dv)
+        S0, aux0 = random_state(inp, seed=dv)
+        check_fwd(rt, inp, S0, aux0, chunk=chunk)
+
+
+@pytest.mark.parametrize("name,variant", [("kda_bf16", "kda"), ("pkda_bf16", "pkda")])
+def test_per_channel_decay_workloads_sampled(rt, name, variant):
+    wl = W.WORKLOADS[name]
+    inp = W.generate(wl, variant)
+    check_fwd(rt, inp, pairs=pick_pairs(wl.B, wl.H, 2))
 
 
 # ------------------------------------------------------------ seeded random shapes, two-phase paths
