@@ -116,13 +116,14 @@ def fwd_bytes(wl, variant, with_final=True):
     el = 2 if wl.dtype == "bf16" else 4
     ht = wl.B * wl.T * wl.H
     per_ht = (2 * wl.dk + 2 * wl.dv) * el          # q, k, v, o
-    gates = {"gdn": 8, "kla": 8, "pgdn": 16, "kdn": 8 * wl.dk + 4}[variant]
+    gates = {"gdn": 8, "kla": 8, "pgdn": 16, "kdn": 8 * wl.dk + 4,
+             "kda": 4 * wl.dk + 4, "pkda": 4 * wl.dk + 12}[variant]
     total = ht * (per_ht + gates)
-    if variant == "pgdn":
+    if variant in ("pgdn", "pkda"):
         total += wl.H * 4
     if with_final:
         total += wl.B * wl.H * wl.dk * wl.dv * 4
-        if variant in ("pgdn", "kdn"):
+        if variant in ("pgdn", "kdn", "pkda"):
             total += wl.B * wl.H * wl.dk * 4
     return total
 
@@ -389,10 +390,10 @@ def main():
                                     wl.dv, wl.chunk)
         if ws is None or path not in ("tc_split", "simt_split"):
             return 1
-        # with few rows the KDN variance takes map and scan kernels first
+        # with few rows the KDN variance takes map and scan kernels first (KDA: none)
         nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
         if path == "simt_split":
-            return 2 if 3 * wl.B * wl.H >= nsm else 4
+            return 2 if (v != "kdn" or 3 * wl.B * wl.H >= nsm) else 4
         return 4 if v == "pgdn" else 2   # PGDN: statistic map and scan kernels first
     launches = args.steps * sum(kernels_per_call(v) for v in variants)
     value = job_tokens_per_s(world, args.steps, len(variants), wl.B, wl.T, total_s)

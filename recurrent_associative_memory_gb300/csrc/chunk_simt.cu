@@ -265,14 +265,14 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
                                  (real ? tok_index(a, nb, nt0 + row, nh) * DK + pc * 8 : 0);
       cp_async16(stg + which * (CM * DK * 2) + row * (DK * 2) + pc * 16, src, real ? 16 : 0);
     }
-    if (tid < CM) {
+    if (kdn && tid < CM) {
       const bool real = tid < nCc;
       cp_async4(sS + tid, a.r + (real ? tok_index(a, nb, nt0 + tid, nh) : 0), real ? 4 : 0);
     }
     cp_async_commit();
-    constexpr int kGatePieces = CM * DK / 4;   // 16-byte pieces of omega
+    constexpr int kGatePieces = CM * DK / 4;   // 16-byte pieces of omega (KDN)
 #pragma unroll
-    for (int r = 0; r < kGatePieces / kThreads; ++r) {
+    for (int r = 0; kdn && r < kGatePieces / kThreads; ++r) {
       const int e4 = tid + r * kThreads, i = (4 * e4) / DK, c = (4 * e4) % DK;
       const bool real = i < nCc;
       const long ti = (real ? tok_index(a, nb, nt0 + i, nh) : tok_index(a, nb, 0, nh)) * DK + c;
@@ -1526,8 +1526,8 @@ namespace dr {
 cudaError_t launch_carry_kdn_tc(const FwdArgs& a, void* workspace, cudaStream_t st);
 
 bool kdn_split_supported(int variant, int dtype, int dk, int dv, int chunk) {
-  return variant == DR_KDN && (dtype == DR_BF16 || dtype == DR_FP32) && dk == 128 && dv == 128 &&
-         chunk == 64;
+  return (variant == DR_KDN || variant == DR_KDA) && (dtype == DR_BF16 || dtype == DR_FP32) &&
+         dk == 128 && dv == 128 && chunk == 64;
 }
 
 size_t kdn_split_workspace_bytes(int B, int T, int H) {
@@ -1544,12 +1544,14 @@ cudaError_t launch_kdn_split(const FwdArgs& a, int dtype, void* workspace, cudaS
   // variance scan, ~6K cycles each), which must stay well inside the prep's own
   // time (NC B H / nsm tasks of ~44K cycles per CTA): NC 6K <= 0.4 NC B H 44K / nsm
   // for 3 B H >= nsm.  Fewer rows: map and scan kernels first.
-  const bool chained = 3L * a.B * a.H >= nsm;
+  // (KDA has no gain state across chunks: neither the chain nor the map and scan)
+  const bool kdn = a.variant == DR_KDN;
+  const bool chained = kdn && 3L * a.B * a.H >= nsm;
   uint32_t* chain = chained ? reinterpret_cast<uint32_t*>(ws + (size_t)ntask * kRecK) : nullptr;
-  cudaError_t err;
+  cudaError_t err = cudaSuccess;
   if (chained) {
     err = cudaMemsetAsync(chain, 0, chain_bytes(ntask), st);
-  } else {
+  } else if (kdn) {
     kdn_map_kernel<<<(int)((ntask + kKdnMapWarps / 2 - 1) / (kKdnMapWarps / 2)), kKdnMapWarps * 32, 0,
                      st>>>(a, ws, dtype == DR_BF16 ? 1 : 0);
     kdn_scan_kernel<<<a.B * a.H, 128, 0, st>>>(a, ws);

@@ -351,16 +351,19 @@ def test_kdn_chained_variance_many_rows(rt, dtype):
 
 # ------------------------------------------------------------ per-channel decay: KDA, PKDA
 
+@pytest.mark.parametrize("workspace", ["auto", None])
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
 @pytest.mark.parametrize("variant", ["kda", "pkda"])
 @pytest.mark.parametrize("T", [1, 63, 130])
-def test_per_channel_decay_variants(rt, variant, dtype, T):
+def test_per_channel_decay_variants(rt, variant, dtype, T, workspace):
     """KDA (w = eta k, D = diag(alpha)) and PKDA (the PGDN write key under
-    per-channel decay) on the fused CUDA-core kernel: ragged lengths, nonzero
+    per-channel decay): with a workspace KDA takes the two-phase path (CUDA-core
+    prep, then the tcgen05 carry for bf16 or the fp32 carry), PKDA and every
+    call without one the fused CUDA-core kernel; ragged lengths, nonzero
     initial state and key statistic."""
     inp = small_inputs(variant, dtype, B=2, T=T, H=3, seed=400 + T)
     S0, aux0 = random_state(inp, seed=401 + T)
-    check_fwd(rt, inp, S0, aux0)
+    check_fwd(rt, inp, S0, aux0, workspace=workspace)
 
 
 @pytest.mark.parametrize("variant", ["kda", "pkda"])
