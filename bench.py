@@ -390,10 +390,13 @@ def main():
                                     wl.dv, wl.chunk)
         if ws is None or path not in ("tc_split", "simt_split"):
             return 1
-        # with few rows the KDN variance takes map and scan kernels first (KDA: none)
+        # with few rows the KDN variance takes map and scan kernels first (KDA: none;
+        # PKDA: the fused kernel alone)
         nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
         if path == "simt_split":
-            return 2 if (v != "kdn" or 3 * wl.B * wl.H >= nsm) else 4
+            if 3 * wl.B * wl.H >= nsm or v == "kda":
+                return 2
+            return 1 if v == "pkda" else 4
         return 4 if v == "pgdn" else 2   # PGDN: statistic map and scan kernels first
     launches = args.steps * sum(kernels_per_call(v) for v in variants)
     value = job_tokens_per_s(world, args.steps, len(variants), wl.B, wl.T, total_s)

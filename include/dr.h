@@ -161,18 +161,18 @@ int dr_decode_step(const void *q, const void *k, const void *v, const float *log
 /* Bytes of the optional dr_chunk_fwd workspace for these sizes: B H ceil(T/64)
  * records on the two-phase paths (dk = dv = 128, chunk 64) of 66560 bytes (GDN,
  * KLA; bf16), 101376 bytes (PGDN, bf16: also the write keys and the key
- * statistic's chunk map and chunk-start value) or 135168 bytes (Diagonal KDN
- * and KDA, bf16 or fp32: the carry's operands -- bf16 hi/lo tile images for
- * bf16 inputs, fp32 for fp32 -- and the variance chunk map and chunk-start
- * value), plus for those two 4 (n + 2) bytes rounded up to 256 (n =
- * B H ceil(T/64) records): the flags of the Diagonal KDN variance chain between
- * chunks, which the call clears itself; 0 where no path uses one. */
+ * statistic's chunk map and chunk-start value) or 135168 bytes (Diagonal KDN,
+ * KDA and PKDA, bf16 or fp32: the carry's operands -- bf16 hi/lo tile images
+ * for bf16 inputs, fp32 for fp32 -- and the variance / statistic chunk map and
+ * chunk-start value), plus for those three 4 (n + 2) bytes rounded up to 256
+ * (n = B H ceil(T/64) records): the flags of the chain between chunks, which
+ * the call clears itself; 0 where no path uses one. */
 size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H, int dk, int dv,
                                     int chunk);
 
 /*
  * Same forward as dr_chunk_fwd on its two-phase paths (GDN, KLA, PGDN in bf16
- * and Diagonal KDN, KDA in bf16 or fp32; dk = dv = 128, chunk 64), for callers that
+ * and Diagonal KDN, KDA, PKDA in bf16 or fp32; dk = dv = 128, chunk 64), for callers that
  * cannot allocate device
  * memory: code that runs where cudaMalloc is off limits (a host framework that
  * owns every byte of device memory through its own allocator, a real-time loop
@@ -216,14 +216,15 @@ const char *dr_status_string(int status);
  *          without a workspace the same shapes take
  * "tc_ws"  the warp-specialised single-kernel tcgen05 path (GDN, KLA), or
  * "tc"     the phase-sequential tcgen05 kernel (PGDN)
- * "simt_split" two-phase Diagonal KDN / KDA path (bf16 or fp32, dk = dv = 128,
- *          chunk 64) when the workspace is supplied: every chunk's local work
- *          on fp32 CUDA cores (the KDN variance at each chunk start handed
- *          over between chunks, or from chunk maps and a scan when the rows
- *          are few), then the state carry -- the tcgen05 carry for bf16
- *          inputs, fp32 CUDA cores for fp32
- * "simt"   fp32 CUDA-core kernel (everything else: fp32 mode, KDN / KDA
- *          without a workspace, PKDA, dk or dv 64, other chunk sizes). */
+ * "simt_split" two-phase Diagonal KDN / KDA / PKDA path (bf16 or fp32,
+ *          dk = dv = 128, chunk 64) when the workspace is supplied: every
+ *          chunk's local work on fp32 CUDA cores (the KDN variance or PKDA key
+ *          statistic at each chunk start handed over between chunks; with few
+ *          rows, 3 B H < SM count, KDN takes chunk maps and a scan instead and
+ *          PKDA the fused kernel), then the state carry -- the tcgen05 carry
+ *          for bf16 inputs, fp32 CUDA cores for fp32
+ * "simt"   fp32 CUDA-core kernel (everything else: fp32 mode, KDN / KDA / PKDA
+ *          without a workspace, dk or dv 64, other chunk sizes). */
 const char *dr_chunk_fwd_path(int variant, int dtype, int dk, int dv, int chunk);
 
 #ifdef __cplusplus

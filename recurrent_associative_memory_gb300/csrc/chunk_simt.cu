@@ -418,8 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
     if (chained && ci > 0 && tid == 0 && !chain_wait(chain + ri, chain + kIters + 1, kChainWaitNs))
       set_status(DR_ERR_TIMEOUT);
     __syncthreads();
-    if (chained && tid < DK)   // p at the chunk start: the row's initial value, or the previous chunk's
-      carry = ci == 0 ? (a.aux0 ? a.aux0[(long)bh * DK + tid] : 1.f)
+    if (chained && tid < DK)   // KDN p / PKDA A at the chunk start: the row's initial
+                               // value (default 1 / 0), or the previous chunk's
+      carry = ci == 0 ? (a.aux0 ? a.aux0[(long)bh * DK + tid] : (kdn ? 1.f : 0.f))
                       : __ldcg(reinterpret_cast<const float*>(rec + rkP0) + tid);
 
     // ---- 3. cumulative decay and write vectors
@@ -489,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
             float scale = 1.f;
             if (pkda) {
               A = sb2[i0 + e] * A + sb3[i0 + e] * kv[e] * kv[e];
-              const float rr = logf(fmaxf(A, a.log_floor)) - mu_h;
+              const float rr = logf(fmaxf(A, a.log_floor)) - (PREP ? a.mu[h] : mu_h);
               scale = expf(-a.ln_x * __fdividef(rr, 1.f + fabsf(rr)));
             }
             w[e] = sb1[i0 + e] * scale * kv[e];
@@ -499,6 +500,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
           *reinterpret_cast<float4*>(sWt + c * CS + i0 + 4) = make_float4(w[4], w[5], w[6], w[7]);
         }
         if (pkda) carry = A;
+        if (chained) {   // A at the chunk end -> the next chunk's record, or aux after the last
+                         // (the flag is raised below, after the barrier)
+          if (ci + 1 < NCk) {
+            __stcg(reinterpret_cast<float*>(rec + kRecK + rkP0) + c, carry);
+            __threadfence();
+          } else if (a.aux) {
+            a.aux[(long)bh * DK + c] = carry;
+          }
+        }
       }
       __syncthreads();
     }
@@ -1526,8 +1536,8 @@ namespace dr {
 cudaError_t launch_carry_kdn_tc(const FwdArgs& a, void* workspace, cudaStream_t st);
 
 bool kdn_split_supported(int variant, int dtype, int dk, int dv, int chunk) {
-  return (variant == DR_KDN || variant == DR_KDA) && (dtype == DR_BF16 || dtype == DR_FP32) &&
-         dk == 128 && dv == 128 && chunk == 64;
+  return (variant == DR_KDN || variant == DR_KDA || variant == DR_PKDA) &&
+         (dtype == DR_BF16 || dtype == DR_FP32) && dk == 128 && dv == 128 && chunk == 64;
 }
 
 size_t kdn_split_workspace_bytes(int B, int T, int H) {
@@ -1544,9 +1554,12 @@ cudaError_t launch_kdn_split(const FwdArgs& a, int dtype, void* workspace, cudaS
   // variance scan, ~6K cycles each), which must stay well inside the prep's own
   // time (NC B H / nsm tasks of ~44K cycles per CTA): NC 6K <= 0.4 NC B H 44K / nsm
   // for 3 B H >= nsm.  Fewer rows: map and scan kernels first.
-  // (KDA has no gain state across chunks: neither the chain nor the map and scan)
+  // KDA has no gain state across chunks: neither the chain nor the map and scan.
+  // PKDA chains its key statistic the same way (a 64-token linear scan per link);
+  // with few rows it runs the fused kernel instead.
   const bool kdn = a.variant == DR_KDN;
-  const bool chained = kdn && 3L * a.B * a.H >= nsm;
+  const bool chained = (kdn || a.variant == DR_PKDA) && 3L * a.B * a.H >= nsm;
+  if (a.variant == DR_PKDA && !chained) return launch_chunk_simt(a, dtype, st);
   uint32_t* chain = chained ? reinterpret_cast<uint32_t*>(ws + (size_t)ntask * kRecK) : nullptr;
   cudaError_t err = cudaSuccess;
   if (chained) {

@@ -101,12 +101,11 @@ def test_status_strings(dr):
     assert dr.dr_chunk_fwd_path(dr.DR_KLA, dr.DR_BF16, 128, 128, 64) == "tc_split"
     assert dr.dr_chunk_fwd_path(dr.DR_PGDN, dr.DR_BF16, 128, 128, 64) == "tc_split"
     assert dr.dr_chunk_fwd_path(dr.DR_KLA, dr.DR_FP32, 64, 64, 64) == "simt"
-    # KDA takes Diagonal KDN's two-phase path (same records); PKDA the fused kernel
-    assert dr.dr_chunk_fwd_path(dr.DR_KDA, dr.DR_BF16, 128, 128, 64) == "simt_split"
-    assert dr.dr_chunk_fwd_workspace_bytes(4, 1, 4, 8192, 16, 128, 128, 64) == \
-        dr.dr_chunk_fwd_workspace_bytes(3, 1, 4, 8192, 16, 128, 128, 64)
-    assert dr.dr_chunk_fwd_path(dr.DR_PKDA, dr.DR_BF16, 128, 128, 64) == "simt"
-    assert dr.dr_chunk_fwd_workspace_bytes(5, 1, 4, 8192, 16, 128, 128, 64) == 0
+    # KDA and PKDA take Diagonal KDN's two-phase path (same records)
+    for vid in (dr.DR_KDA, dr.DR_PKDA):
+        assert dr.dr_chunk_fwd_path(vid, dr.DR_BF16, 128, 128, 64) == "simt_split"
+        assert dr.dr_chunk_fwd_workspace_bytes(vid, 1, 4, 8192, 16, 128, 128, 64) == \
+            dr.dr_chunk_fwd_workspace_bytes(3, 1, 4, 8192, 16, 128, 128, 64)
 
 
 A = 1 << 20          # a 16-byte aligned address that is never dereferenced

@@ -325,17 +325,19 @@ def test_kdn_two_phase_and_fused_paths(rt, dtype, workspace):
     check_fwd(rt, inp, S0, aux0, workspace=workspace)
 
 
+@pytest.mark.parametrize("variant", ["kdn", "pkda"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-def test_kdn_chained_variance_many_rows(rt, dtype):
+def test_kdn_chained_variance_many_rows(rt, dtype, variant):
     """With many (b, h) rows (three times the rows at least the SM count) the
-    prep hands the variance from chunk to chunk itself (chunk-major tickets,
-    flags in the workspace) instead of running the map and scan kernels.  Every
+    prep hands the KDN variance (PKDA: the key statistic) from chunk to chunk
+    itself (chunk-major tickets, flags in the workspace) instead of running the
+    map and scan kernels (PKDA: the fused kernel).  Every
     row checked, more tasks than CTAs, a ragged tail, nonzero initial state and
     variance; a dirty workspace (stale flags and records) gives the same bits."""
     dr, runner = rt
     B, H = 2, 26
     assert 3 * B * H >= torch.cuda.get_device_properties(0).multi_processor_count
-    inp = small_inputs("kdn", dtype, B=B, T=64 * 4 + 21, H=H, seed=311)
+    inp = small_inputs(variant, dtype, B=B, T=64 * 4 + 21, H=H, seed=311)
     S0, aux0 = random_state(inp, seed=312)
     check_fwd(rt, inp, S0, aux0)
     dev = runner.to_device(inp)
