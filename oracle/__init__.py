@@ -10,7 +10,8 @@ holds none of the method's arithmetic.
 Modules
 -------
 recurrence  Tokenwise recurrence (the plain definition) for GDN, KLA, PGDN,
-            Diagonal KDN, KDA and PKDA, one token at a time, in float64.
+            Diagonal KDN, KDA, PKDA and isotropic KDN, one token at a time,
+            in float64.
 chunkwise   A naive chunkwise-parallel restatement (triangular system per
             chunk), written independently of ``recurrence`` as a cross-check.
 ridge       Side oracles fixed by closed forms: exact ridge regression (ATQ),
@@ -32,6 +33,9 @@ from .recurrence import (  # noqa: F401
     kdn_predict,
     kdn_gain,
     kdn_variance_update,
+    ikdn_predict,
+    ikdn_gain,
+    ikdn_variance_update,
     recurrence_step,
     tokenwise,
 )

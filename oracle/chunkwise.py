@@ -29,7 +29,10 @@ forms rather than token by token:
     prefix of the chunk;
   * KDN variance: products of the 2x2 Moebius matrices
     M_t = [[alpha^2, omega], [u alpha^2, 1 + u omega]] acting on the
-    homogeneous pair (n, d) with p = n/d (KDN notes section 6, Eqs. (32)-(39)).
+    homogeneous pair (n, d) with p = n/d (KDN notes section 6, Eqs. (32)-(39));
+    the isotropic variance b is the same scan with one channel, the mean
+    squared decay in place of alpha^2 (KDN notes section 7: "this scalar
+    recursion can also be written as a 2x2 Moebius scan").
 """
 
 from __future__ import annotations
@@ -133,7 +136,8 @@ def chunkwise(q, k, v, log_alpha, variant: str, chunk: int, *, eta=None,
 
     o = np.zeros((B, T, H, dv))
     S_fin = np.zeros((B, H, dk, dv))
-    aux_fin = None if variant in ("gdn", "kla", "kda") else np.zeros((B, H, dk))
+    aux_fin = (None if variant in ("gdn", "kla", "kda")
+               else np.zeros((B, H)) if variant == "ikdn" else np.zeros((B, H, dk)))
     for b in range(B):
         for h in range(H):
             S = np.zeros((dk, dv)) if S0 is None else np.array(S0[b, h], dtype=np.float64)
@@ -141,6 +145,8 @@ def chunkwise(q, k, v, log_alpha, variant: str, chunk: int, *, eta=None,
                 aux = np.zeros(dk) if aux0 is None else np.array(aux0[b, h], dtype=np.float64)
             elif variant == "kdn":
                 aux = np.ones(dk) if aux0 is None else np.array(aux0[b, h], dtype=np.float64)
+            elif variant == "ikdn":
+                aux = 1.0 if aux0 is None else float(aux0[b, h])
             for t0 in range(0, T, chunk):
                 t1 = min(T, t0 + chunk)
                 kc, qc, vc = k[b, t0:t1, h], q[b, t0:t1, h], v[b, t0:t1, h]
@@ -156,6 +162,17 @@ def chunkwise(q, k, v, log_alpha, variant: str, chunk: int, *, eta=None,
                     A = pgdn_stat_chunk(aux, kc * kc, np.log(alphaP[b, t0:t1, h]), betaP[b, t0:t1, h])
                     aux = A[-1]
                     w = eta[b, t0:t1, h][:, None] * pgdn_squash(A, mu[h], x, log_floor) * kc
+                elif variant == "ikdn":
+                    rc = r[b, t0:t1, h]
+                    kk = np.sum(kc * kc, axis=1)
+                    a_mean = np.mean(np.exp(2.0 * la), axis=1)          # [C]
+                    u = info_scale * kk / (dk * rc)
+                    om = omega[b, t0:t1, h]
+                    b_prev, b_post = kdn_mobius_chunk(np.array([aux]), np.sqrt(a_mean)[:, None],
+                                                      om[:, None], u[:, None])
+                    aux = float(b_post[-1, 0])
+                    b_hat = a_mean * b_prev[:, 0] + om
+                    w = (b_hat / (rc + b_hat * kk))[:, None] * kc
                 else:
                     rc = r[b, t0:t1, h]
                     u = (info_scale / rc)[:, None] * kc * kc

@@ -21,6 +21,9 @@ with S in R^{dk x dv}, D_t = alpha_t I (GDN, KLA, PGDN) or diag(alpha_t)
           r = log max(A_t, floor) - mu ; s = r / (1 + |r|)
           B = exp(-log(x) s) ;  w = beta (B * k)
     PKDA  the PGDN write key with D_t = diag(alpha_t)   (PDN notes section 2.5)
+    IKDN  isotropic KDN, one variance b per head       (KDN notes section 7, Eq. (40))
+          a = mean_i alpha_i^2 ; b^ = a b_{t-1} + omega ; beta = b^ / (r + b^ ||k||^2)
+          w = beta k ; b_t = b^ / (1 + u b^), u = mu ||k||^2 / (dk r)
     KDN   p^ = alpha^2 * p_{t-1} + omega            (KDN notes Eq. (23))
           kappa = p^ * k / (r + sum(p^ k^2)) ; w = kappa
           p_t = p^ / (1 + (mu/r) k*k * p^)          (KDN notes Eqs. (60)-(65))
@@ -35,7 +38,7 @@ from __future__ import annotations
 
 import numpy as np
 
-VARIANTS = ("gdn", "kla", "pgdn", "kdn", "kda", "pkda")
+VARIANTS = ("gdn", "kla", "pgdn", "kdn", "kda", "pkda", "ikdn")
 
 
 def l2normalize(x: np.ndarray, floor: float = 1e-30) -> np.ndarray:
@@ -104,6 +107,30 @@ def kdn_variance_update(p_hat, k, r, mu: float):
     return p_hat / (1.0 + u * p_hat)
 
 
+def ikdn_predict(b_prev, alpha, omega):
+    """Isotropic predicted variance b^ = a b + omega, a = (1/dk) sum_i alpha_i^2.
+
+    The prediction keeps P = b I by projecting D P D onto multiples of I by its
+    trace, i.e. the mean eigenvalue (KDN notes section 7, Eq. (40)); alpha may
+    still differ per channel.  b_prev, omega [...]; alpha [..., dk].
+    """
+    return np.mean(alpha * alpha, axis=-1) * b_prev + omega
+
+
+def ikdn_gain(b_hat, k, r):
+    """Isotropic gain: w = beta k, beta = b^ / (r + b^ ||k||^2) (KDN Eq. (40))."""
+    beta = b_hat / (r + b_hat * np.sum(k * k, axis=-1))
+    return beta[..., None] * k
+
+
+def ikdn_variance_update(b_hat, k, r, mu: float):
+    """Reverse-KL isotropic variance with information scaling mu (KDN Eq. (40)):
+    b = b^ / (1 + u b^), u = mu ||k||^2 / (dk r) (the harmonic mean of the
+    posterior eigenvalues)."""
+    u = mu * np.sum(k * k, axis=-1) / (k.shape[-1] * r)
+    return b_hat / (1.0 + u * b_hat)
+
+
 # ---------------------------------------------------------------- the recurrence
 
 def recurrence_step(S, q, k, v, decay, w):
@@ -133,10 +160,11 @@ def tokenwise(q, k, v, log_alpha, variant: str, *, eta=None, eps: float = 1e-6,
     variant  one of VARIANTS.
     eta      [B,T,H]: GDN/KLA eta, PGDN beta.
     alphaP, betaP [B,T,H]; mu [H]          PGDN / PKDA statistic gates and centre.
-    omega [B,T,H,dk]; r [B,T,H]            KDN process / observation noise.
+    omega [B,T,H,dk]; r [B,T,H]            KDN process / observation noise
+                                           (isotropic KDN: omega [B,T,H]).
     log_alpha [B,T,H] (scalar decay) or [B,T,H,dk] (KDA, PKDA, KDN).
     S0 [B,H,dk,dv] (None = 0); aux0 [B,H,dk]: PGDN / PKDA A_0 (None = 0) or
-    KDN p_0 (None = 1).
+    KDN p_0 (None = 1); isotropic KDN b_0 [B,H] (None = 1).
     Returns (o [B,T,H,dv], S_T [B,H,dk,dv], aux_T [B,H,dk] or None); with
     ``return_trace`` also a dict of per-token write vectors and residuals.
     """
@@ -158,6 +186,8 @@ def tokenwise(q, k, v, log_alpha, variant: str, *, eta=None, eps: float = 1e-6,
         aux = np.zeros((B, H, dk)) if aux0 is None else np.array(aux0, dtype=np.float64)
     elif variant == "kdn":
         aux = np.ones((B, H, dk)) if aux0 is None else np.array(aux0, dtype=np.float64)
+    elif variant == "ikdn":
+        aux = np.ones((B, H)) if aux0 is None else np.array(aux0, dtype=np.float64)
 
     o = np.zeros((B, T, H, dv))
     trace = {"w": np.zeros((B, T, H, dk)), "e": np.zeros((B, T, H, dv))} if return_trace else None
@@ -172,6 +202,10 @@ def tokenwise(q, k, v, log_alpha, variant: str, *, eta=None, eps: float = 1e-6,
             aux = pgdn_stat_update(aux, kt, alphaP[:, t], betaP[:, t])
             Bscale = pgdn_squash(aux, mu[None, :, None], x, log_floor)
             w = eta[:, t][..., None] * (Bscale * kt)
+        elif variant == "ikdn":
+            b_hat = ikdn_predict(aux, alpha, omega[:, t])
+            w = ikdn_gain(b_hat, kt, r[:, t])
+            aux = ikdn_variance_update(b_hat, kt, r[:, t], info_scale)
         else:  # kdn: predict, gain, (memory update below), variance update
             p_hat = kdn_predict(aux, alpha, omega[:, t])
             w = kdn_gain(p_hat, kt, r[:, t])

@@ -30,6 +30,10 @@ contexts up to 64K) with these distributions:
 * ``pkda_bf16``        PKDA (the PGDN write key with per-channel decay), bf16,
   B=4 H=16 T=4096 d=128 C=64; the PGDN gates, then per-channel log alpha as
   for KDA.
+* ``ikdn_bf16``        isotropic KDN, bf16, B=4 H=16 T=8192 d=128 C=64; q,k,v
+  as for PGDN; per-channel log alpha as for Diagonal KDN; omega =
+  softplus(N(-3,1)) and r = softplus(N(0,1)) per (b,t,h); b_0 = 1;
+  information scale 1.
 * ``kla_prefill_bf16`` KLA, bf16, B=1 H=16 T=65536 d=128, inputs as
   ``gdn_kla_bf16``.
 * ``kla_decode_bf16``  KLA decode steps at batch 256, H=16, d=128; fresh
@@ -84,6 +88,8 @@ WORKLOADS = {
                          k_l2norm=True, seed=1005),
     "pkda_bf16": Workload("pkda_bf16", ("pkda",), 4, 4096, 16, 128, 128, 64, "bf16",
                           k_l2norm=True, seed=1006),
+    "ikdn_bf16": Workload("ikdn_bf16", ("ikdn",), 4, 8192, 16, 128, 128, 64, "bf16",
+                          k_l2norm=True, seed=1007),
     "kla_prefill_bf16": Workload("kla_prefill_bf16", ("kla",), 1, 65536, 16, 128, 128, 64,
                                  "bf16", key_dist="lognormal_scaled", seed=1004),
     "kla_decode_bf16": Workload("kla_decode_bf16", ("kla",), 256, 1, 16, 128, 128, 64, "bf16",
@@ -131,6 +137,10 @@ def _draw_gates(gen, wl: Workload, variant: str, B, T):
     elif variant == "kdn":
         g["log_alpha"] = -_softplus(torch.randn(B, T, H, dk, generator=gen) + 2.0)
         g["omega"] = _softplus(torch.randn(B, T, H, dk, generator=gen) - 3.0)
+        g["r"] = _softplus(torch.randn(B, T, H, generator=gen))
+    elif variant == "ikdn":
+        g["log_alpha"] = -_softplus(torch.randn(B, T, H, dk, generator=gen) + 2.0)
+        g["omega"] = _softplus(torch.randn(B, T, H, generator=gen) - 3.0)
         g["r"] = _softplus(torch.randn(B, T, H, generator=gen))
     elif variant == "kda":
         g["eta"] = torch.sigmoid(torch.randn(B, T, H, generator=gen))

@@ -82,6 +82,10 @@ def random_inputs(variant, B=2, T=37, H=2, dk=8, dv=6, seed=0, decay_shift=0.5):
         d["log_alpha"] = -sp(r.standard_normal((B, T, H, dk)) + decay_shift)
         d["omega"] = sp(r.standard_normal((B, T, H, dk)) - 3)
         d["r"] = sp(r.standard_normal((B, T, H)))
+    if variant == "ikdn":   # one process noise per (b, t, h)
+        d["log_alpha"] = -sp(r.standard_normal((B, T, H, dk)) + decay_shift)
+        d["omega"] = sp(r.standard_normal((B, T, H)) - 3)
+        d["r"] = sp(r.standard_normal((B, T, H)))
     return d
 
 
@@ -356,6 +360,64 @@ def test_per_channel_decay_scales_key_rows(variant):
         np.testing.assert_allclose(S[0, 0], cum[-1][:, None] * S0[0, 0], rtol=1e-12, atol=1e-14)
 
 
+# ------------------------------------------------------------------ isotropic KDN
+
+@pytest.mark.parametrize("mu", [1.0, 3.0])
+def test_isotropic_kdn_with_one_channel_is_diagonal_kdn(mu):
+    """With dk = 1 the isotropic and diagonal filters are the same scalar Kalman
+    filter (KDN notes section 7 vs Eqs. (23)-(30), (60)-(65)): a = alpha^2,
+    beta k = p^ k/(r + p^ k^2), u = mu k^2 / r."""
+    d = random_inputs("kdn", B=2, T=23, H=2, dk=1, dv=3, seed=31)
+    S0 = rng(32).standard_normal((2, 2, 1, 3))
+    p0 = rng(33).uniform(0.5, 1.5, (2, 2, 1))
+    o1, S1, p1 = call(oracle.tokenwise, "kdn", d, S0=S0, aux0=p0, info_scale=mu)
+    di = dict(d, omega=d["omega"][..., 0])
+    o2, S2, b2 = call(oracle.tokenwise, "ikdn", di, S0=S0, aux0=p0[..., 0], info_scale=mu)
+    np.testing.assert_allclose(o2, o1, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(S2, S1, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(b2, p1[..., 0], rtol=1e-13)
+
+
+def test_isotropic_kdn_scalar_gain_example():
+    """The pages' scalar Kalman gains (k = r = 1: p^ = 9 -> 0.9, p^ = 0.1 -> 0.0909)
+    hold for the isotropic gain beta = b^/(r + b^ ||k||^2) (KDN notes section 7)."""
+    g = golden("kalman_scalar_example.json")
+    tol = 0.5 * 10 ** -g["printed_decimals"]
+    for b_hat, expect in g["gain_at_predicted_variance"].items():
+        w = oracle.ikdn_gain(np.array(float(b_hat)), np.array([g["k"]]), np.array(g["r"]))
+        assert w[0] == pytest.approx(expect, abs=tol)
+
+
+def test_isotropic_kdn_unit_keys_at_mu_dk():
+    """With unit keys and mu = dk the update weight is u = 1/r, so every step
+    gives b = b^/(1 + b^/r) (KDN notes section 7, the remark after Eq. (40))."""
+    d = random_inputs("ikdn", B=1, T=15, H=2, dk=6, dv=3, seed=34)
+    d["k"] = oracle.l2normalize(d["k"])
+    B, T, H, dk = d["k"].shape
+    b = np.ones((B, H))
+    for t in range(T):
+        one = {key: (val[:, t:t + 1] if val.ndim >= 3 else val) for key, val in d.items()}
+        _, _, b_next = call(oracle.tokenwise, "ikdn", one, aux0=b, info_scale=float(dk))
+        b_hat = np.mean(np.exp(2 * d["log_alpha"][:, t]), axis=-1) * b + d["omega"][:, t]
+        np.testing.assert_allclose(b_next, b_hat / (1 + b_hat / d["r"][:, t]), rtol=1e-14)
+        b = b_next
+
+
+def test_isotropic_kdn_predicts_with_the_mean_squared_decay():
+    """The trace projection: with no process noise and no information (r large)
+    the variance only decays, b_t = b_0 prod_s mean_i alpha_{s,i}^2 -- neither the
+    squared mean decay nor the mean decay (KDN notes section 7, Eq. (40) first line)."""
+    d = random_inputs("ikdn", B=1, T=5, H=1, dk=5, dv=2, seed=35)
+    d["omega"] = np.zeros_like(d["omega"])
+    d["r"] = np.full_like(d["r"], 1e300)
+    _, _, b = call(oracle.tokenwise, "ikdn", d, aux0=np.full((1, 1), 2.0))
+    alpha = np.exp(d["log_alpha"][0, :, 0])                       # [T, dk]
+    expect = 2.0 * np.prod(np.mean(alpha * alpha, axis=1))
+    assert b[0, 0] == pytest.approx(expect, rel=1e-12)
+    other = 2.0 * np.prod(np.mean(alpha, axis=1) ** 2)
+    assert abs(other - expect) > 1e-3 * expect
+
+
 # ------------------------------------------------------------------ P8: tokenwise == chunkwise
 
 CASES = [  # (T, dk, dv, chunk)
@@ -371,9 +433,9 @@ def test_tokenwise_equals_chunkwise(variant, T, dk, dv, chunk):
     r = rng(T)
     S0 = r.standard_normal((1, 2, dk, dv))
     aux0 = {"pgdn": r.uniform(0, 2, (1, 2, dk)), "pkda": r.uniform(0, 2, (1, 2, dk)),
-            "kdn": r.uniform(0.5, 1.5, (1, 2, dk))}.get(variant)
-    kw = dict(S0=S0, aux0=aux0, q_l2norm=True, k_l2norm=(variant in ("pgdn", "pkda", "kdn")),
-              eps=1e-6)
+            "kdn": r.uniform(0.5, 1.5, (1, 2, dk)), "ikdn": r.uniform(0.5, 1.5, (1, 2))}.get(variant)
+    kw = dict(S0=S0, aux0=aux0, q_l2norm=True,
+              k_l2norm=(variant in ("pgdn", "pkda", "kdn", "ikdn")), eps=1e-6)
     o1, S1, a1 = call(oracle.tokenwise, variant, d, **kw)
     o2, S2, a2 = call(oracle.chunkwise, variant, d, chunk=chunk, **kw)
     scale = max(1.0, np.abs(o1).max())
