@@ -117,7 +117,7 @@ def fwd_bytes(wl, variant, with_final=True):
     ht = wl.B * wl.T * wl.H
     per_ht = (2 * wl.dk + 2 * wl.dv) * el          # q, k, v, o
     gates = {"gdn": 8, "kla": 8, "pgdn": 16, "kdn": 8 * wl.dk + 4,
-             "kda": 4 * wl.dk + 4, "pkda": 4 * wl.dk + 12}[variant]
+             "kda": 4 * wl.dk + 4, "pkda": 4 * wl.dk + 12, "ikdn": 4 * wl.dk + 8}[variant]
     total = ht * (per_ht + gates)
     if variant in ("pgdn", "pkda"):
         total += wl.H * 4
@@ -125,6 +125,8 @@ def fwd_bytes(wl, variant, with_final=True):
         total += wl.B * wl.H * wl.dk * wl.dv * 4
         if variant in ("pgdn", "kdn", "pkda"):
             total += wl.B * wl.H * wl.dk * 4
+        if variant == "ikdn":   # one variance per head
+            total += wl.B * wl.H * 4
     return total
 
 
@@ -396,7 +398,7 @@ def main():
         if path == "simt_split":
             if 3 * wl.B * wl.H >= nsm or v == "kda":
                 return 2
-            return 1 if v == "pkda" else 4
+            return 1 if v in ("pkda", "ikdn") else 4
         return 4 if v == "pgdn" else 2   # PGDN: statistic map and scan kernels first
     launches = args.steps * sum(kernels_per_call(v) for v in variants)
     value = job_tokens_per_s(world, args.steps, len(variants), wl.B, wl.T, total_s)

@@ -199,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
   const bool pgdn = (a.variant == DR_PGDN);
   const bool kda = (a.variant == DR_KDA);
   const bool pkda = (a.variant == DR_PKDA);
-  const bool perchan = kdn || kda || pkda;   // per-channel decay D = diag(alpha)
+  const bool ikdn = (a.variant == DR_IKDN);  // isotropic KDN: one variance per head
+  const bool perchan = kdn || kda || pkda || ikdn;   // per-channel decay D = diag(alpha)
   const bool pstat = pgdn || pkda;           // the PGDN key statistic and write key
   // W is formed explicitly (not as a per-row multiple of K in the Gram's readout)
   const bool explicit_w = perchan || pgdn;
@@ -224,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
   if (my_c >= 0 && my_c < DK) {
     if (pstat) carry = a.aux0 ? a.aux0[(long)bh * DK + my_c] : 0.f;
     if (kdn) carry = a.aux0 ? a.aux0[(long)bh * DK + my_c] : 1.f;
+    if (ikdn) carry = a.aux0 ? a.aux0[bh] : 1.f;   // used by thread 0
   }
   const float mu_h = pstat ? a.mu[h] : 0.f;
   bool bad = false;
@@ -326,7 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       const int i = tid;
       const bool real = i < Cc;
       const long ti = real ? tok_index(a, b, t0 + i, h) : 0;
-      if (!kdn) {
+      if (ikdn) {   // r, omega (scalar per token); ||k^||^2 comes with the key loads
+        sb1[i] = real ? a.r[ti] : 1.f;
+        sb2[i] = real ? a.omega[ti] : 0.f;
+      } else if (!kdn) {
         if (!perchan) sg[i] = real ? a.log_alpha[ti] : 0.f;
         sb1[i] = real ? a.eta[ti] : 0.f;
       } else {
@@ -402,6 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
           if (!explicit_w) sW[i * DK + c] = kv[e] * kn;
         }
         if (sub == 0 && real && a.variant == DR_KLA) sb1[i] = sb1[i] / (kk * kn * kn + a.eps);
+        if (sub == 0 && ikdn) sb3[i] = kk * kn * kn;   // ||k^||^2 (0 on padding rows)
       }
     }
     if (!PREP) {
@@ -418,9 +424,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
     if (chained && ci > 0 && tid == 0 && !chain_wait(chain + ri, chain + kIters + 1, kChainWaitNs))
       set_status(DR_ERR_TIMEOUT);
     __syncthreads();
-    if (chained && tid < DK)   // KDN p / PKDA A at the chunk start: the row's initial
-                               // value (default 1 / 0), or the previous chunk's
-      carry = ci == 0 ? (a.aux0 ? a.aux0[(long)bh * DK + tid] : (kdn ? 1.f : 0.f))
+    if (chained && tid < DK)   // KDN p / PKDA A / IKDN b (thread 0) at the chunk start: the
+                               // row's initial value (default 1 / 0 / 1), or the previous chunk's
+      carry = ci == 0 ? (a.aux0 ? a.aux0[ikdn ? (long)bh : (long)bh * DK + tid] : (pkda ? 0.f : 1.f))
                       : __ldcg(reinterpret_cast<const float*>(rec + rkP0) + tid);
 
     // ---- 3. cumulative decay and write vectors
@@ -460,6 +466,73 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
           }
         }
         carry = A;
+      }
+      __syncthreads();
+    } else if (ikdn) {
+      // isotropic KDN (KDN notes section 7, Eq. (40)): the mean squared decay of
+      // every token (warp w: tokens 8w .. 8w + 7), then channel c's cumulative
+      // log-decay (thread c) while thread 0 runs the variance scan of the head,
+      // then w = beta k^
+      {
+        const int i0 = 8 * warp;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          float s2 = 0.f;
+#pragma unroll
+          for (int c = lane; c < DK; c += 32) s2 += expf(2.f * sX[(i0 + r) * DK + c]);
+          s2 = warp_sum(s2);
+          if (lane == 0) sz[i0 + r] = s2 * (1.f / DK);
+        }
+      }
+      __syncthreads();
+      if (tid < DK) {
+        const int c = tid;
+        float g = 0.f;
+        for (int i0 = 0; i0 < CM; i0 += 8) {
+          float la[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) la[e] = sX[(i0 + e) * DK + c];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            g += la[e];
+            sX[(i0 + e) * DK + c] = g;
+          }
+        }
+      }
+      if (tid == 0) {   // b^ = a b + omega; beta = b^/(r + b^ |k|^2); b = b^/(1 + u b^)
+        float bv = carry;
+        for (int i = 0; i < CM; ++i) {
+          const float b_hat = sz[i] * bv + sb2[i];
+          const float rr = sb1[i], kk = sb3[i];
+          sz[i] = __fdividef(b_hat, rr + b_hat * kk);
+          bv = __fdividef(b_hat, 1.f + a.info_scale * kk * b_hat / (DK * rr));
+        }
+        carry = bv;
+        if (chained) {   // b at the chunk end -> the next chunk's record, or aux after the last
+          if (ci + 1 < NCk) {
+            __stcg(reinterpret_cast<float*>(rec + kRecK + rkP0), carry);
+            __threadfence();
+          } else if (a.aux) {
+            a.aux[bh] = carry;
+          }
+        }
+      }
+      __syncthreads();
+      if (tid < DK) {
+        const int c = tid;
+        for (int i0 = 0; i0 < CM; i0 += 8) {
+          const float4 k0 = *reinterpret_cast<const float4*>(sKt + c * CS + i0);
+          const float4 k1 = *reinterpret_cast<const float4*>(sKt + c * CS + i0 + 4);
+          const float kv[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+          float w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            w[e] = sz[i0 + e] * kv[e];
+            sW[(i0 + e) * DK + c] = w[e];
+          }
+          *reinterpret_cast<float4*>(sWt + c * CS + i0) = make_float4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<float4*>(sWt + c * CS + i0 + 4) = make_float4(w[4], w[5], w[6], w[7]);
+        }
       }
       __syncthreads();
     } else if (!kdn) {
@@ -1122,6 +1195,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
   }
   if (a.aux && tile == 0 && (pstat || kdn) && my_c >= 0 && my_c < DK)
     a.aux[(long)bh * DK + my_c] = carry;
+  if (a.aux && tile == 0 && ikdn && tid == 0) a.aux[bh] = carry;
   if (bad) set_status(DR_ERR_NONFINITE);
 }
 
@@ -1536,7 +1610,7 @@ namespace dr {
 cudaError_t launch_carry_kdn_tc(const FwdArgs& a, void* workspace, cudaStream_t st);
 
 bool kdn_split_supported(int variant, int dtype, int dk, int dv, int chunk) {
-  return (variant == DR_KDN || variant == DR_KDA || variant == DR_PKDA) &&
+  return (variant == DR_KDN || variant == DR_KDA || variant == DR_PKDA || variant == DR_IKDN) &&
          (dtype == DR_BF16 || dtype == DR_FP32) && dk == 128 && dv == 128 && chunk == 64;
 }
 
@@ -1555,11 +1629,12 @@ cudaError_t launch_kdn_split(const FwdArgs& a, int dtype, void* workspace, cudaS
   // time (NC B H / nsm tasks of ~44K cycles per CTA): NC 6K <= 0.4 NC B H 44K / nsm
   // for 3 B H >= nsm.  Fewer rows: map and scan kernels first.
   // KDA has no gain state across chunks: neither the chain nor the map and scan.
-  // PKDA chains its key statistic the same way (a 64-token linear scan per link);
-  // with few rows it runs the fused kernel instead.
+  // PKDA (key statistic) and isotropic KDN (one variance per head) chain theirs
+  // the same way; with few rows they run the fused kernel instead.
   const bool kdn = a.variant == DR_KDN;
-  const bool chained = (kdn || a.variant == DR_PKDA) && 3L * a.B * a.H >= nsm;
-  if (a.variant == DR_PKDA && !chained) return launch_chunk_simt(a, dtype, st);
+  const bool chain_only = a.variant == DR_PKDA || a.variant == DR_IKDN;
+  const bool chained = (kdn || chain_only) && 3L * a.B * a.H >= nsm;
+  if (chain_only && !chained) return launch_chunk_simt(a, dtype, st);
   uint32_t* chain = chained ? reinterpret_cast<uint32_t*>(ws + (size_t)ntask * kRecK) : nullptr;
   cudaError_t err = cudaSuccess;
   if (chained) {

@@ -9,7 +9,8 @@
 //   2. load q, k, v and the gates; L2-normalise; form the decay d and the write
 //      vector w for the variant (KLA notes Algorithm 1; PDN notes section 2.5,
 //      two states A and S; KDN notes section 2.2, predict -> gain -> update;
-//      KDA / PKDA: the GDN / PGDN write under per-channel decay);
+//      KDA / PKDA: the GDN / PGDN write under per-channel decay; isotropic KDN:
+//      one variance per head, KDN notes section 7);
 //   3. one pass over S gives both S~^T k and S~^T q (S~ = D S), reduced over
 //      rows with registers + shared memory;
 //   4. e = v - S~^T k;  o = S~^T q + (w^T q) e  (= S_t^T q, read after write);
@@ -105,6 +106,20 @@ __global__ void __launch_bounds__(kDecodeThreads, (DK * DVS <= 8192) ? 4 : 2)
         const float u = (a.info_scale / rr) * kc * kc;
         a.aux[tok * DK + tid] = p_hat / (1.f + u * p_hat);
       }
+    }
+  } else if (a.variant == DR_IKDN) {   // one variance per head (aux [B, H])
+    const float alpha = tid < DK ? expf(a.log_alpha[tok * DK + tid]) : 0.f;
+    const float a_mean = block_sum(alpha * alpha, s_red) / DK;
+    const float rr = a.r[tok];
+    const float b_hat = a_mean * a.aux[tok] + a.omega[tok];
+    if (tid < DK) {
+      w = b_hat / (rr + b_hat * kk_eff) * kc;
+      d = alpha;
+    }
+    __syncthreads();   // every thread has read the variance before it is replaced
+    if (slice == 0 && tid == 0) {
+      const float u = a.info_scale * kk_eff / (DK * rr);
+      a.aux[tok] = b_hat / (1.f + u * b_hat);
     }
   } else if (tid < DK) {
     const bool perchan = (a.variant == DR_KDA || a.variant == DR_PKDA);   // decay per row of S

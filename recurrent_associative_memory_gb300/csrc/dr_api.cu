@@ -43,6 +43,7 @@ int check_gates(const dr_params* gp, int variant) {
       if (!(gp->x > 1.f) || !(gp->log_floor > 0.f)) return DR_ERR_ARG;
       return DR_OK;
     case DR_KDN:
+    case DR_IKDN:
       if (!gp->omega || !gp->r) return DR_ERR_NULL;
       if (!(gp->info_scale >= 0.f)) return DR_ERR_ARG;
       return DR_OK;
@@ -187,7 +188,9 @@ int dr_decode_step(const void* q, const void* k, const void* v, const float* log
   if (!(eps >= 0.f)) return DR_ERR_ARG;
   int st = check_gates(gp, variant);
   if (st != DR_OK) return st;
-  if ((variant == DR_PGDN || variant == DR_KDN || variant == DR_PKDA) && !aux_state) return DR_ERR_NULL;
+  if ((variant == DR_PGDN || variant == DR_KDN || variant == DR_PKDA || variant == DR_IKDN) &&
+      !aux_state)
+    return DR_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
       !aligned16(state) || !aligned16(aux_state))
     return DR_ERR_ALIGN;

@@ -101,8 +101,8 @@ def test_status_strings(dr):
     assert dr.dr_chunk_fwd_path(dr.DR_KLA, dr.DR_BF16, 128, 128, 64) == "tc_split"
     assert dr.dr_chunk_fwd_path(dr.DR_PGDN, dr.DR_BF16, 128, 128, 64) == "tc_split"
     assert dr.dr_chunk_fwd_path(dr.DR_KLA, dr.DR_FP32, 64, 64, 64) == "simt"
-    # KDA and PKDA take Diagonal KDN's two-phase path (same records)
-    for vid in (dr.DR_KDA, dr.DR_PKDA):
+    # KDA, PKDA and isotropic KDN take Diagonal KDN's two-phase path (same records)
+    for vid in (dr.DR_KDA, dr.DR_PKDA, dr.DR_IKDN):
         assert dr.dr_chunk_fwd_path(vid, dr.DR_BF16, 128, 128, 64) == "simt_split"
         assert dr.dr_chunk_fwd_workspace_bytes(vid, 1, 4, 8192, 16, 128, 128, 64) == \
             dr.dr_chunk_fwd_workspace_bytes(3, 1, 4, 8192, 16, 128, 128, 64)
@@ -128,6 +128,7 @@ def test_chunk_fwd_rejects_bad_arguments(dr):
     assert fwd(dr, variant=4, eta=None) == dr.DR_ERR_NULL      # KDA without eta
     assert fwd(dr, variant=5) == dr.DR_ERR_NULL                # PKDA without alphaP/betaP/mu
     assert fwd(dr, variant=5, alphaP=A, betaP=A, mu=A, x=0.5) == dr.DR_ERR_ARG
+    assert fwd(dr, variant=6, r=A) == dr.DR_ERR_NULL           # isotropic KDN without omega
     assert fwd(dr, variant=7) == dr.DR_ERR_UNSUPPORTED
     assert fwd(dr, dtype=5) == dr.DR_ERR_DTYPE
     assert fwd(dr, dk=96) == dr.DR_ERR_SHAPE
@@ -153,6 +154,7 @@ def test_decode_rejects_bad_arguments(dr):
     assert dec(variant=2, alphaP=A, betaP=A, mu=A) == dr.DR_ERR_NULL   # aux state required
     assert dec(variant=3, omega=A, r=A) == dr.DR_ERR_NULL
     assert dec(variant=5, alphaP=A, betaP=A, mu=A) == dr.DR_ERR_NULL   # PKDA: aux state required
+    assert dec(variant=6, omega=A, r=A) == dr.DR_ERR_NULL              # isotropic KDN: its b
     assert dec(dk=32) == dr.DR_ERR_SHAPE
     assert dec(state=MIS) == dr.DR_ERR_ALIGN
     assert dec(dtype=2) == dr.DR_ERR_DTYPE

@@ -21,10 +21,12 @@ from recurrent_associative_memory_gb300 import workloads as W  # noqa: E402
 # (KDA), + alphaP, betaP (PKDA)
 @pytest.mark.parametrize("variant,per_head_token", [("gdn", 1032), ("kla", 1032),
                                                      ("pgdn", 1040), ("kdn", 2052),
-                                                     ("kda", 1540), ("pkda", 1548)])
+                                                     ("kda", 1540), ("pkda", 1548),
+                                                     ("ikdn", 1544)])
 def test_forward_bytes_per_head_token(variant, per_head_token):
     name = {"gdn": "gdn_kla_bf16", "kla": "gdn_kla_bf16", "pgdn": "pgdn_bf16",
-            "kdn": "kdn_bf16", "kda": "kda_bf16", "pkda": "pkda_bf16"}[variant]
+            "kdn": "kdn_bf16", "kda": "kda_bf16", "pkda": "pkda_bf16",
+            "ikdn": "ikdn_bf16"}[variant]
     wl = W.WORKLOADS[name]
     ht = wl.B * wl.T * wl.H
     extra = wl.H * 4 if variant in ("pgdn", "pkda") else 0     # the per-head mu

@@ -16,7 +16,7 @@ from recurrent_associative_memory_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 BASE = {"gdn": "gdn_kla_bf16", "kla": "gdn_kla_bf16", "pgdn": "pgdn_bf16", "kdn": "kdn_bf16",
-        "kda": "kda_bf16", "pkda": "pkda_bf16"}
+        "kda": "kda_bf16", "pkda": "pkda_bf16", "ikdn": "ikdn_bf16"}
 
 
 @pytest.fixture(scope="module")
@@ -41,6 +41,8 @@ def random_state(inp, seed=3):
         aux0 = torch.rand(B, H, dk, generator=g) * 2.0
     if inp["variant"] == "kdn":
         aux0 = 0.5 + torch.rand(B, H, dk, generator=g)
+    if inp["variant"] == "ikdn":   # one variance per head
+        aux0 = 0.5 + torch.rand(B, H, generator=g)
     return S0, aux0
 
 
@@ -134,7 +136,7 @@ def test_kdn_information_scale_dk(rt):
 # ------------------------------------------------------------ decode step
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-@pytest.mark.parametrize("variant", ["gdn", "kla", "pgdn", "kdn", "kda", "pkda"])
+@pytest.mark.parametrize("variant", ["gdn", "kla", "pgdn", "kdn", "kda", "pkda", "ikdn"])
 def test_decode_steps_match_oracle(rt, variant, dtype):
     dr, runner = rt
     inp = small_inputs(variant, dtype, B=3, T=12, H=2, seed=21)
@@ -325,7 +327,7 @@ def test_kdn_two_phase_and_fused_paths(rt, dtype, workspace):
     check_fwd(rt, inp, S0, aux0, workspace=workspace)
 
 
-@pytest.mark.parametrize("variant", ["kdn", "pkda"])
+@pytest.mark.parametrize("variant", ["kdn", "pkda", "ikdn"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 def test_kdn_chained_variance_many_rows(rt, dtype, variant):
     """With many (b, h) rows (three times the rows at least the SM count) the
@@ -355,7 +357,7 @@ def test_kdn_chained_variance_many_rows(rt, dtype, variant):
 
 @pytest.mark.parametrize("workspace", ["auto", None])
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-@pytest.mark.parametrize("variant", ["kda", "pkda"])
+@pytest.mark.parametrize("variant", ["kda", "pkda", "ikdn"])
 @pytest.mark.parametrize("T", [1, 63, 130])
 def test_per_channel_decay_variants(rt, variant, dtype, T, workspace):
     """KDA (w = eta k, D = diag(alpha)) and PKDA (the PGDN write key under
@@ -368,7 +370,7 @@ def test_per_channel_decay_variants(rt, variant, dtype, T, workspace):
     check_fwd(rt, inp, S0, aux0, workspace=workspace)
 
 
-@pytest.mark.parametrize("variant", ["kda", "pkda"])
+@pytest.mark.parametrize("variant", ["kda", "pkda", "ikdn"])
 def test_per_channel_decay_head_dims_and_chunks(rt, variant):
     for dk, dv, chunk in [(64, 128, 64), (128, 64, 32), (64, 64, 128)]:
         inp = small_inputs(variant, "bf16", B=1, T=150, H=2, d=dk, dv=dv, chunk=chunk, seed=dk + dv)
@@ -376,7 +378,8 @@ def test_per_channel_decay_head_dims_and_chunks(rt, variant):
         check_fwd(rt, inp, S0, aux0, chunk=chunk)
 
 
-@pytest.mark.parametrize("name,variant", [("kda_bf16", "kda"), ("pkda_bf16", "pkda")])
+@pytest.mark.parametrize("name,variant", [("kda_bf16", "kda"), ("pkda_bf16", "pkda"),
+                                          ("ikdn_bf16", "ikdn")])
 def test_per_channel_decay_workloads_sampled(rt, name, variant):
     wl = W.WORKLOADS[name]
     inp = W.generate(wl, variant)
