@@ -10,8 +10,8 @@ holds none of the method's arithmetic.
 Modules
 -------
 recurrence  Tokenwise recurrence (the plain definition) for GDN, KLA, PGDN,
-            Diagonal KDN, KDA, PKDA and isotropic KDN, one token at a time,
-            in float64.
+            Diagonal KDN, KDA, PKDA, isotropic KDN and the exact Kalman memory
+            (dense key covariance), one token at a time, in float64.
 chunkwise   A naive chunkwise-parallel restatement (triangular system per
             chunk), written independently of ``recurrence`` as a cross-check.
 ridge       Side oracles fixed by closed forms: exact ridge regression (ATQ),
@@ -25,6 +25,7 @@ brute force; none is "parity unpinned".
 
 from .recurrence import (  # noqa: F401
     VARIANTS,
+    TOKENWISE_ONLY,
     l2normalize,
     gdn_write,
     kla_write,
@@ -36,6 +37,9 @@ from .recurrence import (  # noqa: F401
     ikdn_predict,
     ikdn_gain,
     ikdn_variance_update,
+    ekdn_predict,
+    ekdn_gain,
+    ekdn_cov_update,
     recurrence_step,
     tokenwise,
 )

@@ -24,6 +24,9 @@ with S in R^{dk x dv}, D_t = alpha_t I (GDN, KLA, PGDN) or diag(alpha_t)
     IKDN  isotropic KDN, one variance b per head       (KDN notes section 7, Eq. (40))
           a = mean_i alpha_i^2 ; b^ = a b_{t-1} + omega ; beta = b^ / (r + b^ ||k||^2)
           w = beta k ; b_t = b^ / (1 + u b^), u = mu ||k||^2 / (dk r)
+    EKDN  exact Kalman memory, dense key covariance P   (KDN notes section 2.2,
+          P^ = D P D^T + diag(omega) ; w = P^ k / (r + k^T P^ k)   Eqs. (12)-(17))
+          P_t = (I - w k^T) P^       (tokenwise only: the pages give it no chunk form)
     KDN   p^ = alpha^2 * p_{t-1} + omega            (KDN notes Eq. (23))
           kappa = p^ * k / (r + sum(p^ k^2)) ; w = kappa
           p_t = p^ / (1 + (mu/r) k*k * p^)          (KDN notes Eqs. (60)-(65))
@@ -39,6 +42,7 @@ from __future__ import annotations
 import numpy as np
 
 VARIANTS = ("gdn", "kla", "pgdn", "kdn", "kda", "pkda", "ikdn")
+TOKENWISE_ONLY = ("ekdn",)   # a dense Riccati recursion, no chunkwise restatement
 
 
 def l2normalize(x: np.ndarray, floor: float = 1e-30) -> np.ndarray:
@@ -131,6 +135,24 @@ def ikdn_variance_update(b_hat, k, r, mu: float):
     return b_hat / (1.0 + u * b_hat)
 
 
+def ekdn_predict(P_prev, alpha, omega):
+    """Predicted dense key covariance P^ = D P D^T + diag(omega), D = diag(alpha)
+    (KDN notes section 2.2, Eq. (12)).  P [..., dk, dk]; alpha, omega [..., dk]."""
+    P_hat = alpha[..., :, None] * P_prev * alpha[..., None, :]
+    return P_hat + omega[..., :, None] * np.eye(P_prev.shape[-1])
+
+
+def ekdn_gain(P_hat, k, r):
+    """Kalman gain kappa = P^ k / (r + k^T P^ k) (KDN notes section 2.2, Eq. (13))."""
+    Pk = np.einsum("...ij,...j->...i", P_hat, k)
+    return Pk / (r + np.sum(k * Pk, axis=-1))[..., None]
+
+
+def ekdn_cov_update(P_hat, kappa, k):
+    """Posterior covariance P = (I - kappa k^T) P^ (KDN notes section 2.2, Eq. (15))."""
+    return P_hat - kappa[..., :, None] * np.einsum("...j,...jl->...l", k, P_hat)[..., None, :]
+
+
 # ---------------------------------------------------------------- the recurrence
 
 def recurrence_step(S, q, k, v, decay, w):
@@ -164,11 +186,12 @@ def tokenwise(q, k, v, log_alpha, variant: str, *, eta=None, eps: float = 1e-6,
                                            (isotropic KDN: omega [B,T,H]).
     log_alpha [B,T,H] (scalar decay) or [B,T,H,dk] (KDA, PKDA, KDN).
     S0 [B,H,dk,dv] (None = 0); aux0 [B,H,dk]: PGDN / PKDA A_0 (None = 0) or
-    KDN p_0 (None = 1); isotropic KDN b_0 [B,H] (None = 1).
+    KDN p_0 (None = 1); isotropic KDN b_0 [B,H] (None = 1); exact Kalman P_0
+    [B,H,dk,dk] (None = I).
     Returns (o [B,T,H,dv], S_T [B,H,dk,dv], aux_T [B,H,dk] or None); with
     ``return_trace`` also a dict of per-token write vectors and residuals.
     """
-    if variant not in VARIANTS:
+    if variant not in VARIANTS + TOKENWISE_ONLY:
         raise ValueError(f"unknown variant {variant!r}")
     f = lambda a: None if a is None else np.asarray(a, dtype=np.float64)  # noqa: E731
     q, k, v, log_alpha = f(q), f(k), f(v), f(log_alpha)
@@ -188,6 +211,9 @@ def tokenwise(q, k, v, log_alpha, variant: str, *, eta=None, eps: float = 1e-6,
         aux = np.ones((B, H, dk)) if aux0 is None else np.array(aux0, dtype=np.float64)
     elif variant == "ikdn":
         aux = np.ones((B, H)) if aux0 is None else np.array(aux0, dtype=np.float64)
+    elif variant == "ekdn":   # dense covariance P [B, H, dk, dk], P_0 = I by default
+        aux = (np.broadcast_to(np.eye(dk), (B, H, dk, dk)).copy() if aux0 is None
+               else np.array(aux0, dtype=np.float64))
 
     o = np.zeros((B, T, H, dv))
     trace = {"w": np.zeros((B, T, H, dk)), "e": np.zeros((B, T, H, dv))} if return_trace else None
@@ -202,6 +228,10 @@ def tokenwise(q, k, v, log_alpha, variant: str, *, eta=None, eps: float = 1e-6,
             aux = pgdn_stat_update(aux, kt, alphaP[:, t], betaP[:, t])
             Bscale = pgdn_squash(aux, mu[None, :, None], x, log_floor)
             w = eta[:, t][..., None] * (Bscale * kt)
+        elif variant == "ekdn":
+            P_hat = ekdn_predict(aux, alpha, omega[:, t])
+            w = ekdn_gain(P_hat, kt, r[:, t])
+            aux = ekdn_cov_update(P_hat, w, kt)
         elif variant == "ikdn":
             b_hat = ikdn_predict(aux, alpha, omega[:, t])
             w = ikdn_gain(b_hat, kt, r[:, t])

@@ -34,6 +34,9 @@ contexts up to 64K) with these distributions:
   as for PGDN; per-channel log alpha as for Diagonal KDN; omega =
   softplus(N(-3,1)) and r = softplus(N(0,1)) per (b,t,h); b_0 = 1;
   information scale 1.
+* ``ekdn_bf16``        exact Kalman memory (dense key covariance), bf16, B=4
+  H=16 T=2048 d=128; gates as for Diagonal KDN (per-channel log alpha and
+  omega, r per (b,t,h)); P_0 = I.
 * ``kla_prefill_bf16`` KLA, bf16, B=1 H=16 T=65536 d=128, inputs as
   ``gdn_kla_bf16``.
 * ``kla_decode_bf16``  KLA decode steps at batch 256, H=16, d=128; fresh
@@ -90,6 +93,8 @@ WORKLOADS = {
                           k_l2norm=True, seed=1006),
     "ikdn_bf16": Workload("ikdn_bf16", ("ikdn",), 4, 8192, 16, 128, 128, 64, "bf16",
                           k_l2norm=True, seed=1007),
+    "ekdn_bf16": Workload("ekdn_bf16", ("ekdn",), 4, 2048, 16, 128, 128, 64, "bf16",
+                          k_l2norm=True, seed=1008),
     "kla_prefill_bf16": Workload("kla_prefill_bf16", ("kla",), 1, 65536, 16, 128, 128, 64,
                                  "bf16", key_dist="lognormal_scaled", seed=1004),
     "kla_decode_bf16": Workload("kla_decode_bf16", ("kla",), 256, 1, 16, 128, 128, 64, "bf16",
@@ -134,7 +139,7 @@ def _draw_gates(gen, wl: Workload, variant: str, B, T):
         g["mu"] = torch.exp(0.5 * torch.randn(H, generator=gen))
         g["eta"] = torch.sigmoid(torch.randn(B, T, H, generator=gen))
         g["log_alpha"] = -_softplus(torch.randn(B, T, H, generator=gen) + 2.0)
-    elif variant == "kdn":
+    elif variant in ("kdn", "ekdn"):
         g["log_alpha"] = -_softplus(torch.randn(B, T, H, dk, generator=gen) + 2.0)
         g["omega"] = _softplus(torch.randn(B, T, H, dk, generator=gen) - 3.0)
         g["r"] = _softplus(torch.randn(B, T, H, generator=gen))

@@ -418,6 +418,67 @@ def test_isotropic_kdn_predicts_with_the_mean_squared_decay():
     assert abs(other - expect) > 1e-3 * expect
 
 
+# ------------------------------------------------------------------ exact Kalman memory
+
+def test_exact_kalman_tokenwise_matches_dense_side_oracle():
+    """The batched tokenwise exact Kalman variant equals the independently written
+    single-head dense filter (KDN notes section 2.2, Eqs. (12)-(17)) on random
+    data, head by head, from a random SPD P_0."""
+    r_ = rng(41)
+    B, T, H, dk, dv = 2, 13, 2, 5, 3
+    d = random_inputs("kdn", B=B, T=T, H=H, dk=dk, dv=dv, seed=42)
+    A = r_.standard_normal((B, H, dk, dk))
+    P0 = A @ np.swapaxes(A, -1, -2) / dk + 0.5 * np.eye(dk)
+    o, S, P = call(oracle.tokenwise, "ekdn", d, aux0=P0)
+    for b in range(B):
+        for h in range(H):
+            o_r, S_r, P_r, _ = ridge.dense_kalman(d["q"][b, :, h], d["k"][b, :, h], d["v"][b, :, h],
+                                                  np.exp(d["log_alpha"][b, :, h]),
+                                                  d["omega"][b, :, h], d["r"][b, :, h], P0[b, h])
+            np.testing.assert_allclose(o[b, :, h], o_r, rtol=1e-11, atol=1e-12)
+            np.testing.assert_allclose(S[b, h], S_r, rtol=1e-11, atol=1e-12)
+            np.testing.assert_allclose(P[b, h], P_r, rtol=1e-11, atol=1e-12)
+
+
+def test_exact_kalman_with_axis_keys_is_diagonal_kdn():
+    """Keys along coordinate axes keep a diagonal covariance diagonal, so the exact
+    filter and Diagonal KDN (mu = 1) agree (KDN notes Eqs. (12)-(17) vs (23)-(30))."""
+    r_ = rng(43)
+    B, T, H, dk, dv = 1, 17, 2, 4, 3
+    d = random_inputs("kdn", B=B, T=T, H=H, dk=dk, dv=dv, seed=44)
+    axes = r_.integers(0, dk, (B, T, H))
+    d["k"] = np.eye(dk)[axes] * r_.uniform(0.5, 2.0, (B, T, H, 1))
+    p0 = r_.uniform(0.5, 1.5, (B, H, dk))
+    o1, S1, p1 = call(oracle.tokenwise, "kdn", d, aux0=p0, info_scale=1.0)
+    o2, S2, P2 = call(oracle.tokenwise, "ekdn", d, aux0=p0[..., :, None] * np.eye(dk))
+    np.testing.assert_allclose(o2, o1, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(S2, S1, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(np.diagonal(P2, axis1=-2, axis2=-1), p1, rtol=1e-12)
+    np.testing.assert_allclose(P2 - np.diagonal(P2, axis1=-2, axis2=-1)[..., None] * np.eye(dk), 0,
+                               atol=1e-15)
+
+
+def test_exact_kalman_scalar_gain_example():
+    """dk = 1: the pages' scalar gains (k = r = 1: P^ = 9 -> 0.9, 0.1 -> 0.0909)."""
+    g = golden("kalman_scalar_example.json")
+    tol = 0.5 * 10 ** -g["printed_decimals"]
+    for p_hat, expect in g["gain_at_predicted_variance"].items():
+        kap = oracle.ekdn_gain(np.array([[float(p_hat)]]), np.array([g["k"]]), np.array(g["r"]))
+        assert kap[0] == pytest.approx(expect, abs=tol)
+
+
+def test_exact_kalman_resume_split_equals_whole():
+    """The state (S, P) is the whole checkpoint: fwd(T) = fwd(T1) then fwd(T2)."""
+    d = random_inputs("kdn", B=1, T=20, H=2, dk=4, dv=3, seed=45)
+    o, S, P = call(oracle.tokenwise, "ekdn", d, q_l2norm=True)
+    head = {k: (v[:, :9] if v.ndim >= 3 else v) for k, v in d.items()}
+    tail = {k: (v[:, 9:] if v.ndim >= 3 else v) for k, v in d.items()}
+    o1, S1, P1 = call(oracle.tokenwise, "ekdn", head, q_l2norm=True)
+    o2, S2, P2 = call(oracle.tokenwise, "ekdn", tail, S0=S1, aux0=P1, q_l2norm=True)
+    np.testing.assert_allclose(np.concatenate([o1, o2], axis=1), o, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(P2, P, rtol=1e-11, atol=1e-13)
+
+
 # ------------------------------------------------------------------ P8: tokenwise == chunkwise
 
 CASES = [  # (T, dk, dv, chunk)
