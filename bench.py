@@ -72,6 +72,7 @@ KERNEL_SOURCES = {
     "chunk_tc": ["chunk_tc.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh"],
     "chunk_simt": ["chunk_simt.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh", "chain.cuh"],
     "decode": ["decode.cu", "dr_common.cuh"],
+    "kalman": ["kalman.cu", "dr_common.cuh"],
 }
 
 
@@ -117,7 +118,8 @@ def fwd_bytes(wl, variant, with_final=True):
     ht = wl.B * wl.T * wl.H
     per_ht = (2 * wl.dk + 2 * wl.dv) * el          # q, k, v, o
     gates = {"gdn": 8, "kla": 8, "pgdn": 16, "kdn": 8 * wl.dk + 4,
-             "kda": 4 * wl.dk + 4, "pkda": 4 * wl.dk + 12, "ikdn": 4 * wl.dk + 8}[variant]
+             "kda": 4 * wl.dk + 4, "pkda": 4 * wl.dk + 12, "ikdn": 4 * wl.dk + 8,
+             "ekdn": 8 * wl.dk + 4}[variant]
     total = ht * (per_ht + gates)
     if variant in ("pgdn", "pkda"):
         total += wl.H * 4
@@ -127,6 +129,8 @@ def fwd_bytes(wl, variant, with_final=True):
             total += wl.B * wl.H * wl.dk * 4
         if variant == "ikdn":   # one variance per head
             total += wl.B * wl.H * 4
+        if variant == "ekdn":   # the dense covariance
+            total += wl.B * wl.H * wl.dk * wl.dk * 4
     return total
 
 

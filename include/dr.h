@@ -12,7 +12,8 @@
  *
  * S_t is a dk x dv fp32 matrix per (batch, head).  D_t = alpha_t I for GDN, KLA
  * and PGDN, diag(alpha_t) (scaling the rows of S) for Diagonal KDN, KDA and
- * PKDA, isotropic KDN; alpha = exp(log_alpha).  The write vector w_t per variant:
+ * PKDA, isotropic KDN, exact Kalman; alpha = exp(log_alpha).  The write vector w_t
+ * per variant:
  *
  *   DR_GDN   w = eta k                        (KLA notes section 1.1)
  *   DR_KLA   w = eta k / (||k||^2 + eps)      (KLA notes Eq. (3), Algorithm 1)
@@ -29,6 +30,10 @@
  *            a = mean_i alpha_i^2;  b^ = a b_{t-1} + omega;  w = b^ k / (r + b^ ||k||^2);
  *            b_t = b^ / (1 + info_scale ||k||^2 b^ / (dk r))
  *                                             (KDN notes section 7, Eq. (40))
+ *   DR_EKDN  exact Kalman memory, dense key covariance P (dk x dk), per-channel decay:
+ *            P^ = D P D^T + diag(omega);  w = P^ k / (r + k^T P^ k);  P_t = (I - w k^T) P^
+ *                                             (KDN notes section 2.2, Eqs. (12)-(17));
+ *            token by token (no chunked form; `chunk` is checked but unused)
  *
  * q and k are L2-normalised first when the corresponding flag is set
  * (q / max(||q||, 1e-30)); KLA reads out with the normalised query (KLA notes
@@ -36,10 +41,10 @@
  *
  * Layouts (row-major, innermost index last):
  *   q, k     [B, T, H, dk]      v, out [B, T, H, dv]     (decode: T absent)
- *   log_alpha [B, T, H]  (KDN, KDA, PKDA, IKDN: [B, T, H, dk])
+ *   log_alpha [B, T, H]  (KDN, KDA, PKDA, IKDN, EKDN: [B, T, H, dk])
  *   eta, alphaP, betaP, r [B, T, H];  omega [B, T, H, dk] (IKDN [B, T, H]);  mu [H]
  *   state    [B, H, dk, dv] fp32;  aux (PGDN / PKDA A, KDN p) [B, H, dk] fp32,
- *            (IKDN b) [B, H] fp32
+ *            (IKDN b) [B, H] fp32, (EKDN P) [B, H, dk, dk] fp32
  * q/k/v/out are fp32 (DR_FP32) or bf16 (DR_BF16); every gate and state is fp32.
  *
  * Ownership: the caller owns every buffer; all pointers are device pointers
@@ -67,7 +72,8 @@ struct CUstream_st;
 typedef struct CUstream_st *dr_stream_t;
 
 typedef enum {
-  DR_GDN = 0, DR_KLA = 1, DR_PGDN = 2, DR_KDN = 3, DR_KDA = 4, DR_PKDA = 5, DR_IKDN = 6
+  DR_GDN = 0, DR_KLA = 1, DR_PGDN = 2, DR_KDN = 3, DR_KDA = 4, DR_PKDA = 5, DR_IKDN = 6,
+  DR_EKDN = 7
 } dr_variant;
 
 typedef enum { DR_FP32 = 0, DR_BF16 = 1 } dr_dtype;
@@ -98,11 +104,11 @@ typedef struct dr_params {
   const float *mu;         /* PGDN/PKDA per-head centre [H]                           */
   float x;                 /* PGDN bound, B in [1/x, x]; default 1.5                  */
   float log_floor;         /* PGDN guard: ln max(A, log_floor); default 1e-12         */
-  const float *omega;      /* KDN process noise [B,T,H,dk] (decode [B,H,dk]); IKDN [B,T,H] */
+  const float *omega;      /* KDN/EKDN process noise [B,T,H,dk] (decode [B,H,dk]); IKDN [B,T,H] */
   const float *r;          /* KDN/IKDN observation noise [B,T,H] (decode [B,H]), > 0  */
   float info_scale;        /* KDN/IKDN information scaling mu; default 1 (strict)     */
   const float *aux_init;   /* dr_chunk_fwd: PGDN/PKDA A_0, KDN p_0 [B,H,dk], IKDN b_0
-                              [B,H]; NULL => 0, 1, 1                                  */
+                              [B,H], EKDN P_0 [B,H,dk,dk]; NULL => 0, 1, 1, I          */
   float *aux_final;        /* dr_chunk_fwd: final A / p [B,H,dk]; NULL => not written */
   void *workspace;         /* dr_chunk_fwd: caller-owned device scratch, 256-byte     */
   size_t workspace_bytes;  /* aligned, or NULL (see dr_chunk_fwd_workspace_bytes)     */
@@ -232,7 +238,8 @@ const char *dr_status_string(int status);
  *          PKDA the fused kernel), then the state carry -- the tcgen05 carry
  *          for bf16 inputs, fp32 CUDA cores for fp32
  * "simt"   fp32 CUDA-core kernel (everything else: fp32 mode, KDN / KDA / PKDA
- *          without a workspace, dk or dv 64, other chunk sizes). */
+ *          without a workspace, dk or dv 64, other chunk sizes)
+ * "kalman" the exact Kalman memory, token by token (DR_EKDN, any shape). */
 const char *dr_chunk_fwd_path(int variant, int dtype, int dk, int dv, int chunk);
 
 #ifdef __cplusplus

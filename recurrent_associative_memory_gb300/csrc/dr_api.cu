@@ -20,6 +20,8 @@ cudaError_t launch_chunk_tc_split(const FwdArgs& a, void* workspace, cudaStream_
 bool chunk_tc_split_supported(int variant, int dtype, int dk, int dv, int chunk);
 size_t chunk_tc_split_workspace_bytes(int variant, int B, int T, int H);
 cudaError_t launch_kdn_split(const FwdArgs& a, int dtype, void* workspace, cudaStream_t st);
+int kalman_sm_count();
+cudaError_t launch_kalman(const FwdArgs& a, int dtype, cudaStream_t st, bool whole_columns);
 bool kdn_split_supported(int variant, int dtype, int dk, int dv, int chunk);
 size_t kdn_split_workspace_bytes(int B, int T, int H);
 
@@ -44,6 +46,7 @@ int check_gates(const dr_params* gp, int variant) {
       return DR_OK;
     case DR_KDN:
     case DR_IKDN:
+    case DR_EKDN:
       if (!gp->omega || !gp->r) return DR_ERR_NULL;
       if (!(gp->info_scale >= 0.f)) return DR_ERR_ARG;
       return DR_OK;
@@ -127,6 +130,7 @@ size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H,
 }
 
 const char* dr_chunk_fwd_path(int variant, int dtype, int dk, int dv, int chunk) {
+  if (variant == DR_EKDN) return "kalman";
   if (chunk_tc_split_supported(variant, dtype, dk, dv, chunk)) return "tc_split";
   if (kdn_split_supported(variant, dtype, dk, dv, chunk)) return "simt_split";
   if (chunk_tc_ws_supported(variant, dtype, dk, dv, chunk)) return "tc_ws";
@@ -148,7 +152,8 @@ int dr_chunk_fwd(const void* q, const void* k, const void* v, const float* log_a
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
       !aligned16(init_state) || !aligned16(final_state) || !aligned16(log_alpha))
     return DR_ERR_ALIGN;
-  if (variant == DR_KDN && !aligned16(gp->omega)) return DR_ERR_ALIGN;   // copied in 16-byte pieces
+  if ((variant == DR_KDN || variant == DR_EKDN) && !aligned16(gp->omega))
+    return DR_ERR_ALIGN;   // copied in 16-byte pieces
   // per-channel log-decay is copied in 16-byte pieces too (checked above)
 
   FwdArgs a = make_args(q, k, v, log_alpha, gp, variant, eps, B, T, H, dk, dv, chunk);
@@ -174,6 +179,8 @@ int dr_chunk_fwd(const void* q, const void* k, const void* v, const float* log_a
     err = launch_chunk_tc_ws(a, s);          // GDN / KLA: warp-specialised tensor-core kernel
   else if (chunk_tc_supported(variant, gp->dtype, dk, dv, chunk))
     err = launch_chunk_tc(a, s);             // PGDN: phase-sequential tensor-core kernel
+  else if (variant == DR_EKDN)
+    err = launch_kalman(a, gp->dtype, s, B * H * 4 > 2 * kalman_sm_count());   // exact Kalman
   else
     err = launch_chunk_simt(a, gp->dtype, s);
   return err == cudaSuccess ? DR_OK : DR_ERR_CUDA;
@@ -188,7 +195,8 @@ int dr_decode_step(const void* q, const void* k, const void* v, const float* log
   if (!(eps >= 0.f)) return DR_ERR_ARG;
   int st = check_gates(gp, variant);
   if (st != DR_OK) return st;
-  if ((variant == DR_PGDN || variant == DR_KDN || variant == DR_PKDA || variant == DR_IKDN) &&
+  if ((variant == DR_PGDN || variant == DR_KDN || variant == DR_PKDA || variant == DR_IKDN ||
+       variant == DR_EKDN) &&
       !aux_state)
     return DR_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
@@ -198,7 +206,14 @@ int dr_decode_step(const void* q, const void* k, const void* v, const float* log
   a.S = state;
   a.aux = aux_state;
   a.out = out;
-  cudaError_t err = launch_decode(a, gp->dtype, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t err;
+  if (variant == DR_EKDN) {   // the exact filter's step: one CTA per head, S and P in place
+    a.S0 = state;
+    a.aux0 = aux_state;
+    err = launch_kalman(a, gp->dtype, reinterpret_cast<cudaStream_t>(stream), true);
+  } else {
+    err = launch_decode(a, gp->dtype, reinterpret_cast<cudaStream_t>(stream));
+  }
   return err == cudaSuccess ? DR_OK : DR_ERR_CUDA;
 }
 

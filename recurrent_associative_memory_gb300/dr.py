@@ -27,9 +27,9 @@ if not os.path.exists(LIB_PATH):
                       "`python -m recurrent_associative_memory_gb300.build` (needs nvcc)")
 _lib = ctypes.CDLL(LIB_PATH)
 
-DR_GDN, DR_KLA, DR_PGDN, DR_KDN, DR_KDA, DR_PKDA, DR_IKDN = 0, 1, 2, 3, 4, 5, 6
+DR_GDN, DR_KLA, DR_PGDN, DR_KDN, DR_KDA, DR_PKDA, DR_IKDN, DR_EKDN = 0, 1, 2, 3, 4, 5, 6, 7
 VARIANT_IDS = {"gdn": DR_GDN, "kla": DR_KLA, "pgdn": DR_PGDN, "kdn": DR_KDN, "kda": DR_KDA,
-               "pkda": DR_PKDA, "ikdn": DR_IKDN}
+               "pkda": DR_PKDA, "ikdn": DR_IKDN, "ekdn": DR_EKDN}
 DR_FP32, DR_BF16 = 0, 1
 STATUS = {0: "DR_OK", -1: "DR_ERR_NULL", -2: "DR_ERR_SHAPE", -3: "DR_ERR_DTYPE",
           -4: "DR_ERR_ALIGN", -5: "DR_ERR_WORKSPACE", -6: "DR_ERR_CUDA", -7: "DR_ERR_TIMEOUT",

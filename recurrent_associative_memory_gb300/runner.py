@@ -62,6 +62,8 @@ def chunk_fwd(inp: dict, *, init_state=None, aux_init=None, chunk=None, want_fin
         aux_final = torch.empty(B, H, dk, dtype=torch.float32, device=q.device)
     if want_final and aux_final is None and inp["variant"] == "ikdn":   # one variance per head
         aux_final = torch.empty(B, H, dtype=torch.float32, device=q.device)
+    if want_final and aux_final is None and inp["variant"] == "ekdn":   # dense covariance
+        aux_final = torch.empty(B, H, dk, dk, dtype=torch.float32, device=q.device)
     p = params_for(inp, aux_init=aux_init, aux_final=aux_final, check_finite=check_finite)
     if workspace is not None:
         p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()

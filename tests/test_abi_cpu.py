@@ -102,6 +102,8 @@ def test_status_strings(dr):
     assert dr.dr_chunk_fwd_path(dr.DR_PGDN, dr.DR_BF16, 128, 128, 64) == "tc_split"
     assert dr.dr_chunk_fwd_path(dr.DR_KLA, dr.DR_FP32, 64, 64, 64) == "simt"
     # KDA, PKDA and isotropic KDN take Diagonal KDN's two-phase path (same records)
+    assert dr.dr_chunk_fwd_path(dr.DR_EKDN, dr.DR_FP32, 64, 64, 16) == "kalman"
+    assert dr.dr_chunk_fwd_workspace_bytes(7, 1, 4, 2048, 16, 128, 128, 64) == 0
     for vid in (dr.DR_KDA, dr.DR_PKDA, dr.DR_IKDN):
         assert dr.dr_chunk_fwd_path(vid, dr.DR_BF16, 128, 128, 64) == "simt_split"
         assert dr.dr_chunk_fwd_workspace_bytes(vid, 1, 4, 8192, 16, 128, 128, 64) == \
@@ -129,7 +131,8 @@ def test_chunk_fwd_rejects_bad_arguments(dr):
     assert fwd(dr, variant=5) == dr.DR_ERR_NULL                # PKDA without alphaP/betaP/mu
     assert fwd(dr, variant=5, alphaP=A, betaP=A, mu=A, x=0.5) == dr.DR_ERR_ARG
     assert fwd(dr, variant=6, r=A) == dr.DR_ERR_NULL           # isotropic KDN without omega
-    assert fwd(dr, variant=7) == dr.DR_ERR_UNSUPPORTED
+    assert fwd(dr, variant=7, omega=A) == dr.DR_ERR_NULL       # exact Kalman without r
+    assert fwd(dr, variant=8) == dr.DR_ERR_UNSUPPORTED
     assert fwd(dr, dtype=5) == dr.DR_ERR_DTYPE
     assert fwd(dr, dk=96) == dr.DR_ERR_SHAPE
     assert fwd(dr, dv=32) == dr.DR_ERR_SHAPE
@@ -143,6 +146,7 @@ def test_chunk_fwd_rejects_bad_arguments(dr):
     assert fwd(dr, fin=MIS) == dr.DR_ERR_ALIGN
     assert fwd(dr, init=MIS) == dr.DR_ERR_ALIGN
     assert fwd(dr, variant=3, omega=MIS, r=A) == dr.DR_ERR_ALIGN
+    assert fwd(dr, variant=7, omega=MIS, r=A) == dr.DR_ERR_ALIGN
 
 
 def test_decode_rejects_bad_arguments(dr):
@@ -155,6 +159,7 @@ def test_decode_rejects_bad_arguments(dr):
     assert dec(variant=3, omega=A, r=A) == dr.DR_ERR_NULL
     assert dec(variant=5, alphaP=A, betaP=A, mu=A) == dr.DR_ERR_NULL   # PKDA: aux state required
     assert dec(variant=6, omega=A, r=A) == dr.DR_ERR_NULL              # isotropic KDN: its b
+    assert dec(variant=7, omega=A, r=A) == dr.DR_ERR_NULL              # exact Kalman: its P
     assert dec(dk=32) == dr.DR_ERR_SHAPE
     assert dec(state=MIS) == dr.DR_ERR_ALIGN
     assert dec(dtype=2) == dr.DR_ERR_DTYPE

@@ -22,11 +22,11 @@ from recurrent_associative_memory_gb300 import workloads as W  # noqa: E402
 @pytest.mark.parametrize("variant,per_head_token", [("gdn", 1032), ("kla", 1032),
                                                      ("pgdn", 1040), ("kdn", 2052),
                                                      ("kda", 1540), ("pkda", 1548),
-                                                     ("ikdn", 1544)])
+                                                     ("ikdn", 1544), ("ekdn", 2052)])
 def test_forward_bytes_per_head_token(variant, per_head_token):
     name = {"gdn": "gdn_kla_bf16", "kla": "gdn_kla_bf16", "pgdn": "pgdn_bf16",
             "kdn": "kdn_bf16", "kda": "kda_bf16", "pkda": "pkda_bf16",
-            "ikdn": "ikdn_bf16"}[variant]
+            "ikdn": "ikdn_bf16", "ekdn": "ekdn_bf16"}[variant]
     wl = W.WORKLOADS[name]
     ht = wl.B * wl.T * wl.H
     extra = wl.H * 4 if variant in ("pgdn", "pkda") else 0     # the per-head mu

@@ -16,7 +16,7 @@ from recurrent_associative_memory_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 BASE = {"gdn": "gdn_kla_bf16", "kla": "gdn_kla_bf16", "pgdn": "pgdn_bf16", "kdn": "kdn_bf16",
-        "kda": "kda_bf16", "pkda": "pkda_bf16", "ikdn": "ikdn_bf16"}
+        "kda": "kda_bf16", "pkda": "pkda_bf16", "ikdn": "ikdn_bf16", "ekdn": "ekdn_bf16"}
 
 
 @pytest.fixture(scope="module")
@@ -43,6 +43,9 @@ def random_state(inp, seed=3):
         aux0 = 0.5 + torch.rand(B, H, dk, generator=g)
     if inp["variant"] == "ikdn":   # one variance per head
         aux0 = 0.5 + torch.rand(B, H, generator=g)
+    if inp["variant"] == "ekdn":   # a random SPD key covariance
+        A = torch.randn(B, H, dk, dk, generator=g, dtype=torch.float64)
+        aux0 = (A @ A.transpose(-1, -2) / dk + 0.5 * torch.eye(dk, dtype=torch.float64)).float()
     return S0, aux0
 
 
@@ -136,7 +139,7 @@ def test_kdn_information_scale_dk(rt):
 # ------------------------------------------------------------ decode step
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-@pytest.mark.parametrize("variant", ["gdn", "kla", "pgdn", "kdn", "kda", "pkda", "ikdn"])
+@pytest.mark.parametrize("variant", ["gdn", "kla", "pgdn", "kdn", "kda", "pkda", "ikdn", "ekdn"])
 def test_decode_steps_match_oracle(rt, variant, dtype):
     dr, runner = rt
     inp = small_inputs(variant, dtype, B=3, T=12, H=2, seed=21)
@@ -383,6 +386,27 @@ def test_per_channel_decay_head_dims_and_chunks(rt, variant):
 def test_per_channel_decay_workloads_sampled(rt, name, variant):
     wl = W.WORKLOADS[name]
     inp = W.generate(wl, variant)
+    check_fwd(rt, inp, pairs=pick_pairs(wl.B, wl.H, 2))
+
+
+# ------------------------------------------------------------ exact Kalman memory
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("T", [1, 37])
+def test_exact_kalman_forward(rt, dtype, d, T):
+    """The dense-covariance filter token by token (32 state columns per CTA):
+    random initial state and SPD covariance, final state and covariance."""
+    dr, _ = rt
+    assert dr.dr_chunk_fwd_path(dr.DR_EKDN, dr.DR_BF16, 128, 128, 64) == "kalman"
+    inp = small_inputs("ekdn", dtype, B=2, T=T, H=3, d=d, seed=500 + T + d)
+    S0, aux0 = random_state(inp, seed=501 + T)
+    check_fwd(rt, inp, S0, aux0)
+
+
+def test_exact_kalman_workload_sampled(rt):
+    wl = W.WORKLOADS["ekdn_bf16"]
+    inp = W.generate(wl, "ekdn")
     check_fwd(rt, inp, pairs=pick_pairs(wl.B, wl.H, 2))
 
 
