@@ -208,7 +208,7 @@ size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H,
  * Returns DR_ERR_UNSUPPORTED for other variants, dtypes or shapes (dr_chunk_fwd
  * needs no workspace for those), DR_ERR_WORKSPACE when the records
  * (dr_chunk_fwd_workspace_bytes) would exceed DR_NOALLOC_SCRATCH_BYTES, i.e.
- * B H ceil(T/64) > 1008 (GDN, KLA), > 661 (PGDN) or > 496 (KDN), otherwise
+ * B H ceil(T/64) > 1008 (GDN, KLA), > 661 (PGDN) or > 496 (KDN, KDA, PKDA, IKDN), otherwise
  * whatever dr_chunk_fwd returns.
  */
 #define DR_NOALLOC_SCRATCH_BYTES (64u << 20)
