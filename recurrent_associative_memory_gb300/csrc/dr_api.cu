@@ -20,8 +20,7 @@ cudaError_t launch_chunk_tc_split(const FwdArgs& a, void* workspace, cudaStream_
 bool chunk_tc_split_supported(int variant, int dtype, int dk, int dv, int chunk);
 size_t chunk_tc_split_workspace_bytes(int variant, int B, int T, int H);
 cudaError_t launch_kdn_split(const FwdArgs& a, int dtype, void* workspace, cudaStream_t st);
-int kalman_sm_count();
-cudaError_t launch_kalman(const FwdArgs& a, int dtype, cudaStream_t st, bool whole_columns);
+cudaError_t launch_kalman(const FwdArgs& a, int dtype, cudaStream_t st);
 bool kdn_split_supported(int variant, int dtype, int dk, int dv, int chunk);
 size_t kdn_split_workspace_bytes(int B, int T, int H);
 
@@ -180,7 +179,7 @@ int dr_chunk_fwd(const void* q, const void* k, const void* v, const float* log_a
   else if (chunk_tc_supported(variant, gp->dtype, dk, dv, chunk))
     err = launch_chunk_tc(a, s);             // PGDN: phase-sequential tensor-core kernel
   else if (variant == DR_EKDN)
-    err = launch_kalman(a, gp->dtype, s, B * H * 4 > 2 * kalman_sm_count());   // exact Kalman
+    err = launch_kalman(a, gp->dtype, s);   // exact Kalman: token by token
   else
     err = launch_chunk_simt(a, gp->dtype, s);
   return err == cudaSuccess ? DR_OK : DR_ERR_CUDA;
@@ -210,7 +209,7 @@ int dr_decode_step(const void* q, const void* k, const void* v, const float* log
   if (variant == DR_EKDN) {   // the exact filter's step: one CTA per head, S and P in place
     a.S0 = state;
     a.aux0 = aux_state;
-    err = launch_kalman(a, gp->dtype, reinterpret_cast<cudaStream_t>(stream), true);
+    err = launch_kalman(a, gp->dtype, reinterpret_cast<cudaStream_t>(stream));
   } else {
     err = launch_decode(a, gp->dtype, reinterpret_cast<cudaStream_t>(stream));
   }

@@ -10,17 +10,14 @@
 // Riccati recursion with no chunked form (the notes' comparison table), so each
 // CTA walks the tokens of one (b, h) in order.
 //
-// CTA = 512 threads = 16 warps; warp w holds rows DK/16 w .. DK/16 (w + 1) - 1 of P
-// and of the CTA's NVC-column slice of S in registers, lane l the P columns
-// l + 32 c and the S columns l + 32 c.  The inputs arrive 16 tokens at a time
+// CTA = 512 threads = 16 warps, one CTA per (b, h), P and S in registers: warp w
+// holds DK/16 rows of P (lane l the columns l + 32 c) and DV/16 columns of S
+// (lane l the rows l + 32 c), so every reduction of a token stays inside a warp
+// except the two scalars z and y^T q.  The inputs arrive 16 tokens at a time
 // by cp.async into a double-buffered shared area, one block ahead; once a block
 // has landed, the normalised q and k and the decays of its 16 tokens are formed
 // in one pass, so the token loop reads shared memory only.  Two barriers per
-// token.  Forward: 32 state columns per CTA (the covariance is
-// recomputed by every slice, only slice 0 writes it) while those 4 B H CTAs fit
-// in one wave at one CTA per SM, else all columns in one CTA per head; the
-// decode step always takes the latter, so state and covariance are updated in
-// place.
+// token.  The decode step is the same kernel with T = 1.
 #include "dr_common.cuh"
 
 namespace dr {
@@ -44,61 +41,87 @@ __device__ __forceinline__ void kf_cp4(void* dst, const void* src, int src_bytes
                : "memory");
 }
 
+// Full sums over the 32 lanes of x[0 .. N-1] (N a power of two <= 32) by
+// halving exchanges: lane l ends up with the sum of x[(l >> (5 - log2 N)) & (N-1)]
+// (N - 1 + 5 - log2 N shuffles instead of 5 N).
+template <int N>
+__device__ __forceinline__ float reduce_scatter(const float* x, int lane, int mask) {
+  if constexpr (N == 1) {
+    float s = x[0];
+#pragma unroll
+    for (int m = mask; m >= 1; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+    return s;
+  } else {
+    const bool up = (lane & mask) != 0;   // this lane keeps the upper half
+    float w[N / 2];
+#pragma unroll
+    for (int r = 0; r < N / 2; ++r) {
+      const float send = up ? x[r] : x[r + N / 2];
+      const float keep = up ? x[r + N / 2] : x[r];
+      w[r] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+    }
+    return reduce_scatter<N / 2>(w, lane, mask >> 1);
+  }
+}
+template <int N> constexpr int kf_log2() { return N <= 1 ? 0 : 1 + kf_log2<N / 2>(); }
+
 // Dynamic shared memory of one CTA: two raw input blocks, then the processed
 // block (fp32 normalised k, q and the decays).
-template <int DK, int NVC, typename Tin>
+template <int DK, int DV, typename Tin>
 struct KfSmem {
-  static constexpr int kRaw = kKfTB * (2 * DK * (int)sizeof(Tin) + NVC * (int)sizeof(Tin) +
+  static constexpr int kRaw = kKfTB * (2 * DK * (int)sizeof(Tin) + DV * (int)sizeof(Tin) +
                                        2 * DK * 4) + kKfTB * 4;   // k, q, v, log alpha, omega, r
   static constexpr int kProc = 3 * kKfTB * DK * 4;                  // k^, q^, alpha
   static constexpr int bytes = 2 * kRaw + kProc;
 };
 
-template <int DK, int NVC, typename Tin>
+// One CTA per (b, h).  Covariance: warp w rows RW w .. RW w + RW - 1, lane l the
+// columns l + 32 c.  State: warp w the columns CPW w .. CPW w + CPW - 1, lane l
+// the rows l + 32 c -- so S^T k and S^T q reduce within a warp.
+template <int DK, int DV, typename Tin>
 __global__ void __launch_bounds__(kKfThreads, 1) kalman_kernel(FwdArgs a) {
-  constexpr int RW = DK / kKfWarps;   // rows per warp
-  constexpr int CPL = DK / 32;    // covariance columns per lane
-  constexpr int SPL = NVC / 32;   // state columns per lane
-  static_assert(RW <= 32 && CPL >= 1 && SPL >= 1, "tiling");
-  const int nsl = a.dv / NVC;
-  const int slice = blockIdx.x % nsl, bh = blockIdx.x / nsl;
+  constexpr int RW = DK / kKfWarps;   // covariance rows per warp
+  constexpr int CPL = DK / 32;        // covariance columns per lane = state rows per lane
+  constexpr int CPW = DV / kKfWarps;  // state columns per warp
+  constexpr int kOwnRW = 5 - kf_log2<RW>(), kOwnCW = 5 - kf_log2<CPW>();
+  static_assert(RW >= 1 && RW <= 32 && CPW >= 1 && CPW <= 32 && CPL >= 1, "tiling");
+  const int bh = blockIdx.x;
   const int b = bh / a.H, h = bh % a.H;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r0 = warp * RW;
+  const int r0 = warp * RW, v0 = warp * CPW;
 
   extern __shared__ __align__(16) uint8_t kf_smem[];
-  using SM = KfSmem<DK, NVC, Tin>;
+  using SM = KfSmem<DK, DV, Tin>;
   __shared__ float s_y[DK];
   __shared__ float s_zp[kKfWarps], s_yqp[kKfWarps];
-  __shared__ float s_dp[kKfWarps][NVC], s_qp[kKfWarps][NVC];
+  __shared__ float s_e[DV], s_sq[DV];
 
-  float P[RW][CPL], S[RW][SPL];
+  float P[RW][CPL], S[CPL][CPW];
 #pragma unroll
-  for (int i = 0; i < RW; ++i) {
+  for (int i = 0; i < RW; ++i)
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
       const int j = lane + 32 * c;
       P[i][c] = a.aux0 ? a.aux0[((long)bh * DK + r0 + i) * DK + j] : (r0 + i == j ? 1.f : 0.f);
     }
 #pragma unroll
-    for (int c = 0; c < SPL; ++c) {
-      const int v = slice * NVC + lane + 32 * c;
-      S[i][c] = a.S0 ? a.S0[((long)bh * DK + r0 + i) * a.dv + v] : 0.f;
-    }
-  }
+  for (int c = 0; c < CPL; ++c)
+#pragma unroll
+    for (int u = 0; u < CPW; ++u)
+      S[c][u] = a.S0 ? a.S0[((long)bh * DK + lane + 32 * c) * DV + v0 + u] : 0.f;
 
   auto tok = [&](int t) { return ((long)b * a.T + t) * a.H + h; };
-  // raw block layout (bytes): k [TB][DK], q [TB][DK], v [TB][NVC] (Tin), log alpha
+  // raw block layout (bytes): k [TB][DK], q [TB][DK], v [TB][DV] (Tin), log alpha
   // [TB][DK], omega [TB][DK], r [TB] (fp32)
   constexpr int oK = 0, oQ = kKfTB * DK * (int)sizeof(Tin), oV = 2 * oQ;
-  constexpr int oLA = oV + kKfTB * NVC * (int)sizeof(Tin), oOM = oLA + kKfTB * DK * 4;
+  constexpr int oLA = oV + kKfTB * DV * (int)sizeof(Tin), oOM = oLA + kKfTB * DK * 4;
   constexpr int oR = oOM + kKfTB * DK * 4;
   float* pk = reinterpret_cast<float*>(kf_smem + 2 * SM::kRaw);   // k^ [TB][DK]
   float* pq = pk + kKfTB * DK;                                      // q^ [TB][DK]
   float* pal = pq + kKfTB * DK;                                     // alpha [TB][DK]
   auto fetch = [&](int blk) {   // the raw inputs of tokens 16 blk .. 16 blk + 15 (zero past T)
     uint8_t* raw = kf_smem + (blk & 1) * SM::kRaw;
-    constexpr int pr = DK * (int)sizeof(Tin) / 16, pv = NVC * (int)sizeof(Tin) / 16, pf = DK / 4;
+    constexpr int pr = DK * (int)sizeof(Tin) / 16, pv = DV * (int)sizeof(Tin) / 16, pf = DK / 4;
     constexpr int per_tok = 2 * pr + pv + 2 * pf;
     for (int e = tid; e < kKfTB * per_tok; e += kKfThreads) {
       const int tt = e / per_tok, x = e % per_tok, t = blk * kKfTB + tt;
@@ -113,9 +136,8 @@ __global__ void __launch_bounds__(kKfThreads, 1) kalman_kernel(FwdArgs a) {
                 static_cast<const uint8_t*>(a.q) + ti * DK * sizeof(Tin) + y * 16, real ? 16 : 0);
       } else if (x < 2 * pr + pv) {
         const int y = x - 2 * pr;
-        kf_cp16(raw + oV + tt * NVC * sizeof(Tin) + y * 16,
-                static_cast<const uint8_t*>(a.v) + (ti * a.dv + slice * NVC) * sizeof(Tin) + y * 16,
-                real ? 16 : 0);
+        kf_cp16(raw + oV + tt * DV * sizeof(Tin) + y * 16,
+                static_cast<const uint8_t*>(a.v) + ti * DV * sizeof(Tin) + y * 16, real ? 16 : 0);
       } else if (x < 2 * pr + pv + pf) {
         const int y = x - 2 * pr - pv;
         kf_cp16(raw + oLA + tt * DK * 4 + y * 16, a.log_alpha + ti * DK + y * 4, real ? 16 : 0);
@@ -163,7 +185,7 @@ __global__ void __launch_bounds__(kKfThreads, 1) kalman_kernel(FwdArgs a) {
   if (nblk > 1) fetch(1);
   for (int t = 0; t < a.T; ++t) {
     const int tt = t % kKfTB, blk = t / kKfTB;
-    if (tt == 0) {   // a new block: wait for it, form k^, q^, alpha, refill the other buffer
+    if (tt == 0) {   // a new block: wait for it, form k^, q^, alpha
       if (blk + 1 < nblk)
         asm volatile("cp.async.wait_group 1;" ::: "memory");
       else
@@ -177,55 +199,71 @@ __global__ void __launch_bounds__(kKfThreads, 1) kalman_kernel(FwdArgs a) {
     const float* s_qt = pq + tt * DK;
     const float* s_alt = pal + tt * DK;
     const float* s_omt = reinterpret_cast<const float*>(raw + oOM) + tt * DK;
-    const Tin* s_vt = reinterpret_cast<const Tin*>(raw + oV) + tt * NVC;
+    const Tin* s_vt = reinterpret_cast<const Tin*>(raw + oV) + tt * DV;
     const float s_rt = reinterpret_cast<const float*>(raw + oR)[tt];
-    // ---- predict; y = P^ k (row sums), z = k^T y and y^T q (warp partials); S^ = D S
-    //      and the column partials of S^^T k, S^^T q
-    float y[RW];
-    float zp = 0.f, yqp = 0.f;
-    float alj[CPL], kj[CPL];   // this lane's columns
+    // this lane's columns j = lane + 32 c (covariance columns and state rows)
+    float alj[CPL], kj[CPL], qj[CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
       alj[c] = s_alt[lane + 32 * c];
       kj[c] = s_kt[lane + 32 * c];
+      qj[c] = s_qt[lane + 32 * c];
     }
+    // ---- predict P^ = D P D + diag(omega); row partials of y = P^ k
+    float acc[RW];
 #pragma unroll
     for (int i = 0; i < RW; ++i) {
       const int ri = r0 + i;
       const float ai = s_alt[ri];
-      float acc = 0.f;
+      acc[i] = 0.f;
 #pragma unroll
       for (int c = 0; c < CPL; ++c) {
-        const int j = lane + 32 * c;
         float p = ai * alj[c] * P[i][c];
-        if (j == ri) p += s_omt[ri];
+        if (lane + 32 * c == ri) p += s_omt[ri];
         P[i][c] = p;
-        acc += p * kj[c];
+        acc[i] += p * kj[c];
       }
-      acc = warp_sum(acc);
-      y[i] = acc;
-      zp += s_kt[ri] * acc;
-      yqp += s_qt[ri] * acc;
-      if (lane == i) s_y[ri] = acc;
     }
-    if (lane == 0) {
-      s_zp[warp] = zp;
-      s_yqp[warp] = yqp;
-    }
-#pragma unroll
-    for (int c = 0; c < SPL; ++c) {
-      float dk_ = 0.f, dq_ = 0.f;
-#pragma unroll
-      for (int i = 0; i < RW; ++i) {
-        S[i][c] *= s_alt[r0 + i];
-        dk_ += S[i][c] * s_kt[r0 + i];
-        dq_ += S[i][c] * s_qt[r0 + i];
+    {   // y for row rho of this warp on its owner lanes; z and y^T q partials
+      const float yr = reduce_scatter<RW>(acc, lane, 16);
+      const int rho = (lane >> kOwnRW) & (RW - 1);
+      const bool own = (lane & ((1 << kOwnRW) - 1)) == 0;
+      float zp = 0.f, yqp = 0.f;
+      if (own) {
+        s_y[r0 + rho] = yr;
+        zp = s_kt[r0 + rho] * yr;
+        yqp = s_qt[r0 + rho] * yr;
       }
-      s_dp[warp][lane + 32 * c] = dk_;
-      s_qp[warp][lane + 32 * c] = dq_;
+      zp = warp_sum(zp);
+      yqp = warp_sum(yqp);
+      if (lane == 0) {
+        s_zp[warp] = zp;
+        s_yqp[warp] = yqp;
+      }
+    }
+    {   // S^ = D S; this warp's columns of S^^T k and S^^T q -> e = v - S^^T k
+      float dk_[CPW], dq_[CPW];
+#pragma unroll
+      for (int u = 0; u < CPW; ++u) {
+        dk_[u] = 0.f;
+        dq_[u] = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          S[c][u] *= alj[c];
+          dk_[u] += S[c][u] * kj[c];
+          dq_[u] += S[c][u] * qj[c];
+        }
+      }
+      const float sk = reduce_scatter<CPW>(dk_, lane, 16);
+      const float sq = reduce_scatter<CPW>(dq_, lane, 16);
+      if ((lane & ((1 << kOwnCW) - 1)) == 0) {
+        const int col = v0 + ((lane >> kOwnCW) & (CPW - 1));
+        s_e[col] = to_f<Tin>(s_vt[col]) - sk;
+        s_sq[col] = sq;
+      }
     }
     __syncthreads();
-    // ---- update: P = P^ - y y^T/(r + z); e = v - S^^T k; S = S^ + (y/(r + z)) e^T;
+    // ---- update: P = P^ - y y^T/(r + z); S = S^ + (y/(r + z)) e^T;
     //      o = S^^T q + (y^T q/(r + z)) e
     float z = 0.f, yq = 0.f;
 #pragma unroll
@@ -234,29 +272,25 @@ __global__ void __launch_bounds__(kKfThreads, 1) kalman_kernel(FwdArgs a) {
       yq += s_yqp[w];
     }
     const float inv = 1.f / (s_rt + z);
+    float yj[CPL];
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-      const float yj = s_y[lane + 32 * c] * inv;
+    for (int c = 0; c < CPL; ++c) yj[c] = s_y[lane + 32 * c] * inv;
 #pragma unroll
-      for (int i = 0; i < RW; ++i) P[i][c] -= y[i] * yj;
+    for (int i = 0; i < RW; ++i) {
+      const float yi = s_y[r0 + i];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) P[i][c] -= yi * yj[c];
     }
 #pragma unroll
-    for (int c = 0; c < SPL; ++c) {
-      const int vl = lane + 32 * c;
-      float sk = 0.f, sq = 0.f;
+    for (int u = 0; u < CPW; ++u) {
+      const float e = s_e[v0 + u];
 #pragma unroll
-      for (int w = 0; w < kKfWarps; ++w) {
-        sk += s_dp[w][vl];
-        sq += s_qp[w][vl];
-      }
-      const float e = to_f<Tin>(s_vt[vl]) - sk;
-#pragma unroll
-      for (int i = 0; i < RW; ++i) S[i][c] += y[i] * inv * e;
-      if (warp == 0) {
-        const float o = sq + yq * inv * e;
-        static_cast<Tin*>(a.out)[tok(t) * a.dv + slice * NVC + vl] = from_f<Tin>(o);
-        if (a.check_finite) bad |= !finite_f(o);
-      }
+      for (int c = 0; c < CPL; ++c) S[c][u] += yj[c] * e;
+    }
+    if (lane < CPW) {
+      const float o = s_sq[v0 + lane] + yq * inv * s_e[v0 + lane];
+      static_cast<Tin*>(a.out)[tok(t) * DV + v0 + lane] = from_f<Tin>(o);
+      if (a.check_finite) bad |= !finite_f(o);
     }
     __syncthreads();
     if (tt == kKfTB - 1 && blk + 2 < nblk) fetch(blk + 2);   // this block's buffer is free
@@ -264,14 +298,14 @@ __global__ void __launch_bounds__(kKfThreads, 1) kalman_kernel(FwdArgs a) {
 
   if (a.S) {
 #pragma unroll
-    for (int i = 0; i < RW; ++i)
+    for (int c = 0; c < CPL; ++c)
 #pragma unroll
-      for (int c = 0; c < SPL; ++c) {
-        a.S[((long)bh * DK + r0 + i) * a.dv + slice * NVC + lane + 32 * c] = S[i][c];
-        if (a.check_finite) bad |= !finite_f(S[i][c]);
+      for (int u = 0; u < CPW; ++u) {
+        a.S[((long)bh * DK + lane + 32 * c) * DV + v0 + u] = S[c][u];
+        if (a.check_finite) bad |= !finite_f(S[c][u]);
       }
   }
-  if (a.aux && slice == 0) {
+  if (a.aux) {
 #pragma unroll
     for (int i = 0; i < RW; ++i)
 #pragma unroll
@@ -282,35 +316,24 @@ __global__ void __launch_bounds__(kKfThreads, 1) kalman_kernel(FwdArgs a) {
 
 }  // namespace
 
-int kalman_sm_count() {
-  static int count[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (!count[dev]) cudaDeviceGetAttribute(&count[dev], cudaDevAttrMultiProcessorCount, dev);
-  return count[dev];
-}
-
-// Forward with 32 state columns per CTA, or with all of them in one CTA per
-// head (few heads per SM left to use, and the decode step: T = 1, state and
-// covariance in place).
-cudaError_t launch_kalman(const FwdArgs& a, int dtype, cudaStream_t st, bool whole_columns) {
-  const int nvc = whole_columns ? a.dv : 32;
-  const int grid = a.B * a.H * (a.dv / nvc);
-#define DR_KF(DK_, NVC_, T_)                                                          \
-  if (a.dk == DK_ && nvc == NVC_) {                                                   \
-    constexpr int smem = KfSmem<DK_, NVC_, T_>::bytes;                                 \
-    cudaError_t e = cudaFuncSetAttribute(kalman_kernel<DK_, NVC_, T_>,                 \
+// Forward or decode step (T = 1): one CTA per (b, h); state and covariance may
+// be updated in place (each CTA reads its own head's before writing it).
+cudaError_t launch_kalman(const FwdArgs& a, int dtype, cudaStream_t st) {
+  const int grid = a.B * a.H;
+#define DR_KF(DK_, DV_, T_)                                                           \
+  if (a.dk == DK_ && a.dv == DV_) {                                                   \
+    constexpr int smem = KfSmem<DK_, DV_, T_>::bytes;                                  \
+    cudaError_t e = cudaFuncSetAttribute(kalman_kernel<DK_, DV_, T_>,                  \
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem); \
     if (e != cudaSuccess) return e;                                                   \
-    kalman_kernel<DK_, NVC_, T_><<<grid, kKfThreads, smem, st>>>(a);                  \
+    kalman_kernel<DK_, DV_, T_><<<grid, kKfThreads, smem, st>>>(a);                   \
     return cudaGetLastError();                                                        \
   }
   if (dtype == DR_BF16) {
-    DR_KF(64, 32, __nv_bfloat16) DR_KF(128, 32, __nv_bfloat16) DR_KF(64, 64, __nv_bfloat16)
-    DR_KF(128, 64, __nv_bfloat16) DR_KF(64, 128, __nv_bfloat16) DR_KF(128, 128, __nv_bfloat16)
+    DR_KF(64, 64, __nv_bfloat16) DR_KF(128, 64, __nv_bfloat16)
+    DR_KF(64, 128, __nv_bfloat16) DR_KF(128, 128, __nv_bfloat16)
   } else {
-    DR_KF(64, 32, float) DR_KF(128, 32, float) DR_KF(64, 64, float)
-    DR_KF(128, 64, float) DR_KF(64, 128, float) DR_KF(128, 128, float)
+    DR_KF(64, 64, float) DR_KF(128, 64, float) DR_KF(64, 128, float) DR_KF(128, 128, float)
   }
 #undef DR_KF
   return cudaErrorInvalidValue;
