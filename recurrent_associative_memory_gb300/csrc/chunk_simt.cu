@@ -225,8 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
   if (my_c >= 0 && my_c < DK) {
     if (pstat) carry = a.aux0 ? a.aux0[(long)bh * DK + my_c] : 0.f;
     if (kdn) carry = a.aux0 ? a.aux0[(long)bh * DK + my_c] : 1.f;
-    if (ikdn) carry = a.aux0 ? a.aux0[bh] : 1.f;   // used by thread 0
   }
+  if (ikdn && tid == DK) carry = a.aux0 ? a.aux0[bh] : 1.f;   // isotropic KDN: thread DK holds b
   const float mu_h = pstat ? a.mu[h] : 0.f;
   bool bad = false;
 
@@ -424,10 +424,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
     if (chained && ci > 0 && tid == 0 && !chain_wait(chain + ri, chain + kIters + 1, kChainWaitNs))
       set_status(DR_ERR_TIMEOUT);
     __syncthreads();
-    if (chained && tid < DK)   // KDN p / PKDA A / IKDN b (thread 0) at the chunk start: the
-                               // row's initial value (default 1 / 0 / 1), or the previous chunk's
+    if (chained && (ikdn ? tid == DK : tid < DK))   // KDN p / PKDA A (thread c) or IKDN b
+      // (thread DK) at the chunk start: the row's initial value (default 1 / 0 / 1), or
+      // the previous chunk's
       carry = ci == 0 ? (a.aux0 ? a.aux0[ikdn ? (long)bh : (long)bh * DK + tid] : (pkda ? 0.f : 1.f))
-                      : __ldcg(reinterpret_cast<const float*>(rec + rkP0) + tid);
+                      : __ldcg(reinterpret_cast<const float*>(rec + rkP0) + (ikdn ? 0 : tid));
 
     // ---- 3. cumulative decay and write vectors
     if (!perchan) {
@@ -471,8 +472,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
     } else if (ikdn) {
       // isotropic KDN (KDN notes section 7, Eq. (40)): the mean squared decay of
       // every token (warp w: tokens 8w .. 8w + 7), then channel c's cumulative
-      // log-decay (thread c) while thread 0 runs the variance scan of the head,
-      // then w = beta k^
+      // log-decay (thread c) while warp DK/32 scans the head's variance, then
+      // w = beta k^.  The variance recursion b -> b^/(1 + u b^), b^ = a b + omega
+      // is the Moebius map of (n, d) by M = [[a, omega], [u a, 1 + u omega]]
+      // (b = n/d; the notes' remark that it is a 2x2 Moebius scan), so the warp
+      // forms all 64 prefixes in parallel: two tokens' product per lane, then a
+      // shuffle scan of 2x2 products, each rescaled by an exact power of two.
       {
         const int i0 = 8 * warp;
 #pragma unroll
@@ -499,21 +504,64 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
           }
         }
       }
-      if (tid == 0) {   // b^ = a b + omega; beta = b^/(r + b^ |k|^2); b = b^/(1 + u b^)
-        float bv = carry;
-        for (int i = 0; i < CM; ++i) {
-          const float b_hat = sz[i] * bv + sb2[i];
-          const float rr = sb1[i], kk = sb3[i];
-          sz[i] = __fdividef(b_hat, rr + b_hat * kk);
-          bv = __fdividef(b_hat, 1.f + a.info_scale * kk * b_hat / (DK * rr));
+      if (warp == DK / 32) {
+        auto mmul = [](const float (&A)[4], const float (&B)[4], float (&C)[4]) {
+          C[0] = A[0] * B[0] + A[1] * B[2];
+          C[1] = A[0] * B[1] + A[1] * B[3];
+          C[2] = A[2] * B[0] + A[3] * B[2];
+          C[3] = A[2] * B[1] + A[3] * B[3];
+        };
+        auto renorm = [](float (&C)[4]) {   // exact power-of-two rescale (b = n/d is scale-free)
+          int ex;
+          frexpf(fmaxf(fmaxf(fabsf(C[0]), fabsf(C[1])), fmaxf(fabsf(C[2]), fabsf(C[3]))), &ex);
+#pragma unroll
+          for (int z = 0; z < 4; ++z) C[z] = ldexpf(C[z], -ex);
+        };
+        auto token = [&](int i, float (&M)[4]) {
+          const float at = sz[i], om = sb2[i], u = a.info_scale * sb3[i] / (DK * sb1[i]);
+          M[0] = at; M[1] = om; M[2] = u * at; M[3] = 1.f + u * om;
+        };
+        float M0[4], M1[4], Pl[4];
+        token(2 * lane, M0);
+        token(2 * lane + 1, M1);
+        mmul(M1, M0, Pl);   // tokens 2l, 2l + 1 (later factor on the left)
+        renorm(Pl);
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {   // inclusive scan over lanes
+          float Q[4], R[4];
+#pragma unroll
+          for (int z = 0; z < 4; ++z) Q[z] = __shfl_up_sync(0xffffffffu, Pl[z], d);
+          if (lane >= d) {
+            mmul(Pl, Q, R);
+#pragma unroll
+            for (int z = 0; z < 4; ++z) Pl[z] = R[z];
+            renorm(Pl);
+          }
         }
-        carry = bv;
-        if (chained) {   // b at the chunk end -> the next chunk's record, or aux after the last
-          if (ci + 1 < NCk) {
-            __stcg(reinterpret_cast<float*>(rec + kRecK + rkP0), carry);
-            __threadfence();
-          } else if (a.aux) {
-            a.aux[bh] = carry;
+        const float b_in = __shfl_sync(0xffffffffu, carry, 0);
+        float E[4];   // exclusive prefix: tokens 0 .. 2l - 1
+#pragma unroll
+        for (int z = 0; z < 4; ++z) E[z] = __shfl_up_sync(0xffffffffu, Pl[z], 1);
+        if (lane == 0) { E[0] = 1.f; E[1] = 0.f; E[2] = 0.f; E[3] = 1.f; }
+        const float n0 = E[0] * b_in + E[1], d0 = E[2] * b_in + E[3];
+        const float b_prev = __fdividef(n0, d0);                    // b before token 2l
+        const float bh0 = sz[2 * lane] * b_prev + sb2[2 * lane];
+        const float n1 = M0[0] * n0 + M0[1] * d0, d1 = M0[2] * n0 + M0[3] * d0;
+        const float b_mid = __fdividef(n1, d1);                     // b before token 2l + 1
+        const float bh1 = sz[2 * lane + 1] * b_mid + sb2[2 * lane + 1];
+        sz[2 * lane] = __fdividef(bh0, sb1[2 * lane] + bh0 * sb3[2 * lane]);
+        sz[2 * lane + 1] = __fdividef(bh1, sb1[2 * lane + 1] + bh1 * sb3[2 * lane + 1]);
+        const float nE = Pl[0] * b_in + Pl[1], dE = Pl[2] * b_in + Pl[3];
+        const float b_end = __shfl_sync(0xffffffffu, __fdividef(nE, dE), 31);
+        if (lane == 0) {
+          carry = b_end;
+          if (chained) {   // b at the chunk end -> the next chunk's record, or aux after the last
+            if (ci + 1 < NCk) {
+              __stcg(reinterpret_cast<float*>(rec + kRecK + rkP0), carry);
+              __threadfence();
+            } else if (a.aux) {
+              a.aux[bh] = carry;
+            }
           }
         }
       }
@@ -1195,7 +1243,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
   }
   if (a.aux && tile == 0 && (pstat || kdn) && my_c >= 0 && my_c < DK)
     a.aux[(long)bh * DK + my_c] = carry;
-  if (a.aux && tile == 0 && ikdn && tid == 0) a.aux[bh] = carry;
+  if (a.aux && tile == 0 && ikdn && tid == DK) a.aux[bh] = carry;
   if (bad) set_status(DR_ERR_NONFINITE);
 }
 
