@@ -2,12 +2,15 @@
 """Benchmark: chunkwise delta-rule forward tokens/s (+ roofline) and decode-step GB/s.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
 
 Workload (default ``gdn_kla_bf16``): B=8, H=8, T=2048, dk=dv=128, chunk 64,
 bf16 q/k/v, fp32 gates and state, GDN and KLA on the same seeded inputs.  One
 step is one chunkwise forward over the whole batch for each of the two
-variants (2 launches of libdr's forward kernel); ``value`` counts B*T tokens
-per variant pass.  Inputs are resident in HBM before the timed region; L2 is
+variants (each a prep and a carry launch of libdr); ``value`` counts B*T tokens
+per variant pass.  ``--workload`` times any other workload of
+``recurrent_associative_memory_gb300.workloads`` (PGDN, the per-channel-decay
+variants, the exact Kalman memory, the 64K-token prefill) the same way.  Inputs are resident in HBM before the timed region; L2 is
 flushed (a 256 MiB write) between timed steps and the flush is not timed.
 
 The same JSON line carries:
