@@ -611,8 +611,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
             float scale = 1.f;
             if (pkda) {
               A = sb2[i0 + e] * A + sb3[i0 + e] * kv[e] * kv[e];
-              const float rr = logf(fmaxf(A, a.log_floor)) - (PREP ? a.mu[h] : mu_h);
-              scale = expf(-a.ln_x * __fdividef(rr, 1.f + fabsf(rr)));
+              // fast log / exp: ~1e-6 relative in B, far inside either tolerance
+              const float rr = __logf(fmaxf(A, a.log_floor)) - (PREP ? a.mu[h] : mu_h);
+              scale = __expf(-a.ln_x * __fdividef(rr, 1.f + fabsf(rr)));
             }
             w[e] = sb1[i0 + e] * scale * kv[e];
             sW[(i0 + e) * DK + c] = w[e];
