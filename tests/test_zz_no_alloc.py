@@ -63,3 +63,31 @@ def test_noalloc_matches_chunk_fwd_on_two_calls():
         eo = rel_err(np64(out), np64(ref_out))
         es = rel_err(np64(S), np64(ref_S))
         assert eo <= TOL["bf16"] and es <= TOL["bf16"], (variant, eo, es)
+
+
+@pytest.mark.gpu
+def test_noalloc_per_channel_decay_paths_match_chunk_fwd():
+    """The library-owned scratch serves the CUDA-core two-phase path too: Diagonal
+    KDN with its variance chain (many rows: the chain's flags live after the
+    records in the scratch), KDA, and isotropic KDN; same bits as a caller
+    workspace."""
+    from recurrent_associative_memory_gb300 import dr, runner
+
+    cases = [("kdn", "kdn_bf16", 2, 100, 26), ("kda", "kda_bf16", 2, 130, 3),
+             ("ikdn", "ikdn_bf16", 2, 77, 26)]
+    for variant, base, B, T, H in cases:
+        wl = W.small(base, B=B, T=T, H=H, seed=40)
+        dev = runner.to_device(W.generate(wl, variant))
+        ref_out, ref_S, ref_aux = runner.chunk_fwd(dev)
+        out, S = torch.empty_like(ref_out), torch.empty_like(ref_S)
+        aux = None if ref_aux is None else torch.empty_like(ref_aux)
+        p = runner.params_for(dev, aux_final=aux)
+        st = dr.dr_chunk_fwd_noalloc(dev["q"], dev["k"], dev["v"], dev["log_alpha"], p,
+                                     dr.VARIANT_IDS[variant], dev.get("eps", 1e-6), None, out, S,
+                                     B, T, H, 128, 128, 64)
+        dr.check(st, "dr_chunk_fwd_noalloc")
+        torch.cuda.synchronize()
+        assert dr.dr_get_device_status() == 0
+        assert torch.equal(out, ref_out) and torch.equal(S, ref_S), variant
+        if aux is not None:
+            assert torch.equal(aux, ref_aux), variant
