@@ -161,10 +161,12 @@ int dr_chunk_fwd(const void *q, const void *k, const void *v, const float *log_a
  * from the same read (KLA notes Algorithm 1; PDN notes section 2.5; KDN notes
  * section 2.2, predict -> gain -> update -> read).
  *
- * q, k [B,H,dk]; v, out [B,H,dv] (dtype gp->dtype); log_alpha [B,H] (KDN
- * [B,H,dk]); gate arrays without the T axis.  state [B,H,dk,dv] fp32 in/out.
- * aux_state [B,H,dk] fp32 in/out: PGDN A or KDN p (required for those
- * variants, ignored otherwise).  gp->aux_init/aux_final are ignored.
+ * q, k [B,H,dk]; v, out [B,H,dv] (dtype gp->dtype); log_alpha [B,H] (KDN,
+ * KDA, PKDA, IKDN, EKDN [B,H,dk]); gate arrays without the T axis.  state
+ * [B,H,dk,dv] fp32 in/out.  aux_state fp32 in/out, required for the variants
+ * that carry one, ignored otherwise: PGDN / PKDA A or KDN p [B,H,dk], IKDN b
+ * [B,H], EKDN P [B,H,dk,dk] (the exact Kalman step runs one CTA per head and
+ * updates state and P in place).  gp->aux_init/aux_final are ignored.
  * Sizes: B, H >= 1; dk, dv in {64, 128}.
  */
 int dr_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,
