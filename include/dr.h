@@ -188,7 +188,7 @@ size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H,
 
 /*
  * Same forward as dr_chunk_fwd on its two-phase paths (GDN, KLA, PGDN in bf16
- * and Diagonal KDN, KDA, PKDA in bf16 or fp32; dk = dv = 128, chunk 64), for callers that
+ * and Diagonal KDN, KDA, PKDA, isotropic KDN in bf16 or fp32; dk = dv = 128, chunk 64), for callers that
  * cannot allocate device
  * memory: code that runs where cudaMalloc is off limits (a host framework that
  * owns every byte of device memory through its own allocator, a real-time loop

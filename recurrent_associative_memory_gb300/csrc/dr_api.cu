@@ -171,7 +171,7 @@ int dr_chunk_fwd(const void* q, const void* k, const void* v, const float* log_a
   if (split && gp->workspace_bytes < need) return DR_ERR_WORKSPACE;
   if (split && (reinterpret_cast<uintptr_t>(gp->workspace) & 255u)) return DR_ERR_ALIGN;
   if (split && kdn_split)
-    err = launch_kdn_split(a, gp->dtype, gp->workspace, s);   // Diagonal KDN: CUDA-core two phases
+    err = launch_kdn_split(a, gp->dtype, gp->workspace, s);   // per-channel decay: CUDA-core two phases
   else if (split)
     err = launch_chunk_tc_split(a, gp->workspace, s);   // GDN / KLA / PGDN: prep on every SM, then the carry
   else if (chunk_tc_ws_supported(variant, gp->dtype, dk, dv, chunk))
