@@ -573,3 +573,49 @@ def test_resume_split_equals_whole(variant):
     o2, S2, a2 = call(oracle.tokenwise, variant, tail, S0=S1, aux0=a1, **kw)
     np.testing.assert_allclose(np.concatenate([o1, o2], axis=1), o, rtol=1e-9, atol=1e-11)
     np.testing.assert_allclose(S2, S, rtol=1e-9, atol=1e-11)
+
+
+# ------------------------------------------------------------------ backward (reverse mode)
+
+from oracle import backward as obw  # noqa: E402
+
+
+@pytest.mark.parametrize("variant", obw.GRAD_VARIANTS)
+@pytest.mark.parametrize("norm", [False, True])
+def test_backward_matches_central_differences(variant, norm):
+    """Every gradient of L = <dO, O> + <dS_T, S_T> (q, k, v, log alpha, eta, S_0)
+    equals the central difference of the forward oracle, element by element:
+    the reverse sweep is pinned to the independently written forward."""
+    r = rng(60)
+    B, T, H, dk, dv = 1, 6, 2, 3, 2
+    d = random_inputs(variant, B=B, T=T, H=H, dk=dk, dv=dv, seed=61)
+    S0 = r.standard_normal((B, H, dk, dv))
+    dO = r.standard_normal((B, T, H, dv))
+    dS = r.standard_normal((B, H, dk, dv))
+    flags = dict(q_l2norm=norm, k_l2norm=norm, eps=1e-6)
+
+    def loss(dd, S0_):
+        o, S, _ = oracle.tokenwise(dd["q"], dd["k"], dd["v"], dd["log_alpha"], variant,
+                                   eta=dd["eta"], S0=S0_, **flags)
+        return float(np.sum(dO * o) + np.sum(dS * S))
+
+    g = obw.tokenwise_backward(d["q"], d["k"], d["v"], d["log_alpha"], variant, dO, dS,
+                               eta=d["eta"], S0=S0, **flags)
+    h = 1e-6
+    for name, key in [("q", "dq"), ("k", "dk"), ("v", "dv"), ("log_alpha", "dlog_alpha"),
+                      ("eta", "deta")]:
+        num = np.zeros_like(d[name])
+        for idx in np.ndindex(d[name].shape):
+            dp = {kk: vv.copy() for kk, vv in d.items()}
+            dm = {kk: vv.copy() for kk, vv in d.items()}
+            dp[name][idx] += h
+            dm[name][idx] -= h
+            num[idx] = (loss(dp, S0) - loss(dm, S0)) / (2 * h)
+        np.testing.assert_allclose(g[key], num, rtol=1e-5, atol=1e-7, err_msg=name)
+    num = np.zeros_like(S0)
+    for idx in np.ndindex(S0.shape):
+        Sp, Sm = S0.copy(), S0.copy()
+        Sp[idx] += h
+        Sm[idx] -= h
+        num[idx] = (loss(d, Sp) - loss(d, Sm)) / (2 * h)
+    np.testing.assert_allclose(g["dS0"], num, rtol=1e-5, atol=1e-7, err_msg="S0")
