@@ -14,8 +14,9 @@ recurrence  Tokenwise recurrence (the plain definition) for GDN, KLA, PGDN,
             (dense key covariance), one token at a time, in float64.
 chunkwise   A naive chunkwise-parallel restatement (triangular system per
             chunk), written independently of ``recurrence`` as a cross-check.
-backward    Reverse-mode gradients of the tokenwise recurrence (GDN, KLA, KDA)
-            w.r.t. q, k, v, log-decay, eta and the initial state.
+backward    Reverse-mode gradients of the tokenwise recurrence (GDN, KLA, KDA,
+            PGDN, PKDA, Diagonal KDN) w.r.t. q, k, v, log-decay, every gate,
+            the initial state and the gain state's initial value.
 ridge       Side oracles fixed by closed forms: exact ridge regression (ATQ),
             its Sherman-Morrison recursion (ATK), the diagonal counterexample
             and a dense-covariance Kalman filter.

@@ -1,4 +1,5 @@
-"""Reverse-mode gradients of the tokenwise recurrence, fp64 (GDN, KLA, KDA).
+"""Reverse-mode gradients of the tokenwise recurrence, fp64 (GDN, KLA, KDA, PGDN,
+PKDA, Diagonal KDN).
 
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 
@@ -22,14 +23,29 @@ G = dL/dS_t, applying the chain rule to each line above in reverse order:
                              d eta_t = k^T dw_t / (s + eps),   s = ||k||^2
 
 and, with the L2-normalisation flags, x^ = x / ||x|| gives dx = (dx^ - x^ (x^T dx^)) / ||x||.
-The states S_t of the forward are kept (fp64, small test sizes only).
+The gain states carry their own adjoints backwards:
+
+  PGDN / PKDA (PDN notes Eq. (9)): w = eta (B . k), B = exp(-ln(x) s), s = r/(1+|r|),
+      r = ln A - mu (A above the floor), A_t = alphaP A_{t-1} + betaP k.k:
+      dB = eta k . dw, ds = -ln(x) B dB, dr = ds/(1+|r|)^2, dA_t += dr / A_t,
+      d mu -= sum dr, then dA_{t-1} = alphaP dA_t, d alphaP = A_{t-1}^T dA_t,
+      d betaP = (k.k)^T dA_t, dk += 2 betaP k . dA_t.
+  Diagonal KDN (KDN notes Eqs. (23)-(30), (60)-(65)): p^ = alpha^2 p + omega,
+      kappa = p^ . k / (r + z), z = sum p^ k^2, p_t = p^ / (1 + u p^), u = (mu/r) k.k:
+      with c = sum dw . p^ . k and den = r + z,
+      dp^ = dw . k / den - c k.k / den^2 + dp_t / (1 + u p^)^2,
+      du = -dp_t p^^2 / (1 + u p^)^2,  dk = dw . p^ / den - 2 c p^ . k / den^2 + 2 (mu/r) k . du,
+      dr = -c / den^2 - (mu / r^2) sum(k.k du),  d omega = dp^,
+      dp_{t-1} = alpha^2 dp^,  d alpha += 2 alpha p dp^.
+The states S_t (and the gain states) of the forward are kept (fp64, small test
+sizes only).
 """
 
 from __future__ import annotations
 
 import numpy as np
 
-GRAD_VARIANTS = ("gdn", "kla", "kda")
+GRAD_VARIANTS = ("gdn", "kla", "kda", "pgdn", "pkda", "kdn")
 
 
 def _norm_backward(x_raw, dx_hat):
@@ -39,19 +55,27 @@ def _norm_backward(x_raw, dx_hat):
     return (dx_hat - xh * np.sum(xh * dx_hat, axis=-1, keepdims=True)) / n
 
 
-def tokenwise_backward(q, k, v, log_alpha, variant: str, do, dS_T=None, *, eta, eps: float = 1e-6,
-                       q_l2norm: bool = False, k_l2norm: bool = False, S0=None):
-    """Gradients of sum(do * o) + sum(dS_T * S_T) w.r.t. the forward's inputs.
+def tokenwise_backward(q, k, v, log_alpha, variant: str, do, dS_T=None, *, eta=None,
+                       eps: float = 1e-6, q_l2norm: bool = False, k_l2norm: bool = False,
+                       S0=None, alphaP=None, betaP=None, mu=None, x: float = 1.5,
+                       log_floor: float = 1e-12, omega=None, r=None, info_scale: float = 1.0,
+                       aux0=None, daux_T=None):
+    """Gradients of sum(do * o) + sum(dS_T * S_T) + sum(daux_T * aux_T) w.r.t. the
+    forward's inputs.
 
     Shapes as ``recurrence.tokenwise``: q, k [B,T,H,dk]; v [B,T,H,dv]; log_alpha
-    [B,T,H] (GDN, KLA) or [B,T,H,dk] (KDA); eta [B,T,H]; do [B,T,H,dv];
-    dS_T, S0 [B,H,dk,dv] (None = 0).  Returns a dict with dq, dk, dv,
-    dlog_alpha, deta, dS0.
+    [B,T,H] (GDN, KLA, PGDN) or [B,T,H,dk] (KDA, PKDA, KDN); eta, alphaP, betaP,
+    r [B,T,H]; omega [B,T,H,dk]; mu [H]; do [B,T,H,dv]; dS_T, S0 [B,H,dk,dv];
+    aux0, daux_T [B,H,dk] (None = 0, or p_0 = 1 for KDN).  Returns a dict with
+    dq, dk, dv, dlog_alpha, dS0 and the variant's gate gradients (deta; dalphaP,
+    dbetaP, dmu, daux0; domega, dr, daux0).
     """
     if variant not in GRAD_VARIANTS:
         raise ValueError(f"no backward for variant {variant!r}")
-    f = lambda a: np.asarray(a, dtype=np.float64)  # noqa: E731
+    f = lambda a: None if a is None else np.asarray(a, dtype=np.float64)  # noqa: E731
     q_raw, k_raw, v, la, eta, do = f(q), f(k), f(v), f(log_alpha), f(eta), f(do)
+    alphaP, betaP, mu, omega, r = f(alphaP), f(betaP), f(mu), f(omega), f(r)
+    pstat, kdn = variant in ("pgdn", "pkda"), variant == "kdn"
     B, T, H, dk = k_raw.shape
     dv = v.shape[-1]
     qh = q_raw / np.sqrt(np.sum(q_raw * q_raw, axis=-1, keepdims=True)) if q_l2norm else q_raw
@@ -59,18 +83,39 @@ def tokenwise_backward(q, k, v, log_alpha, variant: str, do, dS_T=None, *, eta, 
     per_channel = la.ndim == 4
     alpha = np.exp(la)
 
-    # forward, keeping S_{t-1}, e_t, w_t
+    # forward, keeping S_{t-1}, e_t, w_t and the gain states
     S = np.zeros((B, H, dk, dv)) if S0 is None else f(S0).copy()
     S_prev = np.zeros((T, B, H, dk, dv))
     E = np.zeros((T, B, H, dv))
     Wt = np.zeros((T, B, H, dk))
+    aux = None
+    if pstat:
+        aux = np.zeros((B, H, dk)) if aux0 is None else f(aux0).copy()
+    elif kdn:
+        aux = np.ones((B, H, dk)) if aux0 is None else f(aux0).copy()
+    aux_prev = np.zeros((T, B, H, dk))
+    A_all = np.zeros((T, B, H, dk))      # PGDN statistic A_t / KDN predicted p^_t
     for t in range(T):
         S_prev[t] = S
         a_t = alpha[:, t]
         S_tilde = (a_t[..., :, None] if per_channel else a_t[..., None, None]) * S
         kt = kh[:, t]
+        if aux is not None:
+            aux_prev[t] = aux
         if variant == "kla":
             w = (eta[:, t] / (np.sum(kt * kt, axis=-1) + eps))[..., None] * kt
+        elif pstat:
+            aux = alphaP[:, t][..., None] * aux + betaP[:, t][..., None] * kt * kt
+            A_all[t] = aux
+            rr = np.log(np.maximum(aux, log_floor)) - mu[None, :, None]
+            Bs = np.exp(-np.log(x) * rr / (1 + np.abs(rr)))
+            w = eta[:, t][..., None] * Bs * kt
+        elif kdn:
+            p_hat = a_t * a_t * aux + omega[:, t]
+            A_all[t] = p_hat
+            w = p_hat * kt / (r[:, t] + np.sum(p_hat * kt * kt, axis=-1))[..., None]
+            u = (info_scale / r[:, t])[..., None] * kt * kt
+            aux = p_hat / (1 + u * p_hat)
         else:
             w = eta[:, t][..., None] * kt
         e = v[:, t] - np.einsum("bhkv,bhk->bhv", S_tilde, kt)
@@ -83,7 +128,13 @@ def tokenwise_backward(q, k, v, log_alpha, variant: str, do, dS_T=None, *, eta, 
     dk_ = np.zeros_like(kh)
     dv_ = np.zeros_like(v)
     dla = np.zeros_like(la)
-    deta = np.zeros_like(eta)
+    deta = np.zeros((B, T, H)) if eta is not None else None
+    daux = (np.zeros((B, H, dk)) if daux_T is None else f(daux_T).copy()) if aux is not None else None
+    dalphaP = np.zeros((B, T, H)) if pstat else None
+    dbetaP = np.zeros((B, T, H)) if pstat else None
+    dmu = np.zeros(H) if pstat else None
+    domega = np.zeros((B, T, H, dk)) if kdn else None
+    dr_ = np.zeros((B, T, H)) if kdn else None
     for t in range(T - 1, -1, -1):
         a_t = alpha[:, t]
         S_tilde = (a_t[..., :, None] if per_channel else a_t[..., None, None]) * S_prev[t]
@@ -101,17 +152,48 @@ def tokenwise_backward(q, k, v, log_alpha, variant: str, do, dS_T=None, *, eta, 
         dSt = dSt - kt[..., :, None] * de[..., None, :]
         dk_[:, t] = -np.einsum("bhkv,bhv->bhk", S_tilde, de)
         # w
+        dalpha_gain = 0.0
         if variant == "kla":
             s = np.sum(kt * kt, axis=-1) + eps
             kdw = np.sum(kt * dw, axis=-1)
             dk_[:, t] += (eta[:, t] / s)[..., None] * dw - (2 * eta[:, t] * kdw / s ** 2)[..., None] * kt
             deta[:, t] = kdw / s
+        elif pstat:
+            A = A_all[t]
+            rr = np.log(np.maximum(A, log_floor)) - mu[None, :, None]
+            Bs = np.exp(-np.log(x) * rr / (1 + np.abs(rr)))
+            dB = eta[:, t][..., None] * kt * dw
+            dk_[:, t] += eta[:, t][..., None] * Bs * dw
+            deta[:, t] = np.sum(Bs * kt * dw, axis=-1)
+            drr = -np.log(x) * Bs * dB / (1 + np.abs(rr)) ** 2
+            dA = daux + np.where(A > log_floor, drr / A, 0.0)
+            dmu -= np.sum(np.where(A > log_floor, drr, 0.0), axis=(0, 2))
+            dalphaP[:, t] = np.sum(aux_prev[t] * dA, axis=-1)
+            dbetaP[:, t] = np.sum(kt * kt * dA, axis=-1)
+            dk_[:, t] += 2 * betaP[:, t][..., None] * kt * dA
+            daux = alphaP[:, t][..., None] * dA
+        elif kdn:
+            p_hat = A_all[t]
+            rt = r[:, t]
+            den = rt + np.sum(p_hat * kt * kt, axis=-1)
+            c = np.sum(dw * p_hat * kt, axis=-1)
+            u = (info_scale / rt)[..., None] * kt * kt
+            q1 = 1 + u * p_hat
+            dp_hat = (dw * kt / den[..., None] - (c / den ** 2)[..., None] * kt * kt
+                      + daux / q1 ** 2)
+            du = -daux * p_hat ** 2 / q1 ** 2
+            dk_[:, t] += (dw * p_hat / den[..., None] - (2 * c / den ** 2)[..., None] * p_hat * kt
+                          + 2 * (info_scale / rt)[..., None] * kt * du)
+            dr_[:, t] = -c / den ** 2 - info_scale / rt ** 2 * np.sum(kt * kt * du, axis=-1)
+            domega[:, t] = dp_hat
+            daux = a_t * a_t * dp_hat
+            dalpha_gain = 2 * a_t * aux_prev[t] * dp_hat
         else:
             dk_[:, t] += eta[:, t][..., None] * dw
             deta[:, t] = np.sum(kt * dw, axis=-1)
         # S~ = D S_{t-1}
         if per_channel:
-            dalpha = np.sum(dSt * S_prev[t], axis=-1)              # [B,H,dk]
+            dalpha = np.sum(dSt * S_prev[t], axis=-1) + dalpha_gain   # [B,H,dk]
             G = a_t[..., :, None] * dSt
         else:
             dalpha = np.sum(dSt * S_prev[t], axis=(-2, -1))        # [B,H]
@@ -121,4 +203,11 @@ def tokenwise_backward(q, k, v, log_alpha, variant: str, do, dS_T=None, *, eta, 
         dq = _norm_backward(q_raw, dq)
     if k_l2norm:
         dk_ = _norm_backward(k_raw, dk_)
-    return dict(dq=dq, dk=dk_, dv=dv_, dlog_alpha=dla, deta=deta, dS0=G)
+    out = dict(dq=dq, dk=dk_, dv=dv_, dlog_alpha=dla, dS0=G)
+    if deta is not None and not kdn:
+        out["deta"] = deta
+    if pstat:
+        out.update(dalphaP=dalphaP, dbetaP=dbetaP, dmu=dmu, daux0=daux)
+    if kdn:
+        out.update(domega=domega, dr=dr_, daux0=daux)
+    return out

@@ -583,39 +583,46 @@ from oracle import backward as obw  # noqa: E402
 @pytest.mark.parametrize("variant", obw.GRAD_VARIANTS)
 @pytest.mark.parametrize("norm", [False, True])
 def test_backward_matches_central_differences(variant, norm):
-    """Every gradient of L = <dO, O> + <dS_T, S_T> (q, k, v, log alpha, eta, S_0)
+    """Every gradient of L = <dO, O> + <dS_T, S_T> + <daux_T, aux_T> (q, k, v,
+    log alpha, the variant's gates, S_0 and the gain state's initial value)
     equals the central difference of the forward oracle, element by element:
     the reverse sweep is pinned to the independently written forward."""
     r = rng(60)
     B, T, H, dk, dv = 1, 6, 2, 3, 2
     d = random_inputs(variant, B=B, T=T, H=H, dk=dk, dv=dv, seed=61)
-    S0 = r.standard_normal((B, H, dk, dv))
+    d["S0"] = r.standard_normal((B, H, dk, dv))
+    if variant in ("pgdn", "pkda"):
+        d["aux0"] = r.uniform(0.5, 2.0, (B, H, dk))
+    elif variant == "kdn":
+        d["aux0"] = r.uniform(0.5, 1.5, (B, H, dk))
     dO = r.standard_normal((B, T, H, dv))
     dS = r.standard_normal((B, H, dk, dv))
+    daux = r.standard_normal((B, H, dk)) if "aux0" in d else None
     flags = dict(q_l2norm=norm, k_l2norm=norm, eps=1e-6)
+    gate_keys = [kk for kk in ("eta", "alphaP", "betaP", "mu", "omega", "r") if kk in d]
 
-    def loss(dd, S0_):
-        o, S, _ = oracle.tokenwise(dd["q"], dd["k"], dd["v"], dd["log_alpha"], variant,
-                                   eta=dd["eta"], S0=S0_, **flags)
-        return float(np.sum(dO * o) + np.sum(dS * S))
+    def loss(dd):
+        o, S, aux = oracle.tokenwise(dd["q"], dd["k"], dd["v"], dd["log_alpha"], variant,
+                                     S0=dd["S0"], aux0=dd.get("aux0"),
+                                     **{kk: dd[kk] for kk in gate_keys}, **flags)
+        out = float(np.sum(dO * o) + np.sum(dS * S))
+        return out + (float(np.sum(daux * aux)) if daux is not None else 0.0)
 
     g = obw.tokenwise_backward(d["q"], d["k"], d["v"], d["log_alpha"], variant, dO, dS,
-                               eta=d["eta"], S0=S0, **flags)
+                               S0=d["S0"], aux0=d.get("aux0"), daux_T=daux,
+                               **{kk: d[kk] for kk in gate_keys}, **flags)
+    names = {"q": "dq", "k": "dk", "v": "dv", "log_alpha": "dlog_alpha", "eta": "deta",
+             "alphaP": "dalphaP", "betaP": "dbetaP", "mu": "dmu", "omega": "domega", "r": "dr",
+             "S0": "dS0", "aux0": "daux0"}
     h = 1e-6
-    for name, key in [("q", "dq"), ("k", "dk"), ("v", "dv"), ("log_alpha", "dlog_alpha"),
-                      ("eta", "deta")]:
+    for name, key in names.items():
+        if name not in d:
+            continue
         num = np.zeros_like(d[name])
         for idx in np.ndindex(d[name].shape):
             dp = {kk: vv.copy() for kk, vv in d.items()}
             dm = {kk: vv.copy() for kk, vv in d.items()}
             dp[name][idx] += h
             dm[name][idx] -= h
-            num[idx] = (loss(dp, S0) - loss(dm, S0)) / (2 * h)
+            num[idx] = (loss(dp) - loss(dm)) / (2 * h)
         np.testing.assert_allclose(g[key], num, rtol=1e-5, atol=1e-7, err_msg=name)
-    num = np.zeros_like(S0)
-    for idx in np.ndindex(S0.shape):
-        Sp, Sm = S0.copy(), S0.copy()
-        Sp[idx] += h
-        Sm[idx] -= h
-        num[idx] = (loss(d, Sp) - loss(d, Sm)) / (2 * h)
-    np.testing.assert_allclose(g["dS0"], num, rtol=1e-5, atol=1e-7, err_msg="S0")
