@@ -16,7 +16,8 @@ chunkwise   A naive chunkwise-parallel restatement (triangular system per
             chunk), written independently of ``recurrence`` as a cross-check.
 backward    Reverse-mode gradients of the tokenwise recurrence (GDN, KLA, KDA,
             PGDN, PKDA, Diagonal KDN) w.r.t. q, k, v, log-decay, every gate,
-            the initial state and the gain state's initial value.
+            the initial state and the gain state's initial value; and the same
+            gradients through the chunkwise form (GDN, KLA, KDA).
 ridge       Side oracles fixed by closed forms: exact ridge regression (ATQ),
             its Sherman-Morrison recursion (ATK), the diagonal counterexample
             and a dense-covariance Kalman filter.

@@ -211,3 +211,132 @@ def tokenwise_backward(q, k, v, log_alpha, variant: str, do, dS_T=None, *, eta=N
     if kdn:
         out.update(domega=domega, dr=dr_, daux0=daux)
     return out
+
+
+def chunkwise_backward(q, k, v, log_alpha, variant: str, chunk: int, do, dS_T=None, *, eta,
+                       eps: float = 1e-6, q_l2norm: bool = False, k_l2norm: bool = False,
+                       S0=None):
+    """The same gradients as ``tokenwise_backward`` (GDN, KLA, KDA) through the
+    chunkwise form, chunk by chunk in reverse: the generalised Eqs. (7)-(9) of
+    the KLA notes (section 2.5), per chunk with input state S_0,
+
+        R = V - (Gamma.K) S_0,  (I + L) E = R,  O = (Gamma.Q) S_0 + P E,
+        S_out = gamma_C . S_0 + Wbar^T E,  Wbar_j = exp(g_C - g_j) . w_j,
+
+    differentiated line by line: dS_0 = gamma_C . dS_out + (Gamma.Q)^T dO
+    - (Gamma.K)^T dR;  dE = Wbar dS_out + P^T dO;  dR = (I + L)^-T dE;
+    dL = -dR E^T (strictly lower), dP = dO E^T (lower);  dV = dR; and the Gram
+    entries L_ij = sum_c k_ic w_jc exp(g_ic - g_jc) (P with q) pass their
+    gradients to k, w, q and the log-decay differences.  The per-chunk
+    cumulative log-decay g then gives d log alpha_t = sum_{i >= t} dg_i.
+    """
+    if variant not in ("gdn", "kla", "kda"):
+        raise ValueError(f"no chunkwise backward for variant {variant!r}")
+    f = lambda a: np.asarray(a, dtype=np.float64)  # noqa: E731
+    q_raw, k_raw, v, la, eta, do = f(q), f(k), f(v), f(log_alpha), f(eta), f(do)
+    B, T, H, dk = k_raw.shape
+    dv = v.shape[-1]
+    qh = q_raw / np.sqrt(np.sum(q_raw * q_raw, axis=-1, keepdims=True)) if q_l2norm else q_raw
+    kh = k_raw / np.sqrt(np.sum(k_raw * k_raw, axis=-1, keepdims=True)) if k_l2norm else k_raw
+    per_channel = la.ndim == 4
+    dq, dk_, dv_ = np.zeros_like(qh), np.zeros_like(kh), np.zeros_like(v)
+    dla, deta = np.zeros_like(la), np.zeros_like(eta)
+    dS0_all = np.zeros((B, H, dk, dv))
+    starts = list(range(0, T, chunk))
+    for b in range(B):
+        for h in range(H):
+            # forward: the state at every chunk start, and each chunk's pieces
+            S = np.zeros((dk, dv)) if S0 is None else f(S0)[b, h].copy()
+            saved = []
+            for t0 in starts:
+                t1 = min(T, t0 + chunk)
+                kc, qc, vc = kh[b, t0:t1, h], qh[b, t0:t1, h], v[b, t0:t1, h]
+                lac = la[b, t0:t1, h]
+                g = np.cumsum(lac, axis=0)
+                if not per_channel:
+                    g = np.repeat(g[:, None], dk, axis=1)
+                ec = eta[b, t0:t1, h]
+                if variant == "kla":
+                    sk = np.sum(kc * kc, axis=1) + eps
+                    wc = (ec / sk)[:, None] * kc
+                else:
+                    wc = ec[:, None] * kc
+                C = t1 - t0
+                low_s, low_i = np.tril(np.ones((C, C)), -1), np.tril(np.ones((C, C)), 0)
+                ratio = np.exp(g[:, None, :] - g[None, :, :]) * low_i[:, :, None]
+                L = np.einsum("ic,jc,ijc->ij", kc, wc, ratio) * low_s
+                P = np.einsum("ic,jc,ijc->ij", qc, wc, ratio) * low_i
+                Gm = np.exp(g)
+                Kg, Qg = kc * Gm, qc * Gm
+                A = np.eye(C) + L
+                E = np.linalg.solve(A, vc - Kg @ S)
+                Wb = np.exp(g[-1][None, :] - g) * wc
+                saved.append((t0, t1, kc, qc, wc, g, ratio, L, P, Kg, Qg, A, E, Wb, S.copy()))
+                S = np.exp(g[-1])[:, None] * S + Wb.T @ E
+            # reverse over chunks
+            dS = np.zeros((dk, dv)) if dS_T is None else f(dS_T)[b, h].copy()
+            for (t0, t1, kc, qc, wc, g, ratio, L, P, Kg, Qg, A, E, Wb, Sin) in reversed(saved):
+                C = t1 - t0
+                dOc = do[b, t0:t1, h]
+                gC = np.exp(g[-1])
+                # S_out = gamma_C . S_in + Wbar^T E
+                dSin = gC[:, None] * dS
+                dgC = np.sum(dS * Sin, axis=1) * gC                       # d g_C (per channel)
+                dWb = E @ dS.T                                            # [C, dk]
+                dE = Wb @ dS
+                # O = Qg S_in + P E
+                dQg = dOc @ Sin.T
+                dSin += Qg.T @ dOc
+                dP = (dOc @ E.T) * np.tril(np.ones((C, C)), 0)
+                dE += P.T @ dOc
+                # E = A^-1 R
+                dR = np.linalg.solve(A.T, dE)
+                dL = -(dR @ E.T) * np.tril(np.ones((C, C)), -1)
+                # R = V - Kg S_in
+                dv_[b, t0:t1, h] = dR
+                dKg = -dR @ Sin.T
+                dSin -= Kg.T @ dR
+                # Wbar_j = exp(g_C - g_j) . w_j
+                eW = np.exp(g[-1][None, :] - g)
+                dw = dWb * eW
+                dg = np.zeros_like(g)
+                dgC = dgC + np.sum(dWb * Wb, axis=0)
+                dg -= dWb * Wb
+                # L, P entries: X_ijc = a_ic w_jc exp(g_ic - g_jc)
+                for Mgrad, Xc, dX in ((dL, kc, "k"), (dP, qc, "q")):
+                    X = Xc[:, None, :] * wc[None, :, :] * ratio          # [i, j, c]
+                    contrib = Mgrad[:, :, None] * X
+                    dg += np.sum(contrib, axis=1)                         # + over j (row i)
+                    dg -= np.sum(contrib, axis=0)                         # - over i (column j)
+                    dw += np.einsum("ij,ic,ijc->jc", Mgrad, Xc, ratio)
+                    da = np.einsum("ij,jc,ijc->ic", Mgrad, wc, ratio)
+                    if dX == "k":
+                        dk_[b, t0:t1, h] += da
+                    else:
+                        dq[b, t0:t1, h] += da
+                # Kg = k . exp(g), Qg = q . exp(g)
+                Gm = np.exp(g)
+                dk_[b, t0:t1, h] += dKg * Gm
+                dq[b, t0:t1, h] += dQg * Gm
+                dg += dKg * Kg + dQg * Qg
+                dg[-1] += dgC
+                # w (GDN, KDA: eta k; KLA: eta k / (|k|^2 + eps))
+                ec = eta[b, t0:t1, h]
+                if variant == "kla":
+                    sk = np.sum(kc * kc, axis=1) + eps
+                    kdw = np.sum(kc * dw, axis=1)
+                    dk_[b, t0:t1, h] += (ec / sk)[:, None] * dw - (2 * ec * kdw / sk ** 2)[:, None] * kc
+                    deta[b, t0:t1, h] = kdw / sk
+                else:
+                    dk_[b, t0:t1, h] += ec[:, None] * dw
+                    deta[b, t0:t1, h] = np.sum(kc * dw, axis=1)
+                # g = cumsum(log alpha): reverse cumulative sum (scalar decay: over channels too)
+                rc = np.cumsum(dg[::-1], axis=0)[::-1]
+                dla[b, t0:t1, h] = rc if per_channel else np.sum(rc, axis=1)
+                dS = dSin
+            dS0_all[b, h] = dS
+    if q_l2norm:
+        dq = _norm_backward(q_raw, dq)
+    if k_l2norm:
+        dk_ = _norm_backward(k_raw, dk_)
+    return dict(dq=dq, dk=dk_, dv=dv_, dlog_alpha=dla, deta=deta, dS0=dS0_all)
