@@ -14,8 +14,8 @@ recurrence  Tokenwise recurrence (the plain definition) for GDN, KLA, PGDN,
             (dense key covariance), one token at a time, in float64.
 chunkwise   A naive chunkwise-parallel restatement (triangular system per
             chunk), written independently of ``recurrence`` as a cross-check.
-backward    Reverse-mode gradients of the tokenwise recurrence (GDN, KLA, KDA,
-            PGDN, PKDA, Diagonal KDN) w.r.t. q, k, v, log-decay, every gate,
+backward    Reverse-mode gradients of the tokenwise recurrence (every variant)
+            w.r.t. q, k, v, log-decay, every gate,
             the initial state and the gain state's initial value; and the same
             gradients through the chunkwise form (GDN, KLA, KDA).
 ridge       Side oracles fixed by closed forms: exact ridge regression (ATQ),

@@ -1,5 +1,5 @@
 """Reverse-mode gradients of the tokenwise recurrence, fp64 (GDN, KLA, KDA, PGDN,
-PKDA, Diagonal KDN).
+PKDA, Diagonal KDN, isotropic KDN, the exact Kalman memory).
 
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 
@@ -37,6 +37,15 @@ The gain states carry their own adjoints backwards:
       du = -dp_t p^^2 / (1 + u p^)^2,  dk = dw . p^ / den - 2 c p^ . k / den^2 + 2 (mu/r) k . du,
       dr = -c / den^2 - (mu / r^2) sum(k.k du),  d omega = dp^,
       dp_{t-1} = alpha^2 dp^,  d alpha += 2 alpha p dp^.
+  Isotropic KDN (KDN notes section 7, Eq. (40)): a = mean alpha^2, b^ = a b + omega,
+      beta = b^ / (r + b^ s), s = ||k||^2, w = beta k, b_t = b^ / (1 + u b^),
+      u = mu s / (dk r): the scalar adjoint db follows the same pattern, and
+      d alpha_i += 2 alpha_i (b db^) / dk.
+  Exact Kalman (KDN notes section 2.2): P^ = D P D^T + diag(omega), y = P^ k,
+      x = P^T k, den = r + k^T y, w = y / den, P_t = P^ - y x^T / den: dP^ = dP_t
+      + dy k^T + k dx^T with dy = dw / den - dP_t x / den + dden k, dx = -dP_t^T y / den,
+      dden = y^T dP_t x / den^2 - w^T dw / den, then dP_{t-1} = D dP^ D,
+      d alpha_i += sum_j (dP^_ij P_ij + dP^_ji P_ji) alpha_j, d omega = diag(dP^).
 The states S_t (and the gain states) of the forward are kept (fp64, small test
 sizes only).
 """
@@ -45,7 +54,7 @@ from __future__ import annotations
 
 import numpy as np
 
-GRAD_VARIANTS = ("gdn", "kla", "kda", "pgdn", "pkda", "kdn")
+GRAD_VARIANTS = ("gdn", "kla", "kda", "pgdn", "pkda", "kdn", "ikdn", "ekdn")
 
 
 def _norm_backward(x_raw, dx_hat):
@@ -76,6 +85,7 @@ def tokenwise_backward(q, k, v, log_alpha, variant: str, do, dS_T=None, *, eta=N
     q_raw, k_raw, v, la, eta, do = f(q), f(k), f(v), f(log_alpha), f(eta), f(do)
     alphaP, betaP, mu, omega, r = f(alphaP), f(betaP), f(mu), f(omega), f(r)
     pstat, kdn = variant in ("pgdn", "pkda"), variant == "kdn"
+    ikdn, ekdn = variant == "ikdn", variant == "ekdn"
     B, T, H, dk = k_raw.shape
     dv = v.shape[-1]
     qh = q_raw / np.sqrt(np.sum(q_raw * q_raw, axis=-1, keepdims=True)) if q_l2norm else q_raw
@@ -93,8 +103,13 @@ def tokenwise_backward(q, k, v, log_alpha, variant: str, do, dS_T=None, *, eta=N
         aux = np.zeros((B, H, dk)) if aux0 is None else f(aux0).copy()
     elif kdn:
         aux = np.ones((B, H, dk)) if aux0 is None else f(aux0).copy()
-    aux_prev = np.zeros((T, B, H, dk))
-    A_all = np.zeros((T, B, H, dk))      # PGDN statistic A_t / KDN predicted p^_t
+    elif ikdn:
+        aux = np.ones((B, H)) if aux0 is None else f(aux0).copy()
+    elif ekdn:
+        aux = (np.broadcast_to(np.eye(dk), (B, H, dk, dk)).copy() if aux0 is None
+               else f(aux0).copy())
+    aux_prev = np.zeros((T,) + aux.shape) if aux is not None else None
+    A_all = np.zeros((T,) + aux.shape) if aux is not None else None   # A_t / p^_t / b^_t / P^_t
     for t in range(T):
         S_prev[t] = S
         a_t = alpha[:, t]
@@ -110,6 +125,20 @@ def tokenwise_backward(q, k, v, log_alpha, variant: str, do, dS_T=None, *, eta=N
             rr = np.log(np.maximum(aux, log_floor)) - mu[None, :, None]
             Bs = np.exp(-np.log(x) * rr / (1 + np.abs(rr)))
             w = eta[:, t][..., None] * Bs * kt
+        elif ikdn:
+            b_hat = np.mean(a_t * a_t, axis=-1) * aux + omega[:, t]
+            A_all[t] = b_hat
+            sk = np.sum(kt * kt, axis=-1)
+            w = (b_hat / (r[:, t] + b_hat * sk))[..., None] * kt
+            aux = b_hat / (1 + info_scale * sk / (dk * r[:, t]) * b_hat)
+        elif ekdn:
+            P_hat = a_t[..., :, None] * aux * a_t[..., None, :] + omega[:, t][..., :, None] * np.eye(dk)
+            A_all[t] = P_hat
+            y = np.einsum("bhij,bhj->bhi", P_hat, kt)
+            xv = np.einsum("bhji,bhj->bhi", P_hat, kt)
+            den = r[:, t] + np.sum(kt * y, axis=-1)
+            w = y / den[..., None]
+            aux = P_hat - y[..., :, None] * xv[..., None, :] / den[..., None, None]
         elif kdn:
             p_hat = a_t * a_t * aux + omega[:, t]
             A_all[t] = p_hat
@@ -129,12 +158,12 @@ def tokenwise_backward(q, k, v, log_alpha, variant: str, do, dS_T=None, *, eta=N
     dv_ = np.zeros_like(v)
     dla = np.zeros_like(la)
     deta = np.zeros((B, T, H)) if eta is not None else None
-    daux = (np.zeros((B, H, dk)) if daux_T is None else f(daux_T).copy()) if aux is not None else None
+    daux = (np.zeros(aux.shape) if daux_T is None else f(daux_T).copy()) if aux is not None else None
     dalphaP = np.zeros((B, T, H)) if pstat else None
     dbetaP = np.zeros((B, T, H)) if pstat else None
     dmu = np.zeros(H) if pstat else None
-    domega = np.zeros((B, T, H, dk)) if kdn else None
-    dr_ = np.zeros((B, T, H)) if kdn else None
+    domega = (np.zeros_like(omega) if (kdn or ikdn or ekdn) else None)
+    dr_ = np.zeros((B, T, H)) if (kdn or ikdn or ekdn) else None
     for t in range(T - 1, -1, -1):
         a_t = alpha[:, t]
         S_tilde = (a_t[..., :, None] if per_channel else a_t[..., None, None]) * S_prev[t]
@@ -172,6 +201,43 @@ def tokenwise_backward(q, k, v, log_alpha, variant: str, do, dS_T=None, *, eta=N
             dbetaP[:, t] = np.sum(kt * kt * dA, axis=-1)
             dk_[:, t] += 2 * betaP[:, t][..., None] * kt * dA
             daux = alphaP[:, t][..., None] * dA
+        elif ikdn:
+            b_hat, rt = A_all[t], r[:, t]
+            sk = np.sum(kt * kt, axis=-1)
+            den = rt + b_hat * sk
+            beta = b_hat / den
+            uu = info_scale * sk / (dk * rt)
+            q1 = 1 + uu * b_hat
+            dbeta = np.sum(kt * dw, axis=-1)
+            dk_[:, t] += beta[..., None] * dw
+            db_hat = dbeta * rt / den ** 2 + daux / q1 ** 2
+            du = -daux * b_hat ** 2 / q1 ** 2
+            dsk = -dbeta * b_hat ** 2 / den ** 2 + du * info_scale / (dk * rt)
+            dr_[:, t] = -dbeta * b_hat / den ** 2 - du * info_scale * sk / (dk * rt ** 2)
+            dk_[:, t] += 2 * dsk[..., None] * kt
+            domega[:, t] = db_hat
+            a_mean = np.mean(a_t * a_t, axis=-1)
+            daux = a_mean * db_hat
+            dalpha_gain = 2 * a_t * (aux_prev[t] * db_hat)[..., None] / dk
+        elif ekdn:
+            P_hat, rt, Pp = A_all[t], r[:, t], aux_prev[t]
+            y = np.einsum("bhij,bhj->bhi", P_hat, kt)
+            xv = np.einsum("bhji,bhj->bhi", P_hat, kt)
+            den = rt + np.sum(kt * y, axis=-1)
+            wv = y / den[..., None]
+            dden = (np.einsum("bhi,bhij,bhj->bh", y, daux, xv) / den ** 2
+                    - np.sum(wv * dw, axis=-1) / den)
+            dy = dw / den[..., None] - np.einsum("bhij,bhj->bhi", daux, xv) / den[..., None] \
+                + dden[..., None] * kt
+            dxv = -np.einsum("bhji,bhj->bhi", daux, y) / den[..., None]
+            dr_[:, t] = dden
+            dk_[:, t] += (dden[..., None] * y + np.einsum("bhji,bhj->bhi", P_hat, dy)
+                          + np.einsum("bhij,bhj->bhi", P_hat, dxv))
+            dP_hat = daux + dy[..., :, None] * kt[..., None, :] + kt[..., :, None] * dxv[..., None, :]
+            domega[:, t] = np.diagonal(dP_hat, axis1=-2, axis2=-1)
+            daux = a_t[..., :, None] * dP_hat * a_t[..., None, :]
+            dalpha_gain = (np.einsum("bhij,bhij,bhj->bhi", dP_hat, Pp, a_t)
+                           + np.einsum("bhji,bhji,bhj->bhi", dP_hat, Pp, a_t))
         elif kdn:
             p_hat = A_all[t]
             rt = r[:, t]
@@ -204,11 +270,11 @@ def tokenwise_backward(q, k, v, log_alpha, variant: str, do, dS_T=None, *, eta=N
     if k_l2norm:
         dk_ = _norm_backward(k_raw, dk_)
     out = dict(dq=dq, dk=dk_, dv=dv_, dlog_alpha=dla, dS0=G)
-    if deta is not None and not kdn:
+    if deta is not None and not (kdn or ikdn or ekdn):
         out["deta"] = deta
     if pstat:
         out.update(dalphaP=dalphaP, dbetaP=dbetaP, dmu=dmu, daux0=daux)
-    if kdn:
+    if kdn or ikdn or ekdn:
         out.update(domega=domega, dr=dr_, daux0=daux)
     return out
 

@@ -589,15 +589,20 @@ def test_backward_matches_central_differences(variant, norm):
     the reverse sweep is pinned to the independently written forward."""
     r = rng(60)
     B, T, H, dk, dv = 1, 6, 2, 3, 2
-    d = random_inputs(variant, B=B, T=T, H=H, dk=dk, dv=dv, seed=61)
+    d = random_inputs("kdn" if variant == "ekdn" else variant, B=B, T=T, H=H, dk=dk, dv=dv, seed=61)
     d["S0"] = r.standard_normal((B, H, dk, dv))
     if variant in ("pgdn", "pkda"):
         d["aux0"] = r.uniform(0.5, 2.0, (B, H, dk))
     elif variant == "kdn":
         d["aux0"] = r.uniform(0.5, 1.5, (B, H, dk))
+    elif variant == "ikdn":
+        d["aux0"] = r.uniform(0.5, 1.5, (B, H))
+    elif variant == "ekdn":   # an SPD covariance
+        A = r.standard_normal((B, H, dk, dk))
+        d["aux0"] = A @ np.swapaxes(A, -1, -2) / dk + 0.5 * np.eye(dk)
     dO = r.standard_normal((B, T, H, dv))
     dS = r.standard_normal((B, H, dk, dv))
-    daux = r.standard_normal((B, H, dk)) if "aux0" in d else None
+    daux = r.standard_normal(d["aux0"].shape) if "aux0" in d else None
     flags = dict(q_l2norm=norm, k_l2norm=norm, eps=1e-6)
     gate_keys = [kk for kk in ("eta", "alphaP", "betaP", "mu", "omega", "r") if kk in d]
 
