@@ -17,7 +17,7 @@ chunkwise   A naive chunkwise-parallel restatement (triangular system per
 backward    Reverse-mode gradients of the tokenwise recurrence (every variant)
             w.r.t. q, k, v, log-decay, every gate,
             the initial state and the gain state's initial value; and the same
-            gradients through the chunkwise form (GDN, KLA, KDA).
+            gradients through the chunkwise form (every chunkwise variant).
 ridge       Side oracles fixed by closed forms: exact ridge regression (ATQ),
             its Sherman-Morrison recursion (ATK), the diagonal counterexample
             and a dense-covariance Kalman filter.

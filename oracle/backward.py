@@ -279,9 +279,138 @@ def tokenwise_backward(q, k, v, log_alpha, variant: str, do, dS_T=None, *, eta=N
     return out
 
 
-def chunkwise_backward(q, k, v, log_alpha, variant: str, chunk: int, do, dS_T=None, *, eta,
-                       eps: float = 1e-6, q_l2norm: bool = False, k_l2norm: bool = False,
-                       S0=None):
+def _gain_forward(variant, kh, alpha, *, eta, eps, alphaP, betaP, mu, x, log_floor, omega, r,
+                  info_scale, aux0):
+    """The write vectors w_t of every token from each variant's gain recursion
+    alone (they do not depend on the memory S), and the states the reverse
+    sweep needs: the key statistic A_t (PGDN, PKDA), the predicted variance
+    p^_t / b^_t (Diagonal / isotropic KDN) with the state before each token."""
+    B, T, H, dk = kh.shape
+    w = np.zeros_like(kh)
+    saved = {}
+    if variant in ("gdn", "kda"):
+        w = eta[..., None] * kh
+    elif variant == "kla":
+        w = (eta / (np.sum(kh * kh, axis=-1) + eps))[..., None] * kh
+    elif variant in ("pgdn", "pkda"):
+        A = np.zeros((B, H, dk)) if aux0 is None else np.array(aux0, dtype=np.float64)
+        prev, cur = np.zeros_like(kh), np.zeros_like(kh)
+        for t in range(T):
+            prev[:, t] = A
+            A = alphaP[:, t][..., None] * A + betaP[:, t][..., None] * kh[:, t] ** 2
+            cur[:, t] = A
+            rr = np.log(np.maximum(A, log_floor)) - mu[None, :, None]
+            w[:, t] = eta[:, t][..., None] * np.exp(-np.log(x) * rr / (1 + np.abs(rr))) * kh[:, t]
+        saved = dict(prev=prev, cur=cur, final=A)
+    elif variant == "kdn":
+        p = np.ones((B, H, dk)) if aux0 is None else np.array(aux0, dtype=np.float64)
+        prev, cur = np.zeros_like(kh), np.zeros_like(kh)
+        for t in range(T):
+            prev[:, t] = p
+            a = alpha[:, t]
+            p_hat = a * a * p + omega[:, t]
+            cur[:, t] = p_hat
+            kt = kh[:, t]
+            w[:, t] = p_hat * kt / (r[:, t] + np.sum(p_hat * kt * kt, axis=-1))[..., None]
+            p = p_hat / (1 + (info_scale / r[:, t])[..., None] * kt * kt * p_hat)
+        saved = dict(prev=prev, cur=cur, final=p)
+    elif variant == "ikdn":
+        b = np.ones((B, H)) if aux0 is None else np.array(aux0, dtype=np.float64)
+        prev, cur = np.zeros((B, T, H)), np.zeros((B, T, H))
+        for t in range(T):
+            prev[:, t] = b
+            b_hat = np.mean(alpha[:, t] ** 2, axis=-1) * b + omega[:, t]
+            cur[:, t] = b_hat
+            sk = np.sum(kh[:, t] ** 2, axis=-1)
+            w[:, t] = (b_hat / (r[:, t] + b_hat * sk))[..., None] * kh[:, t]
+            b = b_hat / (1 + info_scale * sk / (dk * r[:, t]) * b_hat)
+        saved = dict(prev=prev, cur=cur, final=b)
+    else:
+        raise ValueError(f"no gain recursion for variant {variant!r}")
+    return w, saved
+
+
+def _gain_backward(variant, dw, kh, alpha, saved, *, eta, eps, alphaP, betaP, mu, x, log_floor,
+                   omega, r, info_scale, daux_T):
+    """Reverse sweep of the gain recursion from dL/dw_t (and dL/daux_T): returns
+    the key gradient through w, dL/dalpha through the gain (per channel), the
+    gate gradients and dL/daux_0."""
+    B, T, H, dk = kh.shape
+    dk_ = np.zeros_like(kh)
+    dal = np.zeros_like(kh)
+    g = {}
+    if variant in ("gdn", "kda"):
+        dk_ = eta[..., None] * dw
+        g["deta"] = np.sum(kh * dw, axis=-1)
+    elif variant == "kla":
+        sk = np.sum(kh * kh, axis=-1) + eps
+        kdw = np.sum(kh * dw, axis=-1)
+        dk_ = (eta / sk)[..., None] * dw - (2 * eta * kdw / sk ** 2)[..., None] * kh
+        g["deta"] = kdw / sk
+    elif variant in ("pgdn", "pkda"):
+        dA_next = np.zeros((B, H, dk)) if daux_T is None else np.array(daux_T, dtype=np.float64)
+        deta, daP, dbP, dmu = (np.zeros((B, T, H)), np.zeros((B, T, H)), np.zeros((B, T, H)),
+                               np.zeros(H))
+        for t in range(T - 1, -1, -1):
+            A, kt = saved["cur"][:, t], kh[:, t]
+            rr = np.log(np.maximum(A, log_floor)) - mu[None, :, None]
+            Bs = np.exp(-np.log(x) * rr / (1 + np.abs(rr)))
+            dk_[:, t] += eta[:, t][..., None] * Bs * dw[:, t]
+            deta[:, t] = np.sum(Bs * kt * dw[:, t], axis=-1)
+            drr = -np.log(x) * Bs * (eta[:, t][..., None] * kt * dw[:, t]) / (1 + np.abs(rr)) ** 2
+            dA = dA_next + np.where(A > log_floor, drr / A, 0.0)
+            dmu -= np.sum(np.where(A > log_floor, drr, 0.0), axis=(0, 2))
+            daP[:, t] = np.sum(saved["prev"][:, t] * dA, axis=-1)
+            dbP[:, t] = np.sum(kt * kt * dA, axis=-1)
+            dk_[:, t] += 2 * betaP[:, t][..., None] * kt * dA
+            dA_next = alphaP[:, t][..., None] * dA
+        g.update(deta=deta, dalphaP=daP, dbetaP=dbP, dmu=dmu, daux0=dA_next)
+    elif variant == "kdn":
+        dp_next = np.zeros((B, H, dk)) if daux_T is None else np.array(daux_T, dtype=np.float64)
+        domega, dr = np.zeros_like(kh), np.zeros((B, T, H))
+        for t in range(T - 1, -1, -1):
+            p_hat, kt, rt, a = saved["cur"][:, t], kh[:, t], r[:, t], alpha[:, t]
+            den = rt + np.sum(p_hat * kt * kt, axis=-1)
+            c = np.sum(dw[:, t] * p_hat * kt, axis=-1)
+            u = (info_scale / rt)[..., None] * kt * kt
+            q1 = 1 + u * p_hat
+            dp_hat = dw[:, t] * kt / den[..., None] - (c / den ** 2)[..., None] * kt * kt + dp_next / q1 ** 2
+            du = -dp_next * p_hat ** 2 / q1 ** 2
+            dk_[:, t] += (dw[:, t] * p_hat / den[..., None] - (2 * c / den ** 2)[..., None] * p_hat * kt
+                          + 2 * (info_scale / rt)[..., None] * kt * du)
+            dr[:, t] = -c / den ** 2 - info_scale / rt ** 2 * np.sum(kt * kt * du, axis=-1)
+            domega[:, t] = dp_hat
+            dal[:, t] = 2 * a * saved["prev"][:, t] * dp_hat
+            dp_next = a * a * dp_hat
+        g.update(domega=domega, dr=dr, daux0=dp_next)
+    elif variant == "ikdn":
+        db_next = np.zeros((B, H)) if daux_T is None else np.array(daux_T, dtype=np.float64)
+        domega, dr = np.zeros((B, T, H)), np.zeros((B, T, H))
+        for t in range(T - 1, -1, -1):
+            b_hat, kt, rt, a = saved["cur"][:, t], kh[:, t], r[:, t], alpha[:, t]
+            sk = np.sum(kt * kt, axis=-1)
+            den = rt + b_hat * sk
+            uu = info_scale * sk / (dk * rt)
+            q1 = 1 + uu * b_hat
+            dbeta = np.sum(kt * dw[:, t], axis=-1)
+            dk_[:, t] += (b_hat / den)[..., None] * dw[:, t]
+            db_hat = dbeta * rt / den ** 2 + db_next / q1 ** 2
+            du = -db_next * b_hat ** 2 / q1 ** 2
+            dsk = -dbeta * b_hat ** 2 / den ** 2 + du * info_scale / (dk * rt)
+            dr[:, t] = -dbeta * b_hat / den ** 2 - du * info_scale * sk / (dk * rt ** 2)
+            dk_[:, t] += 2 * dsk[..., None] * kt
+            domega[:, t] = db_hat
+            dal[:, t] = 2 * a * (saved["prev"][:, t] * db_hat)[..., None] / dk
+            db_next = np.mean(a * a, axis=-1) * db_hat
+        g.update(domega=domega, dr=dr, daux0=db_next)
+    return dk_, dal, g
+
+
+def chunkwise_backward(q, k, v, log_alpha, variant: str, chunk: int, do, dS_T=None, *,
+                       eta=None, eps: float = 1e-6, q_l2norm: bool = False,
+                       k_l2norm: bool = False, S0=None, alphaP=None, betaP=None, mu=None,
+                       x: float = 1.5, log_floor: float = 1e-12, omega=None, r=None,
+                       info_scale: float = 1.0, aux0=None, daux_T=None):
     """The same gradients as ``tokenwise_backward`` (GDN, KLA, KDA) through the
     chunkwise form, chunk by chunk in reverse: the generalised Eqs. (7)-(9) of
     the KLA notes (section 2.5), per chunk with input state S_0,
@@ -294,19 +423,29 @@ def chunkwise_backward(q, k, v, log_alpha, variant: str, chunk: int, do, dS_T=No
     dL = -dR E^T (strictly lower), dP = dO E^T (lower);  dV = dR; and the Gram
     entries L_ij = sum_c k_ic w_jc exp(g_ic - g_jc) (P with q) pass their
     gradients to k, w, q and the log-decay differences.  The per-chunk
-    cumulative log-decay g then gives d log alpha_t = sum_{i >= t} dg_i.
+    cumulative log-decay g then gives d log alpha_t = sum_{i >= t} dg_i.  The write
+    vectors come from each variant's gain recursion, which does not involve the
+    memory: the chunk sweep collects dL/dw_t, and a separate reverse gain sweep
+    turns it into the gate and gain-state gradients (every chunkwise variant:
+    GDN, KLA, KDA, PGDN, PKDA, Diagonal and isotropic KDN).
     """
-    if variant not in ("gdn", "kla", "kda"):
+    if variant not in ("gdn", "kla", "kda", "pgdn", "pkda", "kdn", "ikdn"):
         raise ValueError(f"no chunkwise backward for variant {variant!r}")
-    f = lambda a: np.asarray(a, dtype=np.float64)  # noqa: E731
+    f = lambda a: None if a is None else np.asarray(a, dtype=np.float64)  # noqa: E731
     q_raw, k_raw, v, la, eta, do = f(q), f(k), f(v), f(log_alpha), f(eta), f(do)
+    alphaP, betaP, mu, omega, r = f(alphaP), f(betaP), f(mu), f(omega), f(r)
     B, T, H, dk = k_raw.shape
     dv = v.shape[-1]
     qh = q_raw / np.sqrt(np.sum(q_raw * q_raw, axis=-1, keepdims=True)) if q_l2norm else q_raw
     kh = k_raw / np.sqrt(np.sum(k_raw * k_raw, axis=-1, keepdims=True)) if k_l2norm else k_raw
     per_channel = la.ndim == 4
+    gk = dict(eta=eta, eps=eps, alphaP=alphaP, betaP=betaP, mu=mu, x=x, log_floor=log_floor,
+              omega=omega, r=r, info_scale=info_scale)
+    alpha_c = np.exp(la) if per_channel else np.repeat(np.exp(la)[..., None], dk, axis=-1)
+    w_all, gsaved = _gain_forward(variant, kh, alpha_c, aux0=aux0, **gk)
+    dw_all = np.zeros_like(kh)
     dq, dk_, dv_ = np.zeros_like(qh), np.zeros_like(kh), np.zeros_like(v)
-    dla, deta = np.zeros_like(la), np.zeros_like(eta)
+    dla = np.zeros_like(la)
     dS0_all = np.zeros((B, H, dk, dv))
     starts = list(range(0, T, chunk))
     for b in range(B):
@@ -321,12 +460,7 @@ def chunkwise_backward(q, k, v, log_alpha, variant: str, chunk: int, do, dS_T=No
                 g = np.cumsum(lac, axis=0)
                 if not per_channel:
                     g = np.repeat(g[:, None], dk, axis=1)
-                ec = eta[b, t0:t1, h]
-                if variant == "kla":
-                    sk = np.sum(kc * kc, axis=1) + eps
-                    wc = (ec / sk)[:, None] * kc
-                else:
-                    wc = ec[:, None] * kc
+                wc = w_all[b, t0:t1, h]
                 C = t1 - t0
                 low_s, low_i = np.tril(np.ones((C, C)), -1), np.tril(np.ones((C, C)), 0)
                 ratio = np.exp(g[:, None, :] - g[None, :, :]) * low_i[:, :, None]
@@ -386,23 +520,23 @@ def chunkwise_backward(q, k, v, log_alpha, variant: str, chunk: int, do, dS_T=No
                 dq[b, t0:t1, h] += dQg * Gm
                 dg += dKg * Kg + dQg * Qg
                 dg[-1] += dgC
-                # w (GDN, KDA: eta k; KLA: eta k / (|k|^2 + eps))
-                ec = eta[b, t0:t1, h]
-                if variant == "kla":
-                    sk = np.sum(kc * kc, axis=1) + eps
-                    kdw = np.sum(kc * dw, axis=1)
-                    dk_[b, t0:t1, h] += (ec / sk)[:, None] * dw - (2 * ec * kdw / sk ** 2)[:, None] * kc
-                    deta[b, t0:t1, h] = kdw / sk
-                else:
-                    dk_[b, t0:t1, h] += ec[:, None] * dw
-                    deta[b, t0:t1, h] = np.sum(kc * dw, axis=1)
+                dw_all[b, t0:t1, h] = dw
                 # g = cumsum(log alpha): reverse cumulative sum (scalar decay: over channels too)
                 rc = np.cumsum(dg[::-1], axis=0)[::-1]
                 dla[b, t0:t1, h] = rc if per_channel else np.sum(rc, axis=1)
                 dS = dSin
             dS0_all[b, h] = dS
+    # the gain recursion's reverse sweep from dL/dw
+    dk_g, dal_g, gg = _gain_backward(variant, dw_all, kh, alpha_c, gsaved, daux_T=f(daux_T), **gk)
+    dk_ += dk_g
+    if per_channel:
+        dla += alpha_c * dal_g
+    elif variant not in ("gdn", "kla", "pgdn"):
+        raise ValueError("a per-channel gain needs per-channel decay")
     if q_l2norm:
         dq = _norm_backward(q_raw, dq)
     if k_l2norm:
         dk_ = _norm_backward(k_raw, dk_)
-    return dict(dq=dq, dk=dk_, dv=dv_, dlog_alpha=dla, deta=deta, dS0=dS0_all)
+    out = dict(dq=dq, dk=dk_, dv=dv_, dlog_alpha=dla, dS0=dS0_all)
+    out.update(gg)
+    return out

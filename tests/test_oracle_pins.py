@@ -633,19 +633,26 @@ def test_backward_matches_central_differences(variant, norm):
         np.testing.assert_allclose(g[key], num, rtol=1e-5, atol=1e-7, err_msg=name)
 
 
-@pytest.mark.parametrize("variant", ["gdn", "kla", "kda"])
+@pytest.mark.parametrize("variant", ["gdn", "kla", "kda", "pgdn", "pkda", "kdn", "ikdn"])
 @pytest.mark.parametrize("T,chunk", [(1, 4), (7, 4), (16, 8), (13, 64), (21, 2)])
 def test_chunkwise_backward_equals_tokenwise_backward(variant, T, chunk):
     """The chunk-by-chunk reverse sweep through Eqs. (7)-(9) (the form a kernel
-    follows) gives the tokenwise reverse sweep's gradients to rounding."""
+    follows), with the gain recursion's reverse sweep from dL/dw, gives the
+    tokenwise reverse sweep's gradients to rounding."""
     r = rng(70 + T)
     B, H, dk, dv = 2, 2, 4, 3
     d = random_inputs(variant, B=B, T=T, H=H, dk=dk, dv=dv, seed=71 + T)
     S0 = r.standard_normal((B, H, dk, dv))
     dO = r.standard_normal((B, T, H, dv))
     dS = r.standard_normal((B, H, dk, dv))
-    kw = dict(eta=d["eta"], S0=S0, q_l2norm=True, k_l2norm=(variant == "kda"), eps=1e-6)
+    aux_shape = {"pgdn": (B, H, dk), "pkda": (B, H, dk), "kdn": (B, H, dk), "ikdn": (B, H)}.get(variant)
+    aux0 = r.uniform(0.5, 1.5, aux_shape) if aux_shape else None
+    daux = r.standard_normal(aux_shape) if aux_shape else None
+    gates = {kk: d[kk] for kk in ("eta", "alphaP", "betaP", "mu", "omega", "r") if kk in d}
+    kw = dict(S0=S0, aux0=aux0, daux_T=daux, q_l2norm=True,
+              k_l2norm=(variant not in ("gdn", "kla")), eps=1e-6, **gates)
     g1 = obw.tokenwise_backward(d["q"], d["k"], d["v"], d["log_alpha"], variant, dO, dS, **kw)
     g2 = obw.chunkwise_backward(d["q"], d["k"], d["v"], d["log_alpha"], variant, chunk, dO, dS, **kw)
-    for key in ("dq", "dk", "dv", "dlog_alpha", "deta", "dS0"):
+    assert set(g1) == set(g2), (sorted(g1), sorted(g2))
+    for key in g1:
         np.testing.assert_allclose(g2[key], g1[key], rtol=1e-9, atol=1e-11, err_msg=key)
