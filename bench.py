@@ -143,6 +143,24 @@ def decode_bytes(wl):
     return bh * (2 * wl.dk * wl.dv * 4 + (2 * wl.dk + 2 * wl.dv) * el + 8)
 
 
+def kernels_per_call(path, variant, B, H, has_workspace, nsm):
+    """libdr kernels one dr_chunk_fwd call launches on ``path``.
+
+    The two-phase paths launch a prep and a carry kernel; PGDN adds its key
+    statistic's map and scan kernels; on the CUDA-core two-phase path a few
+    rows (3 B H < nsm) make Diagonal KDN add its variance map and scan kernels
+    and PKDA / isotropic KDN run the fused kernel alone (KDA: never either).
+    Every other path is one kernel.  A memset of the chain flags is not a kernel.
+    """
+    if not has_workspace or path not in ("tc_split", "simt_split"):
+        return 1
+    if path == "simt_split":
+        if 3 * B * H >= nsm or variant == "kda":
+            return 2
+        return 1 if variant in ("pkda", "ikdn") else 4
+    return 4 if variant == "pgdn" else 2
+
+
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -394,20 +412,12 @@ def main():
     step_ms = [s.elapsed_time(e) for s, e in ev]
     total_s = max_over_ranks(sum(step_ms) / 1e3, world)
     dr.check(dr.dr_get_device_status(), "timed region")
-    def kernels_per_call(v):   # the two-phase paths launch a prep and a carry kernel
-        path = dr.dr_chunk_fwd_path(dr.VARIANT_IDS[v], 1 if wl.dtype == "bf16" else 0, wl.dk,
-                                    wl.dv, wl.chunk)
-        if ws is None or path not in ("tc_split", "simt_split"):
-            return 1
-        # with few rows the KDN variance takes map and scan kernels first (KDA: none;
-        # PKDA: the fused kernel alone)
-        nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-        if path == "simt_split":
-            if 3 * wl.B * wl.H >= nsm or v == "kda":
-                return 2
-            return 1 if v in ("pkda", "ikdn") else 4
-        return 4 if v == "pgdn" else 2   # PGDN: statistic map and scan kernels first
-    launches = args.steps * sum(kernels_per_call(v) for v in variants)
+    nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    launches = args.steps * sum(
+        kernels_per_call(dr.dr_chunk_fwd_path(dr.VARIANT_IDS[v], 1 if wl.dtype == "bf16" else 0,
+                                              wl.dk, wl.dv, wl.chunk),
+                         v, wl.B, wl.H, ws is not None, nsm)
+        for v in variants)
     value = job_tokens_per_s(world, args.steps, len(variants), wl.B, wl.T, total_s)
 
     var_stats = {}

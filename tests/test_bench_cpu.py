@@ -67,3 +67,19 @@ def test_default_arguments_are_one_gpu_and_short(monkeypatch):
     args = bench.parse()
     assert args.gpus == 1 and args.impl == "ours" and args.workload == "gdn_kla_bf16"
     assert args.warmup >= 3 and 1 <= args.steps <= 200
+
+
+def test_kernels_per_call_counts_every_path():
+    """The gpu_launches claim: kernels per dr_chunk_fwd call by path and variant."""
+    k = bench.kernels_per_call
+    assert k("tc_split", "kla", 8, 8, True, 152) == 2          # prep + carry
+    assert k("tc_split", "pgdn", 4, 16, True, 152) == 4        # + statistic map and scan
+    assert k("tc_split", "kla", 8, 8, False, 152) == 1         # no workspace: one kernel
+    assert k("tc_ws", "kla", 8, 8, False, 152) == 1
+    assert k("simt_split", "kdn", 4, 16, True, 152) == 2       # variance chained in the prep
+    assert k("simt_split", "kdn", 1, 2, True, 152) == 4        # few rows: map + scan first
+    assert k("simt_split", "kda", 1, 2, True, 152) == 2        # no gain state across chunks
+    assert k("simt_split", "pkda", 1, 2, True, 152) == 1       # few rows: the fused kernel
+    assert k("simt_split", "ikdn", 4, 16, True, 152) == 2
+    assert k("kalman", "ekdn", 4, 16, False, 152) == 1
+    assert k("simt", "kla", 1, 2, False, 152) == 1
