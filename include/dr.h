@@ -33,7 +33,8 @@
  *   DR_EKDN  exact Kalman memory, dense key covariance P (dk x dk), per-channel decay:
  *            P^ = D P D^T + diag(omega);  w = P^ k / (r + k^T P^ k);  P_t = (I - w k^T) P^
  *                                             (KDN notes section 2.2, Eqs. (12)-(17));
- *            token by token (no chunked form; `chunk` is checked but unused)
+ *            token by token (no chunked form; `chunk` is checked but unused); P_0
+ *            must be symmetric (a covariance), which every update preserves
  *
  * q and k are L2-normalised first when the corresponding flag is set
  * (q / max(||q||, 1e-30)); KLA reads out with the normalised query (KLA notes

@@ -4,7 +4,8 @@
 //   S^ = D S,  P^ = D P D^T + diag(omega),  D = diag(alpha)
 //   kappa = P^ k / (r + k^T P^ k)
 //   S = S^ + kappa (v - S^^T k)^T,  P = (I - kappa k^T) P^,  o = S^T q (after the write)
-// With y = P^ k and z = k^T y, k^T P^ = y^T (P^ is symmetric), so the covariance
+// With y = P^ k and z = k^T y, k^T P^ = y^T (P^ is symmetric when P_0 is, as a
+// covariance is, and each update keeps it so), so the covariance
 // update is the symmetric rank-1 downdate P = P^ - y y^T / (r + z), and
 // o = S^^T q + (y^T q / (r + z)) e with e = v - S^^T k.  The covariance follows a
 // Riccati recursion with no chunked form (the notes' comparison table), so each
