@@ -2,30 +2,43 @@
 """Benchmark: chunkwise delta-rule forward tokens/s (+ roofline) and decode-step GB/s.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME]
+                    [--workload NAME] [--no-configs] [--no-decode] [--no-e2e]
+                    [--no-cpu-baseline]
 
-Workload (default ``gdn_kla_bf16``): B=8, H=8, T=2048, dk=dv=128, chunk 64,
-bf16 q/k/v, fp32 gates and state, GDN and KLA on the same seeded inputs.  One
-step is one chunkwise forward over the whole batch for each of the two
-variants (each a prep and a carry launch of libdr); ``value`` counts B*T tokens
-per variant pass.  ``--workload`` times any other workload of
-``recurrent_associative_memory_gb300.workloads`` (PGDN, the per-channel-decay
-variants, the exact Kalman memory, the 64K-token prefill) the same way.  Inputs are resident in HBM before the timed region; L2 is
-flushed (a 256 MiB write) between timed steps and the flush is not timed.
+Headline workload (default ``gdn_kla_bf16``): B=8, H=8, T=2048, dk=dv=128,
+chunk 64, bf16 q/k/v, fp32 gates and state, GDN and KLA on the same seeded
+inputs.  One step is one chunkwise forward over the whole batch for each of the
+two variants (each a prep and a carry launch of libdr); ``value`` counts B*T
+tokens per variant pass.  ``--workload`` makes any other workload of
+``recurrent_associative_memory_gb300.workloads`` the headline.  Inputs are
+resident in HBM before the timed region; L2 is flushed (a 256 MiB write)
+between timed steps and the flush is not timed.
 
 The same JSON line carries:
-  roofline      the forward kernel's algorithmic bytes / CUDA-event time vs the
+  roofline      the forward's algorithmic bytes / CUDA-event time vs the
                 measured HBM peak in MEASURED_PEAKS.json;
-  decode        dr_decode_step at batch 256, H=16, d=128 (KLA): HBM GB/s of the
-                algorithmic bytes (state read + write, q/k/v/o, gates);
-  e2e           the same forward metric with pinned host buffers: every step
-                copies its inputs H2D, runs both forwards and copies both
-                outputs D2H, all inside the timed region; the copies run on
-                their own streams into double-buffered device tensors, so step
-                i+1's inputs arrive and step i-1's outputs leave while step i
-                computes;
+  configs       every workload the method's configurations name, each timed the
+                same way (CUDA events, L2 flushed between steps): the fp32
+                parity case, GDN and KLA, PGDN, Diagonal KDN, the 64K-token KLA
+                prefill and the batch-256 decode step; per entry the time,
+                tokens/s, algorithmic bytes, roofline fraction, the recorded DRAM
+                traffic where an ncu capture exists, and the largest
+                max|gpu - oracle| / max|oracle| over sampled (b, h) rows of the
+                output, the final state and the gain state;
+  decode        dr_decode_step at batch 256, H=16, d=128 (KLA), and per variant
+                (GDN, PGDN, Diagonal KDN, KDA, PKDA, isotropic KDN, exact Kalman):
+                HBM GB/s of the algorithmic bytes (state read + write, q/k/v/o,
+                gates, gain state);
+  e2e           the headline metric with pinned host buffers: every step copies
+                its inputs H2D, runs both forwards and copies both outputs D2H,
+                all inside the timed region; the copies run on their own streams
+                into double-buffered device tensors, so step i+1's inputs arrive
+                and step i-1's outputs leave while step i computes;
   cpu_baseline  the fp64 oracle (numpy, tokenwise) on a bounded sample of the
-                workload (one batch row, all heads), on the host cores;
+                headline workload (batch row 0, all heads, both variants,
+                repeated), on the host cores, in a spawn pool warmed first (the
+                inputs are drawn once per worker, outside the timed calls); also
+                the same oracle on one core;
   clocks        nvidia-smi SM clocks and throttle reasons sampled during the
                 timed region.
 
@@ -53,8 +66,17 @@ sys.path.insert(0, ROOT)
 METRIC = "chunkwise delta-rule fwd tokens/s & % roofline; decode-step HBM GB/s"
 L2_FLUSH_BYTES = 256 << 20
 
+# The workloads of the method's configurations, in their order: the fp32 parity
+# case, GDN vs KLA, PGDN, Diagonal KDN, the long-context prefill, then decode.
+CONFIG_WORKLOADS = [("0", "kla_fp32_small"), ("1", "gdn_kla_bf16"), ("2", "pgdn_bf16"),
+                    ("3", "kdn_bf16"), ("4a", "kla_prefill_bf16"), ("4b", "kla_decode_bf16")]
+# decode-step variants timed besides the headline KLA step, on their own workloads' flags
+DECODE_VARIANTS = {"gdn": "gdn_kla_bf16", "pgdn": "pgdn_bf16", "kdn": "kdn_bf16",
+                   "kda": "kda_bf16", "pkda": "pkda_bf16", "ikdn": "ikdn_bf16",
+                   "ekdn": "ekdn_bf16"}
 
-def parse():
+
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=50)
@@ -65,8 +87,10 @@ def parse():
     p.add_argument("--no-decode", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-configs", action="store_true")
     p.add_argument("--cpu-sample-heads", type=int, default=8)
-    return p.parse_args()
+    p.add_argument("--cpu-sample-reps", type=int, default=10)
+    return p.parse_args(argv)
 
 
 KERNEL_SOURCES = {
@@ -74,6 +98,8 @@ KERNEL_SOURCES = {
     "chunk_tc_ws": ["chunk_tc_ws.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh"],
     "chunk_tc": ["chunk_tc.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh"],
     "chunk_simt": ["chunk_simt.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh", "chain.cuh"],
+    "chunk_simt_split": ["chunk_simt.cu", "chunk_tc_split.cu", "umma.cuh", "tc_common.cuh",
+                         "dr_common.cuh", "chain.cuh"],
     "decode": ["decode.cu", "dr_common.cuh"],
     "kalman": ["kalman.cu", "dr_common.cuh"],
 }
@@ -96,7 +122,7 @@ def measured_traffic(kernel, workload, variant=None):
             rec = json.load(f).get(kernel)
     except Exception:
         return None
-    if not rec or rec.get("source_sha256") != source_hash(kernel):
+    if not rec or kernel not in KERNEL_SOURCES or rec.get("source_sha256") != source_hash(kernel):
         return None
     variants = rec.get("variants", [rec.get("variant")])
     if rec.get("workload") != workload or (variant and variant not in variants):
@@ -115,32 +141,45 @@ def peaks():
 
 # ---------------------------------------------------------------- algorithmic bytes
 
+def gate_bytes(variant, dk):
+    """fp32 gate bytes per (b, t, h): what the variant's write rule reads."""
+    return {"gdn": 8, "kla": 8, "pgdn": 16, "kdn": 8 * dk + 4, "kda": 4 * dk + 4,
+            "pkda": 4 * dk + 12, "ikdn": 4 * dk + 8, "ekdn": 8 * dk + 4}[variant]
+
+
+def aux_elems(variant, dk):
+    """fp32 elements of the gain state per (b, h) (0: none)."""
+    return {"pgdn": dk, "kdn": dk, "pkda": dk, "ikdn": 1, "ekdn": dk * dk}.get(variant, 0)
+
+
+def aux_shape(variant, B, H, dk):
+    n = aux_elems(variant, dk)
+    if n == 0:
+        return None
+    return {1: (B, H), dk: (B, H, dk), dk * dk: (B, H, dk, dk)}[n]
+
+
 def fwd_bytes(wl, variant, with_final=True):
     """Bytes a forward launch must move: q,k,v in, o out, gates, final state (+aux)."""
     el = 2 if wl.dtype == "bf16" else 4
     ht = wl.B * wl.T * wl.H
     per_ht = (2 * wl.dk + 2 * wl.dv) * el          # q, k, v, o
-    gates = {"gdn": 8, "kla": 8, "pgdn": 16, "kdn": 8 * wl.dk + 4,
-             "kda": 4 * wl.dk + 4, "pkda": 4 * wl.dk + 12, "ikdn": 4 * wl.dk + 8,
-             "ekdn": 8 * wl.dk + 4}[variant]
-    total = ht * (per_ht + gates)
+    total = ht * (per_ht + gate_bytes(variant, wl.dk))
     if variant in ("pgdn", "pkda"):
         total += wl.H * 4
     if with_final:
-        total += wl.B * wl.H * wl.dk * wl.dv * 4
-        if variant in ("pgdn", "kdn", "pkda"):
-            total += wl.B * wl.H * wl.dk * 4
-        if variant == "ikdn":   # one variance per head
-            total += wl.B * wl.H * 4
-        if variant == "ekdn":   # the dense covariance
-            total += wl.B * wl.H * wl.dk * wl.dk * 4
+        total += wl.B * wl.H * (wl.dk * wl.dv + aux_elems(variant, wl.dk)) * 4
     return total
 
 
-def decode_bytes(wl):
+def decode_bytes(wl, variant="kla"):
+    """Bytes one decode step must move: the state (and gain state) read and written
+    once, q, k, v in and o out, the step's gates."""
     el = 2 if wl.dtype == "bf16" else 4
     bh = wl.B * wl.H
-    return bh * (2 * wl.dk * wl.dv * 4 + (2 * wl.dk + 2 * wl.dv) * el + 8)
+    per_bh = (2 * (wl.dk * wl.dv + aux_elems(variant, wl.dk)) * 4 + (2 * wl.dk + 2 * wl.dv) * el
+              + gate_bytes(variant, wl.dk))
+    return bh * per_bh + (wl.H * 4 if variant in ("pgdn", "pkda") else 0)
 
 
 def kernels_per_call(path, variant, B, H, has_workspace, nsm):
@@ -214,48 +253,83 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# ---------------------------------------------------------------- oracle (CPU baseline)
+# ---------------------------------------------------------------- oracle (pool workers)
+# These run in spawned worker processes (never in the process that drives the GPU).
 
-def _oracle_heads(args):
-    name, variant, heads = args
-    os.environ.setdefault("OMP_NUM_THREADS", "1")
-    import numpy as np  # noqa: F401
+_INPUT_CACHE = {}
+
+
+def _oracle_call(inp, variant, S0=None, aux0=None):
+    """The fp64 tokenwise oracle on one input dict of numpy arrays."""
+    import numpy as np
     import oracle
-    from recurrent_associative_memory_gb300 import workloads as W
-    wl = W.WORKLOADS[name]
-    inp = W.generate(W.small(name, B=1), variant)      # batch row 0 of the same distributions
-    f = lambda t: None if t is None else t.double().numpy()  # noqa: E731
-    sl = lambda t: None if t is None else f(t[:, :, heads])  # noqa: E731
+    f = lambda t: None if t is None else np.asarray(t, dtype=np.float64)  # noqa: E731
+    return oracle.tokenwise(f(inp["q"]), f(inp["k"]), f(inp["v"]), f(inp["log_alpha"]), variant,
+                            eta=f(inp.get("eta")), eps=inp["eps"], q_l2norm=inp["q_l2norm"],
+                            k_l2norm=inp["k_l2norm"], alphaP=f(inp.get("alphaP")),
+                            betaP=f(inp.get("betaP")), mu=f(inp.get("mu")), x=inp["x"],
+                            log_floor=inp["log_floor"], omega=f(inp.get("omega")),
+                            r=f(inp.get("r")), info_scale=inp["info_scale"], S0=f(S0),
+                            aux0=f(aux0))
+
+
+def _sample_inputs(name, variant, head):
+    """Batch row 0, one head of a workload's inputs (drawn once per worker)."""
+    key = (name, variant)
+    if key not in _INPUT_CACHE:
+        from recurrent_associative_memory_gb300 import workloads as W
+        full = W.generate(W.small(name, B=1), variant)
+        _INPUT_CACHE[key] = full
+    full = _INPUT_CACHE[key]
+    return {k: (t[:, :, head:head + 1].float().numpy() if k != "mu" else
+                t[head:head + 1].float().numpy()) if hasattr(t, "numpy") else t
+            for k, t in full.items()}
+
+
+def _oracle_timed(job):
+    """Worker: run the oracle on one sampled head; return the seconds of the call only."""
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    name, variant, head = job
+    inp = _sample_inputs(name, variant, head)
     t0 = time.perf_counter()
-    oracle.tokenwise(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["log_alpha"]), variant,
-                     eta=sl(inp.get("eta")), eps=wl.eps, q_l2norm=wl.q_l2norm,
-                     k_l2norm=wl.k_l2norm, alphaP=sl(inp.get("alphaP")),
-                     betaP=sl(inp.get("betaP")),
-                     mu=None if inp.get("mu") is None else f(inp["mu"][heads]),
-                     omega=sl(inp.get("omega")), r=sl(inp.get("r")), info_scale=wl.info_scale)
+    _oracle_call(inp, variant)
     return time.perf_counter() - t0
 
 
-def oracle_sample(name, n_heads, pool=None):
-    """Time the oracle on one batch row (n_heads heads) for every variant of the workload.
+def _oracle_parity(job):
+    """Worker: the oracle's output, final state and gain state for one sliced row."""
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    tag, inp, variant, S0, aux0 = job
+    o, S, aux = _oracle_call(inp, variant, S0, aux0)
+    return tag, o, S, aux
 
-    Returns (tokens, seconds, cores): tokens counted like the GPU metric
-    (B*T per variant pass, scaled by the fraction of heads sampled)."""
+
+def oracle_sample(name, n_heads, pool, reps=1):
+    """Time the oracle on batch row 0 (n_heads heads, every variant of the workload).
+
+    The workers draw the inputs on their first call, so the caller warms the pool
+    with one call first; afterwards only the oracle runs inside the timed wall.
+    Returns (tokens, wall seconds, worker seconds, cores): tokens counted like the
+    GPU metric (B*T per variant pass, scaled by the fraction of heads sampled)."""
     from recurrent_associative_memory_gb300 import workloads as W
     wl = W.WORKLOADS[name]
     n_heads = min(n_heads, wl.H)
-    jobs = [(name, v, [h]) for v in wl.variants for h in range(n_heads)]
+    jobs = [(name, v, h) for _ in range(reps) for v in wl.variants for h in range(n_heads)]
     t0 = time.perf_counter()
-    if pool is not None:
-        list(pool.map(_oracle_heads, jobs))
-        cores = min(pool._processes, len(jobs))
-    else:
-        for j in jobs:
-            _oracle_heads(j)
-        cores = 1
+    per_job = list(pool.map(_oracle_timed, jobs, chunksize=1))
     secs = time.perf_counter() - t0
-    tokens = len(wl.variants) * wl.T * n_heads / wl.H
-    return tokens, secs, cores
+    cores = min(pool._processes, len(jobs))
+    tokens = reps * len(wl.variants) * wl.T * n_heads / wl.H
+    return tokens, secs, sum(per_job), cores
+
+
+def oracle_one_core(name, pool):
+    """The oracle on one core: every variant of one head, one job after another in a
+    single worker.  Returns tokens/s in the metric's units."""
+    from recurrent_associative_memory_gb300 import workloads as W
+    wl = W.WORKLOADS[name]
+    secs = sum(pool.apply(_oracle_timed, ((name, v, 0),)) for v in wl.variants)
+    return len(wl.variants) * wl.T / wl.H / secs
 
 
 # ---------------------------------------------------------------- distributed helpers
@@ -304,6 +378,12 @@ def job_tokens_per_s(world, steps, n_variants, B, T, seconds):
 
 # ---------------------------------------------------------------- reference arm
 
+def cpu_sample_text(wl, n_heads, reps):
+    return (f"fp64 tokenwise oracle, batch row 0, {n_heads} of {wl.H} heads, T={wl.T}, "
+            f"variants {list(wl.variants)}, x{reps}, warmed spawn pool (inputs drawn once "
+            f"per worker, outside the timed calls)")
+
+
 def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -319,7 +399,7 @@ def run_reference(args):
             oracle_sample(args.workload, n_heads, pool)
         tok, secs, cores = 0.0, 0.0, 1
         for _ in range(args.steps):
-            t_, s_, cores = oracle_sample(args.workload, n_heads, pool)
+            t_, s_, _, cores = oracle_sample(args.workload, n_heads, pool)
             tok += t_
             secs += s_
     value = tok / secs
@@ -330,18 +410,220 @@ def run_reference(args):
             "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "dk": wl.dk,
                        "dv": wl.dv, "chunk": wl.chunk, "variants": list(wl.variants)},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": f"fp64 tokenwise oracle, batch row 0, {n_heads} of {wl.H} "
-                                       f"heads, T={wl.T}, variants {list(wl.variants)}, per step"},
+                             "sample": cpu_sample_text(wl, n_heads, 1) + ", per step"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
 
 
+# ---------------------------------------------------------------- our arm: helpers
+
+def rel_err(x, ref):
+    import numpy as np
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    d = float(np.abs(ref).max())
+    return float(np.abs(x - ref).max() / d) if d > 0 else float(np.abs(x).max())
+
+
+def sampled_pairs(B, H, n):
+    out = []
+    for p in [(0, 0), (B - 1, H - 1), (B // 2, H // 2)]:
+        if p not in out:
+            out.append(p)
+    return out[:n]
+
+
+def slice_row(inp, b, h):
+    """One (b, h) row of a CPU input dict as [1, T, 1, d] numpy arrays (+ flags)."""
+    out = {}
+    for k, t in inp.items():
+        if not hasattr(t, "numpy"):
+            out[k] = t
+        elif k == "mu":
+            out[k] = t[h:h + 1].float().numpy()
+        else:
+            out[k] = t[b:b + 1, :, h:h + 1].float().numpy()
+    return out
+
+
+class Forward:
+    """One workload's device inputs, outputs and workspace, and its timed forward."""
+
+    def __init__(self, torch, dr, runner, W, wl, host=None):
+        self.torch, self.dr, self.runner, self.wl = torch, dr, runner, wl
+        self.variants = list(wl.variants)
+        self.host = host or {v: W.generate(wl, v) for v in self.variants}
+        self.dev = {v: runner.to_device(self.host[v]) for v in self.variants}
+        dt = self.dev[self.variants[0]]["q"].dtype
+        self.outs = {v: torch.empty(wl.B, wl.T, wl.H, wl.dv, dtype=dt, device="cuda")
+                     for v in self.variants}
+        self.finals = {v: torch.empty(wl.B, wl.H, wl.dk, wl.dv, device="cuda")
+                       for v in self.variants}
+        self.auxf = {}
+        for v in self.variants:
+            shp = aux_shape(v, wl.B, wl.H, wl.dk)
+            self.auxf[v] = None if shp is None else torch.empty(*shp, device="cuda")
+        wss = [runner.workspace_for(self.dev[v]) for v in self.variants]
+        self.ws = max((w for w in wss if w is not None), key=lambda w: w.numel(), default=None)
+        dtype_id = dr.DR_BF16 if wl.dtype == "bf16" else dr.DR_FP32
+        self.paths = {v: dr.dr_chunk_fwd_path(dr.VARIANT_IDS[v], dtype_id, wl.dk, wl.dv,
+                                              wl.chunk) for v in self.variants}
+
+    def call(self, v, stream):
+        self.runner.chunk_fwd(self.dev[v], out=self.outs[v], final_state=self.finals[v],
+                              aux_final=self.auxf[v], stream=stream, workspace=self.ws)
+
+    def launches_per_step(self, nsm):
+        wl = self.wl
+        return sum(kernels_per_call(self.paths[v], v, wl.B, wl.H, self.ws is not None, nsm)
+                   for v in self.variants)
+
+    def time(self, steps, warmup, stream, flush, on_step_start=None):
+        """Per variant, the CUDA-event time of each of ``steps`` forwards (L2 flushed
+        before every step, outside the events); returns ({variant: [ms]}, [step ms])."""
+        torch = self.torch
+        for _ in range(max(3, warmup)):
+            for v in self.variants:
+                self.call(v, stream)
+        torch.cuda.synchronize()
+        self.dr.check(self.dr.dr_get_device_status(), f"{self.wl.name} warm-up")
+        E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+        ev = [(E(), E()) for _ in range(steps)]
+        vev = {v: [(E(), E()) for _ in range(steps)] for v in self.variants}
+        if on_step_start:
+            on_step_start()
+        torch.cuda.synchronize()
+        for i in range(steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            for v in self.variants:
+                vev[v][i][0].record(stream)
+                self.call(v, stream)
+                vev[v][i][1].record(stream)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        self.dr.check(self.dr.dr_get_device_status(), f"{self.wl.name} timed")
+        return ({v: [s.elapsed_time(e) for s, e in vev[v]] for v in self.variants},
+                [s.elapsed_time(e) for s, e in ev])
+
+    def parity_jobs(self, n_pairs):
+        """Oracle jobs for sampled (b, h) rows of every variant (CPU inputs)."""
+        jobs = []
+        for v in self.variants:
+            for b, h in sampled_pairs(self.wl.B, self.wl.H, n_pairs):
+                jobs.append(((self.wl.name, v, b, h), slice_row(self.host[v], b, h), v, None,
+                             None))
+        return jobs
+
+    def parity(self, results):
+        """max rel. error of the GPU's last outputs against the oracle rows."""
+        worst = {"out": 0.0, "state": 0.0, "aux": 0.0}
+        for (name, v, b, h), o, S, aux in results:
+            if name != self.wl.name:
+                continue
+            worst["out"] = max(worst["out"], rel_err(
+                self.outs[v][b, :, h].double().cpu().numpy(), o[0, :, 0]))
+            worst["state"] = max(worst["state"], rel_err(
+                self.finals[v][b, h].double().cpu().numpy(), S[0, 0]))
+            if aux is not None and self.auxf[v] is not None:
+                worst["aux"] = max(worst["aux"], rel_err(
+                    self.auxf[v][b, h].double().cpu().numpy(), aux[0, 0]))
+        return worst
+
+
+def forward_entry(fw, var_ms, pk, launches):
+    """Per-workload record: mean time per variant, tokens/s, bytes, roofline fraction."""
+    wl = fw.wl
+    per = {}
+    for v in fw.variants:
+        ms = statistics.mean(var_ms[v])
+        byt = fwd_bytes(wl, v)
+        path = fw.paths[v]
+        kname = "chunk_" + path
+        per[v] = {"ms": ms, "ms_median": statistics.median(var_ms[v]),
+                  "tokens_per_s": wl.B * wl.T / (ms / 1e3), "algorithmic_bytes": byt,
+                  "gbs": byt / (ms / 1e3) / 1e9, "frac": byt / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                  "path": path, "traffic": measured_traffic(kname, wl.name, v)}
+    return {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "d": wl.dk, "chunk": wl.chunk,
+            "dtype": wl.dtype, "variants": per, "launches_per_step": launches}
+
+
+def decode_setup(torch, runner, W, wl, variant, n_pool=8):
+    """Device inputs for n_pool decode steps, a state and the gain state."""
+    steps = [W.generate_decode_step(wl, s, variant) for s in range(n_pool)]
+    g = torch.Generator().manual_seed(wl.seed + 77)
+    S0 = 0.05 * torch.randn(wl.B, wl.H, wl.dk, wl.dv, generator=g)
+    shp = aux_shape(variant, wl.B, wl.H, wl.dk)
+    aux0 = None
+    if variant in ("pgdn", "pkda"):
+        aux0 = torch.rand(*shp, generator=g)
+    elif variant in ("kdn", "ikdn"):
+        aux0 = 0.5 + torch.rand(*shp, generator=g)
+    elif variant == "ekdn":
+        aux0 = torch.eye(wl.dk).expand(*shp).contiguous()
+    return steps, S0, aux0
+
+
+def time_decode(torch, dr, runner, W, wl, variant, n_steps, stream, pk):
+    steps, S0, aux0 = decode_setup(torch, runner, W, wl, variant)
+    dsteps = [runner.to_device(s) for s in steps]
+    S = S0.cuda()
+    aux = None if aux0 is None else aux0.cuda()
+    dt = dsteps[0]["q"].dtype
+    dout = torch.empty(wl.B, wl.H, wl.dv, dtype=dt, device="cuda")
+    for i in range(5):
+        runner.decode_step(dsteps[i % len(dsteps)], S, aux, out=dout, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n_steps):
+        runner.decode_step(dsteps[i % len(dsteps)], S, aux, out=dout, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dr.check(dr.dr_get_device_status(), f"decode {variant}")
+    ms = e0.elapsed_time(e1) / n_steps
+    db = decode_bytes(wl, variant)
+    gbs = db / (ms / 1e3) / 1e9
+    kernel = "kalman" if variant == "ekdn" else "decode"
+    return {"workload": wl.name, "variant": variant, "B": wl.B, "H": wl.H, "d": wl.dk,
+            "ms_per_step": ms, "gbs": gbs, "frac": gbs / pk["hbm_gbs"],
+            "algorithmic_bytes_per_step": db, "steps": n_steps,
+            "traffic": measured_traffic(kernel, wl.name), "tokens_per_s": wl.B / (ms / 1e3),
+            "launches": n_steps, "kernel": kernel}
+
+
+def decode_parity(torch, runner, W, wl, variant, n_steps, pairs):
+    """Decode n_steps from a seeded state on the full batch; returns the GPU's
+    outputs and final state for the sampled rows, and the oracle jobs for them."""
+    steps, S0, aux0 = decode_setup(torch, runner, W, wl, variant, n_pool=n_steps)
+    S = S0.cuda()
+    aux = None if aux0 is None else aux0.cuda()
+    outs = [runner.decode_step(runner.to_device(s), S, aux).clone() for s in steps]
+    torch.cuda.synchronize()
+    gpu = {(b, h): (torch.stack([o[b, h] for o in outs]).double().cpu().numpy(),
+                    S[b, h].double().cpu().numpy()) for b, h in pairs}
+    jobs = []
+    for b, h in pairs:
+        seq = {}
+        for k, t in steps[0].items():
+            if not hasattr(t, "numpy"):
+                seq[k] = t
+            elif k == "mu":
+                seq[k] = t[h:h + 1].float().numpy()
+            else:
+                seq[k] = torch.stack([s[k][b:b + 1, h:h + 1] for s in steps], 1).float().numpy()
+        s0 = S0[b:b + 1, h:h + 1].numpy()
+        a0 = None if aux0 is None else aux0[b:b + 1, h:h + 1].numpy()
+        jobs.append((("decode", variant, b, h), seq, variant, s0, a0))
+    return gpu, jobs
+
+
 # ---------------------------------------------------------------- our arm
 
-def main():
-    args = parse()
+def main(argv=None):
+    args = parse(argv)
     if args.impl == "reference":
         return run_reference(args)
 
@@ -349,7 +631,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     pool = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    want_oracle = rank == 0 and world == 1 and not (args.no_cpu_baseline and args.no_configs)
+    if want_oracle:
         pool = mp.get_context("spawn").Pool(min(os.cpu_count() or 1, 16))
 
     import torch
@@ -359,126 +642,104 @@ def main():
     world, rank, local = dist_setup(args)
     torch.cuda.set_device(local)
     pk = peaks()
-    wl = W.WORKLOADS[args.workload]
-    variants = list(wl.variants)
-
-    # inputs: shared q/k/v, per-variant gates, generated on the CPU then copied
-    host = {v: W.generate(wl, v) for v in variants}
-    dev = {v: runner.to_device(host[v]) for v in variants}
-    outs = {v: torch.empty(wl.B, wl.T, wl.H, wl.dv, dtype=dev[v]["q"].dtype, device="cuda")
-            for v in variants}
-    finals = {v: torch.empty(wl.B, wl.H, wl.dk, wl.dv, dtype=torch.float32, device="cuda")
-              for v in variants}
-    auxf = {v: (torch.empty(wl.B, wl.H, wl.dk, device="cuda") if v in ("pgdn", "kdn") else None)
-            for v in variants}
-    # one caller-owned workspace, reused by the variants' calls in stream order
-    wss = [runner.workspace_for(dev[v]) for v in variants]
-    ws = max((w for w in wss if w is not None), key=lambda w: w.numel(), default=None)
+    nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
+    parity_async = []   # pending oracle jobs (AsyncResult), collected at the end
 
-    def step():
-        for v in variants:
-            runner.chunk_fwd(dev[v], out=outs[v], final_state=finals[v], aux_final=auxf[v],
-                             stream=stream, workspace=ws)
+    def submit(jobs):
+        if pool is not None and not args.no_configs:
+            parity_async.append(pool.map_async(_oracle_parity, jobs, chunksize=1))
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    dr.check(dr.dr_get_device_status(), "warmup")
-
-    # timed region: per-step events around the forwards; L2 flush between steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    vev = {v: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)] for v in variants}
+    # ---------------- headline workload: the timed region
+    wl = W.WORKLOADS[args.workload]
+    head = Forward(torch, dr, runner, W, wl)
+    variants = head.variants
+    submit(head.parity_jobs(2))
     clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.25)
-    barrier(world)
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.fill_(float(i))
-        ev[i][0].record(stream)
-        for v in variants:
-            vev[v][i][0].record(stream)
-            runner.chunk_fwd(dev[v], out=outs[v], final_state=finals[v], aux_final=auxf[v],
-                             stream=stream, workspace=ws)
-            vev[v][i][1].record(stream)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
+
+    def start_clocks():
+        clocks.start()
+        time.sleep(0.25)
+        barrier(world)
+
+    var_ms, step_ms = head.time(args.steps, args.warmup, stream, flush, start_clocks)
     barrier(world)
     clk = clocks.stop()
-    step_ms = [s.elapsed_time(e) for s, e in ev]
     total_s = max_over_ranks(sum(step_ms) / 1e3, world)
-    dr.check(dr.dr_get_device_status(), "timed region")
-    nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    launches = args.steps * sum(
-        kernels_per_call(dr.dr_chunk_fwd_path(dr.VARIANT_IDS[v], 1 if wl.dtype == "bf16" else 0,
-                                              wl.dk, wl.dv, wl.chunk),
-                         v, wl.B, wl.H, ws is not None, nsm)
-        for v in variants)
+    launches = args.steps * head.launches_per_step(nsm)
     value = job_tokens_per_s(world, args.steps, len(variants), wl.B, wl.T, total_s)
-
-    var_stats = {}
-    for v in variants:
-        ms = statistics.mean(s.elapsed_time(e) for s, e in vev[v])
-        byt = fwd_bytes(wl, v)
-        var_stats[v] = {"ms": ms, "tokens_per_s": wl.B * wl.T / (ms / 1e3),
-                        "gbs": byt / (ms / 1e3) / 1e9,
-                        "frac_hbm": byt / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
-                        "path": dr.dr_chunk_fwd_path(dr.VARIANT_IDS[v], 1 if wl.dtype == "bf16"
-                                                     else 0, wl.dk, wl.dv, wl.chunk)}
-    dom = max(variants, key=lambda v: var_stats[v]["ms"])
-    byt = fwd_bytes(wl, dom)
-    ach = byt / (var_stats[dom]["ms"] / 1e3) / 1e9
-    kname = "chunk_" + var_stats[dom]["path"]
+    entry = forward_entry(head, var_ms, pk, head.launches_per_step(nsm))
+    dom = max(variants, key=lambda v: entry["variants"][v]["ms"])
+    dv_ = entry["variants"][dom]
+    kname = "chunk_" + dv_["path"]
     kdesc = f"{kname} ({dom})"
-    if var_stats[dom]["path"] == "tc_split":
+    if dv_["path"] == "tc_split":
         kdesc = f"{kname}: chunk_prep + chunk_carry of one dr_chunk_fwd call ({dom})"
-    roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
-            "frac": ach / pk["hbm_gbs"], "traffic": measured_traffic(kname, wl.name, dom),
-            "kernel": kdesc,
-            "algorithmic_bytes_per_launch": byt, "peak_source": pk["src"]}
-
+    roof = {"bound": "hbm", "achieved": dv_["gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": dv_["frac"], "traffic": dv_["traffic"], "kernel": kdesc,
+            "algorithmic_bytes_per_launch": dv_["algorithmic_bytes"],
+            "peak_source": pk["src"]}
     result = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
               "steps": args.steps, "warmup": max(3, args.warmup),
               "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
-              "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+              "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
               "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "dk": wl.dk,
                          "dv": wl.dv, "chunk": wl.chunk, "variants": variants,
                          "state": "fp32", "l2": "flushed between timed steps (256 MiB write)",
                          "parallelism": f"replicas x{world}"},
-              "roofline": roof, "variants": var_stats, "gpu_launches": launches, "clocks": clk}
+              "roofline": roof, "variants": entry["variants"], "gpu_launches": launches,
+              "clocks": clk}
+    configs = {}
 
-    # ---- decode step (batch 256, H 16): HBM GB/s
+    # ---------------- every configuration's workload, timed the same way
+    if not args.no_configs:
+        for tag, name in CONFIG_WORKLOADS:
+            if name == "kla_decode_bf16":
+                continue
+            if name == wl.name:
+                configs[tag] = dict(entry, parity=None)
+                configs[tag]["_fw"] = head
+                continue
+            fw = Forward(torch, dr, runner, W, W.WORKLOADS[name])
+            submit(fw.parity_jobs(1 if fw.wl.T > 16384 else 2))
+            vms, _ = fw.time(min(args.steps, 20), 3, stream, flush)
+            configs[tag] = forward_entry(fw, vms, pk, fw.launches_per_step(nsm))
+            configs[tag]["_fw"] = fw
+            # keep only what the parity check reads; free the rest of the device memory
+            fw.dev = fw.ws = None
+            torch.cuda.empty_cache()
+
+    # ---------------- decode step (batch 256, H 16): HBM GB/s, every variant
+    dec_parity = None
     if not args.no_decode:
         dwl = W.WORKLOADS["kla_decode_bf16"]
-        pool_steps = [runner.to_device(W.generate_decode_step(dwl, s)) for s in range(8)]
-        S = torch.zeros(dwl.B, dwl.H, dwl.dk, dwl.dv, device="cuda")
-        S.normal_(0, 0.05)
-        dout = torch.empty(dwl.B, dwl.H, dwl.dv, dtype=torch.bfloat16, device="cuda")
-        for i in range(5):
-            runner.decode_step(pool_steps[i % 8], S, out=dout, stream=stream)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(args.decode_steps):
-            runner.decode_step(pool_steps[i % 8], S, out=dout, stream=stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        dr.check(dr.dr_get_device_status(), "decode")
-        ms = e0.elapsed_time(e1) / args.decode_steps
-        db = decode_bytes(dwl)
-        gbs = db / (ms / 1e3) / 1e9
-        result["decode"] = {"workload": dwl.name, "B": dwl.B, "H": dwl.H, "d": dwl.dk,
-                            "ms_per_step": ms, "gbs": gbs, "frac": gbs / pk["hbm_gbs"],
-                            "algorithmic_bytes_per_step": db, "steps": args.decode_steps,
-                            "traffic": measured_traffic("decode", dwl.name),
-                            "tokens_per_s": dwl.B / (ms / 1e3), "launches": args.decode_steps}
+        result["decode"] = time_decode(torch, dr, runner, W, dwl, "kla", args.decode_steps,
+                                       stream, pk)
+        per_var = {}
+        for v, base in DECODE_VARIANTS.items():
+            vwl = W.small(base, B=dwl.B, T=1, H=dwl.H, seed=dwl.seed)
+            per_var[v] = time_decode(torch, dr, runner, W, vwl, v,
+                                     max(10, args.decode_steps // 4), stream, pk)
+        result["decode"]["variants"] = per_var
+        if not args.no_configs:
+            pairs = [(0, 0), (dwl.B // 2, dwl.H // 2), (dwl.B - 1, dwl.H - 1)]
+            gpu, jobs = decode_parity(torch, runner, W, dwl, "kla", 16, pairs)
+            submit(jobs)
+            dec_parity = gpu
+            configs["4b"] = {"workload": dwl.name, "B": dwl.B, "H": dwl.H, "d": dwl.dk,
+                             "ms_per_step": result["decode"]["ms_per_step"],
+                             "tokens_per_s": result["decode"]["tokens_per_s"],
+                             "algorithmic_bytes": result["decode"]["algorithmic_bytes_per_step"],
+                             "gbs": result["decode"]["gbs"], "frac": result["decode"]["frac"],
+                             "traffic": result["decode"]["traffic"],
+                             "parity_sample": f"{len(pairs)} (b, h) rows x 16 steps from a "
+                                              "seeded state"}
 
-    # ---- end to end through the public API with pinned host buffers
+    # ---------------- end to end through the public API with pinned host buffers
     if not args.no_e2e:
+        dev, outs, finals, auxf, ws = head.dev, head.outs, head.finals, head.auxf, head.ws
+        host = head.host
         keys = [k for k in dev[variants[0]] if torch.is_tensor(dev[variants[0]][k])]
         hpin = {v: {k: host[v][k].pin_memory() for k in keys} for v in variants}
         hout = {v: torch.empty_like(outs[v], device="cpu").pin_memory() for v in variants}
@@ -535,18 +796,52 @@ def main():
             e2e_step(i)
         e1.record(d2h_s)                                # after the last step's D2H
         torch.cuda.synchronize()
+        dr.check(dr.dr_get_device_status(), "e2e")
         sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
         result["e2e"] = {"value": world * n * len(variants) * wl.B * wl.T / sec, "unit": "tokens/s",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+        # the last e2e step wrote set (n - 1) & 1; point the parity check at it
+        head.outs = osets[(n - 1) & 1]
 
-    if pool is not None:
+    # ---------------- parity of every timed configuration against the oracle
+    if parity_async:
+        results = [r for a in parity_async for r in a.get()]
+        for tag, c in configs.items():
+            fw = c.pop("_fw", None)
+            if fw is not None:
+                c["parity"] = fw.parity(results)
+                c["parity_sample"] = (f"{len(sampled_pairs(fw.wl.B, fw.wl.H, 2))} (b, h) rows "
+                                      "per variant" if fw.wl.T <= 16384 else
+                                      "1 (b, h) row")
+        if dec_parity is not None:
+            worst = {"out": 0.0, "state": 0.0}
+            for (name, v, b, h), o, S, _ in results:
+                if name == "decode":
+                    go, gS = dec_parity[(b, h)]
+                    worst["out"] = max(worst["out"], rel_err(go, o[0, :, 0]))
+                    worst["state"] = max(worst["state"], rel_err(gS, S[0, 0]))
+            configs["4b"]["parity"] = worst
+    for c in configs.values():
+        c.pop("_fw", None)
+    if configs:
+        result["configs"] = configs
+        result["parity_bar"] = {"bf16": 5e-3, "fp32": 1e-4,
+                                "measure": "max|gpu - oracle| / max|oracle|"}
+
+    # ---------------- the oracle on the host cores (warm pool)
+    if pool is not None and not args.no_cpu_baseline:
         n_heads = min(args.cpu_sample_heads, wl.H)
-        tok, secs, cores = oracle_sample(args.workload, n_heads, pool)
-        pool.close()
+        oracle_sample(args.workload, n_heads, pool)          # warm: inputs drawn per worker
+        tok, secs, cpu_s, cores = oracle_sample(args.workload, n_heads, pool,
+                                                reps=args.cpu_sample_reps)
+        one = oracle_one_core(args.workload, pool)
         result["cpu_baseline"] = {"value": tok / secs, "unit": "tokens/s", "cores": cores,
-                                  "kind": "oracle",
-                                  "sample": f"fp64 tokenwise oracle on batch row 0, {n_heads} of "
-                                            f"{wl.H} heads, T={wl.T}, variants {variants}"}
+                                  "kind": "oracle", "cpu_seconds": cpu_s, "wall_seconds": secs,
+                                  "one_core_value": one,
+                                  "sample": cpu_sample_text(wl, n_heads, args.cpu_sample_reps)}
+    if pool is not None:
+        pool.close()
+        pool.join()
     if rank == 0:
         print(json.dumps(result))
     if world > 1:

@@ -203,8 +203,12 @@ size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H,
  * passes every input and output; gp->workspace is ignored.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *   - The first call on a device, with that device current, looks up the
- *     array's device address (cudaGetSymbolAddress) and caches it; make that
- *     first call before any stream capture.
+ *     array's device address (cudaGetSymbolAddress) and caches it with the
+ *     current context; make that first call before any stream capture.  A new
+ *     context on the device (after cudaDeviceReset) gets a new array, whose
+ *     address the next call looks up again (again outside any capture).
+ *   - Argument checks come first, in dr_chunk_fwd's order (DR_ERR_NULL,
+ *     DR_ERR_DTYPE, DR_ERR_SHAPE), then the path and size checks below.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind (nothing in it has to start at zero).  Calls that overlap on the
  *     GPU -- two streams, or two host threads -- race on it: serialise them.
@@ -223,6 +227,24 @@ int dr_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const floa
 /* Synchronises `stream`, returns and clears the sticky device status
  * (DR_OK, DR_ERR_NONFINITE or DR_ERR_TIMEOUT), or DR_ERR_CUDA. */
 int dr_get_device_status(dr_stream_t stream);
+
+/*
+ * TEST ONLY -- failure injection on the host side of a device wait.  The
+ * chained prep of the per-channel-decay two-phase path (Diagonal KDN, PKDA,
+ * isotropic KDN with 3 B H >= SM count) hands each row's gain state from a
+ * chunk's task to the next one through a flag per record (record index
+ * b H ceil(T/64) + h ceil(T/64) + chunk), and a task waits for its flag at most
+ * a bounded time.  This call makes the task that would raise flag
+ * `withhold_flag` skip it (-1: none; chunk 0 of a row has no flag) and sets the
+ * wait's limit to `wait_ns` (> 0; the default is 2e9).  The waiting task then
+ * gives up: dr_get_device_status() returns DR_ERR_TIMEOUT, every other waiter
+ * is released, the kernels run to their ends (the affected outputs are
+ * garbage) and the context stays usable.  Restore with (-1, 2000000000).
+ * Synchronous with respect to the host; it affects every later launch on the
+ * current device.  The pages have no counterpart: this exists only to test the
+ * give-up path.  Returns DR_OK, DR_ERR_ARG or DR_ERR_CUDA.
+ */
+int dr_set_chain_fault_for_testing(long long withhold_flag, unsigned long long wait_ns);
 
 /* Static, NUL-terminated description of a dr_status value. */
 const char *dr_status_string(int status);

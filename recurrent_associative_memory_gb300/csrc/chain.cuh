@@ -35,6 +35,12 @@ __device__ __forceinline__ bool chain_wait(const uint32_t* flag, uint32_t* abort
     __nanosleep(64);
   }
 }
+// Test hooks of the hand-over (set by dr_set_chain_fault_for_testing): the limit of
+// a task's wait for its flag, and the index of one flag that is never raised (-1:
+// none), so a test can make a wait run out on a flag that nothing sets.
+extern __device__ unsigned long long g_chain_wait_ns;
+extern __device__ long long g_chain_withhold;
+
 // bytes after the records: one flag per record, the ticket counter, the abort word
 __host__ __device__ inline size_t chain_bytes(long nrec) { return ((size_t)(nrec + 2) * 4 + 255) / 256 * 256; }
 

@@ -160,7 +160,10 @@ constexpr uint32_t rbT = 0, rbWp = 16384, rbP = 49152, rbVec = 65536, rbQ = 6656
 // record and hands p at its end to the next chunk's record (then raises that
 // chunk's flag); the last chunk of a row writes p to aux.  A task only waits on
 // tickets claimed earlier by running CTAs, so the chain needs no co-residency.
-constexpr uint64_t kChainWaitNs = 2000000000ull;   // 2 s: a lost flag, not a slow one
+// The wait for a flag gives up after g_chain_wait_ns (2 s by default: a lost flag,
+// not a slow one), sets DR_ERR_TIMEOUT and the abort word, which releases every
+// other waiter at once; the tasks then run to their ends on whatever the record
+// holds, so the kernel always finishes.
 
 template <int DK, typename Tin, bool PREP>
 __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint8_t* __restrict__ ws,
@@ -421,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       for (int r = 0; r < CM * NV / kThreads; ++r) sV[tid + r * kThreads] = vv[r];
     }
     if (perchan) cp_async_wait_all();
-    if (chained && ci > 0 && tid == 0 && !chain_wait(chain + ri, chain + kIters + 1, kChainWaitNs))
+    if (chained && ci > 0 && tid == 0 && !chain_wait(chain + ri, chain + kIters + 1, g_chain_wait_ns))
       set_status(DR_ERR_TIMEOUT);
     __syncthreads();
     if (chained && (ikdn ? tid == DK : tid < DK))   // KDN p / PKDA A (thread c) or IKDN b
@@ -676,7 +679,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         }
       }
       if (kdn) __syncthreads();
-      if (chained && tid == 0 && ci + 1 < NCk) st_release_gpu(chain + ri + 1, 1u);
+      if (chained && tid == 0 && ci + 1 < NCk && ri + 1 != g_chain_withhold)
+        st_release_gpu(chain + ri + 1, 1u);
       if (kdn) {   // z_i = sum_c p^_ic k_ic^2: warp w takes rows 8w .. 8w + 7 (keys read as two
           // 16-byte pieces per channel), all partial sums first, then the eight
           // reductions side by side

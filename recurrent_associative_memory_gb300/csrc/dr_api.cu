@@ -9,6 +9,8 @@
 namespace dr {
 
 __device__ int g_status = 0;
+__device__ unsigned long long g_chain_wait_ns = 2000000000ull;
+__device__ long long g_chain_withhold = -1;
 
 cudaError_t launch_decode(const FwdArgs& a, int dtype, cudaStream_t st);
 cudaError_t launch_chunk_simt(const FwdArgs& a, int dtype, cudaStream_t st);
@@ -214,6 +216,14 @@ int dr_decode_step(const void* q, const void* k, const void* v, const float* log
     err = launch_decode(a, gp->dtype, reinterpret_cast<cudaStream_t>(stream));
   }
   return err == cudaSuccess ? DR_OK : DR_ERR_CUDA;
+}
+
+int dr_set_chain_fault_for_testing(long long withhold_flag, unsigned long long wait_ns) {
+  if (withhold_flag < -1 || wait_ns == 0) return DR_ERR_ARG;
+  if (cudaMemcpyToSymbol(g_chain_withhold, &withhold_flag, sizeof(withhold_flag)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_chain_wait_ns, &wait_ns, sizeof(wait_ns)) != cudaSuccess)
+    return DR_ERR_CUDA;
+  return DR_OK;
 }
 
 int dr_get_device_status(dr_stream_t stream) {

@@ -70,6 +70,8 @@ _lib.dr_chunk_fwd_path.argtypes = [c_int] * 5
 _lib.dr_chunk_fwd_path.restype = c_char_p
 _lib.dr_chunk_fwd_noalloc.argtypes = _lib.dr_chunk_fwd.argtypes
 _lib.dr_chunk_fwd_noalloc.restype = c_int
+_lib.dr_set_chain_fault_for_testing.argtypes = [ctypes.c_longlong, ctypes.c_ulonglong]
+_lib.dr_set_chain_fault_for_testing.restype = c_int
 
 # size of the library-owned scratch behind dr_chunk_fwd_noalloc (include/dr.h)
 DR_NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -165,3 +167,8 @@ def dr_chunk_fwd_noalloc(q, k, v, log_alpha, params: DrParams, variant: int, eps
                                      ctypes.byref(params), int(variant), float(eps),
                                      _ptr(init_state), _ptr(out), _ptr(final_state), B, T, H, dk,
                                      dv, chunk, _stream(stream))
+
+
+def dr_set_chain_fault_for_testing(withhold_flag: int, wait_ns: int) -> int:
+    """Test only: withhold one hand-over flag of the chained prep and set the wait limit."""
+    return _lib.dr_set_chain_fault_for_testing(int(withhold_flag), int(wait_ns))

@@ -83,3 +83,67 @@ def test_kernels_per_call_counts_every_path():
     assert k("simt_split", "ikdn", 4, 16, True, 152) == 2
     assert k("kalman", "ekdn", 4, 16, False, 152) == 1
     assert k("simt", "kla", 1, 2, False, 152) == 1
+
+
+@pytest.mark.parametrize("variant,gates,aux", [("gdn", 8, 0), ("pgdn", 16, 128), ("kdn", 1028, 128),
+                                               ("kda", 516, 0), ("pkda", 524, 128), ("ikdn", 520, 1),
+                                               ("ekdn", 1028, 128 * 128)])
+def test_decode_step_bytes_per_variant(variant, gates, aux):
+    """Each variant's decode step moves its state and gain state twice (read, write),
+    q, k, v, o once and its own gates; PGDN / PKDA also read the per-head mu."""
+    wl = W.small("kla_decode_bf16", B=4, H=3)
+    per_bh = 2 * (128 * 128 + aux) * 4 + 4 * 128 * 2 + gates
+    mu = 3 * 4 if variant in ("pgdn", "pkda") else 0
+    assert bench.decode_bytes(wl, variant) == 4 * 3 * per_bh + mu
+    shp = bench.aux_shape(variant, 4, 3, 128)
+    assert (shp is None) == (aux == 0)
+    if shp is not None:
+        n = 1
+        for s in shp[2:]:
+            n *= s
+        assert n == aux
+
+
+def test_every_configuration_has_a_workload():
+    tags = [t for t, _ in bench.CONFIG_WORKLOADS]
+    assert tags == ["0", "1", "2", "3", "4a", "4b"]
+    for _, name in bench.CONFIG_WORKLOADS:
+        assert name in W.WORKLOADS
+    for v, base in bench.DECODE_VARIANTS.items():
+        assert v in W.WORKLOADS[base].variants
+
+
+def test_parity_row_slice_matches_the_oracle_on_the_full_input():
+    """The (b, h) row the bench sends to a pool worker gives the oracle's result for
+    that row of the full input (heads are independent)."""
+    import numpy as np
+    import oracle
+    wl = W.small("pgdn_bf16", B=2, T=40, H=3, seed=5)
+    inp = W.generate(wl, "pgdn")
+    row = bench.slice_row(inp, 1, 2)
+    tag, o, S, aux = bench._oracle_parity((("x", "pgdn", 1, 2), row, "pgdn", None, None))
+    f = lambda t: t.double().numpy()  # noqa: E731
+    o_all, S_all, A_all = oracle.tokenwise(f(inp["q"]), f(inp["k"]), f(inp["v"]),
+                                           f(inp["log_alpha"]), "pgdn", eta=f(inp["eta"]),
+                                           eps=wl.eps, q_l2norm=wl.q_l2norm,
+                                           k_l2norm=wl.k_l2norm, alphaP=f(inp["alphaP"]),
+                                           betaP=f(inp["betaP"]), mu=f(inp["mu"]))
+    assert np.allclose(o[0, :, 0], o_all[1, :, 2], rtol=0, atol=1e-12)
+    assert np.allclose(S[0, 0], S_all[1, 2], rtol=0, atol=1e-12)
+    assert np.allclose(aux[0, 0], A_all[1, 2], rtol=0, atol=1e-12)
+
+
+def test_cpu_baseline_times_only_the_oracle_in_a_warm_pool():
+    """oracle_sample counts B*T tokens per variant pass scaled by the heads sampled,
+    and after a warm-up call the wall time is close to the workers' own oracle time
+    (inputs are drawn once per worker, outside the timed calls)."""
+    import multiprocessing as mp
+    with mp.get_context("spawn").Pool(2) as pool:
+        bench.oracle_sample("gdn_kla_bf16", 2, pool)
+        tok, wall, cpu, cores = bench.oracle_sample("gdn_kla_bf16", 2, pool, reps=2)
+        one = bench.oracle_one_core("gdn_kla_bf16", pool)
+    wl = W.WORKLOADS["gdn_kla_bf16"]
+    assert tok == 2 * 2 * wl.T * 2 / wl.H
+    assert cores == 2
+    assert cpu <= 2.0 * wall * cores and wall <= 2.0 * cpu
+    assert one > 0

@@ -8,15 +8,14 @@ per-chunk records in a fixed library-owned device array instead.
 
 The GPU test calls it through the C ABI twice in a row, on different inputs, so
 the second call runs over the first call's leftover records, and compares each
-result with dr_chunk_fwd on a caller-allocated workspace within the parity
-tolerance.  The host test covers the refusals that happen before any CUDA call.
+result with dr_chunk_fwd on a caller-allocated workspace: the same kernels on the
+same inputs, so the same bits.  The host test covers the refusals that happen before any CUDA call.
 This file is collected last on purpose.
 """
 
 import pytest
 import torch
 
-from parity_util import TOL, np64, rel_err
 from recurrent_associative_memory_gb300 import workloads as W
 
 A = 1 << 20   # a 16-byte aligned address that is never dereferenced (refused calls only)
@@ -39,6 +38,20 @@ def test_noalloc_refusals_on_host():
     assert call(dtype=dr.DR_FP32) == dr.DR_ERR_UNSUPPORTED
     assert call(variant=dr.DR_KDN, dk=64, dv=64) == dr.DR_ERR_UNSUPPORTED
     assert call(T=0) == dr.DR_ERR_SHAPE
+    # the per-channel-decay records (135,168 bytes) and the chain flags after them
+    p = dr.make_params(dtype=dr.DR_FP32, omega=A, r=A)
+    kcall = lambda T: dr.dr_chunk_fwd_noalloc(A, A, A, A, p, dr.DR_KDN, 1e-6, None, A, None,  # noqa: E731
+                                              1, T, 1, 128, 128, 64, stream=0)
+    assert kcall(64 * 497) == dr.DR_ERR_WORKSPACE                        # 497 records
+    assert dr.dr_chunk_fwd_workspace_bytes(dr.DR_KDN, dr.DR_FP32, 1, 64 * 496, 1, 128, 128, 64) \
+        <= dr.DR_NOALLOC_SCRATCH_BYTES
+    # the same answers as dr_chunk_fwd for a bad dtype or a missing pointer
+    assert call(dtype=7) == dr.DR_ERR_DTYPE
+    bad = dr.make_params(dtype=dr.DR_BF16, eta=A)
+    assert dr.dr_chunk_fwd_noalloc(A, None, A, A, bad, dr.DR_KLA, 1e-6, None, A, None,
+                                   1, 64, 1, 128, 128, 64, stream=0) == dr.DR_ERR_NULL
+    assert dr.dr_chunk_fwd(A, None, A, A, bad, dr.DR_KLA, 1e-6, None, A, None,
+                           1, 64, 1, 128, 128, 64, stream=0) == dr.DR_ERR_NULL
 
 
 @pytest.mark.gpu
@@ -60,9 +73,8 @@ def test_noalloc_matches_chunk_fwd_on_two_calls():
         dr.check(st, "dr_chunk_fwd_noalloc")
         torch.cuda.synchronize()
         assert dr.dr_get_device_status() == 0
-        eo = rel_err(np64(out), np64(ref_out))
-        es = rel_err(np64(S), np64(ref_S))
-        assert eo <= TOL["bf16"] and es <= TOL["bf16"], (variant, eo, es)
+        # the same kernels on the same inputs: the same bits
+        assert torch.equal(out, ref_out) and torch.equal(S, ref_S), variant
 
 
 @pytest.mark.gpu
@@ -73,9 +85,13 @@ def test_noalloc_per_channel_decay_paths_match_chunk_fwd():
     workspace."""
     from recurrent_associative_memory_gb300 import dr, runner
 
-    cases = [("kdn", "kdn_bf16", 2, 100, 26), ("kda", "kda_bf16", 2, 130, 3),
-             ("ikdn", "ikdn_bf16", 2, 77, 26)]
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    Hc = max(26, -(-nsm // 6))          # 3 B H >= SM count: the chained prep runs
+    cases = [("kdn", "kdn_bf16", 2, 100, Hc), ("kda", "kda_bf16", 2, 130, 3),
+             ("ikdn", "ikdn_bf16", 2, 77, Hc)]
     for variant, base, B, T, H in cases:
+        if variant != "kda":
+            assert 3 * B * H >= nsm and B * H * ((T + 63) // 64) <= 496
         wl = W.small(base, B=B, T=T, H=H, seed=40)
         dev = runner.to_device(W.generate(wl, variant))
         ref_out, ref_S, ref_aux = runner.chunk_fwd(dev)
