@@ -229,6 +229,41 @@ int dr_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const floa
 int dr_get_device_status(dr_stream_t stream);
 
 /*
+ * Backward of dr_chunk_fwd (training): given dL/d out and dL/d final_state,
+ * the gradients of L with respect to q, k, v, log_alpha, eta and init_state, for
+ * the scalar-decay write rules GDN and KLA (KLA notes section 2.5, Eqs. (7)-(9)
+ * differentiated chunk by chunk in reverse; the write gain of section 1.1 / Eq.
+ * (3) and the optional L2 norms differentiated after).  The forward is run again
+ * inside the call (its chunk records, the state at every chunk start and the
+ * chunk residuals E go to the workspace); then a reverse carry over chunks
+ * passes dL/dS from chunk to chunk, and every chunk's local gradients follow in
+ * parallel.
+ *
+ * Inputs as dr_chunk_fwd (same q, k, v, log_alpha, gp gates and flags, eps,
+ * init_state or NULL).  d_out [B,T,H,dv] in gp->dtype; d_final_state fp32
+ * [B,H,dk,dv] or NULL (zero).  Outputs, all device fp32, overwritten: dq, dk
+ * [B,T,H,dk]; dv [B,T,H,dv]; d_log_alpha, d_eta [B,T,H]; d_init_state
+ * [B,H,dk,dv] or NULL (not written).  gp->workspace must hold at least
+ * dr_chunk_bwd_workspace_bytes() (256-byte aligned); its contents are undefined
+ * afterwards.  Supported: DR_GDN, DR_KLA with bf16 q/k/v, dk = dv = 128, chunk
+ * 64 (DR_ERR_UNSUPPORTED otherwise).  Returns DR_OK or a negative dr_status
+ * (DR_ERR_WORKSPACE when the workspace is missing or small).
+ */
+int dr_chunk_bwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                 const dr_params *gp, int variant, float eps, const float *init_state,
+                 const void *d_out, const float *d_final_state,
+                 float *dq, float *dk, float *dv, float *d_log_alpha, float *d_eta,
+                 float *d_init_state, int B, int T, int H, int dk_, int dv_, int chunk,
+                 dr_stream_t stream);
+
+/* Workspace bytes dr_chunk_bwd needs: B H ceil(T/64) x 295,940 rounded up to 256
+ * (the forward's 66,560-byte chunk record, the chunk-start state, E, dL/dS at the
+ * chunk end and three per-chunk products), or 0 where the backward is not
+ * supported. */
+size_t dr_chunk_bwd_workspace_bytes(int variant, int dtype, int B, int T, int H, int dk, int dv,
+                                    int chunk);
+
+/*
  * TEST ONLY -- failure injection on the host side of a device wait.  The
  * chained prep of the per-channel-decay two-phase path (Diagonal KDN, PKDA,
  * isotropic KDN with 3 B H >= SM count) hands each row's gain state from a

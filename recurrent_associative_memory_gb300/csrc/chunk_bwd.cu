@@ -1,0 +1,756 @@
+// chunk_bwd.cu — backward of the chunkwise forward for the scalar-decay write
+// rules GDN (w = eta k^) and KLA (w = eta k^ / (||k^||^2 + eps)): bf16 q/k/v,
+// fp32 gates and state, dk = dv = 128, chunk 64.  Gradients are fp32.
+//
+// Per chunk (local index i, j; KLA notes section 2.5, Eqs. (7)-(9), with the
+// write matrix of the PDN notes section 2.6), with S_c the chunk-start state:
+//
+//   R = V - (Gamma.K^) S_c,  (I + L) E = R,  O = (Gamma.Q^) S_c + P E,
+//   S_{c+1} = gamma S_c + Wbar^T E,  Wbar_j = e^{G - g_j} w_j,
+//   L_ij = (k^_i . w_j) e^{g_i - g_j} (j < i),  P_ij = (q^_i . w_j) e^{g_i - g_j} (j <= i).
+//
+// Differentiating line by line, in reverse chunk order (dS = dL/dS_{c+1}):
+//
+//   dE = P^T dO + Wbar dS,  dR = (I + L)^-T dE = T^T dE,  dV = dR,
+//   dS_c = gamma dS + (Gamma.Q^)^T dO - (Gamma.K^)^T dR,
+//
+// and, per chunk, the local gradients: dP = dO E^T (j <= i), dL = -dR E^T (j < i),
+// dq^ = e^g (dO S_c^T) + (dP.D) W,  dk^ = -e^g (dR S_c^T) + (dL.D) W,
+// dw = (dP.D)^T Q^ + (dL.D)^T K^ + e^{G-g} (E dS^T),  D_ij = e^{g_i - g_j},
+// the decay terms (every entry X_ij . dX_ij of P and L adds to dg_i and takes
+// from dg_j; e^g (dO S_c^T) . q^ and -e^g (dR S_c^T) . k^ add to dg_i;
+// -e^{G-g_j} w_j . (E dS^T)_j to dg_j and its sum plus gamma <dS, S_c> to dG),
+// then d log alpha_t = sum_{i >= t} dg_i with dG on the chunk's last token; the
+// write gain (d beta = dw . k^, dk^ += beta dw; KLA: d eta = d beta / (s + eps),
+// dk^ -= 2 d beta eta / (s + eps)^2 k^) and the L2 norms (dx = (dx^ - x^ (x^ . dx^)) / ||x||).
+//
+// Kernels (after the forward's prep and carry, which saves S_c and E per chunk):
+//   bwd_carry   one CTA per (b, h, 32 columns of dv), chunks in reverse: dE, dR
+//               (written as dV) and dS_c on TF32x3 warp-level tensor-core products,
+//               saving dS = dL/dS_{c+1} per chunk.
+//   bwd_state   one CTA per (b, h, chunk): dO S_c^T, dR S_c^T, E dS^T, dO E^T, dR E^T.
+//   bwd_local   one CTA per (b, h, chunk): gates, Grams, the decay-ratio terms, the
+//               products with W, Q^, K^, the gain and norm backward, d log alpha.
+#include "dr_common.cuh"
+#include "tc_common.cuh"
+
+namespace dr {
+
+cudaError_t launch_chunk_tc_split(const FwdArgs& a, void* workspace, cudaStream_t st);
+
+namespace {
+
+using namespace tc;
+
+constexpr int kBwdThreads = 256;
+// The workspace: the forward's chunk records, then per record the saved state, E,
+// dS_{c+1}, E dS^T, dO E^T, dR E^T and gamma <dS, S_c> (one array each, record-major)
+constexpr size_t kRecF = 66560;                 // the forward's chunk record (tc_split)
+constexpr size_t kBwdPerRec = kRecF + 4 * (16384 + 8192 + 16384 + 8192 + 4096 + 4096 + 1);
+// the forward record's vectors (floats after rVecF): e^g qn, e^{G-g} c, gamma, e^g cr
+constexpr size_t rVecF = 65536;
+constexpr uint32_t rTF = 0, rPF = 49152;
+
+struct BwdWs {
+  uint8_t* rec;   // [n] x kRecF
+  float* S;       // [n][128][128]  S_c
+  float* E;       // [n][64][128]   E
+  float* dS;      // [n][128][128]  dL/dS_{c+1}
+  float* XW;      // [n][64][128]   E dS^T
+  float* dP;      // [n][64][64]    dO E^T
+  float* dL;      // [n][64][64]    dR E^T
+  float* SS;      // [n]            gamma <dS, S_c>
+};
+
+BwdWs bwd_ws(void* base, long n) {
+  BwdWs w;
+  w.rec = static_cast<uint8_t*>(base);
+  w.S = reinterpret_cast<float*>(w.rec + (size_t)n * kRecF);
+  w.E = w.S + (size_t)n * 16384;
+  w.dS = w.E + (size_t)n * 8192;
+  w.XW = w.dS + (size_t)n * 16384;
+  w.dP = w.XW + (size_t)n * 8192;
+  w.dL = w.dP + (size_t)n * 4096;
+  w.SS = w.dL + (size_t)n * 4096;
+  return w;
+}
+
+// ---- warp-level 16 x 8 tile of op(A) op(B) over K = 8 KSTEPS, fp32 operands split
+// into two TF32 terms each (hi + lo) and three products: fp32-accurate.
+// A element (m, k) = TA ? A[k lda + m] : A[m lda + k];
+// B element (k, n) = TB ? B[n ldb + k] : B[k ldb + n].
+template <int KSTEPS, bool TA, bool TB>
+__device__ __forceinline__ void mm3(float (&d)[4], const float* A, int lda, const float* B, int ldb,
+                                    int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  float dc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int ks = 0; ks < KSTEPS; ++ks) {
+    const int k0 = 8 * ks;
+    float af[4], bf[2];
+    if (TA) {
+      af[0] = A[(k0 + t) * lda + g];
+      af[1] = A[(k0 + t) * lda + g + 8];
+      af[2] = A[(k0 + t + 4) * lda + g];
+      af[3] = A[(k0 + t + 4) * lda + g + 8];
+    } else {
+      af[0] = A[g * lda + k0 + t];
+      af[1] = A[(g + 8) * lda + k0 + t];
+      af[2] = A[g * lda + k0 + t + 4];
+      af[3] = A[(g + 8) * lda + k0 + t + 4];
+    }
+    if (TB) {
+      bf[0] = B[g * ldb + k0 + t];
+      bf[1] = B[g * ldb + k0 + t + 4];
+    } else {
+      bf[0] = B[(k0 + t) * ldb + g];
+      bf[1] = B[(k0 + t + 4) * ldb + g];
+    }
+    uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      ah[i] = to_tf32(af[i]);
+      al[i] = to_tf32(af[i] - __uint_as_float(ah[i]));
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      bh[i] = to_tf32(bf[i]);
+      bl[i] = to_tf32(bf[i] - __uint_as_float(bh[i]));
+    }
+    mma_tf32(dc, al, bh);
+    mma_tf32(dc, ah, bl);
+    mma_tf32(d, ah, bh);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] += dc[i];
+}
+
+// fragment element e of a 16 x 8 tile: row and column within the tile
+__device__ __forceinline__ int frag_row(int lane, int e) { return (lane >> 2) + ((e >> 1) << 3); }
+__device__ __forceinline__ int frag_col(int lane, int e) { return 2 * (lane & 3) + (e & 1); }
+
+// 8 bf16 from global (16-byte aligned) -> float
+__device__ __forceinline__ void ld8(const __nv_bfloat16* p, float (&f)[8]) {
+  unpack8(*reinterpret_cast<const uint4*>(p), f);
+}
+
+// One element of a 64 x 64 hi/lo bf16 tile image (128B-swizzled rows) of a record
+__device__ __forceinline__ void tile_row8(const uint8_t* img, int row, int col0, float (&f)[8]) {
+  float h[8], l[8];
+  unpack8(*reinterpret_cast<const uint4*>(img + umma::sw128_offset(row, col0)), h);
+  unpack8(*reinterpret_cast<const uint4*>(img + 8192 + umma::sw128_offset(row, col0)), l);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) f[e] = h[e] + l[e];
+}
+
+__device__ __forceinline__ long tok(const FwdArgs& a, int b, int t, int h) {
+  return ((long)b * a.T + t) * a.H + h;
+}
+
+// ================================================================= bwd_carry
+constexpr int cLD64T = 72;    // 64-wide tiles read transposed (A operand, TA)
+constexpr int cLDW = 132;     // 128-wide, read as A (non-transposed)
+constexpr int cLDQ = 136;     // 128-wide, read transposed
+constexpr int cLDN = 40;      // 32-wide B operands
+constexpr int kCarrySmemF = 2 * 64 * cLD64T + 64 * cLDW + 2 * 64 * cLDQ + 3 * 64 * cLDN + 128 * cLDN;
+
+struct BwdArgs {
+  const void* d_out;         // [B,T,H,dv] bf16
+  const float* dS_final;     // [B,H,dk,dv] or null
+  float* dq;                 // [B,T,H,dk] fp32
+  float* dk;
+  float* dv;                 // [B,T,H,dv]
+  float* dla;                // [B,T,H]
+  float* deta;               // [B,T,H]
+  float* dS0;                // [B,H,dk,dv] or null
+  BwdWs w;
+};
+
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_carry_kernel(FwdArgs a, BwdArgs g) {
+  extern __shared__ __align__(16) float smf[];
+  float* sP = smf;                       // P [i][j]
+  float* sT = sP + 64 * cLD64T;          // T [i][j]
+  float* sWb = sT + 64 * cLD64T;         // Wbar [j][c]
+  float* sQg = sWb + 64 * cLDW;          // (Gamma.Q^) [j][c]
+  float* sKg = sQg + 64 * cLDQ;          // (Gamma.K^) [j][c]
+  float* sdO = sKg + 64 * cLDQ;          // dO [i][n]
+  float* sdE = sdO + 64 * cLDN;
+  float* sdR = sdE + 64 * cLDN;
+  float* sdS = sdR + 64 * cLDN;          // dS [c][n]
+  __shared__ float s_gamma;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x >> 2, cb = blockIdx.x & 3;
+  const int b = bh / a.H, h = bh % a.H;
+  const int NC = (a.T + 63) / 64;
+  const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
+  const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(a.q);
+  const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(g.d_out);
+
+  for (int e = tid; e < 128 * 32; e += kBwdThreads) {
+    const int r = e >> 5, n = e & 31;
+    sdS[r * cLDN + n] = g.dS_final ? g.dS_final[((size_t)bh * 128 + r) * 128 + 32 * cb + n] : 0.f;
+  }
+  for (int c = NC - 1; c >= 0; --c) {
+    const size_t ri = (size_t)bh * NC + c;
+    const uint8_t* rec = g.w.rec + ri * kRecF;
+    const float* rv = reinterpret_cast<const float*>(rec + rVecF);
+    const int t0 = 64 * c, Cc = min(64, a.T - t0);
+    __syncthreads();   // the previous chunk's readers of every buffer are done
+    // ---- dS_{c+1} for the local gradients
+    float* sv = g.w.dS + ri * 16384;
+    for (int e = tid; e < 128 * 32; e += kBwdThreads) {
+      const int r = e >> 5, n = e & 31;
+      sv[r * 128 + 32 * cb + n] = sdS[r * cLDN + n];
+    }
+    // ---- operands: P and T from the record images, K and Q rows scaled, dO
+    for (int e = tid; e < 64 * 8; e += kBwdThreads) {
+      const int i = e >> 3, c0 = 8 * (e & 7);
+      float f[8];
+      tile_row8(rec + rPF, i, c0, f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sP[i * cLD64T + c0 + q] = f[q];
+      tile_row8(rec + rTF, i, c0, f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sT[i * cLD64T + c0 + q] = f[q];
+    }
+    for (int e = tid; e < 64 * 16; e += kBwdThreads) {
+      const int j = e >> 4, c0 = 8 * (e & 15);
+      float kf[8], qf[8];
+      if (j < Cc) {
+        ld8(K + tok(a, b, t0 + j, h) * 128 + c0, kf);
+        ld8(Q + tok(a, b, t0 + j, h) * 128 + c0, qf);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) kf[q] = qf[q] = 0.f;
+      }
+      const float u = rv[64 + j], eqn = rv[j], ekc = rv[192 + j];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        sWb[j * cLDW + c0 + q] = u * kf[q];
+        sKg[j * cLDQ + c0 + q] = ekc * kf[q];
+        sQg[j * cLDQ + c0 + q] = eqn * qf[q];
+      }
+    }
+    {
+      const int i = tid >> 2, c0 = 8 * (tid & 3);
+      float f[8];
+      if (i < Cc) {
+        ld8(dO + tok(a, b, t0 + i, h) * 128 + 32 * cb + c0, f);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) f[q] = 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sdO[i * cLDN + c0 + q] = f[q];
+    }
+    if (tid == 0) s_gamma = rv[128];
+    __syncthreads();
+    // ---- dE = P^T dO + Wbar dS  (64 x 32: 16 tiles, two per warp)
+    const int mt = warp >> 1;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int nt = 2 * (warp & 1) + s;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mm3<8, true, false>(d, sP + 16 * mt, cLD64T, sdO + 8 * nt, cLDN, lane);
+      mm3<16, false, false>(d, sWb + 16 * mt * cLDW, cLDW, sdS + 8 * nt, cLDN, lane);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        sdE[(16 * mt + frag_row(lane, e)) * cLDN + 8 * nt + frag_col(lane, e)] = d[e];
+    }
+    __syncthreads();
+    // ---- dR = T^T dE, also dV
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int nt = 2 * (warp & 1) + s;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mm3<8, true, false>(d, sT + 16 * mt, cLD64T, sdE + 8 * nt, cLDN, lane);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 16 * mt + frag_row(lane, e), n = 8 * nt + frag_col(lane, e);
+        sdR[i * cLDN + n] = d[e];
+        if (i < Cc) g.dv[tok(a, b, t0 + i, h) * 128 + 32 * cb + n] = d[e];
+      }
+    }
+    __syncthreads();
+    // ---- dS_c = gamma dS + (Gamma.Q^)^T dO - (Gamma.K^)^T dR (warp: rows 16 warp .. + 16)
+    const float gam = s_gamma;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      float d[4], m[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        d[e] = gam * sdS[(16 * warp + frag_row(lane, e)) * cLDN + 8 * nt + frag_col(lane, e)];
+      mm3<8, true, false>(d, sQg + 16 * warp, cLDQ, sdO + 8 * nt, cLDN, lane);
+      mm3<8, true, false>(m, sKg + 16 * warp, cLDQ, sdR + 8 * nt, cLDN, lane);
+      __syncwarp();
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        sdS[(16 * warp + frag_row(lane, e)) * cLDN + 8 * nt + frag_col(lane, e)] = d[e] - m[e];
+    }
+  }
+  __syncthreads();
+  if (g.dS0) {
+    for (int e = tid; e < 128 * 32; e += kBwdThreads) {
+      const int r = e >> 5, n = e & 31;
+      g.dS0[((size_t)bh * 128 + r) * 128 + 32 * cb + n] = sdS[r * cLDN + n];
+    }
+  }
+}
+
+// ================================================================= bwd_state
+constexpr int cLDS = 132;   // 128-wide fp32 rows (A non-transposed / B transposed)
+constexpr int kStateSmemF = 128 * cLDS + 3 * 64 * cLDS;
+
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_state_kernel(FwdArgs a, BwdArgs g) {
+  extern __shared__ __align__(16) float smf[];
+  float* sS = smf;                 // S_c [c][v], then dS_{c+1} [c][v]
+  float* sdO = sS + 128 * cLDS;    // dO [i][v]
+  float* sdR = sdO + 64 * cLDS;    // dR [i][v]
+  float* sE = sdR + 64 * cLDS;     // E [j][v]
+  __shared__ float s_red[kBwdThreads / 32];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NC = (a.T + 63) / 64;
+  const long task = blockIdx.x;
+  const int bh = (int)(task / NC), c = (int)(task % NC);
+  const int b = bh / a.H, h = bh % a.H;
+  const int t0 = 64 * c, Cc = min(64, a.T - t0);
+  const float* Sc = g.w.S + (size_t)task * 16384;
+  const float* Ec = g.w.E + (size_t)task * 8192;
+  const float* dSc = g.w.dS + (size_t)task * 16384;
+  const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(g.d_out);
+
+  for (int e = tid; e < 128 * 32; e += kBwdThreads) {
+    const int r = e >> 5, c4 = 4 * (e & 31);
+    *reinterpret_cast<float4*>(sS + r * cLDS + c4) = *reinterpret_cast<const float4*>(Sc + r * 128 + c4);
+  }
+  for (int e = tid; e < 64 * 32; e += kBwdThreads) {
+    const int i = e >> 5, c4 = 4 * (e & 31);
+    float4 r4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i < Cc) r4 = *reinterpret_cast<const float4*>(g.dv + tok(a, b, t0 + i, h) * 128 + c4);
+    *reinterpret_cast<float4*>(sdR + i * cLDS + c4) = r4;
+    *reinterpret_cast<float4*>(sE + i * cLDS + c4) = *reinterpret_cast<const float4*>(Ec + i * 128 + c4);
+  }
+  for (int e = tid; e < 64 * 16; e += kBwdThreads) {
+    const int i = e >> 4, c0 = 8 * (e & 15);
+    float f[8];
+    if (i < Cc) {
+      ld8(dO + tok(a, b, t0 + i, h) * 128 + c0, f);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) f[q] = 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) sdO[i * cLDS + c0 + q] = f[q];
+  }
+  __syncthreads();
+  // X_Q = dO S_c^T -> dq, X_K = dR S_c^T -> dk (raw; bwd_local scales and adds)
+  // 64 x 128 each: 64 tiles, eight per warp (m tile = warp & 3, n tiles 8 (warp >> 2) .. + 8)
+  {
+    const int mt = warp & 3;
+    for (int s = 0; s < 8; ++s) {
+      const int nt = 8 * (warp >> 2) + s;
+      float dq4[4] = {0.f, 0.f, 0.f, 0.f}, dk4[4] = {0.f, 0.f, 0.f, 0.f};
+      mm3<16, false, true>(dq4, sdO + 16 * mt * cLDS, cLDS, sS + 8 * nt * cLDS, cLDS, lane);
+      mm3<16, false, true>(dk4, sdR + 16 * mt * cLDS, cLDS, sS + 8 * nt * cLDS, cLDS, lane);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 16 * mt + frag_row(lane, e), n = 8 * nt + frag_col(lane, e);
+        if (i < Cc) {
+          g.dq[tok(a, b, t0 + i, h) * 128 + n] = dq4[e];
+          g.dk[tok(a, b, t0 + i, h) * 128 + n] = dk4[e];
+        }
+      }
+    }
+  }
+  // dP = dO E^T and dR E^T (64 x 64: 32 tiles, four per warp)
+  {
+    float* xp = g.w.dP + (size_t)task * 4096;
+    float* xl = g.w.dL + (size_t)task * 4096;
+    const int mt = warp & 3;
+    for (int s = 0; s < 4; ++s) {
+      const int nt = 4 * (warp >> 2) + s;
+      float p4[4] = {0.f, 0.f, 0.f, 0.f}, l4[4] = {0.f, 0.f, 0.f, 0.f};
+      mm3<16, false, true>(p4, sdO + 16 * mt * cLDS, cLDS, sE + 8 * nt * cLDS, cLDS, lane);
+      mm3<16, false, true>(l4, sdR + 16 * mt * cLDS, cLDS, sE + 8 * nt * cLDS, cLDS, lane);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 16 * mt + frag_row(lane, e), j = 8 * nt + frag_col(lane, e);
+        xp[i * 64 + j] = p4[e];
+        xl[i * 64 + j] = l4[e];
+      }
+    }
+  }
+  __syncthreads();
+  // dS_{c+1} in place of S_c, and gamma <dS, S_c> on the way
+  float part = 0.f;
+  for (int e = tid; e < 128 * 32; e += kBwdThreads) {
+    const int r = e >> 5, c4 = 4 * (e & 31);
+    const float4 x = *reinterpret_cast<const float4*>(dSc + r * 128 + c4);
+    float4* s4 = reinterpret_cast<float4*>(sS + r * cLDS + c4);
+    const float4 y = *s4;
+    part += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+    *s4 = x;
+  }
+  part = warp_sum(part);
+  if (lane == 0) s_red[warp] = part;
+  __syncthreads();
+  if (tid == 0) {
+    float tsum = 0.f;
+    for (int w = 0; w < kBwdThreads / 32; ++w) tsum += s_red[w];
+    const float gam = reinterpret_cast<const float*>(g.w.rec + (size_t)task * kRecF + rVecF)[128];
+    g.w.SS[task] = gam * tsum;
+  }
+  // X_W = E dS^T
+  {
+    float* xw = g.w.XW + (size_t)task * 8192;
+    const int mt = warp & 3;
+    for (int s = 0; s < 8; ++s) {
+      const int nt = 8 * (warp >> 2) + s;
+      float w4[4] = {0.f, 0.f, 0.f, 0.f};
+      mm3<16, false, true>(w4, sE + 16 * mt * cLDS, cLDS, sS + 8 * nt * cLDS, cLDS, lane);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 16 * mt + frag_row(lane, e), n = 8 * nt + frag_col(lane, e);
+        xw[i * 128 + n] = w4[e];
+      }
+    }
+  }
+}
+
+// ================================================================= bwd_local
+constexpr int cLDK = 132;   // K^, Q^, W, staging [64][132]
+constexpr int cLDM = 68;    // M_P, M_L [64][68]
+constexpr int kLocalSmemF = 5 * 64 * cLDK + 2 * 64 * cLDM;
+
+template <int VARIANT>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_local_kernel(FwdArgs a, BwdArgs g) {
+  extern __shared__ __align__(16) float smf[];
+  float* sK = smf;                 // k^ [j][c]
+  float* sQ = sK + 64 * cLDK;      // q^
+  float* sW = sQ + 64 * cLDK;      // w = beta k^
+  float* sX = sW + 64 * cLDK;      // staging of one product
+  float* sY = sX + 64 * cLDK;      // dw
+  float* sMP = sY + 64 * cLDK;     // (dP . D) [i][j]
+  float* sML = sMP + 64 * cLDM;    // (dL . D) [i][j]
+  __shared__ float s_g[64], s_cr[64], s_qn[64], s_beta[64], s_s[64], s_eta[64];
+  __shared__ float s_dg[64], s_dbeta[64], s_dGt[64];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NC = (a.T + 63) / 64;
+  const long task = blockIdx.x;
+  const int bh = (int)(task / NC), c = (int)(task % NC);
+  const int b = bh / a.H, h = bh % a.H;
+  const int t0 = 64 * c, Cc = min(64, a.T - t0);
+  const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
+  const __nv_bfloat16* Qp = static_cast<const __nv_bfloat16*>(a.q);
+
+  // ---- raw rows, norms, gates
+  for (int e = tid; e < 64 * 16; e += kBwdThreads) {
+    const int j = e >> 4, c0 = 8 * (e & 15);
+    float kf[8], qf[8];
+    if (j < Cc) {
+      ld8(K + tok(a, b, t0 + j, h) * 128 + c0, kf);
+      ld8(Qp + tok(a, b, t0 + j, h) * 128 + c0, qf);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) kf[q] = qf[q] = 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      sK[j * cLDK + c0 + q] = kf[q];
+      sQ[j * cLDK + c0 + q] = qf[q];
+    }
+  }
+  if (tid < 64) {
+    s_g[tid] = (tid < Cc) ? a.log_alpha[tok(a, b, t0 + tid, h)] : 0.f;
+    s_eta[tid] = (tid < Cc) ? a.eta[tok(a, b, t0 + tid, h)] : 0.f;
+  }
+  __syncthreads();
+  {   // norms: four threads per row
+    const int j = tid >> 2, part = tid & 3;
+    float kk = 0.f, qq = 0.f;
+    for (int c0 = 32 * part; c0 < 32 * part + 32; ++c0) {
+      const float x = sK[j * cLDK + c0], y = sQ[j * cLDK + c0];
+      kk += x * x;
+      qq += y * y;
+    }
+    kk += __shfl_xor_sync(0xffffffffu, kk, 1);
+    kk += __shfl_xor_sync(0xffffffffu, kk, 2);
+    qq += __shfl_xor_sync(0xffffffffu, qq, 1);
+    qq += __shfl_xor_sync(0xffffffffu, qq, 2);
+    if (part == 0) {
+      const float cr = a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f;
+      const float qn = a.q_l2norm ? 1.f / fmaxf(sqrtf(qq), 1e-30f) : 1.f;
+      const float s = kk * cr * cr;
+      s_cr[j] = cr;
+      s_qn[j] = qn;
+      s_s[j] = s;
+      s_beta[j] = VARIANT == DR_KLA ? s_eta[j] / (s + a.eps) : s_eta[j];
+    }
+  }
+  if (warp == 0) {   // inclusive cumulative log-decay (two tokens per lane)
+    const float x0 = s_g[2 * lane], x1 = s_g[2 * lane + 1];
+    float s = x0 + x1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    __syncwarp();
+    s_g[2 * lane] = s - x1;
+    s_g[2 * lane + 1] = s;
+  }
+  __syncthreads();
+  for (int e = tid; e < 64 * 128; e += kBwdThreads) {
+    const int j = e >> 7, cc = e & 127;
+    const float kh = sK[j * cLDK + cc] * s_cr[j];
+    sK[j * cLDK + cc] = kh;
+    sQ[j * cLDK + cc] *= s_qn[j];
+    sW[j * cLDK + cc] = s_beta[j] * kh;
+  }
+  // dO E^T and dR E^T from bwd_state
+  const float* xp = g.w.dP + (size_t)task * 4096;
+  const float* xl = g.w.dL + (size_t)task * 4096;
+  __syncthreads();
+  const float G = s_g[Cc - 1];
+  // ---- Grams Q^ W^T and K^ W^T, then M_P = dP . D (j <= i), M_L = dL . D (j < i),
+  //      and the decay terms of every entry (row i gains, column j loses)
+  {
+    const int mt = warp & 3;
+    for (int s = 0; s < 4; ++s) {
+      const int nt = 4 * (warp >> 2) + s;
+      float aq[4] = {0.f, 0.f, 0.f, 0.f}, ak[4] = {0.f, 0.f, 0.f, 0.f};
+      mm3<16, false, true>(aq, sQ + 16 * mt * cLDK, cLDK, sW + 8 * nt * cLDK, cLDK, lane);
+      mm3<16, false, true>(ak, sK + 16 * mt * cLDK, cLDK, sW + 8 * nt * cLDK, cLDK, lane);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 16 * mt + frag_row(lane, e), j = 8 * nt + frag_col(lane, e);
+        const float D = (j <= i) ? __expf(s_g[i] - s_g[j]) : 0.f;
+        const float dP = (j <= i) ? xp[i * 64 + j] : 0.f;
+        const float dL = (j < i) ? -xl[i * 64 + j] : 0.f;
+        const float mp = dP * D, ml = dL * D;
+        sMP[i * cLDM + j] = mp;
+        sML[i * cLDM + j] = ml;
+        sX[i * cLDK + j] = mp * aq[e] + ml * ak[e];   // dP_ij P_ij + dL_ij L_ij
+      }
+    }
+  }
+  __syncthreads();
+  if (tid < 64) {   // each entry adds to dg of its row and takes from dg of its column
+    float r = 0.f, cs = 0.f;
+    for (int j = 0; j < 64; ++j) {
+      r += sX[tid * cLDK + j];
+      cs += sX[j * cLDK + tid];
+    }
+    s_dg[tid] = r - cs;
+  }
+  __syncthreads();
+  // ---- dw = M_P^T Q^ + M_L^T K^ (+ e^{G-g} E dS^T): staged in sY
+  {
+    const int mt = warp & 3;
+    for (int s = 0; s < 8; ++s) {
+      const int nt = 8 * (warp >> 2) + s;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mm3<8, true, false>(d, sMP + 16 * mt, cLDM, sQ + 8 * nt, cLDK, lane);
+      mm3<8, true, false>(d, sML + 16 * mt, cLDM, sK + 8 * nt, cLDK, lane);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        sY[(16 * mt + frag_row(lane, e)) * cLDK + 8 * nt + frag_col(lane, e)] = d[e];
+    }
+  }
+  __syncthreads();
+  {   // rows: four threads per token; dw += e^{G-g} X_W, the decay terms, d beta
+    const int j = tid >> 2, part = tid & 3;
+    const float* xw = g.w.XW + (size_t)task * 8192 + j * 128;
+    const float ew = (j < Cc) ? __expf(G - s_g[j]) : 0.f;
+    float dwk = 0.f, xww = 0.f;
+    for (int c0 = 32 * part; c0 < 32 * part + 32; ++c0) {
+      const float xv = xw[c0];
+      const float dw = sY[j * cLDK + c0] + ew * xv;
+      sY[j * cLDK + c0] = dw;
+      dwk += dw * sK[j * cLDK + c0];
+      xww += xv * sW[j * cLDK + c0];
+    }
+    dwk += __shfl_xor_sync(0xffffffffu, dwk, 1);
+    dwk += __shfl_xor_sync(0xffffffffu, dwk, 2);
+    xww += __shfl_xor_sync(0xffffffffu, xww, 1);
+    xww += __shfl_xor_sync(0xffffffffu, xww, 2);
+    if (part == 0) {
+      s_dbeta[j] = j < Cc ? dwk : 0.f;
+      s_dg[j] -= ew * xww;
+      s_dGt[j] = ew * xww;
+    }
+  }
+  __syncthreads();
+  // ---- dk^ = M_L W - e^g X_K + beta dw (+ KLA norm term), then the key norm
+  {
+    const int mt = warp & 3;
+    for (int s = 0; s < 8; ++s) {
+      const int nt = 8 * (warp >> 2) + s;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mm3<8, false, false>(d, sML + 16 * mt * cLDM, cLDM, sW + 8 * nt, cLDK, lane);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        sX[(16 * mt + frag_row(lane, e)) * cLDK + 8 * nt + frag_col(lane, e)] = d[e];
+    }
+  }
+  __syncthreads();
+  {
+    const int j = tid >> 2, part = tid & 3;
+    const bool live = j < Cc;
+    float* dkrow = g.dk + tok(a, b, t0 + (live ? j : 0), h) * 128;
+    const float eg = __expf(s_g[j]);
+    const float beta = s_beta[j], db = s_dbeta[j];
+    // KLA: beta = eta / (s + eps): d eta = d beta / (s + eps), ds = -d beta eta / (s + eps)^2
+    const float se = s_s[j] + a.eps;
+    const float ds2 = VARIANT == DR_KLA ? -2.f * db * s_eta[j] / (se * se) : 0.f;
+    float dkh[32], xk = 0.f, dot = 0.f;
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+      const int c0 = 32 * part + q;
+      const float xkv = live ? dkrow[c0] : 0.f;
+      const float kh = sK[j * cLDK + c0];
+      xk += xkv * kh;
+      dkh[q] = sX[j * cLDK + c0] - eg * xkv + beta * sY[j * cLDK + c0] + ds2 * kh;
+      dot += dkh[q] * kh;
+    }
+    xk += __shfl_xor_sync(0xffffffffu, xk, 1);
+    xk += __shfl_xor_sync(0xffffffffu, xk, 2);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+    if (live) {
+      const float cr = s_cr[j];
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int c0 = 32 * part + q;
+        // k^ = k cr: dk = (dk^ - k^ (k^ . dk^)) cr  (k^ is unit-norm then)
+        dkrow[c0] = a.k_l2norm ? (dkh[q] - sK[j * cLDK + c0] * dot) * cr : dkh[q];
+      }
+      if (part == 0) {
+        s_dg[j] -= eg * xk;
+        g.deta[tok(a, b, t0 + j, h)] = VARIANT == DR_KLA ? db / se : db;
+      }
+    }
+  }
+  __syncthreads();
+  // ---- dq^ = M_P W + e^g X_Q, then the query norm
+  {
+    const int mt = warp & 3;
+    for (int s = 0; s < 8; ++s) {
+      const int nt = 8 * (warp >> 2) + s;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mm3<8, false, false>(d, sMP + 16 * mt * cLDM, cLDM, sW + 8 * nt, cLDK, lane);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        sX[(16 * mt + frag_row(lane, e)) * cLDK + 8 * nt + frag_col(lane, e)] = d[e];
+    }
+  }
+  __syncthreads();
+  {
+    const int j = tid >> 2, part = tid & 3;
+    const bool live = j < Cc;
+    float* dqrow = g.dq + tok(a, b, t0 + (live ? j : 0), h) * 128;
+    const float eg = __expf(s_g[j]);
+    float dqh[32], xq = 0.f, dot = 0.f;
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+      const int c0 = 32 * part + q;
+      const float xqv = live ? dqrow[c0] : 0.f;
+      const float qh = sQ[j * cLDK + c0];
+      xq += xqv * qh;
+      dqh[q] = sX[j * cLDK + c0] + eg * xqv;
+      dot += dqh[q] * qh;
+    }
+    xq += __shfl_xor_sync(0xffffffffu, xq, 1);
+    xq += __shfl_xor_sync(0xffffffffu, xq, 2);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+    if (live) {
+      const float qn = s_qn[j];
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int c0 = 32 * part + q;
+        dqrow[c0] = a.q_l2norm ? (dqh[q] - sQ[j * cLDK + c0] * dot) * qn : dqh[q];
+      }
+      if (part == 0) s_dg[j] += eg * xq;
+    }
+  }
+  __syncthreads();
+  // ---- d log alpha: reverse cumulative sum of dg, dG (+ gamma <dS, S_c>) on the last token
+  if (warp == 0) {
+    if (lane == 0) {   // dG: the chunk's last token
+      float dG = g.w.SS[task];
+      for (int j = 0; j < 64; ++j) dG += s_dGt[j];
+      s_dg[Cc - 1] += dG;
+    }
+    __syncwarp();
+    // suffix sums over 64 entries, two per lane (lane l: tokens 63 - 2l, 62 - 2l)
+    const float x0 = s_dg[63 - 2 * lane], x1 = s_dg[62 - 2 * lane];
+    float s = x0 + x1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    const int ta = 63 - 2 * lane, tb = 62 - 2 * lane;
+    if (ta < Cc) g.dla[tok(a, b, t0 + ta, h)] = s - x1;
+    if (tb < Cc) g.dla[tok(a, b, t0 + tb, h)] = s;
+  }
+}
+
+}  // namespace
+
+bool chunk_bwd_supported(int variant, int dtype, int dk, int dv, int chunk) {
+  return (variant == DR_GDN || variant == DR_KLA) && dtype == DR_BF16 && dk == 128 && dv == 128 &&
+         chunk == 64;
+}
+
+size_t chunk_bwd_workspace_bytes(int B, int T, int H) {
+  const size_t n = (size_t)B * H * ((T + 63) / 64);
+  return (n * kBwdPerRec + 255) / 256 * 256;
+}
+
+cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* dS_final, float* dq,
+                             float* dk, float* dv, float* dla, float* deta, float* dS0,
+                             void* workspace, cudaStream_t st) {
+  const long n = (long)fa.B * fa.H * ((fa.T + 63) / 64);
+  BwdArgs g{d_out, dS_final, dq, dk, dv, dla, deta, dS0, bwd_ws(workspace, n)};
+  // the forward again: the records, the state at every chunk start and E (no
+  // output, no final state)
+  FwdArgs a = fa;
+  a.out = nullptr;
+  a.S = nullptr;
+  a.aux = nullptr;
+  a.check_finite = 0;
+  a.save_S = g.w.S;
+  a.save_E = g.w.E;
+  cudaError_t e = launch_chunk_tc_split(a, workspace, st);
+  if (e != cudaSuccess) return e;
+  const size_t c_smem = (size_t)kCarrySmemF * 4, s_smem = (size_t)kStateSmemF * 4,
+               l_smem = (size_t)kLocalSmemF * 4;
+  if ((e = cudaFuncSetAttribute(bwd_carry_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)c_smem)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(bwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)s_smem)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(bwd_local_kernel<DR_GDN>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l_smem)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(bwd_local_kernel<DR_KLA>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l_smem)) !=
+          cudaSuccess)
+    return e;
+  bwd_carry_kernel<<<fa.B * fa.H * 4, kBwdThreads, c_smem, st>>>(fa, g);
+  bwd_state_kernel<<<(unsigned)n, kBwdThreads, s_smem, st>>>(fa, g);
+  if (fa.variant == DR_KLA)
+    bwd_local_kernel<DR_KLA><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
+  else
+    bwd_local_kernel<DR_GDN><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
+  return cudaGetLastError();
+}
+
+}  // namespace dr

@@ -50,7 +50,8 @@ constexpr int LDX = 36;                     // fp32 scratch row stride
 constexpr uint32_t rT = 0;          // T hi | T lo       (64 x 64 bf16 each)
 constexpr uint32_t rWp = 16384;     // W'^T hi [128 dk][64 tok], then W'^T lo
 constexpr uint32_t rP = 49152;      // P hi | P lo
-constexpr uint32_t rVec = 65536;    // fp32 [0,64) e^g qn ; [64,128) e^{g_C-g} c ; [128] gamma_C
+constexpr uint32_t rVec = 65536;    // fp32 [0,64) e^g qn ; [64,128) e^{g_C-g} c ; [128] gamma_C ;
+                                    //      [192,256) e^g cr (GDN/KLA)
 constexpr uint32_t kRec = 66560;
 // PGDN records add the explicit write keys and the statistic's chunk map
 constexpr uint32_t rW = 66560;      // W hi [64 tok][128] (2 k-blocks), then W lo      32 KB
@@ -246,6 +247,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         float* rv = reinterpret_cast<float*>(rec + rVec);
         rv[i] = eg * qn;
         rv[64 + i] = __expf(gC - gi) * coef;
+        rv[192 + i] = eg * cr;   // e^g cr: the backward's (Gamma.K^) rows
         if (i == 0) rv[128] = __expf(gC);
       }
       if (kPgdn && leader) bulk_wait_read<0>();   // the previous W'^T copy has left the T region
@@ -918,6 +920,12 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
 
     for (int c = 0; c < NC; ++c) {
       const int slot = c & 1;
+      if (a.save_S) {   // backward: the state at this chunk's start
+        float* dst = a.save_S + (((size_t)bh * NC + c) * 128 + srow) * 128 + half * 64 + 32 * hc;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+      }
       float u_nxt = 0.f, g_nxt = 0.f;
       if (c + 1 < NC) {   // one chunk ahead; consumed next iteration
         const float* rv = reinterpret_cast<const float*>(recs + (size_t)(c + 1) * kRecV + rVec);
@@ -958,6 +966,13 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
             const float4 p = *reinterpret_cast<const float4*>(xk + e);
             kv[e] += p.x; kv[e + 1] += p.y; kv[e + 2] += p.z; kv[e + 3] += p.w;
           }
+        }
+        if (a.save_E) {   // backward: E(c), this thread's row and 16 columns
+          float* dst = a.save_E + (((size_t)bh * NC + c) * 64 + erow) * 128 + half * 64 + 32 * hc +
+                       16 * keep;
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(dst + e) = make_float4(kv[e], kv[e + 1], kv[e + 2], kv[e + 3]);
         }
         uint8_t* Et = sm + cE;
 #pragma unroll
@@ -1115,7 +1130,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 16; ++e) x[e] = qv[hcol][e] + ((lane < 16) ? pa[e] + pb[e] : x[e]);
-        if (i < Cc) {
+        if (a.out && i < Cc) {
           const int col = 32 * hcol + ((lane < 16) ? 0 : 16);
 #pragma unroll
           for (int m = 0; m < 2; ++m) {

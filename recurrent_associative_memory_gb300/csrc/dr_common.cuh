@@ -35,6 +35,11 @@ struct FwdArgs {
   float ln_x;             // ln(x) of the PGDN bound
   float log_floor;
   float info_scale;
+  // backward only (null otherwise): the carry of the scalar-decay two-phase path
+  // saves the state at every chunk start [B H NC][dk][dv] and the chunk's E
+  // [B H NC][64][dv] (fp32), and a null `out` skips the output stores
+  float* save_S;
+  float* save_E;
 };
 
 // Sticky device status: the first non-OK code written stays until read.

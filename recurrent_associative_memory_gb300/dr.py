@@ -70,6 +70,13 @@ _lib.dr_chunk_fwd_path.argtypes = [c_int] * 5
 _lib.dr_chunk_fwd_path.restype = c_char_p
 _lib.dr_chunk_fwd_noalloc.argtypes = _lib.dr_chunk_fwd.argtypes
 _lib.dr_chunk_fwd_noalloc.restype = c_int
+_lib.dr_chunk_bwd.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, ctypes.POINTER(DrParams),
+                             c_int, ctypes.c_float, c_void_p, c_void_p, c_void_p, c_void_p,
+                             c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
+                             c_int, c_int, c_int, c_int, c_void_p]
+_lib.dr_chunk_bwd.restype = c_int
+_lib.dr_chunk_bwd_workspace_bytes.argtypes = [c_int] * 8
+_lib.dr_chunk_bwd_workspace_bytes.restype = c_size_t
 _lib.dr_set_chain_fault_for_testing.argtypes = [ctypes.c_longlong, ctypes.c_ulonglong]
 _lib.dr_set_chain_fault_for_testing.restype = c_int
 
@@ -172,3 +179,17 @@ def dr_chunk_fwd_noalloc(q, k, v, log_alpha, params: DrParams, variant: int, eps
 def dr_set_chain_fault_for_testing(withhold_flag: int, wait_ns: int) -> int:
     """Test only: withhold one hand-over flag of the chained prep and set the wait limit."""
     return _lib.dr_set_chain_fault_for_testing(int(withhold_flag), int(wait_ns))
+
+
+def dr_chunk_bwd(q, k, v, log_alpha, params: DrParams, variant: int, eps: float, init_state,
+                 d_out, d_final_state, dq, dk, dv, d_log_alpha, d_eta, d_init_state, B: int,
+                 T: int, H: int, dk_: int, dv_: int, chunk: int, stream=None) -> int:
+    return _lib.dr_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), ctypes.byref(params),
+                             int(variant), float(eps), _ptr(init_state), _ptr(d_out),
+                             _ptr(d_final_state), _ptr(dq), _ptr(dk), _ptr(dv),
+                             _ptr(d_log_alpha), _ptr(d_eta), _ptr(d_init_state), B, T, H, dk_,
+                             dv_, chunk, _stream(stream))
+
+
+def dr_chunk_bwd_workspace_bytes(variant, dtype, B, T, H, dk, dv, chunk) -> int:
+    return _lib.dr_chunk_bwd_workspace_bytes(variant, dtype, B, T, H, dk, dv, chunk)

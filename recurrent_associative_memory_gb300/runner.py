@@ -85,3 +85,43 @@ def decode_step(inp: dict, state, aux_state=None, out=None, stream=None, check_f
                            inp.get("eps", 1e-6), state, aux_state, out, B, H, dk, dv, stream)
     dr.check(st, "dr_decode_step")
     return out
+
+
+def bwd_workspace_for(inp: dict, chunk=None):
+    """Device scratch for dr_chunk_bwd on these inputs (None where unsupported)."""
+    q, k, v = inp["q"], inp["k"], inp["v"]
+    B, T, H, dk = k.shape
+    dtype = dr.DR_BF16 if q.dtype == torch.bfloat16 else dr.DR_FP32
+    n = dr.dr_chunk_bwd_workspace_bytes(dr.VARIANT_IDS[inp["variant"]], dtype, B, T, H, dk,
+                                        v.shape[-1], chunk or inp.get("chunk", 64))
+    return torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+
+
+def chunk_bwd(inp: dict, d_out, *, d_final_state=None, init_state=None, want_dS0=True,
+              chunk=None, stream=None, workspace="auto", grads=None):
+    """Run dr_chunk_bwd on a device input dict; returns a dict of fp32 gradients
+    (dq, dk, dv, dlog_alpha, deta and, with want_dS0, dS0).  ``grads`` may hold
+    preallocated output tensors under the same names."""
+    q, k, v = inp["q"], inp["k"], inp["v"]
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    if isinstance(workspace, str):
+        workspace = bwd_workspace_for(inp, chunk)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    g = dict(grads or {})
+    g.setdefault("dq", torch.empty(B, T, H, dk, **f32))
+    g.setdefault("dk", torch.empty(B, T, H, dk, **f32))
+    g.setdefault("dv", torch.empty(B, T, H, dv, **f32))
+    g.setdefault("dlog_alpha", torch.empty(B, T, H, **f32))
+    g.setdefault("deta", torch.empty(B, T, H, **f32))
+    if want_dS0:
+        g.setdefault("dS0", torch.empty(B, H, dk, dv, **f32))
+    p = params_for(inp)
+    if workspace is not None:
+        p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    st = dr.dr_chunk_bwd(q, k, v, inp["log_alpha"], p, dr.VARIANT_IDS[inp["variant"]],
+                         inp.get("eps", 1e-6), init_state, d_out, d_final_state, g["dq"], g["dk"],
+                         g["dv"], g["dlog_alpha"], g["deta"], g.get("dS0"), B, T, H, dk, dv,
+                         chunk or inp.get("chunk", 64), stream)
+    dr.check(st, "dr_chunk_bwd")
+    return g

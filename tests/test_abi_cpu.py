@@ -172,3 +172,34 @@ def test_chunk_fwd_workspace_checks(dr):
     base = dict(dtype=dr.DR_BF16, dk=128, dv=128)
     assert fwd(dr, workspace=A, workspace_bytes=need - 16, **base) == dr.DR_ERR_WORKSPACE
     assert fwd(dr, workspace=A + 16, workspace_bytes=need, **base) == dr.DR_ERR_ALIGN
+
+
+def test_backward_refusals_and_workspace_size(dr):
+    """dr_chunk_bwd: argument checks before any launch, the supported shapes, and
+    the workspace it asks for (the forward's record plus the saved per-chunk data)."""
+    A = 1 << 20
+    p = dr.make_params(dtype=dr.DR_BF16, eta=A)
+
+    def call(variant=None, B=1, T=64, H=1, d=128, chunk=64, params=None, dq=A, ws=None):
+        pp = params or p
+        if ws is not None:
+            pp.workspace, pp.workspace_bytes = ws
+        return dr.dr_chunk_bwd(A, A, A, A, pp, dr.DR_KLA if variant is None else variant, 1e-6,
+                               None, A, None, dq, A, A, A, A, None, B, T, H, d, d, chunk,
+                               stream=0)
+
+    assert call(dq=None) == dr.DR_ERR_NULL
+    assert call(T=0) == dr.DR_ERR_SHAPE
+    assert call(chunk=48) == dr.DR_ERR_SHAPE
+    assert call(variant=dr.DR_PGDN, params=dr.make_params(dtype=dr.DR_BF16, eta=A, alphaP=A,
+                                                          betaP=A, mu=A)) == dr.DR_ERR_UNSUPPORTED
+    assert call(d=64) == dr.DR_ERR_UNSUPPORTED
+    assert call(chunk=32) == dr.DR_ERR_UNSUPPORTED
+    assert call(params=dr.make_params(dtype=dr.DR_FP32, eta=A)) == dr.DR_ERR_UNSUPPORTED
+    assert call() == dr.DR_ERR_WORKSPACE                                # no workspace
+    need = dr.dr_chunk_bwd_workspace_bytes(dr.DR_KLA, dr.DR_BF16, 2, 130, 3, 128, 128, 64)
+    per_rec = 66560 + 4 * (16384 + 8192 + 16384 + 8192 + 4096 + 4096 + 1)
+    assert need == -(-(2 * 3 * 3 * per_rec) // 256) * 256
+    assert call(ws=(A, 1000)) == dr.DR_ERR_WORKSPACE
+    assert call(ws=(A + 16, 1 << 30)) == dr.DR_ERR_ALIGN
+    assert dr.dr_chunk_bwd_workspace_bytes(dr.DR_PGDN, dr.DR_BF16, 1, 64, 1, 128, 128, 64) == 0
