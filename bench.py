@@ -88,6 +88,7 @@ def parse(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-configs", action="store_true")
+    p.add_argument("--no-backward", action="store_true")
     p.add_argument("--cpu-sample-heads", type=int, default=8)
     p.add_argument("--cpu-sample-reps", type=int, default=10)
     return p.parse_args(argv)
@@ -170,6 +171,16 @@ def fwd_bytes(wl, variant, with_final=True):
     if with_final:
         total += wl.B * wl.H * (wl.dk * wl.dv + aux_elems(variant, wl.dk)) * 4
     return total
+
+
+def bwd_bytes(wl):
+    """Bytes one backward call must move: q, k, v and dL/do in (the input dtype) and
+    the two gates; dq, dk, dv (fp32), d log alpha and d eta out; the initial state
+    and dL/dS_T in, dL/dS_0 out."""
+    el = 2 if wl.dtype == "bf16" else 4
+    ht = wl.B * wl.T * wl.H
+    per_ht = (2 * wl.dk + 2 * wl.dv) * el + 8 + (2 * wl.dk + wl.dv) * 4 + 8
+    return ht * per_ht + 3 * wl.B * wl.H * wl.dk * wl.dv * 4
 
 
 def decode_bytes(wl, variant="kla"):
@@ -294,6 +305,19 @@ def _oracle_timed(job):
     t0 = time.perf_counter()
     _oracle_call(inp, variant)
     return time.perf_counter() - t0
+
+
+def _oracle_bwd_parity(job):
+    """Worker: the oracle's reverse sweep (every gradient) for one sliced row."""
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    import numpy as np
+    from oracle import backward as obw
+    tag, inp, variant, dO, dS, S0 = job
+    f = lambda t: None if t is None else np.asarray(t, dtype=np.float64)  # noqa: E731
+    g = obw.tokenwise_backward(f(inp["q"]), f(inp["k"]), f(inp["v"]), f(inp["log_alpha"]),
+                               variant, f(dO), f(dS), eta=f(inp["eta"]), eps=inp["eps"],
+                               q_l2norm=inp["q_l2norm"], k_l2norm=inp["k_l2norm"], S0=f(S0))
+    return tag, {k: g[k] for k in ("dq", "dk", "dv", "dlog_alpha", "deta", "dS0")}
 
 
 def _oracle_parity(job):
@@ -550,6 +574,61 @@ def forward_entry(fw, var_ms, pk, launches):
             "dtype": wl.dtype, "variants": per, "launches_per_step": launches}
 
 
+BWD_GRADS = ("dq", "dk", "dv", "dlog_alpha", "deta", "dS0")
+
+
+def time_backward(torch, dr, runner, fw, steps, stream, flush, pk, pool_submit):
+    """dr_chunk_bwd on a forward workload's inputs (every variant it lists that the
+    backward supports): CUDA-event time per call, L2 flushed between calls; oracle
+    jobs for two sampled (b, h) rows per variant.  Returns (entry, gpu rows)."""
+    wl = fw.wl
+    gen = torch.Generator().manual_seed(wl.seed + 500)
+    dO = torch.randn(wl.B, wl.T, wl.H, wl.dv, generator=gen).to(fw.host[fw.variants[0]]["q"].dtype)
+    dS = 0.1 * torch.randn(wl.B, wl.H, wl.dk, wl.dv, generator=gen)
+    S0 = 0.3 * torch.randn(wl.B, wl.H, wl.dk, wl.dv, generator=gen)
+    dOd, dSd, S0d = dO.cuda(), dS.cuda(), S0.cuda()
+    entry, rows = {"workload": wl.name, "variants": {}}, {}
+    pairs = sampled_pairs(wl.B, wl.H, 2)
+    for v in fw.variants:
+        ws = runner.bwd_workspace_for(fw.dev[v])
+        if ws is None:
+            continue
+        grads = runner.chunk_bwd(fw.dev[v], dOd, d_final_state=dSd, init_state=S0d,
+                                 workspace=ws, stream=stream)
+        for _ in range(2):
+            runner.chunk_bwd(fw.dev[v], dOd, d_final_state=dSd, init_state=S0d, workspace=ws,
+                             stream=stream, grads=grads)
+        torch.cuda.synchronize()
+        dr.check(dr.dr_get_device_status(), "backward warm-up")
+        E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+        ev = [(E(), E()) for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            runner.chunk_bwd(fw.dev[v], dOd, d_final_state=dSd, init_state=S0d, workspace=ws,
+                             stream=stream, grads=grads)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        dr.check(dr.dr_get_device_status(), "backward")
+        ms = statistics.mean(s_.elapsed_time(e_) for s_, e_ in ev)
+        byt = bwd_bytes(wl)
+        entry["variants"][v] = {"ms": ms, "tokens_per_s": wl.B * wl.T / (ms / 1e3),
+                                "algorithmic_bytes": byt, "gbs": byt / (ms / 1e3) / 1e9,
+                                "frac": byt / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                                "launches_per_call": 5}
+        for b, h in pairs:
+            rows[(v, b, h)] = {n: (grads[n][b, h] if n == "dS0" else grads[n][b, :, h])
+                               .double().cpu().numpy() for n in BWD_GRADS}
+            pool_submit([((v, b, h), slice_row(fw.host[v], b, h), v,
+                          dO[b:b + 1, :, h:h + 1].float().numpy(),
+                          dS[b:b + 1, h:h + 1].numpy(), S0[b:b + 1, h:h + 1].numpy())])
+        del ws
+    entry["parity_sample"] = f"{len(pairs)} (b, h) rows per variant"
+    entry["kernels"] = ("forward prep + carry (saving chunk-start states and E), reverse "
+                        "carry, per-chunk state products, per-chunk local gradients")
+    return entry, rows
+
+
 def decode_setup(torch, runner, W, wl, variant, n_pool=8):
     """Device inputs for n_pool decode steps, a state and the gain state."""
     steps = [W.generate_decode_step(wl, s, variant) for s in range(n_pool)]
@@ -651,6 +730,12 @@ def main(argv=None):
         if pool is not None and not args.no_configs:
             parity_async.append(pool.map_async(_oracle_parity, jobs, chunksize=1))
 
+    bwd_async = []
+
+    def submit_bwd(jobs):
+        if pool is not None and not args.no_configs:
+            bwd_async.append(pool.map_async(_oracle_bwd_parity, jobs, chunksize=1))
+
     # ---------------- headline workload: the timed region
     wl = W.WORKLOADS[args.workload]
     head = Forward(torch, dr, runner, W, wl)
@@ -691,6 +776,15 @@ def main(argv=None):
               "roofline": roof, "variants": entry["variants"], "gpu_launches": launches,
               "clocks": clk}
     configs = {}
+
+    # ---------------- the backward (GDN and KLA) on the headline workload
+    bwd_rows = None
+    if not args.no_backward:
+        bent, bwd_rows = time_backward(torch, dr, runner, head, min(args.steps, 20), stream,
+                                       flush, pk, submit_bwd)
+        if bent["variants"]:
+            result["backward"] = bent
+        torch.cuda.empty_cache()
 
     # ---------------- every configuration's workload, timed the same way
     if not args.no_configs:
@@ -821,6 +915,15 @@ def main(argv=None):
                     worst["out"] = max(worst["out"], rel_err(go, o[0, :, 0]))
                     worst["state"] = max(worst["state"], rel_err(gS, S[0, 0]))
             configs["4b"]["parity"] = worst
+    if bwd_async and "backward" in result:
+        worst = {n: 0.0 for n in BWD_GRADS}
+        for a_ in bwd_async:
+            for tag, ref in a_.get():
+                gpu = bwd_rows[tag]
+                for n in BWD_GRADS:
+                    r = ref[n][0, 0] if n == "dS0" else ref[n][0, :, 0]
+                    worst[n] = max(worst[n], rel_err(gpu[n], r))
+        result["backward"]["parity"] = worst
     for c in configs.values():
         c.pop("_fw", None)
     if configs:

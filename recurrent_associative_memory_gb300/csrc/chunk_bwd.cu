@@ -75,19 +75,27 @@ BwdWs bwd_ws(void* base, long n) {
   return w;
 }
 
-// ---- warp-level 16 x 8 tile of op(A) op(B) over K = 8 KSTEPS, fp32 operands split
-// into two TF32 terms each (hi + lo) and three products: fp32-accurate.
+// ---- warp-level tensor-core products, fp32 operands split into two TF32 terms each
+// (hi + lo) and three products: fp32-accurate.
 // A element (m, k) = TA ? A[k lda + m] : A[m lda + k];
 // B element (k, n) = TB ? B[n ldb + k] : B[k ldb + n].
-template <int KSTEPS, bool TA, bool TB>
-__device__ __forceinline__ void mm3(float (&d)[4], const float* A, int lda, const float* B, int ldb,
-                                    int lane) {
+// NT tiles side by side: D_j (16 x 8) += op(A)[16 x 8K] op(B)[8K x 8] at B columns
+// 8 j .. 8 j + 8.  The A fragment is split once per k-step for all NT tiles, and each
+// tile keeps its three products in separate accumulators, so 3 NT independent chains
+// are in flight per warp.
+template <int NT, int KSTEPS, bool TA, bool TB>
+__device__ __forceinline__ void mm3x(float (&d)[NT][4], const float* A, int lda, const float* B,
+                                     int ldb, int lane) {
   const int g = lane >> 2, t = lane & 3;
-  float dc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
+  float c1[NT][4], c2[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c1[j][i] = c2[j][i] = 0.f;
+#pragma unroll 2
   for (int ks = 0; ks < KSTEPS; ++ks) {
     const int k0 = 8 * ks;
-    float af[4], bf[2];
+    float af[4];
     if (TA) {
       af[0] = A[(k0 + t) * lda + g];
       af[1] = A[(k0 + t) * lda + g + 8];
@@ -99,49 +107,50 @@ __device__ __forceinline__ void mm3(float (&d)[4], const float* A, int lda, cons
       af[2] = A[g * lda + k0 + t + 4];
       af[3] = A[(g + 8) * lda + k0 + t + 4];
     }
-    if (TB) {
-      bf[0] = B[g * ldb + k0 + t];
-      bf[1] = B[g * ldb + k0 + t + 4];
-    } else {
-      bf[0] = B[(k0 + t) * ldb + g];
-      bf[1] = B[(k0 + t + 4) * ldb + g];
-    }
-    uint32_t ah[4], al[4], bh[2], bl[2];
+    uint32_t ah[4], al[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       ah[i] = to_tf32(af[i]);
       al[i] = to_tf32(af[i] - __uint_as_float(ah[i]));
     }
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      bh[i] = to_tf32(bf[i]);
-      bl[i] = to_tf32(bf[i] - __uint_as_float(bh[i]));
+    for (int j = 0; j < NT; ++j) {
+      float bf[2];
+      if (TB) {
+        bf[0] = B[(8 * j + g) * ldb + k0 + t];
+        bf[1] = B[(8 * j + g) * ldb + k0 + t + 4];
+      } else {
+        bf[0] = B[(k0 + t) * ldb + 8 * j + g];
+        bf[1] = B[(k0 + t + 4) * ldb + 8 * j + g];
+      }
+      uint32_t bh[2], bl[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        bh[i] = to_tf32(bf[i]);
+        bl[i] = to_tf32(bf[i] - __uint_as_float(bh[i]));
+      }
+      mma_tf32(d[j], ah, bh);
+      mma_tf32(c1[j], al, bh);
+      mma_tf32(c2[j], ah, bl);
     }
-    mma_tf32(dc, al, bh);
-    mma_tf32(dc, ah, bl);
-    mma_tf32(d, ah, bh);
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) d[i] += dc[i];
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[j][i] += c1[j][i] + c2[j][i];
 }
 
 // fragment element e of a 16 x 8 tile: row and column within the tile
 __device__ __forceinline__ int frag_row(int lane, int e) { return (lane >> 2) + ((e >> 1) << 3); }
 __device__ __forceinline__ int frag_col(int lane, int e) { return 2 * (lane & 3) + (e & 1); }
 
-// 8 bf16 from global (16-byte aligned) -> float
-__device__ __forceinline__ void ld8(const __nv_bfloat16* p, float (&f)[8]) {
-  unpack8(*reinterpret_cast<const uint4*>(p), f);
+// 16-byte asynchronous copy global -> shared; src_bytes 0 fills zeros
+__device__ __forceinline__ void cpa16(void* dst, const void* src, int src_bytes = 16) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(umma::smem_u32(dst)),
+               "l"(src), "r"(src_bytes)
+               : "memory");
 }
-
-// One element of a 64 x 64 hi/lo bf16 tile image (128B-swizzled rows) of a record
-__device__ __forceinline__ void tile_row8(const uint8_t* img, int row, int col0, float (&f)[8]) {
-  float h[8], l[8];
-  unpack8(*reinterpret_cast<const uint4*>(img + umma::sw128_offset(row, col0)), h);
-  unpack8(*reinterpret_cast<const uint4*>(img + 8192 + umma::sw128_offset(row, col0)), l);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) f[e] = h[e] + l[e];
-}
+__device__ __forceinline__ void cpa_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ long tok(const FwdArgs& a, int b, int t, int h) {
   return ((long)b * a.T + t) * a.H + h;
@@ -192,10 +201,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int r = e >> 5, n = e & 31;
     sdS[r * cLDN + n] = g.dS_final ? g.dS_final[((size_t)bh * 128 + r) * 128 + 32 * cb + n] : 0.f;
   }
+  // The next chunk's raw operands (P and T tile images, K and Q rows, dO, the
+  // record's row vectors) are fetched into registers while this chunk computes.
+  uint4 rPT[2][4], rK[4], rQ[4], rO;
+  float rU[4], rEq[4], rEk[4], rG = 0.f;
+  auto fetch = [&](int c) {
+    const uint8_t* rec = g.w.rec + ((size_t)bh * NC + c) * kRecF;
+    const float* rv = reinterpret_cast<const float*>(rec + rVecF);
+    const int t0 = 64 * c, Cc = min(64, a.T - t0);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int e = tid + r * kBwdThreads, i = e >> 3, c0 = 8 * (e & 7);
+      const uint32_t off = umma::sw128_offset(i, c0);
+      rPT[r][0] = *reinterpret_cast<const uint4*>(rec + rPF + off);
+      rPT[r][1] = *reinterpret_cast<const uint4*>(rec + rPF + 8192 + off);
+      rPT[r][2] = *reinterpret_cast<const uint4*>(rec + rTF + off);
+      rPT[r][3] = *reinterpret_cast<const uint4*>(rec + rTF + 8192 + off);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
+      const bool live = j < Cc;
+      rK[r] = live ? *reinterpret_cast<const uint4*>(K + tok(a, b, t0 + j, h) * 128 + c0)
+                   : make_uint4(0u, 0u, 0u, 0u);
+      rQ[r] = live ? *reinterpret_cast<const uint4*>(Q + tok(a, b, t0 + j, h) * 128 + c0)
+                   : make_uint4(0u, 0u, 0u, 0u);
+      rU[r] = rv[64 + j];
+      rEq[r] = rv[j];
+      rEk[r] = rv[192 + j];
+    }
+    {
+      const int i = tid >> 2, c0 = 8 * (tid & 3);
+      rO = i < Cc ? *reinterpret_cast<const uint4*>(dO + tok(a, b, t0 + i, h) * 128 + 32 * cb + c0)
+                  : make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (tid == 0) rG = rv[128];
+  };
+  fetch(NC - 1);
   for (int c = NC - 1; c >= 0; --c) {
     const size_t ri = (size_t)bh * NC + c;
-    const uint8_t* rec = g.w.rec + ri * kRecF;
-    const float* rv = reinterpret_cast<const float*>(rec + rVecF);
     const int t0 = 64 * c, Cc = min(64, a.T - t0);
     __syncthreads();   // the previous chunk's readers of every buffer are done
     // ---- dS_{c+1} for the local gradients
@@ -204,90 +248,88 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int r = e >> 5, n = e & 31;
       sv[r * 128 + 32 * cb + n] = sdS[r * cLDN + n];
     }
-    // ---- operands: P and T from the record images, K and Q rows scaled, dO
-    for (int e = tid; e < 64 * 8; e += kBwdThreads) {
-      const int i = e >> 3, c0 = 8 * (e & 7);
-      float f[8];
-      tile_row8(rec + rPF, i, c0, f);
+    // ---- operands from the registers: P and T (hi + lo), K and Q rows scaled, dO
 #pragma unroll
-      for (int q = 0; q < 8; ++q) sP[i * cLD64T + c0 + q] = f[q];
-      tile_row8(rec + rTF, i, c0, f);
+    for (int r = 0; r < 2; ++r) {
+      const int e = tid + r * kBwdThreads, i = e >> 3, c0 = 8 * (e & 7);
+      float hh[8], ll[8];
+      unpack8(rPT[r][0], hh);
+      unpack8(rPT[r][1], ll);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) sT[i * cLD64T + c0 + q] = f[q];
+      for (int q = 0; q < 8; ++q) sP[i * cLD64T + c0 + q] = hh[q] + ll[q];
+      unpack8(rPT[r][2], hh);
+      unpack8(rPT[r][3], ll);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sT[i * cLD64T + c0 + q] = hh[q] + ll[q];
     }
-    for (int e = tid; e < 64 * 16; e += kBwdThreads) {
-      const int j = e >> 4, c0 = 8 * (e & 15);
-      float kf[8], qf[8];
-      if (j < Cc) {
-        ld8(K + tok(a, b, t0 + j, h) * 128 + c0, kf);
-        ld8(Q + tok(a, b, t0 + j, h) * 128 + c0, qf);
-      } else {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) kf[q] = qf[q] = 0.f;
-      }
-      const float u = rv[64 + j], eqn = rv[j], ekc = rv[192 + j];
+    for (int r = 0; r < 4; ++r) {
+      const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
+      float kf[8], qf[8];
+      unpack8(rK[r], kf);
+      unpack8(rQ[r], qf);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        sWb[j * cLDW + c0 + q] = u * kf[q];
-        sKg[j * cLDQ + c0 + q] = ekc * kf[q];
-        sQg[j * cLDQ + c0 + q] = eqn * qf[q];
+        sWb[j * cLDW + c0 + q] = rU[r] * kf[q];
+        sKg[j * cLDQ + c0 + q] = rEk[r] * kf[q];
+        sQg[j * cLDQ + c0 + q] = rEq[r] * qf[q];
       }
     }
     {
       const int i = tid >> 2, c0 = 8 * (tid & 3);
       float f[8];
-      if (i < Cc) {
-        ld8(dO + tok(a, b, t0 + i, h) * 128 + 32 * cb + c0, f);
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) f[q] = 0.f;
-      }
+      unpack8(rO, f);
 #pragma unroll
       for (int q = 0; q < 8; ++q) sdO[i * cLDN + c0 + q] = f[q];
     }
-    if (tid == 0) s_gamma = rv[128];
+    if (tid == 0) s_gamma = rG;
+    if (c > 0) fetch(c - 1);
     __syncthreads();
-    // ---- dE = P^T dO + Wbar dS  (64 x 32: 16 tiles, two per warp)
-    const int mt = warp >> 1;
+    // warps 0-3: row tile `warp` of dE / dR (all 32 columns); the dS rows below
+    // are spread over all eight warps
+    if (warp < 4) {
+      float d[4][4] = {};
+      mm3x<4, 8, true, false>(d, sP + 16 * warp, cLD64T, sdO, cLDN, lane);
+      mm3x<4, 16, false, false>(d, sWb + 16 * warp * cLDW, cLDW, sdS, cLDN, lane);
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      const int nt = 2 * (warp & 1) + s;
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      mm3<8, true, false>(d, sP + 16 * mt, cLD64T, sdO + 8 * nt, cLDN, lane);
-      mm3<16, false, false>(d, sWb + 16 * mt * cLDW, cLDW, sdS + 8 * nt, cLDN, lane);
+      for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        sdE[(16 * mt + frag_row(lane, e)) * cLDN + 8 * nt + frag_col(lane, e)] = d[e];
+        for (int e = 0; e < 4; ++e)
+          sdE[(16 * warp + frag_row(lane, e)) * cLDN + 8 * nt + frag_col(lane, e)] = d[nt][e];
     }
     __syncthreads();
     // ---- dR = T^T dE, also dV
+    if (warp < 4) {
+      float d[4][4] = {};
+      mm3x<4, 8, true, false>(d, sT + 16 * warp, cLD64T, sdE, cLDN, lane);
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      const int nt = 2 * (warp & 1) + s;
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      mm3<8, true, false>(d, sT + 16 * mt, cLD64T, sdE + 8 * nt, cLDN, lane);
+      for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = 16 * mt + frag_row(lane, e), n = 8 * nt + frag_col(lane, e);
-        sdR[i * cLDN + n] = d[e];
-        if (i < Cc) g.dv[tok(a, b, t0 + i, h) * 128 + 32 * cb + n] = d[e];
-      }
+        for (int e = 0; e < 4; ++e) {
+          const int i = 16 * warp + frag_row(lane, e), n = 8 * nt + frag_col(lane, e);
+          sdR[i * cLDN + n] = d[nt][e];
+          if (i < Cc) g.dv[tok(a, b, t0 + i, h) * 128 + 32 * cb + n] = d[nt][e];
+        }
     }
     __syncthreads();
     // ---- dS_c = gamma dS + (Gamma.Q^)^T dO - (Gamma.K^)^T dR (warp: rows 16 warp .. + 16)
-    const float gam = s_gamma;
+    {
+      const float gam = s_gamma;
+      float d[4][4], m[4][4] = {};
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      float d[4], m[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        d[e] = gam * sdS[(16 * warp + frag_row(lane, e)) * cLDN + 8 * nt + frag_col(lane, e)];
-      mm3<8, true, false>(d, sQg + 16 * warp, cLDQ, sdO + 8 * nt, cLDN, lane);
-      mm3<8, true, false>(m, sKg + 16 * warp, cLDQ, sdR + 8 * nt, cLDN, lane);
+        for (int e = 0; e < 4; ++e)
+          d[nt][e] = gam * sdS[(16 * warp + frag_row(lane, e)) * cLDN + 8 * nt + frag_col(lane, e)];
+      mm3x<4, 8, true, false>(d, sQg + 16 * warp, cLDQ, sdO, cLDN, lane);
+      mm3x<4, 8, true, false>(m, sKg + 16 * warp, cLDQ, sdR, cLDN, lane);
       __syncwarp();
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        sdS[(16 * warp + frag_row(lane, e)) * cLDN + 8 * nt + frag_col(lane, e)] = d[e] - m[e];
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          sdS[(16 * warp + frag_row(lane, e)) * cLDN + 8 * nt + frag_col(lane, e)] =
+              d[nt][e] - m[nt][e];
     }
   }
   __syncthreads();
@@ -323,77 +365,88 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const float* dSc = g.w.dS + (size_t)task * 16384;
   const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(g.d_out);
 
-  for (int e = tid; e < 128 * 32; e += kBwdThreads) {
-    const int r = e >> 5, c4 = 4 * (e & 31);
-    *reinterpret_cast<float4*>(sS + r * cLDS + c4) = *reinterpret_cast<const float4*>(Sc + r * 128 + c4);
-  }
-  for (int e = tid; e < 64 * 32; e += kBwdThreads) {
-    const int i = e >> 5, c4 = 4 * (e & 31);
-    float4 r4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (i < Cc) r4 = *reinterpret_cast<const float4*>(g.dv + tok(a, b, t0 + i, h) * 128 + c4);
-    *reinterpret_cast<float4*>(sdR + i * cLDS + c4) = r4;
-    *reinterpret_cast<float4*>(sE + i * cLDS + c4) = *reinterpret_cast<const float4*>(Ec + i * 128 + c4);
-  }
-  for (int e = tid; e < 64 * 16; e += kBwdThreads) {
-    const int i = e >> 4, c0 = 8 * (e & 15);
-    float f[8];
-    if (i < Cc) {
-      ld8(dO + tok(a, b, t0 + i, h) * 128 + c0, f);
-    } else {
+  {   // dO rows (bf16) into registers first, the fp32 blocks by asynchronous copies
+    uint4 raw[4];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) f[q] = 0.f;
+    for (int r = 0; r < 4; ++r) {
+      const int e = tid + r * kBwdThreads, i = e >> 4, c0 = 8 * (e & 15);
+      raw[r] = i < Cc ? *reinterpret_cast<const uint4*>(dO + tok(a, b, t0 + i, h) * 128 + c0)
+                      : make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (int e = tid; e < 128 * 32; e += kBwdThreads) {
+      const int r = e >> 5, c4 = 4 * (e & 31);
+      cpa16(sS + r * cLDS + c4, Sc + r * 128 + c4);
+    }
+    for (int e = tid; e < 64 * 32; e += kBwdThreads) {
+      const int i = e >> 5, c4 = 4 * (e & 31);
+      cpa16(sdR + i * cLDS + c4, g.dv + tok(a, b, t0 + min(i, Cc - 1), h) * 128 + c4,
+            i < Cc ? 16 : 0);
+      cpa16(sE + i * cLDS + c4, Ec + i * 128 + c4);
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) sdO[i * cLDS + c0 + q] = f[q];
+    for (int r = 0; r < 4; ++r) {
+      const int e = tid + r * kBwdThreads, i = e >> 4, c0 = 8 * (e & 15);
+      float f[8];
+      unpack8(raw[r], f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sdO[i * cLDS + c0 + q] = f[q];
+    }
+    cpa_wait_all();
   }
   __syncthreads();
   // X_Q = dO S_c^T -> dq, X_K = dR S_c^T -> dk (raw; bwd_local scales and adds)
   // 64 x 128 each: 64 tiles, eight per warp (m tile = warp & 3, n tiles 8 (warp >> 2) .. + 8)
   {
     const int mt = warp & 3;
-    for (int s = 0; s < 8; ++s) {
-      const int nt = 8 * (warp >> 2) + s;
-      float dq4[4] = {0.f, 0.f, 0.f, 0.f}, dk4[4] = {0.f, 0.f, 0.f, 0.f};
-      mm3<16, false, true>(dq4, sdO + 16 * mt * cLDS, cLDS, sS + 8 * nt * cLDS, cLDS, lane);
-      mm3<16, false, true>(dk4, sdR + 16 * mt * cLDS, cLDS, sS + 8 * nt * cLDS, cLDS, lane);
+    for (int s = 0; s < 2; ++s) {
+      const int nt0 = 8 * (warp >> 2) + 4 * s;
+      float dq4[4][4] = {}, dk4[4][4] = {};
+      mm3x<4, 16, false, true>(dq4, sdO + 16 * mt * cLDS, cLDS, sS + 8 * nt0 * cLDS, cLDS, lane);
+      mm3x<4, 16, false, true>(dk4, sdR + 16 * mt * cLDS, cLDS, sS + 8 * nt0 * cLDS, cLDS, lane);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = 16 * mt + frag_row(lane, e), n = 8 * nt + frag_col(lane, e);
-        if (i < Cc) {
-          g.dq[tok(a, b, t0 + i, h) * 128 + n] = dq4[e];
-          g.dk[tok(a, b, t0 + i, h) * 128 + n] = dk4[e];
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 16 * mt + frag_row(lane, e), n = 8 * (nt0 + j) + frag_col(lane, e);
+          if (i < Cc) {
+            g.dq[tok(a, b, t0 + i, h) * 128 + n] = dq4[j][e];
+            g.dk[tok(a, b, t0 + i, h) * 128 + n] = dk4[j][e];
+          }
         }
-      }
     }
   }
   // dP = dO E^T and dR E^T (64 x 64: 32 tiles, four per warp)
   {
     float* xp = g.w.dP + (size_t)task * 4096;
     float* xl = g.w.dL + (size_t)task * 4096;
-    const int mt = warp & 3;
-    for (int s = 0; s < 4; ++s) {
-      const int nt = 4 * (warp >> 2) + s;
-      float p4[4] = {0.f, 0.f, 0.f, 0.f}, l4[4] = {0.f, 0.f, 0.f, 0.f};
-      mm3<16, false, true>(p4, sdO + 16 * mt * cLDS, cLDS, sE + 8 * nt * cLDS, cLDS, lane);
-      mm3<16, false, true>(l4, sdR + 16 * mt * cLDS, cLDS, sE + 8 * nt * cLDS, cLDS, lane);
+    const int mt = warp & 3, nt0 = 4 * (warp >> 2);
+    float p4[4][4] = {}, l4[4][4] = {};
+    mm3x<4, 16, false, true>(p4, sdO + 16 * mt * cLDS, cLDS, sE + 8 * nt0 * cLDS, cLDS, lane);
+    mm3x<4, 16, false, true>(l4, sdR + 16 * mt * cLDS, cLDS, sE + 8 * nt0 * cLDS, cLDS, lane);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int i = 16 * mt + frag_row(lane, e), j = 8 * nt + frag_col(lane, e);
-        xp[i * 64 + j] = p4[e];
-        xl[i * 64 + j] = l4[e];
+        const int i = 16 * mt + frag_row(lane, e), j = 8 * (nt0 + q) + frag_col(lane, e);
+        xp[i * 64 + j] = p4[q][e];
+        xl[i * 64 + j] = l4[q][e];
       }
-    }
   }
   __syncthreads();
-  // dS_{c+1} in place of S_c, and gamma <dS, S_c> on the way
+  // dS_{c+1} over the dO and dR rows (both read by now); gamma <dS, S_c>
+  float* sD = sdO;                 // [128][cLDS]: the dO and dR buffers, contiguous
+  for (int e = tid; e < 128 * 32; e += kBwdThreads) {
+    const int r = e >> 5, c4 = 4 * (e & 31);
+    cpa16(sD + r * cLDS + c4, dSc + r * 128 + c4);
+  }
+  cpa_wait_all();
+  __syncthreads();
   float part = 0.f;
   for (int e = tid; e < 128 * 32; e += kBwdThreads) {
     const int r = e >> 5, c4 = 4 * (e & 31);
-    const float4 x = *reinterpret_cast<const float4*>(dSc + r * 128 + c4);
-    float4* s4 = reinterpret_cast<float4*>(sS + r * cLDS + c4);
-    const float4 y = *s4;
+    const float4 x = *reinterpret_cast<const float4*>(sD + r * cLDS + c4);
+    const float4 y = *reinterpret_cast<const float4*>(sS + r * cLDS + c4);
     part += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
-    *s4 = x;
   }
   part = warp_sum(part);
   if (lane == 0) s_red[warp] = part;
@@ -408,15 +461,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   {
     float* xw = g.w.XW + (size_t)task * 8192;
     const int mt = warp & 3;
-    for (int s = 0; s < 8; ++s) {
-      const int nt = 8 * (warp >> 2) + s;
-      float w4[4] = {0.f, 0.f, 0.f, 0.f};
-      mm3<16, false, true>(w4, sE + 16 * mt * cLDS, cLDS, sS + 8 * nt * cLDS, cLDS, lane);
+    for (int s = 0; s < 2; ++s) {
+      const int nt0 = 8 * (warp >> 2) + 4 * s;
+      float w4[4][4] = {};
+      mm3x<4, 16, false, true>(w4, sE + 16 * mt * cLDS, cLDS, sD + 8 * nt0 * cLDS, cLDS, lane);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = 16 * mt + frag_row(lane, e), n = 8 * nt + frag_col(lane, e);
-        xw[i * 128 + n] = w4[e];
-      }
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 16 * mt + frag_row(lane, e), n = 8 * (nt0 + j) + frag_col(lane, e);
+          xw[i * 128 + n] = w4[j][e];
+        }
     }
   }
 }
@@ -449,21 +504,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
   const __nv_bfloat16* Qp = static_cast<const __nv_bfloat16*>(a.q);
 
-  // ---- raw rows, norms, gates
-  for (int e = tid; e < 64 * 16; e += kBwdThreads) {
-    const int j = e >> 4, c0 = 8 * (e & 15);
-    float kf[8], qf[8];
-    if (j < Cc) {
-      ld8(K + tok(a, b, t0 + j, h) * 128 + c0, kf);
-      ld8(Qp + tok(a, b, t0 + j, h) * 128 + c0, qf);
-    } else {
+  // ---- raw rows (bf16, all loads in flight first), dO E^T and dR E^T by
+  //      asynchronous copies into the M_P / M_L buffers, norms, gates
+  {
+    uint4 rk[4], rq[4];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) kf[q] = qf[q] = 0.f;
+    for (int r = 0; r < 4; ++r) {
+      const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
+      const bool live = j < Cc;
+      rk[r] = live ? *reinterpret_cast<const uint4*>(K + tok(a, b, t0 + j, h) * 128 + c0)
+                   : make_uint4(0u, 0u, 0u, 0u);
+      rq[r] = live ? *reinterpret_cast<const uint4*>(Qp + tok(a, b, t0 + j, h) * 128 + c0)
+                   : make_uint4(0u, 0u, 0u, 0u);
+    }
+    const float* xp = g.w.dP + (size_t)task * 4096;
+    const float* xl = g.w.dL + (size_t)task * 4096;
+    for (int e = tid; e < 64 * 16; e += kBwdThreads) {
+      const int i = e >> 4, c4 = 4 * (e & 15);
+      cpa16(sMP + i * cLDM + c4, xp + i * 64 + c4);
+      cpa16(sML + i * cLDM + c4, xl + i * 64 + c4);
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      sK[j * cLDK + c0 + q] = kf[q];
-      sQ[j * cLDK + c0 + q] = qf[q];
+    for (int r = 0; r < 4; ++r) {
+      const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
+      float kf[8], qf[8];
+      unpack8(rk[r], kf);
+      unpack8(rq[r], qf);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        sK[j * cLDK + c0 + q] = kf[q];
+        sQ[j * cLDK + c0 + q] = qf[q];
+      }
     }
   }
   if (tid < 64) {
@@ -513,26 +584,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     sQ[j * cLDK + cc] *= s_qn[j];
     sW[j * cLDK + cc] = s_beta[j] * kh;
   }
-  // dO E^T and dR E^T from bwd_state
-  const float* xp = g.w.dP + (size_t)task * 4096;
-  const float* xl = g.w.dL + (size_t)task * 4096;
+  cpa_wait_all();
   __syncthreads();
   const float G = s_g[Cc - 1];
   // ---- Grams Q^ W^T and K^ W^T, then M_P = dP . D (j <= i), M_L = dL . D (j < i),
   //      and the decay terms of every entry (row i gains, column j loses)
   {
-    const int mt = warp & 3;
+    const int mt = warp & 3, nt0 = 4 * (warp >> 2);
+    float aq4[4][4] = {}, ak4[4][4] = {};
+    mm3x<4, 16, false, true>(aq4, sQ + 16 * mt * cLDK, cLDK, sW + 8 * nt0 * cLDK, cLDK, lane);
+    mm3x<4, 16, false, true>(ak4, sK + 16 * mt * cLDK, cLDK, sW + 8 * nt0 * cLDK, cLDK, lane);
     for (int s = 0; s < 4; ++s) {
-      const int nt = 4 * (warp >> 2) + s;
-      float aq[4] = {0.f, 0.f, 0.f, 0.f}, ak[4] = {0.f, 0.f, 0.f, 0.f};
-      mm3<16, false, true>(aq, sQ + 16 * mt * cLDK, cLDK, sW + 8 * nt * cLDK, cLDK, lane);
-      mm3<16, false, true>(ak, sK + 16 * mt * cLDK, cLDK, sW + 8 * nt * cLDK, cLDK, lane);
+      const int nt = nt0 + s;
+      const float* aq = aq4[s];
+      const float* ak = ak4[s];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = 16 * mt + frag_row(lane, e), j = 8 * nt + frag_col(lane, e);
         const float D = (j <= i) ? __expf(s_g[i] - s_g[j]) : 0.f;
-        const float dP = (j <= i) ? xp[i * 64 + j] : 0.f;
-        const float dL = (j < i) ? -xl[i * 64 + j] : 0.f;
+        const float dP = (j <= i) ? sMP[i * cLDM + j] : 0.f;
+        const float dL = (j < i) ? -sML[i * cLDM + j] : 0.f;
         const float mp = dP * D, ml = dL * D;
         sMP[i * cLDM + j] = mp;
         sML[i * cLDM + j] = ml;
@@ -550,23 +621,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     s_dg[tid] = r - cs;
   }
   __syncthreads();
+  {   // E dS^T from bwd_state into the staging buffer, under the dw product
+    const float* xw = g.w.XW + (size_t)task * 8192;
+    for (int e = tid; e < 64 * 32; e += kBwdThreads) {
+      const int j = e >> 5, c4 = 4 * (e & 31);
+      cpa16(sX + j * cLDK + c4, xw + j * 128 + c4);
+    }
+  }
   // ---- dw = M_P^T Q^ + M_L^T K^ (+ e^{G-g} E dS^T): staged in sY
   {
     const int mt = warp & 3;
-    for (int s = 0; s < 8; ++s) {
-      const int nt = 8 * (warp >> 2) + s;
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      mm3<8, true, false>(d, sMP + 16 * mt, cLDM, sQ + 8 * nt, cLDK, lane);
-      mm3<8, true, false>(d, sML + 16 * mt, cLDM, sK + 8 * nt, cLDK, lane);
+    for (int s = 0; s < 2; ++s) {
+      const int nt0 = 8 * (warp >> 2) + 4 * s;
+      float d[4][4] = {};
+      mm3x<4, 8, true, false>(d, sMP + 16 * mt, cLDM, sQ + 8 * nt0, cLDK, lane);
+      mm3x<4, 8, true, false>(d, sML + 16 * mt, cLDM, sK + 8 * nt0, cLDK, lane);
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        sY[(16 * mt + frag_row(lane, e)) * cLDK + 8 * nt + frag_col(lane, e)] = d[e];
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          sY[(16 * mt + frag_row(lane, e)) * cLDK + 8 * (nt0 + j) + frag_col(lane, e)] = d[j][e];
     }
   }
+  cpa_wait_all();
   __syncthreads();
   {   // rows: four threads per token; dw += e^{G-g} X_W, the decay terms, d beta
     const int j = tid >> 2, part = tid & 3;
-    const float* xw = g.w.XW + (size_t)task * 8192 + j * 128;
+    const float* xw = sX + j * cLDK;
     const float ew = (j < Cc) ? __expf(G - s_g[j]) : 0.f;
     float dwk = 0.f, xww = 0.f;
     for (int c0 = 32 * part; c0 < 32 * part + 32; ++c0) {
@@ -590,13 +671,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // ---- dk^ = M_L W - e^g X_K + beta dw (+ KLA norm term), then the key norm
   {
     const int mt = warp & 3;
-    for (int s = 0; s < 8; ++s) {
-      const int nt = 8 * (warp >> 2) + s;
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      mm3<8, false, false>(d, sML + 16 * mt * cLDM, cLDM, sW + 8 * nt, cLDK, lane);
+    for (int s = 0; s < 2; ++s) {
+      const int nt0 = 8 * (warp >> 2) + 4 * s;
+      float d[4][4] = {};
+      mm3x<4, 8, false, false>(d, sML + 16 * mt * cLDM, cLDM, sW + 8 * nt0, cLDK, lane);
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        sX[(16 * mt + frag_row(lane, e)) * cLDK + 8 * nt + frag_col(lane, e)] = d[e];
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          sX[(16 * mt + frag_row(lane, e)) * cLDK + 8 * (nt0 + j) + frag_col(lane, e)] = d[j][e];
     }
   }
   __syncthreads();
@@ -610,10 +693,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float se = s_s[j] + a.eps;
     const float ds2 = VARIANT == DR_KLA ? -2.f * db * s_eta[j] / (se * se) : 0.f;
     float dkh[32], xk = 0.f, dot = 0.f;
+    float xkr[32];
+#pragma unroll
+    for (int q = 0; q < 32; q += 4) {
+      const float4 v4 = live ? *reinterpret_cast<const float4*>(dkrow + 32 * part + q)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+      xkr[q] = v4.x; xkr[q + 1] = v4.y; xkr[q + 2] = v4.z; xkr[q + 3] = v4.w;
+    }
 #pragma unroll
     for (int q = 0; q < 32; ++q) {
       const int c0 = 32 * part + q;
-      const float xkv = live ? dkrow[c0] : 0.f;
+      const float xkv = xkr[q];
       const float kh = sK[j * cLDK + c0];
       xk += xkv * kh;
       dkh[q] = sX[j * cLDK + c0] - eg * xkv + beta * sY[j * cLDK + c0] + ds2 * kh;
@@ -641,13 +731,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // ---- dq^ = M_P W + e^g X_Q, then the query norm
   {
     const int mt = warp & 3;
-    for (int s = 0; s < 8; ++s) {
-      const int nt = 8 * (warp >> 2) + s;
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      mm3<8, false, false>(d, sMP + 16 * mt * cLDM, cLDM, sW + 8 * nt, cLDK, lane);
+    for (int s = 0; s < 2; ++s) {
+      const int nt0 = 8 * (warp >> 2) + 4 * s;
+      float d[4][4] = {};
+      mm3x<4, 8, false, false>(d, sMP + 16 * mt * cLDM, cLDM, sW + 8 * nt0, cLDK, lane);
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        sX[(16 * mt + frag_row(lane, e)) * cLDK + 8 * nt + frag_col(lane, e)] = d[e];
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          sX[(16 * mt + frag_row(lane, e)) * cLDK + 8 * (nt0 + j) + frag_col(lane, e)] = d[j][e];
     }
   }
   __syncthreads();
@@ -657,10 +749,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     float* dqrow = g.dq + tok(a, b, t0 + (live ? j : 0), h) * 128;
     const float eg = __expf(s_g[j]);
     float dqh[32], xq = 0.f, dot = 0.f;
+    float xqr[32];
+#pragma unroll
+    for (int q = 0; q < 32; q += 4) {
+      const float4 v4 = live ? *reinterpret_cast<const float4*>(dqrow + 32 * part + q)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+      xqr[q] = v4.x; xqr[q + 1] = v4.y; xqr[q + 2] = v4.z; xqr[q + 3] = v4.w;
+    }
 #pragma unroll
     for (int q = 0; q < 32; ++q) {
       const int c0 = 32 * part + q;
-      const float xqv = live ? dqrow[c0] : 0.f;
+      const float xqv = xqr[q];
       const float qh = sQ[j * cLDK + c0];
       xq += xqv * qh;
       dqh[q] = sX[j * cLDK + c0] + eg * xqv;

@@ -147,3 +147,30 @@ def test_cpu_baseline_times_only_the_oracle_in_a_warm_pool():
     assert cores == 2
     assert cpu <= 2.0 * wall * cores and wall <= 2.0 * cpu
     assert one > 0
+
+
+def test_backward_bytes():
+    """Per head-token: q, k, v, dL/do in bf16 (1024), two fp32 gates (8), dq, dk, dv in
+    fp32 (1536), d log alpha and d eta (8); per (b, h): S_0 and dL/dS_T in, dL/dS_0 out."""
+    wl = W.WORKLOADS["gdn_kla_bf16"]
+    assert bench.bwd_bytes(wl) == wl.B * wl.T * wl.H * 2576 + 3 * wl.B * wl.H * 128 * 128 * 4
+
+
+def test_backward_parity_row_slice_matches_the_oracle_on_the_full_input():
+    import numpy as np
+    from oracle import backward as obw
+    wl = W.small("gdn_kla_bf16", B=2, T=30, H=2, dk=8, dv=8, seed=6)
+    inp = W.generate(wl, "kla")
+    g = np.random.default_rng(0)
+    dO = g.standard_normal((2, 30, 2, 8))
+    dS = g.standard_normal((2, 2, 8, 8))
+    S0 = g.standard_normal((2, 2, 8, 8))
+    tag, ref = bench._oracle_bwd_parity((("kla", 1, 0), bench.slice_row(inp, 1, 0), "kla",
+                                         dO[1:2, :, 0:1], dS[1:2, 0:1], S0[1:2, 0:1]))
+    f = lambda t: t.double().numpy()  # noqa: E731
+    full = obw.tokenwise_backward(f(inp["q"]), f(inp["k"]), f(inp["v"]), f(inp["log_alpha"]),
+                                  "kla", dO, dS, eta=f(inp["eta"]), eps=wl.eps,
+                                  q_l2norm=wl.q_l2norm, k_l2norm=wl.k_l2norm, S0=S0)
+    for n in ("dq", "dk", "dv", "dlog_alpha", "deta"):
+        assert np.allclose(ref[n][0, :, 0], full[n][1, :, 0], rtol=0, atol=1e-10), n
+    assert np.allclose(ref["dS0"][0, 0], full["dS0"][1, 0], rtol=0, atol=1e-10)
