@@ -183,7 +183,12 @@ int dr_decode_step(const void *q, const void *k, const void *v, const float *log
  * for bf16 inputs, fp32 for fp32 -- and the variance / statistic chunk map and
  * chunk-start value), plus for those three 4 (n + 2) bytes rounded up to 256
  * (n = B H ceil(T/64) records): the flags of the chain between chunks, which
- * the call clears itself; 0 where no path uses one. */
+ * the call clears itself; 0 where no path uses one.  On the GDN / KLA / PGDN
+ * path, when the rows are few against the current device's SM count (6 B H <=
+ * SMs) and the rows long, the carry is cut into G segments run in parallel and
+ * the workspace adds 3 B H G x 64 KB for the segments' end states, transition
+ * maps and start states (G depends on the SM count: query on the device that
+ * runs the call). */
 size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H, int dk, int dv,
                                     int chunk);
 
@@ -213,10 +218,11 @@ size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H,
  *     behind (nothing in it has to start at zero).  Calls that overlap on the
  *     GPU -- two streams, or two host threads -- race on it: serialise them.
  * Returns DR_ERR_UNSUPPORTED for other variants, dtypes or shapes (dr_chunk_fwd
- * needs no workspace for those), DR_ERR_WORKSPACE when the records
- * (dr_chunk_fwd_workspace_bytes) would exceed DR_NOALLOC_SCRATCH_BYTES, i.e.
- * B H ceil(T/64) > 1008 (GDN, KLA), > 661 (PGDN) or > 496 (KDN, KDA, PKDA, IKDN), otherwise
- * whatever dr_chunk_fwd returns.
+ * needs no workspace for those), DR_ERR_WORKSPACE when the workspace
+ * (dr_chunk_fwd_workspace_bytes) would exceed DR_NOALLOC_SCRATCH_BYTES: about
+ * B H ceil(T/64) > 1008 records (GDN, KLA), > 661 (PGDN) or > 496 (KDN, KDA,
+ * PKDA, IKDN), fewer when the segment area of a few-row call is added;
+ * otherwise whatever dr_chunk_fwd returns.
  */
 #define DR_NOALLOC_SCRATCH_BYTES (64u << 20)
 int dr_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *log_alpha,

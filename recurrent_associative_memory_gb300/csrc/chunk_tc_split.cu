@@ -799,14 +799,61 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int half = blockIdx.x & 1;
-  const int bh = blockIdx.x >> 1;
+  const int NCt = (a.T + 63) / 64;
+  // This CTA's work: a row (b, h), a 64-column half of the state, and a run of
+  // chunks c0 .. c0 + NC - 1 (the whole row unless the carry is segmented).  The
+  // loops below count chunks locally (barrier phases, buffer slots); records,
+  // tokens and saved states are addressed by the absolute chunk c0 + c.
+  int half, bh, c0 = 0, NC = NCt;
+  int s0mode = 0;                  // 0: init_state (or zero), 1: zero, 2: identity, 3: seg start
+  bool out_on = a.out != nullptr, vzero = false, fin_out = true;
+  float* sfin = nullptr;           // this row's final state [dk][dv], or null
+  const float* s0p = nullptr;      // this row's start state [dk][dv] (s0mode 0 / 3)
+  auto segmat = [&](int row, int g, int which) -> float* {   // 0: end, 1: map, 2: start
+    return a.seg_buf + (((size_t)row * a.seg_G + g) * 3 + which) * 128 * 128;
+  };
+  if (a.seg_pass == 0) {
+    half = blockIdx.x & 1;
+    bh = blockIdx.x >> 1;
+    s0p = a.S0 ? a.S0 + (size_t)bh * 128 * a.dv : nullptr;
+    sfin = a.S ? a.S + (size_t)bh * 128 * a.dv : nullptr;
+  } else if (a.seg_pass == 1) {
+    const int per = 2 + 4 * (a.seg_G - 2);
+    bh = blockIdx.x / per;
+    const int j = blockIdx.x % per;
+    if (j < 2) {   // segment 0 from the true initial state, with its outputs
+      half = j;
+      NC = a.seg_len;
+      s0p = a.S0 ? a.S0 + (size_t)bh * 128 * a.dv : nullptr;
+      sfin = segmat(bh, 0, 0);
+      fin_out = false;
+    } else {       // a middle segment: the end state from zero, or the transition map
+      const int g = 1 + (j - 2) / 4, r = (j - 2) % 4;
+      half = r & 1;
+      c0 = g * a.seg_len;
+      NC = a.seg_len;
+      out_on = false;
+      s0mode = r < 2 ? 1 : 2;
+      vzero = r >= 2;
+      sfin = segmat(bh, g, r < 2 ? 0 : 1);
+      fin_out = false;
+    }
+  } else {         // replay of segment g >= 1 from its start state
+    const int per = 2 * (a.seg_G - 1);
+    bh = blockIdx.x / per;
+    const int g = 1 + (blockIdx.x % per) / 2;
+    half = blockIdx.x & 1;
+    c0 = g * a.seg_len;
+    NC = min(a.seg_len, NCt - c0);
+    s0mode = 3;
+    s0p = segmat(bh, g, 2);
+    sfin = (g == a.seg_G - 1 && a.S) ? a.S + (size_t)bh * 128 * a.dv : nullptr;
+  }
   const int b = bh / a.H, h = bh % a.H;
-  const int NC = (a.T + 63) / 64;
   using CM = CarryMap<MODE>;
   constexpr uint32_t cS = CM::S, cE = CM::E, kRecV = CM::rec, cKP = CM::KP;
   constexpr bool kKdn = (MODE == 2), kExplicitW = (MODE != 0);
-  const uint8_t* recs = ws + (size_t)bh * NC * kRecV;
+  const uint8_t* recs = ws + ((size_t)bh * NCt + c0) * kRecV;
 
   if (tid == 0) {
     for (int i = 0; i < C_COUNT; ++i) mbar_init(&bars[i], 1);
@@ -815,6 +862,11 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+  }
+  if (vzero) {   // the map's carry reads V = 0 (U' = 0); no V copy ever lands here
+    for (int e = tid; e < 8192 / 16; e += kCarryThreads)
+      reinterpret_cast<uint4*>(sm + cV)[e] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async();
   }
   if (warp == 0) tmem_alloc(&tmem_base_s, kCarryTmem);
   tc_fence_before();
@@ -854,8 +906,8 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       if (kExplicitW) {
         bulk_load(sm + cKP, recs + (size_t)c * kRecV + CM::rW_, 32768, &bars[C_K]);
       } else {
-        tma_load_4d(sm + cKP, &tmK, &bars[C_K], 0, h, c * 64, b);
-        tma_load_4d(sm + cKP + 8192, &tmK, &bars[C_K], 64, h, c * 64, b);
+        tma_load_4d(sm + cKP, &tmK, &bars[C_K], 0, h, (c0 + c) * 64, b);
+        tma_load_4d(sm + cKP + 8192, &tmK, &bars[C_K], 64, h, (c0 + c) * 64, b);
       }
       n_k = c + 1;
     };
@@ -892,12 +944,17 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       last_par = c & 1;
     };
     {
-      const long base = ((long)bh * 128 + srow) * a.dv + half * 64 + 32 * hc;
+      const long base = (long)srow * a.dv + half * 64 + 32 * hc;
 #pragma unroll
       for (int j = 0; j < 32; j += 4) {
-        const float4 v = a.S0 ? *reinterpret_cast<const float4*>(a.S0 + base + j)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 v = (s0mode == 0 || s0mode == 3) && s0p
+                             ? *reinterpret_cast<const float4*>(s0p + base + j)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
         S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
+      }
+      if (s0mode == 2) {   // the identity's columns: the transition map of the segment
+#pragma unroll
+        for (int j = 0; j < 32; ++j) S[j] = (srow == half * 64 + 32 * hc + j) ? 1.f : 0.f;
       }
       store_state_tiles();
     }
@@ -921,7 +978,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
     for (int c = 0; c < NC; ++c) {
       const int slot = c & 1;
       if (a.save_S) {   // backward: the state at this chunk's start
-        float* dst = a.save_S + (((size_t)bh * NC + c) * 128 + srow) * 128 + half * 64 + 32 * hc;
+        float* dst = a.save_S + (((size_t)bh * NCt + c0 + c) * 128 + srow) * 128 + half * 64 + 32 * hc;
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
           *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
@@ -968,7 +1025,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
           }
         }
         if (a.save_E) {   // backward: E(c), this thread's row and 16 columns
-          float* dst = a.save_E + (((size_t)bh * NC + c) * 64 + erow) * 128 + half * 64 + 32 * hc +
+          float* dst = a.save_E + (((size_t)bh * NCt + c0 + c) * 64 + erow) * 128 + half * 64 + 32 * hc +
                        16 * keep;
 #pragma unroll
           for (int e = 0; e < 16; e += 4)
@@ -1067,12 +1124,12 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
     // and its K copies land before the CTA exits
     if (leader && last_bar) mbar_wait(last_bar, last_par, kWait / 4);
     if (leader && n_k > 0) mbar_wait(&bars[C_K], (n_k - 1) & 1, kWait / 4);
-    if (!s_abort && a.S) {
-      const long base = ((long)bh * 128 + srow) * a.dv + half * 64 + 32 * hc;
+    if (!s_abort && sfin) {
+      const long base = (long)srow * a.dv + half * 64 + 32 * hc;
 #pragma unroll
       for (int j = 0; j < 32; j += 4) {
-        *reinterpret_cast<float4*>(a.S + base + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-        if (a.check_finite)
+        *reinterpret_cast<float4*>(sfin + base + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        if (a.check_finite && fin_out)
           bad |= !(finite_f(S[j]) && finite_f(S[j + 1]) && finite_f(S[j + 2]) && finite_f(S[j + 3]));
       }
     }
@@ -1088,7 +1145,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
     for (int c = 0; c < NC; ++c) {
       float qs_nxt = 0.f;
       if (c + 1 < NC) qs_nxt = reinterpret_cast<const float*>(recs + (size_t)(c + 1) * kRecV + rVec)[i];
-      const int t0 = c * 64, Cc = min(64, a.T - t0);
+      const int t0 = (c0 + c) * 64, Cc = min(64, a.T - t0);
       // e^g qn . Q S first; the accumulator is released as soon as it is read,
       // and PE(c) lands in it next
       float qv[2][16];
@@ -1130,7 +1187,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 16; ++e) x[e] = qv[hcol][e] + ((lane < 16) ? pa[e] + pb[e] : x[e]);
-        if (a.out && i < Cc) {
+        if (out_on && i < Cc) {
           const int col = 32 * hcol + ((lane < 16) ? 0 : 16);
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
@@ -1165,9 +1222,9 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
     uint32_t last_par = 0;
     auto load_tv = [&](int c) {
       const uint8_t* rec = recs + (size_t)c * kRecV;
-      mbar_expect_tx(&bars[C_TV], 16384 + 8192);
+      mbar_expect_tx(&bars[C_TV], vzero ? 16384 : 16384 + 8192);
       bulk_load(sm + cT, rec + rT, 16384, &bars[C_TV]);
-      tma_load_4d(sm + cV, &tmV, &bars[C_TV], half * 64, h, c * 64, b);
+      if (!vzero) tma_load_4d(sm + cV, &tmV, &bars[C_TV], half * 64, h, (c0 + c) * 64, b);
       n_tv = c + 1;
     };
     auto load_w = [&](int c) {   // slot c & 1
@@ -1181,8 +1238,8 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
       if (kKdn) {
         bulk_load(sm + cQ, recs + (size_t)c * kRecV + rQk, 32768, &bars[C_Q]);
       } else {
-        tma_load_4d(sm + cQ, &tmQ, &bars[C_Q], 0, h, c * 64, b);
-        tma_load_4d(sm + cQ + 8192, &tmQ, &bars[C_Q], 64, h, c * 64, b);
+        tma_load_4d(sm + cQ, &tmQ, &bars[C_Q], 0, h, (c0 + c) * 64, b);
+        tma_load_4d(sm + cQ + 8192, &tmQ, &bars[C_Q], 64, h, (c0 + c) * 64, b);
       }
       n_q = c + 1;
     };
@@ -1312,6 +1369,47 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, kCarryTmem);
 }
 
+// ================================================================= segment composition
+// Start state of every replayed segment: S_1 = the end state of segment 0, and
+// S_{g+1} = M_g S_g + N_g (the middle segment's transition map applied to its
+// start, plus its end state from zero).  One CTA per (row, 32 state columns).
+__global__ void __launch_bounds__(256) seg_compose_kernel(FwdArgs a) {
+  __shared__ float sM[128][129];
+  __shared__ float sX[128][33];
+  const int tid = threadIdx.x, bh = blockIdx.x >> 2, cb = blockIdx.x & 3;
+  const int r = tid >> 1, c16 = 16 * (tid & 1);
+  auto mat = [&](int g, int which) {
+    return a.seg_buf + (((size_t)bh * a.seg_G + g) * 3 + which) * 128 * 128;
+  };
+  for (int e = tid; e < 128 * 32; e += 256) {
+    const int i = e >> 5, j = e & 31;
+    const float x = mat(0, 0)[i * 128 + 32 * cb + j];
+    sX[i][j] = x;
+    mat(1, 2)[i * 128 + 32 * cb + j] = x;
+  }
+  for (int g = 1; g + 1 < a.seg_G; ++g) {
+    __syncthreads();
+    for (int e = tid; e < 128 * 128; e += 256) sM[e >> 7][e & 127] = mat(g, 1)[e];
+    __syncthreads();
+    float acc[16];
+    const float* N = mat(g, 0) + r * 128 + 32 * cb + c16;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) acc[q] = N[q];
+    for (int k = 0; k < 128; ++k) {
+      const float m = sM[r][k];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) acc[q] = fmaf(m, sX[k][c16 + q], acc[q]);
+    }
+    __syncthreads();
+    float* dst = mat(g + 1, 2) + r * 128 + 32 * cb + c16;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      sX[r][c16 + q] = acc[q];
+      dst[q] = acc[q];
+    }
+  }
+}
+
 int sm_count() {
   static int count[64] = {0};
   int dev = 0;
@@ -1327,8 +1425,37 @@ bool chunk_tc_split_supported(int variant, int dtype, int dk, int dv, int chunk)
          dk == 128 && dv == 128 && chunk == 64;
 }
 
+// Segments for the carry: with few rows the carry runs on few SMs, so each row
+// is cut into G segments.  A first pass runs segment 0 and, for every middle
+// segment, its end state from a zero start and its transition map (the same
+// carry over V = 0 from the identity); a small kernel composes the start states;
+// a second pass replays segments 1 .. G-1 from them.  Two passes over Ls chunks
+// instead of one over NC: worth it from G = 3.  The first pass has
+// rows (2 + 4 (G - 2)) CTAs, at most one wave of the SM count.
+bool seg_plan(int nsm, long rows, int NC, int* G_out, int* Ls_out) {
+  *G_out = 0;
+  *Ls_out = 0;
+  if (nsm <= 0 || rows * 6 > nsm) return false;
+  int G = (int)((nsm / rows - 2) / 4) + 2;
+  if (G > 64) G = 64;
+  for (; G >= 3; --G) {
+    const int Ls = (NC + G - 1) / G;
+    if (Ls >= 2 && (long)(G - 1) * Ls < NC) {
+      *G_out = G;
+      *Ls_out = Ls;
+      return true;
+    }
+  }
+  return false;
+}
+
 size_t chunk_tc_split_workspace_bytes(int variant, int B, int T, int H) {
-  return (size_t)B * H * ((T + 63) / 64) * (variant == DR_PGDN ? kRecP : kRec);
+  const int NC = (T + 63) / 64;
+  size_t bytes = (size_t)B * H * NC * (variant == DR_PGDN ? kRecP : kRec);
+  int G, Ls;
+  if (seg_plan(sm_count(), (long)B * H, NC, &G, &Ls))
+    bytes += (size_t)B * H * G * 3 * 128 * 128 * sizeof(float);
+  return bytes;
 }
 
 cudaError_t launch_chunk_tc_split(const FwdArgs& a, void* workspace, cudaStream_t st) {
@@ -1367,6 +1494,33 @@ cudaError_t launch_chunk_tc_split(const FwdArgs& a, void* workspace, cudaStream_
     if (e != cudaSuccess) return e;                                                        \
     chunk_carry_kernel<M_><<<a.B * a.H * 2, kCarryThreads, CarryMap<M_>::bytes, st>>>(     \
         mq, mk, mv, a, ws);                                                                \
+  }
+  const int NC = (a.T + 63) / 64;
+  int G, Ls;
+  if (!a.save_S && seg_plan(nsm, (long)a.B * a.H, NC, &G, &Ls)) {
+    FwdArgs s1 = a;
+    s1.seg_pass = 1;
+    s1.seg_G = G;
+    s1.seg_len = Ls;
+    s1.seg_buf = reinterpret_cast<float*>(ws + (size_t)a.B * a.H * NC *
+                                               (a.variant == DR_PGDN ? kRecP : kRec));
+    FwdArgs s3 = s1;
+    s3.seg_pass = 2;
+#define DR_CARRY_SEG(M_)                                                                   \
+  {                                                                                        \
+    e = cudaFuncSetAttribute(chunk_carry_kernel<M_>,                                       \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,                  \
+                             (int)CarryMap<M_>::bytes);                                    \
+    if (e != cudaSuccess) return e;                                                        \
+    chunk_carry_kernel<M_><<<a.B * a.H * (2 + 4 * (G - 2)), kCarryThreads,                 \
+                             CarryMap<M_>::bytes, st>>>(mq, mk, mv, s1, ws);               \
+    seg_compose_kernel<<<a.B * a.H * 4, 256, 0, st>>>(s1);                                 \
+    chunk_carry_kernel<M_><<<a.B * a.H * 2 * (G - 1), kCarryThreads,                       \
+                             CarryMap<M_>::bytes, st>>>(mq, mk, mv, s3, ws);               \
+  }
+    if (a.variant == DR_PGDN) DR_CARRY_SEG(1) else DR_CARRY_SEG(0)
+#undef DR_CARRY_SEG
+    return cudaGetLastError();
   }
   if (a.variant == DR_PGDN) DR_CARRY(1) else DR_CARRY(0)
   return cudaGetLastError();

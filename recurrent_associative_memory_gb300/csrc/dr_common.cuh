@@ -40,6 +40,14 @@ struct FwdArgs {
   // [B H NC][64][dv] (fp32), and a null `out` skips the output stores
   float* save_S;
   float* save_E;
+  // segment-parallel carry (scalar-decay two-phase path, few rows and many
+  // chunks): 0 = whole rows; 1 = first pass (segment 0 with its outputs, and
+  // every middle segment's zero-start state and transition map); 2 = replay of
+  // segments 1 .. G-1 from their composed start states.  seg_buf holds per
+  // (row, segment) the end state from zero (or segment 0's true end state), the
+  // transition map and the start state, each [dk][dv] fp32.
+  int seg_pass, seg_G, seg_len;
+  float* seg_buf;
 };
 
 // Sticky device status: the first non-OK code written stays until read.

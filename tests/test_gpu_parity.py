@@ -428,3 +428,17 @@ def test_two_phase_random_shapes(rt, variant):
         inp = small_inputs(variant, "bf16", B=B, T=T, H=H, seed=1000 + 10 * vid + case)
         S0, aux0 = random_state(inp, seed=2000 + 10 * vid + case)
         check_fwd(rt, inp, S0, aux0)
+
+
+# ------------------------------------------------------------ segment-parallel carry
+
+@pytest.mark.parametrize("variant", ["gdn", "kla", "pgdn"])
+@pytest.mark.parametrize("B,H,T", [(1, 2, 64 * 40 + 17), (2, 3, 64 * 41), (1, 1, 64 * 9 + 1)])
+def test_segmented_carry_matches_oracle(rt, variant, B, H, T):
+    """Few rows and long rows: the carry runs as segments in parallel (segment 0
+    and every middle segment's end state and transition map, then the replay of
+    the rest from the composed start states); outputs, final state and gain
+    state against the oracle, with a nonzero initial state."""
+    inp = small_inputs(variant, "bf16", B=B, T=T, H=H, seed=61)
+    S0, aux0 = random_state(inp, seed=8)
+    check_fwd(rt, inp, S0, aux0)
