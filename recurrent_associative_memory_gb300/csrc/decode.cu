@@ -28,6 +28,13 @@ __device__ __forceinline__ float ld_in(const void* p, long i) {
   return to_f<T>(static_cast<const T*>(p)[i]);
 }
 
+// Both CTAs of a cluster pass this point before either goes on (release /
+// acquire: the other CTA's global reads before it are complete).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+
 // Block-wide sum of one value per thread (all threads must call).
 __device__ __forceinline__ float block_sum(float v, float* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -76,13 +83,26 @@ __global__ void __launch_bounds__(kDecodeThreads, (DK * DVS <= 8192) ? 4 : 2)
     s[m] = __ldcs(S4 + (((srow0 + r) * a.dv + col0) >> 2));
   }
 
-  // 2. token inputs and gates
+  // 2. token inputs and gates (every load issued before the first reduction)
   const long tok = (long)bh;                    // decode layout [B, H, d]
-  float kc = 0.f, qc = 0.f;
+  const bool perchan_la = a.variant == DR_KDN || a.variant == DR_IKDN || a.variant == DR_KDA ||
+                          a.variant == DR_PKDA;
+  float kc = 0.f, qc = 0.f, g_la = 0.f, g_aux = 0.f, g_om = 0.f;
   if (tid < DK) {
     kc = ld_in<Tin>(a.k, tok * DK + tid);
     qc = ld_in<Tin>(a.q, tok * DK + tid);
+    g_la = a.log_alpha[perchan_la ? tok * DK + tid : tok];
+    if (a.variant == DR_KDN || a.variant == DR_PGDN || a.variant == DR_PKDA)
+      g_aux = a.aux[tok * DK + tid];
+    if (a.variant == DR_KDN) g_om = a.omega[tok * DK + tid];
   }
+  const float g_r = (a.variant == DR_KDN || a.variant == DR_IKDN) ? a.r[tok] : 0.f;
+  const float g_eta = (a.variant == DR_KDN || a.variant == DR_IKDN) ? 0.f : a.eta[tok];
+  const float g_aP = (a.variant == DR_PGDN || a.variant == DR_PKDA) ? a.alphaP[tok] : 0.f;
+  const float g_bP = (a.variant == DR_PGDN || a.variant == DR_PKDA) ? a.betaP[tok] : 0.f;
+  const float g_mu = (a.variant == DR_PGDN || a.variant == DR_PKDA) ? a.mu[h] : 0.f;
+  const float g_auxh = a.variant == DR_IKDN ? a.aux[tok] : 0.f;
+  const float g_omh = a.variant == DR_IKDN ? a.omega[tok] : 0.f;
   if (tid < DVS) s_v[tid] = ld_in<Tin>(a.v, tok * a.dv + slice * DVS + tid);
   const float kk = block_sum(kc * kc, s_red);
   const float qq = block_sum(qc * qc, s_red);
@@ -90,53 +110,52 @@ __global__ void __launch_bounds__(kDecodeThreads, (DK * DVS <= 8192) ? 4 : 2)
   if (a.q_l2norm) qc = qc / fmaxf(sqrtf(qq), 1e-30f);
   const float kk_eff = a.k_l2norm ? block_sum(kc * kc, s_red) : kk;
 
-  float w = 0.f, d = 0.f;
+  // The gain state (PGDN / PKDA statistic, KDN variance, isotropic KDN variance)
+  // is updated in place.  Every slice of a head forms the same gains from it; the
+  // slices of a head form one cluster, and the new value is written by slice 0
+  // only after every slice has read the old one (cluster barrier below).
+  float w = 0.f, d = 0.f, aux_new = 0.f;
   if (a.variant == DR_KDN) {
     float p_hat = 0.f, alpha = 0.f;
     if (tid < DK) {
-      alpha = expf(a.log_alpha[tok * DK + tid]);
-      p_hat = alpha * alpha * a.aux[tok * DK + tid] + a.omega[tok * DK + tid];
+      alpha = expf(g_la);
+      p_hat = alpha * alpha * g_aux + g_om;
     }
     const float z = block_sum(tid < DK ? p_hat * kc * kc : 0.f, s_red);
     if (tid < DK) {
-      const float rr = a.r[tok];
+      const float rr = g_r;
       w = p_hat * kc / (rr + z);
       d = alpha;
-      if (slice == 0) {
-        const float u = (a.info_scale / rr) * kc * kc;
-        a.aux[tok * DK + tid] = p_hat / (1.f + u * p_hat);
-      }
+      const float u = (a.info_scale / rr) * kc * kc;
+      aux_new = p_hat / (1.f + u * p_hat);
     }
   } else if (a.variant == DR_IKDN) {   // one variance per head (aux [B, H])
-    const float alpha = tid < DK ? expf(a.log_alpha[tok * DK + tid]) : 0.f;
+    const float alpha = tid < DK ? expf(g_la) : 0.f;
     const float a_mean = block_sum(alpha * alpha, s_red) / DK;
-    const float rr = a.r[tok];
-    const float b_hat = a_mean * a.aux[tok] + a.omega[tok];
+    const float rr = g_r;
+    const float b_hat = a_mean * g_auxh + g_omh;
     if (tid < DK) {
       w = b_hat / (rr + b_hat * kk_eff) * kc;
       d = alpha;
     }
-    __syncthreads();   // every thread has read the variance before it is replaced
-    if (slice == 0 && tid == 0) {
-      const float u = a.info_scale * kk_eff / (DK * rr);
-      a.aux[tok] = b_hat / (1.f + u * b_hat);
-    }
+    const float u = a.info_scale * kk_eff / (DK * rr);
+    aux_new = b_hat / (1.f + u * b_hat);
   } else if (tid < DK) {
-    const bool perchan = (a.variant == DR_KDA || a.variant == DR_PKDA);   // decay per row of S
-    d = expf(a.log_alpha[perchan ? tok * DK + tid : tok]);
-    const float eta = a.eta[tok];
+    d = expf(g_la);   // per row of S for KDA / PKDA, per head otherwise
+    const float eta = g_eta;
     if (a.variant == DR_GDN || a.variant == DR_KDA) {
       w = eta * kc;
     } else if (a.variant == DR_KLA) {
       w = eta / (kk_eff + a.eps) * kc;
     } else {  // DR_PGDN, DR_PKDA
-      const float A = a.alphaP[tok] * a.aux[tok * DK + tid] + a.betaP[tok] * kc * kc;
-      const float rr = logf(fmaxf(A, a.log_floor)) - a.mu[h];
+      const float A = g_aP * g_aux + g_bP * kc * kc;
+      const float rr = logf(fmaxf(A, a.log_floor)) - g_mu;
       const float sq = rr / (1.f + fabsf(rr));
       w = eta * expf(-a.ln_x * sq) * kc;
-      if (slice == 0) a.aux[tok * DK + tid] = A;
+      aux_new = A;
     }
   }
+
   if (tid < DK) {
     s_k[tid] = kc;
     s_q[tid] = qc;
@@ -192,21 +211,47 @@ __global__ void __launch_bounds__(kDecodeThreads, (DK * DVS <= 8192) ? 4 : 2)
     __stcs(S4 + (((srow0 + r) * a.dv + col0) >> 2), n);
   }
   if (bad) set_status(DR_ERR_NONFINITE);
+  // 6. the gain state, in place, once every slice of this head has read the old one
+  //    (at the start of step 2; the barrier comes last so that it costs no stall)
+  const bool has_aux = a.variant == DR_PGDN || a.variant == DR_PKDA || a.variant == DR_KDN ||
+                       a.variant == DR_IKDN;
+  if (has_aux) {
+    if (nslice > 1) cluster_sync();
+    if (slice == 0) {
+      if (a.variant == DR_IKDN) {
+        if (tid == 0) a.aux[tok] = aux_new;
+      } else if (tid < DK) {
+        a.aux[tok * DK + tid] = aux_new;
+      }
+    }
+  }
 }
 
 }  // namespace
 
-// Dispatch on (dtype, dk, slice width).  Variants with an aux state (PGDN, KDN)
-// keep one CTA per (b, h) so the in-place aux update is written by the CTA that
-// read it; GDN/KLA split dv = 128 into two slices for more CTAs.
+// Dispatch on (dtype, dk, slice width).  dv = 128 is split into two 64-column
+// slices, one CTA each (four per SM): the two slices of a head are launched as a
+// cluster of two, so the in-place update of a gain state can wait for both
+// slices' reads of it.
 cudaError_t launch_decode(const FwdArgs& a, int dtype, cudaStream_t st) {
-  const bool split = (a.dv == 128) && (a.variant == DR_GDN || a.variant == DR_KLA);
+  const bool split = (a.dv == 128);
   const int dvs = split ? 64 : a.dv;
   const int grid = a.B * a.H * (a.dv / dvs);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.dv / dvs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
 #define DR_DEC(DK_, DVS_, T_)                                                  \
   if (a.dk == DK_ && dvs == DVS_) {                                            \
-    decode_kernel<DK_, DVS_, T_><<<grid, kDecodeThreads, 0, st>>>(a);          \
-    return cudaGetLastError();                                                 \
+    return cudaLaunchKernelEx(&cfg, decode_kernel<DK_, DVS_, T_>, a);          \
   }
   if (dtype == DR_BF16) {
     DR_DEC(64, 64, __nv_bfloat16) DR_DEC(128, 64, __nv_bfloat16)
