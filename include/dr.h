@@ -234,38 +234,56 @@ int dr_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const floa
  * (DR_OK, DR_ERR_NONFINITE or DR_ERR_TIMEOUT), or DR_ERR_CUDA. */
 int dr_get_device_status(dr_stream_t stream);
 
+/* Gradient buffers of dr_chunk_bwd (device fp32, overwritten; NULL where a
+ * field says so).  Layouts as the forward's inputs. */
+typedef struct dr_grads {
+  float *dq;               /* [B,T,H,dk]                                              */
+  float *dk;               /* [B,T,H,dk]                                              */
+  float *dv;               /* [B,T,H,dv]                                              */
+  float *d_log_alpha;      /* [B,T,H]                                                 */
+  float *d_eta;            /* [B,T,H] (GDN / KLA eta, PGDN beta)                      */
+  float *d_init_state;     /* [B,H,dk,dv] or NULL (not written)                       */
+  float *d_alphaP;         /* PGDN: [B,T,H]                                           */
+  float *d_betaP;          /* PGDN: [B,T,H]                                           */
+  float *d_mu;             /* PGDN: [H]                                               */
+  float *d_aux_init;       /* PGDN: dL/dA_0 [B,H,dk] or NULL                          */
+  const float *d_aux_final;/* PGDN: input dL/dA_T [B,H,dk] or NULL (zero)             */
+} dr_grads;
+
 /*
- * Backward of dr_chunk_fwd (training): given dL/d out and dL/d final_state,
- * the gradients of L with respect to q, k, v, log_alpha, eta and init_state, for
- * the scalar-decay write rules GDN and KLA (KLA notes section 2.5, Eqs. (7)-(9)
- * differentiated chunk by chunk in reverse; the write gain of section 1.1 / Eq.
- * (3) and the optional L2 norms differentiated after).  The forward is run again
- * inside the call (its chunk records, the state at every chunk start and the
- * chunk residuals E go to the workspace); then a reverse carry over chunks
- * passes dL/dS from chunk to chunk, and every chunk's local gradients follow in
- * parallel.
+ * Backward of dr_chunk_fwd (training): given dL/d out, dL/d final_state (and for
+ * PGDN dL/d A_T), the gradients of L with respect to q, k, v, log_alpha, the
+ * write gates and init_state (PGDN also alphaP, betaP, mu and A_0), for the
+ * scalar-decay write rules GDN, KLA and PGDN (KLA notes section 2.5, Eqs.
+ * (7)-(9) differentiated chunk by chunk in reverse; then the write gain: GDN /
+ * KLA section 1.1 / Eq. (3); PGDN the bounded map of the key statistic, PDN
+ * notes Eq. (9), whose adjoint is carried backwards through the statistic's
+ * recursion; then the optional L2 norms).  The forward is run again inside the
+ * call (its chunk records, the state at every chunk start and the chunk
+ * residuals E go to the workspace); a reverse carry over chunks passes dL/dS
+ * from chunk to chunk, and every chunk's local gradients follow in parallel.
  *
- * Inputs as dr_chunk_fwd (same q, k, v, log_alpha, gp gates and flags, eps,
- * init_state or NULL).  d_out [B,T,H,dv] in gp->dtype; d_final_state fp32
- * [B,H,dk,dv] or NULL (zero).  Outputs, all device fp32, overwritten: dq, dk
- * [B,T,H,dk]; dv [B,T,H,dv]; d_log_alpha, d_eta [B,T,H]; d_init_state
- * [B,H,dk,dv] or NULL (not written).  gp->workspace must hold at least
- * dr_chunk_bwd_workspace_bytes() (256-byte aligned); its contents are undefined
- * afterwards.  Supported: DR_GDN, DR_KLA with bf16 q/k/v, dk = dv = 128, chunk
- * 64 (DR_ERR_UNSUPPORTED otherwise).  Returns DR_OK or a negative dr_status
- * (DR_ERR_WORKSPACE when the workspace is missing or small).
+ * Inputs as dr_chunk_fwd (same q, k, v, log_alpha, gp gates and flags --
+ * gp->aux_init is PGDN's A_0 --, eps, init_state or NULL).  d_out [B,T,H,dv] in
+ * gp->dtype; d_final_state fp32 [B,H,dk,dv] or NULL (zero).  g: host pointer to
+ * the gradient buffers (the PGDN fields are ignored for GDN / KLA).
+ * gp->workspace must hold at least dr_chunk_bwd_workspace_bytes() (256-byte
+ * aligned); its contents are undefined afterwards.  Supported: DR_GDN, DR_KLA,
+ * DR_PGDN with bf16 q/k/v, dk = dv = 128, chunk 64 (DR_ERR_UNSUPPORTED
+ * otherwise).  Returns DR_OK or a negative dr_status (DR_ERR_WORKSPACE when the
+ * workspace is missing or small).
  */
 int dr_chunk_bwd(const void *q, const void *k, const void *v, const float *log_alpha,
                  const dr_params *gp, int variant, float eps, const float *init_state,
-                 const void *d_out, const float *d_final_state,
-                 float *dq, float *dk, float *dv, float *d_log_alpha, float *d_eta,
-                 float *d_init_state, int B, int T, int H, int dk_, int dv_, int chunk,
-                 dr_stream_t stream);
+                 const void *d_out, const float *d_final_state, const dr_grads *g,
+                 int B, int T, int H, int dk, int dv, int chunk, dr_stream_t stream);
 
-/* Workspace bytes dr_chunk_bwd needs: B H ceil(T/64) x 295,940 rounded up to 256
- * (the forward's 66,560-byte chunk record, the chunk-start state, E, dL/dS at the
- * chunk end and three per-chunk products), or 0 where the backward is not
- * supported. */
+/* Workspace bytes dr_chunk_bwd needs, each array on a 256-byte boundary: per
+ * chunk record (n = B H ceil(T/64)) the forward's record (66,560 bytes; PGDN
+ * 101,376), the chunk-start state (65,536), E (32,768), dL/dS at the chunk end
+ * (65,536) and three per-chunk products (32,768 + 2 x 16,384), 4 bytes of
+ * gamma <dS, S_c>; PGDN also dL/dw (32,768) and the key-norm factors (256) per
+ * record and 4 B H bytes; 0 where the backward is not supported. */
 size_t dr_chunk_bwd_workspace_bytes(int variant, int dtype, int B, int T, int H, int dk, int dv,
                                     int chunk);
 

@@ -24,6 +24,13 @@
 // write gain (d beta = dw . k^, dk^ += beta dw; KLA: d eta = d beta / (s + eps),
 // dk^ -= 2 d beta eta / (s + eps)^2 k^) and the L2 norms (dx = (dx^ - x^ (x^ . dx^)) / ||x||).
 //
+// PGDN's write vector w = eta B(A) . k^ comes from the key statistic A_t =
+// alphaP A_{t-1} + betaP k^.k^ (PDN notes Eq. (9)): the chunk part collects
+// dL/dw with the record's explicit write keys in place of eta k^, and
+// `pgdn_gain_bwd` carries the statistic's adjoint dA backwards over the whole
+// row (dA_{t-1} = alphaP_t dA_t plus each token's own term through B),
+// giving the gradients of k^, beta, alphaP, betaP, mu and A_0.
+//
 // Kernels (after the forward's prep and carry, which saves S_c and E per chunk):
 //   bwd_carry   one CTA per (b, h, 32 columns of dv), chunks in reverse: dE, dR
 //               (written as dV) and dS_c on TF32x3 warp-level tensor-core products,
@@ -45,8 +52,9 @@ using namespace tc;
 constexpr int kBwdThreads = 256;
 // The workspace: the forward's chunk records, then per record the saved state, E,
 // dS_{c+1}, E dS^T, dO E^T, dR E^T and gamma <dS, S_c> (one array each, record-major)
-constexpr size_t kRecF = 66560;                 // the forward's chunk record (tc_split)
-constexpr size_t kBwdPerRec = kRecF + 4 * (16384 + 8192 + 16384 + 8192 + 4096 + 4096 + 1);
+constexpr size_t kRecF = 66560;                 // the forward's GDN / KLA chunk record (tc_split)
+constexpr size_t kRecFP = 101376;               // the forward's PGDN chunk record
+constexpr uint32_t rWF = 66560, rAuxF = 99328;    // PGDN record: write keys, statistic
 // the forward record's vectors (floats after rVecF): e^g qn, e^{G-g} c, gamma, e^g cr
 constexpr size_t rVecF = 65536;
 constexpr uint32_t rTF = 0, rPF = 49152;
@@ -60,18 +68,46 @@ struct BwdWs {
   float* dP;      // [n][64][64]    dO E^T
   float* dL;      // [n][64][64]    dR E^T
   float* SS;      // [n]            gamma <dS, S_c>
+  float* DW;      // PGDN [n][64][128]  dL/dw
+  float* CR;      // PGDN [n][64]       key-norm factors
+  float* MU;      // PGDN [B H]         each row's part of dL/dmu
+  size_t recb;    // bytes of one forward record
 };
 
-BwdWs bwd_ws(void* base, long n) {
+// Every array starts on a 256-byte boundary (the 16-byte copies need 16).
+inline size_t al256(size_t bytes) { return (bytes + 255) / 256 * 256; }
+
+// Lays the arrays out from `base` (null: only the size), returns the bytes used.
+size_t bwd_layout(void* base, long n, int rows, bool pgdn, BwdWs* w) {
+  uint8_t* p = static_cast<uint8_t*>(base);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* q = p ? p + off : nullptr;
+    off += al256(bytes);
+    return q;
+  };
+  BwdWs v{};
+  v.recb = pgdn ? kRecFP : kRecF;
+  v.rec = take((size_t)n * v.recb);
+  v.S = reinterpret_cast<float*>(take((size_t)n * 16384 * 4));
+  v.E = reinterpret_cast<float*>(take((size_t)n * 8192 * 4));
+  v.dS = reinterpret_cast<float*>(take((size_t)n * 16384 * 4));
+  v.XW = reinterpret_cast<float*>(take((size_t)n * 8192 * 4));
+  v.dP = reinterpret_cast<float*>(take((size_t)n * 4096 * 4));
+  v.dL = reinterpret_cast<float*>(take((size_t)n * 4096 * 4));
+  v.SS = reinterpret_cast<float*>(take((size_t)n * 4));
+  if (pgdn) {
+    v.DW = reinterpret_cast<float*>(take((size_t)n * 8192 * 4));
+    v.CR = reinterpret_cast<float*>(take((size_t)n * 64 * 4));
+    v.MU = reinterpret_cast<float*>(take((size_t)rows * 4));
+  }
+  if (w) *w = v;
+  return off;
+}
+
+BwdWs bwd_ws(void* base, long n, int rows, bool pgdn) {
   BwdWs w;
-  w.rec = static_cast<uint8_t*>(base);
-  w.S = reinterpret_cast<float*>(w.rec + (size_t)n * kRecF);
-  w.E = w.S + (size_t)n * 16384;
-  w.dS = w.E + (size_t)n * 8192;
-  w.XW = w.dS + (size_t)n * 16384;
-  w.dP = w.XW + (size_t)n * 8192;
-  w.dL = w.dP + (size_t)n * 4096;
-  w.SS = w.dL + (size_t)n * 4096;
+  bwd_layout(base, n, rows, pgdn, &w);
   return w;
 }
 
@@ -172,9 +208,15 @@ struct BwdArgs {
   float* dla;                // [B,T,H]
   float* deta;               // [B,T,H]
   float* dS0;                // [B,H,dk,dv] or null
+  float* daP;                // PGDN [B,T,H]
+  float* dbP;                // PGDN [B,T,H]
+  float* dmu;                // PGDN [H]
+  float* daux0;              // PGDN [B,H,dk] or null
+  const float* daux_T;       // PGDN [B,H,dk] or null
   BwdWs w;
 };
 
+template <bool PG>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_carry_kernel(FwdArgs a, BwdArgs g) {
   extern __shared__ __align__(16) float smf[];
@@ -203,10 +245,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   // The next chunk's raw operands (P and T tile images, K and Q rows, dO, the
   // record's row vectors) are fetched into registers while this chunk computes.
-  uint4 rPT[2][4], rK[4], rQ[4], rO;
+  uint4 rPT[2][4], rK[4], rQ[4], rO, rWh[PG ? 4 : 1], rWl[PG ? 4 : 1];
   float rU[4], rEq[4], rEk[4], rG = 0.f;
   auto fetch = [&](int c) {
-    const uint8_t* rec = g.w.rec + ((size_t)bh * NC + c) * kRecF;
+    const uint8_t* rec = g.w.rec + ((size_t)bh * NC + c) * g.w.recb;
     const float* rv = reinterpret_cast<const float*>(rec + rVecF);
     const int t0 = 64 * c, Cc = min(64, a.T - t0);
 #pragma unroll
@@ -224,6 +266,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const bool live = j < Cc;
       rK[r] = live ? *reinterpret_cast<const uint4*>(K + tok(a, b, t0 + j, h) * 128 + c0)
                    : make_uint4(0u, 0u, 0u, 0u);
+      if (PG) {   // the explicit write keys (hi, lo) of the record, tile [tok][ch] per 64 ch
+        const uint32_t off = (c0 >> 6) * 8192 + umma::sw128_offset(j, c0 & 63);
+        rWh[r] = *reinterpret_cast<const uint4*>(rec + rWF + off);
+        rWl[r] = *reinterpret_cast<const uint4*>(rec + rWF + 16384 + off);
+      }
       rQ[r] = live ? *reinterpret_cast<const uint4*>(Q + tok(a, b, t0 + j, h) * 128 + c0)
                    : make_uint4(0u, 0u, 0u, 0u);
       rU[r] = rv[64 + j];
@@ -265,12 +312,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
-      float kf[8], qf[8];
+      float kf[8], qf[8], wf[8];
       unpack8(rK[r], kf);
       unpack8(rQ[r], qf);
+      if (PG) {
+        float wl[8];
+        unpack8(rWh[r], wf);
+        unpack8(rWl[r], wl);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) wf[q] += wl[q];
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) wf[q] = kf[q];
+      }
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        sWb[j * cLDW + c0 + q] = rU[r] * kf[q];
+        sWb[j * cLDW + c0 + q] = rU[r] * wf[q];
         sKg[j * cLDQ + c0 + q] = rEk[r] * kf[q];
         sQg[j * cLDQ + c0 + q] = rEq[r] * qf[q];
       }
@@ -454,7 +511,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (tid == 0) {
     float tsum = 0.f;
     for (int w = 0; w < kBwdThreads / 32; ++w) tsum += s_red[w];
-    const float gam = reinterpret_cast<const float*>(g.w.rec + (size_t)task * kRecF + rVecF)[128];
+    const float gam = reinterpret_cast<const float*>(g.w.rec + (size_t)task * g.w.recb + rVecF)[128];
     g.w.SS[task] = gam * tsum;
   }
   // X_W = E dS^T
@@ -484,6 +541,7 @@ constexpr int kLocalSmemF = 5 * 64 * cLDK + 2 * 64 * cLDM;
 template <int VARIANT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_local_kernel(FwdArgs a, BwdArgs g) {
+  constexpr bool PG = VARIANT == DR_PGDN;
   extern __shared__ __align__(16) float smf[];
   float* sK = smf;                 // k^ [j][c]
   float* sQ = sK + 64 * cLDK;      // q^
@@ -562,6 +620,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       s_qn[j] = qn;
       s_s[j] = s;
       s_beta[j] = VARIANT == DR_KLA ? s_eta[j] / (s + a.eps) : s_eta[j];
+      if (PG && j < Cc) g.w.CR[(size_t)task * 64 + j] = cr;
     }
   }
   if (warp == 0) {   // inclusive cumulative log-decay (two tokens per lane)
@@ -582,7 +641,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float kh = sK[j * cLDK + cc] * s_cr[j];
     sK[j * cLDK + cc] = kh;
     sQ[j * cLDK + cc] *= s_qn[j];
-    sW[j * cLDK + cc] = s_beta[j] * kh;
+    if (PG) {   // PGDN: the explicit write keys of the record (hi + lo)
+      const uint8_t* rec = g.w.rec + (size_t)task * g.w.recb;
+      const uint32_t off = (cc >> 6) * 8192 + umma::sw128_offset(j, cc & 63);
+      sW[j * cLDK + cc] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(rec + rWF + off)) +
+                          __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(rec + rWF + 16384 + off));
+    } else {
+      sW[j * cLDK + cc] = s_beta[j] * kh;
+    }
   }
   cpa_wait_all();
   __syncthreads();
@@ -654,6 +720,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float xv = xw[c0];
       const float dw = sY[j * cLDK + c0] + ew * xv;
       sY[j * cLDK + c0] = dw;
+      if (PG) g.w.DW[(size_t)task * 8192 + j * 128 + c0] = dw;
       dwk += dw * sK[j * cLDK + c0];
       xww += xv * sW[j * cLDK + c0];
     }
@@ -692,6 +759,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // KLA: beta = eta / (s + eps): d eta = d beta / (s + eps), ds = -d beta eta / (s + eps)^2
     const float se = s_s[j] + a.eps;
     const float ds2 = VARIANT == DR_KLA ? -2.f * db * s_eta[j] / (se * se) : 0.f;
+    const float bgain = PG ? 0.f : beta;   // PGDN: the gain's terms come in pgdn_gain_bwd
     float dkh[32], xk = 0.f, dot = 0.f;
     float xkr[32];
 #pragma unroll
@@ -706,7 +774,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float xkv = xkr[q];
       const float kh = sK[j * cLDK + c0];
       xk += xkv * kh;
-      dkh[q] = sX[j * cLDK + c0] - eg * xkv + beta * sY[j * cLDK + c0] + ds2 * kh;
+      dkh[q] = sX[j * cLDK + c0] - eg * xkv + bgain * sY[j * cLDK + c0] + ds2 * kh;
       dot += dkh[q] * kh;
     }
     xk += __shfl_xor_sync(0xffffffffu, xk, 1);
@@ -718,12 +786,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int q = 0; q < 32; ++q) {
         const int c0 = 32 * part + q;
-        // k^ = k cr: dk = (dk^ - k^ (k^ . dk^)) cr  (k^ is unit-norm then)
-        dkrow[c0] = a.k_l2norm ? (dkh[q] - sK[j * cLDK + c0] * dot) * cr : dkh[q];
+        // k^ = k cr: dk = (dk^ - k^ (k^ . dk^)) cr  (k^ is unit-norm then); PGDN keeps
+        // dL/dk^ of the memory part here for pgdn_gain_bwd
+        dkrow[c0] = (a.k_l2norm && !PG) ? (dkh[q] - sK[j * cLDK + c0] * dot) * cr : dkh[q];
       }
       if (part == 0) {
         s_dg[j] -= eg * xk;
-        g.deta[tok(a, b, t0 + j, h)] = VARIANT == DR_KLA ? db / se : db;
+        if (!PG) g.deta[tok(a, b, t0 + j, h)] = VARIANT == DR_KLA ? db / se : db;
       }
     }
   }
@@ -802,23 +871,167 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// ================================================================= pgdn_gain_bwd
+// One CTA per (b, h), a thread per key channel, chunks in reverse.  Per chunk the
+// statistic A_t is recomputed forward from its chunk-start value (the forward's
+// record), then the tokens are walked backwards (PDN notes Eq. (9)):
+//   r = ln max(A, floor) - mu,  B = exp(-ln(x) r / (1 + |r|)),  w = eta B . k^
+//   d eta  = sum_i B k^ dw,   dr = -ln(x) B eta k^ dw / (1 + |r|)^2,
+//   dA_t = dA + [A > floor] dr / A,   d mu -= [A > floor] dr,
+//   d alphaP = sum_i A_{t-1} dA_t,   d betaP = sum_i k^2 dA_t,
+//   dk^ += eta B dw + 2 betaP k^ dA_t,   dA <- alphaP dA_t (to token t-1),
+// then the key norm; sums over channels take a warp shuffle and four warp
+// partials in a fixed order.  dA at the row start is dL/dA_0.
+constexpr int kGainSmemF = 4 * 64 * 128 + 4 * 64 * 4;
+
+__global__ void __launch_bounds__(128, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
+  extern __shared__ __align__(16) float smf[];
+  float* sK = smf;                  // k^ [t][i]
+  float* sDW = sK + 64 * 128;       // dL/dw [t][i]
+  float* sDK = sDW + 64 * 128;      // dL/dk^ [t][i]: the memory part, then the total
+  float* sA = sDK + 64 * 128;       // A_t [t][i]
+  float* sPart = sA + 64 * 128;     // [warp][t][3]: d eta, d alphaP, d betaP partials
+  __shared__ float s_aP[64], s_bP[64], s_eta[64], s_cr[64], s_mu[4];
+  const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
+  const int bh = blockIdx.x, b = bh / a.H, h = bh % a.H;
+  const int NC = (a.T + 63) / 64;
+  const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
+  const float mu_h = a.mu[h];
+  float dA = g.daux_T ? g.daux_T[(size_t)bh * 128 + i] : 0.f;
+  float dmu = 0.f;
+  for (int c = NC - 1; c >= 0; --c) {
+    const size_t ri = (size_t)bh * NC + c;
+    const int t0 = 64 * c, Cc = min(64, a.T - t0);
+    __syncthreads();
+    if (i < 64) {
+      const bool live = i < Cc;
+      const long ti = tok(a, b, t0 + (live ? i : 0), h);
+      s_aP[i] = live ? a.alphaP[ti] : 1.f;
+      s_bP[i] = live ? a.betaP[ti] : 0.f;
+      s_eta[i] = live ? a.eta[ti] : 0.f;
+      s_cr[i] = live ? g.w.CR[ri * 64 + i] : 0.f;
+    }
+    for (int e = i; e < 64 * 32; e += 128) {   // dL/dw and the memory part of dL/dk^
+      const int t = e >> 5, c4 = 4 * (e & 31);
+      const bool live = t < Cc;
+      cpa16(sDW + t * 128 + c4, g.w.DW + ri * 8192 + t * 128 + c4, live ? 16 : 0);
+      cpa16(sDK + t * 128 + c4, g.dk + tok(a, b, t0 + (live ? t : 0), h) * 128 + c4, live ? 16 : 0);
+    }
+    cpa_wait_all();
+    __syncthreads();
+    for (int e = i; e < 64 * 16; e += 128) {   // k^ = k cr
+      const int t = e >> 4, c0 = 8 * (e & 15);
+      float f[8];
+      if (t < Cc) {
+        unpack8(*reinterpret_cast<const uint4*>(K + tok(a, b, t0 + t, h) * 128 + c0), f);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) f[q] = 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sK[t * 128 + c0 + q] = f[q] * s_cr[t];
+    }
+    __syncthreads();
+    // the statistic over the chunk from its chunk-start value
+    const float A0 = reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rAuxF)[256 + i];
+    {
+      float A = A0;
+      for (int t = 0; t < Cc; ++t) {
+        const float kv = sK[t * 128 + i];
+        A = s_aP[t] * A + s_bP[t] * kv * kv;
+        sA[t * 128 + i] = A;
+      }
+    }
+    // backwards over the chunk's tokens
+    for (int t = Cc - 1; t >= 0; --t) {
+      const float A = sA[t * 128 + i], Ap = t > 0 ? sA[(t - 1) * 128 + i] : A0;
+      const float rr = logf(fmaxf(A, a.log_floor)) - mu_h;
+      const float den = 1.f + fabsf(rr);
+      const float Bv = expf(-a.ln_x * rr / den);
+      const float dwv = sDW[t * 128 + i], kv = sK[t * 128 + i], et = s_eta[t];
+      const float drr = -a.ln_x * Bv * (et * kv * dwv) / (den * den);
+      const bool above = A > a.log_floor;
+      const float dAt = dA + (above ? drr / A : 0.f);
+      if (above) dmu -= drr;
+      sDK[t * 128 + i] += et * Bv * dwv + 2.f * s_bP[t] * kv * dAt;
+      float ceta = Bv * kv * dwv, caP = Ap * dAt, cbP = kv * kv * dAt;
+      ceta = warp_sum(ceta);
+      caP = warp_sum(caP);
+      cbP = warp_sum(cbP);
+      if (lane == 0) {
+        sPart[(warp * 64 + t) * 4 + 0] = ceta;
+        sPart[(warp * 64 + t) * 4 + 1] = caP;
+        sPart[(warp * 64 + t) * 4 + 2] = cbP;
+      }
+      dA = s_aP[t] * dAt;
+    }
+    __syncthreads();
+    if (i < Cc) {   // per-token sums over the four warps, in order
+      const long ti = tok(a, b, t0 + i, h);
+      float se = 0.f, sa = 0.f, sb = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        se += sPart[(w * 64 + i) * 4 + 0];
+        sa += sPart[(w * 64 + i) * 4 + 1];
+        sb += sPart[(w * 64 + i) * 4 + 2];
+      }
+      g.deta[ti] = se;
+      g.daP[ti] = sa;
+      g.dbP[ti] = sb;
+    }
+    // the key norm: warp w takes tokens 16 w .. 16 w + 15, a lane four channels each
+    for (int tt = 0; tt < 16; ++tt) {
+      const int t = 16 * warp + tt;
+      if (t >= Cc) break;
+      float dot = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) dot += sK[t * 128 + lane + 32 * m] * sDK[t * 128 + lane + 32 * m];
+      dot = warp_sum(dot);
+      const float cr = s_cr[t];
+      float* dkrow = g.dk + tok(a, b, t0 + t, h) * 128;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int ch = lane + 32 * m;
+        const float v = sDK[t * 128 + ch];
+        dkrow[ch] = a.k_l2norm ? (v - sK[t * 128 + ch] * dot) * cr : v;
+      }
+    }
+  }
+  if (g.daux0) g.daux0[(size_t)bh * 128 + i] = dA;
+  dmu = warp_sum(dmu);
+  if (lane == 0) s_mu[warp] = dmu;
+  __syncthreads();
+  if (i == 0) g.w.MU[bh] = s_mu[0] + s_mu[1] + s_mu[2] + s_mu[3];
+}
+
+// dL/dmu_h: the rows' parts summed over the batch in order
+__global__ void pgdn_dmu_kernel(FwdArgs a, BwdArgs g) {
+  const int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h >= a.H) return;
+  float s = 0.f;
+  for (int b = 0; b < a.B; ++b) s += g.w.MU[(size_t)b * a.H + h];
+  g.dmu[h] = s;
+}
+
 }  // namespace
 
 bool chunk_bwd_supported(int variant, int dtype, int dk, int dv, int chunk) {
-  return (variant == DR_GDN || variant == DR_KLA) && dtype == DR_BF16 && dk == 128 && dv == 128 &&
-         chunk == 64;
+  return (variant == DR_GDN || variant == DR_KLA || variant == DR_PGDN) && dtype == DR_BF16 &&
+         dk == 128 && dv == 128 && chunk == 64;
 }
 
-size_t chunk_bwd_workspace_bytes(int B, int T, int H) {
-  const size_t n = (size_t)B * H * ((T + 63) / 64);
-  return (n * kBwdPerRec + 255) / 256 * 256;
+size_t chunk_bwd_workspace_bytes(int variant, int B, int T, int H) {
+  const long n = (long)B * H * ((T + 63) / 64);
+  return bwd_layout(nullptr, n, B * H, variant == DR_PGDN, nullptr);
 }
 
-cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* dS_final, float* dq,
-                             float* dk, float* dv, float* dla, float* deta, float* dS0,
-                             void* workspace, cudaStream_t st) {
+cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* dS_final,
+                             const dr_grads& gr, void* workspace, cudaStream_t st) {
   const long n = (long)fa.B * fa.H * ((fa.T + 63) / 64);
-  BwdArgs g{d_out, dS_final, dq, dk, dv, dla, deta, dS0, bwd_ws(workspace, n)};
+  const bool pg = fa.variant == DR_PGDN;
+  BwdArgs g{d_out,      dS_final,    gr.dq,      gr.dk,      gr.dv,     gr.d_log_alpha,
+            gr.d_eta,   gr.d_init_state, gr.d_alphaP, gr.d_betaP, gr.d_mu, gr.d_aux_init,
+            gr.d_aux_final, bwd_ws(workspace, n, fa.B * fa.H, pg)};
   // the forward again: the records, the state at every chunk start and E (no
   // output, no final state)
   FwdArgs a = fa;
@@ -831,9 +1044,18 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
   cudaError_t e = launch_chunk_tc_split(a, workspace, st);
   if (e != cudaSuccess) return e;
   const size_t c_smem = (size_t)kCarrySmemF * 4, s_smem = (size_t)kStateSmemF * 4,
-               l_smem = (size_t)kLocalSmemF * 4;
-  if ((e = cudaFuncSetAttribute(bwd_carry_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)c_smem)) != cudaSuccess ||
+               l_smem = (size_t)kLocalSmemF * 4, p_smem = (size_t)kGainSmemF * 4;
+  if ((e = cudaFuncSetAttribute(bwd_carry_kernel<false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c_smem)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(bwd_carry_kernel<true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c_smem)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(bwd_local_kernel<DR_PGDN>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l_smem)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(pgdn_gain_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)p_smem)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(bwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)s_smem)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(bwd_local_kernel<DR_GDN>,
@@ -843,12 +1065,20 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l_smem)) !=
           cudaSuccess)
     return e;
-  bwd_carry_kernel<<<fa.B * fa.H * 4, kBwdThreads, c_smem, st>>>(fa, g);
-  bwd_state_kernel<<<(unsigned)n, kBwdThreads, s_smem, st>>>(fa, g);
-  if (fa.variant == DR_KLA)
-    bwd_local_kernel<DR_KLA><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
+  if (pg)
+    bwd_carry_kernel<true><<<fa.B * fa.H * 4, kBwdThreads, c_smem, st>>>(fa, g);
   else
+    bwd_carry_kernel<false><<<fa.B * fa.H * 4, kBwdThreads, c_smem, st>>>(fa, g);
+  bwd_state_kernel<<<(unsigned)n, kBwdThreads, s_smem, st>>>(fa, g);
+  if (fa.variant == DR_KLA) {
+    bwd_local_kernel<DR_KLA><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
+  } else if (pg) {
+    bwd_local_kernel<DR_PGDN><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
+    pgdn_gain_bwd_kernel<<<fa.B * fa.H, 128, p_smem, st>>>(fa, g);
+    pgdn_dmu_kernel<<<(fa.H + 127) / 128, 128, 0, st>>>(fa, g);
+  } else {
     bwd_local_kernel<DR_GDN><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
+  }
   return cudaGetLastError();
 }
 

@@ -26,10 +26,9 @@ cudaError_t launch_kalman(const FwdArgs& a, int dtype, cudaStream_t st);
 bool kdn_split_supported(int variant, int dtype, int dk, int dv, int chunk);
 size_t kdn_split_workspace_bytes(int B, int T, int H);
 bool chunk_bwd_supported(int variant, int dtype, int dk, int dv, int chunk);
-size_t chunk_bwd_workspace_bytes(int B, int T, int H);
-cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* dS_final, float* dq,
-                             float* dk, float* dv, float* dla, float* deta, float* dS0,
-                             void* workspace, cudaStream_t st);
+size_t chunk_bwd_workspace_bytes(int variant, int B, int T, int H);
+cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* dS_final,
+                             const dr_grads& g, void* workspace, cudaStream_t st);
 
 namespace {
 
@@ -226,16 +225,15 @@ int dr_decode_step(const void* q, const void* k, const void* v, const float* log
 size_t dr_chunk_bwd_workspace_bytes(int variant, int dtype, int B, int T, int H, int dk, int dv,
                                     int chunk) {
   if (B < 1 || T < 1 || H < 1 || !chunk_bwd_supported(variant, dtype, dk, dv, chunk)) return 0;
-  return chunk_bwd_workspace_bytes(B, T, H);
+  return chunk_bwd_workspace_bytes(variant, B, T, H);
 }
 
 int dr_chunk_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
                  const dr_params* gp, int variant, float eps, const float* init_state,
-                 const void* d_out, const float* d_final_state, float* dq, float* dk, float* dv,
-                 float* d_log_alpha, float* d_eta, float* d_init_state, int B, int T, int H,
-                 int dk_, int dv_, int chunk, dr_stream_t stream) {
-  if (!gp || !q || !k || !v || !log_alpha || !d_out || !dq || !dk || !dv || !d_log_alpha ||
-      !d_eta)
+                 const void* d_out, const float* d_final_state, const dr_grads* g, int B, int T,
+                 int H, int dk_, int dv_, int chunk, dr_stream_t stream) {
+  if (!gp || !g || !q || !k || !v || !log_alpha || !d_out || !g->dq || !g->dk || !g->dv ||
+      !g->d_log_alpha || !g->d_eta)
     return DR_ERR_NULL;
   if (gp->dtype != DR_FP32 && gp->dtype != DR_BF16) return DR_ERR_DTYPE;
   if (B < 1 || T < 1 || H < 1 || !dim_ok(dk_) || !dim_ok(dv_)) return DR_ERR_SHAPE;
@@ -245,17 +243,18 @@ int dr_chunk_bwd(const void* q, const void* k, const void* v, const float* log_a
   int st = check_gates(gp, variant);
   if (st != DR_OK) return st;
   if (!chunk_bwd_supported(variant, gp->dtype, dk_, dv_, chunk)) return DR_ERR_UNSUPPORTED;
+  if (variant == DR_PGDN && (!g->d_alphaP || !g->d_betaP || !g->d_mu)) return DR_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
-      !aligned16(d_out) || !aligned16(d_final_state) || !aligned16(dq) || !aligned16(dk) ||
-      !aligned16(dv) || !aligned16(init_state) || !aligned16(d_init_state))
+      !aligned16(d_out) || !aligned16(d_final_state) || !aligned16(g->dq) || !aligned16(g->dk) ||
+      !aligned16(g->dv) || !aligned16(init_state) || !aligned16(g->d_init_state))
     return DR_ERR_ALIGN;
-  const size_t need = chunk_bwd_workspace_bytes(B, T, H);
+  const size_t need = chunk_bwd_workspace_bytes(variant, B, T, H);
   if (!gp->workspace || gp->workspace_bytes < need) return DR_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(gp->workspace) & 255u) return DR_ERR_ALIGN;
   FwdArgs a = make_args(q, k, v, log_alpha, gp, variant, eps, B, T, H, dk_, dv_, chunk);
   a.S0 = init_state;
-  cudaError_t err = launch_chunk_bwd(a, d_out, d_final_state, dq, dk, dv, d_log_alpha, d_eta,
-                                     d_init_state, gp->workspace,
+  a.aux0 = gp->aux_init;
+  cudaError_t err = launch_chunk_bwd(a, d_out, d_final_state, *g, gp->workspace,
                                      reinterpret_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? DR_OK : DR_ERR_CUDA;
 }

@@ -70,10 +70,20 @@ _lib.dr_chunk_fwd_path.argtypes = [c_int] * 5
 _lib.dr_chunk_fwd_path.restype = c_char_p
 _lib.dr_chunk_fwd_noalloc.argtypes = _lib.dr_chunk_fwd.argtypes
 _lib.dr_chunk_fwd_noalloc.restype = c_int
+
+
+class DrGrads(ctypes.Structure):
+    """Mirror of dr_grads (include/dr.h): device pointers of the backward's outputs."""
+    _fields_ = [("dq", c_void_p), ("dk", c_void_p), ("dv", c_void_p), ("d_log_alpha", c_void_p),
+                ("d_eta", c_void_p), ("d_init_state", c_void_p), ("d_alphaP", c_void_p),
+                ("d_betaP", c_void_p), ("d_mu", c_void_p), ("d_aux_init", c_void_p),
+                ("d_aux_final", c_void_p)]
+
+
 _lib.dr_chunk_bwd.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, ctypes.POINTER(DrParams),
-                             c_int, ctypes.c_float, c_void_p, c_void_p, c_void_p, c_void_p,
-                             c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
-                             c_int, c_int, c_int, c_int, c_void_p]
+                             c_int, ctypes.c_float, c_void_p, c_void_p, c_void_p,
+                             ctypes.POINTER(DrGrads), c_int, c_int, c_int, c_int, c_int, c_int,
+                             c_void_p]
 _lib.dr_chunk_bwd.restype = c_int
 _lib.dr_chunk_bwd_workspace_bytes.argtypes = [c_int] * 8
 _lib.dr_chunk_bwd_workspace_bytes.restype = c_size_t
@@ -181,14 +191,21 @@ def dr_set_chain_fault_for_testing(withhold_flag: int, wait_ns: int) -> int:
     return _lib.dr_set_chain_fault_for_testing(int(withhold_flag), int(wait_ns))
 
 
+def make_grads(**ptrs) -> DrGrads:
+    """A dr_grads with the given fields set (tensors or raw addresses; others NULL)."""
+    g = DrGrads()
+    for name, value in ptrs.items():
+        setattr(g, name, _ptr(value))
+    return g
+
+
 def dr_chunk_bwd(q, k, v, log_alpha, params: DrParams, variant: int, eps: float, init_state,
-                 d_out, d_final_state, dq, dk, dv, d_log_alpha, d_eta, d_init_state, B: int,
-                 T: int, H: int, dk_: int, dv_: int, chunk: int, stream=None) -> int:
+                 d_out, d_final_state, grads: DrGrads, B: int, T: int, H: int, dk: int, dv: int,
+                 chunk: int, stream=None) -> int:
     return _lib.dr_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), ctypes.byref(params),
                              int(variant), float(eps), _ptr(init_state), _ptr(d_out),
-                             _ptr(d_final_state), _ptr(dq), _ptr(dk), _ptr(dv),
-                             _ptr(d_log_alpha), _ptr(d_eta), _ptr(d_init_state), B, T, H, dk_,
-                             dv_, chunk, _stream(stream))
+                             _ptr(d_final_state), ctypes.byref(grads), B, T, H, dk, dv, chunk,
+                             _stream(stream))
 
 
 def dr_chunk_bwd_workspace_bytes(variant, dtype, B, T, H, dk, dv, chunk) -> int:

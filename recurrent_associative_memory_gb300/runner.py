@@ -97,11 +97,13 @@ def bwd_workspace_for(inp: dict, chunk=None):
     return torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
 
 
-def chunk_bwd(inp: dict, d_out, *, d_final_state=None, init_state=None, want_dS0=True,
-              chunk=None, stream=None, workspace="auto", grads=None):
+def chunk_bwd(inp: dict, d_out, *, d_final_state=None, init_state=None, aux_init=None,
+              d_aux_final=None, want_dS0=True, chunk=None, stream=None, workspace="auto",
+              grads=None):
     """Run dr_chunk_bwd on a device input dict; returns a dict of fp32 gradients
-    (dq, dk, dv, dlog_alpha, deta and, with want_dS0, dS0).  ``grads`` may hold
-    preallocated output tensors under the same names."""
+    (dq, dk, dv, dlog_alpha, deta, with want_dS0 dS0, and for PGDN dalphaP,
+    dbetaP, dmu, daux0).  ``grads`` may hold preallocated output tensors under
+    the same names."""
     q, k, v = inp["q"], inp["k"], inp["v"]
     B, T, H, dk = k.shape
     dv = v.shape[-1]
@@ -116,12 +118,20 @@ def chunk_bwd(inp: dict, d_out, *, d_final_state=None, init_state=None, want_dS0
     g.setdefault("deta", torch.empty(B, T, H, **f32))
     if want_dS0:
         g.setdefault("dS0", torch.empty(B, H, dk, dv, **f32))
-    p = params_for(inp)
+    if inp["variant"] == "pgdn":
+        g.setdefault("dalphaP", torch.empty(B, T, H, **f32))
+        g.setdefault("dbetaP", torch.empty(B, T, H, **f32))
+        g.setdefault("dmu", torch.empty(H, **f32))
+        g.setdefault("daux0", torch.empty(B, H, dk, **f32))
+    p = params_for(inp, aux_init=aux_init)
     if workspace is not None:
         p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    gs = dr.make_grads(dq=g["dq"], dk=g["dk"], dv=g["dv"], d_log_alpha=g["dlog_alpha"],
+                       d_eta=g["deta"], d_init_state=g.get("dS0"), d_alphaP=g.get("dalphaP"),
+                       d_betaP=g.get("dbetaP"), d_mu=g.get("dmu"), d_aux_init=g.get("daux0"),
+                       d_aux_final=d_aux_final)
     st = dr.dr_chunk_bwd(q, k, v, inp["log_alpha"], p, dr.VARIANT_IDS[inp["variant"]],
-                         inp.get("eps", 1e-6), init_state, d_out, d_final_state, g["dq"], g["dk"],
-                         g["dv"], g["dlog_alpha"], g["deta"], g.get("dS0"), B, T, H, dk, dv,
-                         chunk or inp.get("chunk", 64), stream)
+                         inp.get("eps", 1e-6), init_state, d_out, d_final_state, gs, B, T, H, dk,
+                         dv, chunk or inp.get("chunk", 64), stream)
     dr.check(st, "dr_chunk_bwd")
     return g

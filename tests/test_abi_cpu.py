@@ -179,27 +179,55 @@ def test_backward_refusals_and_workspace_size(dr):
     the workspace it asks for (the forward's record plus the saved per-chunk data)."""
     A = 1 << 20
     p = dr.make_params(dtype=dr.DR_BF16, eta=A)
+    full = dict(dq=A, dk=A, dv=A, d_log_alpha=A, d_eta=A)
 
-    def call(variant=None, B=1, T=64, H=1, d=128, chunk=64, params=None, dq=A, ws=None):
+    def call(variant=None, B=1, T=64, H=1, d=128, chunk=64, params=None, ws=None, **g):
         pp = params or p
         if ws is not None:
             pp.workspace, pp.workspace_bytes = ws
+        grads = dr.make_grads(**{**full, **g})
         return dr.dr_chunk_bwd(A, A, A, A, pp, dr.DR_KLA if variant is None else variant, 1e-6,
-                               None, A, None, dq, A, A, A, A, None, B, T, H, d, d, chunk,
-                               stream=0)
+                               None, A, None, grads, B, T, H, d, d, chunk, stream=0)
 
+    pg = dr.make_params(dtype=dr.DR_BF16, eta=A, alphaP=A, betaP=A, mu=A)
     assert call(dq=None) == dr.DR_ERR_NULL
     assert call(T=0) == dr.DR_ERR_SHAPE
     assert call(chunk=48) == dr.DR_ERR_SHAPE
-    assert call(variant=dr.DR_PGDN, params=dr.make_params(dtype=dr.DR_BF16, eta=A, alphaP=A,
-                                                          betaP=A, mu=A)) == dr.DR_ERR_UNSUPPORTED
+    assert call(variant=dr.DR_KDN, params=dr.make_params(dtype=dr.DR_BF16, omega=A, r=A)) == \
+        dr.DR_ERR_UNSUPPORTED
     assert call(d=64) == dr.DR_ERR_UNSUPPORTED
     assert call(chunk=32) == dr.DR_ERR_UNSUPPORTED
     assert call(params=dr.make_params(dtype=dr.DR_FP32, eta=A)) == dr.DR_ERR_UNSUPPORTED
+    assert call(variant=dr.DR_PGDN, params=pg) == dr.DR_ERR_NULL        # no PGDN gate gradients
     assert call() == dr.DR_ERR_WORKSPACE                                # no workspace
+    # every array on a 256-byte boundary: the record, S_c, E, dS, E dS^T, dO E^T,
+    # dR E^T, gamma <dS, S_c> (PGDN also dL/dw, the key-norm factors, the rows' dL/dmu)
+    al = lambda x: -(-x // 256) * 256  # noqa: E731
+    n, rows = 2 * 3 * 3, 2 * 3
+    arrays = [65536, 32768, 65536, 32768, 16384, 16384]
     need = dr.dr_chunk_bwd_workspace_bytes(dr.DR_KLA, dr.DR_BF16, 2, 130, 3, 128, 128, 64)
-    per_rec = 66560 + 4 * (16384 + 8192 + 16384 + 8192 + 4096 + 4096 + 1)
-    assert need == -(-(2 * 3 * 3 * per_rec) // 256) * 256
+    assert need == al(n * 66560) + sum(al(n * x) for x in arrays) + al(4 * n)
+    need_p = dr.dr_chunk_bwd_workspace_bytes(dr.DR_PGDN, dr.DR_BF16, 2, 130, 3, 128, 128, 64)
+    assert need_p == (al(n * 101376) + sum(al(n * x) for x in arrays) + al(4 * n) + al(n * 32768)
+                      + al(n * 256) + al(4 * rows))
     assert call(ws=(A, 1000)) == dr.DR_ERR_WORKSPACE
     assert call(ws=(A + 16, 1 << 30)) == dr.DR_ERR_ALIGN
-    assert dr.dr_chunk_bwd_workspace_bytes(dr.DR_PGDN, dr.DR_BF16, 1, 64, 1, 128, 128, 64) == 0
+    assert dr.dr_chunk_bwd_workspace_bytes(dr.DR_KDN, dr.DR_BF16, 1, 64, 1, 128, 128, 64) == 0
+
+
+def test_grads_struct_layout_matches_c(dr):
+    fields = [f for f, _ in dr.DrGrads._fields_]
+    src = "#include <stdio.h>\n#include <stddef.h>\n#include \"dr.h\"\nint main(void){\n"
+    src += 'printf("%zu\\n", sizeof(dr_grads));\n'
+    for f in fields:
+        src += f'printf("%zu\\n", offsetof(dr_grads, {f}));\n'
+    src += "return 0;}\n"
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "g.c")
+        exe = os.path.join(d, "g")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
+        out = [int(x) for x in subprocess.run([exe], capture_output=True, text=True,
+                                              check=True).stdout.split()]
+    assert out[0] == ctypes.sizeof(dr.DrGrads)
+    assert out[1:] == [getattr(dr.DrGrads, f).offset for f in fields]
