@@ -173,14 +173,27 @@ def fwd_bytes(wl, variant, with_final=True):
     return total
 
 
-def bwd_bytes(wl):
+def bwd_bytes(wl, variant="kla"):
     """Bytes one backward call must move: q, k, v and dL/do in (the input dtype) and
-    the two gates; dq, dk, dv (fp32), d log alpha and d eta out; the initial state
-    and dL/dS_T in, dL/dS_0 out."""
+    the gates; dq, dk, dv (fp32) and the gates' gradients out; the initial state
+    and dL/dS_T in, dL/dS_0 out (PGDN: also mu, A_0 and dL/dA_T in, dL/dmu and
+    dL/dA_0 out)."""
     el = 2 if wl.dtype == "bf16" else 4
     ht = wl.B * wl.T * wl.H
-    per_ht = (2 * wl.dk + 2 * wl.dv) * el + 8 + (2 * wl.dk + wl.dv) * 4 + 8
-    return ht * per_ht + 3 * wl.B * wl.H * wl.dk * wl.dv * 4
+    gates = gate_bytes(variant, wl.dk)
+    per_ht = (2 * wl.dk + 2 * wl.dv) * el + gates + (2 * wl.dk + wl.dv) * 4 + gates
+    total = ht * per_ht + 3 * wl.B * wl.H * wl.dk * wl.dv * 4
+    if variant == "pgdn":
+        total += 2 * wl.H * 4 + 3 * wl.B * wl.H * wl.dk * 4
+    return total
+
+
+def bwd_kernels_per_call(variant):
+    """libdr kernels one dr_chunk_bwd call launches: the forward again (prep and
+    carry; PGDN also its statistic's map and scan), the reverse carry, the state
+    products, the local gradients (PGDN also its statistic's adjoint and the
+    d mu sum)."""
+    return 9 if variant == "pgdn" else 5
 
 
 def decode_bytes(wl, variant="kla"):
@@ -316,8 +329,14 @@ def _oracle_bwd_parity(job):
     f = lambda t: None if t is None else np.asarray(t, dtype=np.float64)  # noqa: E731
     g = obw.tokenwise_backward(f(inp["q"]), f(inp["k"]), f(inp["v"]), f(inp["log_alpha"]),
                                variant, f(dO), f(dS), eta=f(inp["eta"]), eps=inp["eps"],
-                               q_l2norm=inp["q_l2norm"], k_l2norm=inp["k_l2norm"], S0=f(S0))
-    return tag, {k: g[k] for k in ("dq", "dk", "dv", "dlog_alpha", "deta", "dS0")}
+                               q_l2norm=inp["q_l2norm"], k_l2norm=inp["k_l2norm"], S0=f(S0),
+                               alphaP=f(inp.get("alphaP")), betaP=f(inp.get("betaP")),
+                               mu=f(inp.get("mu")), x=inp.get("x", 1.5),
+                               log_floor=inp.get("log_floor", 1e-12))
+    names = ("dq", "dk", "dv", "dlog_alpha", "deta", "dS0")
+    if variant == "pgdn":
+        names += ("dalphaP", "dbetaP")
+    return tag, {k: g[k] for k in names}
 
 
 def _oracle_parity(job):
@@ -577,7 +596,7 @@ def forward_entry(fw, var_ms, pk, launches):
 BWD_GRADS = ("dq", "dk", "dv", "dlog_alpha", "deta", "dS0")
 
 
-def time_backward(torch, dr, runner, fw, steps, stream, flush, pk, pool_submit):
+def time_backward(torch, dr, runner, fw, steps, stream, flush, pk, pool_submit, n_pairs=2):
     """dr_chunk_bwd on a forward workload's inputs (every variant it lists that the
     backward supports): CUDA-event time per call, L2 flushed between calls; oracle
     jobs for two sampled (b, h) rows per variant.  Returns (entry, gpu rows)."""
@@ -588,7 +607,7 @@ def time_backward(torch, dr, runner, fw, steps, stream, flush, pk, pool_submit):
     S0 = 0.3 * torch.randn(wl.B, wl.H, wl.dk, wl.dv, generator=gen)
     dOd, dSd, S0d = dO.cuda(), dS.cuda(), S0.cuda()
     entry, rows = {"workload": wl.name, "variants": {}}, {}
-    pairs = sampled_pairs(wl.B, wl.H, 2)
+    pairs = sampled_pairs(wl.B, wl.H, n_pairs)
     for v in fw.variants:
         ws = runner.bwd_workspace_for(fw.dev[v])
         if ws is None:
@@ -611,15 +630,16 @@ def time_backward(torch, dr, runner, fw, steps, stream, flush, pk, pool_submit):
         torch.cuda.synchronize()
         dr.check(dr.dr_get_device_status(), "backward")
         ms = statistics.mean(s_.elapsed_time(e_) for s_, e_ in ev)
-        byt = bwd_bytes(wl)
+        byt = bwd_bytes(wl, v)
         entry["variants"][v] = {"ms": ms, "tokens_per_s": wl.B * wl.T / (ms / 1e3),
                                 "algorithmic_bytes": byt, "gbs": byt / (ms / 1e3) / 1e9,
                                 "frac": byt / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
-                                "launches_per_call": 5}
+                                "launches_per_call": bwd_kernels_per_call(v)}
+        names = BWD_GRADS + (("dalphaP", "dbetaP") if v == "pgdn" else ())
         for b, h in pairs:
-            rows[(v, b, h)] = {n: (grads[n][b, h] if n == "dS0" else grads[n][b, :, h])
-                               .double().cpu().numpy() for n in BWD_GRADS}
-            pool_submit([((v, b, h), slice_row(fw.host[v], b, h), v,
+            rows[(wl.name, v, b, h)] = {n: (grads[n][b, h] if n == "dS0" else grads[n][b, :, h])
+                                        .double().cpu().numpy() for n in names}
+            pool_submit([((wl.name, v, b, h), slice_row(fw.host[v], b, h), v,
                           dO[b:b + 1, :, h:h + 1].float().numpy(),
                           dS[b:b + 1, h:h + 1].numpy(), S0[b:b + 1, h:h + 1].numpy())])
         del ws
@@ -778,12 +798,13 @@ def main(argv=None):
     configs = {}
 
     # ---------------- the backward (GDN and KLA) on the headline workload
-    bwd_rows = None
+    bwd_rows, bwd_entries = {}, {}
     if not args.no_backward:
-        bent, bwd_rows = time_backward(torch, dr, runner, head, min(args.steps, 20), stream,
-                                       flush, pk, submit_bwd)
+        bent, rows_ = time_backward(torch, dr, runner, head, min(args.steps, 20), stream,
+                                    flush, pk, submit_bwd)
         if bent["variants"]:
-            result["backward"] = bent
+            bwd_entries[bent["workload"]] = bent
+            bwd_rows.update(rows_)
         torch.cuda.empty_cache()
 
     # ---------------- every configuration's workload, timed the same way
@@ -800,6 +821,13 @@ def main(argv=None):
             vms, _ = fw.time(min(args.steps, 20), 3, stream, flush)
             configs[tag] = forward_entry(fw, vms, pk, fw.launches_per_step(nsm))
             configs[tag]["_fw"] = fw
+            if not args.no_backward and "pgdn" in fw.variants:   # PGDN's backward too
+                bent, rows_ = time_backward(torch, dr, runner, fw, min(args.steps, 10), stream,
+                                            flush, pk, submit_bwd, n_pairs=1)
+                if bent["variants"]:
+                    bwd_entries[bent["workload"]] = bent
+                    bwd_rows.update(rows_)
+                torch.cuda.empty_cache()
             # keep only what the parity check reads; free the rest of the device memory
             fw.dev = fw.ws = None
             torch.cuda.empty_cache()
@@ -915,14 +943,16 @@ def main(argv=None):
                     worst["out"] = max(worst["out"], rel_err(go, o[0, :, 0]))
                     worst["state"] = max(worst["state"], rel_err(gS, S[0, 0]))
             configs["4b"]["parity"] = worst
-    if bwd_async and "backward" in result:
-        worst = {n: 0.0 for n in BWD_GRADS}
+    if bwd_entries:
+        result["backward"] = {"workloads": bwd_entries}
+    if bwd_async and bwd_entries:
+        worst = {}
         for a_ in bwd_async:
             for tag, ref in a_.get():
                 gpu = bwd_rows[tag]
-                for n in BWD_GRADS:
-                    r = ref[n][0, 0] if n == "dS0" else ref[n][0, :, 0]
-                    worst[n] = max(worst[n], rel_err(gpu[n], r))
+                for n, r_ in ref.items():
+                    r = r_[0, 0] if n == "dS0" else r_[0, :, 0]
+                    worst[n] = max(worst.get(n, 0.0), rel_err(gpu[n], r))
         result["backward"]["parity"] = worst
     for c in configs.values():
         c.pop("_fw", None)

@@ -174,3 +174,14 @@ def test_backward_parity_row_slice_matches_the_oracle_on_the_full_input():
     for n in ("dq", "dk", "dv", "dlog_alpha", "deta"):
         assert np.allclose(ref[n][0, :, 0], full[n][1, :, 0], rtol=0, atol=1e-10), n
     assert np.allclose(ref["dS0"][0, 0], full["dS0"][1, 0], rtol=0, atol=1e-10)
+
+
+def test_backward_bytes_pgdn_and_kernel_counts():
+    """PGDN's backward also moves alphaP, betaP in and their gradients out (16 more
+    bytes per head-token: 2592), mu / dmu and A_0, dA_T, dA_0; it launches its
+    statistic's map and scan, adjoint and d mu sum besides the five kernels."""
+    wl = W.WORKLOADS["pgdn_bf16"]
+    ht = wl.B * wl.T * wl.H
+    per_bh = 3 * 128 * 128 * 4 + 3 * 128 * 4
+    assert bench.bwd_bytes(wl, "pgdn") == ht * 2592 + wl.B * wl.H * per_bh + 2 * wl.H * 4
+    assert bench.bwd_kernels_per_call("kla") == 5 and bench.bwd_kernels_per_call("pgdn") == 9
