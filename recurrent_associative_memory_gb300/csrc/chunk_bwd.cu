@@ -880,17 +880,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 //   dA_t = dA + [A > floor] dr / A,   d mu -= [A > floor] dr,
 //   d alphaP = sum_i A_{t-1} dA_t,   d betaP = sum_i k^2 dA_t,
 //   dk^ += eta B dw + 2 betaP k^ dA_t,   dA <- alphaP dA_t (to token t-1),
-// then the key norm; sums over channels take a warp shuffle and four warp
-// partials in a fixed order.  dA at the row start is dL/dA_0.
-constexpr int kGainSmemF = 4 * 64 * 128 + 4 * 64 * 4;
+// then the key norm.  The walk backwards is per channel (the chain through dA);
+// the sums over channels follow per token, a warp per 16 tokens, A_{t-1}
+// recomputed from the chunk start.  dA at the row start is dL/dA_0.
+constexpr int kGainSmemF = 4 * 64 * 128;
 
 __global__ void __launch_bounds__(128, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
   extern __shared__ __align__(16) float smf[];
   float* sK = smf;                  // k^ [t][i]
   float* sDW = sK + 64 * 128;       // dL/dw [t][i]
   float* sDK = sDW + 64 * 128;      // dL/dk^ [t][i]: the memory part, then the total
-  float* sA = sDK + 64 * 128;       // A_t [t][i]
-  float* sPart = sA + 64 * 128;     // [warp][t][3]: d eta, d alphaP, d betaP partials
+  float* sA = sDK + 64 * 128;       // A_t [t][i], then dA_t
   __shared__ float s_aP[64], s_bP[64], s_eta[64], s_cr[64], s_mu[4];
   const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
   const int bh = blockIdx.x, b = bh / a.H, h = bh % a.H;
@@ -942,51 +942,62 @@ __global__ void __launch_bounds__(128, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArg
         sA[t * 128 + i] = A;
       }
     }
-    // backwards over the chunk's tokens
+    // backwards over the chunk's tokens: per channel only (the chain through dA);
+    // dA_t replaces A_t, and B k^ dw replaces dL/dw, for the sums over channels
     for (int t = Cc - 1; t >= 0; --t) {
-      const float A = sA[t * 128 + i], Ap = t > 0 ? sA[(t - 1) * 128 + i] : A0;
+      const float A = sA[t * 128 + i];
       const float rr = logf(fmaxf(A, a.log_floor)) - mu_h;
       const float den = 1.f + fabsf(rr);
       const float Bv = expf(-a.ln_x * rr / den);
       const float dwv = sDW[t * 128 + i], kv = sK[t * 128 + i], et = s_eta[t];
       const float drr = -a.ln_x * Bv * (et * kv * dwv) / (den * den);
       const bool above = A > a.log_floor;
-      const float dAt = dA + (above ? drr / A : 0.f);
+      const float dAt = dA + (above ? __fdividef(drr, A) : 0.f);
       if (above) dmu -= drr;
       sDK[t * 128 + i] += et * Bv * dwv + 2.f * s_bP[t] * kv * dAt;
-      float ceta = Bv * kv * dwv, caP = Ap * dAt, cbP = kv * kv * dAt;
-      ceta = warp_sum(ceta);
-      caP = warp_sum(caP);
-      cbP = warp_sum(cbP);
-      if (lane == 0) {
-        sPart[(warp * 64 + t) * 4 + 0] = ceta;
-        sPart[(warp * 64 + t) * 4 + 1] = caP;
-        sPart[(warp * 64 + t) * 4 + 2] = cbP;
-      }
+      sDW[t * 128 + i] = Bv * kv * dwv;
+      sA[t * 128 + i] = dAt;
       dA = s_aP[t] * dAt;
     }
     __syncthreads();
-    if (i < Cc) {   // per-token sums over the four warps, in order
-      const long ti = tok(a, b, t0 + i, h);
-      float se = 0.f, sa = 0.f, sb = 0.f;
+    // per token: d eta = sum B k^ dw, d alphaP = sum A_{t-1} dA_t, d betaP = sum k^2 dA_t,
+    // and the key norm (dk = (dk^ - k^ (k^ . dk^)) cr); warp w takes tokens 16 w .. + 15,
+    // a lane four channels, A_{t-1} recomputed from the chunk start on the way
+    float Ap[4];
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        se += sPart[(w * 64 + i) * 4 + 0];
-        sa += sPart[(w * 64 + i) * 4 + 1];
-        sb += sPart[(w * 64 + i) * 4 + 2];
+    for (int m = 0; m < 4; ++m)
+      Ap[m] = reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rAuxF)[256 + lane + 32 * m];
+    for (int t = 0; t < 16 * warp && t < Cc; ++t) {   // A up to this warp's first token
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float kv = sK[t * 128 + lane + 32 * m];
+        Ap[m] = s_aP[t] * Ap[m] + s_bP[t] * kv * kv;
       }
-      g.deta[ti] = se;
-      g.daP[ti] = sa;
-      g.dbP[ti] = sb;
     }
-    // the key norm: warp w takes tokens 16 w .. 16 w + 15, a lane four channels each
     for (int tt = 0; tt < 16; ++tt) {
       const int t = 16 * warp + tt;
       if (t >= Cc) break;
-      float dot = 0.f;
+      float se = 0.f, sa = 0.f, sb = 0.f, dot = 0.f;
 #pragma unroll
-      for (int m = 0; m < 4; ++m) dot += sK[t * 128 + lane + 32 * m] * sDK[t * 128 + lane + 32 * m];
+      for (int m = 0; m < 4; ++m) {
+        const int ch = lane + 32 * m;
+        const float kv = sK[t * 128 + ch], dAt = sA[t * 128 + ch];
+        se += sDW[t * 128 + ch];
+        sa += Ap[m] * dAt;
+        sb += kv * kv * dAt;
+        dot += kv * sDK[t * 128 + ch];
+        Ap[m] = s_aP[t] * Ap[m] + s_bP[t] * kv * kv;
+      }
+      se = warp_sum(se);
+      sa = warp_sum(sa);
+      sb = warp_sum(sb);
       dot = warp_sum(dot);
+      if (lane == 0) {
+        const long ti = tok(a, b, t0 + t, h);
+        g.deta[ti] = se;
+        g.daP[ti] = sa;
+        g.dbP[ti] = sb;
+      }
       const float cr = s_cr[t];
       float* dkrow = g.dk + tok(a, b, t0 + t, h) * 128;
 #pragma unroll
