@@ -206,7 +206,7 @@ def decode_bytes(wl, variant="kla"):
     return bh * per_bh + (wl.H * 4 if variant in ("pgdn", "pkda") else 0)
 
 
-def kernels_per_call(path, variant, B, H, has_workspace, nsm):
+def kernels_per_call(path, variant, B, H, has_workspace, nsm, NC=0):
     """libdr kernels one dr_chunk_fwd call launches on ``path``.
 
     The two-phase paths launch a prep and a carry kernel; PGDN adds its key
@@ -221,7 +221,25 @@ def kernels_per_call(path, variant, B, H, has_workspace, nsm):
         if 3 * B * H >= nsm or variant == "kda":
             return 2
         return 1 if variant in ("pkda", "ikdn") else 4
-    return 4 if variant == "pgdn" else 2
+    n = 4 if variant == "pgdn" else 2
+    return n + 2 if seg_segments(nsm, B * H, NC) else n
+
+
+def seg_segments(nsm, rows, NC):
+    """Segments per row of the tensor-core path's segment-parallel carry (0: not
+    used).  With few rows (6 rows <= SMs) the carry runs as a first pass, a
+    composition of segment start states and a replay pass (two more launches);
+    the library picks the largest G <= (SMs / rows - 2) / 4 + 2 (at most 64,
+    at least 3) whose segments of ceil(NC / G) chunks are >= 2 long and all
+    non-empty."""
+    if nsm <= 0 or rows * 6 > nsm:
+        return 0
+    G = min((nsm // rows - 2) // 4 + 2, 64)
+    for g in range(G, 2, -1):
+        Ls = -(-NC // g)
+        if Ls >= 2 and (g - 1) * Ls < NC:
+            return g
+    return 0
 
 
 # ---------------------------------------------------------------- clocks
@@ -520,7 +538,8 @@ class Forward:
 
     def launches_per_step(self, nsm):
         wl = self.wl
-        return sum(kernels_per_call(self.paths[v], v, wl.B, wl.H, self.ws is not None, nsm)
+        NC = -(-wl.T // wl.chunk)
+        return sum(kernels_per_call(self.paths[v], v, wl.B, wl.H, self.ws is not None, nsm, NC)
                    for v in self.variants)
 
     def time(self, steps, warmup, stream, flush, on_step_start=None):

@@ -83,6 +83,23 @@ def test_kernels_per_call_counts_every_path():
     assert k("simt_split", "ikdn", 4, 16, True, 152) == 2
     assert k("kalman", "ekdn", 4, 16, False, 152) == 1
     assert k("simt", "kla", 1, 2, False, 152) == 1
+    # few long rows: segment-parallel carry, + segment composition + replay pass
+    assert k("tc_split", "kla", 1, 16, True, 152, 1024) == 4
+    assert k("tc_split", "pgdn", 1, 16, True, 152, 1024) == 6
+    assert k("tc_split", "kla", 8, 8, True, 152, 32) == 2      # 64 rows: one pass
+    assert k("tc_split", "kla", 1, 16, True, 152, 4) == 2      # too short to cut in 3
+
+
+def test_segment_count_rule():
+    """Segments per row: G = (SMs / rows - 2) / 4 + 2, shrunk until the
+    segments (ceil(NC / G) chunks, at least 2) are all non-empty."""
+    s = bench.seg_segments
+    assert s(152, 16, 1024) == 3           # 64K-token prefill, 16 heads
+    assert s(152, 1, 1024) == 38           # one row: 39 would leave the last one empty
+    assert s(152, 26, 1024) == 0           # 6 rows > SMs / 26: one pass
+    assert s(152, 2, 7) == 4               # 7 chunks: segments of 2, 2, 2, 1
+    assert s(152, 2, 5) == 3               # 2, 2, 1
+    assert s(152, 2, 4) == 0               # 3 segments of 2 would leave one empty
 
 
 @pytest.mark.parametrize("variant,gates,aux", [("gdn", 8, 0), ("pgdn", 16, 128), ("kdn", 1028, 128),
