@@ -99,8 +99,9 @@ KERNEL_SOURCES = {
     "chunk_tc_ws": ["chunk_tc_ws.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh"],
     "chunk_tc": ["chunk_tc.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh"],
     "chunk_simt": ["chunk_simt.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh", "chain.cuh"],
-    "chunk_simt_split": ["chunk_simt.cu", "chunk_tc_split.cu", "umma.cuh", "tc_common.cuh",
-                         "dr_common.cuh", "chain.cuh"],
+    "chunk_simt_split": ["chunk_simt.cu", "umma.cuh", "tc_common.cuh", "dr_common.cuh", "chain.cuh"],
+    "chunk_tc_pc_split": ["chunk_tc_pc.cu", "chunk_simt.cu", "chunk_tc_split.cu", "umma.cuh",
+                          "tc_common.cuh", "dr_common.cuh", "chain.cuh"],
     "decode": ["decode.cu", "dr_common.cuh"],
     "kalman": ["kalman.cu", "dr_common.cuh"],
 }
@@ -215,9 +216,9 @@ def kernels_per_call(path, variant, B, H, has_workspace, nsm, NC=0):
     and PKDA / isotropic KDN run the fused kernel alone (KDA: never either).
     Every other path is one kernel.  A memset of the chain flags is not a kernel.
     """
-    if not has_workspace or path not in ("tc_split", "simt_split"):
+    if not has_workspace or path not in ("tc_split", "simt_split", "tc_pc_split"):
         return 1
-    if path == "simt_split":
+    if path in ("simt_split", "tc_pc_split"):
         if 3 * B * H >= nsm or variant == "kda":
             return 2
         return 1 if variant in ("pkda", "ikdn") else 4

@@ -314,13 +314,14 @@ const char *dr_status_string(int status);
  *          without a workspace the same shapes take
  * "tc_ws"  the warp-specialised single-kernel tcgen05 path (GDN, KLA), or
  * "tc"     the phase-sequential tcgen05 kernel (PGDN)
- * "simt_split" two-phase Diagonal KDN / KDA / PKDA path (bf16 or fp32,
- *          dk = dv = 128, chunk 64) when the workspace is supplied: every
- *          chunk's local work on fp32 CUDA cores (the KDN variance or PKDA key
- *          statistic at each chunk start handed over between chunks; with few
- *          rows, 3 B H < SM count, KDN takes chunk maps and a scan instead and
- *          PKDA the fused kernel), then the state carry -- the tcgen05 carry
- *          for bf16 inputs, fp32 CUDA cores for fp32
+ * "tc_pc_split" two-phase per-channel-decay path (Diagonal KDN, KDA, PKDA,
+ *          isotropic KDN; bf16, dk = dv = 128, chunk 64) when the workspace is
+ *          supplied: every chunk's local work in a tcgen05 prep (the KDN
+ *          variance, PKDA key statistic or isotropic variance at each chunk
+ *          start handed over between chunks; with few rows, 3 B H < SM count,
+ *          Diagonal KDN takes chunk maps and a scan instead and PKDA / isotropic
+ *          KDN the fused kernel), then the tcgen05 state carry
+ * "simt_split" the same two phases for fp32 inputs on fp32 CUDA cores
  * "simt"   fp32 CUDA-core kernel (everything else: fp32 mode, KDN / KDA / PKDA
  *          without a workspace, dk or dv 64, other chunk sizes)
  * "kalman" the exact Kalman memory, token by token (DR_EKDN, any shape). */

@@ -1663,6 +1663,7 @@ cudaError_t launch_chunk_simt(const FwdArgs& a, int dtype, cudaStream_t st) {
 namespace dr {
 
 cudaError_t launch_carry_kdn_tc(const FwdArgs& a, void* workspace, cudaStream_t st);
+cudaError_t launch_pc_prep(const FwdArgs& a, void* workspace, uint32_t* chain, int nsm, cudaStream_t st);
 
 bool kdn_split_supported(int variant, int dtype, int dk, int dv, int chunk) {
   return (variant == DR_KDN || variant == DR_KDA || variant == DR_PKDA || variant == DR_IKDN) &&
@@ -1711,8 +1712,8 @@ cudaError_t launch_kdn_split(const FwdArgs& a, int dtype, void* workspace, cudaS
     chunk_simt_kernel<128, T_, true><<<pgrid, kThreads, psmem, st>>>(a, ws, chain);       \
     if ((err = cudaGetLastError()) != cudaSuccess) return err;                             \
   }
-  if (dtype == DR_BF16) {   // bf16 records -> the tensor-core carry
-    DR_KDN_PREP(__nv_bfloat16)
+  if (dtype == DR_BF16) {   // tensor-core prep, bf16 records -> the tensor-core carry
+    if ((err = launch_pc_prep(a, ws, chain, nsm, st)) != cudaSuccess) return err;
     return launch_carry_kdn_tc(a, ws, st);
   }
   DR_KDN_PREP(float)

@@ -137,7 +137,8 @@ size_t dr_chunk_fwd_workspace_bytes(int variant, int dtype, int B, int T, int H,
 const char* dr_chunk_fwd_path(int variant, int dtype, int dk, int dv, int chunk) {
   if (variant == DR_EKDN) return "kalman";
   if (chunk_tc_split_supported(variant, dtype, dk, dv, chunk)) return "tc_split";
-  if (kdn_split_supported(variant, dtype, dk, dv, chunk)) return "simt_split";
+  if (kdn_split_supported(variant, dtype, dk, dv, chunk))
+    return dtype == DR_BF16 ? "tc_pc_split" : "simt_split";
   if (chunk_tc_ws_supported(variant, dtype, dk, dv, chunk)) return "tc_ws";
   return chunk_tc_supported(variant, dtype, dk, dv, chunk) ? "tc" : "simt";
 }

@@ -152,6 +152,20 @@ static inline bool make_map(CUtensorMap* m, const void* ptr, int B, int T, int H
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [B, T, H, 128] fp32 tensor (per-channel gates), box of 128 features x 1 head x
+// 64 tokens x 1 batch without swizzle: lands as a row-major [64][128] fp32 tile
+// (32 KB); tokens past the end read as zero.
+static inline bool make_map_f32(CUtensorMap* m, const void* ptr, int B, int T, int H) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {128, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[3] = {512, (cuuint64_t)H * 512, (cuuint64_t)T * H * 512};
+  cuuint32_t box[4] = {128, 1, 64, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(ptr), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace tc
 }  // namespace dr

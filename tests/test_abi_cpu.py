@@ -97,7 +97,8 @@ def test_status_strings(dr):
                  (1, 1, 8, 2048, 8, 128, 128, 32), (3, 1, 8, 2048, 8, 64, 64, 64),
                  (3, 1, 8, 2048, 8, 128, 128, 32)]:
         assert dr.dr_chunk_fwd_workspace_bytes(*args) == 0, args
-    assert dr.dr_chunk_fwd_path(dr.DR_KDN, dr.DR_BF16, 128, 128, 64) == "simt_split"
+    assert dr.dr_chunk_fwd_path(dr.DR_KDN, dr.DR_BF16, 128, 128, 64) == "tc_pc_split"
+    assert dr.dr_chunk_fwd_path(dr.DR_KDN, dr.DR_FP32, 128, 128, 64) == "simt_split"
     assert dr.dr_chunk_fwd_path(dr.DR_KLA, dr.DR_BF16, 128, 128, 64) == "tc_split"
     assert dr.dr_chunk_fwd_path(dr.DR_PGDN, dr.DR_BF16, 128, 128, 64) == "tc_split"
     assert dr.dr_chunk_fwd_path(dr.DR_KLA, dr.DR_FP32, 64, 64, 64) == "simt"
@@ -105,7 +106,7 @@ def test_status_strings(dr):
     assert dr.dr_chunk_fwd_path(dr.DR_EKDN, dr.DR_FP32, 64, 64, 16) == "kalman"
     assert dr.dr_chunk_fwd_workspace_bytes(7, 1, 4, 2048, 16, 128, 128, 64) == 0
     for vid in (dr.DR_KDA, dr.DR_PKDA, dr.DR_IKDN):
-        assert dr.dr_chunk_fwd_path(vid, dr.DR_BF16, 128, 128, 64) == "simt_split"
+        assert dr.dr_chunk_fwd_path(vid, dr.DR_BF16, 128, 128, 64) == "tc_pc_split"
         assert dr.dr_chunk_fwd_workspace_bytes(vid, 1, 4, 8192, 16, 128, 128, 64) == \
             dr.dr_chunk_fwd_workspace_bytes(3, 1, 4, 8192, 16, 128, 128, 64)
 

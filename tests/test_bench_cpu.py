@@ -76,11 +76,12 @@ def test_kernels_per_call_counts_every_path():
     assert k("tc_split", "pgdn", 4, 16, True, 152) == 4        # + statistic map and scan
     assert k("tc_split", "kla", 8, 8, False, 152) == 1         # no workspace: one kernel
     assert k("tc_ws", "kla", 8, 8, False, 152) == 1
-    assert k("simt_split", "kdn", 4, 16, True, 152) == 2       # variance chained in the prep
-    assert k("simt_split", "kdn", 1, 2, True, 152) == 4        # few rows: map + scan first
-    assert k("simt_split", "kda", 1, 2, True, 152) == 2        # no gain state across chunks
-    assert k("simt_split", "pkda", 1, 2, True, 152) == 1       # few rows: the fused kernel
-    assert k("simt_split", "ikdn", 4, 16, True, 152) == 2
+    assert k("tc_pc_split", "kdn", 4, 16, True, 152) == 2      # variance chained in the prep
+    assert k("tc_pc_split", "kdn", 1, 2, True, 152) == 4       # few rows: map + scan first
+    assert k("tc_pc_split", "kda", 1, 2, True, 152) == 2       # no gain state across chunks
+    assert k("tc_pc_split", "pkda", 1, 2, True, 152) == 1      # few rows: the fused kernel
+    assert k("tc_pc_split", "ikdn", 4, 16, True, 152) == 2
+    assert k("simt_split", "kdn", 4, 16, True, 152) == 2       # fp32: CUDA-core prep
     assert k("kalman", "ekdn", 4, 16, False, 152) == 1
     assert k("simt", "kla", 1, 2, False, 152) == 1
     # few long rows: segment-parallel carry, + segment composition + replay pass

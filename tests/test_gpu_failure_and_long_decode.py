@@ -44,7 +44,7 @@ def test_chained_prep_wait_gives_up_on_a_withheld_flag(rt, variant):
     base = {"kdn": "kdn_bf16", "pkda": "pkda_bf16"}[variant]
     inp = W.generate(W.small(base, B=B, T=T, H=H, seed=41), variant)
     dev = runner.to_device(inp)
-    assert dr.dr_chunk_fwd_path(dr.VARIANT_IDS[variant], dr.DR_BF16, 128, 128, 64) == "simt_split"
+    assert dr.dr_chunk_fwd_path(dr.VARIANT_IDS[variant], dr.DR_BF16, 128, 128, 64) == "tc_pc_split"
     flag = (1 * H + 2) * NC + 2       # row (b = 1, h = 2), the hand-over into chunk 2
     assert dr.dr_get_device_status() == 0
     try:

@@ -324,7 +324,7 @@ def test_kdn_two_phase_and_fused_paths(rt, dtype, workspace):
     dr, runner = rt
     if workspace == "auto":
         assert dr.dr_chunk_fwd_path(dr.DR_KDN, dr.DR_BF16 if dtype == "bf16" else dr.DR_FP32,
-                                    128, 128, 64) == "simt_split"
+                                    128, 128, 64) == ("tc_pc_split" if dtype == "bf16" else "simt_split")
     inp = small_inputs("kdn", dtype, B=2, T=64 * 5 + 13, H=3, seed=301)
     S0, aux0 = random_state(inp, seed=302)
     check_fwd(rt, inp, S0, aux0, workspace=workspace)
@@ -419,7 +419,7 @@ def test_two_phase_random_shapes(rt, variant):
     counts, lengths that end anywhere inside a chunk, one to nine chunks."""
     dr, _ = rt
     vid = dr.VARIANT_IDS[variant]
-    assert dr.dr_chunk_fwd_path(vid, dr.DR_BF16, 128, 128, 64) in ("tc_split", "simt_split")
+    assert dr.dr_chunk_fwd_path(vid, dr.DR_BF16, 128, 128, 64) in ("tc_split", "tc_pc_split")
     g = torch.Generator().manual_seed(900 + vid)
     for case in range(3):
         B = int(torch.randint(1, 3, (1,), generator=g))
