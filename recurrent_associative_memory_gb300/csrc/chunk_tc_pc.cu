@@ -72,6 +72,8 @@ constexpr uint32_t sB = 131072;      // Gram B image: 160 rows x 128, hi (40 KB)
 constexpr uint32_t sLT = sB;                    // after the Gram: L/T fp32 [64][LDL]
 constexpr uint32_t sXS = sB + 64 * LDL * 4;     //   inverse scratch [64][LDX]
 constexpr uint32_t sTi = sB + 32768;            //   T hi | T lo (the W' MMA's B operand)
+constexpr uint32_t sGK = sB + 49152;            //   (Gamma.K) hi [64 tok][128] (two 8 KB
+                                                //   channel blocks), then lo at +16 KB
 constexpr uint32_t sVec = 212992;    // vectors below
 constexpr int kTokVecs = 13;         // per-token vectors of 64 floats
 constexpr int kChVecs = 15;          // per-channel vectors of 128 floats
@@ -165,20 +167,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base_s;
   const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
+  // task -> (row b h, chunk); tickets are chunk-major when chained (32-bit: a
+  // launch has fewer than 2^31 tasks)
+  const int nrow_i = (int)nrow;
   auto decode = [&](long it, int& bh, int& ci) {
+    const int t = (int)it;
     if (chained) {
-      ci = (int)(it / nrow);
-      bh = (int)(it % nrow);
+      ci = t / nrow_i;
+      bh = t - ci * nrow_i;
     } else {
-      bh = (int)(it / NC);
-      ci = (int)(it % NC);
+      bh = t / NC;
+      ci = t - bh * NC;
     }
   };
   // issue counts per barrier (thread 0), for the drain after an abort
   int c_kq = 0, c_la = 0, c_om = 0, c_gram = 0, c_wp = 0;
-  auto load_kq = [&](long it) {
-    int bh, ci;
-    decode(it, bh, ci);
+  auto load_kq = [&](int bh, int ci) {
     const int b = bh / a.H, h = bh % a.H;
     uint8_t* base = sm + sKQ;
     mbar_expect_tx(&bars[B_KQ], 32768);
@@ -188,16 +192,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_load_4d(base + 24576, &tmQ, &bars[B_KQ], 64, h, ci * 64, b);
     ++c_kq;
   };
-  auto load_la = [&](long it) {
-    int bh, ci;
-    decode(it, bh, ci);
+  auto load_la = [&](int bh, int ci) {
     mbar_expect_tx(&bars[B_LA], 32768);
     tma_load_4d(sm + sG, &tmLA, &bars[B_LA], 0, bh % a.H, ci * 64, bh / a.H);
     ++c_la;
   };
-  auto load_om = [&](long it) {
-    int bh, ci;
-    decode(it, bh, ci);
+  auto load_om = [&](int bh, int ci) {
     mbar_expect_tx(&bars[B_OM], 32768);
     tma_load_4d(sm + sA, &tmOM, &bars[B_OM], 0, bh % a.H, ci * 64, bh / a.H);
     ++c_om;
@@ -214,9 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // per-token gates of the next task, held in registers by threads 0..63
   float n_r = 1.f, n_eta = 0.f, n_aP = 1.f, n_bP = 0.f, n_om = 0.f;
-  auto prefetch_gates = [&](long it) {
-    int bh, ci;
-    decode(it, bh, ci);
+  auto prefetch_gates = [&](int bh, int ci) {
     const int i = tid, tok = ci * 64 + i;
     const bool real = i < 64 && tok < a.T;
     const long ti = real ? ((long)(bh / a.H) * a.T + tok) * a.H + (bh % a.H) : 0;
@@ -246,12 +244,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     it = blockIdx.x;
   }
   if (it < ntask) {
+    int bh0, ci0;
+    decode(it, bh0, ci0);
     if (tid == 0) {
-      load_kq(it);
-      load_la(it);
-      if (kKdn) load_om(it);
+      load_kq(bh0, ci0);
+      load_la(bh0, ci0);
+      if (kKdn) load_om(bh0, ci0);
     }
-    if (tid < 64) prefetch_gates(it);
+    if (tid < 64) prefetch_gates(bh0, ci0);
   }
   bool abort = false;
 
@@ -267,6 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       break;
     }
     const long nxt = chained ? s_next : it + gridDim.x;
+    const bool has_next = nxt < ntask;
+    int nbh = 0, nci = 0;
+    if (has_next) decode(nxt, nbh, nci);
 
     // ---- 1. per-token gates and norms
     if (tid < 64) {
@@ -276,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       vaP[tid] = n_aP;
       vbP[tid] = n_bP;
       vom[tid] = n_om;
-      if (nxt < ntask) prefetch_gates(nxt);
+      if (has_next) prefetch_gates(nbh, nci);
     }
     {
       const uint8_t* KQ = sm + sKQ;
@@ -309,6 +312,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         !chain_wait(chain + ri, chain + ntask + 1, g_chain_wait_ns))
       set_status(DR_ERR_TIMEOUT);
     __syncthreads();
+    // the gain state at the chunk start (its load flies under the passes below):
+    // thread c < 128 = channel c (KDN p, PKDA A), isotropic KDN: the head's b (warp 4)
+    float st = 0.f;
+    if ((kKdn || kPkda) && tid < 128) {
+      if (chained)
+        st = ci == 0 ? (a.aux0 ? a.aux0[(long)bh * 128 + tid] : (kKdn ? 1.f : 0.f))
+                     : __ldcg(reinterpret_cast<const float*>(rec + rkP0) + tid);
+      else
+        st = reinterpret_cast<const float*>(rec + rkP0)[tid];
+    }
+    if (kIkdn && warp == 4) {
+      st = 1.f;
+      if (chained)
+        st = ci == 0 ? (a.aux0 ? a.aux0[bh] : 1.f) : __ldcg(reinterpret_cast<const float*>(rec + rkP0));
+    }
     if (kIkdn) {   // mean squared decay of every token (warp w: tokens 8w .. 8w + 7)
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr) {
@@ -322,62 +340,87 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
     }
 
-    // ---- 2. scans: thread c = channel c (cumulative log-decay, KDN variance, PKDA
-    //         statistic); isotropic KDN: warp 4 scans the head variance
+    // ---- 2. scans.  First every term off the recurrences' chains, for all (token,
+    //         channel) at once in the B-image region (free until the B pass): KDN
+    //         a^2 and u = (information scale / r) k^2, PKDA betaP k^2.  Then thread c =
+    //         channel c walks the chunk: cumulative log-decay g, KDN variance, PKDA
+    //         statistic; isotropic KDN: warp 4 scans the head variance.
+    float* fX_ = reinterpret_cast<float*>(sm + sB);   // [64][128] KDN a^2
+    float* fY_ = fX_ + 64 * 128;                      // [64][128] KDN u, PKDA betaP k^2
+    if (kKdn || kPkda) {
+#pragma unroll 2
+      for (int r = 0; r < 4; ++r) {
+        const int u = tid + r * kThreads, i = u >> 4, cg = u & 15, kb = cg >> 3, c8 = (cg & 7) * 8;
+        const int cc = 64 * kb + c8;
+        float k8[8], y[8];
+        unpack8(*reinterpret_cast<const uint4*>(sm + sKQ + kb * 16384 + sw128_offset(i, c8)), k8);
+        const float cr = vcr[i], sc = kKdn ? vus[i] : vbP[i];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float kh = k8[e] * cr;   // normalised first: cr is 1e30 on padding rows
+          y[e] = sc * kh * kh;
+        }
+        float4* yp = reinterpret_cast<float4*>(fY_ + i * 128 + cc);
+        yp[0] = make_float4(y[0], y[1], y[2], y[3]);
+        yp[1] = make_float4(y[4], y[5], y[6], y[7]);
+        if (kKdn) {
+          const float4* lp = reinterpret_cast<const float4*>(fG_ + i * 128 + cc);
+          const float4 l0 = lp[0], l1 = lp[1];
+          float4* xp = reinterpret_cast<float4*>(fX_ + i * 128 + cc);
+          xp[0] = make_float4(__expf(2.f * l0.x), __expf(2.f * l0.y), __expf(2.f * l0.z), __expf(2.f * l0.w));
+          xp[1] = make_float4(__expf(2.f * l1.x), __expf(2.f * l1.y), __expf(2.f * l1.z), __expf(2.f * l1.w));
+        }
+      }
+      __syncthreads();
+    }
     if (tid < 128) {
       const int c = tid;
-      const uint8_t* KQ = sm + sKQ;
-      float st = 0.f;   // gain state at the chunk start
-      if (kKdn || kPkda) {
-        if (chained)
-          st = ci == 0 ? (a.aux0 ? a.aux0[(long)bh * 128 + c] : (kKdn ? 1.f : 0.f))
-                       : __ldcg(reinterpret_cast<const float*>(rec + rkP0) + c);
-        else
-          st = reinterpret_cast<const float*>(rec + rkP0)[c];
-      }
-      const float mu_h = kPkda ? a.mu[h] : 0.f;
       float g = 0.f, n = st, d = 1.f;
+#pragma unroll 1
       for (int i0 = 0; i0 < 64; i0 += 8) {
-        float la[8], kh[8], om[8];
+        float la[8], x[8], y[8], om[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          la[e] = fG_[(i0 + e) * 128 + c];
-          if (kKdn || kPkda) kh[e] = bf16_at(KQ, i0 + e, c) * vcr[i0 + e];
-          if (kKdn) om[e] = fA_[(i0 + e) * 128 + c];
+          const int o = (i0 + e) * 128 + c;
+          la[e] = fG_[o];
+          if (kKdn) {
+            x[e] = fX_[o];
+            om[e] = fA_[o];
+          }
+          if (kKdn || kPkda) y[e] = fY_[o];
         }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int i = i0 + e;
           g += la[e];
-          fG_[i * 128 + c] = g;
-          if (kKdn) {   // (n, d) <- [[a^2, w], [u a^2, 1 + u w]] (n, d); p^_i = n_i / d_{i-1}
-            const float al = __expf(la[e]);
-            const float n1 = al * al * n + om[e] * d;
-            fA_[i * 128 + c] = __fdividef(n1, d);
-            d = d + vus[i] * kh[e] * kh[e] * n1;
+          fG_[(i0 + e) * 128 + c] = g;
+        }
+        if (kKdn) {   // (n, d) <- [[a^2, w], [u a^2, 1 + u w]] (n, d); p^_i = n_i / d_{i-1}
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float n1 = fmaf(x[e], n, om[e] * d);
+            fA_[(i0 + e) * 128 + c] = __fdividef(n1, d);
+            d = fmaf(y[e], n1, d);
             n = n1;
           }
-          if (kPkda) {   // A_t = alphaP A + betaP k^2, bound B(A) (fast log / exp)
-            n = vaP[i] * n + vbP[i] * kh[e] * kh[e];
-            const float rr = __logf(fmaxf(n, a.log_floor)) - mu_h;
-            fA_[i * 128 + c] = __expf(-a.ln_x * __fdividef(rr, 1.f + fabsf(rr)));
-          }
+          // exact power-of-two rescale to d in [1, 2) (p = n / d is scale-free; d >= 1)
+          const float sc = __uint_as_float(0x7f000000u - (__float_as_uint(d) & 0x7f800000u));
+          n *= sc;
+          d *= sc;
         }
-        if (kKdn) {   // exact power-of-two rescale (p = n / d is scale-free)
-          int ex;
-          frexpf(d, &ex);
-          n = ldexpf(n, -ex);
-          d = ldexpf(d, -ex);
+        if (kPkda) {   // A_t = alphaP A + betaP k^2 (the bound follows below)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            n = fmaf(vaP[i0 + e], n, y[e]);
+            fA_[(i0 + e) * 128 + c] = n;
+          }
         }
       }
       if (chained && (kKdn || kPkda)) {   // state at the chunk end -> next record, or aux
         const float end = kKdn ? n / d : n;
-        if (ci + 1 < NC) {
+        if (ci + 1 < NC)   // published by thread 0's release after the barrier below
           __stcg(reinterpret_cast<float*>(rec + kRec + rkP0) + c, end);
-          __threadfence();
-        } else if (a.aux) {
+        else if (a.aux)
           a.aux[(long)bh * 128 + c] = end;
-        }
       }
     } else if (kIkdn && warp == 4) {
       // b -> b^ / (1 + u b^), b^ = a b + omega is the Moebius map of (n, d) by
@@ -403,9 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         M[2] = u * at;
         M[3] = 1.f + u * om;
       };
-      float b_in = 1.f;
-      if (chained)
-        b_in = ci == 0 ? (a.aux0 ? a.aux0[bh] : 1.f) : __ldcg(reinterpret_cast<const float*>(rec + rkP0));
+      const float b_in = st;
       float M0[4], M1[4], Pl[4];
       token(2 * lane, M0);
       token(2 * lane + 1, M1);
@@ -441,33 +482,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float nE = Pl[0] * b_in + Pl[1], dE = Pl[2] * b_in + Pl[3];
       const float b_end = __shfl_sync(0xffffffffu, __fdividef(nE, dE), 31);
       if (lane == 0 && chained) {
-        if (ci + 1 < NC) {
+        if (ci + 1 < NC)
           __stcg(reinterpret_cast<float*>(rec + kRec + rkP0), b_end);
-          __threadfence();
-        } else if (a.aux) {
+        else if (a.aux)
           a.aux[bh] = b_end;
-        }
       }
     }
     __syncthreads();
-    if (chained && (kKdn || kPkda || kIkdn) && tid == 0 && ci + 1 < NC && ri + 1 != g_chain_withhold)
+    // every thread's hand-over store precedes the barrier; thread 0's fence and
+    // release store publish them at GPU scope (cumulative over the barrier)
+    if (chained && (kKdn || kPkda || kIkdn) && tid == 0 && ci + 1 < NC && ri + 1 != g_chain_withhold) {
+      __threadfence();
       st_release_gpu(chain + ri + 1, 1u);
+    }
+    if (kPkda) {   // the bound B(A) = exp(-ln(x) r / (1 + |r|)), r = log max(A, floor) - mu
+                   // (PDN notes Eq. (9); fast log / exp), in place
+      const float mu_h = a.mu[h];
+      float4* f4 = reinterpret_cast<float4*>(fA_);
+#pragma unroll 2
+      for (int e4 = tid; e4 < 64 * 128 / 4; e4 += kThreads) {
+        float4 v = f4[e4];
+        float* x = reinterpret_cast<float*>(&v);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float rr = __logf(fmaxf(x[e], a.log_floor)) - mu_h;
+          x[e] = __expf(-a.ln_x * __fdividef(rr, 1.f + fabsf(rr)));
+        }
+        f4[e4] = v;
+      }
+    }
 
     // ---- 3. per-token write scale; per-channel factors of the sub-chunk references
-    if (kKdn) {   // 1 / (r_i + sum_c p^_ic k^_ic^2): warp w takes rows 8w .. 8w + 7
+    if (kKdn) {   // 1 / (r_i + sum_c p^_ic k^_ic^2): four threads per token, 32 channels each
+      const int i = tid >> 2, part = tid & 3, kb = part >> 1, c0 = (part & 1) * 32;
       const uint8_t* KQ = sm + sKQ;
+      float z = 0.f;
 #pragma unroll
-      for (int rr = 0; rr < 8; ++rr) {
-        const int i = 8 * warp + rr;
-        float z = 0.f;
+      for (int m = 0; m < 4; ++m) {
+        float k8[8];
+        unpack8(*reinterpret_cast<const uint4*>(KQ + kb * 16384 + sw128_offset(i, c0 + 8 * m)), k8);
+        const float4* pp = reinterpret_cast<const float4*>(fA_ + i * 128 + 64 * kb + c0 + 8 * m);
+        const float4 p0 = pp[0], p1 = pp[1];
+        const float p8[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
-        for (int c = lane; c < 128; c += 32) {
-          const float kh = bf16_at(KQ, i, c) * vcr[i];
-          z += fA_[i * 128 + c] * kh * kh;
-        }
-        z = warp_sum(z);
-        if (lane == 0) vsc[i] = 1.f / (vr[i] + z);
+        for (int e = 0; e < 8; ++e) z += p8[e] * k8[e] * k8[e];
       }
+      z += __shfl_xor_sync(0xffffffffu, z, 1);
+      z += __shfl_xor_sync(0xffffffffu, z, 2);
+      if (part == 0) vsc[i] = 1.f / (vr[i] + z * vcr[i] * vcr[i]);
     } else if (!kIkdn) {
       if (tid < 64) vsc[tid] = veta[tid];
     }
@@ -490,9 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
 
     // ---- 4. B image: for token j of sub-chunk J, w~_j = w_j exp(g_m(J) - g_j), then
-    //         block I >= J gets w~_j exp(g_m(I) - g_m(J)); Wbar_j = w~_j exp(g_C - g_m(J))
-    //         goes to the record.  Unit = (token, 8 channels).
-#pragma unroll 1
+    //         block I >= J gets w~_j exp(g_m(I) - g_m(J)).  Unit = (token, 8 channels).
+#pragma unroll 2
     for (int r = 0; r < 4; ++r) {
       const int u = tid + r * kThreads, j = u >> 4, cg = u & 15, kb = cg >> 3, c8 = (cg & 7) * 8;
       const int cc = 64 * kb + c8, J = j >> 4;
@@ -531,27 +592,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(sm + off) = hi;
         *reinterpret_cast<uint4*>(sm + off + kBLo) = lo;
       }
-      {
-        const float* Gm = fGm + J * 128 + cc;
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = w[e] * Gm[e];
-        split8(x, hi, lo);
-        const uint32_t off = kb * 8192 + sw128_offset(j, c8);
-        st_global16(rec + rbW + off, hi);
-        st_global16(rec + rbW + 16384 + off, lo);
-      }
     }
     __syncthreads();
 
-    // ---- 5. A image [K~ ; Q~] = [k^_i ; q^_i] exp(g_i - g_m(I)); (Gamma.Q) to the record;
-    //         (Gamma.K) over the K / Q tiles (each thread rewrites only what it read)
-#pragma unroll 1
+    // ---- 5. A image [K~ ; Q~] = [k^_i ; q^_i] exp(g_i - g_m(I))
+#pragma unroll 2
     for (int r = 0; r < 4; ++r) {
       const int u = tid + r * kThreads, i = u >> 4, cg = u & 15, kb = cg >> 3, c8 = (cg & 7) * 8;
       const int cc = 64 * kb + c8, I = i >> 4;
-      uint8_t* kp = sm + sKQ + kb * 16384 + sw128_offset(i, c8);
-      uint8_t* qp = sm + sKQ + kb * 16384 + sw128_offset(64 + i, c8);
+      const uint8_t* kp = sm + sKQ + kb * 16384 + sw128_offset(i, c8);
+      const uint8_t* qp = sm + sKQ + kb * 16384 + sw128_offset(64 + i, c8);
       float k8[8], q8[8];
       unpack8(*reinterpret_cast<const uint4*>(kp), k8);
       unpack8(*reinterpret_cast<const uint4*>(qp), q8);
@@ -560,16 +610,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4 g0 = gp[0], g1 = gp[1], m0 = mp[0], m1 = mp[1];
       const float gi[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
       const float gm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-      const float* Em = fEm + I * 128 + cc;
       const float cr = vcr[i], qn = vqn[i];
-      float xk[8], xq[8], yk[8], yq[8];
+      float xk[8], xq[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float f = __expf(gi[e] - gm[e]);
         xk[e] = k8[e] * cr * f;
         xq[e] = q8[e] * qn * f;
-        yk[e] = xk[e] * Em[e];
-        yq[e] = xq[e] * Em[e];
       }
       uint4 hi, lo;
       split8(xk, hi, lo);
@@ -580,13 +627,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t oq = sA + kb * 16384 + sw128_offset(64 + i, c8);
       *reinterpret_cast<uint4*>(sm + oq) = hi;
       *reinterpret_cast<uint4*>(sm + oq + 32768) = lo;
-      split8(yq, hi, lo);
-      const uint32_t og = kb * 8192 + sw128_offset(i, c8);
-      st_global16(rec + rbQ + og, hi);
-      st_global16(rec + rbQ + 16384 + og, lo);
-      split8(yk, hi, lo);
-      *reinterpret_cast<uint4*>(kp) = hi;
-      *reinterpret_cast<uint4*>(qp) = lo;
     }
     if (tid < 128) {
       float* rv = reinterpret_cast<float*>(rec + rbVec);
@@ -596,8 +636,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async();
     __syncthreads();
 
-    // ---- 6. the Gram [K~ ; Q~] B^T (three hi/lo products); the log-decay tile of the
-    //         next task may load now
+    // ---- 6. the Gram [K~ ; Q~] B^T (three hi/lo products); the next task's K / Q and
+    //         log-decay tiles may load now
     if (tid == 0) {
       tc_fence_after();
       const uint32_t ab = smem_u32(sm + sA), bb = smem_u32(sm + sB);
@@ -614,14 +654,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_commit(&bars[B_GRAM]);
       ++c_gram;
-      if (nxt < ntask) load_la(nxt);
+      if (has_next) {
+        load_kq(nbh, nci);
+        load_la(nbh, nci);
+      }
+    }
+    // While the Gram runs (its operands are only read): (Gamma.Q) = Q~ exp(g_m(I)) and
+    // Wbar = B_3 exp(g_C - g_m(3)) (block 3 of the B image holds every token's
+    // w_j exp(g_m(3) - g_j)) to the record from the images' hi + lo, and (Gamma.K) =
+    // K~ exp(g_m(I)) into registers, stored once the B image is free.
+    uint4 gk_hi[4], gk_lo[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int u = tid + r * kThreads, i = u >> 4, cg = u & 15, kb = cg >> 3, c8 = (cg & 7) * 8;
+      const int cc = 64 * kb + c8;
+      const float* Em = fEm + (i >> 4) * 128 + cc;
+      const float* G3 = fGm + 3 * 128 + cc;
+      const uint32_t ok = sA + kb * 16384 + sw128_offset(i, c8);
+      const uint32_t oq = sA + kb * 16384 + sw128_offset(64 + i, c8);
+      const uint32_t ob = sB + kb * kBBlk + sw128_offset(brow(3, i), c8);
+      float xh[8], xl[8], y[8];
+      uint4 hi, lo;
+      unpack8(*reinterpret_cast<const uint4*>(sm + oq), xh);
+      unpack8(*reinterpret_cast<const uint4*>(sm + oq + 32768), xl);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = (xh[e] + xl[e]) * Em[e];
+      split8(y, hi, lo);
+      const uint32_t og = kb * 8192 + sw128_offset(i, c8);
+      st_global16(rec + rbQ + og, hi);
+      st_global16(rec + rbQ + 16384 + og, lo);
+      unpack8(*reinterpret_cast<const uint4*>(sm + ob), xh);
+      unpack8(*reinterpret_cast<const uint4*>(sm + ob + kBLo), xl);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = (xh[e] + xl[e]) * G3[e];
+      split8(y, hi, lo);
+      st_global16(rec + rbW + og, hi);
+      st_global16(rec + rbW + 16384 + og, lo);
+      unpack8(*reinterpret_cast<const uint4*>(sm + ok), xh);
+      unpack8(*reinterpret_cast<const uint4*>(sm + ok + 32768), xl);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = (xh[e] + xl[e]) * Em[e];
+      split8(y, gk_hi[r], gk_lo[r]);
     }
     if (!cta_wait(B_GRAM, k & 1)) {
       abort = true;
       break;
     }
     tc_fence_after();
-    if (kKdn && tid == 0 && nxt < ntask) load_om(nxt);   // the A image has been read
 
     // ---- 7. Gram readout: row r < 64 -> L (fp32, j < i), r >= 64 -> P (j <= i) as a
     //         bf16 hi/lo image in the record.  Row i of sub-chunk I finds its columns
@@ -682,8 +761,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    // (Gamma.K) as the W' MMA's A operand [64 tok][128] (MN-major, two 64-channel
+    // blocks 8 KB apart)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int u = tid + r * kThreads, i = u >> 4, cg = u & 15, kb = cg >> 3, c8 = (cg & 7) * 8;
+      const uint32_t og = sGK + kb * 8192 + sw128_offset(i, c8);
+      *reinterpret_cast<uint4*>(sm + og) = gk_hi[r];
+      *reinterpret_cast<uint4*>(sm + og + 16384) = gk_lo[r];
+    }
     tc_fence_before();
     __syncthreads();
+    if (kKdn && tid == 0 && has_next) load_om(nbh, nci);   // the A image has been read
 
     // ---- 8. T = (I + L)^-1 in place: diagonal 16x16 blocks (threads 0-63, a column each)
     float* LT = reinterpret_cast<float*>(sm + sLT);
@@ -771,14 +860,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     //          [Gamma.K_lo] x T_hi (N = 64) into the first half
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t tb = smem_u32(sm + sTi), kq = smem_u32(sm + sKQ);
+      const uint32_t tb = smem_u32(sm + sTi), gk = smem_u32(sm + sGK);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + tW, desc_sw128(kq + ks * 2048, 16384, 1024), desc_sw128(tb + ks * 32, 16, 1024),
+        mma_bf16(tmem + tW, desc_sw128(gk + ks * 2048, 8192, 1024), desc_sw128(tb + ks * 32, 16, 1024),
                  I_WT, ks > 0);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + tW, desc_sw128(kq + 8192 + ks * 2048, 16384, 1024),
+        mma_bf16(tmem + tW, desc_sw128(gk + 16384 + ks * 2048, 8192, 1024),
                  desc_sw128(tb + ks * 32, 16, 1024), I_WT64, true);
       mma_commit(&bars[B_WP]);
       ++c_wp;
@@ -814,7 +903,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && nxt < ntask) load_kq(nxt);   // (Gamma.K) has been read
     it = nxt;
   }
 
