@@ -240,14 +240,16 @@ typedef struct dr_grads {
   float *dq;               /* [B,T,H,dk]                                              */
   float *dk;               /* [B,T,H,dk]                                              */
   float *dv;               /* [B,T,H,dv]                                              */
-  float *d_log_alpha;      /* [B,T,H]                                                 */
-  float *d_eta;            /* [B,T,H] (GDN / KLA eta, PGDN beta)                      */
+  float *d_log_alpha;      /* [B,T,H]; per-channel decay (KDA, KDN): [B,T,H,dk]      */
+  float *d_eta;            /* [B,T,H] (GDN / KLA eta, PGDN beta, KDA eta); KDN: NULL  */
   float *d_init_state;     /* [B,H,dk,dv] or NULL (not written)                       */
   float *d_alphaP;         /* PGDN: [B,T,H]                                           */
   float *d_betaP;          /* PGDN: [B,T,H]                                           */
   float *d_mu;             /* PGDN: [H]                                               */
-  float *d_aux_init;       /* PGDN: dL/dA_0 [B,H,dk] or NULL                          */
-  const float *d_aux_final;/* PGDN: input dL/dA_T [B,H,dk] or NULL (zero)             */
+  float *d_aux_init;       /* PGDN: dL/dA_0, Diagonal KDN: dL/dp_0 [B,H,dk] or NULL   */
+  const float *d_aux_final;/* PGDN: input dL/dA_T, KDN dL/dp_T [B,H,dk] or NULL (zero) */
+  float *d_omega;          /* Diagonal KDN: [B,T,H,dk]                                */
+  float *d_r;              /* Diagonal KDN: [B,T,H]                                   */
 } dr_grads;
 
 /*

@@ -38,12 +38,14 @@
 //   bwd_state   one CTA per (b, h, chunk): dO S_c^T, dR S_c^T, E dS^T, dO E^T, dR E^T.
 //   bwd_local   one CTA per (b, h, chunk): gates, Grams, the decay-ratio terms, the
 //               products with W, Q^, K^, the gain and norm backward, d log alpha.
+#include "chain.cuh"
 #include "dr_common.cuh"
 #include "tc_common.cuh"
 
 namespace dr {
 
 cudaError_t launch_chunk_tc_split(const FwdArgs& a, void* workspace, cudaStream_t st);
+cudaError_t launch_kdn_split(const FwdArgs& a, int dtype, void* workspace, cudaStream_t st);
 
 namespace {
 
@@ -58,6 +60,19 @@ constexpr uint32_t rWF = 66560, rAuxF = 99328;    // PGDN record: write keys, st
 // the forward record's vectors (floats after rVecF): e^g qn, e^{G-g} c, gamma, e^g cr
 constexpr size_t rVecF = 65536;
 constexpr uint32_t rTF = 0, rPF = 49152;
+// the per-channel-decay record (tensor-core prep): W'^T [128 c][64 j] hi | lo, and
+// (Gamma.Q), Wbar as [64 tok][128] (two 64-column blocks) hi | lo; gamma_C per
+// channel at float 128 of the vectors; the gain state at the chunk start
+constexpr size_t kRecPC = 135168;
+constexpr uint32_t rWpPC = 16384, rQPC = 66560, rWbPC = 99328, rP0PC = 134144;
+
+// workspace layouts: scalar decay (GDN, KLA), PGDN (+ dL/dw, key norms, d mu
+// parts), per-channel decay (KDA: + the forward's write vectors, dG per channel),
+// Diagonal KDN (+ dL/dw)
+enum { BW_SCALAR = 0, BW_PGDN = 1, BW_PC = 2, BW_KDN = 3 };
+inline int bwd_mode(int variant) {
+  return variant == DR_PGDN ? BW_PGDN : variant == DR_KDA ? BW_PC : variant == DR_KDN ? BW_KDN : BW_SCALAR;
+}
 
 struct BwdWs {
   uint8_t* rec;   // [n] x kRecF
@@ -67,10 +82,11 @@ struct BwdWs {
   float* XW;      // [n][64][128]   E dS^T
   float* dP;      // [n][64][64]    dO E^T
   float* dL;      // [n][64][64]    dR E^T
-  float* SS;      // [n]            gamma <dS, S_c>
-  float* DW;      // PGDN [n][64][128]  dL/dw
+  float* SS;      // [n]            gamma <dS, S_c>  (per-channel decay: [n][128])
+  float* DW;      // PGDN, KDN [n][64][128]  dL/dw
   float* CR;      // PGDN [n][64]       key-norm factors
   float* MU;      // PGDN [B H]         each row's part of dL/dmu
+  float* Wf;      // per-channel decay [n][64][128]  the forward's write vectors
   size_t recb;    // bytes of one forward record
 };
 
@@ -78,7 +94,8 @@ struct BwdWs {
 inline size_t al256(size_t bytes) { return (bytes + 255) / 256 * 256; }
 
 // Lays the arrays out from `base` (null: only the size), returns the bytes used.
-size_t bwd_layout(void* base, long n, int rows, bool pgdn, BwdWs* w) {
+size_t bwd_layout(void* base, long n, int rows, int mode, BwdWs* w) {
+  const bool pgdn = mode == BW_PGDN, pc = mode >= BW_PC;
   uint8_t* p = static_cast<uint8_t*>(base);
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -87,27 +104,29 @@ size_t bwd_layout(void* base, long n, int rows, bool pgdn, BwdWs* w) {
     return q;
   };
   BwdWs v{};
-  v.recb = pgdn ? kRecFP : kRecF;
-  v.rec = take((size_t)n * v.recb);
+  v.recb = pgdn ? kRecFP : (pc ? kRecPC : kRecF);
+  // (per-channel decay: the forward's hand-over flags follow its records)
+  v.rec = take((size_t)n * v.recb + (pc ? chain_bytes(n) : 0));
   v.S = reinterpret_cast<float*>(take((size_t)n * 16384 * 4));
   v.E = reinterpret_cast<float*>(take((size_t)n * 8192 * 4));
   v.dS = reinterpret_cast<float*>(take((size_t)n * 16384 * 4));
   v.XW = reinterpret_cast<float*>(take((size_t)n * 8192 * 4));
   v.dP = reinterpret_cast<float*>(take((size_t)n * 4096 * 4));
   v.dL = reinterpret_cast<float*>(take((size_t)n * 4096 * 4));
-  v.SS = reinterpret_cast<float*>(take((size_t)n * 4));
+  v.SS = reinterpret_cast<float*>(take((size_t)n * (pc ? 128 : 1) * 4));
+  if (pgdn || mode == BW_KDN) v.DW = reinterpret_cast<float*>(take((size_t)n * 8192 * 4));
   if (pgdn) {
-    v.DW = reinterpret_cast<float*>(take((size_t)n * 8192 * 4));
     v.CR = reinterpret_cast<float*>(take((size_t)n * 64 * 4));
     v.MU = reinterpret_cast<float*>(take((size_t)rows * 4));
   }
+  if (pc) v.Wf = reinterpret_cast<float*>(take((size_t)n * 8192 * 4));
   if (w) *w = v;
   return off;
 }
 
-BwdWs bwd_ws(void* base, long n, int rows, bool pgdn) {
+BwdWs bwd_ws(void* base, long n, int rows, int mode) {
   BwdWs w;
-  bwd_layout(base, n, rows, pgdn, &w);
+  bwd_layout(base, n, rows, mode, &w);
   return w;
 }
 
@@ -211,12 +230,17 @@ struct BwdArgs {
   float* daP;                // PGDN [B,T,H]
   float* dbP;                // PGDN [B,T,H]
   float* dmu;                // PGDN [H]
-  float* daux0;              // PGDN [B,H,dk] or null
-  const float* daux_T;       // PGDN [B,H,dk] or null
+  float* daux0;              // PGDN / KDN [B,H,dk] or null
+  const float* daux_T;       // PGDN / KDN [B,H,dk] or null
+  float* domega;             // KDN [B,T,H,dk]
+  float* dr;                 // KDN [B,T,H]
   BwdWs w;
 };
 
-template <bool PG>
+// PC (per-channel decay): (Gamma.Q), Wbar and W'^T come from the record's images,
+// gamma per state row, and dS_c = gamma . dS + (Gamma.Q)^T dO - W'^T dE, as
+// (Gamma.K)^T dR = (Gamma.K)^T T^T dE = (T Gamma.K)^T dE.
+template <bool PG, bool PC>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_carry_kernel(FwdArgs a, BwdArgs g) {
   extern __shared__ __align__(16) float smf[];
@@ -230,6 +254,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   float* sdR = sdE + 64 * cLDN;
   float* sdS = sdR + 64 * cLDN;          // dS [c][n]
   __shared__ float s_gamma;
+  __shared__ float s_gam[PC ? 128 : 1];   // per-channel decay: gamma of each state row
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x >> 2, cb = blockIdx.x & 3;
@@ -261,7 +286,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       rPT[r][3] = *reinterpret_cast<const uint4*>(rec + rTF + 8192 + off);
     }
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < 4 && !PC; ++r) {
       const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
       const bool live = j < Cc;
       rK[r] = live ? *reinterpret_cast<const uint4*>(K + tok(a, b, t0 + j, h) * 128 + c0)
@@ -309,8 +334,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int q = 0; q < 8; ++q) sT[i * cLD64T + c0 + q] = hh[q] + ll[q];
     }
+    if (PC) {   // the record's images (hi + lo); W'^T [c][j] -> W' [j][c]
+      const uint8_t* rec = g.w.rec + ri * g.w.recb;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < 4; ++r) {
+        const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
+        const uint32_t off = (c0 >> 6) * 8192 + umma::sw128_offset(j, c0 & 63);
+        float qh[8], ql[8], wh[8], wl[8];
+        unpack8(*reinterpret_cast<const uint4*>(rec + rQPC + off), qh);
+        unpack8(*reinterpret_cast<const uint4*>(rec + rQPC + 16384 + off), ql);
+        unpack8(*reinterpret_cast<const uint4*>(rec + rWbPC + off), wh);
+        unpack8(*reinterpret_cast<const uint4*>(rec + rWbPC + 16384 + off), wl);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          sQg[j * cLDQ + c0 + q] = qh[q] + ql[q];
+          sWb[j * cLDW + c0 + q] = wh[q] + wl[q];
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int e = tid + r * kBwdThreads, cr = e >> 3, j0 = 8 * (e & 7);
+        const uint32_t off = umma::sw128_offset(cr, j0);
+        float hh[8], ll[8];
+        unpack8(*reinterpret_cast<const uint4*>(rec + rWpPC + off), hh);
+        unpack8(*reinterpret_cast<const uint4*>(rec + rWpPC + 16384 + off), ll);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) sKg[(j0 + q) * cLDQ + cr] = hh[q] + ll[q];
+      }
+      if (tid < 128) s_gam[tid] = reinterpret_cast<const float*>(rec + rVecF)[128 + tid];
+    }
+#pragma unroll
+    for (int r = 0; r < 4 && !PC; ++r) {
       const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
       float kf[8], qf[8], wf[8];
       unpack8(rK[r], kf);
@@ -376,10 +430,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          d[nt][e] = gam * sdS[(16 * warp + frag_row(lane, e)) * cLDN + 8 * nt + frag_col(lane, e)];
+        for (int e = 0; e < 4; ++e) {
+          const int row = 16 * warp + frag_row(lane, e);
+          d[nt][e] = (PC ? s_gam[row] : gam) * sdS[row * cLDN + 8 * nt + frag_col(lane, e)];
+        }
       mm3x<4, 8, true, false>(d, sQg + 16 * warp, cLDQ, sdO, cLDN, lane);
-      mm3x<4, 8, true, false>(m, sKg + 16 * warp, cLDQ, sdR, cLDN, lane);
+      mm3x<4, 8, true, false>(m, sKg + 16 * warp, cLDQ, PC ? sdE : sdR, cLDN, lane);
       __syncwarp();
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
@@ -498,21 +554,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   cpa_wait_all();
   __syncthreads();
-  float part = 0.f;
-  for (int e = tid; e < 128 * 32; e += kBwdThreads) {
-    const int r = e >> 5, c4 = 4 * (e & 31);
-    const float4 x = *reinterpret_cast<const float4*>(sD + r * cLDS + c4);
-    const float4 y = *reinterpret_cast<const float4*>(sS + r * cLDS + c4);
-    part += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
-  }
-  part = warp_sum(part);
-  if (lane == 0) s_red[warp] = part;
-  __syncthreads();
-  if (tid == 0) {
-    float tsum = 0.f;
-    for (int w = 0; w < kBwdThreads / 32; ++w) tsum += s_red[w];
-    const float gam = reinterpret_cast<const float*>(g.w.rec + (size_t)task * g.w.recb + rVecF)[128];
-    g.w.SS[task] = gam * tsum;
+  if (a.variant == DR_KDA || a.variant == DR_KDN) {   // per-channel decay: gamma_c <dS_c, S_c>
+    const float* gam = reinterpret_cast<const float*>(g.w.rec + (size_t)task * g.w.recb + rVecF) + 128;
+    for (int rr = 0; rr < 16; ++rr) {
+      const int r = 16 * warp + rr;
+      const float4 x = *reinterpret_cast<const float4*>(sD + r * cLDS + 4 * lane);
+      const float4 y = *reinterpret_cast<const float4*>(sS + r * cLDS + 4 * lane);
+      const float p = warp_sum(x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w);
+      if (lane == 0) g.w.SS[(size_t)task * 128 + r] = gam[r] * p;
+    }
+  } else {
+    float part = 0.f;
+    for (int e = tid; e < 128 * 32; e += kBwdThreads) {
+      const int r = e >> 5, c4 = 4 * (e & 31);
+      const float4 x = *reinterpret_cast<const float4*>(sD + r * cLDS + c4);
+      const float4 y = *reinterpret_cast<const float4*>(sS + r * cLDS + c4);
+      part += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+    }
+    part = warp_sum(part);
+    if (lane == 0) s_red[warp] = part;
+    __syncthreads();
+    if (tid == 0) {
+      float tsum = 0.f;
+      for (int w = 0; w < kBwdThreads / 32; ++w) tsum += s_red[w];
+      const float gam = reinterpret_cast<const float*>(g.w.rec + (size_t)task * g.w.recb + rVecF)[128];
+      g.w.SS[task] = gam * tsum;
+    }
   }
   // X_W = E dS^T
   {
@@ -871,6 +938,235 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// ================================================================= bwd_local_pc
+// Per-channel decay (KDA; the chunk part of Diagonal KDN): one CTA per (b, h,
+// chunk).  With D_ijc = exp(g_ic - g_jc) per channel the Gram gradients do not
+// factor into whole-chunk products; each 16-token block row I takes its middle
+// token m(I) as reference, as the forward's Gram does (every factor bounded by the
+// decay over 8 tokens or <= 1):
+//   dq^_i += e^{g_i - g_m(I)} . sum_j (M_P)_ij [w_j e^{g_m(I) - g_j}]     (i in I, j <= i)
+//   dk^_i += e^{g_i - g_m(I)} . sum_j (M_L)_ij [w_j e^{g_m(I) - g_j}]
+//   dw_j  += sum_{I >= J} e^{g_m(I) - g_j} . sum_{i in I} ((M_P)_ij q~_i + (M_L)_ij k~_i),
+//            q~_i = q^_i e^{g_i - g_m(I)},  k~ likewise,
+// with M_P = dP (j <= i) and M_L = -dR E^T (j < i), on TF32x3 tiles.  Every Gram
+// entry adds x_ic dx_ic to dg_ic and takes w_jc dw_jc from dg_jc, so per channel
+//   dg = q^ . dq^_P + k^ . dk^_L - w . dw_{P,L} + e^g (X_Q . q^ - X_K . k^) - Wbar . X_W,
+// dG_c = gamma_c <dS_c, S_c> + sum_j Wbar_jc X_W,jc on the chunk's last token, and
+// d log alpha = the reverse cumulative sum of dg per channel.  dq^ and dk^ gather
+// in the gradient arrays (bwd_state left X_Q = dO S_c^T, X_K = dR S_c^T there).
+// KDA's gain (w = eta k^): d eta = dw . k^, dk^ += eta dw, then the L2 norms;
+// Diagonal KDN keeps dw and dk^ for kdn_gain_bwd.
+constexpr int kPcLocalSmem = (4 * 64 * cLDK + 2 * 64 * cLDM + 2 * 16 * cLDK) * 4 + 2 * 64 * 128 * 2;
+
+template <int VARIANT>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_local_pc_kernel(FwdArgs a, BwdArgs g) {
+  constexpr bool kKdn = VARIANT == DR_KDN;
+  extern __shared__ __align__(16) float smf[];
+  float* sW = smf;                   // w [j][c]
+  float* sG = sW + 64 * cLDK;        // cumulative log-decay g [j][c]
+  float* sMP = sG + 64 * cLDK;       // M_P [i][j]
+  float* sML = sMP + 64 * cLDM;      // M_L [i][j]
+  float* sWt = sML + 64 * cLDM;      // w~ of block row I [j][c]
+  float* sAq = sWt + 64 * cLDK;      // q~ of block row I [16][c]
+  float* sAk = sAq + 16 * cLDK;      // k~
+  float* sDW = sAk + 16 * cLDK;      // dw, Gram part [j][c]
+  uint16_t* sKr = reinterpret_cast<uint16_t*>(sDW + 64 * cLDK);   // raw k, q (bf16) [j][128]
+  uint16_t* sQr = sKr + 64 * 128;
+  __shared__ float s_cr[64], s_qn[64], s_eta[64];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NC = (a.T + 63) / 64;
+  const long task = blockIdx.x;
+  const int bh = (int)(task / NC), c = (int)(task % NC);
+  const int b = bh / a.H, h = bh % a.H;
+  const int t0 = 64 * c, Cc = min(64, a.T - t0);
+  auto bf = [](uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); };
+
+  // ---- raw rows, w, log-decay, dP and dR E^T
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
+    const bool live = j < Cc;
+    const long o = tok(a, b, t0 + (live ? j : 0), h) * 128 + c0;
+    *reinterpret_cast<uint4*>(sKr + j * 128 + c0) =
+        live ? *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.k) + o) : make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(sQr + j * 128 + c0) =
+        live ? *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + o) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  for (int e = tid; e < 64 * 32; e += kBwdThreads) {
+    const int j = e >> 5, c4 = 4 * (e & 31);
+    const bool live = j < Cc;
+    cpa16(sW + j * cLDK + c4, g.w.Wf + (size_t)task * 8192 + j * 128 + c4);
+    cpa16(sG + j * cLDK + c4, a.log_alpha + tok(a, b, t0 + (live ? j : 0), h) * 128 + c4, live ? 16 : 0);
+  }
+  for (int e = tid; e < 64 * 16; e += kBwdThreads) {
+    const int i = e >> 4, c4 = 4 * (e & 15);
+    cpa16(sMP + i * cLDM + c4, g.w.dP + (size_t)task * 4096 + i * 64 + c4);
+    cpa16(sML + i * cLDM + c4, g.w.dL + (size_t)task * 4096 + i * 64 + c4);
+  }
+  if (tid < 64) s_eta[tid] = (!kKdn && tid < Cc) ? a.eta[tok(a, b, t0 + tid, h)] : 0.f;
+  for (int e = tid; e < 64 * 128; e += kBwdThreads) sDW[(e >> 7) * cLDK + (e & 127)] = 0.f;
+  cpa_wait_all();
+  __syncthreads();
+  {   // norms: four threads per row
+    const int j = tid >> 2, part = tid & 3;
+    float kk = 0.f, qq = 0.f;
+    for (int c0 = 32 * part; c0 < 32 * part + 32; ++c0) {
+      const float x = bf(sKr[j * 128 + c0]), y = bf(sQr[j * 128 + c0]);
+      kk += x * x;
+      qq += y * y;
+    }
+    kk += __shfl_xor_sync(0xffffffffu, kk, 1);
+    kk += __shfl_xor_sync(0xffffffffu, kk, 2);
+    qq += __shfl_xor_sync(0xffffffffu, qq, 1);
+    qq += __shfl_xor_sync(0xffffffffu, qq, 2);
+    if (part == 0) {
+      s_cr[j] = a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f;
+      s_qn[j] = a.q_l2norm ? 1.f / fmaxf(sqrtf(qq), 1e-30f) : 1.f;
+    }
+  }
+  if (tid < 128) {   // cumulative log-decay, channel tid
+    float gg = 0.f;
+    for (int j = 0; j < 64; ++j) {
+      gg += sG[j * cLDK + tid];
+      sG[j * cLDK + tid] = gg;
+    }
+  }
+  for (int e = tid; e < 64 * 64; e += kBwdThreads) {
+    const int i = e >> 6, j = e & 63;
+    sMP[i * cLDM + j] = (j <= i) ? sMP[i * cLDM + j] : 0.f;
+    sML[i * cLDM + j] = (j < i) ? -sML[i * cLDM + j] : 0.f;
+  }
+  __syncthreads();
+
+  // ---- block rows I = 0..3
+  for (int I = 0; I < 4; ++I) {
+    const int nJ = 16 * (I + 1), m = 16 * I + 7;
+    for (int e = tid; e < nJ * 32; e += kBwdThreads) {   // w~ = w e^{g_m(I) - g}, rows j < 16 (I + 1)
+      const int j = e >> 5, c4 = 4 * (e & 31);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        sWt[j * cLDK + c4 + q] =
+            sW[j * cLDK + c4 + q] * __expf(sG[m * cLDK + c4 + q] - sG[j * cLDK + c4 + q]);
+    }
+    for (int e = tid; e < 16 * 32; e += kBwdThreads) {   // q~, k~ of the block's rows
+      const int r = e >> 5, c4 = 4 * (e & 31), i = 16 * I + r;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float f = __expf(sG[i * cLDK + c4 + q] - sG[m * cLDK + c4 + q]);
+        sAq[r * cLDK + c4 + q] = bf(sQr[i * 128 + c4 + q]) * s_qn[i] * f;
+        sAk[r * cLDK + c4 + q] = bf(sKr[i * 128 + c4 + q]) * s_cr[i] * f;
+      }
+    }
+    __syncthreads();
+    {   // dq^_P, dk^_L of the block's 16 rows (warp: columns 16 warp .. + 16)
+      float dq2[2][4] = {}, dk2[2][4] = {};
+      for (int kk = 0; kk <= I; ++kk) {
+        mm3x<2, 2, false, false>(dq2, sMP + 16 * I * cLDM + 16 * kk, cLDM, sWt + 16 * kk * cLDK + 16 * warp,
+                                 cLDK, lane);
+        mm3x<2, 2, false, false>(dk2, sML + 16 * I * cLDM + 16 * kk, cLDM, sWt + 16 * kk * cLDK + 16 * warp,
+                                 cLDK, lane);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 16 * I + frag_row(lane, e), cc = 16 * warp + 8 * nt + frag_col(lane, e);
+          if (i < Cc) {
+            const float gi = sG[i * cLDK + cc];
+            const float sc = __expf(gi - sG[m * cLDK + cc]), eg = __expf(gi);
+            const float dqp = dq2[nt][e] * sc, dkl = dk2[nt][e] * sc;
+            const long o = tok(a, b, t0 + i, h) * 128 + cc;
+            const float xq = g.dq[o], xk = g.dk[o];
+            const float qh = bf(sQr[i * 128 + cc]) * s_qn[i], kh = bf(sKr[i * 128 + cc]) * s_cr[i];
+            g.dq[o] = dqp + eg * xq;
+            g.dk[o] = dkl - eg * xk;
+            g.dla[o] = qh * dqp + kh * dkl + eg * (xq * qh - xk * kh);
+          }
+        }
+    }
+    // dw of rows j < 16 (I + 1): M_P^T q~ + M_L^T k~ over the block's rows, times e^{g_m(I) - g_j}
+    for (int pp = warp; pp < 8 * (I + 1); pp += 8) {
+      const int mt = pp >> 3, nt0 = 2 * (pp & 7);
+      float d2[2][4] = {};
+      mm3x<2, 2, true, false>(d2, sMP + 16 * I * cLDM + 16 * mt, cLDM, sAq + 8 * nt0, cLDK, lane);
+      mm3x<2, 2, true, false>(d2, sML + 16 * I * cLDM + 16 * mt, cLDM, sAk + 8 * nt0, cLDK, lane);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = 16 * mt + frag_row(lane, e), cc = 8 * (nt0 + nt) + frag_col(lane, e);
+          sDW[j * cLDK + cc] += d2[nt][e] * __expf(sG[m * cLDK + cc] - sG[j * cLDK + cc]);
+        }
+    }
+    __syncthreads();
+  }
+
+  // ---- rows (four threads per token): dw += e^{G - g} X_W, the column terms of dg,
+  //      the write gain and the norms
+  {
+    const int j = tid >> 2, part = tid & 3;
+    const bool live = j < Cc;
+    const long o = tok(a, b, t0 + (live ? j : 0), h) * 128;
+    const float* xw = g.w.XW + (size_t)task * 8192 + j * 128;
+    const float cr = s_cr[j], qn = s_qn[j], eta = s_eta[j];
+    float dkh[32], dqh[32], deta = 0.f, dotk = 0.f, dotq = 0.f;
+#pragma unroll 4
+    for (int q = 0; q < 32; ++q) {
+      const int cc = 32 * part + q;
+      const float gj = sG[j * cLDK + cc], ew = __expf(sG[63 * cLDK + cc] - gj);
+      const float w = sW[j * cLDK + cc], x = xw[cc];
+      const float dwg = sDW[j * cLDK + cc], dw = dwg + ew * x;
+      const float kh = bf(sKr[j * 128 + cc]) * cr, qh = bf(sQr[j * 128 + cc]) * qn;
+      dkh[q] = live ? g.dk[o + cc] : 0.f;
+      dqh[q] = live ? g.dq[o + cc] : 0.f;
+      if (kKdn) {
+        g.w.DW[(size_t)task * 8192 + j * 128 + cc] = dw;
+      } else {
+        dkh[q] += eta * dw;
+        deta += kh * dw;
+      }
+      if (live) g.dla[o + cc] += -w * dwg - w * ew * x;
+      dotk += dkh[q] * kh;
+      dotq += dqh[q] * qh;
+    }
+    deta += __shfl_xor_sync(0xffffffffu, deta, 1);
+    deta += __shfl_xor_sync(0xffffffffu, deta, 2);
+    dotk += __shfl_xor_sync(0xffffffffu, dotk, 1);
+    dotk += __shfl_xor_sync(0xffffffffu, dotk, 2);
+    dotq += __shfl_xor_sync(0xffffffffu, dotq, 1);
+    dotq += __shfl_xor_sync(0xffffffffu, dotq, 2);
+    if (live) {
+#pragma unroll 4
+      for (int q = 0; q < 32; ++q) {
+        const int cc = 32 * part + q;
+        const float kh = bf(sKr[j * 128 + cc]) * cr, qh = bf(sQr[j * 128 + cc]) * qn;
+        g.dq[o + cc] = a.q_l2norm ? (dqh[q] - qh * dotq) * qn : dqh[q];
+        // Diagonal KDN: dk^ of the memory part stays for kdn_gain_bwd
+        if (!kKdn) g.dk[o + cc] = a.k_l2norm ? (dkh[q] - kh * dotk) * cr : dkh[q];
+      }
+      if (!kKdn && part == 0) g.deta[tok(a, b, t0 + j, h)] = deta;
+    }
+  }
+  __syncthreads();
+  // ---- per channel: dG on the last token, then d log alpha = the reverse cumulative sum
+  if (tid < 128) {
+    const int cc = tid;
+    const float gC = sG[63 * cLDK + cc];
+    float dG = g.w.SS[(size_t)task * 128 + cc];
+    const float* xw = g.w.XW + (size_t)task * 8192;
+    for (int j = 0; j < Cc; ++j)
+      dG += sW[j * cLDK + cc] * __expf(gC - sG[j * cLDK + cc]) * xw[j * 128 + cc];
+    float acc = 0.f;
+    for (int j = Cc - 1; j >= 0; --j) {
+      const long o = tok(a, b, t0 + j, h) * 128 + cc;
+      acc += g.dla[o] + (j == Cc - 1 ? dG : 0.f);
+      g.dla[o] = acc;
+    }
+  }
+}
+
 // ================================================================= pgdn_gain_bwd
 // One CTA per (b, h), a thread per key channel, chunks in reverse.  Per chunk the
 // statistic A_t is recomputed forward from its chunk-start value (the forward's
@@ -1027,22 +1323,24 @@ __global__ void pgdn_dmu_kernel(FwdArgs a, BwdArgs g) {
 }  // namespace
 
 bool chunk_bwd_supported(int variant, int dtype, int dk, int dv, int chunk) {
-  return (variant == DR_GDN || variant == DR_KLA || variant == DR_PGDN) && dtype == DR_BF16 &&
-         dk == 128 && dv == 128 && chunk == 64;
+  return (variant == DR_GDN || variant == DR_KLA || variant == DR_PGDN || variant == DR_KDA) &&
+         dtype == DR_BF16 && dk == 128 && dv == 128 && chunk == 64;
 }
 
 size_t chunk_bwd_workspace_bytes(int variant, int B, int T, int H) {
   const long n = (long)B * H * ((T + 63) / 64);
-  return bwd_layout(nullptr, n, B * H, variant == DR_PGDN, nullptr);
+  return bwd_layout(nullptr, n, B * H, bwd_mode(variant), nullptr);
 }
 
 cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* dS_final,
                              const dr_grads& gr, void* workspace, cudaStream_t st) {
   const long n = (long)fa.B * fa.H * ((fa.T + 63) / 64);
   const bool pg = fa.variant == DR_PGDN;
+  const int mode = bwd_mode(fa.variant);
+  const bool pc = mode >= BW_PC;
   BwdArgs g{d_out,      dS_final,    gr.dq,      gr.dk,      gr.dv,     gr.d_log_alpha,
             gr.d_eta,   gr.d_init_state, gr.d_alphaP, gr.d_betaP, gr.d_mu, gr.d_aux_init,
-            gr.d_aux_final, bwd_ws(workspace, n, fa.B * fa.H, pg)};
+            gr.d_aux_final, gr.d_omega, gr.d_r, bwd_ws(workspace, n, fa.B * fa.H, mode)};
   // the forward again: the records, the state at every chunk start and E (no
   // output, no final state)
   FwdArgs a = fa;
@@ -1052,15 +1350,25 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
   a.check_finite = 0;
   a.save_S = g.w.S;
   a.save_E = g.w.E;
-  cudaError_t e = launch_chunk_tc_split(a, workspace, st);
+  if (pc) a.save_W = g.w.Wf;
+  cudaError_t e = pc ? launch_kdn_split(a, DR_BF16, workspace, st) : launch_chunk_tc_split(a, workspace, st);
   if (e != cudaSuccess) return e;
   const size_t c_smem = (size_t)kCarrySmemF * 4, s_smem = (size_t)kStateSmemF * 4,
                l_smem = (size_t)kLocalSmemF * 4, p_smem = (size_t)kGainSmemF * 4;
-  if ((e = cudaFuncSetAttribute(bwd_carry_kernel<false>,
+  if ((e = cudaFuncSetAttribute(bwd_carry_kernel<false, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c_smem)) !=
           cudaSuccess ||
-      (e = cudaFuncSetAttribute(bwd_carry_kernel<true>,
+      (e = cudaFuncSetAttribute(bwd_carry_kernel<true, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c_smem)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(bwd_carry_kernel<false, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c_smem)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(bwd_local_pc_kernel<DR_KDA>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kPcLocalSmem)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(bwd_local_pc_kernel<DR_KDN>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kPcLocalSmem)) !=
           cudaSuccess ||
       (e = cudaFuncSetAttribute(bwd_local_kernel<DR_PGDN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l_smem)) !=
@@ -1077,11 +1385,17 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
           cudaSuccess)
     return e;
   if (pg)
-    bwd_carry_kernel<true><<<fa.B * fa.H * 4, kBwdThreads, c_smem, st>>>(fa, g);
+    bwd_carry_kernel<true, false><<<fa.B * fa.H * 4, kBwdThreads, c_smem, st>>>(fa, g);
+  else if (pc)
+    bwd_carry_kernel<false, true><<<fa.B * fa.H * 4, kBwdThreads, c_smem, st>>>(fa, g);
   else
-    bwd_carry_kernel<false><<<fa.B * fa.H * 4, kBwdThreads, c_smem, st>>>(fa, g);
+    bwd_carry_kernel<false, false><<<fa.B * fa.H * 4, kBwdThreads, c_smem, st>>>(fa, g);
   bwd_state_kernel<<<(unsigned)n, kBwdThreads, s_smem, st>>>(fa, g);
-  if (fa.variant == DR_KLA) {
+  if (fa.variant == DR_KDA) {
+    bwd_local_pc_kernel<DR_KDA><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
+  } else if (fa.variant == DR_KDN) {
+    bwd_local_pc_kernel<DR_KDN><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
+  } else if (fa.variant == DR_KLA) {
     bwd_local_kernel<DR_KLA><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
   } else if (pg) {
     bwd_local_kernel<DR_PGDN><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);

@@ -574,7 +574,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float s = vsc[j] * vcr[j];
       float w[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) w[e] = s * k8[e] * f8[e] * __expf(gm[e] - gj[e]);
+      for (int e = 0; e < 8; ++e) w[e] = s * k8[e] * f8[e];
+      if (a.save_W) {   // backward: the write vectors themselves
+        float4* sw = reinterpret_cast<float4*>(a.save_W + ((size_t)ri * 64 + j) * 128 + cc);
+        sw[0] = make_float4(w[0], w[1], w[2], w[3]);
+        sw[1] = make_float4(w[4], w[5], w[6], w[7]);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] *= __expf(gm[e] - gj[e]);
       uint4 hi, lo;
 #pragma unroll 1
       for (int I = J; I < 4; ++I) {

@@ -40,6 +40,9 @@ struct FwdArgs {
   // [B H NC][64][dv] (fp32), and a null `out` skips the output stores
   float* save_S;
   float* save_E;
+  // backward only: the per-channel-decay prep saves every chunk's write vectors
+  // w [B H NC][64][dk] (fp32; zero on padding rows)
+  float* save_W;
   // segment-parallel carry (scalar-decay two-phase path, few rows and many
   // chunks): 0 = whole rows; 1 = first pass (segment 0 with its outputs, and
   // every middle segment's zero-start state and transition map); 2 = replay of

@@ -77,7 +77,7 @@ class DrGrads(ctypes.Structure):
     _fields_ = [("dq", c_void_p), ("dk", c_void_p), ("dv", c_void_p), ("d_log_alpha", c_void_p),
                 ("d_eta", c_void_p), ("d_init_state", c_void_p), ("d_alphaP", c_void_p),
                 ("d_betaP", c_void_p), ("d_mu", c_void_p), ("d_aux_init", c_void_p),
-                ("d_aux_final", c_void_p)]
+                ("d_aux_final", c_void_p), ("d_omega", c_void_p), ("d_r", c_void_p)]
 
 
 _lib.dr_chunk_bwd.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, ctypes.POINTER(DrParams),

@@ -102,8 +102,9 @@ def chunk_bwd(inp: dict, d_out, *, d_final_state=None, init_state=None, aux_init
               grads=None):
     """Run dr_chunk_bwd on a device input dict; returns a dict of fp32 gradients
     (dq, dk, dv, dlog_alpha, deta, with want_dS0 dS0, and for PGDN dalphaP,
-    dbetaP, dmu, daux0).  ``grads`` may hold preallocated output tensors under
-    the same names."""
+    dbetaP, dmu, daux0; Diagonal KDN domega, dr, daux0 and no deta).  With
+    per-channel decay (KDA, KDN) dlog_alpha is [B,T,H,dk].  ``grads`` may hold
+    preallocated output tensors under the same names."""
     q, k, v = inp["q"], inp["k"], inp["v"]
     B, T, H, dk = k.shape
     dv = v.shape[-1]
@@ -114,8 +115,10 @@ def chunk_bwd(inp: dict, d_out, *, d_final_state=None, init_state=None, aux_init
     g.setdefault("dq", torch.empty(B, T, H, dk, **f32))
     g.setdefault("dk", torch.empty(B, T, H, dk, **f32))
     g.setdefault("dv", torch.empty(B, T, H, dv, **f32))
-    g.setdefault("dlog_alpha", torch.empty(B, T, H, **f32))
-    g.setdefault("deta", torch.empty(B, T, H, **f32))
+    per_channel = inp["variant"] in ("kda", "kdn", "pkda", "ikdn")
+    g.setdefault("dlog_alpha", torch.empty(*((B, T, H, dk) if per_channel else (B, T, H)), **f32))
+    if inp["variant"] != "kdn":
+        g.setdefault("deta", torch.empty(B, T, H, **f32))
     if want_dS0:
         g.setdefault("dS0", torch.empty(B, H, dk, dv, **f32))
     if inp["variant"] == "pgdn":
@@ -123,13 +126,17 @@ def chunk_bwd(inp: dict, d_out, *, d_final_state=None, init_state=None, aux_init
         g.setdefault("dbetaP", torch.empty(B, T, H, **f32))
         g.setdefault("dmu", torch.empty(H, **f32))
         g.setdefault("daux0", torch.empty(B, H, dk, **f32))
+    if inp["variant"] == "kdn":
+        g.setdefault("domega", torch.empty(B, T, H, dk, **f32))
+        g.setdefault("dr", torch.empty(B, T, H, **f32))
+        g.setdefault("daux0", torch.empty(B, H, dk, **f32))
     p = params_for(inp, aux_init=aux_init)
     if workspace is not None:
         p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
     gs = dr.make_grads(dq=g["dq"], dk=g["dk"], dv=g["dv"], d_log_alpha=g["dlog_alpha"],
-                       d_eta=g["deta"], d_init_state=g.get("dS0"), d_alphaP=g.get("dalphaP"),
+                       d_eta=g.get("deta"), d_init_state=g.get("dS0"), d_alphaP=g.get("dalphaP"),
                        d_betaP=g.get("dbetaP"), d_mu=g.get("dmu"), d_aux_init=g.get("daux0"),
-                       d_aux_final=d_aux_final)
+                       d_aux_final=d_aux_final, d_omega=g.get("domega"), d_r=g.get("dr"))
     st = dr.dr_chunk_bwd(q, k, v, inp["log_alpha"], p, dr.VARIANT_IDS[inp["variant"]],
                          inp.get("eps", 1e-6), init_state, d_out, d_final_state, gs, B, T, H, dk,
                          dv, chunk or inp.get("chunk", 64), stream)

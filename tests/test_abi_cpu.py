@@ -211,6 +211,12 @@ def test_backward_refusals_and_workspace_size(dr):
     need_p = dr.dr_chunk_bwd_workspace_bytes(dr.DR_PGDN, dr.DR_BF16, 2, 130, 3, 128, 128, 64)
     assert need_p == (al(n * 101376) + sum(al(n * x) for x in arrays) + al(4 * n) + al(n * 32768)
                       + al(n * 256) + al(4 * rows))
+    # per-channel decay (KDA): the per-channel record and the forward's hand-over
+    # flags, gamma_c <dS_c, S_c> per channel, the forward's write vectors
+    chain = -(-((n + 2) * 4) // 256) * 256
+    need_a = dr.dr_chunk_bwd_workspace_bytes(dr.DR_KDA, dr.DR_BF16, 2, 130, 3, 128, 128, 64)
+    assert need_a == (al(n * 135168 + chain) + sum(al(n * x) for x in arrays) + al(4 * 128 * n)
+                      + al(n * 32768))
     assert call(ws=(A, 1000)) == dr.DR_ERR_WORKSPACE
     assert call(ws=(A + 16, 1 << 30)) == dr.DR_ERR_ALIGN
     assert dr.dr_chunk_bwd_workspace_bytes(dr.DR_KDN, dr.DR_BF16, 1, 64, 1, 128, 128, 64) == 0

@@ -32,15 +32,22 @@ def rt():
 PG_NAMES = ("dalphaP", "dbetaP", "dmu", "daux0")
 
 
+KDN_NAMES = ("dq", "dk", "dv", "dlog_alpha", "dS0", "domega", "dr", "daux0")
+
+
 def oracle_grads(inp, dO, dS, S0, aux0=None, daux=None):
     f = lambda t: None if t is None else t.double().cpu().numpy()  # noqa: E731
     g = obw.tokenwise_backward(f(inp["q"]), f(inp["k"]), f(inp["v"]), f(inp["log_alpha"]),
-                               inp["variant"], f(dO), f(dS), eta=f(inp["eta"]), eps=inp["eps"],
-                               q_l2norm=inp["q_l2norm"], k_l2norm=inp["k_l2norm"], S0=f(S0),
+                               inp["variant"], f(dO), f(dS), eta=f(inp.get("eta")),
+                               eps=inp["eps"], q_l2norm=inp["q_l2norm"],
+                               k_l2norm=inp["k_l2norm"], S0=f(S0),
                                alphaP=f(inp.get("alphaP")), betaP=f(inp.get("betaP")),
                                mu=f(inp.get("mu")), x=inp.get("x", 1.5),
-                               log_floor=inp.get("log_floor", 1e-12), aux0=f(aux0),
-                               daux_T=f(daux))
+                               log_floor=inp.get("log_floor", 1e-12), omega=f(inp.get("omega")),
+                               r=f(inp.get("r")), info_scale=inp.get("info_scale", 1.0),
+                               aux0=f(aux0), daux_T=f(daux))
+    if inp["variant"] == "kdn":
+        return {n: g[n] for n in KDN_NAMES}
     names = NAMES + (PG_NAMES if inp["variant"] == "pgdn" else ())
     return {n: g[n] for n in names}
 
@@ -165,5 +172,57 @@ def test_pgdn_backward_workload_sampled(rt):
     for n, r in ref.items():
         x = torch.stack([g[n][b, :, h] for b, h in pairs])
         x = x[:, :, None]
+        errs[n] = rel_err(np64(x), r)
+    assert all(e <= TOL["bf16"] for e in errs.values()), errs
+
+
+# ------------------------------------------------------------ per-channel decay (KDA)
+
+@pytest.mark.parametrize("T,norms", [(64, True), (200, True), (333, False), (1, True), (130, True)])
+def test_kda_backward_matches_oracle(rt, T, norms):
+    """KDA (w = eta k^, D = diag(alpha) per channel): the sub-chunk-referenced
+    Gram gradients, the per-channel decay gradient [B,T,H,dk], d eta, dL/dS_0."""
+    wl = W.small("kda_bf16", B=2, T=T, H=3, seed=90 + T, k_l2norm=norms, q_l2norm=norms)
+    inp = W.generate(wl, "kda")
+    g, dO, dS, S0 = run_case(rt, inp, seed=T)
+    assert g["dlog_alpha"].shape == (2, T, 3, 128)
+    check(g, oracle_grads(inp, dO, dS, S0))
+
+
+def test_kda_backward_many_rows_chained_shape(rt):
+    """Enough rows that the forward's per-channel prep runs its chunk-major order
+    (3 B H >= SM count), a ragged tail."""
+    dr, runner = rt
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    H = -(-nsm // 6)
+    wl = W.small("kda_bf16", B=2, T=150, H=H, seed=7)
+    inp = W.generate(wl, "kda")
+    g, dO, dS, S0 = run_case(rt, inp, seed=3)
+    pairs = [(0, 0), (1, H - 1)]
+    sub = slice_heads(inp, pairs)
+    dO_s = torch.stack([dO[b, :, h] for b, h in pairs])[:, :, None]
+    dS_s = torch.stack([dS[b, h] for b, h in pairs])[:, None]
+    S0_s = torch.stack([S0[b, h] for b, h in pairs])[:, None]
+    check(g, oracle_grads(sub, dO_s, dS_s, S0_s), pairs=pairs)
+
+
+def test_kda_backward_workload_sampled(rt):
+    """B4 H16 T8192 (the KDA workload): one sampled row's per-token gradients."""
+    dr, runner = rt
+    wl = W.WORKLOADS["kda_bf16"]
+    inp = W.generate(wl, "kda")
+    gen = torch.Generator().manual_seed(13)
+    dO = torch.randn(wl.B, wl.T, wl.H, 128, generator=gen).to(torch.bfloat16)
+    g = runner.chunk_bwd(runner.to_device(inp), dO.cuda())
+    torch.cuda.synchronize()
+    assert dr.dr_get_device_status() == 0
+    pairs = [(wl.B - 1, 7)]
+    sub = slice_heads(inp, pairs)
+    dO_s = torch.stack([dO[b, :, h] for b, h in pairs])[:, :, None]
+    ref = oracle_grads(sub, dO_s, None, None)
+    ref.pop("dS0")
+    errs = {}
+    for n, r in ref.items():
+        x = torch.stack([g[n][b, :, h] for b, h in pairs])[:, :, None]
         errs[n] = rel_err(np64(x), r)
     assert all(e <= TOL["bf16"] for e in errs.values()), errs
