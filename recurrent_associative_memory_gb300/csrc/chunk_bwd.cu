@@ -1311,6 +1311,156 @@ __global__ void __launch_bounds__(128, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArg
   if (i == 0) g.w.MU[bh] = s_mu[0] + s_mu[1] + s_mu[2] + s_mu[3];
 }
 
+// ================================================================= kdn_gain_bwd
+// Diagonal KDN's write vector is the Kalman gain w = p^ . k^ / (r + sum_c p^ k^2)
+// with the predicted variance p^_t = alpha_t^2 p_{t-1} + omega_t and the posterior
+// p_t = p^_t / (1 + u_t p^_t), u_t = (mu / r_t) k^_t^2 (KDN notes Eq. (23) and
+// section 5).  One CTA per (b, h), a thread per key channel, chunks in reverse:
+// p^ and p are recomputed over the chunk from its chunk-start variance (the
+// forward's record), den_t = r_t + sum_c p^ k^2 and c_t = sum_c dw p^ k^ per token,
+// then the tokens are walked backwards with the variance adjoint dp (from dL/dp_T):
+//   dp^ = dw k^ / den - (c / den^2) k^2 + dp / q^2,  q = 1 + u p^,  du = -dp p^2 / q^2,
+//   dk^ += dw p^ / den - 2 (c / den^2) p^ k^ + 2 (mu / r) k^ du,
+//   d omega = dp^,  d log alpha += 2 alpha^2 p_{t-1} dp^,  dp <- alpha^2 dp^,
+// and per token d r = -c / den^2 - (mu / r^2) sum_c k^2 du and the key norm.  dp at
+// the row start is dL/dp_0.
+constexpr int kKdnGainSmemF = 6 * 64 * 128;
+
+__global__ void __launch_bounds__(128, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
+  extern __shared__ __align__(16) float smf[];
+  float* sK = smf;                  // k^ [t][c]
+  float* sDW = sK + 64 * 128;       // dL/dw, then k^2 du
+  float* sDK = sDW + 64 * 128;      // dL/dk^: the memory part, then the total
+  float* sA = sDK + 64 * 128;       // log-decay, then alpha
+  float* sPh = sA + 64 * 128;       // omega, then p^
+  float* sPo = sPh + 64 * 128;      // p (posterior)
+  __shared__ float s_r[64], s_cr[64], s_den[64], s_cc[64];
+  const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
+  const int bh = blockIdx.x, b = bh / a.H, h = bh % a.H;
+  const int NC = (a.T + 63) / 64;
+  const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
+  const float mu = a.info_scale;
+  float dp = g.daux_T ? g.daux_T[(size_t)bh * 128 + i] : 0.f;
+  for (int c = NC - 1; c >= 0; --c) {
+    const size_t ri = (size_t)bh * NC + c;
+    const int t0 = 64 * c, Cc = min(64, a.T - t0);
+    __syncthreads();
+    if (i < 64) s_r[i] = i < Cc ? a.r[tok(a, b, t0 + i, h)] : 1.f;
+    for (int e = i; e < 64 * 32; e += 128) {
+      const int t = e >> 5, c4 = 4 * (e & 31);
+      const bool live = t < Cc;
+      const long o = tok(a, b, t0 + (live ? t : 0), h) * 128 + c4;
+      cpa16(sDW + t * 128 + c4, g.w.DW + ri * 8192 + t * 128 + c4, live ? 16 : 0);
+      cpa16(sDK + t * 128 + c4, g.dk + o, live ? 16 : 0);
+      cpa16(sA + t * 128 + c4, a.log_alpha + o, live ? 16 : 0);
+      cpa16(sPh + t * 128 + c4, a.omega + o, live ? 16 : 0);
+    }
+    for (int e = i; e < 64 * 16; e += 128) {   // raw keys
+      const int t = e >> 4, c0 = 8 * (e & 15);
+      float f[8];
+      if (t < Cc) {
+        unpack8(*reinterpret_cast<const uint4*>(K + tok(a, b, t0 + t, h) * 128 + c0), f);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) f[q] = 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sK[t * 128 + c0 + q] = f[q];
+    }
+    cpa_wait_all();
+    __syncthreads();
+    for (int tt = 0; tt < 16; ++tt) {   // key norms: warp w takes tokens 16 w .. + 15
+      const int t = 16 * warp + tt;
+      float kk = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float x = sK[t * 128 + lane + 32 * m];
+        kk += x * x;
+      }
+      kk = warp_sum(kk);
+      if (lane == 0) s_cr[t] = a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f;
+    }
+    __syncthreads();
+    // the variance over the chunk from its chunk-start value (thread i = channel i)
+    const float p0 = c == 0 ? (a.aux0 ? a.aux0[(size_t)bh * 128 + i] : 1.f)
+                            : reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rP0PC)[i];
+    {
+      float pv = p0;
+      for (int t = 0; t < Cc; ++t) {
+        const float kh = sK[t * 128 + i] * s_cr[t];
+        sK[t * 128 + i] = kh;
+        const float al = expf(sA[t * 128 + i]);
+        const float ph = al * al * pv + sPh[t * 128 + i];
+        pv = ph / (1.f + (mu / s_r[t]) * kh * kh * ph);
+        sA[t * 128 + i] = al;
+        sPh[t * 128 + i] = ph;
+        sPo[t * 128 + i] = pv;
+      }
+    }
+    __syncthreads();
+    for (int tt = 0; tt < 16; ++tt) {   // den_t and c_t
+      const int t = 16 * warp + tt;
+      if (t >= Cc) break;
+      float z = 0.f, cc = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int ch = lane + 32 * m;
+        const float kh = sK[t * 128 + ch], ph = sPh[t * 128 + ch];
+        z += ph * kh * kh;
+        cc += sDW[t * 128 + ch] * ph * kh;
+      }
+      z = warp_sum(z);
+      cc = warp_sum(cc);
+      if (lane == 0) {
+        s_den[t] = s_r[t] + z;
+        s_cc[t] = cc;
+      }
+    }
+    __syncthreads();
+    // backwards over the chunk's tokens, per channel (the chain through dp)
+    for (int t = Cc - 1; t >= 0; --t) {
+      const float kh = sK[t * 128 + i], ph = sPh[t * 128 + i], al = sA[t * 128 + i];
+      const float dwv = sDW[t * 128 + i], den = s_den[t], cc = s_cc[t], mr = mu / s_r[t];
+      const float q1 = 1.f + mr * kh * kh * ph;
+      const float iq2 = 1.f / (q1 * q1), cd2 = cc / (den * den);
+      const float dph = dwv * kh / den - cd2 * kh * kh + dp * iq2;
+      const float du = -dp * ph * ph * iq2;
+      sDK[t * 128 + i] += dwv * ph / den - 2.f * cd2 * ph * kh + 2.f * mr * kh * du;
+      sDW[t * 128 + i] = kh * kh * du;
+      const float prev = t > 0 ? sPo[(t - 1) * 128 + i] : p0;
+      const long o = tok(a, b, t0 + t, h) * 128 + i;
+      g.domega[o] = dph;
+      g.dla[o] += 2.f * al * al * prev * dph;
+      dp = al * al * dph;
+    }
+    __syncthreads();
+    for (int tt = 0; tt < 16; ++tt) {   // d r and the key norm, warp w: tokens 16 w .. + 15
+      const int t = 16 * warp + tt;
+      if (t >= Cc) break;
+      float su = 0.f, dot = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int ch = lane + 32 * m;
+        su += sDW[t * 128 + ch];
+        dot += sK[t * 128 + ch] * sDK[t * 128 + ch];
+      }
+      su = warp_sum(su);
+      dot = warp_sum(dot);
+      const float rt = s_r[t], den = s_den[t];
+      if (lane == 0) g.dr[tok(a, b, t0 + t, h)] = -s_cc[t] / (den * den) - mu / (rt * rt) * su;
+      const float cr = s_cr[t];
+      float* dkrow = g.dk + tok(a, b, t0 + t, h) * 128;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int ch = lane + 32 * m;
+        const float v = sDK[t * 128 + ch];
+        dkrow[ch] = a.k_l2norm ? (v - sK[t * 128 + ch] * dot) * cr : v;
+      }
+    }
+  }
+  if (g.daux0) g.daux0[(size_t)bh * 128 + i] = dp;
+}
+
 // dL/dmu_h: the rows' parts summed over the batch in order
 __global__ void pgdn_dmu_kernel(FwdArgs a, BwdArgs g) {
   const int h = blockIdx.x * blockDim.x + threadIdx.x;
@@ -1323,7 +1473,8 @@ __global__ void pgdn_dmu_kernel(FwdArgs a, BwdArgs g) {
 }  // namespace
 
 bool chunk_bwd_supported(int variant, int dtype, int dk, int dv, int chunk) {
-  return (variant == DR_GDN || variant == DR_KLA || variant == DR_PGDN || variant == DR_KDA) &&
+  return (variant == DR_GDN || variant == DR_KLA || variant == DR_PGDN || variant == DR_KDA ||
+          variant == DR_KDN) &&
          dtype == DR_BF16 && dk == 128 && dv == 128 && chunk == 64;
 }
 
@@ -1370,6 +1521,8 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
       (e = cudaFuncSetAttribute(bwd_local_pc_kernel<DR_KDN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kPcLocalSmem)) !=
           cudaSuccess ||
+      (e = cudaFuncSetAttribute(kdn_gain_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kKdnGainSmemF * 4)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(bwd_local_kernel<DR_PGDN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l_smem)) !=
           cudaSuccess ||
@@ -1395,6 +1548,7 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
     bwd_local_pc_kernel<DR_KDA><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
   } else if (fa.variant == DR_KDN) {
     bwd_local_pc_kernel<DR_KDN><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
+    kdn_gain_bwd_kernel<<<fa.B * fa.H, 128, kKdnGainSmemF * 4, st>>>(fa, g);
   } else if (fa.variant == DR_KLA) {
     bwd_local_kernel<DR_KLA><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
   } else if (pg) {

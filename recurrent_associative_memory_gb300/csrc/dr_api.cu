@@ -234,8 +234,9 @@ int dr_chunk_bwd(const void* q, const void* k, const void* v, const float* log_a
                  const void* d_out, const float* d_final_state, const dr_grads* g, int B, int T,
                  int H, int dk_, int dv_, int chunk, dr_stream_t stream) {
   if (!gp || !g || !q || !k || !v || !log_alpha || !d_out || !g->dq || !g->dk || !g->dv ||
-      !g->d_log_alpha || !g->d_eta)
+      !g->d_log_alpha)
     return DR_ERR_NULL;
+  if (variant == DR_KDN ? (!g->d_omega || !g->d_r) : !g->d_eta) return DR_ERR_NULL;
   if (gp->dtype != DR_FP32 && gp->dtype != DR_BF16) return DR_ERR_DTYPE;
   if (B < 1 || T < 1 || H < 1 || !dim_ok(dk_) || !dim_ok(dv_)) return DR_ERR_SHAPE;
   if (chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128) return DR_ERR_SHAPE;
@@ -249,6 +250,7 @@ int dr_chunk_bwd(const void* q, const void* k, const void* v, const float* log_a
       !aligned16(d_out) || !aligned16(d_final_state) || !aligned16(g->dq) || !aligned16(g->dk) ||
       !aligned16(g->dv) || !aligned16(init_state) || !aligned16(g->d_init_state))
     return DR_ERR_ALIGN;
+  if (variant == DR_KDN && !aligned16(gp->omega)) return DR_ERR_ALIGN;   // 16-byte copies
   const size_t need = chunk_bwd_workspace_bytes(variant, B, T, H);
   if (!gp->workspace || gp->workspace_bytes < need) return DR_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(gp->workspace) & 255u) return DR_ERR_ALIGN;

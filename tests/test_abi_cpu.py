@@ -194,8 +194,11 @@ def test_backward_refusals_and_workspace_size(dr):
     assert call(dq=None) == dr.DR_ERR_NULL
     assert call(T=0) == dr.DR_ERR_SHAPE
     assert call(chunk=48) == dr.DR_ERR_SHAPE
-    assert call(variant=dr.DR_KDN, params=dr.make_params(dtype=dr.DR_BF16, omega=A, r=A)) == \
-        dr.DR_ERR_UNSUPPORTED
+    kp = dr.make_params(dtype=dr.DR_BF16, omega=A, r=A)
+    assert call(variant=dr.DR_KDN, params=kp) == dr.DR_ERR_NULL        # no d omega, d r
+    assert call(variant=dr.DR_KDN, params=kp, d_eta=None, d_omega=A, d_r=A) == dr.DR_ERR_WORKSPACE
+    assert call(variant=dr.DR_PKDA, params=dr.make_params(dtype=dr.DR_BF16, eta=A, alphaP=A,
+                                                           betaP=A, mu=A)) == dr.DR_ERR_UNSUPPORTED
     assert call(d=64) == dr.DR_ERR_UNSUPPORTED
     assert call(chunk=32) == dr.DR_ERR_UNSUPPORTED
     assert call(params=dr.make_params(dtype=dr.DR_FP32, eta=A)) == dr.DR_ERR_UNSUPPORTED
@@ -219,7 +222,10 @@ def test_backward_refusals_and_workspace_size(dr):
                       + al(n * 32768))
     assert call(ws=(A, 1000)) == dr.DR_ERR_WORKSPACE
     assert call(ws=(A + 16, 1 << 30)) == dr.DR_ERR_ALIGN
-    assert dr.dr_chunk_bwd_workspace_bytes(dr.DR_KDN, dr.DR_BF16, 1, 64, 1, 128, 128, 64) == 0
+    # Diagonal KDN: as KDA plus dL/dw
+    need_k = dr.dr_chunk_bwd_workspace_bytes(dr.DR_KDN, dr.DR_BF16, 2, 130, 3, 128, 128, 64)
+    assert need_k == need_a + al(n * 32768)
+    assert dr.dr_chunk_bwd_workspace_bytes(dr.DR_PKDA, dr.DR_BF16, 1, 64, 1, 128, 128, 64) == 0
 
 
 def test_grads_struct_layout_matches_c(dr):

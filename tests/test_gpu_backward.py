@@ -226,3 +226,91 @@ def test_kda_backward_workload_sampled(rt):
         x = torch.stack([g[n][b, :, h] for b, h in pairs])[:, :, None]
         errs[n] = rel_err(np64(x), r)
     assert all(e <= TOL["bf16"] for e in errs.values()), errs
+
+
+# ------------------------------------------------------------ Diagonal KDN
+
+def run_kdn(rt, inp, seed, with_aux=True):
+    dr, runner = rt
+    B, T, H, dk = inp["k"].shape
+    gen = torch.Generator().manual_seed(seed)
+    dO = torch.randn(B, T, H, 128, generator=gen).to(torch.bfloat16)
+    dS = 0.1 * torch.randn(B, H, 128, 128, generator=gen)
+    S0 = 0.3 * torch.randn(B, H, 128, 128, generator=gen)
+    p0 = (0.5 + torch.rand(B, H, 128, generator=gen)) if with_aux else None
+    dp = (0.1 * torch.randn(B, H, 128, generator=gen)) if with_aux else None
+    g = runner.chunk_bwd(runner.to_device(inp), dO.cuda(), d_final_state=dS.cuda(),
+                         init_state=S0.cuda(), aux_init=None if p0 is None else p0.cuda(),
+                         d_aux_final=None if dp is None else dp.cuda())
+    torch.cuda.synchronize()
+    assert dr.dr_get_device_status() == 0
+    return g, dO, dS, S0, p0, dp
+
+
+@pytest.mark.parametrize("T,norms", [(64, True), (200, True), (333, False), (1, True)])
+def test_kdn_backward_matches_oracle(rt, T, norms):
+    """Diagonal KDN: the chunk part as KDA with the Kalman gains as write vectors,
+    then the variance adjoint carried backwards over the row (d omega, d r, the key
+    gradient through the gain and the variance update, the decay gradient through
+    alpha^2 p, dL/dp_0), with a nonzero p_0 and dL/dp_T."""
+    wl = W.small("kdn_bf16", B=2, T=T, H=3, seed=110 + T, k_l2norm=norms, q_l2norm=norms)
+    inp = W.generate(wl, "kdn")
+    g, dO, dS, S0, p0, dp = run_kdn(rt, inp, seed=T)
+    assert "deta" not in g and g["domega"].shape == (2, T, 3, 128)
+    check(g, oracle_grads(inp, dO, dS, S0, aux0=p0, daux=dp))
+
+
+def test_kdn_backward_information_scale_and_default_variance(rt):
+    """mu = d_k (the information-scaled update) and p_0 = 1 (no aux_init)."""
+    wl = W.small("kdn_bf16", B=1, T=150, H=2, seed=5, info_scale=128.0)
+    inp = W.generate(wl, "kdn")
+    g, dO, dS, S0, p0, dp = run_kdn(rt, inp, seed=6, with_aux=False)
+    check(g, oracle_grads(inp, dO, dS, S0))
+
+
+def test_kdn_backward_many_rows_chained_shape(rt):
+    """Enough rows for the forward's chained variance hand-over (3 B H >= SMs)."""
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    H = -(-nsm // 6)
+    wl = W.small("kdn_bf16", B=2, T=150, H=H, seed=8)
+    inp = W.generate(wl, "kdn")
+    g, dO, dS, S0, p0, dp = run_kdn(rt, inp, seed=9)
+    pairs = [(0, 1), (1, H - 1)]
+    sub = slice_heads(inp, pairs)
+    dO_s = torch.stack([dO[b, :, h] for b, h in pairs])[:, :, None]
+    dS_s = torch.stack([dS[b, h] for b, h in pairs])[:, None]
+    S0_s = torch.stack([S0[b, h] for b, h in pairs])[:, None]
+    p0_s = torch.stack([p0[b, h] for b, h in pairs])[:, None]
+    dp_s = torch.stack([dp[b, h] for b, h in pairs])[:, None]
+    ref = oracle_grads(sub, dO_s, dS_s, S0_s, aux0=p0_s, daux=dp_s)
+    errs = {}
+    for n, r in ref.items():
+        if n in ("dS0", "daux0"):
+            x = torch.stack([g[n][b, h] for b, h in pairs])[:, None]
+        else:
+            x = torch.stack([g[n][b, :, h] for b, h in pairs])[:, :, None]
+        errs[n] = rel_err(np64(x), r)
+    assert all(e <= TOL["bf16"] for e in errs.values()), errs
+
+
+def test_kdn_backward_workload_sampled(rt):
+    """B4 H16 T8192 (the Diagonal KDN workload): one sampled row's per-token gradients."""
+    dr, runner = rt
+    wl = W.WORKLOADS["kdn_bf16"]
+    inp = W.generate(wl, "kdn")
+    gen = torch.Generator().manual_seed(14)
+    dO = torch.randn(wl.B, wl.T, wl.H, 128, generator=gen).to(torch.bfloat16)
+    g = runner.chunk_bwd(runner.to_device(inp), dO.cuda())
+    torch.cuda.synchronize()
+    assert dr.dr_get_device_status() == 0
+    pairs = [(1, 9)]
+    sub = slice_heads(inp, pairs)
+    dO_s = torch.stack([dO[b, :, h] for b, h in pairs])[:, :, None]
+    ref = oracle_grads(sub, dO_s, None, None)
+    for n in ("dS0", "daux0"):
+        ref.pop(n)
+    errs = {}
+    for n, r in ref.items():
+        x = torch.stack([g[n][b, :, h] for b, h in pairs])[:, :, None]
+        errs[n] = rel_err(np64(x), r)
+    assert all(e <= TOL["bf16"] for e in errs.values()), errs
