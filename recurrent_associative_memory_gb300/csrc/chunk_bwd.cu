@@ -69,9 +69,14 @@ constexpr uint32_t rWpPC = 16384, rQPC = 66560, rWbPC = 99328, rP0PC = 134144;
 // workspace layouts: scalar decay (GDN, KLA), PGDN (+ dL/dw, key norms, d mu
 // parts), per-channel decay (KDA: + the forward's write vectors, dG per channel),
 // Diagonal KDN (+ dL/dw)
-enum { BW_SCALAR = 0, BW_PGDN = 1, BW_PC = 2, BW_KDN = 3 };
+// (BW_GAIN: Diagonal KDN, PKDA, isotropic KDN, whose gain kernels take dL/dw; PKDA
+// also each row's part of dL/dmu)
+enum { BW_SCALAR = 0, BW_PGDN = 1, BW_PC = 2, BW_GAIN = 3 };
 inline int bwd_mode(int variant) {
-  return variant == DR_PGDN ? BW_PGDN : variant == DR_KDA ? BW_PC : variant == DR_KDN ? BW_KDN : BW_SCALAR;
+  if (variant == DR_PGDN) return BW_PGDN;
+  if (variant == DR_KDA) return BW_PC;
+  if (variant == DR_KDN || variant == DR_PKDA || variant == DR_IKDN) return BW_GAIN;
+  return BW_SCALAR;
 }
 
 struct BwdWs {
@@ -95,7 +100,7 @@ inline size_t al256(size_t bytes) { return (bytes + 255) / 256 * 256; }
 
 // Lays the arrays out from `base` (null: only the size), returns the bytes used.
 size_t bwd_layout(void* base, long n, int rows, int mode, BwdWs* w) {
-  const bool pgdn = mode == BW_PGDN, pc = mode >= BW_PC;
+  const bool pgdn = mode == BW_PGDN, pc = mode >= BW_PC, gain = mode == BW_GAIN;
   uint8_t* p = static_cast<uint8_t*>(base);
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -114,11 +119,9 @@ size_t bwd_layout(void* base, long n, int rows, int mode, BwdWs* w) {
   v.dP = reinterpret_cast<float*>(take((size_t)n * 4096 * 4));
   v.dL = reinterpret_cast<float*>(take((size_t)n * 4096 * 4));
   v.SS = reinterpret_cast<float*>(take((size_t)n * (pc ? 128 : 1) * 4));
-  if (pgdn || mode == BW_KDN) v.DW = reinterpret_cast<float*>(take((size_t)n * 8192 * 4));
-  if (pgdn) {
-    v.CR = reinterpret_cast<float*>(take((size_t)n * 64 * 4));
-    v.MU = reinterpret_cast<float*>(take((size_t)rows * 4));
-  }
+  if (pgdn || gain) v.DW = reinterpret_cast<float*>(take((size_t)n * 8192 * 4));
+  if (pgdn) v.CR = reinterpret_cast<float*>(take((size_t)n * 64 * 4));
+  if (pgdn || gain) v.MU = reinterpret_cast<float*>(take((size_t)rows * 4));
   if (pc) v.Wf = reinterpret_cast<float*>(take((size_t)n * 8192 * 4));
   if (w) *w = v;
   return off;
@@ -554,7 +557,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   cpa_wait_all();
   __syncthreads();
-  if (a.variant == DR_KDA || a.variant == DR_KDN) {   // per-channel decay: gamma_c <dS_c, S_c>
+  if (a.variant == DR_KDA || a.variant == DR_KDN || a.variant == DR_PKDA || a.variant == DR_IKDN) {
+    // per-channel decay: gamma_c <dS_c, S_c>
     const float* gam = reinterpret_cast<const float*>(g.w.rec + (size_t)task * g.w.recb + rVecF) + 128;
     for (int rr = 0; rr < 16; ++rr) {
       const int r = 16 * warp + rr;
@@ -955,13 +959,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // d log alpha = the reverse cumulative sum of dg per channel.  dq^ and dk^ gather
 // in the gradient arrays (bwd_state left X_Q = dO S_c^T, X_K = dR S_c^T there).
 // KDA's gain (w = eta k^): d eta = dw . k^, dk^ += eta dw, then the L2 norms;
-// Diagonal KDN keeps dw and dk^ for kdn_gain_bwd.
+// Diagonal KDN, PKDA and isotropic KDN keep dw and dk^ for their gain kernels.
 constexpr int kPcLocalSmem = (4 * 64 * cLDK + 2 * 64 * cLDM + 2 * 16 * cLDK) * 4 + 2 * 64 * 128 * 2;
 
 template <int VARIANT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_local_pc_kernel(FwdArgs a, BwdArgs g) {
-  constexpr bool kKdn = VARIANT == DR_KDN;
+  // every variant but KDA finishes its gain (and the key norm) in a gain kernel
+  constexpr bool kGainK = VARIANT != DR_KDA;
   extern __shared__ __align__(16) float smf[];
   float* sW = smf;                   // w [j][c]
   float* sG = sW + 64 * cLDK;        // cumulative log-decay g [j][c]
@@ -1005,7 +1010,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     cpa16(sMP + i * cLDM + c4, g.w.dP + (size_t)task * 4096 + i * 64 + c4);
     cpa16(sML + i * cLDM + c4, g.w.dL + (size_t)task * 4096 + i * 64 + c4);
   }
-  if (tid < 64) s_eta[tid] = (!kKdn && tid < Cc) ? a.eta[tok(a, b, t0 + tid, h)] : 0.f;
+  if (tid < 64) s_eta[tid] = (!kGainK && tid < Cc) ? a.eta[tok(a, b, t0 + tid, h)] : 0.f;
   for (int e = tid; e < 64 * 128; e += kBwdThreads) sDW[(e >> 7) * cLDK + (e & 127)] = 0.f;
   cpa_wait_all();
   __syncthreads();
@@ -1121,7 +1126,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float kh = bf(sKr[j * 128 + cc]) * cr, qh = bf(sQr[j * 128 + cc]) * qn;
       dkh[q] = live ? g.dk[o + cc] : 0.f;
       dqh[q] = live ? g.dq[o + cc] : 0.f;
-      if (kKdn) {
+      if (kGainK) {
         g.w.DW[(size_t)task * 8192 + j * 128 + cc] = dw;
       } else {
         dkh[q] += eta * dw;
@@ -1144,9 +1149,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float kh = bf(sKr[j * 128 + cc]) * cr, qh = bf(sQr[j * 128 + cc]) * qn;
         g.dq[o + cc] = a.q_l2norm ? (dqh[q] - qh * dotq) * qn : dqh[q];
         // Diagonal KDN: dk^ of the memory part stays for kdn_gain_bwd
-        if (!kKdn) g.dk[o + cc] = a.k_l2norm ? (dkh[q] - kh * dotk) * cr : dkh[q];
+        if (!kGainK) g.dk[o + cc] = a.k_l2norm ? (dkh[q] - kh * dotk) * cr : dkh[q];
       }
-      if (!kKdn && part == 0) g.deta[tok(a, b, t0 + j, h)] = deta;
+      if (!kGainK && part == 0) g.deta[tok(a, b, t0 + j, h)] = deta;
     }
   }
   __syncthreads();
@@ -1178,9 +1183,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 //   dk^ += eta B dw + 2 betaP k^ dA_t,   dA <- alphaP dA_t (to token t-1),
 // then the key norm.  The walk backwards is per channel (the chain through dA);
 // the sums over channels follow per token, a warp per 16 tokens, A_{t-1}
-// recomputed from the chunk start.  dA at the row start is dL/dA_0.
+// recomputed from the chunk start.  dA at the row start is dL/dA_0.  PC (PKDA, the
+// same statistic with per-channel decay, which the statistic does not involve):
+// the chunk-start statistic comes from the per-channel record and the key norms
+// are formed here.
 constexpr int kGainSmemF = 4 * 64 * 128;
 
+template <bool PC>
 __global__ void __launch_bounds__(128, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
   extern __shared__ __align__(16) float smf[];
   float* sK = smf;                  // k^ [t][i]
@@ -1205,7 +1214,7 @@ __global__ void __launch_bounds__(128, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArg
       s_aP[i] = live ? a.alphaP[ti] : 1.f;
       s_bP[i] = live ? a.betaP[ti] : 0.f;
       s_eta[i] = live ? a.eta[ti] : 0.f;
-      s_cr[i] = live ? g.w.CR[ri * 64 + i] : 0.f;
+      if (!PC) s_cr[i] = live ? g.w.CR[ri * 64 + i] : 0.f;
     }
     for (int e = i; e < 64 * 32; e += 128) {   // dL/dw and the memory part of dL/dk^
       const int t = e >> 5, c4 = 4 * (e & 31);
@@ -1225,11 +1234,30 @@ __global__ void __launch_bounds__(128, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArg
         for (int q = 0; q < 8; ++q) f[q] = 0.f;
       }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) sK[t * 128 + c0 + q] = f[q] * s_cr[t];
+      for (int q = 0; q < 8; ++q) sK[t * 128 + c0 + q] = PC ? f[q] : f[q] * s_cr[t];
     }
     __syncthreads();
+    if (PC) {   // key norms (warp w: tokens 16 w .. + 15), then k^ = k cr
+      for (int tt = 0; tt < 16; ++tt) {
+        const int t = 16 * warp + tt;
+        float kk = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const float x = sK[t * 128 + lane + 32 * m];
+          kk += x * x;
+        }
+        kk = warp_sum(kk);
+        if (lane == 0) s_cr[t] = t < Cc ? (a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f) : 0.f;
+      }
+      __syncthreads();
+      for (int e = i; e < 64 * 128; e += 128) sK[e] *= s_cr[e >> 7];
+      __syncthreads();
+    }
     // the statistic over the chunk from its chunk-start value
-    const float A0 = reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rAuxF)[256 + i];
+    const float A0 =
+        PC ? (c == 0 ? (a.aux0 ? a.aux0[(size_t)bh * 128 + i] : 0.f)
+                     : reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rP0PC)[i])
+           : reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rAuxF)[256 + i];
     {
       float A = A0;
       for (int t = 0; t < Cc; ++t) {
@@ -1261,8 +1289,12 @@ __global__ void __launch_bounds__(128, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArg
     // a lane four channels, A_{t-1} recomputed from the chunk start on the way
     float Ap[4];
 #pragma unroll
-    for (int m = 0; m < 4; ++m)
-      Ap[m] = reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rAuxF)[256 + lane + 32 * m];
+    for (int m = 0; m < 4; ++m) {
+      const int ch = lane + 32 * m;
+      Ap[m] = PC ? (c == 0 ? (a.aux0 ? a.aux0[(size_t)bh * 128 + ch] : 0.f)
+                           : reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rP0PC)[ch])
+                 : reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rAuxF)[256 + ch];
+    }
     for (int t = 0; t < 16 * warp && t < Cc; ++t) {   // A up to this warp's first token
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
@@ -1461,6 +1493,150 @@ __global__ void __launch_bounds__(128, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs
   if (g.daux0) g.daux0[(size_t)bh * 128 + i] = dp;
 }
 
+// ================================================================= ikdn_gain_bwd
+// Isotropic KDN keeps one variance b per head: b^_t = abar_t b_{t-1} + omega_t with
+// abar_t = mean_c alpha_tc^2, w_t = beta_t k^_t, beta = b^ / (r + b^ s), s = ||k^||^2,
+// b_t = b^ / (1 + u b^), u = mu s / (dk r) (KDN notes Eq. (40)).  One CTA per (b, h),
+// chunks in reverse: per token (in parallel) s, abar and d beta = k^ . dw; the
+// scalar chain over the chunk's tokens (thread 0; b^ recomputed from the chunk-start
+// variance of the record) with db (from dL/db_T):
+//   db^ = d beta r / den^2 + db / q^2,  q = 1 + u b^,  du = -db b^2 / q^2,  den = r + b^ s,
+//   d omega = db^,  db <- abar db^;
+// then per (token, channel): dk^ += (b^ / den) dw + 2 ds k^ with
+// ds = -d beta b^2 / den^2 + du mu / (dk r),  d r = -d beta b^ / den^2 - du mu s / (dk r^2),
+// d log alpha += 2 alpha^2 b_{t-1} db^ / dk, and the key norm.  db at the row start
+// is dL/db_0.
+constexpr int kIkdnGainSmemF = 3 * 64 * 128;
+
+__global__ void __launch_bounds__(128, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
+  extern __shared__ __align__(16) float smf[];
+  float* sK = smf;                  // k^ [t][c]
+  float* sDW = sK + 64 * 128;       // dL/dw [t][c]
+  float* sA = sDW + 64 * 128;       // log-decay [t][c], then alpha^2
+  __shared__ float s_r[64], s_om[64], s_cr[64], s_s[64], s_ab[64], s_db[64];
+  __shared__ float s_bh[64], s_prev[64], s_dbh[64], s_du[64];
+  const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
+  const int bh = blockIdx.x, b = bh / a.H, h = bh % a.H;
+  const int NC = (a.T + 63) / 64;
+  const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
+  const float mu = a.info_scale;
+  float db = g.daux_T ? g.daux_T[bh] : 0.f;   // thread 0's chain
+  for (int c = NC - 1; c >= 0; --c) {
+    const size_t ri = (size_t)bh * NC + c;
+    const int t0 = 64 * c, Cc = min(64, a.T - t0);
+    __syncthreads();
+    if (i < 64) {
+      const bool live = i < Cc;
+      const long ti = tok(a, b, t0 + (live ? i : 0), h);
+      s_r[i] = live ? a.r[ti] : 1.f;
+      s_om[i] = live ? a.omega[ti] : 0.f;
+    }
+    for (int e = i; e < 64 * 32; e += 128) {
+      const int t = e >> 5, c4 = 4 * (e & 31);
+      const bool live = t < Cc;
+      const long o = tok(a, b, t0 + (live ? t : 0), h) * 128 + c4;
+      cpa16(sDW + t * 128 + c4, g.w.DW + ri * 8192 + t * 128 + c4, live ? 16 : 0);
+      cpa16(sA + t * 128 + c4, a.log_alpha + o, live ? 16 : 0);
+    }
+    for (int e = i; e < 64 * 16; e += 128) {
+      const int t = e >> 4, c0 = 8 * (e & 15);
+      float f[8];
+      if (t < Cc) {
+        unpack8(*reinterpret_cast<const uint4*>(K + tok(a, b, t0 + t, h) * 128 + c0), f);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) f[q] = 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sK[t * 128 + c0 + q] = f[q];
+    }
+    cpa_wait_all();
+    __syncthreads();
+    for (int tt = 0; tt < 16; ++tt) {   // per token: norm, s, abar, d beta (warp w: 16 w .. + 15)
+      const int t = 16 * warp + tt;
+      float kk = 0.f, a2 = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int ch = lane + 32 * m;
+        const float x = sK[t * 128 + ch], al = expf(sA[t * 128 + ch]);
+        kk += x * x;
+        a2 += al * al;
+        sA[t * 128 + ch] = al * al;
+      }
+      kk = warp_sum(kk);
+      a2 = warp_sum(a2);
+      const float cr = a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f;
+      float kd = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int ch = lane + 32 * m;
+        const float kh = sK[t * 128 + ch] * cr;
+        sK[t * 128 + ch] = kh;
+        kd += kh * sDW[t * 128 + ch];
+      }
+      kd = warp_sum(kd);
+      if (lane == 0) {
+        s_cr[t] = t < Cc ? cr : 0.f;
+        s_s[t] = kk * cr * cr;
+        s_ab[t] = a2 * (1.f / 128.f);
+        s_db[t] = kd;
+      }
+    }
+    __syncthreads();
+    if (i == 0) {   // the chunk's variances forward, then the chain backwards
+      float bv = c == 0 ? (a.aux0 ? a.aux0[bh] : 1.f)
+                        : reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rP0PC)[0];
+      for (int t = 0; t < Cc; ++t) {
+        s_prev[t] = bv;
+        const float bhat = s_ab[t] * bv + s_om[t];
+        s_bh[t] = bhat;
+        bv = bhat / (1.f + mu * s_s[t] / (128.f * s_r[t]) * bhat);
+      }
+      for (int t = Cc - 1; t >= 0; --t) {
+        const float bhat = s_bh[t], rt = s_r[t], st = s_s[t];
+        const float den = rt + bhat * st, q1 = 1.f + mu * st / (128.f * rt) * bhat;
+        const float iq2 = 1.f / (q1 * q1);
+        const float dbh = s_db[t] * rt / (den * den) + db * iq2;
+        s_du[t] = -db * bhat * bhat * iq2;
+        s_dbh[t] = dbh;
+        db = s_ab[t] * dbh;
+      }
+    }
+    __syncthreads();
+    for (int tt = 0; tt < 16; ++tt) {   // per (token, channel), warp w: tokens 16 w .. + 15
+      const int t = 16 * warp + tt;
+      if (t >= Cc) break;
+      const float bhat = s_bh[t], rt = s_r[t], st = s_s[t], dbt = s_db[t], du = s_du[t];
+      const float den = rt + bhat * st;
+      const float ds = -dbt * bhat * bhat / (den * den) + du * mu / (128.f * rt);
+      const long tt_ = tok(a, b, t0 + t, h);
+      if (lane == 0) {
+        g.domega[tt_] = s_dbh[t];
+        g.dr[tt_] = -dbt * bhat / (den * den) - du * mu * st / (128.f * rt * rt);
+      }
+      const float fa = 2.f * s_prev[t] * s_dbh[t] / 128.f;
+      float dkh[4], dot = 0.f;
+      float* dkrow = g.dk + tt_ * 128;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int ch = lane + 32 * m;
+        const float kh = sK[t * 128 + ch];
+        dkh[m] = dkrow[ch] + (bhat / den) * sDW[t * 128 + ch] + 2.f * ds * kh;
+        dot += kh * dkh[m];
+        g.dla[tt_ * 128 + ch] += fa * sA[t * 128 + ch];
+      }
+      dot = warp_sum(dot);
+      const float cr = s_cr[t];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int ch = lane + 32 * m;
+        dkrow[ch] = a.k_l2norm ? (dkh[m] - sK[t * 128 + ch] * dot) * cr : dkh[m];
+      }
+    }
+  }
+  if (i == 0 && g.daux0) g.daux0[bh] = db;
+}
+
 // dL/dmu_h: the rows' parts summed over the batch in order
 __global__ void pgdn_dmu_kernel(FwdArgs a, BwdArgs g) {
   const int h = blockIdx.x * blockDim.x + threadIdx.x;
@@ -1474,7 +1650,7 @@ __global__ void pgdn_dmu_kernel(FwdArgs a, BwdArgs g) {
 
 bool chunk_bwd_supported(int variant, int dtype, int dk, int dv, int chunk) {
   return (variant == DR_GDN || variant == DR_KLA || variant == DR_PGDN || variant == DR_KDA ||
-          variant == DR_KDN) &&
+          variant == DR_KDN || variant == DR_PKDA || variant == DR_IKDN) &&
          dtype == DR_BF16 && dk == 128 && dv == 128 && chunk == 64;
 }
 
@@ -1526,8 +1702,20 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
       (e = cudaFuncSetAttribute(bwd_local_kernel<DR_PGDN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l_smem)) !=
           cudaSuccess ||
-      (e = cudaFuncSetAttribute(pgdn_gain_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)p_smem)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(pgdn_gain_bwd_kernel<false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p_smem)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(pgdn_gain_bwd_kernel<true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p_smem)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(bwd_local_pc_kernel<DR_PKDA>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kPcLocalSmem)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(bwd_local_pc_kernel<DR_IKDN>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kPcLocalSmem)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(ikdn_gain_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kIkdnGainSmemF * 4)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(bwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)s_smem)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(bwd_local_kernel<DR_GDN>,
@@ -1549,11 +1737,18 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
   } else if (fa.variant == DR_KDN) {
     bwd_local_pc_kernel<DR_KDN><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
     kdn_gain_bwd_kernel<<<fa.B * fa.H, 128, kKdnGainSmemF * 4, st>>>(fa, g);
+  } else if (fa.variant == DR_PKDA) {
+    bwd_local_pc_kernel<DR_PKDA><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
+    pgdn_gain_bwd_kernel<true><<<fa.B * fa.H, 128, p_smem, st>>>(fa, g);
+    pgdn_dmu_kernel<<<(fa.H + 127) / 128, 128, 0, st>>>(fa, g);
+  } else if (fa.variant == DR_IKDN) {
+    bwd_local_pc_kernel<DR_IKDN><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
+    ikdn_gain_bwd_kernel<<<fa.B * fa.H, 128, kIkdnGainSmemF * 4, st>>>(fa, g);
   } else if (fa.variant == DR_KLA) {
     bwd_local_kernel<DR_KLA><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
   } else if (pg) {
     bwd_local_kernel<DR_PGDN><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
-    pgdn_gain_bwd_kernel<<<fa.B * fa.H, 128, p_smem, st>>>(fa, g);
+    pgdn_gain_bwd_kernel<false><<<fa.B * fa.H, 128, p_smem, st>>>(fa, g);
     pgdn_dmu_kernel<<<(fa.H + 127) / 128, 128, 0, st>>>(fa, g);
   } else {
     bwd_local_kernel<DR_GDN><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);

@@ -1687,9 +1687,11 @@ cudaError_t launch_kdn_split(const FwdArgs& a, int dtype, void* workspace, cudaS
   // KDA has no gain state across chunks: neither the chain nor the map and scan.
   // PKDA (key statistic) and isotropic KDN (one variance per head) chain theirs
   // the same way; with few rows they run the fused kernel instead.
+  // The backward's rerun of the forward (a.save_S set) needs the two phases and
+  // their records whatever the row count, so PKDA and isotropic KDN chain then.
   const bool kdn = a.variant == DR_KDN;
   const bool chain_only = a.variant == DR_PKDA || a.variant == DR_IKDN;
-  const bool chained = (kdn || chain_only) && 3L * a.B * a.H >= nsm;
+  const bool chained = (kdn || chain_only) && (3L * a.B * a.H >= nsm || (chain_only && a.save_S));
   if (chain_only && !chained) return launch_chunk_simt(a, dtype, st);
   uint32_t* chain = chained ? reinterpret_cast<uint32_t*>(ws + (size_t)ntask * kRecK) : nullptr;
   cudaError_t err = cudaSuccess;

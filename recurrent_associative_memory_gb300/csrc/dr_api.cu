@@ -236,7 +236,8 @@ int dr_chunk_bwd(const void* q, const void* k, const void* v, const float* log_a
   if (!gp || !g || !q || !k || !v || !log_alpha || !d_out || !g->dq || !g->dk || !g->dv ||
       !g->d_log_alpha)
     return DR_ERR_NULL;
-  if (variant == DR_KDN ? (!g->d_omega || !g->d_r) : !g->d_eta) return DR_ERR_NULL;
+  const bool kalman = variant == DR_KDN || variant == DR_IKDN;   // gains from a variance
+  if (kalman ? (!g->d_omega || !g->d_r) : !g->d_eta) return DR_ERR_NULL;
   if (gp->dtype != DR_FP32 && gp->dtype != DR_BF16) return DR_ERR_DTYPE;
   if (B < 1 || T < 1 || H < 1 || !dim_ok(dk_) || !dim_ok(dv_)) return DR_ERR_SHAPE;
   if (chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128) return DR_ERR_SHAPE;
@@ -245,7 +246,8 @@ int dr_chunk_bwd(const void* q, const void* k, const void* v, const float* log_a
   int st = check_gates(gp, variant);
   if (st != DR_OK) return st;
   if (!chunk_bwd_supported(variant, gp->dtype, dk_, dv_, chunk)) return DR_ERR_UNSUPPORTED;
-  if (variant == DR_PGDN && (!g->d_alphaP || !g->d_betaP || !g->d_mu)) return DR_ERR_NULL;
+  if ((variant == DR_PGDN || variant == DR_PKDA) && (!g->d_alphaP || !g->d_betaP || !g->d_mu))
+    return DR_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
       !aligned16(d_out) || !aligned16(d_final_state) || !aligned16(g->dq) || !aligned16(g->dk) ||
       !aligned16(g->dv) || !aligned16(init_state) || !aligned16(g->d_init_state))

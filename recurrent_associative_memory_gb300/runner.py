@@ -101,9 +101,9 @@ def chunk_bwd(inp: dict, d_out, *, d_final_state=None, init_state=None, aux_init
               d_aux_final=None, want_dS0=True, chunk=None, stream=None, workspace="auto",
               grads=None):
     """Run dr_chunk_bwd on a device input dict; returns a dict of fp32 gradients
-    (dq, dk, dv, dlog_alpha, deta, with want_dS0 dS0, and for PGDN dalphaP,
-    dbetaP, dmu, daux0; Diagonal KDN domega, dr, daux0 and no deta).  With
-    per-channel decay (KDA, KDN) dlog_alpha is [B,T,H,dk].  ``grads`` may hold
+    (dq, dk, dv, dlog_alpha, deta, with want_dS0 dS0, and for PGDN / PKDA dalphaP,
+    dbetaP, dmu, daux0; Diagonal / isotropic KDN domega, dr, daux0 and no deta).
+    With per-channel decay (KDA, PKDA, KDN, isotropic KDN) dlog_alpha is [B,T,H,dk].  ``grads`` may hold
     preallocated output tensors under the same names."""
     q, k, v = inp["q"], inp["k"], inp["v"]
     B, T, H, dk = k.shape
@@ -117,11 +117,11 @@ def chunk_bwd(inp: dict, d_out, *, d_final_state=None, init_state=None, aux_init
     g.setdefault("dv", torch.empty(B, T, H, dv, **f32))
     per_channel = inp["variant"] in ("kda", "kdn", "pkda", "ikdn")
     g.setdefault("dlog_alpha", torch.empty(*((B, T, H, dk) if per_channel else (B, T, H)), **f32))
-    if inp["variant"] != "kdn":
+    if inp["variant"] not in ("kdn", "ikdn"):
         g.setdefault("deta", torch.empty(B, T, H, **f32))
     if want_dS0:
         g.setdefault("dS0", torch.empty(B, H, dk, dv, **f32))
-    if inp["variant"] == "pgdn":
+    if inp["variant"] in ("pgdn", "pkda"):
         g.setdefault("dalphaP", torch.empty(B, T, H, **f32))
         g.setdefault("dbetaP", torch.empty(B, T, H, **f32))
         g.setdefault("dmu", torch.empty(H, **f32))
@@ -130,6 +130,10 @@ def chunk_bwd(inp: dict, d_out, *, d_final_state=None, init_state=None, aux_init
         g.setdefault("domega", torch.empty(B, T, H, dk, **f32))
         g.setdefault("dr", torch.empty(B, T, H, **f32))
         g.setdefault("daux0", torch.empty(B, H, dk, **f32))
+    if inp["variant"] == "ikdn":   # one variance per head: omega per token
+        g.setdefault("domega", torch.empty(B, T, H, **f32))
+        g.setdefault("dr", torch.empty(B, T, H, **f32))
+        g.setdefault("daux0", torch.empty(B, H, **f32))
     p = params_for(inp, aux_init=aux_init)
     if workspace is not None:
         p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()

@@ -198,7 +198,8 @@ def test_backward_refusals_and_workspace_size(dr):
     assert call(variant=dr.DR_KDN, params=kp) == dr.DR_ERR_NULL        # no d omega, d r
     assert call(variant=dr.DR_KDN, params=kp, d_eta=None, d_omega=A, d_r=A) == dr.DR_ERR_WORKSPACE
     assert call(variant=dr.DR_PKDA, params=dr.make_params(dtype=dr.DR_BF16, eta=A, alphaP=A,
-                                                           betaP=A, mu=A)) == dr.DR_ERR_UNSUPPORTED
+                                                           betaP=A, mu=A)) == dr.DR_ERR_NULL
+    assert call(variant=dr.DR_EKDN, params=kp) == dr.DR_ERR_UNSUPPORTED   # no chunkwise form
     assert call(d=64) == dr.DR_ERR_UNSUPPORTED
     assert call(chunk=32) == dr.DR_ERR_UNSUPPORTED
     assert call(params=dr.make_params(dtype=dr.DR_FP32, eta=A)) == dr.DR_ERR_UNSUPPORTED
@@ -222,10 +223,12 @@ def test_backward_refusals_and_workspace_size(dr):
                       + al(n * 32768))
     assert call(ws=(A, 1000)) == dr.DR_ERR_WORKSPACE
     assert call(ws=(A + 16, 1 << 30)) == dr.DR_ERR_ALIGN
-    # Diagonal KDN: as KDA plus dL/dw
+    # Diagonal KDN, PKDA, isotropic KDN: as KDA plus dL/dw and 4 B per row
     need_k = dr.dr_chunk_bwd_workspace_bytes(dr.DR_KDN, dr.DR_BF16, 2, 130, 3, 128, 128, 64)
-    assert need_k == need_a + al(n * 32768)
-    assert dr.dr_chunk_bwd_workspace_bytes(dr.DR_PKDA, dr.DR_BF16, 1, 64, 1, 128, 128, 64) == 0
+    assert need_k == need_a + al(n * 32768) + al(4 * rows)
+    for vid in (dr.DR_PKDA, dr.DR_IKDN):   # the same layout (with PKDA's rows' dL/dmu parts)
+        assert dr.dr_chunk_bwd_workspace_bytes(vid, dr.DR_BF16, 2, 130, 3, 128, 128, 64) == need_k
+    assert dr.dr_chunk_bwd_workspace_bytes(dr.DR_EKDN, dr.DR_BF16, 1, 64, 1, 128, 128, 64) == 0
 
 
 def test_grads_struct_layout_matches_c(dr):

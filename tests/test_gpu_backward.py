@@ -46,9 +46,9 @@ def oracle_grads(inp, dO, dS, S0, aux0=None, daux=None):
                                log_floor=inp.get("log_floor", 1e-12), omega=f(inp.get("omega")),
                                r=f(inp.get("r")), info_scale=inp.get("info_scale", 1.0),
                                aux0=f(aux0), daux_T=f(daux))
-    if inp["variant"] == "kdn":
+    if inp["variant"] in ("kdn", "ikdn"):
         return {n: g[n] for n in KDN_NAMES}
-    names = NAMES + (PG_NAMES if inp["variant"] == "pgdn" else ())
+    names = NAMES + (PG_NAMES if inp["variant"] in ("pgdn", "pkda") else ())
     return {n: g[n] for n in names}
 
 
@@ -309,6 +309,79 @@ def test_kdn_backward_workload_sampled(rt):
     ref = oracle_grads(sub, dO_s, None, None)
     for n in ("dS0", "daux0"):
         ref.pop(n)
+    errs = {}
+    for n, r in ref.items():
+        x = torch.stack([g[n][b, :, h] for b, h in pairs])[:, :, None]
+        errs[n] = rel_err(np64(x), r)
+    assert all(e <= TOL["bf16"] for e in errs.values()), errs
+
+
+# ------------------------------------------------------------ PKDA, isotropic KDN
+
+@pytest.mark.parametrize("T,norms", [(200, True), (333, False), (64, True)])
+def test_pkda_backward_matches_oracle(rt, T, norms):
+    """PKDA: KDA's chunk part with the PGDN write keys, then the key statistic's
+    adjoint (d beta, d alphaP, d betaP, d mu, dL/dA_0); nonzero A_0 and dL/dA_T."""
+    dr, runner = rt
+    wl = W.small("pkda_bf16", B=2, T=T, H=3, seed=130 + T, k_l2norm=norms)
+    inp = W.generate(wl, "pkda")
+    B, H = 2, 3
+    gen = torch.Generator().manual_seed(T)
+    dO = torch.randn(B, T, H, 128, generator=gen).to(torch.bfloat16)
+    dS = 0.1 * torch.randn(B, H, 128, 128, generator=gen)
+    S0 = 0.3 * torch.randn(B, H, 128, 128, generator=gen)
+    A0 = torch.rand(B, H, 128, generator=gen) * 2.0
+    dA = 0.1 * torch.randn(B, H, 128, generator=gen)
+    g = runner.chunk_bwd(runner.to_device(inp), dO.cuda(), d_final_state=dS.cuda(),
+                         init_state=S0.cuda(), aux_init=A0.cuda(), d_aux_final=dA.cuda())
+    torch.cuda.synchronize()
+    assert dr.dr_get_device_status() == 0
+    check(g, oracle_grads(inp, dO, dS, S0, aux0=A0, daux=dA))
+
+
+@pytest.mark.parametrize("T,norms", [(200, True), (333, False), (1, True)])
+def test_ikdn_backward_matches_oracle(rt, T, norms):
+    """Isotropic KDN: the chunk part with w = beta k^, then the head variance's
+    scalar adjoint (d omega and d r per token, d log alpha through the mean squared
+    decay, the key gradient through beta and ||k^||^2, dL/db_0)."""
+    wl = W.small("ikdn_bf16", B=2, T=T, H=3, seed=150 + T, k_l2norm=norms)
+    inp = W.generate(wl, "ikdn")
+    dr, runner = rt
+    B, H = 2, 3
+    gen = torch.Generator().manual_seed(T)
+    dO = torch.randn(B, T, H, 128, generator=gen).to(torch.bfloat16)
+    dS = 0.1 * torch.randn(B, H, 128, 128, generator=gen)
+    S0 = 0.3 * torch.randn(B, H, 128, 128, generator=gen)
+    b0 = 0.5 + torch.rand(B, H, generator=gen)
+    db = 0.1 * torch.randn(B, H, generator=gen)
+    g = runner.chunk_bwd(runner.to_device(inp), dO.cuda(), d_final_state=dS.cuda(),
+                         init_state=S0.cuda(), aux_init=b0.cuda(), d_aux_final=db.cuda())
+    torch.cuda.synchronize()
+    assert dr.dr_get_device_status() == 0
+    check(g, oracle_grads(inp, dO, dS, S0, aux0=b0, daux=db))
+
+
+@pytest.mark.parametrize("variant", ["pkda", "ikdn"])
+def test_gain_variants_backward_many_rows_chained_shape(rt, variant):
+    """Enough rows for the forward's chained hand-over of the gain state."""
+    dr, runner = rt
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    H = -(-nsm // 6)
+    wl = W.small(f"{variant}_bf16", B=2, T=150, H=H, seed=17)
+    inp = W.generate(wl, variant)
+    gen = torch.Generator().manual_seed(2)
+    dO = torch.randn(2, 150, H, 128, generator=gen).to(torch.bfloat16)
+    g = runner.chunk_bwd(runner.to_device(inp), dO.cuda())
+    torch.cuda.synchronize()
+    assert dr.dr_get_device_status() == 0
+    pairs = [(0, H - 1), (1, H - 1)]   # one head: the slice keeps PKDA's mu per head
+    sub = slice_heads(inp, pairs)
+    if variant == "pkda":
+        sub["mu"] = sub["mu"][:1]
+    dO_s = torch.stack([dO[b, :, h] for b, h in pairs])[:, :, None]
+    ref = oracle_grads(sub, dO_s, None, None)
+    for n in ("dS0", "daux0", "dmu"):
+        ref.pop(n, None)
     errs = {}
     for n, r in ref.items():
         x = torch.stack([g[n][b, :, h] for b, h in pairs])[:, :, None]
