@@ -70,6 +70,11 @@ L2_FLUSH_BYTES = 256 << 20
 # case, GDN vs KLA, PGDN, Diagonal KDN, the long-context prefill, then decode.
 CONFIG_WORKLOADS = [("0", "kla_fp32_small"), ("1", "gdn_kla_bf16"), ("2", "pgdn_bf16"),
                     ("3", "kdn_bf16"), ("4a", "kla_prefill_bf16"), ("4b", "kla_decode_bf16")]
+# the per-channel-decay and exact-Kalman rows beyond the configurations: forward
+# (and, where it exists, backward) timed on their own workloads with oracle parity
+NEXT_WORKLOADS = [("kda", "kda_bf16"), ("pkda", "pkda_bf16"), ("ikdn", "ikdn_bf16"),
+                  ("ekdn", "ekdn_bf16")]
+BWD_VARIANTS = ("gdn", "kla", "pgdn", "kda", "kdn", "pkda", "ikdn")
 # decode-step variants timed besides the headline KLA step, on their own workloads' flags
 DECODE_VARIANTS = {"gdn": "gdn_kla_bf16", "pgdn": "pgdn_bf16", "kdn": "kdn_bf16",
                    "kda": "kda_bf16", "pkda": "pkda_bf16", "ikdn": "ikdn_bf16",
@@ -89,6 +94,8 @@ def parse(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-configs", action="store_true")
     p.add_argument("--no-backward", action="store_true")
+    p.add_argument("--no-next", action="store_true",
+                   help="skip the KDA / PKDA / isotropic KDN / exact Kalman rows")
     p.add_argument("--cpu-sample-heads", type=int, default=8)
     p.add_argument("--cpu-sample-reps", type=int, default=10)
     return p.parse_args(argv)
@@ -176,25 +183,30 @@ def fwd_bytes(wl, variant, with_final=True):
 
 def bwd_bytes(wl, variant="kla"):
     """Bytes one backward call must move: q, k, v and dL/do in (the input dtype) and
-    the gates; dq, dk, dv (fp32) and the gates' gradients out; the initial state
-    and dL/dS_T in, dL/dS_0 out (PGDN: also mu, A_0 and dL/dA_T in, dL/dmu and
-    dL/dA_0 out)."""
+    the gates; dq, dk, dv (fp32) and the gates' gradients out (the same sizes as
+    the gates: per-channel decay gives d log alpha per channel); the initial state
+    and dL/dS_T in, dL/dS_0 out; the gain state's initial value and dL/d(final) in
+    and its gradient out (PGDN / PKDA: also mu in and dL/dmu out)."""
     el = 2 if wl.dtype == "bf16" else 4
     ht = wl.B * wl.T * wl.H
     gates = gate_bytes(variant, wl.dk)
     per_ht = (2 * wl.dk + 2 * wl.dv) * el + gates + (2 * wl.dk + wl.dv) * 4 + gates
     total = ht * per_ht + 3 * wl.B * wl.H * wl.dk * wl.dv * 4
-    if variant == "pgdn":
-        total += 2 * wl.H * 4 + 3 * wl.B * wl.H * wl.dk * 4
+    total += 3 * wl.B * wl.H * aux_elems(variant, wl.dk) * 4
+    if variant in ("pgdn", "pkda"):
+        total += 2 * wl.H * 4
     return total
 
 
-def bwd_kernels_per_call(variant):
+def bwd_kernels_per_call(variant, B=1, H=1, nsm=152):
     """libdr kernels one dr_chunk_bwd call launches: the forward again (prep and
-    carry; PGDN also its statistic's map and scan), the reverse carry, the state
-    products, the local gradients (PGDN also its statistic's adjoint and the
-    d mu sum)."""
-    return 9 if variant == "pgdn" else 5
+    carry; PGDN also its statistic's map and scan; Diagonal KDN with few rows,
+    3 B H < SMs, its variance map and scan), the reverse carry, the state
+    products, the local gradients, then the gain's adjoint (PGDN / PKDA: and the
+    d mu sum; Diagonal / isotropic KDN: one kernel)."""
+    fwd = {"pgdn": 4, "kdn": 2 if 3 * B * H >= nsm else 4}.get(variant, 2)
+    gain = {"pgdn": 2, "pkda": 2, "kdn": 1, "ikdn": 1}.get(variant, 0)
+    return fwd + 3 + gain
 
 
 def decode_bytes(wl, variant="kla"):
@@ -347,14 +359,18 @@ def _oracle_bwd_parity(job):
     tag, inp, variant, dO, dS, S0 = job
     f = lambda t: None if t is None else np.asarray(t, dtype=np.float64)  # noqa: E731
     g = obw.tokenwise_backward(f(inp["q"]), f(inp["k"]), f(inp["v"]), f(inp["log_alpha"]),
-                               variant, f(dO), f(dS), eta=f(inp["eta"]), eps=inp["eps"],
+                               variant, f(dO), f(dS), eta=f(inp.get("eta")), eps=inp["eps"],
                                q_l2norm=inp["q_l2norm"], k_l2norm=inp["k_l2norm"], S0=f(S0),
                                alphaP=f(inp.get("alphaP")), betaP=f(inp.get("betaP")),
                                mu=f(inp.get("mu")), x=inp.get("x", 1.5),
-                               log_floor=inp.get("log_floor", 1e-12))
-    names = ("dq", "dk", "dv", "dlog_alpha", "deta", "dS0")
-    if variant == "pgdn":
-        names += ("dalphaP", "dbetaP")
+                               log_floor=inp.get("log_floor", 1e-12), omega=f(inp.get("omega")),
+                               r=f(inp.get("r")), info_scale=inp.get("info_scale", 1.0))
+    if variant in ("kdn", "ikdn"):
+        names = ("dq", "dk", "dv", "dlog_alpha", "dS0", "domega", "dr")
+    else:
+        names = ("dq", "dk", "dv", "dlog_alpha", "deta", "dS0")
+        if variant in ("pgdn", "pkda"):
+            names += ("dalphaP", "dbetaP")
     return tag, {k: g[k] for k in names}
 
 
@@ -616,6 +632,13 @@ def forward_entry(fw, var_ms, pk, launches):
 BWD_GRADS = ("dq", "dk", "dv", "dlog_alpha", "deta", "dS0")
 
 
+def bwd_grad_names(variant):
+    """The gradients the bench checks per variant (per token or per row)."""
+    if variant in ("kdn", "ikdn"):
+        return ("dq", "dk", "dv", "dlog_alpha", "dS0", "domega", "dr")
+    return BWD_GRADS + (("dalphaP", "dbetaP") if variant in ("pgdn", "pkda") else ())
+
+
 def time_backward(torch, dr, runner, fw, steps, stream, flush, pk, pool_submit, n_pairs=2):
     """dr_chunk_bwd on a forward workload's inputs (every variant it lists that the
     backward supports): CUDA-event time per call, L2 flushed between calls; oracle
@@ -629,7 +652,7 @@ def time_backward(torch, dr, runner, fw, steps, stream, flush, pk, pool_submit, 
     entry, rows = {"workload": wl.name, "variants": {}}, {}
     pairs = sampled_pairs(wl.B, wl.H, n_pairs)
     for v in fw.variants:
-        ws = runner.bwd_workspace_for(fw.dev[v])
+        ws = runner.bwd_workspace_for(fw.dev[v]) if v in BWD_VARIANTS else None
         if ws is None:
             continue
         grads = runner.chunk_bwd(fw.dev[v], dOd, d_final_state=dSd, init_state=S0d,
@@ -651,11 +674,12 @@ def time_backward(torch, dr, runner, fw, steps, stream, flush, pk, pool_submit, 
         dr.check(dr.dr_get_device_status(), "backward")
         ms = statistics.mean(s_.elapsed_time(e_) for s_, e_ in ev)
         byt = bwd_bytes(wl, v)
+        nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
         entry["variants"][v] = {"ms": ms, "tokens_per_s": wl.B * wl.T / (ms / 1e3),
                                 "algorithmic_bytes": byt, "gbs": byt / (ms / 1e3) / 1e9,
                                 "frac": byt / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
-                                "launches_per_call": bwd_kernels_per_call(v)}
-        names = BWD_GRADS + (("dalphaP", "dbetaP") if v == "pgdn" else ())
+                                "launches_per_call": bwd_kernels_per_call(v, wl.B, wl.H, nsm)}
+        names = bwd_grad_names(v)
         for b, h in pairs:
             rows[(wl.name, v, b, h)] = {n: (grads[n][b, h] if n == "dS0" else grads[n][b, :, h])
                                         .double().cpu().numpy() for n in names}
@@ -841,7 +865,8 @@ def main(argv=None):
             vms, _ = fw.time(min(args.steps, 20), 3, stream, flush)
             configs[tag] = forward_entry(fw, vms, pk, fw.launches_per_step(nsm))
             configs[tag]["_fw"] = fw
-            if not args.no_backward and "pgdn" in fw.variants:   # PGDN's backward too
+            if not args.no_backward and ("pgdn" in fw.variants or "kdn" in fw.variants):
+                # PGDN's and Diagonal KDN's backward too
                 bent, rows_ = time_backward(torch, dr, runner, fw, min(args.steps, 10), stream,
                                             flush, pk, submit_bwd, n_pairs=1)
                 if bent["variants"]:
@@ -849,6 +874,26 @@ def main(argv=None):
                     bwd_rows.update(rows_)
                 torch.cuda.empty_cache()
             # keep only what the parity check reads; free the rest of the device memory
+            fw.dev = fw.ws = None
+            torch.cuda.empty_cache()
+
+    # ---------------- the rows beyond the configurations (KDA, PKDA, isotropic KDN,
+    #                  exact Kalman): forward, and the backward where it exists
+    next_rows = {}
+    if not args.no_configs and not args.no_next:
+        for tag, name in NEXT_WORKLOADS:
+            fw = Forward(torch, dr, runner, W, W.WORKLOADS[name])
+            submit(fw.parity_jobs(1))
+            vms, _ = fw.time(min(args.steps, 10), 3, stream, flush)
+            next_rows[tag] = forward_entry(fw, vms, pk, fw.launches_per_step(nsm))
+            next_rows[tag]["_fw"] = fw
+            if not args.no_backward and any(v in BWD_VARIANTS for v in fw.variants):
+                bent, rows_ = time_backward(torch, dr, runner, fw, min(args.steps, 10), stream,
+                                            flush, pk, submit_bwd, n_pairs=1)
+                if bent["variants"]:
+                    bwd_entries[bent["workload"]] = bent
+                    bwd_rows.update(rows_)
+                torch.cuda.empty_cache()
             fw.dev = fw.ws = None
             torch.cuda.empty_cache()
 
@@ -955,6 +1000,11 @@ def main(argv=None):
                 c["parity_sample"] = (f"{len(sampled_pairs(fw.wl.B, fw.wl.H, 2))} (b, h) rows "
                                       "per variant" if fw.wl.T <= 16384 else
                                       "1 (b, h) row")
+        for tag, c in next_rows.items():
+            fw = c.pop("_fw", None)
+            if fw is not None:
+                c["parity"] = fw.parity(results)
+                c["parity_sample"] = "1 (b, h) row"
         if dec_parity is not None:
             worst = {"out": 0.0, "state": 0.0}
             for (name, v, b, h), o, S, _ in results:
@@ -970,12 +1020,17 @@ def main(argv=None):
         for a_ in bwd_async:
             for tag, ref in a_.get():
                 gpu = bwd_rows[tag]
+                ent = bwd_entries[tag[0]].setdefault("parity", {})
                 for n, r_ in ref.items():
                     r = r_[0, 0] if n == "dS0" else r_[0, :, 0]
-                    worst[n] = max(worst.get(n, 0.0), rel_err(gpu[n], r))
+                    e = rel_err(gpu[n], r)
+                    worst[n] = max(worst.get(n, 0.0), e)
+                    ent[n] = max(ent.get(n, 0.0), e)
         result["backward"]["parity"] = worst
-    for c in configs.values():
+    for c in list(configs.values()) + list(next_rows.values()):
         c.pop("_fw", None)
+    if next_rows:
+        result["next_rows"] = next_rows
     if configs:
         result["configs"] = configs
         result["parity_bar"] = {"bf16": 5e-3, "fp32": 1e-4,

@@ -203,3 +203,26 @@ def test_backward_bytes_pgdn_and_kernel_counts():
     per_bh = 3 * 128 * 128 * 4 + 3 * 128 * 4
     assert bench.bwd_bytes(wl, "pgdn") == ht * 2592 + wl.B * wl.H * per_bh + 2 * wl.H * 4
     assert bench.bwd_kernels_per_call("kla") == 5 and bench.bwd_kernels_per_call("pgdn") == 9
+
+
+def test_backward_bytes_and_kernel_counts_per_channel_decay():
+    """Per-channel decay: d log alpha per channel (512 bytes in, 512 out); Diagonal
+    KDN also omega per channel and r in, their gradients out, and p_0, dL/dp_T in,
+    dL/dp_0 out; isotropic KDN one variance per head.  Kernels: the forward again
+    (prep and carry; Diagonal KDN with few rows also its variance map and scan),
+    the reverse carry, the state products, the local gradients, the gain's adjoint."""
+    ht = lambda wl: wl.B * wl.T * wl.H  # noqa: E731
+    S3 = lambda wl: 3 * wl.B * wl.H * 128 * 128 * 4  # noqa: E731
+    kda, kdn, ikdn = (W.WORKLOADS[n] for n in ("kda_bf16", "kdn_bf16", "ikdn_bf16"))
+    base = 1024 + 1536
+    assert bench.bwd_bytes(kda, "kda") == ht(kda) * (base + 2 * 516) + S3(kda)
+    assert bench.bwd_bytes(kdn, "kdn") == (ht(kdn) * (base + 2 * 1028) + S3(kdn)
+                                           + 3 * kdn.B * kdn.H * 128 * 4)
+    assert bench.bwd_bytes(ikdn, "ikdn") == (ht(ikdn) * (base + 2 * 520) + S3(ikdn)
+                                             + 3 * ikdn.B * ikdn.H * 4)
+    k = bench.bwd_kernels_per_call
+    assert k("kda", 4, 16) == 5 and k("ikdn", 4, 16) == 6 and k("pkda", 4, 16) == 7
+    assert k("kdn", 4, 16, 152) == 6 and k("kdn", 1, 2, 152) == 8
+    assert set(bench.bwd_grad_names("kdn")) == {"dq", "dk", "dv", "dlog_alpha", "dS0", "domega",
+                                                 "dr"}
+    assert "dalphaP" in bench.bwd_grad_names("pkda") and "deta" in bench.bwd_grad_names("kda")
