@@ -960,7 +960,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // in the gradient arrays (bwd_state left X_Q = dO S_c^T, X_K = dR S_c^T there).
 // KDA's gain (w = eta k^): d eta = dw . k^, dk^ += eta dw, then the L2 norms;
 // Diagonal KDN, PKDA and isotropic KDN keep dw and dk^ for their gain kernels.
-constexpr int kPcLocalSmem = (4 * 64 * cLDK + 2 * 64 * cLDM + 2 * 16 * cLDK) * 4 + 2 * 64 * 128 * 2;
+constexpr int cKRS = 136;   // raw k, q rows (bf16): 272 bytes, 4 banks apart
+constexpr int kPcLocalSmem = (4 * 64 * cLDK + 2 * 64 * cLDM + 2 * 16 * cLDK) * 4 + 2 * 64 * cKRS * 2;
 
 template <int VARIANT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -976,8 +977,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   float* sAq = sWt + 64 * cLDK;      // q~ of block row I [16][c]
   float* sAk = sAq + 16 * cLDK;      // k~
   float* sDW = sAk + 16 * cLDK;      // dw, Gram part [j][c]
-  uint16_t* sKr = reinterpret_cast<uint16_t*>(sDW + 64 * cLDK);   // raw k, q (bf16) [j][128]
-  uint16_t* sQr = sKr + 64 * 128;
+  uint16_t* sKr = reinterpret_cast<uint16_t*>(sDW + 64 * cLDK);   // raw k, q (bf16) [j][cKRS]
+  uint16_t* sQr = sKr + 64 * cKRS;
   __shared__ float s_cr[64], s_qn[64], s_eta[64];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -994,9 +995,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
     const bool live = j < Cc;
     const long o = tok(a, b, t0 + (live ? j : 0), h) * 128 + c0;
-    *reinterpret_cast<uint4*>(sKr + j * 128 + c0) =
+    *reinterpret_cast<uint4*>(sKr + j * cKRS + c0) =
         live ? *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.k) + o) : make_uint4(0u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(sQr + j * 128 + c0) =
+    *reinterpret_cast<uint4*>(sQr + j * cKRS + c0) =
         live ? *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + o) : make_uint4(0u, 0u, 0u, 0u);
   }
   for (int e = tid; e < 64 * 32; e += kBwdThreads) {
@@ -1018,7 +1019,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int j = tid >> 2, part = tid & 3;
     float kk = 0.f, qq = 0.f;
     for (int c0 = 32 * part; c0 < 32 * part + 32; ++c0) {
-      const float x = bf(sKr[j * 128 + c0]), y = bf(sQr[j * 128 + c0]);
+      const float x = bf(sKr[j * cKRS + c0]), y = bf(sQr[j * cKRS + c0]);
       kk += x * x;
       qq += y * y;
     }
@@ -1050,19 +1051,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int nJ = 16 * (I + 1), m = 16 * I + 7;
     for (int e = tid; e < nJ * 32; e += kBwdThreads) {   // w~ = w e^{g_m(I) - g}, rows j < 16 (I + 1)
       const int j = e >> 5, c4 = 4 * (e & 31);
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        sWt[j * cLDK + c4 + q] =
-            sW[j * cLDK + c4 + q] * __expf(sG[m * cLDK + c4 + q] - sG[j * cLDK + c4 + q]);
+      const float4 w4 = *reinterpret_cast<const float4*>(sW + j * cLDK + c4);
+      const float4 g4 = *reinterpret_cast<const float4*>(sG + j * cLDK + c4);
+      const float4 m4 = *reinterpret_cast<const float4*>(sG + m * cLDK + c4);
+      *reinterpret_cast<float4*>(sWt + j * cLDK + c4) =
+          make_float4(w4.x * __expf(m4.x - g4.x), w4.y * __expf(m4.y - g4.y),
+                      w4.z * __expf(m4.z - g4.z), w4.w * __expf(m4.w - g4.w));
     }
     for (int e = tid; e < 16 * 32; e += kBwdThreads) {   // q~, k~ of the block's rows
       const int r = e >> 5, c4 = 4 * (e & 31), i = 16 * I + r;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float f = __expf(sG[i * cLDK + c4 + q] - sG[m * cLDK + c4 + q]);
-        sAq[r * cLDK + c4 + q] = bf(sQr[i * 128 + c4 + q]) * s_qn[i] * f;
-        sAk[r * cLDK + c4 + q] = bf(sKr[i * 128 + c4 + q]) * s_cr[i] * f;
-      }
+      const float4 g4 = *reinterpret_cast<const float4*>(sG + i * cLDK + c4);
+      const float4 m4 = *reinterpret_cast<const float4*>(sG + m * cLDK + c4);
+      const uint2 kr = *reinterpret_cast<const uint2*>(sKr + i * cKRS + c4);
+      const uint2 qr = *reinterpret_cast<const uint2*>(sQr + i * cKRS + c4);
+      const float f[4] = {__expf(g4.x - m4.x), __expf(g4.y - m4.y), __expf(g4.z - m4.z),
+                          __expf(g4.w - m4.w)};
+      const float kf[4] = {__uint_as_float(kr.x << 16), __uint_as_float(kr.x & 0xFFFF0000u),
+                           __uint_as_float(kr.y << 16), __uint_as_float(kr.y & 0xFFFF0000u)};
+      const float qf[4] = {__uint_as_float(qr.x << 16), __uint_as_float(qr.x & 0xFFFF0000u),
+                           __uint_as_float(qr.y << 16), __uint_as_float(qr.y & 0xFFFF0000u)};
+      const float cr = s_cr[i], qn = s_qn[i];
+      *reinterpret_cast<float4*>(sAq + r * cLDK + c4) =
+          make_float4(qf[0] * qn * f[0], qf[1] * qn * f[1], qf[2] * qn * f[2], qf[3] * qn * f[3]);
+      *reinterpret_cast<float4*>(sAk + r * cLDK + c4) =
+          make_float4(kf[0] * cr * f[0], kf[1] * cr * f[1], kf[2] * cr * f[2], kf[3] * cr * f[3]);
     }
     __syncthreads();
     {   // dq^_P, dk^_L of the block's 16 rows (warp: columns 16 warp .. + 16)
@@ -1084,7 +1096,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float dqp = dq2[nt][e] * sc, dkl = dk2[nt][e] * sc;
             const long o = tok(a, b, t0 + i, h) * 128 + cc;
             const float xq = g.dq[o], xk = g.dk[o];
-            const float qh = bf(sQr[i * 128 + cc]) * s_qn[i], kh = bf(sKr[i * 128 + cc]) * s_cr[i];
+            const float qh = bf(sQr[i * cKRS + cc]) * s_qn[i], kh = bf(sKr[i * cKRS + cc]) * s_cr[i];
             g.dq[o] = dqp + eg * xq;
             g.dk[o] = dkl - eg * xk;
             g.dla[o] = qh * dqp + kh * dkl + eg * (xq * qh - xk * kh);
@@ -1108,48 +1120,85 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
   }
 
-  // ---- rows (four threads per token): dw += e^{G - g} X_W, the column terms of dg,
-  //      the write gain and the norms
-  {
-    const int j = tid >> 2, part = tid & 3;
+  // ---- rows (eight threads per token, 16-byte pieces of the row side by side, two
+  //      passes of 32 tokens): dw += e^{G - g} X_W, the column terms of dg, the write
+  //      gain and the norms
+  for (int pass = 0; pass < 2; ++pass) {
+    const int j = 32 * pass + (tid >> 3), part = tid & 7;
     const bool live = j < Cc;
     const long o = tok(a, b, t0 + (live ? j : 0), h) * 128;
     const float* xw = g.w.XW + (size_t)task * 8192 + j * 128;
     const float cr = s_cr[j], qn = s_qn[j], eta = s_eta[j];
-    float dkh[32], dqh[32], deta = 0.f, dotk = 0.f, dotq = 0.f;
-#pragma unroll 4
-    for (int q = 0; q < 32; ++q) {
-      const int cc = 32 * part + q;
-      const float gj = sG[j * cLDK + cc], ew = __expf(sG[63 * cLDK + cc] - gj);
-      const float w = sW[j * cLDK + cc], x = xw[cc];
-      const float dwg = sDW[j * cLDK + cc], dw = dwg + ew * x;
-      const float kh = bf(sKr[j * 128 + cc]) * cr, qh = bf(sQr[j * 128 + cc]) * qn;
-      dkh[q] = live ? g.dk[o + cc] : 0.f;
-      dqh[q] = live ? g.dq[o + cc] : 0.f;
-      if (kGainK) {
-        g.w.DW[(size_t)task * 8192 + j * 128 + cc] = dw;
-      } else {
-        dkh[q] += eta * dw;
-        deta += kh * dw;
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    float dkh[16], dqh[16], kh[16], qh[16], deta = 0.f, dotk = 0.f, dotq = 0.f;
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+      const int c0 = 4 * part + 32 * k4;
+      const float4 g4 = *reinterpret_cast<const float4*>(sG + j * cLDK + c0);
+      const float4 gC4 = *reinterpret_cast<const float4*>(sG + 63 * cLDK + c0);
+      const float4 w4 = *reinterpret_cast<const float4*>(sW + j * cLDK + c0);
+      const float4 d4 = *reinterpret_cast<const float4*>(sDW + j * cLDK + c0);
+      const float4 x4 = live ? *reinterpret_cast<const float4*>(xw + c0) : z4;
+      const float4 k4v = live ? *reinterpret_cast<const float4*>(g.dk + o + c0) : z4;
+      const float4 q4v = live ? *reinterpret_cast<const float4*>(g.dq + o + c0) : z4;
+      const float4 l4 = live ? *reinterpret_cast<const float4*>(g.dla + o + c0) : z4;
+      const uint2 kr = *reinterpret_cast<const uint2*>(sKr + j * cKRS + c0);
+      const uint2 qr = *reinterpret_cast<const uint2*>(sQr + j * cKRS + c0);
+      const float gg[4] = {g4.x, g4.y, g4.z, g4.w}, gc[4] = {gC4.x, gC4.y, gC4.z, gC4.w};
+      const float ww[4] = {w4.x, w4.y, w4.z, w4.w}, dg4[4] = {d4.x, d4.y, d4.z, d4.w};
+      const float xx[4] = {x4.x, x4.y, x4.z, x4.w}, ll[4] = {l4.x, l4.y, l4.z, l4.w};
+      const float kk[4] = {k4v.x, k4v.y, k4v.z, k4v.w}, qq[4] = {q4v.x, q4v.y, q4v.z, q4v.w};
+      const float kf[4] = {__uint_as_float(kr.x << 16), __uint_as_float(kr.x & 0xFFFF0000u),
+                           __uint_as_float(kr.y << 16), __uint_as_float(kr.y & 0xFFFF0000u)};
+      const float qf[4] = {__uint_as_float(qr.x << 16), __uint_as_float(qr.x & 0xFFFF0000u),
+                           __uint_as_float(qr.y << 16), __uint_as_float(qr.y & 0xFFFF0000u)};
+      float dwo[4], dgo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int q = 4 * k4 + e;
+        const float ew = __expf(gc[e] - gg[e]);
+        const float dw = dg4[e] + ew * xx[e];
+        kh[q] = kf[e] * cr;
+        qh[q] = qf[e] * qn;
+        dkh[q] = kk[e];
+        dqh[q] = qq[e];
+        if (!kGainK) {
+          dkh[q] += eta * dw;
+          deta += kh[q] * dw;
+        }
+        dwo[e] = dw;
+        // the token's whole dg (the Gram's row terms and the state terms came from the
+        // block rows through d log alpha's array); kept here for the sums below
+        dgo[e] = live ? ll[e] - ww[e] * dg4[e] - ww[e] * ew * xx[e] : 0.f;
+        dotk += dkh[q] * kh[q];
+        dotq += dqh[q] * qh[q];
       }
-      if (live) g.dla[o + cc] += -w * dwg - w * ew * x;
-      dotk += dkh[q] * kh;
-      dotq += dqh[q] * qh;
+      if (kGainK)
+        *reinterpret_cast<float4*>(g.w.DW + (size_t)task * 8192 + j * 128 + c0) =
+            make_float4(dwo[0], dwo[1], dwo[2], dwo[3]);
+      *reinterpret_cast<float4*>(sDW + j * cLDK + c0) = make_float4(dgo[0], dgo[1], dgo[2], dgo[3]);
     }
-    deta += __shfl_xor_sync(0xffffffffu, deta, 1);
-    deta += __shfl_xor_sync(0xffffffffu, deta, 2);
-    dotk += __shfl_xor_sync(0xffffffffu, dotk, 1);
-    dotk += __shfl_xor_sync(0xffffffffu, dotk, 2);
-    dotq += __shfl_xor_sync(0xffffffffu, dotq, 1);
-    dotq += __shfl_xor_sync(0xffffffffu, dotq, 2);
+#pragma unroll
+    for (int o2 = 1; o2 < 8; o2 <<= 1) {
+      deta += __shfl_xor_sync(0xffffffffu, deta, o2);
+      dotk += __shfl_xor_sync(0xffffffffu, dotk, o2);
+      dotq += __shfl_xor_sync(0xffffffffu, dotq, o2);
+    }
     if (live) {
-#pragma unroll 4
-      for (int q = 0; q < 32; ++q) {
-        const int cc = 32 * part + q;
-        const float kh = bf(sKr[j * 128 + cc]) * cr, qh = bf(sQr[j * 128 + cc]) * qn;
-        g.dq[o + cc] = a.q_l2norm ? (dqh[q] - qh * dotq) * qn : dqh[q];
-        // Diagonal KDN: dk^ of the memory part stays for kdn_gain_bwd
-        if (!kGainK) g.dk[o + cc] = a.k_l2norm ? (dkh[q] - kh * dotk) * cr : dkh[q];
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const int c0 = 4 * part + 32 * k4;
+        float dq4[4], dk4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int q = 4 * k4 + e;
+          dq4[e] = a.q_l2norm ? (dqh[q] - qh[q] * dotq) * qn : dqh[q];
+          dk4[e] = a.k_l2norm ? (dkh[q] - kh[q] * dotk) * cr : dkh[q];
+        }
+        *reinterpret_cast<float4*>(g.dq + o + c0) = make_float4(dq4[0], dq4[1], dq4[2], dq4[3]);
+        // the gain kernels' variants keep dk^ of the memory part for them
+        if (!kGainK)
+          *reinterpret_cast<float4*>(g.dk + o + c0) = make_float4(dk4[0], dk4[1], dk4[2], dk4[3]);
       }
       if (!kGainK && part == 0) g.deta[tok(a, b, t0 + j, h)] = deta;
     }
@@ -1165,10 +1214,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       dG += sW[j * cLDK + cc] * __expf(gC - sG[j * cLDK + cc]) * xw[j * 128 + cc];
     float acc = 0.f;
     for (int j = Cc - 1; j >= 0; --j) {
-      const long o = tok(a, b, t0 + j, h) * 128 + cc;
-      acc += g.dla[o] + (j == Cc - 1 ? dG : 0.f);
-      g.dla[o] = acc;
+      acc += sDW[j * cLDK + cc] + (j == Cc - 1 ? dG : 0.f);
+      sDW[j * cLDK + cc] = acc;
     }
+  }
+  __syncthreads();
+  for (int e = tid; e < Cc * 32; e += kBwdThreads) {   // d log alpha out (coalesced)
+    const int j = e >> 5, c4 = 4 * (e & 31);
+    *reinterpret_cast<float4*>(g.dla + tok(a, b, t0 + j, h) * 128 + c4) =
+        *reinterpret_cast<const float4*>(sDW + j * cLDK + c4);
   }
 }
 
@@ -1366,7 +1420,7 @@ __global__ void __launch_bounds__(128, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs
   float* sA = sDK + 64 * 128;       // log-decay, then alpha
   float* sPh = sA + 64 * 128;       // omega, then p^
   float* sPo = sPh + 64 * 128;      // p (posterior)
-  __shared__ float s_r[64], s_cr[64], s_den[64], s_cc[64];
+  __shared__ float s_r[64], s_mr[64], s_cr[64], s_den[64], s_cc[64], s_iden[64], s_cd2[64];
   const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
   const int bh = blockIdx.x, b = bh / a.H, h = bh % a.H;
   const int NC = (a.T + 63) / 64;
@@ -1377,7 +1431,10 @@ __global__ void __launch_bounds__(128, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs
     const size_t ri = (size_t)bh * NC + c;
     const int t0 = 64 * c, Cc = min(64, a.T - t0);
     __syncthreads();
-    if (i < 64) s_r[i] = i < Cc ? a.r[tok(a, b, t0 + i, h)] : 1.f;
+    if (i < 64) {
+      s_r[i] = i < Cc ? a.r[tok(a, b, t0 + i, h)] : 1.f;
+      s_mr[i] = mu / s_r[i];
+    }
     for (int e = i; e < 64 * 32; e += 128) {
       const int t = e >> 5, c4 = 4 * (e & 31);
       const bool live = t < Cc;
@@ -1421,9 +1478,9 @@ __global__ void __launch_bounds__(128, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs
       for (int t = 0; t < Cc; ++t) {
         const float kh = sK[t * 128 + i] * s_cr[t];
         sK[t * 128 + i] = kh;
-        const float al = expf(sA[t * 128 + i]);
+        const float al = __expf(sA[t * 128 + i]);
         const float ph = al * al * pv + sPh[t * 128 + i];
-        pv = ph / (1.f + (mu / s_r[t]) * kh * kh * ph);
+        pv = __fdividef(ph, 1.f + s_mr[t] * kh * kh * ph);
         sA[t * 128 + i] = al;
         sPh[t * 128 + i] = ph;
         sPo[t * 128 + i] = pv;
@@ -1444,28 +1501,39 @@ __global__ void __launch_bounds__(128, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs
       z = warp_sum(z);
       cc = warp_sum(cc);
       if (lane == 0) {
-        s_den[t] = s_r[t] + z;
+        const float den = s_r[t] + z;
+        s_den[t] = den;
         s_cc[t] = cc;
+        s_iden[t] = 1.f / den;
+        s_cd2[t] = cc / (den * den);
       }
     }
     __syncthreads();
     // backwards over the chunk's tokens, per channel (the chain through dp)
     for (int t = Cc - 1; t >= 0; --t) {
       const float kh = sK[t * 128 + i], ph = sPh[t * 128 + i], al = sA[t * 128 + i];
-      const float dwv = sDW[t * 128 + i], den = s_den[t], cc = s_cc[t], mr = mu / s_r[t];
+      const float dwv = sDW[t * 128 + i], iden = s_iden[t], cd2 = s_cd2[t], mr = s_mr[t];
       const float q1 = 1.f + mr * kh * kh * ph;
-      const float iq2 = 1.f / (q1 * q1), cd2 = cc / (den * den);
-      const float dph = dwv * kh / den - cd2 * kh * kh + dp * iq2;
+      const float iq2 = __fdividef(1.f, q1 * q1);
+      const float dph = dwv * kh * iden - cd2 * kh * kh + dp * iq2;
       const float du = -dp * ph * ph * iq2;
-      sDK[t * 128 + i] += dwv * ph / den - 2.f * cd2 * ph * kh + 2.f * mr * kh * du;
+      sDK[t * 128 + i] += dwv * ph * iden - 2.f * cd2 * ph * kh + 2.f * mr * kh * du;
       sDW[t * 128 + i] = kh * kh * du;
       const float prev = t > 0 ? sPo[(t - 1) * 128 + i] : p0;
-      const long o = tok(a, b, t0 + t, h) * 128 + i;
-      g.domega[o] = dph;
-      g.dla[o] += 2.f * al * al * prev * dph;
+      sA[t * 128 + i] = dph;                            // d omega
+      sPh[t * 128 + i] = 2.f * al * al * prev * dph;    // d log alpha through alpha^2 p
       dp = al * al * dph;
     }
     __syncthreads();
+    for (int e = i; e < Cc * 32; e += 128) {   // d omega out, d log alpha updated (coalesced)
+      const int t = e >> 5, c4 = 4 * (e & 31);
+      const long o = tok(a, b, t0 + t, h) * 128 + c4;
+      *reinterpret_cast<float4*>(g.domega + o) = *reinterpret_cast<const float4*>(sA + t * 128 + c4);
+      float4 la = *reinterpret_cast<const float4*>(g.dla + o);
+      const float4 x = *reinterpret_cast<const float4*>(sPh + t * 128 + c4);
+      la.x += x.x; la.y += x.y; la.z += x.z; la.w += x.w;
+      *reinterpret_cast<float4*>(g.dla + o) = la;
+    }
     for (int tt = 0; tt < 16; ++tt) {   // d r and the key norm, warp w: tokens 16 w .. + 15
       const int t = 16 * warp + tt;
       if (t >= Cc) break;
