@@ -26,11 +26,11 @@
 // This path serves the fp32 mode (tolerance 1e-4), per-channel decay and the
 // shapes the tensor-core kernels do not take.
 //
-// Two-phase Diagonal KDN (dk = dv = 128, chunk 64, with a workspace): the same
-// kernel in prep mode (PREP = true) does every chunk's local work in parallel and
-// writes a per-chunk record -- bf16 hi/lo tile images for the tcgen05 carry of
-// chunk_tc_split.cu when the inputs are bf16, an fp32 record for kdn_carry_kernel
-// (CUDA cores) when they are fp32.  Only the variance p at the chunk start is
+// Two-phase per-channel decay with fp32 inputs (dk = dv = 128, chunk 64, with a
+// workspace): the same kernel in prep mode (PREP = true) does every chunk's local
+// work in parallel and writes an fp32 per-chunk record for kdn_carry_kernel (CUDA
+// cores); bf16 inputs take chunk_tc_pc.cu's tensor-core prep and the tcgen05
+// carry, with the same chains and variance maps.  Only the variance p at the chunk start is
 // sequential across chunks.  With many (b, h) rows the prep chains it itself:
 // tasks are taken in chunk-major ticket order and each one hands p at its end to
 // the next chunk of its row through the workspace (a release flag; the wait is
@@ -101,18 +101,6 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_b
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
-// 4-byte variant (through L1); src_bytes = 0 zero-fills
-__device__ __forceinline__ void cp_async4(void* dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-               "l"(src), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// waits for the committed groups but the newest (copies issued since stay in flight)
-__device__ __forceinline__ void cp_async_wait_but_newest() {
-  asm volatile("cp.async.wait_group 1;" ::: "memory");
-}
 
 
 // m16n8k16 bf16 mma.sync, fp32 accumulate (the bf16-input Gram's split products)
@@ -143,12 +131,9 @@ constexpr uint32_t rkG = 131072;     // gamma_C [128]
 constexpr uint32_t rkMap = 132096;   // variance chunk map, 4 floats per channel
 constexpr uint32_t rkP0 = 134144;    // variance p at the chunk start [128]
 constexpr uint32_t kRecK = 135168;
-// bf16 inputs: the record is read by the tensor-core carry instead, as bf16 hi/lo
-// 128-byte-swizzled tile images (same offsets as the GDN/KLA records for the
-// shared pieces): T [64][64], W'^T = ((Gamma.K)^T T^T) [128][64], P [64][64],
-// vectors (ones for the e^g qn and u slots, gamma_C per channel at float 128),
-// (Gamma.Q) and (exp(g_C - g_j).w_j) as [64 tok][128] in two 64-column blocks.
-constexpr uint32_t rbT = 0, rbWp = 16384, rbP = 49152, rbVec = 65536, rbQ = 66560, rbW = 99328;
+// (bf16 inputs take the tensor-core prep of chunk_tc_pc.cu, whose records of the
+// same size hold bf16 hi/lo tile images for the tcgen05 carry; the variance map
+// and the chain fields below are shared.)
 
 // PREP = false: the fused forward, one CTA per (b, h, 32 columns), chunks in order.
 // PREP = true (Diagonal KDN, dk = 128): one task per (b, h, chunk), all chunks in
@@ -242,52 +227,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
     __syncthreads();
     it0 = s_ticket;
   }
-  // bf16 prep: the raw K and Q rows of a task (2 x 16 KB, row-major) and its
-  // observation noise are copied into shared memory the previous task no longer
-  // needs (the fp32 Q^T buffer once the Q image is built; the state buffer,
-  // unused in prep mode), and its process noise straight into W (dead once the
-  // Wbar image is built), so their latency hides behind the record copies.  Two
-  // groups: rows and r, then the process noise (waited with the log-decay).
-  constexpr bool kStage = PREP && sizeof(Tin) == 2;
-  auto prefetch_task = [&](long nit) {
-    int nbh, nci;
-    if (chained) {
-      nci = (int)(nit / (a.B * a.H));
-      nbh = (int)(nit % (a.B * a.H));
-    } else {
-      nbh = (int)(nit / NCk);
-      nci = (int)(nit % NCk);
-    }
-    const int nb = nbh / a.H, nh = nbh % a.H, nt0 = nci * CM, nCc = min(CM, a.T - nt0);
-    uint8_t* stg = reinterpret_cast<uint8_t*>(sQt);
-    constexpr int kPieces = 2 * CM * DK * 2 / 16;   // 16-byte pieces of K and Q
-#pragma unroll
-    for (int r = 0; r < kPieces / kThreads; ++r) {
-      const int e = tid + r * kThreads, which = e / (kPieces / 2), row = (e / (DK / 8)) % CM,
-                pc = e % (DK / 8);
-      const bool real = row < nCc;
-      const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(which ? a.q : a.k) +
-                                 (real ? tok_index(a, nb, nt0 + row, nh) * DK + pc * 8 : 0);
-      cp_async16(stg + which * (CM * DK * 2) + row * (DK * 2) + pc * 16, src, real ? 16 : 0);
-    }
-    if (kdn && tid < CM) {
-      const bool real = tid < nCc;
-      cp_async4(sS + tid, a.r + (real ? tok_index(a, nb, nt0 + tid, nh) : 0), real ? 4 : 0);
-    }
-    cp_async_commit();
-    constexpr int kGatePieces = CM * DK / 4;   // 16-byte pieces of omega (KDN)
-#pragma unroll
-    for (int r = 0; kdn && r < kGatePieces / kThreads; ++r) {
-      const int e4 = tid + r * kThreads, i = (4 * e4) / DK, c = (4 * e4) % DK;
-      const bool real = i < nCc;
-      const long ti = (real ? tok_index(a, nb, nt0 + i, nh) : tok_index(a, nb, 0, nh)) * DK + c;
-      cp_async16(sW + 4 * e4, a.omega + ti, real ? 16 : 0);
-    }
-    cp_async_commit();
-  };
-  if constexpr (kStage) {
-    if (it0 < kIters) prefetch_task(it0);
-  }
   for (long it = it0; it < kIters; it = chained ? s_ticket : it + (PREP ? gridDim.x : 1)) {
     int t0 = (int)it * CM;
     int ci = 0;       // chunk of a prep task
@@ -309,7 +248,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       if (!chained && tid < DK) carry = reinterpret_cast<const float*>(rec + rkP0)[tid];
     }
     const int Cc = min(CM, a.T - t0);
-    if constexpr (kStage) cp_async_wait_but_newest();   // this task's staged rows and r
     __syncthreads();
     if (chained && tid == 0) s_ticket = atomicAdd(chain + kIters, 1u);
 
@@ -322,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         const bool real = i < Cc;
         const long ti = (real ? tok_index(a, b, t0 + i, h) : tok_index(a, b, 0, h)) * DK + c;
         cp_async16(sX + 4 * e4, a.log_alpha + ti, real ? 16 : 0);
-        if (kdn && !kStage) cp_async16(sW + 4 * e4, a.omega + ti, real ? 16 : 0);   // staged: in flight
+        if (kdn) cp_async16(sW + 4 * e4, a.omega + ti, real ? 16 : 0);
       }
     }
 
@@ -338,16 +276,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
         if (!perchan) sg[i] = real ? a.log_alpha[ti] : 0.f;
         sb1[i] = real ? a.eta[ti] : 0.f;
       } else {
-        sb1[i] = real ? (kStage ? sS[i] : a.r[ti]) : 1.f;
+        sb1[i] = real ? a.r[ti] : 1.f;
         sb2[i] = a.info_scale / sb1[i];   // information scale over r, used by the variance scan
       }
       if (pstat) {
         sb2[i] = real ? a.alphaP[ti] : 1.f;
         sb3[i] = real ? a.betaP[ti] : 0.f;
       }
-    }
-    if constexpr (PREP && sizeof(Tin) == 2) {
-      if (tid == 0) umma::bulk_wait_read<0>();   // the previous task's record copies
     }
     __syncthreads();
 
@@ -357,30 +292,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       const int sub = tid % TPR;
       constexpr int kPasses = CM / RPP;
       float kvp[kPasses][8], qvp[kPasses][8];   // every pass's loads in flight first
-      if constexpr (kStage) {   // from the staged rows (zero past the end)
-        const unsigned short* stK = reinterpret_cast<const unsigned short*>(sQt);
-        const unsigned short* stQ = stK + CM * DK;
 #pragma unroll
-        for (int pz = 0; pz < kPasses; ++pz) {
-          const int i = pz * RPP + tid / TPR;
+      for (int pz = 0; pz < kPasses; ++pz) {
+        const int i = pz * RPP + tid / TPR;
+        const bool real = i < Cc;
+        const long base = real ? tok_index(a, b, t0 + i, h) * DK : 0;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            kvp[pz][e] = __uint_as_float(static_cast<uint32_t>(stK[i * DK + sub + TPR * e]) << 16);
-            qvp[pz][e] = __uint_as_float(static_cast<uint32_t>(stQ[i * DK + sub + TPR * e]) << 16);
-          }
-        }
-        __syncthreads();   // the staging area is the Q^T buffer written below
-      } else {
-#pragma unroll
-        for (int pz = 0; pz < kPasses; ++pz) {
-          const int i = pz * RPP + tid / TPR;
-          const bool real = i < Cc;
-          const long base = real ? tok_index(a, b, t0 + i, h) * DK : 0;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            kvp[pz][e] = real ? ldg_in<Tin>(a.k, base + sub + TPR * e) : 0.f;
-            qvp[pz][e] = real ? ldg_in<Tin>(a.q, base + sub + TPR * e) : 0.f;
-          }
+        for (int e = 0; e < 8; ++e) {
+          kvp[pz][e] = real ? ldg_in<Tin>(a.k, base + sub + TPR * e) : 0.f;
+          qvp[pz][e] = real ? ldg_in<Tin>(a.q, base + sub + TPR * e) : 0.f;
         }
       }
 #pragma unroll
@@ -956,145 +876,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
       tile_store(sLT + (32 + 16 * mt) * LDL + 8 * nt, LDL, d, -1.f, lane);
     }
     __syncthreads();
-    if constexpr (PREP && sizeof(Tin) == 2) {   // tile images for the tensor-core carry
-      // Each image is built in shared memory regions this task no longer needs and
-      // leaves with one bulk copy (thread 0): T and P over the L/T buffer, then
-      // W'^T there too, (Gamma.Q) over (Gamma.K)^T and Wbar over T^T.
-      // T^T, zero above the diagonal of T: thread (j, tokens 4 i4 .. 4 i4 + 3), one
-      // 16-byte store into the token-minor buffer
-      for (int e4 = tid; e4 < CM * CM / 4; e4 += kThreads) {
-        const int j = e4 & 63, i0 = 4 * (e4 >> 6);
-        float t[4];
-#pragma unroll
-        for (int y = 0; y < 4; ++y) t[y] = (j <= i0 + y) ? sLT[(i0 + y) * LDL + j] : 0.f;
-        *reinterpret_cast<float4*>(sTt + j * CS + i0) = make_float4(t[0], t[1], t[2], t[3]);
-      }
-      __syncthreads();
-      uint8_t* stX = reinterpret_cast<uint8_t*>(sX);
-      auto put = [&](uint8_t* base, int row, int col, const float (&x)[8], uint32_t lo_off) {
-        uint4 hi, lo;
-        tc::split8(x, hi, lo);
-        const uint32_t off = umma::sw128_offset(row, col);
-        *reinterpret_cast<uint4*>(base + off) = hi;
-        *reinterpret_cast<uint4*>(base + lo_off + off) = lo;
-      };
-      // T and P [64 i][64 j] from token-minor buffers: lanes take consecutive tokens
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int e = tid + r * kThreads, i = e & 63, g = e >> 6;
-        float xt[8], xp[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          xt[q] = sTt[(8 * g + q) * CS + i];
-          xp[q] = sPt[(8 * g + q) * CS + i];
-        }
-        put(stX, i, 8 * g, xt, 8192);
-        put(stX + 16384, i, 8 * g, xp, 8192);
-      }
-      umma::fence_proxy_async();
-      __syncthreads();
-      if (tid == 0) {
-        umma::bulk_store(rec + rbT, stX, 16384);
-        umma::bulk_store(rec + rbP, stX + 16384, 16384);
-        umma::bulk_commit();
-      }
-      // W'^T [c][i] = sum_{j <= i} (Gamma.K)^T[c][j] T[i][j] on m16n8k16 bf16 products of
-      // hi/lo splits: warp w takes rows 16w .. 16w + 15 and every 8-token column tile,
-      // whose k-steps stop at its last token (T is lower triangular).  The fp32
-      // fragments stay in registers until the record image is written.
-      float wacc[8][4];
-      {
-        const int g = lane >> 2, t = lane & 3, r0 = 16 * warp + g;
-        uint32_t ah[4][4], al[4][4];   // A = (Gamma.K)^T fragments of the 4 k-steps
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const int c0 = 16 * kk + 2 * t, c1 = c0 + 8;
-          const float2 x0 = *reinterpret_cast<const float2*>(sKt + r0 * CS + c0);
-          const float2 x1 = *reinterpret_cast<const float2*>(sKt + (r0 + 8) * CS + c0);
-          const float2 x2 = *reinterpret_cast<const float2*>(sKt + r0 * CS + c1);
-          const float2 x3 = *reinterpret_cast<const float2*>(sKt + (r0 + 8) * CS + c1);
-          split2(x0.x, x0.y, ah[kk][0], al[kk][0]);
-          split2(x1.x, x1.y, ah[kk][1], al[kk][1]);
-          split2(x2.x, x2.y, ah[kk][2], al[kk][2]);
-          split2(x3.x, x3.y, ah[kk][3], al[kk][3]);
-        }
-#pragma unroll
-        for (int n = 0; n < 8; ++n) {
-          float dh[4] = {0.f, 0.f, 0.f, 0.f}, dl[4] = {0.f, 0.f, 0.f, 0.f}, dr[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int kk = 0; kk <= n / 2; ++kk) {
-            const int j0 = 16 * kk + 2 * t, col = 8 * n + g;
-            uint32_t bh[2], bl[2];
-            split2(sTt[j0 * CS + col], sTt[(j0 + 1) * CS + col], bh[0], bl[0]);
-            split2(sTt[(j0 + 8) * CS + col], sTt[(j0 + 9) * CS + col], bh[1], bl[1]);
-            mma_bf16_16816(dl, al[kk], bh);
-            mma_bf16_16816(dr, ah[kk], bl);
-            mma_bf16_16816(dh, ah[kk], bh);
-          }
-#pragma unroll
-          for (int x = 0; x < 4; ++x) wacc[n][x] = dh[x] + (dl[x] + dr[x]);
-        }
-      }
-      if (tid == 0) umma::bulk_wait_read<0>();   // T, P have left the L/T buffer
-      __syncthreads();                           // (Gamma.K)^T and T^T are read too
-      uint8_t* stK = reinterpret_cast<uint8_t*>(sKt);
-      uint8_t* stT = reinterpret_cast<uint8_t*>(sTt);
-      {   // W'^T fragments -> hi/lo image: element pairs (row c, tokens 2t, 2t + 1)
-        const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-        for (int n = 0; n < 8; ++n)
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const int c = 16 * warp + g + 8 * hr, i = 8 * n + 2 * t;
-            uint32_t hi, lo;
-            split2(wacc[n][2 * hr], wacc[n][2 * hr + 1], hi, lo);
-            const uint32_t off = umma::sw128_offset(c, i);
-            *reinterpret_cast<uint32_t*>(stX + off) = hi;
-            *reinterpret_cast<uint32_t*>(stX + 16384 + off) = lo;
-          }
-      }
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {   // (Gamma.Q) and Wbar: [64 tok][128] as two 64-column blocks
-        {
-          const int e = tid + r * kThreads, i = e & 63, g = e >> 6, kb = g >> 3, cg = g & 7;
-          float xq[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) xq[q] = sQt[(8 * g + q) * CS + i];
-          put(stK + kb * 8192, i, 8 * cg, xq, 16384);
-        }
-        {   // Wbar is token-major: lanes take consecutive 8-channel groups of one row
-          const int e = tid + r * kThreads, i = e >> 4, g = e & 15, kb = g >> 3, cg = g & 7;
-          const float4 w0 = *reinterpret_cast<const float4*>(sW + i * DK + 8 * g);
-          const float4 w1 = *reinterpret_cast<const float4*>(sW + i * DK + 8 * g + 4);
-          const float xw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-          put(stT + kb * 8192, i, 8 * cg, xw, 16384);
-        }
-      }
-      if (tid < CM) {
-        float* rv = reinterpret_cast<float*>(rec + rbVec);
-        rv[tid] = 1.f;          // e^g qn: folded into (Gamma.Q)
-        rv[64 + tid] = 1.f;     // u: folded into Wbar
-        rv[128 + tid] = sgC[tid];
-        rv[192 + tid] = sgC[64 + tid];
-      }
-      umma::fence_proxy_async();
-      __syncthreads();
-      {   // the next task's rows: the Q^T buffer is dead once the Q image is built
-        const long nit = chained ? s_ticket : it + gridDim.x;
-        if (nit < kIters) prefetch_task(nit);
-      }
-      if (tid == 0) {
-        umma::bulk_store(rec + rbWp, stX, 32768);
-        umma::bulk_commit();
-        umma::bulk_store(rec + rbQ, stK, 32768);
-        umma::bulk_store(rec + rbW, stT, 32768);
-        umma::bulk_commit();
-        // the next task's gate copies overwrite the L/T buffer at once; the two
-        // token-minor buffers only at its key loads (waited there)
-        umma::bulk_wait_read<1>();
-      }
-      continue;
-    }
     if constexpr (PREP) {   // the carry's operands -> the record (float4 stores, coalesced)
       float4* rT = reinterpret_cast<float4*>(rec + rkT);
       float4* rP = reinterpret_cast<float4*>(rec + rkP);
@@ -1236,9 +1017,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(FwdArgs a, uint
   __syncthreads();
 
   // final state and aux
-  if constexpr (PREP && sizeof(Tin) == 2) {
-    if (tid == 0) umma::bulk_wait_all();   // every record byte is in global memory before exit
-  }
   if (PREP) return;
   if (a.S) {
     for (int e = tid; e < DK * NV; e += kThreads) {
