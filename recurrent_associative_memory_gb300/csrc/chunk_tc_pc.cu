@@ -50,7 +50,9 @@ using namespace tc;
 constexpr uint64_t kWait = 2000000000ull;   // 2 s per bounded wait
 constexpr int LDL = 68;                     // fp32 L/T row stride
 constexpr int LDX = 36;                     // fp32 scratch row stride
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;              // 16 warps: two per scheduler in every phase
+constexpr int kUnits = 1024 / kThreads;     // (token, 8-channel) units per thread
+constexpr int kWarps = kThreads / 32;
 
 // ---- record of one chunk (bytes; read by the carry's per-channel mode)
 constexpr uint32_t rbT = 0;          // T hi | T lo [64 i][64 j]
@@ -281,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       vom[tid] = n_om;
       if (has_next) prefetch_gates(nbh, nci);
     }
-    {
+    if (tid < 256) {
       const uint8_t* KQ = sm + sKQ;
       const int i = tid >> 2, part = tid & 3, kb = part >> 1, c0 = (part & 1) * 32;
       float kk = 0.f, qq = 0.f;
@@ -329,8 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (kIkdn) {   // mean squared decay of every token (warp w: tokens 8w .. 8w + 7)
 #pragma unroll
-      for (int rr = 0; rr < 8; ++rr) {
-        const int i = 8 * warp + rr;
+      for (int rr = 0; rr < 64 / kWarps; ++rr) {
+        const int i = (64 / kWarps) * warp + rr;
         float s2 = 0.f;
 #pragma unroll
         for (int c = lane; c < 128; c += 32) s2 += __expf(2.f * fG_[i * 128 + c]);
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* fY_ = fX_ + 64 * 128;                      // [64][128] KDN u, PKDA betaP k^2
     if (kKdn || kPkda) {
 #pragma unroll 2
-      for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < kUnits; ++r) {
         const int u = tid + r * kThreads, i = u >> 4, cg = u & 15, kb = cg >> 3, c8 = (cg & 7) * 8;
         const int cc = 64 * kb + c8;
         float k8[8], y[8];
@@ -513,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- 3. per-token write scale; per-channel factors of the sub-chunk references
-    if (kKdn) {   // 1 / (r_i + sum_c p^_ic k^_ic^2): four threads per token, 32 channels each
+    if (kKdn && tid < 256) {   // 1 / (r_i + sum_c p^_ic k^_ic^2): four threads per token
       const int i = tid >> 2, part = tid & 3, kb = part >> 1, c0 = (part & 1) * 32;
       const uint8_t* KQ = sm + sKQ;
       float z = 0.f;
@@ -554,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- 4. B image: for token j of sub-chunk J, w~_j = w_j exp(g_m(J) - g_j), then
     //         block I >= J gets w~_j exp(g_m(I) - g_m(J)).  Unit = (token, 8 channels).
 #pragma unroll 2
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < kUnits; ++r) {
       const int u = tid + r * kThreads, j = u >> 4, cg = u & 15, kb = cg >> 3, c8 = (cg & 7) * 8;
       const int cc = 64 * kb + c8, J = j >> 4;
       float k8[8];
@@ -604,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- 5. A image [K~ ; Q~] = [k^_i ; q^_i] exp(g_i - g_m(I))
 #pragma unroll 2
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < kUnits; ++r) {
       const int u = tid + r * kThreads, i = u >> 4, cg = u & 15, kb = cg >> 3, c8 = (cg & 7) * 8;
       const int cc = 64 * kb + c8, I = i >> 4;
       const uint8_t* kp = sm + sKQ + kb * 16384 + sw128_offset(i, c8);
@@ -670,9 +672,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Wbar = B_3 exp(g_C - g_m(3)) (block 3 of the B image holds every token's
     // w_j exp(g_m(3) - g_j)) to the record from the images' hi + lo, and (Gamma.K) =
     // K~ exp(g_m(I)) into registers, stored once the B image is free.
-    uint4 gk_hi[4], gk_lo[4];
+    uint4 gk_hi[kUnits], gk_lo[kUnits];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < kUnits; ++r) {
       const int u = tid + r * kThreads, i = u >> 4, cg = u & 15, kb = cg >> 3, c8 = (cg & 7) * 8;
       const int cc = 64 * kb + c8;
       const float* Em = fEm + (i >> 4) * 128 + cc;
@@ -714,13 +716,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     //         j = 0 .. 16 I + 15 at brow(I, j); warps of a TMEM quadrant split its
     //         16-column pieces.
     {
-      const int q = warp & 3, pch = warp >> 2;
+      const int q = warp & 3, pch = warp >> 2, npch = kWarps / 4;
       const int row = 32 * q + lane, i = row & 63, I = i >> 4;
       const bool isq = row >= 64;
       float* LT = reinterpret_cast<float*>(sm + sLT);
       const int pb = (q & 1) ? 3 : 0, pe = (q & 1) ? 10 : 3;
       const int p0 = I * (I + 1) / 2;   // first piece of this row's block
-      for (int p = pb + pch; p < pe; p += 2) {
+      for (int p = pb + pch; p < pe; p += npch) {
         float v[16];
         tmem_ld16(tmem + lane_off + tGram + 16 * p, v);
         tmem_ld_wait();
@@ -752,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      for (int jc = I + 1 + pch; jc < 4; jc += 2) {   // above the row's block: zero
+      for (int jc = I + 1 + pch; jc < 4; jc += npch) {   // above the row's block: zero
         if (!isq) {
 #pragma unroll
           for (int e = 0; e < 16; e += 4)
@@ -771,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (Gamma.K) as the W' MMA's A operand [64 tok][128] (MN-major, two 64-channel
     // blocks 8 KB apart)
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < kUnits; ++r) {
       const int u = tid + r * kThreads, i = u >> 4, cg = u & 15, kb = cg >> 3, c8 = (cg & 7) * 8;
       const uint32_t og = sGK + kb * 8192 + sw128_offset(i, c8);
       *reinterpret_cast<uint4*>(sm + og) = gk_hi[r];
@@ -822,14 +824,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_store(LT + r0 * LDL + c0 + 8 * nt, LDL, d, -1.f, lane);
     }
     __syncthreads();
-    {
+    if (warp < 8) {
       const int mt = warp >> 2, nt = warp & 3;
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       tile_mm3<4>(d, LT + (32 + 16 * mt) * LDL, LDL, LT + 8 * nt, LDL, lane);
       tile_store(XS + 16 * mt * LDX + 8 * nt, LDX, d, 1.f, lane);
     }
     __syncthreads();
-    {
+    if (warp < 8) {
       const int mt = warp >> 2, nt = warp & 3;
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       if (mt == 0)
@@ -841,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
 
     // ---- 9. T as bf16 hi/lo: the record and the W' MMA's B operand [T_hi ; T_lo]
-    {
+    if (tid < 256) {
       const int i = tid >> 2, c0 = (tid & 3) * 16;
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
@@ -884,26 +886,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       break;
     }
     tc_fence_after();
-    {   // row = channel c (TMEM lane), 32 tokens per thread
+    {   // row = channel c (TMEM lane), 16 tokens per thread
       const int c = (warp & 3) * 32 + lane, pch = warp >> 2;
-      float w[32];
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
+      float w[16];
+      {
         float t16[16], u16[16];
-        tmem_ld16(tmem + lane_off + tW + 32 * pch + 16 * part, t16);
-        tmem_ld16(tmem + lane_off + tW + 64 + 32 * pch + 16 * part, u16);
+        tmem_ld16(tmem + lane_off + tW + 16 * pch, t16);
+        tmem_ld16(tmem + lane_off + tW + 64 + 16 * pch, u16);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) w[16 * part + e] = t16[e] + u16[e];
+        for (int e = 0; e < 16; ++e) w[e] = t16[e] + u16[e];
       }
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
+      for (int m = 0; m < 2; ++m) {
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = w[8 * m + e];
         uint4 hi, lo;
         split8(x, hi, lo);
-        const uint32_t off = sw128_offset(c, 32 * pch + 8 * m);
+        const uint32_t off = sw128_offset(c, 16 * pch + 8 * m);
         st_global16(rec + rbWp + off, hi);
         st_global16(rec + rbWp + 16384 + off, lo);
       }
