@@ -28,11 +28,17 @@ __device__ __forceinline__ float ld_in(const void* p, long i) {
   return to_f<T>(static_cast<const T*>(p)[i]);
 }
 
-// Both CTAs of a cluster pass this point before either goes on (release /
-// acquire: the other CTA's global reads before it are complete).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
-                   "memory");
+// The cluster barrier in two halves: every thread of every CTA in the cluster
+// arrives, and a wait (acquire) returns once all have arrived.  The arrive is
+// relaxed: a release would hold the thread until its streaming state loads,
+// still in flight, had completed; the value it must order (the old gain state)
+// has been consumed before the arrive, so the write after the partner's wait
+// cannot reach it.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Block-wide sum of one value per thread (all threads must call).
@@ -46,6 +52,29 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
   for (int i = 0; i < kDecodeThreads / 32; ++i) s += red[i];
   return s;
+}
+
+// Block-wide sums of N values per thread in one pass (two barriers in all);
+// red holds N x (warps) floats.
+template <int N>
+__device__ __forceinline__ void block_sums(float (&v)[N], float* red) {
+  constexpr int NW = kDecodeThreads / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = 0; i < N; ++i) v[i] = warp_sum(v[i]);
+  __syncthreads();
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) red[i * NW + warp] = v[i];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) t += red[i * NW + w];
+    v[i] = t;
+  }
 }
 
 // DK rows x DVS columns of S per CTA.  Slices of up to 128 x 64 keep 32 state
@@ -62,7 +91,7 @@ __global__ void __launch_bounds__(kDecodeThreads, (DK * DVS <= 8192) ? 4 : 2)
 
   __shared__ float s_k[DK], s_q[DK], s_w[DK], s_d[DK];
   __shared__ float s_v[DVS], s_e[DVS];
-  __shared__ float s_red[kDecodeThreads / 32];
+  __shared__ float s_red[5 * (kDecodeThreads / 32)];
   __shared__ float4 s_pk[NROWG][NCG], s_pq[NROWG][NCG];
 
   const int nslice = a.dv / DVS;
@@ -104,54 +133,62 @@ __global__ void __launch_bounds__(kDecodeThreads, (DK * DVS <= 8192) ? 4 : 2)
   const float g_auxh = a.variant == DR_IKDN ? a.aux[tok] : 0.f;
   const float g_omh = a.variant == DR_IKDN ? a.omega[tok] : 0.f;
   if (tid < DVS) s_v[tid] = ld_in<Tin>(a.v, tok * a.dv + slice * DVS + tid);
-  const float kk = block_sum(kc * kc, s_red);
-  const float qq = block_sum(qc * qc, s_red);
-  if (a.k_l2norm) kc = kc / fmaxf(sqrtf(kk), 1e-30f);
-  if (a.q_l2norm) qc = qc / fmaxf(sqrtf(qq), 1e-30f);
-  const float kk_eff = a.k_l2norm ? block_sum(kc * kc, s_red) : kk;
+
+  // One block reduction for every sum over channels that needs no normalised key
+  // (the norms are applied to the sums): ||k||^2, ||q||^2, k.q, and for Diagonal
+  // KDN sum p^ k^2 and sum p^ k q, for isotropic KDN sum alpha^2.
+  const bool kdn = a.variant == DR_KDN, ikdn = a.variant == DR_IKDN;
+  float alpha = 0.f, p_hat = 0.f;
+  if (tid < DK) {
+    alpha = expf(g_la);   // per row of S for the per-channel variants, per head otherwise
+    if (kdn) p_hat = alpha * alpha * g_aux + g_om;
+  }
+  float sums[5] = {kc * kc, qc * qc, kc * qc, kdn ? p_hat * kc * kc : (ikdn ? alpha * alpha : 0.f),
+                   kdn ? p_hat * kc * qc : 0.f};
+  block_sums<5>(sums, s_red);
+  const float kk = sums[0], qq = sums[1];
+  const float cr = a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f;
+  const float qn = a.q_l2norm ? 1.f / fmaxf(sqrtf(qq), 1e-30f) : 1.f;
+  kc *= cr;
+  qc *= qn;
+  const float kk_eff = kk * cr * cr;          // ||k^||^2
+  const float kq = sums[2] * cr * qn;         // k^ . q^
 
   // The gain state (PGDN / PKDA statistic, KDN variance, isotropic KDN variance)
   // is updated in place.  Every slice of a head forms the same gains from it; the
   // slices of a head form one cluster, and the new value is written by slice 0
   // only after every slice has read the old one (cluster barrier below).
-  float w = 0.f, d = 0.f, aux_new = 0.f;
-  if (a.variant == DR_KDN) {
-    float p_hat = 0.f, alpha = 0.f;
+  float w = 0.f, d = alpha, aux_new = 0.f, wq = 0.f;
+  if (kdn) {
+    const float rr = g_r, den = rr + sums[3] * cr * cr;   // r + sum p^ k^2
     if (tid < DK) {
-      alpha = expf(g_la);
-      p_hat = alpha * alpha * g_aux + g_om;
-    }
-    const float z = block_sum(tid < DK ? p_hat * kc * kc : 0.f, s_red);
-    if (tid < DK) {
-      const float rr = g_r;
-      w = p_hat * kc / (rr + z);
-      d = alpha;
+      w = p_hat * kc / den;
       const float u = (a.info_scale / rr) * kc * kc;
       aux_new = p_hat / (1.f + u * p_hat);
     }
-  } else if (a.variant == DR_IKDN) {   // one variance per head (aux [B, H])
-    const float alpha = tid < DK ? expf(g_la) : 0.f;
-    const float a_mean = block_sum(alpha * alpha, s_red) / DK;
+    wq = sums[4] * cr * qn / den;
+  } else if (ikdn) {   // one variance per head (aux [B, H])
     const float rr = g_r;
-    const float b_hat = a_mean * g_auxh + g_omh;
-    if (tid < DK) {
-      w = b_hat / (rr + b_hat * kk_eff) * kc;
-      d = alpha;
-    }
+    const float b_hat = sums[3] / DK * g_auxh + g_omh;
+    const float beta = b_hat / (rr + b_hat * kk_eff);
+    if (tid < DK) w = beta * kc;
+    wq = beta * kq;
     const float u = a.info_scale * kk_eff / (DK * rr);
     aux_new = b_hat / (1.f + u * b_hat);
-  } else if (tid < DK) {
-    d = expf(g_la);   // per row of S for KDA / PKDA, per head otherwise
-    const float eta = g_eta;
-    if (a.variant == DR_GDN || a.variant == DR_KDA) {
-      w = eta * kc;
-    } else if (a.variant == DR_KLA) {
-      w = eta / (kk_eff + a.eps) * kc;
-    } else {  // DR_PGDN, DR_PKDA
+  } else if (a.variant == DR_GDN || a.variant == DR_KDA) {
+    if (tid < DK) w = g_eta * kc;
+    wq = g_eta * kq;
+  } else if (a.variant == DR_KLA) {
+    const float beta = g_eta / (kk_eff + a.eps);
+    if (tid < DK) w = beta * kc;
+    wq = beta * kq;
+  } else {   // DR_PGDN, DR_PKDA: the bound is per channel, so w . q needs its own sum
+    if (tid < DK) {
       const float A = g_aP * g_aux + g_bP * kc * kc;
-      const float rr = logf(fmaxf(A, a.log_floor)) - g_mu;
-      const float sq = rr / (1.f + fabsf(rr));
-      w = eta * expf(-a.ln_x * sq) * kc;
+      // fast log / exp, as in the chunkwise preps (~1e-6 relative in the bound)
+      const float rr = __logf(fmaxf(A, a.log_floor)) - g_mu;
+      const float sq = __fdividef(rr, 1.f + fabsf(rr));
+      w = g_eta * __expf(-a.ln_x * sq) * kc;
       aux_new = A;
     }
   }
@@ -162,7 +199,16 @@ __global__ void __launch_bounds__(kDecodeThreads, (DK * DVS <= 8192) ? 4 : 2)
     s_w[tid] = w;
     s_d[tid] = d;
   }
-  const float wq = block_sum(tid < DK ? w * qc : 0.f, s_red);  // includes a __syncthreads
+  if (a.variant == DR_PGDN || a.variant == DR_PKDA)
+    wq = block_sum(tid < DK ? w * qc : 0.f, s_red);   // includes a __syncthreads
+  else
+    __syncthreads();
+  // every slice has read the old gain state by now (its gains are formed): arrive
+  // at the cluster barrier here and wait only before the write at the end, so no
+  // slice waits for its partner's whole state pass
+  const bool has_aux = a.variant == DR_PGDN || a.variant == DR_PKDA || a.variant == DR_KDN ||
+                       a.variant == DR_IKDN;
+  if (has_aux && nslice > 1) cluster_arrive();
 
   // 3. S~^T k and S~^T q partials over this thread's rows
   float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), pq = pk;
@@ -212,11 +258,8 @@ __global__ void __launch_bounds__(kDecodeThreads, (DK * DVS <= 8192) ? 4 : 2)
   }
   if (bad) set_status(DR_ERR_NONFINITE);
   // 6. the gain state, in place, once every slice of this head has read the old one
-  //    (at the start of step 2; the barrier comes last so that it costs no stall)
-  const bool has_aux = a.variant == DR_PGDN || a.variant == DR_PKDA || a.variant == DR_KDN ||
-                       a.variant == DR_IKDN;
   if (has_aux) {
-    if (nslice > 1) cluster_sync();
+    if (nslice > 1) cluster_wait();
     if (slice == 0) {
       if (a.variant == DR_IKDN) {
         if (tid == 0) a.aux[tok] = aux_new;
