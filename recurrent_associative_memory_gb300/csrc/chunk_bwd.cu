@@ -92,6 +92,8 @@ struct BwdWs {
   float* CR;      // PGDN [n][64]       key-norm factors
   float* MU;      // PGDN [B H]         each row's part of dL/dmu
   float* Wf;      // per-channel decay [n][64][128]  the forward's write vectors
+  float* GM;      // gain variants [n][2][128]  each chunk's affine map of the gain adjoint
+  float* GE;      // gain variants [n][128]     the gain adjoint at each chunk's end
   size_t recb;    // bytes of one forward record
 };
 
@@ -123,6 +125,10 @@ size_t bwd_layout(void* base, long n, int rows, int mode, BwdWs* w) {
   if (pgdn) v.CR = reinterpret_cast<float*>(take((size_t)n * 64 * 4));
   if (pgdn || gain) v.MU = reinterpret_cast<float*>(take((size_t)rows * 4));
   if (pc) v.Wf = reinterpret_cast<float*>(take((size_t)n * 8192 * 4));
+  if (gain) {
+    v.GM = reinterpret_cast<float*>(take((size_t)n * 256 * 4));
+    v.GE = reinterpret_cast<float*>(take((size_t)n * 128 * 4));
+  }
   if (w) *w = v;
   return off;
 }
@@ -1410,8 +1416,15 @@ __global__ void __launch_bounds__(128, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArg
 //   d omega = dp^,  d log alpha += 2 alpha^2 p_{t-1} dp^,  dp <- alpha^2 dp^,
 // and per token d r = -c / den^2 - (mu / r^2) sum_c k^2 du and the key norm.  dp at
 // the row start is dL/dp_0.
+// The chain is affine in dp: token t maps dL/dp_t to dL/dp_{t-1} = alpha^2 (X_t +
+// dp / q^2) with X_t = dw k^ / den - (c / den^2) k^2, so each chunk composes to
+// dp_start = A dp_end + B per channel.  PHASE 0 (every chunk at once) forms the
+// chunk's (A, B); gain_scan walks each row's maps backwards and leaves dp at
+// every chunk's end (and dL/dp_0); PHASE 1 (every chunk at once) runs the
+// chunk's tokens backwards from it and writes the gradients.
 constexpr int kKdnGainSmemF = 6 * 64 * 128;
 
+template <int PHASE>
 __global__ void __launch_bounds__(128, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
   extern __shared__ __align__(16) float smf[];
   float* sK = smf;                  // k^ [t][c]
@@ -1422,15 +1435,14 @@ __global__ void __launch_bounds__(128, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs
   float* sPo = sPh + 64 * 128;      // p (posterior)
   __shared__ float s_r[64], s_mr[64], s_cr[64], s_den[64], s_cc[64], s_iden[64], s_cd2[64];
   const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
-  const int bh = blockIdx.x, b = bh / a.H, h = bh % a.H;
   const int NC = (a.T + 63) / 64;
+  const size_t ri = blockIdx.x;
+  const int bh = (int)(ri / NC), c = (int)(ri % NC), b = bh / a.H, h = bh % a.H;
   const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
   const float mu = a.info_scale;
-  float dp = g.daux_T ? g.daux_T[(size_t)bh * 128 + i] : 0.f;
-  for (int c = NC - 1; c >= 0; --c) {
-    const size_t ri = (size_t)bh * NC + c;
+  float dp = PHASE == 1 ? g.w.GE[ri * 128 + i] : 0.f;
+  {
     const int t0 = 64 * c, Cc = min(64, a.T - t0);
-    __syncthreads();
     if (i < 64) {
       s_r[i] = i < Cc ? a.r[tok(a, b, t0 + i, h)] : 1.f;
       s_mr[i] = mu / s_r[i];
@@ -1440,7 +1452,7 @@ __global__ void __launch_bounds__(128, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs
       const bool live = t < Cc;
       const long o = tok(a, b, t0 + (live ? t : 0), h) * 128 + c4;
       cpa16(sDW + t * 128 + c4, g.w.DW + ri * 8192 + t * 128 + c4, live ? 16 : 0);
-      cpa16(sDK + t * 128 + c4, g.dk + o, live ? 16 : 0);
+      if (PHASE == 1) cpa16(sDK + t * 128 + c4, g.dk + o, live ? 16 : 0);
       cpa16(sA + t * 128 + c4, a.log_alpha + o, live ? 16 : 0);
       cpa16(sPh + t * 128 + c4, a.omega + o, live ? 16 : 0);
     }
@@ -1509,6 +1521,20 @@ __global__ void __launch_bounds__(128, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs
       }
     }
     __syncthreads();
+    if (PHASE == 0) {   // the chunk's affine map dp_start = A dp_end + B, channel i
+      float A = 1.f, Bm = 0.f;
+      for (int t = Cc - 1; t >= 0; --t) {
+        const float kh = sK[t * 128 + i], ph = sPh[t * 128 + i], al = sA[t * 128 + i];
+        const float q1 = 1.f + s_mr[t] * kh * kh * ph;
+        const float a2 = al * al, f = a2 * __fdividef(1.f, q1 * q1);
+        const float x = sDW[t * 128 + i] * kh * s_iden[t] - s_cd2[t] * kh * kh;
+        A = f * A;
+        Bm = f * Bm + a2 * x;
+      }
+      g.w.GM[ri * 256 + i] = A;
+      g.w.GM[ri * 256 + 128 + i] = Bm;
+      return;
+    }
     // backwards over the chunk's tokens, per channel (the chain through dp)
     for (int t = Cc - 1; t >= 0; --t) {
       const float kh = sK[t * 128 + i], ph = sPh[t * 128 + i], al = sA[t * 128 + i];
@@ -1558,7 +1584,22 @@ __global__ void __launch_bounds__(128, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs
       }
     }
   }
-  if (g.daux0) g.daux0[(size_t)bh * 128 + i] = dp;
+}
+
+// Each row's chunk maps in reverse chunk order (one thread per channel, or one
+// per row for a scalar adjoint, nch = 1): the adjoint at every chunk's end, from
+// dL/d(final) (0 when absent), and at the row start dL/d(initial).
+__global__ void gain_scan_kernel(FwdArgs a, BwdArgs g, int nch) {
+  const int bh = blockIdx.x, i = threadIdx.x;
+  if (i >= nch) return;
+  const int NC = (a.T + 63) / 64;
+  float dp = g.daux_T ? g.daux_T[(size_t)bh * nch + i] : 0.f;
+  for (int c = NC - 1; c >= 0; --c) {
+    const size_t ri = (size_t)bh * NC + c;
+    g.w.GE[ri * 128 + i] = dp;
+    dp = g.w.GM[ri * 256 + i] * dp + g.w.GM[ri * 256 + 128 + i];
+  }
+  if (g.daux0) g.daux0[(size_t)bh * nch + i] = dp;
 }
 
 // ================================================================= ikdn_gain_bwd
@@ -1765,7 +1806,9 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
       (e = cudaFuncSetAttribute(bwd_local_pc_kernel<DR_KDN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kPcLocalSmem)) !=
           cudaSuccess ||
-      (e = cudaFuncSetAttribute(kdn_gain_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (e = cudaFuncSetAttribute(kdn_gain_bwd_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kKdnGainSmemF * 4)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(kdn_gain_bwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kKdnGainSmemF * 4)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(bwd_local_kernel<DR_PGDN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l_smem)) !=
@@ -1804,7 +1847,9 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
     bwd_local_pc_kernel<DR_KDA><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
   } else if (fa.variant == DR_KDN) {
     bwd_local_pc_kernel<DR_KDN><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
-    kdn_gain_bwd_kernel<<<fa.B * fa.H, 128, kKdnGainSmemF * 4, st>>>(fa, g);
+    kdn_gain_bwd_kernel<0><<<(unsigned)n, 128, kKdnGainSmemF * 4, st>>>(fa, g);
+    gain_scan_kernel<<<fa.B * fa.H, 128, 0, st>>>(fa, g, 128);
+    kdn_gain_bwd_kernel<1><<<(unsigned)n, 128, kKdnGainSmemF * 4, st>>>(fa, g);
   } else if (fa.variant == DR_PKDA) {
     bwd_local_pc_kernel<DR_PKDA><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
     pgdn_gain_bwd_kernel<true><<<fa.B * fa.H, 128, p_smem, st>>>(fa, g);

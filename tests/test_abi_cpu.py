@@ -225,7 +225,8 @@ def test_backward_refusals_and_workspace_size(dr):
     assert call(ws=(A + 16, 1 << 30)) == dr.DR_ERR_ALIGN
     # Diagonal KDN, PKDA, isotropic KDN: as KDA plus dL/dw and 4 B per row
     need_k = dr.dr_chunk_bwd_workspace_bytes(dr.DR_KDN, dr.DR_BF16, 2, 130, 3, 128, 128, 64)
-    assert need_k == need_a + al(n * 32768) + al(4 * rows)
+    # (+ each chunk's affine map of the gain adjoint and the adjoint at its end)
+    assert need_k == need_a + al(n * 32768) + al(4 * rows) + al(n * 1024) + al(n * 512)
     for vid in (dr.DR_PKDA, dr.DR_IKDN):   # the same layout (with PKDA's rows' dL/dmu parts)
         assert dr.dr_chunk_bwd_workspace_bytes(vid, dr.DR_BF16, 2, 130, 3, 128, 128, 64) == need_k
     assert dr.dr_chunk_bwd_workspace_bytes(dr.DR_EKDN, dr.DR_BF16, 1, 64, 1, 128, 128, 64) == 0

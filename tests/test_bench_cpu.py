@@ -222,7 +222,7 @@ def test_backward_bytes_and_kernel_counts_per_channel_decay():
                                              + 3 * ikdn.B * ikdn.H * 4)
     k = bench.bwd_kernels_per_call
     assert k("kda", 4, 16) == 5 and k("ikdn", 4, 16) == 6 and k("pkda", 4, 16) == 7
-    assert k("kdn", 4, 16, 152) == 6 and k("kdn", 1, 2, 152) == 8
+    assert k("kdn", 4, 16, 152) == 8 and k("kdn", 1, 2, 152) == 10
     assert set(bench.bwd_grad_names("kdn")) == {"dq", "dk", "dv", "dlog_alpha", "dS0", "domega",
                                                  "dr"}
     assert "dalphaP" in bench.bwd_grad_names("pkda") and "deta" in bench.bwd_grad_names("kda")
