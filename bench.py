@@ -202,11 +202,11 @@ def bwd_kernels_per_call(variant, B=1, H=1, nsm=152):
     """libdr kernels one dr_chunk_bwd call launches: the forward again (prep and
     carry; PGDN also its statistic's map and scan; Diagonal KDN with few rows,
     3 B H < SMs, its variance map and scan), the reverse carry, the state
-    products, the local gradients, then the gain's adjoint (PGDN / PKDA: and the
-    d mu sum; Diagonal KDN: each chunk's map, the scan over chunks, each chunk's
-    gradients; isotropic KDN: one kernel)."""
+    products, the local gradients, then the gain's adjoint (each chunk's affine
+    map, the scan over chunks, each chunk's gradients; PGDN / PKDA also the d mu
+    sum)."""
     fwd = {"pgdn": 4, "kdn": 2 if 3 * B * H >= nsm else 4}.get(variant, 2)
-    gain = {"pgdn": 2, "pkda": 2, "kdn": 3, "ikdn": 1}.get(variant, 0)
+    gain = {"pgdn": 4, "pkda": 4, "kdn": 3, "ikdn": 3}.get(variant, 0)
     return fwd + 3 + gain
 
 

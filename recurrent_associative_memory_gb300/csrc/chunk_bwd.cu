@@ -123,9 +123,9 @@ size_t bwd_layout(void* base, long n, int rows, int mode, BwdWs* w) {
   v.SS = reinterpret_cast<float*>(take((size_t)n * (pc ? 128 : 1) * 4));
   if (pgdn || gain) v.DW = reinterpret_cast<float*>(take((size_t)n * 8192 * 4));
   if (pgdn) v.CR = reinterpret_cast<float*>(take((size_t)n * 64 * 4));
-  if (pgdn || gain) v.MU = reinterpret_cast<float*>(take((size_t)rows * 4));
+  if (pgdn || gain) v.MU = reinterpret_cast<float*>(take((size_t)n * 4));
   if (pc) v.Wf = reinterpret_cast<float*>(take((size_t)n * 8192 * 4));
-  if (gain) {
+  if (pgdn || gain) {
     v.GM = reinterpret_cast<float*>(take((size_t)n * 256 * 4));
     v.GE = reinterpret_cast<float*>(take((size_t)n * 128 * 4));
   }
@@ -1233,9 +1233,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ================================================================= pgdn_gain_bwd
-// One CTA per (b, h), a thread per key channel, chunks in reverse.  Per chunk the
-// statistic A_t is recomputed forward from its chunk-start value (the forward's
-// record), then the tokens are walked backwards (PDN notes Eq. (9)):
+// One CTA per chunk, a thread per key channel.  The statistic A_t is recomputed
+// forward from its chunk-start value (the forward's record), then the tokens are
+// walked backwards (PDN notes Eq. (9)):
 //   r = ln max(A, floor) - mu,  B = exp(-ln(x) r / (1 + |r|)),  w = eta B . k^
 //   d eta  = sum_i B k^ dw,   dr = -ln(x) B eta k^ dw / (1 + |r|)^2,
 //   dA_t = dA + [A > floor] dr / A,   d mu -= [A > floor] dr,
@@ -1247,9 +1247,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // same statistic with per-channel decay, which the statistic does not involve):
 // the chunk-start statistic comes from the per-channel record and the key norms
 // are formed here.
+// The chain is affine in dA: token t maps dA_t's carry to alphaP_t (dA + y_t) with
+// y_t = [A_t > floor] dr_t / A_t free of dA, so a chunk composes to dA_start =
+// M dA_end + N per channel.  PHASE 0 (every chunk at once) forms (M, N);
+// gain_scan walks each row's maps backwards (dA at every chunk's end, dL/dA_0);
+// PHASE 1 (every chunk at once) runs the chunk backwards from it, writes the
+// gradients and the chunk's part of dL/dmu.
 constexpr int kGainSmemF = 4 * 64 * 128;
 
-template <bool PC>
+template <bool PC, int PHASE>
 __global__ void __launch_bounds__(128, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
   extern __shared__ __align__(16) float smf[];
   float* sK = smf;                  // k^ [t][i]
@@ -1258,16 +1264,15 @@ __global__ void __launch_bounds__(128, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArg
   float* sA = sDK + 64 * 128;       // A_t [t][i], then dA_t
   __shared__ float s_aP[64], s_bP[64], s_eta[64], s_cr[64], s_mu[4];
   const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
-  const int bh = blockIdx.x, b = bh / a.H, h = bh % a.H;
   const int NC = (a.T + 63) / 64;
+  const size_t ri = blockIdx.x;
+  const int bh = (int)(ri / NC), c = (int)(ri % NC), b = bh / a.H, h = bh % a.H;
   const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
   const float mu_h = a.mu[h];
-  float dA = g.daux_T ? g.daux_T[(size_t)bh * 128 + i] : 0.f;
+  float dA = PHASE == 1 ? g.w.GE[ri * 128 + i] : 0.f;
   float dmu = 0.f;
-  for (int c = NC - 1; c >= 0; --c) {
-    const size_t ri = (size_t)bh * NC + c;
+  {
     const int t0 = 64 * c, Cc = min(64, a.T - t0);
-    __syncthreads();
     if (i < 64) {
       const bool live = i < Cc;
       const long ti = tok(a, b, t0 + (live ? i : 0), h);
@@ -1280,7 +1285,8 @@ __global__ void __launch_bounds__(128, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArg
       const int t = e >> 5, c4 = 4 * (e & 31);
       const bool live = t < Cc;
       cpa16(sDW + t * 128 + c4, g.w.DW + ri * 8192 + t * 128 + c4, live ? 16 : 0);
-      cpa16(sDK + t * 128 + c4, g.dk + tok(a, b, t0 + (live ? t : 0), h) * 128 + c4, live ? 16 : 0);
+      if (PHASE == 1)
+        cpa16(sDK + t * 128 + c4, g.dk + tok(a, b, t0 + (live ? t : 0), h) * 128 + c4, live ? 16 : 0);
     }
     cpa_wait_all();
     __syncthreads();
@@ -1325,6 +1331,22 @@ __global__ void __launch_bounds__(128, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArg
         A = s_aP[t] * A + s_bP[t] * kv * kv;
         sA[t * 128 + i] = A;
       }
+    }
+    if (PHASE == 0) {   // the chunk's affine map dA_start = M dA_end + N, channel i
+      float M = 1.f, N = 0.f;
+      for (int t = Cc - 1; t >= 0; --t) {
+        const float A = sA[t * 128 + i];
+        const float rr = logf(fmaxf(A, a.log_floor)) - mu_h;
+        const float den = 1.f + fabsf(rr);
+        const float Bv = expf(-a.ln_x * rr / den);
+        const float drr = -a.ln_x * Bv * (s_eta[t] * sK[t * 128 + i] * sDW[t * 128 + i]) / (den * den);
+        const float y = A > a.log_floor ? __fdividef(drr, A) : 0.f;
+        N = s_aP[t] * (N + y);
+        M = s_aP[t] * M;
+      }
+      g.w.GM[ri * 256 + i] = M;
+      g.w.GM[ri * 256 + 128 + i] = N;
+      return;
     }
     // backwards over the chunk's tokens: per channel only (the chain through dA);
     // dA_t replaces A_t, and B k^ dw replaces dL/dw, for the sums over channels
@@ -1396,19 +1418,17 @@ __global__ void __launch_bounds__(128, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArg
       }
     }
   }
-  if (g.daux0) g.daux0[(size_t)bh * 128 + i] = dA;
   dmu = warp_sum(dmu);
   if (lane == 0) s_mu[warp] = dmu;
   __syncthreads();
-  if (i == 0) g.w.MU[bh] = s_mu[0] + s_mu[1] + s_mu[2] + s_mu[3];
+  if (i == 0) g.w.MU[ri] = s_mu[0] + s_mu[1] + s_mu[2] + s_mu[3];
 }
 
 // ================================================================= kdn_gain_bwd
 // Diagonal KDN's write vector is the Kalman gain w = p^ . k^ / (r + sum_c p^ k^2)
 // with the predicted variance p^_t = alpha_t^2 p_{t-1} + omega_t and the posterior
 // p_t = p^_t / (1 + u_t p^_t), u_t = (mu / r_t) k^_t^2 (KDN notes Eq. (23) and
-// section 5).  One CTA per (b, h), a thread per key channel, chunks in reverse:
-// p^ and p are recomputed over the chunk from its chunk-start variance (the
+// section 5).  One CTA per chunk, a thread per key channel: p^ and p are recomputed over the chunk from its chunk-start variance (the
 // forward's record), den_t = r_t + sum_c p^ k^2 and c_t = sum_c dw p^ k^ per token,
 // then the tokens are walked backwards with the variance adjoint dp (from dL/dp_T):
 //   dp^ = dw k^ / den - (c / den^2) k^2 + dp / q^2,  q = 1 + u p^,  du = -dp p^2 / q^2,
@@ -1605,8 +1625,8 @@ __global__ void gain_scan_kernel(FwdArgs a, BwdArgs g, int nch) {
 // ================================================================= ikdn_gain_bwd
 // Isotropic KDN keeps one variance b per head: b^_t = abar_t b_{t-1} + omega_t with
 // abar_t = mean_c alpha_tc^2, w_t = beta_t k^_t, beta = b^ / (r + b^ s), s = ||k^||^2,
-// b_t = b^ / (1 + u b^), u = mu s / (dk r) (KDN notes Eq. (40)).  One CTA per (b, h),
-// chunks in reverse: per token (in parallel) s, abar and d beta = k^ . dw; the
+// b_t = b^ / (1 + u b^), u = mu s / (dk r) (KDN notes Eq. (40)).  One CTA per chunk:
+// per token (in parallel) s, abar and d beta = k^ . dw; the
 // scalar chain over the chunk's tokens (thread 0; b^ recomputed from the chunk-start
 // variance of the record) with db (from dL/db_T):
 //   db^ = d beta r / den^2 + db / q^2,  q = 1 + u b^,  du = -db b^2 / q^2,  den = r + b^ s,
@@ -1614,9 +1634,13 @@ __global__ void gain_scan_kernel(FwdArgs a, BwdArgs g, int nch) {
 // then per (token, channel): dk^ += (b^ / den) dw + 2 ds k^ with
 // ds = -d beta b^2 / den^2 + du mu / (dk r),  d r = -d beta b^ / den^2 - du mu s / (dk r^2),
 // d log alpha += 2 alpha^2 b_{t-1} db^ / dk, and the key norm.  db at the row start
-// is dL/db_0.
+// is dL/db_0.  The chain is affine in db (db <- abar (d beta r / den^2 + db / q^2)),
+// so, as for Diagonal KDN, PHASE 0 forms each chunk's map (M, N), gain_scan (one
+// thread per row) the value at every chunk's end and PHASE 1 the gradients, all
+// chunks at once.
 constexpr int kIkdnGainSmemF = 3 * 64 * 128;
 
+template <int PHASE>
 __global__ void __launch_bounds__(128, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
   extern __shared__ __align__(16) float smf[];
   float* sK = smf;                  // k^ [t][c]
@@ -1625,15 +1649,14 @@ __global__ void __launch_bounds__(128, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArg
   __shared__ float s_r[64], s_om[64], s_cr[64], s_s[64], s_ab[64], s_db[64];
   __shared__ float s_bh[64], s_prev[64], s_dbh[64], s_du[64];
   const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
-  const int bh = blockIdx.x, b = bh / a.H, h = bh % a.H;
   const int NC = (a.T + 63) / 64;
+  const size_t ri = blockIdx.x;
+  const int bh = (int)(ri / NC), c = (int)(ri % NC), b = bh / a.H, h = bh % a.H;
   const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
   const float mu = a.info_scale;
-  float db = g.daux_T ? g.daux_T[bh] : 0.f;   // thread 0's chain
-  for (int c = NC - 1; c >= 0; --c) {
-    const size_t ri = (size_t)bh * NC + c;
+  float db = PHASE == 1 ? g.w.GE[ri * 128] : 0.f;   // thread 0's chain
+  {
     const int t0 = 64 * c, Cc = min(64, a.T - t0);
-    __syncthreads();
     if (i < 64) {
       const bool live = i < Cc;
       const long ti = tok(a, b, t0 + (live ? i : 0), h);
@@ -1701,7 +1724,19 @@ __global__ void __launch_bounds__(128, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArg
         s_bh[t] = bhat;
         bv = bhat / (1.f + mu * s_s[t] / (128.f * s_r[t]) * bhat);
       }
-      for (int t = Cc - 1; t >= 0; --t) {
+      if (PHASE == 0) {   // the chunk's affine map db_start = M db_end + N
+        float M = 1.f, N = 0.f;
+        for (int t = Cc - 1; t >= 0; --t) {
+          const float bhat = s_bh[t], rt = s_r[t], st = s_s[t];
+          const float den = rt + bhat * st, q1 = 1.f + mu * st / (128.f * rt) * bhat;
+          const float iq2 = 1.f / (q1 * q1);
+          N = s_ab[t] * (s_db[t] * rt / (den * den) + N * iq2);
+          M = s_ab[t] * iq2 * M;
+        }
+        g.w.GM[ri * 256] = M;
+        g.w.GM[ri * 256 + 128] = N;
+      }
+      for (int t = Cc - 1; PHASE == 1 && t >= 0; --t) {
         const float bhat = s_bh[t], rt = s_r[t], st = s_s[t];
         const float den = rt + bhat * st, q1 = 1.f + mu * st / (128.f * rt) * bhat;
         const float iq2 = 1.f / (q1 * q1);
@@ -1712,6 +1747,7 @@ __global__ void __launch_bounds__(128, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArg
       }
     }
     __syncthreads();
+    if (PHASE == 0) return;
     for (int tt = 0; tt < 16; ++tt) {   // per (token, channel), warp w: tokens 16 w .. + 15
       const int t = 16 * warp + tt;
       if (t >= Cc) break;
@@ -1743,15 +1779,16 @@ __global__ void __launch_bounds__(128, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArg
       }
     }
   }
-  if (i == 0 && g.daux0) g.daux0[bh] = db;
 }
 
-// dL/dmu_h: the rows' parts summed over the batch in order
+// dL/dmu_h: the chunks' parts summed over the batch and the chunks in order
 __global__ void pgdn_dmu_kernel(FwdArgs a, BwdArgs g) {
   const int h = blockIdx.x * blockDim.x + threadIdx.x;
   if (h >= a.H) return;
+  const int NC = (a.T + 63) / 64;
   float s = 0.f;
-  for (int b = 0; b < a.B; ++b) s += g.w.MU[(size_t)b * a.H + h];
+  for (int b = 0; b < a.B; ++b)
+    for (int c = 0; c < NC; ++c) s += g.w.MU[((size_t)b * a.H + h) * NC + c];
   g.dmu[h] = s;
 }
 
@@ -1813,10 +1850,16 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
       (e = cudaFuncSetAttribute(bwd_local_kernel<DR_PGDN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l_smem)) !=
           cudaSuccess ||
-      (e = cudaFuncSetAttribute(pgdn_gain_bwd_kernel<false>,
+      (e = cudaFuncSetAttribute(pgdn_gain_bwd_kernel<false, 0>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p_smem)) !=
           cudaSuccess ||
-      (e = cudaFuncSetAttribute(pgdn_gain_bwd_kernel<true>,
+      (e = cudaFuncSetAttribute(pgdn_gain_bwd_kernel<false, 1>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p_smem)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(pgdn_gain_bwd_kernel<true, 0>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p_smem)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(pgdn_gain_bwd_kernel<true, 1>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p_smem)) !=
           cudaSuccess ||
       (e = cudaFuncSetAttribute(bwd_local_pc_kernel<DR_PKDA>,
@@ -1825,7 +1868,9 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
       (e = cudaFuncSetAttribute(bwd_local_pc_kernel<DR_IKDN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kPcLocalSmem)) !=
           cudaSuccess ||
-      (e = cudaFuncSetAttribute(ikdn_gain_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      (e = cudaFuncSetAttribute(ikdn_gain_bwd_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kIkdnGainSmemF * 4)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(ikdn_gain_bwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kIkdnGainSmemF * 4)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(bwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)s_smem)) != cudaSuccess ||
@@ -1852,16 +1897,22 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
     kdn_gain_bwd_kernel<1><<<(unsigned)n, 128, kKdnGainSmemF * 4, st>>>(fa, g);
   } else if (fa.variant == DR_PKDA) {
     bwd_local_pc_kernel<DR_PKDA><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
-    pgdn_gain_bwd_kernel<true><<<fa.B * fa.H, 128, p_smem, st>>>(fa, g);
+    pgdn_gain_bwd_kernel<true, 0><<<(unsigned)n, 128, p_smem, st>>>(fa, g);
+    gain_scan_kernel<<<fa.B * fa.H, 128, 0, st>>>(fa, g, 128);
+    pgdn_gain_bwd_kernel<true, 1><<<(unsigned)n, 128, p_smem, st>>>(fa, g);
     pgdn_dmu_kernel<<<(fa.H + 127) / 128, 128, 0, st>>>(fa, g);
   } else if (fa.variant == DR_IKDN) {
     bwd_local_pc_kernel<DR_IKDN><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
-    ikdn_gain_bwd_kernel<<<fa.B * fa.H, 128, kIkdnGainSmemF * 4, st>>>(fa, g);
+    ikdn_gain_bwd_kernel<0><<<(unsigned)n, 128, kIkdnGainSmemF * 4, st>>>(fa, g);
+    gain_scan_kernel<<<fa.B * fa.H, 32, 0, st>>>(fa, g, 1);
+    ikdn_gain_bwd_kernel<1><<<(unsigned)n, 128, kIkdnGainSmemF * 4, st>>>(fa, g);
   } else if (fa.variant == DR_KLA) {
     bwd_local_kernel<DR_KLA><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
   } else if (pg) {
     bwd_local_kernel<DR_PGDN><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
-    pgdn_gain_bwd_kernel<false><<<fa.B * fa.H, 128, p_smem, st>>>(fa, g);
+    pgdn_gain_bwd_kernel<false, 0><<<(unsigned)n, 128, p_smem, st>>>(fa, g);
+    gain_scan_kernel<<<fa.B * fa.H, 128, 0, st>>>(fa, g, 128);
+    pgdn_gain_bwd_kernel<false, 1><<<(unsigned)n, 128, p_smem, st>>>(fa, g);
     pgdn_dmu_kernel<<<(fa.H + 127) / 128, 128, 0, st>>>(fa, g);
   } else {
     bwd_local_kernel<DR_GDN><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);

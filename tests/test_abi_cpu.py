@@ -206,7 +206,9 @@ def test_backward_refusals_and_workspace_size(dr):
     assert call(variant=dr.DR_PGDN, params=pg) == dr.DR_ERR_NULL        # no PGDN gate gradients
     assert call() == dr.DR_ERR_WORKSPACE                                # no workspace
     # every array on a 256-byte boundary: the record, S_c, E, dS, E dS^T, dO E^T,
-    # dR E^T, gamma <dS, S_c> (PGDN also dL/dw, the key-norm factors, the rows' dL/dmu)
+    # dR E^T, gamma <dS, S_c> (PGDN also dL/dw, the key-norm factors, each chunk's part
+    # of dL/dmu, each chunk's affine map of the statistic's adjoint and its value at the
+    # chunk's end)
     al = lambda x: -(-x // 256) * 256  # noqa: E731
     n, rows = 2 * 3 * 3, 2 * 3
     arrays = [65536, 32768, 65536, 32768, 16384, 16384]
@@ -214,7 +216,7 @@ def test_backward_refusals_and_workspace_size(dr):
     assert need == al(n * 66560) + sum(al(n * x) for x in arrays) + al(4 * n)
     need_p = dr.dr_chunk_bwd_workspace_bytes(dr.DR_PGDN, dr.DR_BF16, 2, 130, 3, 128, 128, 64)
     assert need_p == (al(n * 101376) + sum(al(n * x) for x in arrays) + al(4 * n) + al(n * 32768)
-                      + al(n * 256) + al(4 * rows))
+                      + al(n * 256) + al(4 * n) + al(n * 1024) + al(n * 512))
     # per-channel decay (KDA): the per-channel record and the forward's hand-over
     # flags, gamma_c <dS_c, S_c> per channel, the forward's write vectors
     chain = -(-((n + 2) * 4) // 256) * 256
@@ -223,11 +225,11 @@ def test_backward_refusals_and_workspace_size(dr):
                       + al(n * 32768))
     assert call(ws=(A, 1000)) == dr.DR_ERR_WORKSPACE
     assert call(ws=(A + 16, 1 << 30)) == dr.DR_ERR_ALIGN
-    # Diagonal KDN, PKDA, isotropic KDN: as KDA plus dL/dw and 4 B per row
+    # Diagonal KDN, PKDA, isotropic KDN: as KDA plus dL/dw, 4 B per chunk, each
+    # chunk's affine map of the gain adjoint and the adjoint at its end
     need_k = dr.dr_chunk_bwd_workspace_bytes(dr.DR_KDN, dr.DR_BF16, 2, 130, 3, 128, 128, 64)
-    # (+ each chunk's affine map of the gain adjoint and the adjoint at its end)
-    assert need_k == need_a + al(n * 32768) + al(4 * rows) + al(n * 1024) + al(n * 512)
-    for vid in (dr.DR_PKDA, dr.DR_IKDN):   # the same layout (with PKDA's rows' dL/dmu parts)
+    assert need_k == need_a + al(n * 32768) + al(4 * n) + al(n * 1024) + al(n * 512)
+    for vid in (dr.DR_PKDA, dr.DR_IKDN):   # the same layout (with PKDA's chunks' dL/dmu parts)
         assert dr.dr_chunk_bwd_workspace_bytes(vid, dr.DR_BF16, 2, 130, 3, 128, 128, 64) == need_k
     assert dr.dr_chunk_bwd_workspace_bytes(dr.DR_EKDN, dr.DR_BF16, 1, 64, 1, 128, 128, 64) == 0
 

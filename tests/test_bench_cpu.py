@@ -197,12 +197,13 @@ def test_backward_parity_row_slice_matches_the_oracle_on_the_full_input():
 def test_backward_bytes_pgdn_and_kernel_counts():
     """PGDN's backward also moves alphaP, betaP in and their gradients out (16 more
     bytes per head-token: 2592), mu / dmu and A_0, dA_T, dA_0; it launches its
-    statistic's map and scan, adjoint and d mu sum besides the five kernels."""
+    statistic's map and scan, the adjoint's chunk maps, scan and gradients and the
+    d mu sum besides the five kernels."""
     wl = W.WORKLOADS["pgdn_bf16"]
     ht = wl.B * wl.T * wl.H
     per_bh = 3 * 128 * 128 * 4 + 3 * 128 * 4
     assert bench.bwd_bytes(wl, "pgdn") == ht * 2592 + wl.B * wl.H * per_bh + 2 * wl.H * 4
-    assert bench.bwd_kernels_per_call("kla") == 5 and bench.bwd_kernels_per_call("pgdn") == 9
+    assert bench.bwd_kernels_per_call("kla") == 5 and bench.bwd_kernels_per_call("pgdn") == 11
 
 
 def test_backward_bytes_and_kernel_counts_per_channel_decay():
@@ -221,7 +222,7 @@ def test_backward_bytes_and_kernel_counts_per_channel_decay():
     assert bench.bwd_bytes(ikdn, "ikdn") == (ht(ikdn) * (base + 2 * 520) + S3(ikdn)
                                              + 3 * ikdn.B * ikdn.H * 4)
     k = bench.bwd_kernels_per_call
-    assert k("kda", 4, 16) == 5 and k("ikdn", 4, 16) == 6 and k("pkda", 4, 16) == 7
+    assert k("kda", 4, 16) == 5 and k("ikdn", 4, 16) == 8 and k("pkda", 4, 16) == 9
     assert k("kdn", 4, 16, 152) == 8 and k("kdn", 1, 2, 152) == 10
     assert set(bench.bwd_grad_names("kdn")) == {"dq", "dk", "dv", "dlog_alpha", "dS0", "domega",
                                                  "dr"}
