@@ -27,12 +27,13 @@
 // PGDN's write vector w = eta B(A) . k^ comes from the key statistic A_t =
 // alphaP A_{t-1} + betaP k^.k^ (PDN notes Eq. (9)): the chunk part collects
 // dL/dw with the record's explicit write keys in place of eta k^, and
-// `pgdn_gain_bwd` carries the statistic's adjoint dA backwards over the whole
-// row (dA_{t-1} = alphaP_t dA_t plus each token's own term through B),
-// giving the gradients of k^, beta, alphaP, betaP, mu and A_0.
+// `pgdn_gain_bwd` carries the statistic's adjoint dA backwards (dA_{t-1} =
+// alphaP_t dA_t plus each token's own term through B: affine per chunk, so each
+// chunk's map, a scan over the row's chunks, then every chunk at once), giving
+// the gradients of k^, beta, alphaP, betaP, mu and A_0.
 //
 // Kernels (after the forward's prep and carry, which saves S_c and E per chunk):
-//   bwd_carry   one CTA per (b, h, 32 columns of dv), chunks in reverse: dE, dR
+//   bwd_carry   one CTA per (b, h, 64 columns of dv), chunks in reverse: dE, dR
 //               (written as dV) and dS_c on TF32x3 warp-level tensor-core products,
 //               saving dS = dL/dS_{c+1} per chunk.
 //   bwd_state   one CTA per (b, h, chunk): dO S_c^T, dR S_c^T, E dS^T, dO E^T, dR E^T.
@@ -52,6 +53,15 @@ namespace {
 using namespace tc;
 
 constexpr int kBwdThreads = 256;
+constexpr uint64_t kWait = 2000000000ull;   // 2 s per bounded wait
+
+int bwd_sm_count() {
+  static int count[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!count[dev]) cudaDeviceGetAttribute(&count[dev], cudaDevAttrMultiProcessorCount, dev);
+  return count[dev];
+}
 // The workspace: the forward's chunk records, then per record the saved state, E,
 // dS_{c+1}, E dS^T, dO E^T, dR E^T and gamma <dS, S_c> (one array each, record-major)
 constexpr size_t kRecF = 66560;                 // the forward's GDN / KLA chunk record (tc_split)
@@ -69,8 +79,9 @@ constexpr uint32_t rWpPC = 16384, rQPC = 66560, rWbPC = 99328, rP0PC = 134144;
 // workspace layouts: scalar decay (GDN, KLA), PGDN (+ dL/dw, key norms, d mu
 // parts), per-channel decay (KDA: + the forward's write vectors, dG per channel),
 // Diagonal KDN (+ dL/dw)
-// (BW_GAIN: Diagonal KDN, PKDA, isotropic KDN, whose gain kernels take dL/dw; PKDA
-// also each row's part of dL/dmu)
+// (BW_GAIN: Diagonal KDN, PKDA, isotropic KDN, whose gain kernels take dL/dw, each
+// chunk's affine map of the gain adjoint and its value at the chunk's end; PKDA
+// also each chunk's part of dL/dmu)
 enum { BW_SCALAR = 0, BW_PGDN = 1, BW_PC = 2, BW_GAIN = 3 };
 inline int bwd_mode(int variant) {
   if (variant == DR_PGDN) return BW_PGDN;
@@ -90,10 +101,10 @@ struct BwdWs {
   float* SS;      // [n]            gamma <dS, S_c>  (per-channel decay: [n][128])
   float* DW;      // PGDN, KDN [n][64][128]  dL/dw
   float* CR;      // PGDN [n][64]       key-norm factors
-  float* MU;      // PGDN [B H]         each row's part of dL/dmu
+  float* MU;      // PGDN / PKDA [n]     each chunk's part of dL/dmu
   float* Wf;      // per-channel decay [n][64][128]  the forward's write vectors
-  float* GM;      // gain variants [n][2][128]  each chunk's affine map of the gain adjoint
-  float* GE;      // gain variants [n][128]     the gain adjoint at each chunk's end
+  float* GM;      // gain variants and PGDN [n][2][128]  each chunk's affine map of the gain adjoint
+  float* GE;      // gain variants and PGDN [n][128]     the gain adjoint at each chunk's end
   size_t recb;    // bytes of one forward record
 };
 
@@ -221,11 +232,14 @@ __device__ __forceinline__ long tok(const FwdArgs& a, int b, int t, int h) {
 }
 
 // ================================================================= bwd_carry
+// A CTA carries one half of dS's columns (kNV = 64) for one (b, h): 2 B H CTAs,
+// one per SM, so up to 76 rows run in a single wave.
+constexpr int kNV = 64;       // dS columns per CTA
 constexpr int cLD64T = 72;    // 64-wide tiles read transposed (A operand, TA)
 constexpr int cLDW = 132;     // 128-wide, read as A (non-transposed)
 constexpr int cLDQ = 136;     // 128-wide, read transposed
-constexpr int cLDN = 40;      // 32-wide B operands
-constexpr int kCarrySmemF = 2 * 64 * cLD64T + 64 * cLDW + 2 * 64 * cLDQ + 3 * 64 * cLDN + 128 * cLDN;
+constexpr int cLDN = kNV + 8; // kNV-wide B operands
+constexpr int kCarrySmemF = 2 * 64 * cLD64T + 64 * cLDW + 2 * 64 * cLDQ + 2 * 64 * cLDN + 128 * cLDN;
 
 struct BwdArgs {
   const void* d_out;         // [B,T,H,dv] bf16
@@ -259,27 +273,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   float* sQg = sWb + 64 * cLDW;          // (Gamma.Q^) [j][c]
   float* sKg = sQg + 64 * cLDQ;          // (Gamma.K^) [j][c]
   float* sdO = sKg + 64 * cLDQ;          // dO [i][n]
-  float* sdE = sdO + 64 * cLDN;
-  float* sdR = sdE + 64 * cLDN;
-  float* sdS = sdR + 64 * cLDN;          // dS [c][n]
+  float* sdE = sdO + 64 * cLDN;          // dE [i][n], then (scalar decay) dR
+  float* sdS = sdE + 64 * cLDN;          // dS [c][n]
   __shared__ float s_gamma;
   __shared__ float s_gam[PC ? 128 : 1];   // per-channel decay: gamma of each state row
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x >> 2, cb = blockIdx.x & 3;
+  const int bh = blockIdx.x >> 1, cb = blockIdx.x & 1;
+  const int n0 = kNV * cb;               // this CTA's first dS column
   const int b = bh / a.H, h = bh % a.H;
   const int NC = (a.T + 63) / 64;
   const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
   const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(a.q);
   const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(g.d_out);
 
-  for (int e = tid; e < 128 * 32; e += kBwdThreads) {
-    const int r = e >> 5, n = e & 31;
-    sdS[r * cLDN + n] = g.dS_final ? g.dS_final[((size_t)bh * 128 + r) * 128 + 32 * cb + n] : 0.f;
+  for (int e = tid; e < 128 * kNV; e += kBwdThreads) {
+    const int r = e / kNV, n = e % kNV;
+    sdS[r * cLDN + n] = g.dS_final ? g.dS_final[((size_t)bh * 128 + r) * 128 + n0 + n] : 0.f;
   }
   // The next chunk's raw operands (P and T tile images, K and Q rows, dO, the
   // record's row vectors) are fetched into registers while this chunk computes.
-  uint4 rPT[2][4], rK[4], rQ[4], rO, rWh[PG ? 4 : 1], rWl[PG ? 4 : 1];
+  uint4 rPT[2][4], rK[4], rQ[4], rO[2], rWh[PG ? 4 : 1], rWl[PG ? 4 : 1];
   float rU[4], rEq[4], rEk[4], rG = 0.f;
   auto fetch = [&](int c) {
     const uint8_t* rec = g.w.rec + ((size_t)bh * NC + c) * g.w.recb;
@@ -311,10 +325,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       rEq[r] = rv[j];
       rEk[r] = rv[192 + j];
     }
-    {
-      const int i = tid >> 2, c0 = 8 * (tid & 3);
-      rO = i < Cc ? *reinterpret_cast<const uint4*>(dO + tok(a, b, t0 + i, h) * 128 + 32 * cb + c0)
-                  : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int e = tid + r * kBwdThreads, i = e >> 3, c0 = 8 * (e & 7);
+      rO[r] = i < Cc ? *reinterpret_cast<const uint4*>(dO + tok(a, b, t0 + i, h) * 128 + n0 + c0)
+                     : make_uint4(0u, 0u, 0u, 0u);
     }
     if (tid == 0) rG = rv[128];
   };
@@ -325,9 +340,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();   // the previous chunk's readers of every buffer are done
     // ---- dS_{c+1} for the local gradients
     float* sv = g.w.dS + ri * 16384;
-    for (int e = tid; e < 128 * 32; e += kBwdThreads) {
-      const int r = e >> 5, n = e & 31;
-      sv[r * 128 + 32 * cb + n] = sdS[r * cLDN + n];
+    for (int e = tid; e < 128 * kNV / 4; e += kBwdThreads) {
+      const int r = e / (kNV / 4), n = 4 * (e % (kNV / 4));
+      *reinterpret_cast<float4*>(sv + r * 128 + n0 + n) =
+          *reinterpret_cast<const float4*>(sdS + r * cLDN + n);
     }
     // ---- operands from the registers: P and T (hi + lo), K and Q rows scaled, dO
 #pragma unroll
@@ -395,45 +411,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         sQg[j * cLDQ + c0 + q] = rEq[r] * qf[q];
       }
     }
-    {
-      const int i = tid >> 2, c0 = 8 * (tid & 3);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int e = tid + r * kBwdThreads, i = e >> 3, c0 = 8 * (e & 7);
       float f[8];
-      unpack8(rO, f);
+      unpack8(rO[r], f);
 #pragma unroll
       for (int q = 0; q < 8; ++q) sdO[i * cLDN + c0 + q] = f[q];
     }
     if (tid == 0) s_gamma = rG;
     if (c > 0) fetch(c - 1);
     __syncthreads();
-    // warps 0-3: row tile `warp` of dE / dR (all 32 columns); the dS rows below
-    // are spread over all eight warps
-    if (warp < 4) {
+    // dE and dR: warp w takes row tile w & 3 and the 32 columns from 32 (w >> 2); the
+    // dS rows below are a row tile per warp
+    const int rt = 16 * (warp & 3), cq = 32 * (warp >> 2);
+    {
       float d[4][4] = {};
-      mm3x<4, 8, true, false>(d, sP + 16 * warp, cLD64T, sdO, cLDN, lane);
-      mm3x<4, 16, false, false>(d, sWb + 16 * warp * cLDW, cLDW, sdS, cLDN, lane);
+      mm3x<4, 8, true, false>(d, sP + rt, cLD64T, sdO + cq, cLDN, lane);
+      mm3x<4, 16, false, false>(d, sWb + rt * cLDW, cLDW, sdS + cq, cLDN, lane);
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          sdE[(16 * warp + frag_row(lane, e)) * cLDN + 8 * nt + frag_col(lane, e)] = d[nt][e];
+          sdE[(rt + frag_row(lane, e)) * cLDN + cq + 8 * nt + frag_col(lane, e)] = d[nt][e];
     }
     __syncthreads();
-    // ---- dR = T^T dE, also dV
-    if (warp < 4) {
+    // ---- dR = T^T dE, also dV (scalar decay: dR replaces dE once every warp has read it)
+    {
       float d[4][4] = {};
-      mm3x<4, 8, true, false>(d, sT + 16 * warp, cLD64T, sdE, cLDN, lane);
+      mm3x<4, 8, true, false>(d, sT + rt, cLD64T, sdE + cq, cLDN, lane);
+      if (!PC) __syncthreads();
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int i = 16 * warp + frag_row(lane, e), n = 8 * nt + frag_col(lane, e);
-          sdR[i * cLDN + n] = d[nt][e];
-          if (i < Cc) g.dv[tok(a, b, t0 + i, h) * 128 + 32 * cb + n] = d[nt][e];
+          const int i = rt + frag_row(lane, e), n = cq + 8 * nt + frag_col(lane, e);
+          if (!PC) sdE[i * cLDN + n] = d[nt][e];
+          if (i < Cc) g.dv[tok(a, b, t0 + i, h) * 128 + n0 + n] = d[nt][e];
         }
     }
     __syncthreads();
-    // ---- dS_c = gamma dS + (Gamma.Q^)^T dO - (Gamma.K^)^T dR (warp: rows 16 warp .. + 16)
-    {
+    // ---- dS_c = gamma dS + (Gamma.Q^)^T dO - (Gamma.K^)^T dR (per-channel decay:
+    // (T Gamma.K)^T dE), warp: rows 16 warp .. + 16, 32 columns at a time
+#pragma unroll 1
+    for (int n32 = 0; n32 < kNV; n32 += 32) {
       const float gam = s_gamma;
       float d[4][4], m[4][4] = {};
 #pragma unroll
@@ -441,173 +462,258 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int row = 16 * warp + frag_row(lane, e);
-          d[nt][e] = (PC ? s_gam[row] : gam) * sdS[row * cLDN + 8 * nt + frag_col(lane, e)];
+          d[nt][e] = (PC ? s_gam[row] : gam) * sdS[row * cLDN + n32 + 8 * nt + frag_col(lane, e)];
         }
-      mm3x<4, 8, true, false>(d, sQg + 16 * warp, cLDQ, sdO, cLDN, lane);
-      mm3x<4, 8, true, false>(m, sKg + 16 * warp, cLDQ, PC ? sdE : sdR, cLDN, lane);
+      mm3x<4, 8, true, false>(d, sQg + 16 * warp, cLDQ, sdO + n32, cLDN, lane);
+      mm3x<4, 8, true, false>(m, sKg + 16 * warp, cLDQ, sdE + n32, cLDN, lane);
       __syncwarp();
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          sdS[(16 * warp + frag_row(lane, e)) * cLDN + 8 * nt + frag_col(lane, e)] =
+          sdS[(16 * warp + frag_row(lane, e)) * cLDN + n32 + 8 * nt + frag_col(lane, e)] =
               d[nt][e] - m[nt][e];
     }
   }
   __syncthreads();
   if (g.dS0) {
-    for (int e = tid; e < 128 * 32; e += kBwdThreads) {
-      const int r = e >> 5, n = e & 31;
-      g.dS0[((size_t)bh * 128 + r) * 128 + 32 * cb + n] = sdS[r * cLDN + n];
+    for (int e = tid; e < 128 * kNV; e += kBwdThreads) {
+      const int r = e / kNV, n = e % kNV;
+      g.dS0[((size_t)bh * 128 + r) * 128 + n0 + n] = sdS[r * cLDN + n];
     }
   }
 }
 
 // ================================================================= bwd_state
-constexpr int cLDS = 132;   // 128-wide fp32 rows (A non-transposed / B transposed)
-constexpr int kStateSmemF = 128 * cLDS + 3 * 64 * cLDS;
+// Per chunk, five products over the dv index v (all fp32 data, K = 128):
+//   X_Q = dO S_c^T, X_K = dR S_c^T (64 x 128, raw dq / dk for bwd_local),
+//   dO E^T, dR E^T (64 x 64) and X_W = E dS^T (64 x 128),
+// plus gamma <dS, S_c> (per-channel decay: per state row).  On tcgen05 (M = 128,
+// fp32 in TMEM) as three MMA groups on bf16 hi/lo images (hi.hi + lo.hi + hi.lo):
+//   G1  A = [dO ; dR] (128 rows),  B = S_c (128 rows)  -> D1 = [X_Q ; X_K]
+//   G2  A = [dO ; dR],             B = E (64 rows)     -> D2 = [dO E^T ; dR E^T]
+//   G3  A = dS (128 rows),         B = E               -> D3 = X_W^T
+// (dO is bf16, so its lo rows are zero).  A persistent CTA of 16 warps per SM
+// takes tasks (b, h, chunk) in turn: the fp32 blocks are read with coalesced
+// 16-byte loads and split into 128B-swizzled K-major images, G1 and G2 run while
+// dS is read (and <dS, S_c> formed from registers), dS's image replaces S_c's
+// once G1 is done, and the readouts of D1 / D2 overlap G3.
+constexpr int kStateThreads = 512;
+constexpr uint32_t sAh = 0;           // [dO ; dR] hi, 2 k-blocks x 128 rows x 128 B
+constexpr uint32_t sAl = 32768;       // [0 ; dR] lo
+constexpr uint32_t sBh = 65536;       // S_c hi, then dS hi
+constexpr uint32_t sBl = 98304;       // S_c lo, then dS lo
+constexpr uint32_t sEh = 131072;      // E hi, 2 k-blocks x 64 rows x 128 B
+constexpr uint32_t sEl = 147456;      // E lo
+constexpr uint32_t kStateSmem = 163840 + 1024;
+constexpr uint32_t tD1 = 0, tD2 = 128, tD3 = 192, kStateTmem = 256;
+constexpr uint32_t I_S128 = idesc_bf16(128, 128, 0, 0);
+constexpr uint32_t I_S64 = idesc_bf16(128, 64, 0, 0);
 
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    bwd_state_kernel(FwdArgs a, BwdArgs g) {
-  extern __shared__ __align__(16) float smf[];
-  float* sS = smf;                 // S_c [c][v], then dS_{c+1} [c][v]
-  float* sdO = sS + 128 * cLDS;    // dO [i][v]
-  float* sdR = sdO + 64 * cLDS;    // dR [i][v]
-  float* sE = sdR + 64 * cLDS;     // E [j][v]
-  __shared__ float s_red[kBwdThreads / 32];
+// 4 fp32 -> bf16 hi (8 bytes) and lo (8 bytes) at a swizzled K-major position
+__device__ __forceinline__ void put4(uint8_t* hi, uint8_t* lo, uint32_t off, const float4& x) {
+  const float f[4] = {x.x, x.y, x.z, x.w};
+  uint32_t h[2], l[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    h[i] = pack_bf16(f[2 * i], f[2 * i + 1]);
+    l[i] = pack_bf16(f[2 * i] - __uint_as_float(h[i] << 16),
+                     f[2 * i + 1] - __uint_as_float(h[i] & 0xFFFF0000u));
+  }
+  *reinterpret_cast<uint2*>(hi + off) = make_uint2(h[0], h[1]);
+  *reinterpret_cast<uint2*>(lo + off) = make_uint2(l[0], l[1]);
+}
 
+__global__ void __launch_bounds__(kStateThreads, 1)
+    bwd_state_kernel(FwdArgs a, BwdArgs g, long n) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t bars[2];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ float s_red[kStateThreads / 32];
+  __shared__ volatile int s_abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NC = (a.T + 63) / 64;
-  const long task = blockIdx.x;
-  const int bh = (int)(task / NC), c = (int)(task % NC);
-  const int b = bh / a.H, h = bh % a.H;
-  const int t0 = 64 * c, Cc = min(64, a.T - t0);
-  const float* Sc = g.w.S + (size_t)task * 16384;
-  const float* Ec = g.w.E + (size_t)task * 8192;
-  const float* dSc = g.w.dS + (size_t)task * 16384;
+  const bool pc = a.variant == DR_KDA || a.variant == DR_KDN || a.variant == DR_PKDA ||
+                  a.variant == DR_IKDN;
   const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(g.d_out);
+  // this thread's 4 columns of v in every 128-wide row: k-block and swizzled column
+  const uint32_t kb = lane >> 4, col = 4 * (lane & 15);
 
-  {   // dO rows (bf16) into registers first, the fp32 blocks by asynchronous copies
-    uint4 raw[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int e = tid + r * kBwdThreads, i = e >> 4, c0 = 8 * (e & 15);
-      raw[r] = i < Cc ? *reinterpret_cast<const uint4*>(dO + tok(a, b, t0 + i, h) * 128 + c0)
-                      : make_uint4(0u, 0u, 0u, 0u);
-    }
-    for (int e = tid; e < 128 * 32; e += kBwdThreads) {
-      const int r = e >> 5, c4 = 4 * (e & 31);
-      cpa16(sS + r * cLDS + c4, Sc + r * 128 + c4);
-    }
-    for (int e = tid; e < 64 * 32; e += kBwdThreads) {
-      const int i = e >> 5, c4 = 4 * (e & 31);
-      cpa16(sdR + i * cLDS + c4, g.dv + tok(a, b, t0 + min(i, Cc - 1), h) * 128 + c4,
-            i < Cc ? 16 : 0);
-      cpa16(sE + i * cLDS + c4, Ec + i * 128 + c4);
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int e = tid + r * kBwdThreads, i = e >> 4, c0 = 8 * (e & 15);
-      float f[8];
-      unpack8(raw[r], f);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) sdO[i * cLDS + c0 + q] = f[q];
-    }
-    cpa_wait_all();
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+    s_abort = 0;
   }
+  if (warp == 0) tmem_alloc(&tmem_base_s, kStateTmem);
+  for (int e = tid; e < 64 * 16; e += kStateThreads) {   // the dO rows' lo image: zero
+    const int r = e >> 4, c = e & 15;
+    *reinterpret_cast<uint4*>(sm + sAl + (c >> 3) * 16384 + r * 128 + (c & 7) * 16) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+  tc_fence_before();
   __syncthreads();
-  // X_Q = dO S_c^T -> dq, X_K = dR S_c^T -> dk (raw; bwd_local scales and adds)
-  // 64 x 128 each: 64 tiles, eight per warp (m tile = warp & 3, n tiles 8 (warp >> 2) .. + 8)
-  {
-    const int mt = warp & 3;
-    for (int s = 0; s < 2; ++s) {
-      const int nt0 = 8 * (warp >> 2) + 4 * s;
-      float dq4[4][4] = {}, dk4[4][4] = {};
-      mm3x<4, 16, false, true>(dq4, sdO + 16 * mt * cLDS, cLDS, sS + 8 * nt0 * cLDS, cLDS, lane);
-      mm3x<4, 16, false, true>(dk4, sdR + 16 * mt * cLDS, cLDS, sS + 8 * nt0 * cLDS, cLDS, lane);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = 16 * mt + frag_row(lane, e), n = 8 * (nt0 + j) + frag_col(lane, e);
-          if (i < Cc) {
-            g.dq[tok(a, b, t0 + i, h) * 128 + n] = dq4[j][e];
-            g.dk[tok(a, b, t0 + i, h) * 128 + n] = dk4[j][e];
-          }
-        }
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  const uint32_t a_h = smem_u32(sm + sAh), a_l = smem_u32(sm + sAl);
+  const uint32_t b_h = smem_u32(sm + sBh), b_l = smem_u32(sm + sBl);
+  const uint32_t e_h = smem_u32(sm + sEh), e_l = smem_u32(sm + sEl);
+  int it = 0, n1 = 0, n2 = 0;   // tasks done; groups committed (thread 0)
+
+  for (long task = blockIdx.x; task < n; task += gridDim.x, ++it) {
+    const int bh = (int)(task / NC), c = (int)(task % NC);
+    const int b = bh / a.H, h = bh % a.H;
+    const int t0 = 64 * c, Cc = min(64, a.T - t0);
+    const float* Sc = g.w.S + (size_t)task * 16384;
+    const float* Ec = g.w.E + (size_t)task * 8192;
+    const float* dSc = g.w.dS + (size_t)task * 16384;
+    // ---- images: dO (bf16, copied as is), dR, S_c and E (hi / lo)
+    for (int e = tid; e < 64 * 16; e += kStateThreads) {
+      const int r = e >> 4, cc = e & 15;
+      cpa16(sm + sAh + (cc >> 3) * 16384 + sw128_offset(r, 8 * (cc & 7)),
+            dO + tok(a, b, t0 + min(r, Cc - 1), h) * 128 + 8 * cc, r < Cc ? 16 : 0);
     }
-  }
-  // dP = dO E^T and dR E^T (64 x 64: 32 tiles, four per warp)
-  {
-    float* xp = g.w.dP + (size_t)task * 4096;
-    float* xl = g.w.dL + (size_t)task * 4096;
-    const int mt = warp & 3, nt0 = 4 * (warp >> 2);
-    float p4[4][4] = {}, l4[4][4] = {};
-    mm3x<4, 16, false, true>(p4, sdO + 16 * mt * cLDS, cLDS, sE + 8 * nt0 * cLDS, cLDS, lane);
-    mm3x<4, 16, false, true>(l4, sdR + 16 * mt * cLDS, cLDS, sE + 8 * nt0 * cLDS, cLDS, lane);
+    float4 sv[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+    for (int j = 0; j < 8; ++j)
+      sv[j] = *reinterpret_cast<const float4*>(Sc + (16 * j + warp) * 128 + 4 * lane);
+    {
+      float4 ev[4], rv[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = 16 * mt + frag_row(lane, e), j = 8 * (nt0 + q) + frag_col(lane, e);
-        xp[i * 64 + j] = p4[q][e];
-        xl[i * 64 + j] = l4[q][e];
+      for (int j = 0; j < 4; ++j) {
+        const int r = 16 * j + warp;
+        ev[j] = *reinterpret_cast<const float4*>(Ec + r * 128 + 4 * lane);
+        rv[j] = r < Cc ? *reinterpret_cast<const float4*>(g.dv + tok(a, b, t0 + r, h) * 128 + 4 * lane)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-  }
-  __syncthreads();
-  // dS_{c+1} over the dO and dR rows (both read by now); gamma <dS, S_c>
-  float* sD = sdO;                 // [128][cLDS]: the dO and dR buffers, contiguous
-  for (int e = tid; e < 128 * 32; e += kBwdThreads) {
-    const int r = e >> 5, c4 = 4 * (e & 31);
-    cpa16(sD + r * cLDS + c4, dSc + r * 128 + c4);
-  }
-  cpa_wait_all();
-  __syncthreads();
-  if (a.variant == DR_KDA || a.variant == DR_KDN || a.variant == DR_PKDA || a.variant == DR_IKDN) {
-    // per-channel decay: gamma_c <dS_c, S_c>
-    const float* gam = reinterpret_cast<const float*>(g.w.rec + (size_t)task * g.w.recb + rVecF) + 128;
-    for (int rr = 0; rr < 16; ++rr) {
-      const int r = 16 * warp + rr;
-      const float4 x = *reinterpret_cast<const float4*>(sD + r * cLDS + 4 * lane);
-      const float4 y = *reinterpret_cast<const float4*>(sS + r * cLDS + 4 * lane);
-      const float p = warp_sum(x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w);
-      if (lane == 0) g.w.SS[(size_t)task * 128 + r] = gam[r] * p;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = 16 * j + warp;
+        put4(sm + sEh + kb * 8192, sm + sEl + kb * 8192, sw128_offset(r, col), ev[j]);
+        put4(sm + sAh + kb * 16384, sm + sAl + kb * 16384, sw128_offset(64 + r, col), rv[j]);
+      }
     }
-  } else {
-    float part = 0.f;
-    for (int e = tid; e < 128 * 32; e += kBwdThreads) {
-      const int r = e >> 5, c4 = 4 * (e & 31);
-      const float4 x = *reinterpret_cast<const float4*>(sD + r * cLDS + c4);
-      const float4 y = *reinterpret_cast<const float4*>(sS + r * cLDS + c4);
-      part += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
-    }
-    part = warp_sum(part);
-    if (lane == 0) s_red[warp] = part;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      put4(sm + sBh + kb * 16384, sm + sBl + kb * 16384, sw128_offset(16 * j + warp, col), sv[j]);
+    cpa_wait_all();
+    fence_proxy_async();
     __syncthreads();
-    if (tid == 0) {
+    if (tid == 0) {   // G1 and G2
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32, oe = (ks >> 2) * 8192 + (ks & 3) * 32;
+        const uint64_t ah = desc_sw128(a_h + o, 16, 1024), al = desc_sw128(a_l + o, 16, 1024);
+        const uint64_t bh_ = desc_sw128(b_h + o, 16, 1024), bl = desc_sw128(b_l + o, 16, 1024);
+        const uint64_t eh = desc_sw128(e_h + oe, 16, 1024), el = desc_sw128(e_l + oe, 16, 1024);
+        mma_bf16(tmem + tD1, ah, bh_, I_S128, ks > 0);
+        mma_bf16(tmem + tD1, al, bh_, I_S128, true);
+        mma_bf16(tmem + tD1, ah, bl, I_S128, true);
+        mma_bf16(tmem + tD2, ah, eh, I_S64, ks > 0);
+        mma_bf16(tmem + tD2, al, eh, I_S64, true);
+        mma_bf16(tmem + tD2, ah, el, I_S64, true);
+      }
+      mma_commit(&bars[0]);
+      ++n1;
+    }
+    // ---- dS into registers; gamma <dS, S_c> from the S_c values already held
+    float4 dv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      dv[j] = *reinterpret_cast<const float4*>(dSc + (16 * j + warp) * 128 + 4 * lane);
+    const float* rvec = reinterpret_cast<const float*>(g.w.rec + (size_t)task * g.w.recb + rVecF);
+    float part = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float p = dv[j].x * sv[j].x + dv[j].y * sv[j].y + dv[j].z * sv[j].z + dv[j].w * sv[j].w;
+      if (pc) {
+        p = warp_sum(p);
+        if (lane == 0) g.w.SS[(size_t)task * 128 + 16 * j + warp] = rvec[128 + 16 * j + warp] * p;
+      } else {
+        part += p;
+      }
+    }
+    if (!pc) {
+      part = warp_sum(part);
+      if (lane == 0) s_red[warp] = part;
+    }
+    if (!mbar_wait(&bars[0], it & 1, kWait)) s_abort = 1;
+    __syncthreads();
+    if (s_abort) break;
+    if (!pc && tid == 0) {
       float tsum = 0.f;
-      for (int w = 0; w < kBwdThreads / 32; ++w) tsum += s_red[w];
-      const float gam = reinterpret_cast<const float*>(g.w.rec + (size_t)task * g.w.recb + rVecF)[128];
-      g.w.SS[task] = gam * tsum;
+      for (int w = 0; w < kStateThreads / 32; ++w) tsum += s_red[w];
+      g.w.SS[task] = rvec[128] * tsum;
     }
-  }
-  // X_W = E dS^T
-  {
-    float* xw = g.w.XW + (size_t)task * 8192;
-    const int mt = warp & 3;
-    for (int s = 0; s < 2; ++s) {
-      const int nt0 = 8 * (warp >> 2) + 4 * s;
-      float w4[4][4] = {};
-      mm3x<4, 16, false, true>(w4, sE + 16 * mt * cLDS, cLDS, sD + 8 * nt0 * cLDS, cLDS, lane);
+    // ---- dS's image over S_c's (G1 has read it), then G3
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < 8; ++j)
+      put4(sm + sBh + kb * 16384, sm + sBl + kb * 16384, sw128_offset(16 * j + warp, col), dv[j]);
+    fence_proxy_async();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = 16 * mt + frag_row(lane, e), n = 8 * (nt0 + j) + frag_col(lane, e);
-          xw[i * 128 + n] = w4[j][e];
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32, oe = (ks >> 2) * 8192 + (ks & 3) * 32;
+        const uint64_t dh = desc_sw128(b_h + o, 16, 1024), dl = desc_sw128(b_l + o, 16, 1024);
+        const uint64_t eh = desc_sw128(e_h + oe, 16, 1024), el = desc_sw128(e_l + oe, 16, 1024);
+        mma_bf16(tmem + tD3, dh, eh, I_S64, ks > 0);
+        mma_bf16(tmem + tD3, dl, eh, I_S64, true);
+        mma_bf16(tmem + tD3, dh, el, I_S64, true);
+      }
+      mma_commit(&bars[1]);
+      ++n2;
+    }
+    // ---- D1, D2 out: warp (quadrant q, column quarter cq); lane = TMEM row
+    const int q = warp & 3, cq = warp >> 2, row = 32 * q + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+    const int i = row & 63;
+    {
+      float x[16], y[16], z[16];
+      tmem_ld16(tl + tD1 + 32 * cq, x);
+      tmem_ld16(tl + tD1 + 32 * cq + 16, y);
+      tmem_ld16(tl + tD2 + 16 * cq, z);
+      tmem_ld_wait();
+      if (i < Cc) {
+        float* dst = (row < 64 ? g.dq : g.dk) + tok(a, b, t0 + i, h) * 128 + 32 * cq;
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          *reinterpret_cast<float4*>(dst + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+          *reinterpret_cast<float4*>(dst + 16 + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
         }
+      }
+      float* xd = (row < 64 ? g.w.dP : g.w.dL) + (size_t)task * 4096 + i * 64 + 16 * cq;
+#pragma unroll
+      for (int e = 0; e < 16; e += 4)
+        *reinterpret_cast<float4*>(xd + e) = make_float4(z[e], z[e + 1], z[e + 2], z[e + 3]);
     }
+    if (!mbar_wait(&bars[1], it & 1, kWait)) s_abort = 1;
+    __syncthreads();
+    if (s_abort) break;
+    tc_fence_after();
+    {   // D3 = X_W^T: lane = state row n, column = token j -> X_W[j][n] (coalesced in n)
+      float z[16];
+      tmem_ld16(tl + tD3 + 16 * cq, z);
+      tmem_ld_wait();
+      float* xw = g.w.XW + (size_t)task * 8192 + row;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) xw[(16 * cq + e) * 128] = z[e];
+    }
+    tc_fence_before();
+    __syncthreads();   // TMEM read and every image consumed before the next task
   }
+  if (s_abort && tid == 0) {   // drain: no MMA may still write TMEM after the dealloc
+    set_status(DR_ERR_TIMEOUT);
+    if (n1 > 0) mbar_wait(&bars[0], (n1 - 1) & 1, kWait / 4);
+    if (n2 > 0) mbar_wait(&bars[1], (n2 - 1) & 1, kWait / 4);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kStateTmem);
 }
 
 // ================================================================= bwd_local
@@ -1254,14 +1360,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // PHASE 1 (every chunk at once) runs the chunk backwards from it, writes the
 // gradients and the chunk's part of dL/dmu.
 constexpr int kGainSmemF = 4 * 64 * 128;
+constexpr int kGainMapSmemF = 3 * 64 * 128;   // PHASE 0 has no dL/dk^ buffer: two CTAs per SM
 
 template <bool PC, int PHASE>
-__global__ void __launch_bounds__(128, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
+__global__ void __launch_bounds__(128, 2) pgdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
   extern __shared__ __align__(16) float smf[];
   float* sK = smf;                  // k^ [t][i]
   float* sDW = sK + 64 * 128;       // dL/dw [t][i]
-  float* sDK = sDW + 64 * 128;      // dL/dk^ [t][i]: the memory part, then the total
-  float* sA = sDK + 64 * 128;       // A_t [t][i], then dA_t
+  float* sA = sDW + 64 * 128;       // A_t [t][i], then dA_t
+  float* sDK = sA + 64 * 128;       // dL/dk^ [t][i]: the memory part, then the total (PHASE 1)
   __shared__ float s_aP[64], s_bP[64], s_eta[64], s_cr[64], s_mu[4];
   const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
   const int NC = (a.T + 63) / 64;
@@ -1826,8 +1933,9 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
   if (pc) a.save_W = g.w.Wf;
   cudaError_t e = pc ? launch_kdn_split(a, DR_BF16, workspace, st) : launch_chunk_tc_split(a, workspace, st);
   if (e != cudaSuccess) return e;
-  const size_t c_smem = (size_t)kCarrySmemF * 4, s_smem = (size_t)kStateSmemF * 4,
-               l_smem = (size_t)kLocalSmemF * 4, p_smem = (size_t)kGainSmemF * 4;
+  const size_t c_smem = (size_t)kCarrySmemF * 4, s_smem = kStateSmem,
+               l_smem = (size_t)kLocalSmemF * 4, p_smem = (size_t)kGainSmemF * 4,
+               pm_smem = (size_t)kGainMapSmemF * 4;
   if ((e = cudaFuncSetAttribute(bwd_carry_kernel<false, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c_smem)) !=
           cudaSuccess ||
@@ -1851,13 +1959,13 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l_smem)) !=
           cudaSuccess ||
       (e = cudaFuncSetAttribute(pgdn_gain_bwd_kernel<false, 0>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p_smem)) !=
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pm_smem)) !=
           cudaSuccess ||
       (e = cudaFuncSetAttribute(pgdn_gain_bwd_kernel<false, 1>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p_smem)) !=
           cudaSuccess ||
       (e = cudaFuncSetAttribute(pgdn_gain_bwd_kernel<true, 0>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p_smem)) !=
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pm_smem)) !=
           cudaSuccess ||
       (e = cudaFuncSetAttribute(pgdn_gain_bwd_kernel<true, 1>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p_smem)) !=
@@ -1882,12 +1990,14 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
           cudaSuccess)
     return e;
   if (pg)
-    bwd_carry_kernel<true, false><<<fa.B * fa.H * 4, kBwdThreads, c_smem, st>>>(fa, g);
+    bwd_carry_kernel<true, false><<<fa.B * fa.H * 2, kBwdThreads, c_smem, st>>>(fa, g);
   else if (pc)
-    bwd_carry_kernel<false, true><<<fa.B * fa.H * 4, kBwdThreads, c_smem, st>>>(fa, g);
+    bwd_carry_kernel<false, true><<<fa.B * fa.H * 2, kBwdThreads, c_smem, st>>>(fa, g);
   else
-    bwd_carry_kernel<false, false><<<fa.B * fa.H * 4, kBwdThreads, c_smem, st>>>(fa, g);
-  bwd_state_kernel<<<(unsigned)n, kBwdThreads, s_smem, st>>>(fa, g);
+    bwd_carry_kernel<false, false><<<fa.B * fa.H * 2, kBwdThreads, c_smem, st>>>(fa, g);
+  const int nsm = bwd_sm_count();
+  if (nsm <= 0) return cudaErrorInvalidValue;
+  bwd_state_kernel<<<(unsigned)(n < nsm ? n : nsm), kStateThreads, s_smem, st>>>(fa, g, n);
   if (fa.variant == DR_KDA) {
     bwd_local_pc_kernel<DR_KDA><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
   } else if (fa.variant == DR_KDN) {
@@ -1897,7 +2007,7 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
     kdn_gain_bwd_kernel<1><<<(unsigned)n, 128, kKdnGainSmemF * 4, st>>>(fa, g);
   } else if (fa.variant == DR_PKDA) {
     bwd_local_pc_kernel<DR_PKDA><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
-    pgdn_gain_bwd_kernel<true, 0><<<(unsigned)n, 128, p_smem, st>>>(fa, g);
+    pgdn_gain_bwd_kernel<true, 0><<<(unsigned)n, 128, pm_smem, st>>>(fa, g);
     gain_scan_kernel<<<fa.B * fa.H, 128, 0, st>>>(fa, g, 128);
     pgdn_gain_bwd_kernel<true, 1><<<(unsigned)n, 128, p_smem, st>>>(fa, g);
     pgdn_dmu_kernel<<<(fa.H + 127) / 128, 128, 0, st>>>(fa, g);
@@ -1910,7 +2020,7 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
     bwd_local_kernel<DR_KLA><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
   } else if (pg) {
     bwd_local_kernel<DR_PGDN><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
-    pgdn_gain_bwd_kernel<false, 0><<<(unsigned)n, 128, p_smem, st>>>(fa, g);
+    pgdn_gain_bwd_kernel<false, 0><<<(unsigned)n, 128, pm_smem, st>>>(fa, g);
     gain_scan_kernel<<<fa.B * fa.H, 128, 0, st>>>(fa, g, 128);
     pgdn_gain_bwd_kernel<false, 1><<<(unsigned)n, 128, p_smem, st>>>(fa, g);
     pgdn_dmu_kernel<<<(fa.H + 127) / 128, 128, 0, st>>>(fa, g);
