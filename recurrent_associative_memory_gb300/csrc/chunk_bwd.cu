@@ -150,63 +150,61 @@ BwdWs bwd_ws(void* base, long n, int rows, int mode) {
   return w;
 }
 
-// ---- warp-level tensor-core products, fp32 operands split into two TF32 terms each
-// (hi + lo) and three products: fp32-accurate.
+// ---- warp-level tensor-core products on fp32 shared-memory operands: each value
+// split into bf16 hi + lo (x = hi + lo to ~2^-17 of |x|) and three m16n8k16
+// products hi.hi + lo.hi + hi.lo, accumulated in fp32.
 // A element (m, k) = TA ? A[k lda + m] : A[m lda + k];
 // B element (k, n) = TB ? B[n ldb + k] : B[k ldb + n].
 // NT tiles side by side: D_j (16 x 8) += op(A)[16 x 8K] op(B)[8K x 8] at B columns
-// 8 j .. 8 j + 8.  The A fragment is split once per k-step for all NT tiles, and each
-// tile keeps its three products in separate accumulators, so 3 NT independent chains
-// are in flight per warp.
+// 8 j .. 8 j + 8 (K = KSTEPS x 8, KSTEPS even).  The A fragment is split once per
+// k-step for all NT tiles, and each tile keeps its three products in separate
+// accumulators, so 3 NT independent chains are in flight per warp.  The fragment's
+// k slots (2t, 2t+1, 2t+8, 2t+9) of lane (g, t) hold k0 + t + (0, 4, 8, 12) in A
+// and B alike (a sum over k is order-free), so a lane reads the same
+// bank-conflict-free addresses as an 8-wide step per 8 of K.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32"
+      " {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// (x0, x1) -> packed bf16x2 hi = bf16(x) and lo = bf16(x - hi)
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(x0, x1);
+  lo = pack_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xFFFF0000u));
+}
+
 template <int NT, int KSTEPS, bool TA, bool TB>
 __device__ __forceinline__ void mm3x(float (&d)[NT][4], const float* A, int lda, const float* B,
                                      int ldb, int lane) {
+  static_assert(KSTEPS % 2 == 0, "K must be a multiple of 16");
   const int g = lane >> 2, t = lane & 3;
   float c1[NT][4], c2[NT][4];
 #pragma unroll
   for (int j = 0; j < NT; ++j)
 #pragma unroll
     for (int i = 0; i < 4; ++i) c1[j][i] = c2[j][i] = 0.f;
+  auto ae = [&](int m, int k) { return TA ? A[k * lda + m] : A[m * lda + k]; };
+  auto be = [&](int k, int n) { return TB ? B[n * ldb + k] : B[k * ldb + n]; };
 #pragma unroll 2
-  for (int ks = 0; ks < KSTEPS; ++ks) {
-    const int k0 = 8 * ks;
-    float af[4];
-    if (TA) {
-      af[0] = A[(k0 + t) * lda + g];
-      af[1] = A[(k0 + t) * lda + g + 8];
-      af[2] = A[(k0 + t + 4) * lda + g];
-      af[3] = A[(k0 + t + 4) * lda + g + 8];
-    } else {
-      af[0] = A[g * lda + k0 + t];
-      af[1] = A[(g + 8) * lda + k0 + t];
-      af[2] = A[g * lda + k0 + t + 4];
-      af[3] = A[(g + 8) * lda + k0 + t + 4];
-    }
+  for (int ks = 0; ks < KSTEPS / 2; ++ks) {
+    const int k0 = 16 * ks + t;
     uint32_t ah[4], al[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      ah[i] = to_tf32(af[i]);
-      al[i] = to_tf32(af[i] - __uint_as_float(ah[i]));
-    }
+    split2(ae(g, k0), ae(g, k0 + 4), ah[0], al[0]);
+    split2(ae(g + 8, k0), ae(g + 8, k0 + 4), ah[1], al[1]);
+    split2(ae(g, k0 + 8), ae(g, k0 + 12), ah[2], al[2]);
+    split2(ae(g + 8, k0 + 8), ae(g + 8, k0 + 12), ah[3], al[3]);
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      float bf[2];
-      if (TB) {
-        bf[0] = B[(8 * j + g) * ldb + k0 + t];
-        bf[1] = B[(8 * j + g) * ldb + k0 + t + 4];
-      } else {
-        bf[0] = B[(k0 + t) * ldb + 8 * j + g];
-        bf[1] = B[(k0 + t + 4) * ldb + 8 * j + g];
-      }
+      const int n = 8 * j + g;
       uint32_t bh[2], bl[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        bh[i] = to_tf32(bf[i]);
-        bl[i] = to_tf32(bf[i] - __uint_as_float(bh[i]));
-      }
-      mma_tf32(d[j], ah, bh);
-      mma_tf32(c1[j], al, bh);
-      mma_tf32(c2[j], ah, bl);
+      split2(be(k0, n), be(k0 + 4, n), bh[0], bl[0]);
+      split2(be(k0 + 8, n), be(k0 + 12, n), bh[1], bl[1]);
+      mma16816(d[j], ah, bh);
+      mma16816(c1[j], al, bh);
+      mma16816(c2[j], ah, bl);
     }
   }
 #pragma unroll
