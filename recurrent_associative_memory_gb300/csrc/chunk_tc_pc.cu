@@ -591,10 +591,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (I == J) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = w[e];
-        } else {
-          const float* F = fF + pair_index(I, J) * 128 + cc;
+        } else {   // two 16-byte loads (8 scalar loads of a channel vector conflict 4 ways)
+          const float4* F = reinterpret_cast<const float4*>(fF + pair_index(I, J) * 128 + cc);
+          const float4 f0 = F[0], f1 = F[1];
+          const float ff[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = w[e] * F[e];
+          for (int e = 0; e < 8; ++e) x[e] = w[e] * ff[e];
         }
         split8(x, hi, lo);
         const uint32_t off = sB + kb * kBBlk + sw128_offset(brow(I, j), c8);
@@ -677,8 +679,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; r < kUnits; ++r) {
       const int u = tid + r * kThreads, i = u >> 4, cg = u & 15, kb = cg >> 3, c8 = (cg & 7) * 8;
       const int cc = 64 * kb + c8;
-      const float* Em = fEm + (i >> 4) * 128 + cc;
-      const float* G3 = fGm + 3 * 128 + cc;
+      float Em[8], G3[8];
+      {
+        const float4* ep = reinterpret_cast<const float4*>(fEm + (i >> 4) * 128 + cc);
+        const float4* gp = reinterpret_cast<const float4*>(fGm + 3 * 128 + cc);
+        const float4 e0 = ep[0], e1 = ep[1], g0 = gp[0], g1 = gp[1];
+        Em[0] = e0.x; Em[1] = e0.y; Em[2] = e0.z; Em[3] = e0.w;
+        Em[4] = e1.x; Em[5] = e1.y; Em[6] = e1.z; Em[7] = e1.w;
+        G3[0] = g0.x; G3[1] = g0.y; G3[2] = g0.z; G3[3] = g0.w;
+        G3[4] = g1.x; G3[5] = g1.y; G3[6] = g1.z; G3[7] = g1.w;
+      }
       const uint32_t ok = sA + kb * 16384 + sw128_offset(i, c8);
       const uint32_t oq = sA + kb * 16384 + sw128_offset(64 + i, c8);
       const uint32_t ob = sB + kb * kBBlk + sw128_offset(brow(3, i), c8);
