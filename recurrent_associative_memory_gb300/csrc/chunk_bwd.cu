@@ -717,339 +717,411 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 // ================================================================= bwd_local
 constexpr int cLDK = 132;   // K^, Q^, W, staging [64][132]
 constexpr int cLDM = 68;    // M_P, M_L [64][68]
-constexpr int kLocalSmemF = 5 * 64 * cLDK + 2 * 64 * cLDM;
+// Scalar decay (GDN, KLA, PGDN): a persistent CTA per SM takes tasks (b, h, chunk).
+// The chunk's products run on tcgen05 (M = 128, fp32 in TMEM) over three bf16 hi/lo
+// images (hi.hi + lo.hi + hi.lo):
+//   IA = [Q^ ; K^] (128 rows i, K-major in c),  IW = W (64 rows j),
+//   IM = [M_P ; M_L] (128 rows i, K-major in j),  M_P = dP.D (j <= i),
+//   M_L = -dL.D (j < i), D_ij = e^{g_i - g_j},
+// and three MMA groups issued together:
+//   G1 = IA IW^T            -> [Q^ W^T ; K^ W^T]   (the Grams, for the decay terms)
+//   G2 = IA^T IM (MN-major) -> dw^T = Q^^T M_P + K^^T M_L   (lane = channel)
+//   G3 = IM IW  (MN-major)  -> [M_P W ; M_L W] = [dq^_P ; dk^_L]  (lane = token)
+// Every Gram entry X_ij = M_P,ij (Q^W^T)_ij + M_L,ij (K^W^T)_ij adds to dg_i and takes
+// from dg_j; dw = dw_G2 + e^{G-g} X_W; the rows then add e^g X_Q / -e^g X_K (the
+// raw dO S_c^T, dR S_c^T that bwd_state left in dq / dk), the write gain (GDN eta,
+// KLA eta / (s + eps)) and the norms; d log alpha is dg's reverse cumulative sum
+// with dG = gamma <dS, S_c> + sum_j e^{G-g_j} X_W,j . w_j on the chunk's last token.
+// PGDN takes W from the record's explicit write keys, keeps dL/dw and the memory
+// part of dL/dk^ (and the key norms) for pgdn_gain_bwd.
+constexpr uint32_t lA = 0;            // IA hi (2 k-blocks x 128 rows x 128 B) | lo at +32 KB
+constexpr uint32_t lW = 65536;        // IW hi (2 k-blocks x 64 rows) | lo at +16 KB
+constexpr uint32_t lM = 98304;        // IM hi (128 rows x 64 j) | lo at +16 KB
+constexpr uint32_t lD = 131072;       // fp32 dw [64 j][cLDK]
+constexpr uint32_t lX = lD + 64 * cLDK * 4;   // fp32 Gram terms X [64 i][65]
+constexpr uint32_t lR = lX + 64 * 65 * 4;     // raw k | q rows, bf16 [64][cKR] each
+constexpr int cKR = 136;
+constexpr uint32_t kLocalSmem = lR + 2 * 64 * cKR * 2 + 1024;
+constexpr uint32_t tG1 = 0, tG2 = 64, tG3 = 128, kLocalTmem = 256;
+constexpr uint32_t I_L1 = idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t I_L2 = idesc_bf16(128, 64, 1, 1);
+constexpr uint32_t I_L3 = idesc_bf16(128, 128, 0, 1);
 
 template <int VARIANT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-    bwd_local_kernel(FwdArgs a, BwdArgs g) {
+    bwd_local_kernel(FwdArgs a, BwdArgs g, long n) {
   constexpr bool PG = VARIANT == DR_PGDN;
-  extern __shared__ __align__(16) float smf[];
-  float* sK = smf;                 // k^ [j][c]
-  float* sQ = sK + 64 * cLDK;      // q^
-  float* sW = sQ + 64 * cLDK;      // w = beta k^
-  float* sX = sW + 64 * cLDK;      // staging of one product
-  float* sY = sX + 64 * cLDK;      // dw
-  float* sMP = sY + 64 * cLDK;     // (dP . D) [i][j]
-  float* sML = sMP + 64 * cLDM;    // (dL . D) [i][j]
-  __shared__ float s_g[64], s_cr[64], s_qn[64], s_beta[64], s_s[64], s_eta[64];
-  __shared__ float s_dg[64], s_dbeta[64], s_dGt[64];
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  float* sD = reinterpret_cast<float*>(sm + lD);
+  float* sX = reinterpret_cast<float*>(sm + lX);
+  uint16_t* sKr = reinterpret_cast<uint16_t*>(sm + lR);
+  uint16_t* sQr = sKr + 64 * cKR;
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int s_abort;
+  __shared__ float s_g[64], s_cr[64], s_qn[64], s_beta[64], s_s[64], s_eta[64], s_ew[64];
+  __shared__ float s_dgx[64], s_dgr[64], s_dgq[64], s_dgk[64], s_dbeta[64], s_dGt[64];
+  __shared__ float s_dot[2][128], s_xd[2][128], s_p1[4][64], s_p2[4][64];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NC = (a.T + 63) / 64;
-  const long task = blockIdx.x;
-  const int bh = (int)(task / NC), c = (int)(task % NC);
-  const int b = bh / a.H, h = bh % a.H;
-  const int t0 = 64 * c, Cc = min(64, a.T - t0);
   const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
   const __nv_bfloat16* Qp = static_cast<const __nv_bfloat16*>(a.q);
+  auto bf = [](uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); };
+  // element (row, col) of a bf16 hi/lo image with 128-byte rows (one 64-wide block)
+  auto hl = [&](uint32_t base, uint32_t lo_off, int row, int col) {
+    const uint32_t o = base + sw128_offset(row, col);
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + o)) +
+           __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + o + lo_off));
+  };
 
-  // ---- raw rows (bf16, all loads in flight first), dO E^T and dR E^T by
-  //      asynchronous copies into the M_P / M_L buffers, norms, gates
-  {
-    uint4 rk[4], rq[4];
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  if (warp == 0) tmem_alloc(&tmem_base_s, kLocalTmem);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  const int q4 = warp & 3, hc = warp >> 2, trow = 32 * q4 + lane;
+  const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+  int it = 0, nc = 0;
+
+  for (long task = blockIdx.x; task < n; task += gridDim.x, ++it) {
+    const int bh = (int)(task / NC), c = (int)(task % NC);
+    const int b = bh / a.H, h = bh % a.H;
+    const int t0 = 64 * c, Cc = min(64, a.T - t0);
+    // ---- raw rows, gates, PGDN's write-key images
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
       const bool live = j < Cc;
-      rk[r] = live ? *reinterpret_cast<const uint4*>(K + tok(a, b, t0 + j, h) * 128 + c0)
-                   : make_uint4(0u, 0u, 0u, 0u);
-      rq[r] = live ? *reinterpret_cast<const uint4*>(Qp + tok(a, b, t0 + j, h) * 128 + c0)
-                   : make_uint4(0u, 0u, 0u, 0u);
+      const long o = tok(a, b, t0 + (live ? j : 0), h) * 128 + c0;
+      *reinterpret_cast<uint4*>(sKr + j * cKR + c0) =
+          live ? *reinterpret_cast<const uint4*>(K + o) : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(sQr + j * cKR + c0) =
+          live ? *reinterpret_cast<const uint4*>(Qp + o) : make_uint4(0u, 0u, 0u, 0u);
     }
-    const float* xp = g.w.dP + (size_t)task * 4096;
-    const float* xl = g.w.dL + (size_t)task * 4096;
-    for (int e = tid; e < 64 * 16; e += kBwdThreads) {
-      const int i = e >> 4, c4 = 4 * (e & 15);
-      cpa16(sMP + i * cLDM + c4, xp + i * 64 + c4);
-      cpa16(sML + i * cLDM + c4, xl + i * 64 + c4);
+    if (PG) {
+      const uint8_t* rw = g.w.rec + (size_t)task * g.w.recb + rWF;
+      for (int e = tid; e < 32768 / 16; e += kBwdThreads) cpa16(sm + lW + 16 * e, rw + 16 * e);
+    }
+    if (tid < 64) {
+      s_g[tid] = (tid < Cc) ? a.log_alpha[tok(a, b, t0 + tid, h)] : 0.f;
+      s_eta[tid] = (tid < Cc) ? a.eta[tok(a, b, t0 + tid, h)] : 0.f;
+    }
+    __syncthreads();
+    {   // norms: four threads per row
+      const int j = tid >> 2, part = tid & 3;
+      float kk = 0.f, qq = 0.f;
+#pragma unroll 8
+      for (int c0 = 32 * part; c0 < 32 * part + 32; ++c0) {
+        const float x = bf(sKr[j * cKR + c0]), y = bf(sQr[j * cKR + c0]);
+        kk += x * x;
+        qq += y * y;
+      }
+      kk += __shfl_xor_sync(0xffffffffu, kk, 1);
+      kk += __shfl_xor_sync(0xffffffffu, kk, 2);
+      qq += __shfl_xor_sync(0xffffffffu, qq, 1);
+      qq += __shfl_xor_sync(0xffffffffu, qq, 2);
+      if (part == 0) {
+        const float cr = a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f;
+        const float qn = a.q_l2norm ? 1.f / fmaxf(sqrtf(qq), 1e-30f) : 1.f;
+        const float s = kk * cr * cr;
+        s_cr[j] = cr;
+        s_qn[j] = qn;
+        s_s[j] = s;
+        s_beta[j] = VARIANT == DR_KLA ? s_eta[j] / (s + a.eps) : s_eta[j];
+        if (PG && j < Cc) g.w.CR[(size_t)task * 64 + j] = cr;
+      }
+    }
+    if (warp == 0) {   // inclusive cumulative log-decay (two tokens per lane)
+      const float x0 = s_g[2 * lane], x1 = s_g[2 * lane + 1];
+      float s = x0 + x1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += y;
+      }
+      __syncwarp();
+      s_g[2 * lane] = s - x1;
+      s_g[2 * lane + 1] = s;
+    }
+    __syncthreads();
+    const float G = s_g[Cc - 1];
+    if (tid < 64) s_ew[tid] = tid < Cc ? __expf(G - s_g[tid]) : 0.f;
+    // ---- images: IA = [q^ ; k^], IW = beta k^ (PGDN: copied above), IM = [M_P ; M_L]
+#pragma unroll 2
+    for (int r = 0; r < 8; ++r) {
+      const int u = tid + r * kBwdThreads, row = u >> 4, cg = u & 15, kb = cg >> 3, c8 = (cg & 7) * 8;
+      const bool isk = row >= 64;
+      const int j = row & 63;
+      const uint16_t* src = (isk ? sKr : sQr) + j * cKR + 64 * kb + c8;
+      const uint4 raw = *reinterpret_cast<const uint4*>(src);
+      float x[8];
+      unpack8(raw, x);
+      const float sc = isk ? s_cr[j] : s_qn[j];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] *= sc;
+      uint4 hi, lo;
+      split8(x, hi, lo);
+      const uint32_t o = lA + kb * 16384 + sw128_offset(row, c8);
+      *reinterpret_cast<uint4*>(sm + o) = hi;
+      *reinterpret_cast<uint4*>(sm + o + 32768) = lo;
+      if (!PG && isk) {
+        const float bt = s_beta[j];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] *= bt;
+        split8(x, hi, lo);
+        const uint32_t ow = lW + kb * 8192 + sw128_offset(j, c8);
+        *reinterpret_cast<uint4*>(sm + ow) = hi;
+        *reinterpret_cast<uint4*>(sm + ow + 16384) = lo;
+      }
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
-      float kf[8], qf[8];
-      unpack8(rk[r], kf);
-      unpack8(rq[r], qf);
+      const int u = tid + r * kBwdThreads, row = u >> 3, j0 = 8 * (u & 7);
+      const bool isl = row >= 64;
+      const int i = row & 63;
+      const float4* src = reinterpret_cast<const float4*>((isl ? g.w.dL : g.w.dP) +
+                                                          (size_t)task * 4096 + i * 64 + j0);
+      const float4 v0 = src[0], v1 = src[1];
+      const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      const float gi = s_g[i];
+      float x[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        sK[j * cLDK + c0 + q] = kf[q];
-        sQ[j * cLDK + c0 + q] = qf[q];
+      for (int e = 0; e < 8; ++e) {
+        const int j = j0 + e;
+        const bool keep = isl ? j < i : j <= i;
+        x[e] = keep ? (isl ? -v[e] : v[e]) * __expf(gi - s_g[j]) : 0.f;
+      }
+      uint4 hi, lo;
+      split8(x, hi, lo);
+      const uint32_t o = lM + sw128_offset(row, j0);
+      *reinterpret_cast<uint4*>(sm + o) = hi;
+      *reinterpret_cast<uint4*>(sm + o + 16384) = lo;
+    }
+    cpa_wait_all();
+    fence_proxy_async();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t ah = smem_u32(sm + lA), al = ah + 32768;
+      const uint32_t wh = smem_u32(sm + lW), wl = wh + 16384;
+      const uint32_t mh = smem_u32(sm + lM), ml = mh + 16384;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {   // G1: K = 128 channels (K-major A and B)
+        const uint32_t oa = (ks >> 2) * 16384 + (ks & 3) * 32, ow = (ks >> 2) * 8192 + (ks & 3) * 32;
+        const uint64_t dah = desc_sw128(ah + oa, 16, 1024), dal = desc_sw128(al + oa, 16, 1024);
+        const uint64_t dwh = desc_sw128(wh + ow, 16, 1024), dwl = desc_sw128(wl + ow, 16, 1024);
+        mma_bf16(tmem + tG1, dah, dwh, I_L1, ks > 0);
+        mma_bf16(tmem + tG1, dal, dwh, I_L1, true);
+        mma_bf16(tmem + tG1, dah, dwl, I_L1, true);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {   // G2: K = 128 rows i (A = IA^T and B = IM, MN-major)
+        const uint32_t o = ks * 2048;
+        const uint64_t dah = desc_sw128(ah + o, 16384, 1024), dal = desc_sw128(al + o, 16384, 1024);
+        const uint64_t dmh = desc_sw128(mh + o, 16384, 1024), dml = desc_sw128(ml + o, 16384, 1024);
+        mma_bf16(tmem + tG2, dah, dmh, I_L2, ks > 0);
+        mma_bf16(tmem + tG2, dal, dmh, I_L2, true);
+        mma_bf16(tmem + tG2, dah, dml, I_L2, true);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {   // G3: K = 64 tokens j (A = IM K-major, B = IW MN-major)
+        const uint64_t dmh = desc_sw128(mh + ks * 32, 16, 1024), dml = desc_sw128(ml + ks * 32, 16, 1024);
+        const uint64_t dwh = desc_sw128(wh + ks * 2048, 8192, 1024);
+        const uint64_t dwl = desc_sw128(wl + ks * 2048, 8192, 1024);
+        mma_bf16(tmem + tG3, dmh, dwh, I_L3, ks > 0);
+        mma_bf16(tmem + tG3, dml, dwh, I_L3, true);
+        mma_bf16(tmem + tG3, dmh, dwl, I_L3, true);
+      }
+      mma_commit(&bar);
+      ++nc;
+    }
+    if (!mbar_wait(&bar, it & 1, kWait)) s_abort = 1;
+    __syncthreads();
+    if (s_abort) break;
+    tc_fence_after();
+    // ---- G1: X_ij = M_P,ij (Q^W^T)_ij + M_L,ij (K^W^T)_ij (query rows first, then key rows)
+    {
+      float v[32];
+      tmem_ld16(tl + tG1 + 32 * hc, *reinterpret_cast<float(*)[16]>(v));
+      tmem_ld16(tl + tG1 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tmem_ld_wait();
+      const int i = trow & 63;
+      if (trow < 64) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sX[i * 65 + 32 * hc + e] = hl(lM, 16384, trow, 32 * hc + e) * v[e];
+      }
+      __syncthreads();
+      if (trow >= 64) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sX[i * 65 + 32 * hc + e] += hl(lM, 16384, trow, 32 * hc + e) * v[e];
       }
     }
-  }
-  if (tid < 64) {
-    s_g[tid] = (tid < Cc) ? a.log_alpha[tok(a, b, t0 + tid, h)] : 0.f;
-    s_eta[tid] = (tid < Cc) ? a.eta[tok(a, b, t0 + tid, h)] : 0.f;
-  }
-  __syncthreads();
-  {   // norms: four threads per row
-    const int j = tid >> 2, part = tid & 3;
-    float kk = 0.f, qq = 0.f;
-    for (int c0 = 32 * part; c0 < 32 * part + 32; ++c0) {
-      const float x = sK[j * cLDK + c0], y = sQ[j * cLDK + c0];
-      kk += x * x;
-      qq += y * y;
-    }
-    kk += __shfl_xor_sync(0xffffffffu, kk, 1);
-    kk += __shfl_xor_sync(0xffffffffu, kk, 2);
-    qq += __shfl_xor_sync(0xffffffffu, qq, 1);
-    qq += __shfl_xor_sync(0xffffffffu, qq, 2);
-    if (part == 0) {
-      const float cr = a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f;
-      const float qn = a.q_l2norm ? 1.f / fmaxf(sqrtf(qq), 1e-30f) : 1.f;
-      const float s = kk * cr * cr;
-      s_cr[j] = cr;
-      s_qn[j] = qn;
-      s_s[j] = s;
-      s_beta[j] = VARIANT == DR_KLA ? s_eta[j] / (s + a.eps) : s_eta[j];
-      if (PG && j < Cc) g.w.CR[(size_t)task * 64 + j] = cr;
-    }
-  }
-  if (warp == 0) {   // inclusive cumulative log-decay (two tokens per lane)
-    const float x0 = s_g[2 * lane], x1 = s_g[2 * lane + 1];
-    float s = x0 + x1;
+    // ---- G2: dw_jc = (dw^T)_cj + e^{G-g_j} X_W,jc, transposed into sD (lane = channel);
+    //      per token j the sums over channels d beta_j = dw_j . k^_j and X_W,j . w_j, by
+    //      a butterfly over the warp's lanes (lane l ends with token 32 hc + l) and the
+    //      four quadrants' parts in shared memory
+    {
+      float v[32], xv[32];
+      const float* xw = g.w.XW + (size_t)task * 8192 + trow;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    __syncwarp();
-    s_g[2 * lane] = s - x1;
-    s_g[2 * lane + 1] = s;
-  }
-  __syncthreads();
-  for (int e = tid; e < 64 * 128; e += kBwdThreads) {
-    const int j = e >> 7, cc = e & 127;
-    const float kh = sK[j * cLDK + cc] * s_cr[j];
-    sK[j * cLDK + cc] = kh;
-    sQ[j * cLDK + cc] *= s_qn[j];
-    if (PG) {   // PGDN: the explicit write keys of the record (hi + lo)
-      const uint8_t* rec = g.w.rec + (size_t)task * g.w.recb;
-      const uint32_t off = (cc >> 6) * 8192 + umma::sw128_offset(j, cc & 63);
-      sW[j * cLDK + cc] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(rec + rWF + off)) +
-                          __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(rec + rWF + 16384 + off));
-    } else {
-      sW[j * cLDK + cc] = s_beta[j] * kh;
-    }
-  }
-  cpa_wait_all();
-  __syncthreads();
-  const float G = s_g[Cc - 1];
-  // ---- Grams Q^ W^T and K^ W^T, then M_P = dP . D (j <= i), M_L = dL . D (j < i),
-  //      and the decay terms of every entry (row i gains, column j loses)
-  {
-    const int mt = warp & 3, nt0 = 4 * (warp >> 2);
-    float aq4[4][4] = {}, ak4[4][4] = {};
-    mm3x<4, 16, false, true>(aq4, sQ + 16 * mt * cLDK, cLDK, sW + 8 * nt0 * cLDK, cLDK, lane);
-    mm3x<4, 16, false, true>(ak4, sK + 16 * mt * cLDK, cLDK, sW + 8 * nt0 * cLDK, cLDK, lane);
-    for (int s = 0; s < 4; ++s) {
-      const int nt = nt0 + s;
-      const float* aq = aq4[s];
-      const float* ak = ak4[s];
+      for (int e = 0; e < 32; ++e) xv[e] = xw[(32 * hc + e) * 128];
+      tmem_ld16(tl + tG2 + 32 * hc, *reinterpret_cast<float(*)[16]>(v));
+      tmem_ld16(tl + tG2 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tmem_ld_wait();
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = 16 * mt + frag_row(lane, e), j = 8 * nt + frag_col(lane, e);
-        const float D = (j <= i) ? __expf(s_g[i] - s_g[j]) : 0.f;
-        const float dP = (j <= i) ? sMP[i * cLDM + j] : 0.f;
-        const float dL = (j < i) ? -sML[i * cLDM + j] : 0.f;
-        const float mp = dP * D, ml = dL * D;
-        sMP[i * cLDM + j] = mp;
-        sML[i * cLDM + j] = ml;
-        sX[i * cLDK + j] = mp * aq[e] + ml * ak[e];   // dP_ij P_ij + dL_ij L_ij
+      for (int e = 0; e < 32; ++e) {
+        const int j = 32 * hc + e;
+        const float dw = v[e] + s_ew[j] * xv[e];
+        sD[j * cLDK + trow] = dw;
+        if (PG) g.w.DW[(size_t)task * 8192 + j * 128 + trow] = dw;
+        const float kh = bf(sKr[j * cKR + trow]) * s_cr[j];
+        const float w = PG ? hl(lW + (trow >> 6) * 8192, 16384, j, trow & 63) : s_beta[j] * kh;
+        v[e] = dw * kh;
+        xv[e] = xv[e] * w;
       }
-    }
-  }
-  __syncthreads();
-  if (tid < 64) {   // each entry adds to dg of its row and takes from dg of its column
-    float r = 0.f, cs = 0.f;
-    for (int j = 0; j < 64; ++j) {
-      r += sX[tid * cLDK + j];
-      cs += sX[j * cLDK + tid];
-    }
-    s_dg[tid] = r - cs;
-  }
-  __syncthreads();
-  {   // E dS^T from bwd_state into the staging buffer, under the dw product
-    const float* xw = g.w.XW + (size_t)task * 8192;
-    for (int e = tid; e < 64 * 32; e += kBwdThreads) {
-      const int j = e >> 5, c4 = 4 * (e & 31);
-      cpa16(sX + j * cLDK + c4, xw + j * 128 + c4);
-    }
-  }
-  // ---- dw = M_P^T Q^ + M_L^T K^ (+ e^{G-g} E dS^T): staged in sY
-  {
-    const int mt = warp & 3;
-    for (int s = 0; s < 2; ++s) {
-      const int nt0 = 8 * (warp >> 2) + 4 * s;
-      float d[4][4] = {};
-      mm3x<4, 8, true, false>(d, sMP + 16 * mt, cLDM, sQ + 8 * nt0, cLDK, lane);
-      mm3x<4, 8, true, false>(d, sML + 16 * mt, cLDM, sK + 8 * nt0, cLDK, lane);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
+      for (int st = 16; st >= 1; st >>= 1) {
+        const bool up = (lane & st) != 0;
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          sY[(16 * mt + frag_row(lane, e)) * cLDK + 8 * (nt0 + j) + frag_col(lane, e)] = d[j][e];
+        for (int i = 0; i < st; ++i) {
+          const float s1 = up ? v[i] : v[i + st], s2 = up ? xv[i] : xv[i + st];
+          const float r1 = __shfl_xor_sync(0xffffffffu, s1, st);
+          const float r2 = __shfl_xor_sync(0xffffffffu, s2, st);
+          v[i] = (up ? v[i + st] : v[i]) + r1;
+          xv[i] = (up ? xv[i + st] : xv[i]) + r2;
+        }
+      }
+      s_p1[q4][32 * hc + lane] = v[0];
+      s_p2[q4][32 * hc + lane] = xv[0];
     }
-  }
-  cpa_wait_all();
-  __syncthreads();
-  {   // rows: four threads per token; dw += e^{G-g} X_W, the decay terms, d beta
-    const int j = tid >> 2, part = tid & 3;
-    const float* xw = sX + j * cLDK;
-    const float ew = (j < Cc) ? __expf(G - s_g[j]) : 0.f;
-    float dwk = 0.f, xww = 0.f;
-    for (int c0 = 32 * part; c0 < 32 * part + 32; ++c0) {
-      const float xv = xw[c0];
-      const float dw = sY[j * cLDK + c0] + ew * xv;
-      sY[j * cLDK + c0] = dw;
-      if (PG) g.w.DW[(size_t)task * 8192 + j * 128 + c0] = dw;
-      dwk += dw * sK[j * cLDK + c0];
-      xww += xv * sW[j * cLDK + c0];
-    }
-    dwk += __shfl_xor_sync(0xffffffffu, dwk, 1);
-    dwk += __shfl_xor_sync(0xffffffffu, dwk, 2);
-    xww += __shfl_xor_sync(0xffffffffu, xww, 1);
-    xww += __shfl_xor_sync(0xffffffffu, xww, 2);
-    if (part == 0) {
+    __syncthreads();
+    if (tid < 64) {   // each Gram entry adds to dg of its row and takes from dg of its column
+      float r = 0.f;
+      for (int j = 0; j < 64; ++j) r += sX[tid * 65 + j];
+      s_dgr[tid] = r;
+    } else if (tid < 128) {
+      const int j = tid - 64;
+      float cs = 0.f;
+      for (int i = 0; i < 64; ++i) cs += sX[i * 65 + j];
+      s_dgx[j] = cs;
+    } else if (tid < 192) {   // d beta_j and e^{G-g_j} X_W,j . w_j from the quadrants' parts
+      const int j = tid - 128;
+      const float dwk = s_p1[0][j] + s_p1[1][j] + s_p1[2][j] + s_p1[3][j];
+      const float xww = s_p2[0][j] + s_p2[1][j] + s_p2[2][j] + s_p2[3][j];
       s_dbeta[j] = j < Cc ? dwk : 0.f;
-      s_dg[j] -= ew * xww;
-      s_dGt[j] = ew * xww;
+      s_dGt[j] = s_ew[j] * xww;
     }
-  }
-  __syncthreads();
-  // ---- dk^ = M_L W - e^g X_K + beta dw (+ KLA norm term), then the key norm
-  {
-    const int mt = warp & 3;
-    for (int s = 0; s < 2; ++s) {
-      const int nt0 = 8 * (warp >> 2) + 4 * s;
-      float d[4][4] = {};
-      mm3x<4, 8, false, false>(d, sML + 16 * mt * cLDM, cLDM, sW + 8 * nt0, cLDK, lane);
+    __syncthreads();
+    // ---- G3: rows of dq^ (TMEM rows 0-63) and dk^ (64-127); warp half hc takes 64 columns
+    {
+      const bool isk = trow >= 64;
+      const int i = trow & 63;
+      const bool live = i < Cc;
+      const float eg = __expf(s_g[i]);
+      float* orow = (isk ? g.dk : g.dq) + tok(a, b, t0 + (live ? i : 0), h) * 128 + 64 * hc;
+      const uint16_t* rr = (isk ? sKr : sQr) + i * cKR + 64 * hc;
+      const float sc = isk ? s_cr[i] : s_qn[i];
+      const float bgain = (PG || !isk) ? 0.f : s_beta[i];
+      const float se = s_s[i] + a.eps, db = s_dbeta[i];
+      const float ds2 = (VARIANT == DR_KLA && isk) ? -2.f * db * s_eta[i] / (se * se) : 0.f;
+      float d[64];
+      float dot = 0.f, xd = 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
+      for (int p = 0; p < 2; ++p) {   // 32 columns: the raw row's loads first, then TMEM
+        float4 x4[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          sX[(16 * mt + frag_row(lane, e)) * cLDK + 8 * (nt0 + j) + frag_col(lane, e)] = d[j][e];
-    }
-  }
-  __syncthreads();
-  {
-    const int j = tid >> 2, part = tid & 3;
-    const bool live = j < Cc;
-    float* dkrow = g.dk + tok(a, b, t0 + (live ? j : 0), h) * 128;
-    const float eg = __expf(s_g[j]);
-    const float beta = s_beta[j], db = s_dbeta[j];
-    // KLA: beta = eta / (s + eps): d eta = d beta / (s + eps), ds = -d beta eta / (s + eps)^2
-    const float se = s_s[j] + a.eps;
-    const float ds2 = VARIANT == DR_KLA ? -2.f * db * s_eta[j] / (se * se) : 0.f;
-    const float bgain = PG ? 0.f : beta;   // PGDN: the gain's terms come in pgdn_gain_bwd
-    float dkh[32], xk = 0.f, dot = 0.f;
-    float xkr[32];
+        for (int e = 0; e < 8; ++e)
+          x4[e] = live ? *reinterpret_cast<const float4*>(orow + 32 * p + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float v[32];
+        tmem_ld16(tl + tG3 + 64 * hc + 32 * p, *reinterpret_cast<float(*)[16]>(v));
+        tmem_ld16(tl + tG3 + 64 * hc + 32 * p + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+        tmem_ld_wait();
 #pragma unroll
-    for (int q = 0; q < 32; q += 4) {
-      const float4 v4 = live ? *reinterpret_cast<const float4*>(dkrow + 32 * part + q)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-      xkr[q] = v4.x; xkr[q + 1] = v4.y; xkr[q + 2] = v4.z; xkr[q + 3] = v4.w;
-    }
+        for (int e = 0; e < 8; ++e) {
+          const float xs[4] = {x4[e].x, x4[e].y, x4[e].z, x4[e].w};
 #pragma unroll
-    for (int q = 0; q < 32; ++q) {
-      const int c0 = 32 * part + q;
-      const float xkv = xkr[q];
-      const float kh = sK[j * cLDK + c0];
-      xk += xkv * kh;
-      dkh[q] = sX[j * cLDK + c0] - eg * xkv + bgain * sY[j * cLDK + c0] + ds2 * kh;
-      dot += dkh[q] * kh;
-    }
-    xk += __shfl_xor_sync(0xffffffffu, xk, 1);
-    xk += __shfl_xor_sync(0xffffffffu, xk, 2);
-    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-    if (live) {
-      const float cr = s_cr[j];
-#pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const int c0 = 32 * part + q;
-        // k^ = k cr: dk = (dk^ - k^ (k^ . dk^)) cr  (k^ is unit-norm then); PGDN keeps
-        // dL/dk^ of the memory part here for pgdn_gain_bwd
-        dkrow[c0] = (a.k_l2norm && !PG) ? (dkh[q] - sK[j * cLDK + c0] * dot) * cr : dkh[q];
+          for (int f = 0; f < 4; ++f) {
+            const int cc = 32 * p + 4 * e + f;
+            const float xh = bf(rr[cc]) * sc;
+            const float val = isk ? v[4 * e + f] - eg * xs[f] + bgain * sD[i * cLDK + 64 * hc + cc] + ds2 * xh
+                                  : v[4 * e + f] + eg * xs[f];
+            d[cc] = val;
+            dot += val * xh;
+            xd += xs[f] * xh;
+          }
+        }
       }
-      if (part == 0) {
-        s_dg[j] -= eg * xk;
-        if (!PG) g.deta[tok(a, b, t0 + j, h)] = VARIANT == DR_KLA ? db / se : db;
+      s_dot[hc][trow] = dot;
+      s_xd[hc][trow] = xd;
+      __syncthreads();
+      dot = s_dot[0][trow] + s_dot[1][trow];
+      if (live) {
+        const bool norm = isk ? (a.k_l2norm && !PG) : a.q_l2norm;
+#pragma unroll
+        for (int cc = 0; cc < 64; cc += 4) {
+          float o4[4];
+#pragma unroll
+          for (int f = 0; f < 4; ++f) {
+            const float xh = bf(rr[cc + f]) * sc;
+            o4[f] = norm ? (d[cc + f] - xh * dot) * sc : d[cc + f];
+          }
+          *reinterpret_cast<float4*>(orow + cc) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+        }
+        if (hc == 0) {
+          const float x = s_xd[0][trow] + s_xd[1][trow];
+          if (isk) {
+            s_dgk[i] = -eg * x;
+            if (!PG) g.deta[tok(a, b, t0 + i, h)] = VARIANT == DR_KLA ? db / se : db;
+          } else {
+            s_dgq[i] = eg * x;
+          }
+        }
+      } else if (hc == 0) {
+        if (isk) s_dgk[i] = 0.f; else s_dgq[i] = 0.f;
       }
     }
-  }
-  __syncthreads();
-  // ---- dq^ = M_P W + e^g X_Q, then the query norm
-  {
-    const int mt = warp & 3;
-    for (int s = 0; s < 2; ++s) {
-      const int nt0 = 8 * (warp >> 2) + 4 * s;
-      float d[4][4] = {};
-      mm3x<4, 8, false, false>(d, sMP + 16 * mt * cLDM, cLDM, sW + 8 * nt0, cLDK, lane);
+    tc_fence_before();
+    __syncthreads();
+    // ---- d log alpha: reverse cumulative sum of dg, dG (+ gamma <dS, S_c>) on the last token
+    if (warp == 0) {
+      float x[2];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          sX[(16 * mt + frag_row(lane, e)) * cLDK + 8 * (nt0 + j) + frag_col(lane, e)] = d[j][e];
-    }
-  }
-  __syncthreads();
-  {
-    const int j = tid >> 2, part = tid & 3;
-    const bool live = j < Cc;
-    float* dqrow = g.dq + tok(a, b, t0 + (live ? j : 0), h) * 128;
-    const float eg = __expf(s_g[j]);
-    float dqh[32], xq = 0.f, dot = 0.f;
-    float xqr[32];
-#pragma unroll
-    for (int q = 0; q < 32; q += 4) {
-      const float4 v4 = live ? *reinterpret_cast<const float4*>(dqrow + 32 * part + q)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-      xqr[q] = v4.x; xqr[q + 1] = v4.y; xqr[q + 2] = v4.z; xqr[q + 3] = v4.w;
-    }
-#pragma unroll
-    for (int q = 0; q < 32; ++q) {
-      const int c0 = 32 * part + q;
-      const float xqv = xqr[q];
-      const float qh = sQ[j * cLDK + c0];
-      xq += xqv * qh;
-      dqh[q] = sX[j * cLDK + c0] + eg * xqv;
-      dot += dqh[q] * qh;
-    }
-    xq += __shfl_xor_sync(0xffffffffu, xq, 1);
-    xq += __shfl_xor_sync(0xffffffffu, xq, 2);
-    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-    if (live) {
-      const float qn = s_qn[j];
-#pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const int c0 = 32 * part + q;
-        dqrow[c0] = a.q_l2norm ? (dqh[q] - sQ[j * cLDK + c0] * dot) * qn : dqh[q];
+      for (int m = 0; m < 2; ++m) {
+        const int t = 63 - 2 * lane - m;
+        x[m] = s_dgr[t] - s_dgx[t] - s_dGt[t] + s_dgq[t] + s_dgk[t];
       }
-      if (part == 0) s_dg[j] += eg * xq;
-    }
-  }
-  __syncthreads();
-  // ---- d log alpha: reverse cumulative sum of dg, dG (+ gamma <dS, S_c>) on the last token
-  if (warp == 0) {
-    if (lane == 0) {   // dG: the chunk's last token
-      float dG = g.w.SS[task];
-      for (int j = 0; j < 64; ++j) dG += s_dGt[j];
-      s_dg[Cc - 1] += dG;
-    }
-    __syncwarp();
-    // suffix sums over 64 entries, two per lane (lane l: tokens 63 - 2l, 62 - 2l)
-    const float x0 = s_dg[63 - 2 * lane], x1 = s_dg[62 - 2 * lane];
-    float s = x0 + x1;
+      float dG = 0.f;
+      for (int j = lane; j < 64; j += 32) dG += s_dGt[j];
+      dG = warp_sum(dG) + g.w.SS[task];
+      if (63 - 2 * lane == Cc - 1) x[0] += dG;
+      if (62 - 2 * lane == Cc - 1) x[1] += dG;
+      float s = x[0] + x[1];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += y;
+      }
+      const int ta = 63 - 2 * lane, tb = 62 - 2 * lane;
+      if (ta < Cc) g.dla[tok(a, b, t0 + ta, h)] = s - x[1];
+      if (tb < Cc) g.dla[tok(a, b, t0 + tb, h)] = s;
     }
-    const int ta = 63 - 2 * lane, tb = 62 - 2 * lane;
-    if (ta < Cc) g.dla[tok(a, b, t0 + ta, h)] = s - x1;
-    if (tb < Cc) g.dla[tok(a, b, t0 + tb, h)] = s;
+    __syncthreads();   // every buffer read before the next task writes it
   }
+  if (s_abort && tid == 0) {   // drain: no MMA may still write TMEM after the dealloc
+    set_status(DR_ERR_TIMEOUT);
+    if (nc > 0) mbar_wait(&bar, (nc - 1) & 1, kWait / 4);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kLocalTmem);
 }
 
 // ================================================================= bwd_local_pc
@@ -1932,7 +2004,7 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
   cudaError_t e = pc ? launch_kdn_split(a, DR_BF16, workspace, st) : launch_chunk_tc_split(a, workspace, st);
   if (e != cudaSuccess) return e;
   const size_t c_smem = (size_t)kCarrySmemF * 4, s_smem = kStateSmem,
-               l_smem = (size_t)kLocalSmemF * 4, p_smem = (size_t)kGainSmemF * 4,
+               l_smem = kLocalSmem, p_smem = (size_t)kGainSmemF * 4,
                pm_smem = (size_t)kGainMapSmemF * 4;
   if ((e = cudaFuncSetAttribute(bwd_carry_kernel<false, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c_smem)) !=
@@ -1996,6 +2068,7 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
   const int nsm = bwd_sm_count();
   if (nsm <= 0) return cudaErrorInvalidValue;
   bwd_state_kernel<<<(unsigned)(n < nsm ? n : nsm), kStateThreads, s_smem, st>>>(fa, g, n);
+  const unsigned lgrid = (unsigned)(n < nsm ? n : nsm);
   if (fa.variant == DR_KDA) {
     bwd_local_pc_kernel<DR_KDA><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
   } else if (fa.variant == DR_KDN) {
@@ -2015,15 +2088,15 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
     gain_scan_kernel<<<fa.B * fa.H, 32, 0, st>>>(fa, g, 1);
     ikdn_gain_bwd_kernel<1><<<(unsigned)n, 128, kIkdnGainSmemF * 4, st>>>(fa, g);
   } else if (fa.variant == DR_KLA) {
-    bwd_local_kernel<DR_KLA><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
+    bwd_local_kernel<DR_KLA><<<lgrid, kBwdThreads, l_smem, st>>>(fa, g, n);
   } else if (pg) {
-    bwd_local_kernel<DR_PGDN><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
+    bwd_local_kernel<DR_PGDN><<<lgrid, kBwdThreads, l_smem, st>>>(fa, g, n);
     pgdn_gain_bwd_kernel<false, 0><<<(unsigned)n, 128, pm_smem, st>>>(fa, g);
     gain_scan_kernel<<<fa.B * fa.H, 128, 0, st>>>(fa, g, 128);
     pgdn_gain_bwd_kernel<false, 1><<<(unsigned)n, 128, p_smem, st>>>(fa, g);
     pgdn_dmu_kernel<<<(fa.H + 127) / 128, 128, 0, st>>>(fa, g);
   } else {
-    bwd_local_kernel<DR_GDN><<<(unsigned)n, kBwdThreads, l_smem, st>>>(fa, g);
+    bwd_local_kernel<DR_GDN><<<lgrid, kBwdThreads, l_smem, st>>>(fa, g, n);
   }
   return cudaGetLastError();
 }
