@@ -1267,6 +1267,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mm3x<2, 2, false, false>(dk2, sML + 16 * I * cLDM + 16 * kk, cLDM, sWt + 16 * kk * cLDK + 16 * warp,
                                  cLDK, lane);
       }
+      // every raw X_Q / X_K value first (the stores below could alias them)
+      float xqa[2][4], xka[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 16 * I + frag_row(lane, e), cc = 16 * warp + 8 * nt + frag_col(lane, e);
+          const long o = tok(a, b, t0 + (i < Cc ? i : 0), h) * 128 + cc;
+          xqa[nt][e] = i < Cc ? g.dq[o] : 0.f;
+          xka[nt][e] = i < Cc ? g.dk[o] : 0.f;
+        }
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -1277,7 +1288,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float sc = __expf(gi - sG[m * cLDK + cc]), eg = __expf(gi);
             const float dqp = dq2[nt][e] * sc, dkl = dk2[nt][e] * sc;
             const long o = tok(a, b, t0 + i, h) * 128 + cc;
-            const float xq = g.dq[o], xk = g.dk[o];
+            const float xq = xqa[nt][e], xk = xka[nt][e];
             const float qh = bf(sQr[i * cKRS + cc]) * s_qn[i], kh = bf(sKr[i * cKRS + cc]) * s_cr[i];
             g.dq[o] = dqp + eg * xq;
             g.dk[o] = dkl - eg * xk;
@@ -1312,7 +1323,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float* xw = g.w.XW + (size_t)task * 8192 + j * 128;
     const float cr = s_cr[j], qn = s_qn[j], eta = s_eta[j];
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    float dkh[16], dqh[16], kh[16], qh[16], deta = 0.f, dotk = 0.f, dotq = 0.f;
+    float dkh[16], dqh[16], kh[16], qh[16], dwa[16], deta = 0.f, dotk = 0.f, dotq = 0.f;
 #pragma unroll
     for (int k4 = 0; k4 < 4; ++k4) {
       const int c0 = 4 * part + 32 * k4;
@@ -1334,12 +1345,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                            __uint_as_float(kr.y << 16), __uint_as_float(kr.y & 0xFFFF0000u)};
       const float qf[4] = {__uint_as_float(qr.x << 16), __uint_as_float(qr.x & 0xFFFF0000u),
                            __uint_as_float(qr.y << 16), __uint_as_float(qr.y & 0xFFFF0000u)};
-      float dwo[4], dgo[4];
+      float dwo[4], dgo[4], tgo[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int q = 4 * k4 + e;
         const float ew = __expf(gc[e] - gg[e]);
         const float dw = dg4[e] + ew * xx[e];
+        tgo[e] = live ? ww[e] * ew * xx[e] : 0.f;   // this token's part of dG_c
         kh[q] = kf[e] * cr;
         qh[q] = qf[e] * qn;
         dkh[q] = kk[e];
@@ -1355,10 +1367,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         dotk += dkh[q] * kh[q];
         dotq += dqh[q] * qh[q];
       }
-      if (kGainK)
-        *reinterpret_cast<float4*>(g.w.DW + (size_t)task * 8192 + j * 128 + c0) =
-            make_float4(dwo[0], dwo[1], dwo[2], dwo[3]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dwa[4 * k4 + e] = dwo[e];
       *reinterpret_cast<float4*>(sDW + j * cLDK + c0) = make_float4(dgo[0], dgo[1], dgo[2], dgo[3]);
+      *reinterpret_cast<float4*>(sWt + j * cLDK + c0) = make_float4(tgo[0], tgo[1], tgo[2], tgo[3]);
+    }
+    if (kGainK) {   // dL/dw for the gain kernel (after every load of the row above)
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4)
+        *reinterpret_cast<float4*>(g.w.DW + (size_t)task * 8192 + j * 128 + 4 * part + 32 * k4) =
+            make_float4(dwa[4 * k4], dwa[4 * k4 + 1], dwa[4 * k4 + 2], dwa[4 * k4 + 3]);
     }
 #pragma unroll
     for (int o2 = 1; o2 < 8; o2 <<= 1) {
@@ -1387,13 +1405,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   __syncthreads();
   // ---- per channel: dG on the last token, then d log alpha = the reverse cumulative sum
-  if (tid < 128) {
+  if (tid < 128) {   // (the tokens' parts of dG_c were left in the w~ buffer by the rows)
     const int cc = tid;
-    const float gC = sG[63 * cLDK + cc];
     float dG = g.w.SS[(size_t)task * 128 + cc];
-    const float* xw = g.w.XW + (size_t)task * 8192;
-    for (int j = 0; j < Cc; ++j)
-      dG += sW[j * cLDK + cc] * __expf(gC - sG[j * cLDK + cc]) * xw[j * 128 + cc];
+    for (int j = 0; j < Cc; ++j) dG += sWt[j * cLDK + cc];
     float acc = 0.f;
     for (int j = Cc - 1; j >= 0; --j) {
       acc += sDW[j * cLDK + cc] + (j == Cc - 1 ? dG : 0.f);
@@ -1748,14 +1763,24 @@ __global__ void __launch_bounds__(128, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs
       dp = al * al * dph;
     }
     __syncthreads();
-    for (int e = i; e < Cc * 32; e += 128) {   // d omega out, d log alpha updated (coalesced)
-      const int t = e >> 5, c4 = 4 * (e & 31);
-      const long o = tok(a, b, t0 + t, h) * 128 + c4;
-      *reinterpret_cast<float4*>(g.domega + o) = *reinterpret_cast<const float4*>(sA + t * 128 + c4);
-      float4 la = *reinterpret_cast<const float4*>(g.dla + o);
-      const float4 x = *reinterpret_cast<const float4*>(sPh + t * 128 + c4);
-      la.x += x.x; la.y += x.y; la.z += x.z; la.w += x.w;
-      *reinterpret_cast<float4*>(g.dla + o) = la;
+    {   // d omega out, d log alpha updated (coalesced; every load before the stores)
+      float4 la[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const int e = i + 128 * r, t = e >> 5, c4 = 4 * (e & 31);
+        la[r] = t < Cc ? *reinterpret_cast<const float4*>(g.dla + tok(a, b, t0 + t, h) * 128 + c4)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const int e = i + 128 * r, t = e >> 5, c4 = 4 * (e & 31);
+        if (t >= Cc) continue;
+        const long o = tok(a, b, t0 + t, h) * 128 + c4;
+        *reinterpret_cast<float4*>(g.domega + o) = *reinterpret_cast<const float4*>(sA + t * 128 + c4);
+        const float4 x = *reinterpret_cast<const float4*>(sPh + t * 128 + c4);
+        la[r].x += x.x; la[r].y += x.y; la[r].z += x.z; la[r].w += x.w;
+        *reinterpret_cast<float4*>(g.dla + o) = la[r];
+      }
     }
     for (int tt = 0; tt < 16; ++tt) {   // d r and the key norm, warp w: tokens 16 w .. + 15
       const int t = 16 * warp + tt;
@@ -1925,9 +1950,23 @@ __global__ void __launch_bounds__(128, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArg
     }
     __syncthreads();
     if (PHASE == 0) return;
+    float xk8[8][4], xl8[8][4];
+#pragma unroll
     for (int tt = 0; tt < 16; ++tt) {   // per (token, channel), warp w: tokens 16 w .. + 15
       const int t = 16 * warp + tt;
-      if (t >= Cc) break;
+      if (t >= Cc) continue;
+      if ((tt & 7) == 0) {   // the next 8 tokens' dk^ and d log alpha rows, before any store
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int tu = t + u;
+          const long ou = tok(a, b, t0 + (tu < Cc ? tu : 0), h) * 128;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            xk8[u][m] = tu < Cc ? g.dk[ou + lane + 32 * m] : 0.f;
+            xl8[u][m] = tu < Cc ? g.dla[ou + lane + 32 * m] : 0.f;
+          }
+        }
+      }
       const float bhat = s_bh[t], rt = s_r[t], st = s_s[t], dbt = s_db[t], du = s_du[t];
       const float den = rt + bhat * st;
       const float ds = -dbt * bhat * bhat / (den * den) + du * mu / (128.f * rt);
@@ -1943,9 +1982,9 @@ __global__ void __launch_bounds__(128, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArg
       for (int m = 0; m < 4; ++m) {
         const int ch = lane + 32 * m;
         const float kh = sK[t * 128 + ch];
-        dkh[m] = dkrow[ch] + (bhat / den) * sDW[t * 128 + ch] + 2.f * ds * kh;
+        dkh[m] = xk8[tt & 7][m] + (bhat / den) * sDW[t * 128 + ch] + 2.f * ds * kh;
         dot += kh * dkh[m];
-        g.dla[tt_ * 128 + ch] += fa * sA[t * 128 + ch];
+        g.dla[tt_ * 128 + ch] = xl8[tt & 7][m] + fa * sA[t * 128 + ch];
       }
       dot = warp_sum(dot);
       const float cr = s_cr[t];
