@@ -309,47 +309,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         vkn[i] = kk * cr * cr;
       }
     }
-    // the chained gain state: wait for the previous chunk's hand-over
-    if (chained && ci > 0 && (kKdn || kPkda || kIkdn) && tid == 0 &&
-        !chain_wait(chain + ri, chain + ntask + 1, g_chain_wait_ns))
-      set_status(DR_ERR_TIMEOUT);
-    __syncthreads();
-    // the gain state at the chunk start (its load flies under the passes below):
-    // thread c < 128 = channel c (KDN p, PKDA A), isotropic KDN: the head's b (warp 4)
-    float st = 0.f;
-    if ((kKdn || kPkda) && tid < 128) {
-      if (chained)
-        st = ci == 0 ? (a.aux0 ? a.aux0[(long)bh * 128 + tid] : (kKdn ? 1.f : 0.f))
-                     : __ldcg(reinterpret_cast<const float*>(rec + rkP0) + tid);
-      else
-        st = reinterpret_cast<const float*>(rec + rkP0)[tid];
-    }
-    if (kIkdn && warp == 4) {
-      st = 1.f;
-      if (chained)
-        st = ci == 0 ? (a.aux0 ? a.aux0[bh] : 1.f) : __ldcg(reinterpret_cast<const float*>(rec + rkP0));
-    }
-    if (kIkdn) {   // mean squared decay of every token (warp w: tokens 8w .. 8w + 7)
-#pragma unroll
-      for (int rr = 0; rr < 64 / kWarps; ++rr) {
-        const int i = (64 / kWarps) * warp + rr;
-        float s2 = 0.f;
-#pragma unroll
-        for (int c = lane; c < 128; c += 32) s2 += __expf(2.f * fG_[i * 128 + c]);
-        s2 = warp_sum(s2);
-        if (lane == 0) vaa[i] = s2 * (1.f / 128.f);
-      }
-      __syncthreads();
-    }
-
     // ---- 2. scans.  First every term off the recurrences' chains, for all (token,
     //         channel) at once in the B-image region (free until the B pass): KDN
-    //         a^2 and u = (information scale / r) k^2, PKDA betaP k^2.  Then thread c =
-    //         channel c walks the chunk: cumulative log-decay g, KDN variance, PKDA
+    //         a^2 and u = (information scale / r) k^2, PKDA betaP k^2.  Then the
+    //         channels' recurrences: cumulative log-decay g, KDN variance, PKDA
     //         statistic; isotropic KDN: warp 4 scans the head variance.
     float* fX_ = reinterpret_cast<float*>(sm + sB);   // [64][128] KDN a^2
     float* fY_ = fX_ + 64 * 128;                      // [64][128] KDN u, PKDA betaP k^2
+    float st = 0.f;   // the gain state at the chunk start
     if (kKdn || kPkda) {
+      // Four threads per channel (part = tid / 128 takes tokens 16 part .. + 15).  Each
+      // first composes its tokens' maps of (n, d) — KDN M = [[a^2, w], [u a^2, 1 + u w]],
+      // PKDA n <- alphaP n + betaP k^2 (d = 1) — and its log-decay sum, before the
+      // hand-over wait; after it, the chunk-start state through the parts' maps gives
+      // each part its start and the chunk's end state (handed over at once), and only
+      // then does each part walk its tokens.
+      __syncthreads();   // the norms
 #pragma unroll 2
       for (int r = 0; r < kUnits; ++r) {
         const int u = tid + r * kThreads, i = u >> 4, cg = u & 15, kb = cg >> 3, c8 = (cg & 7) * 8;
@@ -374,128 +349,202 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncthreads();
-    }
-    if (tid < 128) {
-      const int c = tid;
-      float g = 0.f, n = st, d = 1.f;
-#pragma unroll 1
-      for (int i0 = 0; i0 < 64; i0 += 8) {
-        float la[8], x[8], y[8], om[8];
+      const int c = tid & 127, part = tid >> 7, i0 = 16 * part;
+      float P0 = 1.f, P1 = 0.f, P2 = 0.f, P3 = 1.f, gs = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int o = (i0 + e) * 128 + c;
-          la[e] = fG_[o];
-          if (kKdn) {
-            x[e] = fX_[o];
-            om[e] = fA_[o];
+      for (int e = 0; e < 16; ++e) {
+        const int o = (i0 + e) * 128 + c;
+        gs += fG_[o];
+        const float y = fY_[o];
+        if (kKdn) {
+          const float x = fX_[o], om = fA_[o];
+          const float q0 = fmaf(x, P0, om * P2), q1 = fmaf(x, P1, om * P3);
+          P2 = fmaf(y, q0, P2);
+          P3 = fmaf(y, q1, P3);
+          P0 = q0;
+          P1 = q1;
+          if ((e & 7) == 7) {   // exact power-of-two rescale (the map acts projectively)
+            const float sc = __uint_as_float(0x7f000000u - (__float_as_uint(fmaxf(P3, P2)) & 0x7f800000u));
+            P0 *= sc;
+            P1 *= sc;
+            P2 *= sc;
+            P3 *= sc;
           }
-          if (kKdn || kPkda) y[e] = fY_[o];
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          g += la[e];
-          fG_[(i0 + e) * 128 + c] = g;
-        }
-        if (kKdn) {   // (n, d) <- [[a^2, w], [u a^2, 1 + u w]] (n, d); p^_i = n_i / d_{i-1}
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float n1 = fmaf(x[e], n, om[e] * d);
-            fA_[(i0 + e) * 128 + c] = __fdividef(n1, d);
-            d = fmaf(y[e], n1, d);
-            n = n1;
-          }
-          // exact power-of-two rescale to d in [1, 2) (p = n / d is scale-free; d >= 1)
-          const float sc = __uint_as_float(0x7f000000u - (__float_as_uint(d) & 0x7f800000u));
-          n *= sc;
-          d *= sc;
-        }
-        if (kPkda) {   // A_t = alphaP A + betaP k^2 (the bound follows below)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            n = fmaf(vaP[i0 + e], n, y[e]);
-            fA_[(i0 + e) * 128 + c] = n;
-          }
+        } else {
+          const float x = vaP[i0 + e];
+          P0 *= x;
+          P1 = fmaf(x, P1, y);
         }
       }
-      if (chained && (kKdn || kPkda)) {   // state at the chunk end -> next record, or aux
+      float4* sMap = reinterpret_cast<float4*>(sm + sB + 65536);       // [4][128] part maps
+      float* sGs = reinterpret_cast<float*>(sm + sB + 65536 + 8192);   // [4][128] part sums
+      sMap[part * 128 + c] = make_float4(P0, P1, P2, P3);
+      sGs[part * 128 + c] = gs;
+      // the chained gain state: wait for the previous chunk's hand-over
+      if (chained && ci > 0 && tid == 0 && !chain_wait(chain + ri, chain + ntask + 1, g_chain_wait_ns))
+        set_status(DR_ERR_TIMEOUT);
+      __syncthreads();
+      if (chained)
+        st = ci == 0 ? (a.aux0 ? a.aux0[(long)bh * 128 + c] : (kKdn ? 1.f : 0.f))
+                     : __ldcg(reinterpret_cast<const float*>(rec + rkP0) + c);
+      else
+        st = reinterpret_cast<const float*>(rec + rkP0)[c];
+      float g = 0.f, n = st, d = 1.f;
+      auto apply = [&](const float4& Q) {
+        const float n1 = fmaf(Q.x, n, Q.y * d), d1 = fmaf(Q.z, n, Q.w * d);
+        const float sc = kKdn ? __uint_as_float(0x7f000000u - (__float_as_uint(d1) & 0x7f800000u)) : 1.f;
+        n = n1 * sc;
+        d = d1 * sc;
+      };
+      for (int q = 0; q < part; ++q) {
+        g += sGs[q * 128 + c];
+        apply(sMap[q * 128 + c]);
+      }
+      if (chained && part == 3) {   // state at the chunk end -> next record, or aux
+        const float ns = n, ds = d;
+        apply(make_float4(P0, P1, P2, P3));
         const float end = kKdn ? n / d : n;
+        n = ns;
+        d = ds;
         if (ci + 1 < NC)   // published by thread 0's release after the barrier below
           __stcg(reinterpret_cast<float*>(rec + kRec + rkP0) + c, end);
         else if (a.aux)
           a.aux[(long)bh * 128 + c] = end;
       }
-    } else if (kIkdn && warp == 4) {
-      // b -> b^ / (1 + u b^), b^ = a b + omega is the Moebius map of (n, d) by
-      // M = [[a, omega], [u a, 1 + u omega]]: two tokens' product per lane, a shuffle
-      // scan of 2x2 products (each rescaled by an exact power of two), then b^ of
-      // every token and beta = b^ / (r + b^ ||k^||^2) (KDN notes Eq. (40))
-      auto mmul = [](const float (&A)[4], const float (&B)[4], float (&C)[4]) {
-        C[0] = A[0] * B[0] + A[1] * B[2];
-        C[1] = A[0] * B[1] + A[1] * B[3];
-        C[2] = A[2] * B[0] + A[3] * B[2];
-        C[3] = A[2] * B[1] + A[3] * B[3];
-      };
-      auto renorm = [](float (&C)[4]) {
-        int ex;
-        frexpf(fmaxf(fmaxf(fabsf(C[0]), fabsf(C[1])), fmaxf(fabsf(C[2]), fabsf(C[3]))), &ex);
-#pragma unroll
-        for (int z = 0; z < 4; ++z) C[z] = ldexpf(C[z], -ex);
-      };
-      auto token = [&](int i, float (&M)[4]) {
-        const float at = vaa[i], om = vom[i], u = a.info_scale * vkn[i] / (128.f * vr[i]);
-        M[0] = at;
-        M[1] = om;
-        M[2] = u * at;
-        M[3] = 1.f + u * om;
-      };
-      const float b_in = st;
-      float M0[4], M1[4], Pl[4];
-      token(2 * lane, M0);
-      token(2 * lane + 1, M1);
-      mmul(M1, M0, Pl);
-      renorm(Pl);
-#pragma unroll
-      for (int dd = 1; dd < 32; dd <<= 1) {
-        float Q[4], R[4];
-#pragma unroll
-        for (int z = 0; z < 4; ++z) Q[z] = __shfl_up_sync(0xffffffffu, Pl[z], dd);
-        if (lane >= dd) {
-          mmul(Pl, Q, R);
-#pragma unroll
-          for (int z = 0; z < 4; ++z) Pl[z] = R[z];
-          renorm(Pl);
-        }
-      }
-      float E[4];
-#pragma unroll
-      for (int z = 0; z < 4; ++z) E[z] = __shfl_up_sync(0xffffffffu, Pl[z], 1);
-      if (lane == 0) {
-        E[0] = 1.f;
-        E[1] = 0.f;
-        E[2] = 0.f;
-        E[3] = 1.f;
-      }
-      const float n0 = E[0] * b_in + E[1], d0 = E[2] * b_in + E[3];
-      const float bh0 = vaa[2 * lane] * __fdividef(n0, d0) + vom[2 * lane];
-      const float n1 = M0[0] * n0 + M0[1] * d0, d1 = M0[2] * n0 + M0[3] * d0;
-      const float bh1 = vaa[2 * lane + 1] * __fdividef(n1, d1) + vom[2 * lane + 1];
-      vsc[2 * lane] = __fdividef(bh0, vr[2 * lane] + bh0 * vkn[2 * lane]);
-      vsc[2 * lane + 1] = __fdividef(bh1, vr[2 * lane + 1] + bh1 * vkn[2 * lane + 1]);
-      const float nE = Pl[0] * b_in + Pl[1], dE = Pl[2] * b_in + Pl[3];
-      const float b_end = __shfl_sync(0xffffffffu, __fdividef(nE, dE), 31);
-      if (lane == 0 && chained) {
-        if (ci + 1 < NC)
-          __stcg(reinterpret_cast<float*>(rec + kRec + rkP0), b_end);
-        else if (a.aux)
-          a.aux[bh] = b_end;
-      }
-    }
-    __syncthreads();
+      __syncthreads();
     // every thread's hand-over store precedes the barrier; thread 0's fence and
     // release store publish them at GPU scope (cumulative over the barrier)
     if (chained && (kKdn || kPkda || kIkdn) && tid == 0 && ci + 1 < NC && ri + 1 != g_chain_withhold) {
       __threadfence();
       st_release_gpu(chain + ri + 1, 1u);
+    }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int o = (i0 + e) * 128 + c;
+        g += fG_[o];
+        fG_[o] = g;
+        const float y = fY_[o];
+        if (kKdn) {   // p^_i = n_i / d_{i-1}
+          const float n1 = fmaf(fX_[o], n, fA_[o] * d);
+          fA_[o] = __fdividef(n1, d);
+          d = fmaf(y, n1, d);
+          n = n1;
+          if ((e & 7) == 7) {   // exact power-of-two rescale to d in [1, 2) (d >= 1)
+            const float sc = __uint_as_float(0x7f000000u - (__float_as_uint(d) & 0x7f800000u));
+            n *= sc;
+            d *= sc;
+          }
+        } else {   // A_t = alphaP A + betaP k^2 (the bound follows below)
+          n = fmaf(vaP[i0 + e], n, y);
+          fA_[o] = n;
+        }
+      }
+      __syncthreads();
+    } else {
+      // the chained gain state (isotropic KDN): wait for the previous chunk's hand-over
+      if (chained && ci > 0 && kIkdn && tid == 0 && !chain_wait(chain + ri, chain + ntask + 1, g_chain_wait_ns))
+        set_status(DR_ERR_TIMEOUT);
+      __syncthreads();
+      if (kIkdn && warp == 4) {
+        st = 1.f;
+        if (chained)
+          st = ci == 0 ? (a.aux0 ? a.aux0[bh] : 1.f) : __ldcg(reinterpret_cast<const float*>(rec + rkP0));
+      }
+      if (kIkdn) {   // mean squared decay of every token (warp w: tokens 8w .. 8w + 7)
+#pragma unroll
+        for (int rr = 0; rr < 64 / kWarps; ++rr) {
+          const int i = (64 / kWarps) * warp + rr;
+          float s2 = 0.f;
+#pragma unroll
+          for (int c = lane; c < 128; c += 32) s2 += __expf(2.f * fG_[i * 128 + c]);
+          s2 = warp_sum(s2);
+          if (lane == 0) vaa[i] = s2 * (1.f / 128.f);
+        }
+        __syncthreads();
+      }
+
+      if (tid < 128) {   // the cumulative log-decay, channel tid
+        const int c = tid;
+        float g = 0.f;
+#pragma unroll 8
+        for (int i = 0; i < 64; ++i) {
+          g += fG_[i * 128 + c];
+          fG_[i * 128 + c] = g;
+        }
+      }
+      if (kIkdn && warp == 4) {
+        // b -> b^ / (1 + u b^), b^ = a b + omega is the Moebius map of (n, d) by
+        // M = [[a, omega], [u a, 1 + u omega]]: two tokens' product per lane, a shuffle
+        // scan of 2x2 products (each rescaled by an exact power of two), then b^ of
+        // every token and beta = b^ / (r + b^ ||k^||^2) (KDN notes Eq. (40))
+        auto mmul = [](const float (&A)[4], const float (&B)[4], float (&C)[4]) {
+          C[0] = A[0] * B[0] + A[1] * B[2];
+          C[1] = A[0] * B[1] + A[1] * B[3];
+          C[2] = A[2] * B[0] + A[3] * B[2];
+          C[3] = A[2] * B[1] + A[3] * B[3];
+        };
+        auto renorm = [](float (&C)[4]) {
+          int ex;
+          frexpf(fmaxf(fmaxf(fabsf(C[0]), fabsf(C[1])), fmaxf(fabsf(C[2]), fabsf(C[3]))), &ex);
+#pragma unroll
+          for (int z = 0; z < 4; ++z) C[z] = ldexpf(C[z], -ex);
+        };
+        auto token = [&](int i, float (&M)[4]) {
+          const float at = vaa[i], om = vom[i], u = a.info_scale * vkn[i] / (128.f * vr[i]);
+          M[0] = at;
+          M[1] = om;
+          M[2] = u * at;
+          M[3] = 1.f + u * om;
+        };
+        const float b_in = st;
+        float M0[4], M1[4], Pl[4];
+        token(2 * lane, M0);
+        token(2 * lane + 1, M1);
+        mmul(M1, M0, Pl);
+        renorm(Pl);
+#pragma unroll
+        for (int dd = 1; dd < 32; dd <<= 1) {
+          float Q[4], R[4];
+#pragma unroll
+          for (int z = 0; z < 4; ++z) Q[z] = __shfl_up_sync(0xffffffffu, Pl[z], dd);
+          if (lane >= dd) {
+            mmul(Pl, Q, R);
+#pragma unroll
+            for (int z = 0; z < 4; ++z) Pl[z] = R[z];
+            renorm(Pl);
+          }
+        }
+        float E[4];
+#pragma unroll
+        for (int z = 0; z < 4; ++z) E[z] = __shfl_up_sync(0xffffffffu, Pl[z], 1);
+        if (lane == 0) {
+          E[0] = 1.f;
+          E[1] = 0.f;
+          E[2] = 0.f;
+          E[3] = 1.f;
+        }
+        const float n0 = E[0] * b_in + E[1], d0 = E[2] * b_in + E[3];
+        const float bh0 = vaa[2 * lane] * __fdividef(n0, d0) + vom[2 * lane];
+        const float n1 = M0[0] * n0 + M0[1] * d0, d1 = M0[2] * n0 + M0[3] * d0;
+        const float bh1 = vaa[2 * lane + 1] * __fdividef(n1, d1) + vom[2 * lane + 1];
+        vsc[2 * lane] = __fdividef(bh0, vr[2 * lane] + bh0 * vkn[2 * lane]);
+        vsc[2 * lane + 1] = __fdividef(bh1, vr[2 * lane + 1] + bh1 * vkn[2 * lane + 1]);
+        const float nE = Pl[0] * b_in + Pl[1], dE = Pl[2] * b_in + Pl[3];
+        const float b_end = __shfl_sync(0xffffffffu, __fdividef(nE, dE), 31);
+        if (lane == 0 && chained) {
+          if (ci + 1 < NC)
+            __stcg(reinterpret_cast<float*>(rec + kRec + rkP0), b_end);
+          else if (a.aux)
+            a.aux[bh] = b_end;
+        }
+      }
+      __syncthreads();
+      // every thread's hand-over store precedes the barrier; thread 0's fence and
+      // release store publish them at GPU scope (cumulative over the barrier)
+      if (chained && (kKdn || kPkda || kIkdn) && tid == 0 && ci + 1 < NC && ri + 1 != g_chain_withhold) {
+        __threadfence();
+        st_release_gpu(chain + ri + 1, 1u);
+      }
     }
     if (kPkda) {   // the bound B(A) = exp(-ln(x) r / (1 + |r|)), r = log max(A, floor) - mu
                    // (PDN notes Eq. (9); fast log / exp), in place
