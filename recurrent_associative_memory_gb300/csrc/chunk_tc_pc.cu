@@ -102,12 +102,6 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
 
-__device__ __forceinline__ float bf16_at(const uint8_t* tile, int row, int col) {
-  // element (row, col) of a [rows][128] bf16 tile stored as 64-column blocks 16 KB apart
-  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-      tile + (col >> 6) * 16384 + sw128_offset(row, col & 63)));
-}
-
 __device__ __forceinline__ void st_global16(uint8_t* p, const uint4& v) {
   *reinterpret_cast<uint4*>(p) = v;
 }
