@@ -482,6 +482,301 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// ================================================================= bwd_carry_tc
+// The reverse carry of the scalar-decay variants (GDN, KLA) on tcgen05: one CTA
+// per (b, h, dv half), chunks in reverse, dL/dS (128 x 64 fp32) in registers.
+// Per chunk, with the record's P and T images (bf16 hi | lo), the raw K and Q rows
+// (bf16, exact) and the row vectors sq = e^g qn, u = e^{G-g} c, sk = e^g cr, gamma:
+//   G1  D1 = [P_hi ; P_lo]^T dO                 (A MN-major, M = 128)
+//   G2  D2 = [K ; Q] [dS_hi | dS_lo]            (the Q rows are not used)
+//   G4a D4 = Q^T [dO'_hi | dO'_lo],  dO' = sq . dO
+//   dE  = D1 (both halves) + u . (K dS_hi + K dS_lo)
+//   G3  D3 = [T_hi ; T_lo]^T [dE_hi | dE_lo],    dR = dV = hi.hi + hi.lo + lo.hi
+//   G4b D4 -= K^T [dR'_hi | dR'_lo],  dR' = sk . dR
+//   dS <- gamma dS + D4 (both halves)
+// G1, G2 and G4a are issued together; the chain is G2 -> dE -> G3 -> dR -> G4b -> dS.
+// The M = 128 halves of D1 and D3 meet through shared memory (the quadrant of lanes
+// 64-127 hands its rows to the quadrant of lanes 0-63).  The next chunk's operands
+// arrive by asynchronous copies under the current chunk's dR and dS steps.
+constexpr uint32_t kcKQ = 0;            // 2 buffers x [K kb0 | Q kb0 | K kb1 | Q kb1] (8 KB each)
+constexpr uint32_t kcP = 65536;         // P hi | P lo (the record's images)
+constexpr uint32_t kcT = kcP + 16384;   // T hi | T lo
+constexpr uint32_t kcO = kcT + 16384;   // dO [64 j][64 n] bf16 (MN-major B)
+constexpr uint32_t kcVec = kcO + 8192;  // 2 x fp32 [256]: sq [0, 64), u [64, 128), gamma, sk [192, 256)
+constexpr uint32_t kcS = kcVec + 2048;  // dS hi | dS lo: [128 c][64 n] each (16 KB)
+constexpr uint32_t kcE = kcS + 32768;   // dE hi | dE lo [64][64] (8 KB each); then the dR exchange
+constexpr uint32_t kcR = kcE + 16384;   // dR' hi | lo; before it, the dE exchange
+constexpr uint32_t kcO2 = kcR + 16384;  // dO' hi | lo
+constexpr uint32_t kCarryTcSmem = kcO2 + 16384 + 1024;
+constexpr uint32_t tcD1 = 0, tcD2 = 64, tcD3 = 192, tcD4 = 320, kCarryTcTmem = 512;
+constexpr uint32_t I_C1 = idesc_bf16(128, 64, 1, 1);
+constexpr uint32_t I_C2 = idesc_bf16(128, 128, 0, 1);
+constexpr uint32_t I_C3 = idesc_bf16(128, 128, 1, 1);
+constexpr uint32_t I_C4N = idesc_bf16(128, 128, 1, 1, 1);
+
+__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// 32 fp32 values of one row -> bf16 hi / lo at columns col0 .. col0 + 31 of a
+// 128B-swizzled image with 128-byte rows (hi at base, lo at base + lo_off)
+__device__ __forceinline__ void put_row32(uint8_t* base, uint32_t lo_off, int row, int col0,
+                                          const float (&v)[32]) {
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = v[8 * m + e];
+    uint4 hi, lo;
+    split8(x, hi, lo);
+    const uint32_t o = sw128_offset(row, col0 + 8 * m);
+    *reinterpret_cast<uint4*>(base + o) = hi;
+    *reinterpret_cast<uint4*>(base + o + lo_off) = lo;
+  }
+}
+
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_carry_tc_kernel(FwdArgs a, BwdArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t bars[3];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q4 = warp & 3, hc = warp >> 2, trow = 32 * q4 + lane;   // TMEM lane = trow
+  const int bh = blockIdx.x >> 1, cb = blockIdx.x & 1, n0 = 64 * cb;
+  const int b = bh / a.H, h = bh % a.H;
+  const int NC = (a.T + 63) / 64;
+  const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
+  const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(a.q);
+  const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(g.d_out);
+  float* xch = reinterpret_cast<float*>(sm + kcR);    // dE exchange [64][64], XOR-swizzled
+  float* xch2 = reinterpret_cast<float*>(sm + kcE);   // dR exchange
+
+  if (tid == 0) {
+    for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  if (warp == 0) tmem_alloc(&tmem_base_s, kCarryTcTmem);
+  // chunk c's operands: P, T, dO, vectors, and K / Q into buffer kq (one commit group)
+  auto load = [&](int c, int kq) {
+    const uint8_t* rec = g.w.rec + ((size_t)bh * NC + c) * g.w.recb;
+    const int t0 = 64 * c, Cc = min(64, a.T - t0);
+    for (int e = tid; e < 2048; e += kBwdThreads) {   // P, T images: 16 KB each
+      const uint32_t o = 16 * e;
+      cpa16(sm + (o < 16384 ? kcP + o : kcT + o - 16384),
+            rec + (o < 16384 ? rPF + o : rTF + o - 16384));
+    }
+    for (int e = tid; e < 64 * 8; e += kBwdThreads) {   // dO rows: 8 16-byte pieces of 64 columns
+      const int j = e >> 3, p = e & 7;
+      const bool live = j < Cc;
+      cpa16(sm + kcO + sw128_offset(j, 8 * p), dO + tok(a, b, t0 + (live ? j : 0), h) * 128 + n0 + 8 * p,
+            live ? 16 : 0);
+    }
+    for (int e = tid; e < 64 * 32; e += kBwdThreads) {   // K and Q rows: 16 pieces of 128 channels each
+      const int j = e >> 5, isq = (e >> 4) & 1, p = e & 15, kb = p >> 3;
+      const bool live = j < Cc;
+      cpa16(sm + kcKQ + kq * 32768 + kb * 16384 + isq * 8192 + sw128_offset(j, 8 * (p & 7)),
+            (isq ? Q : K) + tok(a, b, t0 + (live ? j : 0), h) * 128 + 8 * p, live ? 16 : 0);
+    }
+    for (int e = tid; e < 64; e += kBwdThreads) {   // vectors: sq, u, gamma at 128, sk at 192
+      const float* rv = reinterpret_cast<const float*>(rec + rVecF);
+      cpa16(sm + kcVec + (c & 1) * 1024 + 16 * e, rv + 4 * e);
+    }
+    cpa_commit();
+  };
+  // dS = dL/dS_T (or 0): rows c = trow, columns 32 hc .. + 31 of this half
+  float ds[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    ds[e] = g.dS_final ? g.dS_final[((size_t)bh * 128 + trow) * 128 + n0 + 32 * hc + e] : 0.f;
+  load(NC - 1, (NC - 1) & 1);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+  int nA = 0, nB = 0, nC = 0;
+
+  for (int c = NC - 1; c >= 0; --c) {
+    const int it = NC - 1 - c, kq = c & 1;
+    const size_t ri = (size_t)bh * NC + c;
+    const int t0 = 64 * c, Cc = min(64, a.T - t0);
+    // dL/dS_{c+1} for the local gradients; its hi / lo image for G2
+    {
+      float* sv = g.w.dS + ri * 16384 + (size_t)trow * 128 + n0 + 32 * hc;
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(sv + e) = make_float4(ds[e], ds[e + 1], ds[e + 2], ds[e + 3]);
+      put_row32(sm + kcS, 16384, trow, 32 * hc, ds);
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();   // chunk c's operands landed (every thread's copies)
+    const float* vec = reinterpret_cast<const float*>(sm + kcVec + (c & 1) * 1024);
+    // dO' = sq . dO (hi / lo): row j, 8 columns per unit
+    for (int e = tid; e < 64 * 8; e += kBwdThreads) {
+      const int j = e >> 3, p = e & 7;
+      const uint32_t o = sw128_offset(j, 8 * p);
+      float x[8];
+      unpack8(*reinterpret_cast<const uint4*>(sm + kcO + o), x);
+      const float s = vec[j];
+#pragma unroll
+      for (int f = 0; f < 8; ++f) x[f] *= s;
+      uint4 hi, lo;
+      split8(x, hi, lo);
+      *reinterpret_cast<uint4*>(sm + kcO2 + o) = hi;
+      *reinterpret_cast<uint4*>(sm + kcO2 + 8192 + o) = lo;
+    }
+    fence_proxy_async();
+    __syncthreads();
+    const uint32_t kqb = smem_u32(sm + kcKQ + kq * 32768);
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t pb = smem_u32(sm + kcP), ob = smem_u32(sm + kcO), o2 = smem_u32(sm + kcO2);
+      const uint32_t sb = smem_u32(sm + kcS);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)   // G1: K = 64 tokens
+        mma_bf16(tmem + tcD1, desc_sw128(pb + ks * 2048, 8192, 1024), desc_sw128(ob + ks * 2048, 8192, 1024),
+                 I_C1, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)   // G2: K = 128 channels
+        mma_bf16(tmem + tcD2, desc_sw128(kqb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                 desc_sw128(sb + ks * 2048, 16384, 1024), I_C2, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)   // G4a: K = 64 tokens, A = Q^T (MN-major)
+        mma_bf16(tmem + tcD4, desc_sw128(kqb + 8192 + ks * 2048, 16384, 1024),
+                 desc_sw128(o2 + ks * 2048, 8192, 1024), I_C3, ks > 0);
+      mma_commit(&bars[0]);
+      ++nA;
+    }
+    if (!mbar_wait(&bars[0], it & 1, kWait)) s_abort = 1;
+    __syncthreads();
+    if (s_abort) break;
+    tc_fence_after();
+    // ---- dE: lanes 64-127 hand D1's lo rows over; lanes 0-63 sum and write dE hi / lo
+    if (trow >= 64) {
+      float v[32];
+      tmem_ld16(tl + tcD1 + 32 * hc, *reinterpret_cast<float(*)[16]>(v));
+      tmem_ld16(tl + tcD1 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tmem_ld_wait();
+      const int i = trow - 64;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) xch[i * 64 + ((32 * hc + e) ^ (i & 31))] = v[e];
+    }
+    __syncthreads();
+    if (trow < 64) {
+      float v[32], k0[32], k1[32];
+      tmem_ld16(tl + tcD1 + 32 * hc, *reinterpret_cast<float(*)[16]>(v));
+      tmem_ld16(tl + tcD1 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tmem_ld16(tl + tcD2 + 32 * hc, *reinterpret_cast<float(*)[16]>(k0));
+      tmem_ld16(tl + tcD2 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(k0 + 16));
+      tmem_ld16(tl + tcD2 + 64 + 32 * hc, *reinterpret_cast<float(*)[16]>(k1));
+      tmem_ld16(tl + tcD2 + 64 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(k1 + 16));
+      tmem_ld_wait();
+      const int i = trow;
+      const float u = vec[64 + i];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] += xch[i * 64 + ((32 * hc + e) ^ (i & 31))] + u * (k0[e] + k1[e]);
+      put_row32(sm + kcE, 8192, i, 32 * hc, v);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {   // G3: dR = T^T dE
+      tc_fence_after();
+      const uint32_t tb = smem_u32(sm + kcT), eb = smem_u32(sm + kcE);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + tcD3, desc_sw128(tb + ks * 2048, 8192, 1024), desc_sw128(eb + ks * 2048, 8192, 1024),
+                 I_C3, ks > 0);
+      mma_commit(&bars[1]);
+      ++nB;
+    }
+    if (!mbar_wait(&bars[1], it & 1, kWait)) s_abort = 1;
+    __syncthreads();
+    if (s_abort) break;
+    tc_fence_after();
+    // the next chunk's operands (G1, G3 are done with P, T, dO; the other K/Q buffer
+    // was last read by the previous chunk)
+    if (c > 0) load(c - 1, (c - 1) & 1);
+    // ---- dR = T_hi^T dE_hi + T_hi^T dE_lo + T_lo^T dE_hi; dV out; dR' = sk . dR
+    if (trow >= 64) {
+      float v[32];
+      tmem_ld16(tl + tcD3 + 32 * hc, *reinterpret_cast<float(*)[16]>(v));
+      tmem_ld16(tl + tcD3 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tmem_ld_wait();
+      const int i = trow - 64;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) xch2[i * 64 + ((32 * hc + e) ^ (i & 31))] = v[e];
+    }
+    __syncthreads();
+    if (trow < 64) {
+      float v[32], w[32];
+      tmem_ld16(tl + tcD3 + 32 * hc, *reinterpret_cast<float(*)[16]>(v));
+      tmem_ld16(tl + tcD3 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tmem_ld16(tl + tcD3 + 64 + 32 * hc, *reinterpret_cast<float(*)[16]>(w));
+      tmem_ld16(tl + tcD3 + 64 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(w + 16));
+      tmem_ld_wait();
+      const int i = trow;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] += w[e] + xch2[i * 64 + ((32 * hc + e) ^ (i & 31))];
+      if (i < Cc) {
+        float* dv = g.dv + tok(a, b, t0 + i, h) * 128 + n0 + 32 * hc;
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(dv + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+      }
+      const float sk = vec[192 + i];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] *= sk;
+      put_row32(sm + kcR, 8192, i, 32 * hc, v);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {   // G4b: D4 -= K^T dR'
+      tc_fence_after();
+      const uint32_t rb = smem_u32(sm + kcR);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + tcD4, desc_sw128(kqb + ks * 2048, 16384, 1024), desc_sw128(rb + ks * 2048, 8192, 1024),
+                 I_C4N, true);
+      mma_commit(&bars[2]);
+      ++nC;
+    }
+    if (!mbar_wait(&bars[2], it & 1, kWait)) s_abort = 1;
+    __syncthreads();
+    if (s_abort) break;
+    tc_fence_after();
+    {   // ---- dS_c = gamma dS + D4 (both halves); lane = state row
+      float v[32], w[32];
+      tmem_ld16(tl + tcD4 + 32 * hc, *reinterpret_cast<float(*)[16]>(v));
+      tmem_ld16(tl + tcD4 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tmem_ld16(tl + tcD4 + 64 + 32 * hc, *reinterpret_cast<float(*)[16]>(w));
+      tmem_ld16(tl + tcD4 + 64 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(w + 16));
+      tmem_ld_wait();
+      const float gam = vec[128];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) ds[e] = fmaf(gam, ds[e], v[e] + w[e]);
+    }
+    tc_fence_before();
+    __syncthreads();   // every buffer of this chunk read before the next one's writes
+  }
+  if (s_abort) {
+    if (tid == 0) {   // drain: no MMA may still write TMEM after the dealloc
+      set_status(DR_ERR_TIMEOUT);
+      if (nA > 0) mbar_wait(&bars[0], (nA - 1) & 1, kWait / 4);
+      if (nB > 0) mbar_wait(&bars[1], (nB - 1) & 1, kWait / 4);
+      if (nC > 0) mbar_wait(&bars[2], (nC - 1) & 1, kWait / 4);
+    }
+  } else if (g.dS0) {
+    float* d0 = g.dS0 + ((size_t)bh * 128 + trow) * 128 + n0 + 32 * hc;
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(d0 + e) = make_float4(ds[e], ds[e + 1], ds[e + 2], ds[e + 3]);
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kCarryTcTmem);
+}
+
 // ================================================================= bwd_state
 // Per chunk, five products over the dv index v (all fp32 data, K = 128):
 //   X_Q = dO S_c^T, X_K = dR S_c^T (64 x 128, raw dq / dk for bwd_local),
@@ -2045,8 +2340,8 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
   const size_t c_smem = (size_t)kCarrySmemF * 4, s_smem = kStateSmem,
                l_smem = kLocalSmem, p_smem = (size_t)kGainSmemF * 4,
                pm_smem = (size_t)kGainMapSmemF * 4;
-  if ((e = cudaFuncSetAttribute(bwd_carry_kernel<false, false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c_smem)) !=
+  if ((e = cudaFuncSetAttribute(bwd_carry_tc_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCarryTcSmem)) !=
           cudaSuccess ||
       (e = cudaFuncSetAttribute(bwd_carry_kernel<true, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c_smem)) !=
@@ -2103,7 +2398,7 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
   else if (pc)
     bwd_carry_kernel<false, true><<<fa.B * fa.H * 2, kBwdThreads, c_smem, st>>>(fa, g);
   else
-    bwd_carry_kernel<false, false><<<fa.B * fa.H * 2, kBwdThreads, c_smem, st>>>(fa, g);
+    bwd_carry_tc_kernel<<<fa.B * fa.H * 2, kBwdThreads, kCarryTcSmem, st>>>(fa, g);
   const int nsm = bwd_sm_count();
   if (nsm <= 0) return cudaErrorInvalidValue;
   bwd_state_kernel<<<(unsigned)(n < nsm ? n : nsm), kStateThreads, s_smem, st>>>(fa, g, n);
