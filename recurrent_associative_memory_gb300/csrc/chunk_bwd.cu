@@ -777,6 +777,253 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_carry_tc_kernel(FwdArgs a,
   if (warp == 0) tmem_dealloc(tmem, kCarryTcTmem);
 }
 
+// The per-channel-decay variants' reverse carry on tcgen05 (KDA, Diagonal /
+// isotropic KDN, PKDA): the record holds (Gamma.Q), Wbar and W'^T as bf16 hi / lo
+// images and gamma per state row, and dS_c = gamma . dS + (Gamma.Q)^T dO - W'^T dE
+// ((Gamma.K)^T dR = (T Gamma.K)^T dE), so the dS step needs dE only:
+//   G1  D1 = [P_hi ; P_lo]^T dO,   G2  D2 = [Wbar_hi ; Wbar_lo] [dS_hi | dS_lo]
+//   dE  = D1 (both halves) + hi.hi + hi.lo + lo.hi of D2
+//   G3  D3 = [T_hi ; T_lo]^T [dE_hi | dE_lo]       (dR = dV)
+//   G4  D4 = -W'^T_hi [dE_hi | dE_lo] - W'^T_lo dE_hi + (Gamma.Q)^T_hi dO + (Gamma.Q)^T_lo dO
+// G3 and G4 are issued together once dE is written.
+constexpr uint32_t kpW = 0;             // Wbar as [hi kb0 | lo kb0 | hi kb1 | lo kb1] (8 KB each)
+constexpr uint32_t kpQ = 32768;         // (Gamma.Q) hi kb0 | hi kb1 | lo kb0 | lo kb1 (the record's order)
+constexpr uint32_t kpWp = 65536;        // W'^T hi | lo [128 c][64 j]
+constexpr uint32_t kpP = 98304;         // P hi | lo
+constexpr uint32_t kpT = 114688;        // T hi | lo
+constexpr uint32_t kpO = 131072;        // 2 x dO [64 j][64 n] bf16
+constexpr uint32_t kpVec = 147456;      // 2 x fp32 [256]: gamma per state row at [128, 256)
+constexpr uint32_t kpS = 149504;        // dS hi | lo [128 c][64 n]
+constexpr uint32_t kpE = kpS + 32768;   // dE hi | lo; then the dR exchange
+constexpr uint32_t kpX = kpE + 16384;   // the dE exchange [64][64] fp32
+constexpr uint32_t kCarryPcSmem = kpX + 16384 + 1024;
+constexpr uint32_t I_P4N = idesc_bf16(128, 128, 0, 1, 1);
+constexpr uint32_t I_P4N64 = idesc_bf16(128, 64, 0, 1, 1);
+
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_carry_tc_pc_kernel(FwdArgs a, BwdArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t bars[2];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q4 = warp & 3, hc = warp >> 2, trow = 32 * q4 + lane;
+  const int bh = blockIdx.x >> 1, cb = blockIdx.x & 1, n0 = 64 * cb;
+  const int b = bh / a.H, h = bh % a.H;
+  const int NC = (a.T + 63) / 64;
+  const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(g.d_out);
+  float* xch = reinterpret_cast<float*>(sm + kpX);
+  float* xch2 = reinterpret_cast<float*>(sm + kpE);
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  if (warp == 0) tmem_alloc(&tmem_base_s, kCarryTcTmem);
+  // chunk c's first group: P, Wbar, dO (slot c & 1), vectors (slot c & 1)
+  auto load_a = [&](int c) {
+    const uint8_t* rec = g.w.rec + ((size_t)bh * NC + c) * g.w.recb;
+    const int t0 = 64 * c, Cc = min(64, a.T - t0);
+    for (int e = tid; e < 1024; e += kBwdThreads) {   // P (16 KB)
+      cpa16(sm + kpP + 16 * e, rec + rPF + 16 * e);
+    }
+    for (int e = tid; e < 2048; e += kBwdThreads) {   // Wbar (32 KB), rearranged per k-block
+      const uint32_t o = 16 * e, piece = o >> 13;
+      cpa16(sm + kpW + (piece & 1) * 16384 + (piece >> 1) * 8192 + (o & 8191), rec + rWbPC + o);
+    }
+    for (int e = tid; e < 64 * 8; e += kBwdThreads) {
+      const int j = e >> 3, p = e & 7;
+      const bool live = j < Cc;
+      cpa16(sm + kpO + (c & 1) * 8192 + sw128_offset(j, 8 * p),
+            dO + tok(a, b, t0 + (live ? j : 0), h) * 128 + n0 + 8 * p, live ? 16 : 0);
+    }
+    for (int e = tid; e < 64; e += kBwdThreads)
+      cpa16(sm + kpVec + (c & 1) * 1024 + 16 * e, rec + rVecF + 16 * e);
+    cpa_commit();
+  };
+  // the second group: (Gamma.Q), T, W'^T
+  auto load_b = [&](int c) {
+    const uint8_t* rec = g.w.rec + ((size_t)bh * NC + c) * g.w.recb;
+    for (int e = tid; e < 2048; e += kBwdThreads) cpa16(sm + kpQ + 16 * e, rec + rQPC + 16 * e);
+    for (int e = tid; e < 1024; e += kBwdThreads) cpa16(sm + kpT + 16 * e, rec + rTF + 16 * e);
+    for (int e = tid; e < 2048; e += kBwdThreads) cpa16(sm + kpWp + 16 * e, rec + rWpPC + 16 * e);
+    cpa_commit();
+  };
+  float ds[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    ds[e] = g.dS_final ? g.dS_final[((size_t)bh * 128 + trow) * 128 + n0 + 32 * hc + e] : 0.f;
+  load_a(NC - 1);
+  load_b(NC - 1);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+  int nA = 0, nB = 0;
+
+  for (int c = NC - 1; c >= 0; --c) {
+    const int it = NC - 1 - c;
+    const size_t ri = (size_t)bh * NC + c;
+    const int t0 = 64 * c, Cc = min(64, a.T - t0);
+    {
+      float* sv = g.w.dS + ri * 16384 + (size_t)trow * 128 + n0 + 32 * hc;
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(sv + e) = make_float4(ds[e], ds[e + 1], ds[e + 2], ds[e + 3]);
+      put_row32(sm + kpS, 16384, trow, 32 * hc, ds);
+    }
+    asm volatile("cp.async.wait_group 1;" ::: "memory");   // this chunk's first group
+    fence_proxy_async();
+    __syncthreads();
+    const float* vec = reinterpret_cast<const float*>(sm + kpVec + (c & 1) * 1024);
+    const uint32_t ob = smem_u32(sm + kpO + (c & 1) * 8192);
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t pb = smem_u32(sm + kpP), wb = smem_u32(sm + kpW), sb = smem_u32(sm + kpS);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)   // G1
+        mma_bf16(tmem + tcD1, desc_sw128(pb + ks * 2048, 8192, 1024), desc_sw128(ob + ks * 2048, 8192, 1024),
+                 I_C1, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)   // G2
+        mma_bf16(tmem + tcD2, desc_sw128(wb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                 desc_sw128(sb + ks * 2048, 16384, 1024), I_C2, ks > 0);
+      mma_commit(&bars[0]);
+      ++nA;
+    }
+    if (!mbar_wait(&bars[0], it & 1, kWait)) s_abort = 1;
+    __syncthreads();
+    if (s_abort) break;
+    tc_fence_after();
+    if (c > 0) load_a(c - 1);   // P and Wbar are read; dO and the vectors take the other slot
+    // ---- dE
+    if (trow >= 64) {
+      float v[32], w[32];
+      tmem_ld16(tl + tcD1 + 32 * hc, *reinterpret_cast<float(*)[16]>(v));
+      tmem_ld16(tl + tcD1 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tmem_ld16(tl + tcD2 + 32 * hc, *reinterpret_cast<float(*)[16]>(w));
+      tmem_ld16(tl + tcD2 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(w + 16));
+      tmem_ld_wait();
+      const int i = trow - 64;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) xch[i * 64 + ((32 * hc + e) ^ (i & 31))] = v[e] + w[e];
+    }
+    __syncthreads();
+    if (trow < 64) {
+      float v[32], k0[32], k1[32];
+      tmem_ld16(tl + tcD1 + 32 * hc, *reinterpret_cast<float(*)[16]>(v));
+      tmem_ld16(tl + tcD1 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tmem_ld16(tl + tcD2 + 32 * hc, *reinterpret_cast<float(*)[16]>(k0));
+      tmem_ld16(tl + tcD2 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(k0 + 16));
+      tmem_ld16(tl + tcD2 + 64 + 32 * hc, *reinterpret_cast<float(*)[16]>(k1));
+      tmem_ld16(tl + tcD2 + 64 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(k1 + 16));
+      tmem_ld_wait();
+      const int i = trow;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] += k0[e] + k1[e] + xch[i * 64 + ((32 * hc + e) ^ (i & 31))];
+      put_row32(sm + kpE, 8192, i, 32 * hc, v);
+    }
+    if (c > 0)   // this chunk's second group (the next chunk's first one may still fly)
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {   // G3 and G4
+      tc_fence_after();
+      const uint32_t tb = smem_u32(sm + kpT), eb = smem_u32(sm + kpE), wp = smem_u32(sm + kpWp);
+      const uint32_t qb = smem_u32(sm + kpQ);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + tcD3, desc_sw128(tb + ks * 2048, 8192, 1024), desc_sw128(eb + ks * 2048, 8192, 1024),
+                 I_C3, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + tcD4, desc_sw128(wp + ks * 32, 16, 1024), desc_sw128(eb + ks * 2048, 8192, 1024),
+                 I_P4N, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + tcD4, desc_sw128(wp + 16384 + ks * 32, 16, 1024), desc_sw128(eb + ks * 2048, 8192, 1024),
+                 I_P4N64, true);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        mma_bf16(tmem + tcD4, desc_sw128(qb + ks * 2048, 8192, 1024), desc_sw128(ob + ks * 2048, 8192, 1024),
+                 I_C1, true);
+        mma_bf16(tmem + tcD4, desc_sw128(qb + 16384 + ks * 2048, 8192, 1024),
+                 desc_sw128(ob + ks * 2048, 8192, 1024), I_C1, true);
+      }
+      mma_commit(&bars[1]);
+      ++nB;
+    }
+    if (!mbar_wait(&bars[1], it & 1, kWait)) s_abort = 1;
+    __syncthreads();
+    if (s_abort) break;
+    tc_fence_after();
+    if (c > 0) load_b(c - 1);   // (Gamma.Q), T and W'^T are read
+    // ---- dR = dV: lanes 64-127 hand over T_lo^T dE_hi
+    if (trow >= 64) {
+      float v[32];
+      tmem_ld16(tl + tcD3 + 32 * hc, *reinterpret_cast<float(*)[16]>(v));
+      tmem_ld16(tl + tcD3 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tmem_ld_wait();
+      const int i = trow - 64;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) xch2[i * 64 + ((32 * hc + e) ^ (i & 31))] = v[e];
+    }
+    {   // ---- dS_c = gamma . dS + D4 (both halves); lane = state row
+      float v[32], w[32];
+      tmem_ld16(tl + tcD4 + 32 * hc, *reinterpret_cast<float(*)[16]>(v));
+      tmem_ld16(tl + tcD4 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tmem_ld16(tl + tcD4 + 64 + 32 * hc, *reinterpret_cast<float(*)[16]>(w));
+      tmem_ld16(tl + tcD4 + 64 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(w + 16));
+      tmem_ld_wait();
+      const float gam = vec[128 + trow];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) ds[e] = fmaf(gam, ds[e], v[e] + w[e]);
+    }
+    __syncthreads();
+    if (trow < 64) {
+      float v[32], w[32];
+      tmem_ld16(tl + tcD3 + 32 * hc, *reinterpret_cast<float(*)[16]>(v));
+      tmem_ld16(tl + tcD3 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tmem_ld16(tl + tcD3 + 64 + 32 * hc, *reinterpret_cast<float(*)[16]>(w));
+      tmem_ld16(tl + tcD3 + 64 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(w + 16));
+      tmem_ld_wait();
+      const int i = trow;
+      if (i < Cc) {
+        float* dv = g.dv + tok(a, b, t0 + i, h) * 128 + n0 + 32 * hc;
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(dv + e) =
+              make_float4(v[e] + w[e] + xch2[i * 64 + ((32 * hc + e) ^ (i & 31))],
+                          v[e + 1] + w[e + 1] + xch2[i * 64 + ((32 * hc + e + 1) ^ (i & 31))],
+                          v[e + 2] + w[e + 2] + xch2[i * 64 + ((32 * hc + e + 2) ^ (i & 31))],
+                          v[e + 3] + w[e + 3] + xch2[i * 64 + ((32 * hc + e + 3) ^ (i & 31))]);
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+  if (s_abort) {
+    if (tid == 0) {
+      set_status(DR_ERR_TIMEOUT);
+      if (nA > 0) mbar_wait(&bars[0], (nA - 1) & 1, kWait / 4);
+      if (nB > 0) mbar_wait(&bars[1], (nB - 1) & 1, kWait / 4);
+    }
+  } else if (g.dS0) {
+    float* d0 = g.dS0 + ((size_t)bh * 128 + trow) * 128 + n0 + 32 * hc;
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(d0 + e) = make_float4(ds[e], ds[e + 1], ds[e + 2], ds[e + 3]);
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kCarryTcTmem);
+}
+
 // ================================================================= bwd_state
 // Per chunk, five products over the dv index v (all fp32 data, K = 128):
 //   X_Q = dO S_c^T, X_K = dR S_c^T (64 x 128, raw dq / dk for bwd_local),
@@ -2346,8 +2593,8 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
       (e = cudaFuncSetAttribute(bwd_carry_kernel<true, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c_smem)) !=
           cudaSuccess ||
-      (e = cudaFuncSetAttribute(bwd_carry_kernel<false, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c_smem)) !=
+      (e = cudaFuncSetAttribute(bwd_carry_tc_pc_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCarryPcSmem)) !=
           cudaSuccess ||
       (e = cudaFuncSetAttribute(bwd_local_pc_kernel<DR_KDA>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kPcLocalSmem)) !=
@@ -2396,7 +2643,7 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
   if (pg)
     bwd_carry_kernel<true, false><<<fa.B * fa.H * 2, kBwdThreads, c_smem, st>>>(fa, g);
   else if (pc)
-    bwd_carry_kernel<false, true><<<fa.B * fa.H * 2, kBwdThreads, c_smem, st>>>(fa, g);
+    bwd_carry_tc_pc_kernel<<<fa.B * fa.H * 2, kBwdThreads, kCarryPcSmem, st>>>(fa, g);
   else
     bwd_carry_tc_kernel<<<fa.B * fa.H * 2, kBwdThreads, kCarryTcSmem, st>>>(fa, g);
   const int nsm = bwd_sm_count();
