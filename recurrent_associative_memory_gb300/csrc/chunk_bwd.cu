@@ -34,11 +34,14 @@
 //
 // Kernels (after the forward's prep and carry, which saves S_c and E per chunk):
 //   bwd_carry   one CTA per (b, h, 64 columns of dv), chunks in reverse: dE, dR
-//               (written as dV) and dS_c on TF32x3 warp-level tensor-core products,
-//               saving dS = dL/dS_{c+1} per chunk.
-//   bwd_state   one CTA per (b, h, chunk): dO S_c^T, dR S_c^T, E dS^T, dO E^T, dR E^T.
-//   bwd_local   one CTA per (b, h, chunk): gates, Grams, the decay-ratio terms, the
-//               products with W, Q^, K^, the gain and norm backward, d log alpha.
+//               (written as dV) and dS_c on tcgen05 (dL/dS in registers), saving
+//               dS = dL/dS_{c+1} per chunk.
+//   bwd_state   a persistent CTA per SM over the chunks: dO S_c^T, dR S_c^T, E dS^T,
+//               dO E^T, dR E^T on tcgen05.
+//   bwd_local   GDN, KLA, PGDN: a persistent CTA per SM, the Grams and the products
+//               with W, Q^, K^ on tcgen05, then the decay terms, the gain and norm
+//               backward, d log alpha; bwd_local_pc (per-channel decay): one CTA per
+//               chunk, block rows on warp-level products.
 #include "chain.cuh"
 #include "dr_common.cuh"
 #include "tc_common.cuh"
@@ -229,16 +232,6 @@ __device__ __forceinline__ long tok(const FwdArgs& a, int b, int t, int h) {
   return ((long)b * a.T + t) * a.H + h;
 }
 
-// ================================================================= bwd_carry
-// A CTA carries one half of dS's columns (kNV = 64) for one (b, h): 2 B H CTAs,
-// one per SM, so up to 76 rows run in a single wave.
-constexpr int kNV = 64;       // dS columns per CTA
-constexpr int cLD64T = 72;    // 64-wide tiles read transposed (A operand, TA)
-constexpr int cLDW = 132;     // 128-wide, read as A (non-transposed)
-constexpr int cLDQ = 136;     // 128-wide, read transposed
-constexpr int cLDN = kNV + 8; // kNV-wide B operands
-constexpr int kCarrySmemF = 2 * 64 * cLD64T + 64 * cLDW + 2 * 64 * cLDQ + 2 * 64 * cLDN + 128 * cLDN;
-
 struct BwdArgs {
   const void* d_out;         // [B,T,H,dv] bf16
   const float* dS_final;     // [B,H,dk,dv] or null
@@ -257,230 +250,6 @@ struct BwdArgs {
   float* dr;                 // KDN [B,T,H]
   BwdWs w;
 };
-
-// PC (per-channel decay): (Gamma.Q), Wbar and W'^T come from the record's images,
-// gamma per state row, and dS_c = gamma . dS + (Gamma.Q)^T dO - W'^T dE, as
-// (Gamma.K)^T dR = (Gamma.K)^T T^T dE = (T Gamma.K)^T dE.
-template <bool PG, bool PC>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    bwd_carry_kernel(FwdArgs a, BwdArgs g) {
-  extern __shared__ __align__(16) float smf[];
-  float* sP = smf;                       // P [i][j]
-  float* sT = sP + 64 * cLD64T;          // T [i][j]
-  float* sWb = sT + 64 * cLD64T;         // Wbar [j][c]
-  float* sQg = sWb + 64 * cLDW;          // (Gamma.Q^) [j][c]
-  float* sKg = sQg + 64 * cLDQ;          // (Gamma.K^) [j][c]
-  float* sdO = sKg + 64 * cLDQ;          // dO [i][n]
-  float* sdE = sdO + 64 * cLDN;          // dE [i][n], then (scalar decay) dR
-  float* sdS = sdE + 64 * cLDN;          // dS [c][n]
-  __shared__ float s_gamma;
-  __shared__ float s_gam[PC ? 128 : 1];   // per-channel decay: gamma of each state row
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x >> 1, cb = blockIdx.x & 1;
-  const int n0 = kNV * cb;               // this CTA's first dS column
-  const int b = bh / a.H, h = bh % a.H;
-  const int NC = (a.T + 63) / 64;
-  const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
-  const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(a.q);
-  const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(g.d_out);
-
-  for (int e = tid; e < 128 * kNV; e += kBwdThreads) {
-    const int r = e / kNV, n = e % kNV;
-    sdS[r * cLDN + n] = g.dS_final ? g.dS_final[((size_t)bh * 128 + r) * 128 + n0 + n] : 0.f;
-  }
-  // The next chunk's raw operands (P and T tile images, K and Q rows, dO, the
-  // record's row vectors) are fetched into registers while this chunk computes.
-  uint4 rPT[2][4], rK[4], rQ[4], rO[2], rWh[PG ? 4 : 1], rWl[PG ? 4 : 1];
-  float rU[4], rEq[4], rEk[4], rG = 0.f;
-  auto fetch = [&](int c) {
-    const uint8_t* rec = g.w.rec + ((size_t)bh * NC + c) * g.w.recb;
-    const float* rv = reinterpret_cast<const float*>(rec + rVecF);
-    const int t0 = 64 * c, Cc = min(64, a.T - t0);
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int e = tid + r * kBwdThreads, i = e >> 3, c0 = 8 * (e & 7);
-      const uint32_t off = umma::sw128_offset(i, c0);
-      rPT[r][0] = *reinterpret_cast<const uint4*>(rec + rPF + off);
-      rPT[r][1] = *reinterpret_cast<const uint4*>(rec + rPF + 8192 + off);
-      rPT[r][2] = *reinterpret_cast<const uint4*>(rec + rTF + off);
-      rPT[r][3] = *reinterpret_cast<const uint4*>(rec + rTF + 8192 + off);
-    }
-#pragma unroll
-    for (int r = 0; r < 4 && !PC; ++r) {
-      const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
-      const bool live = j < Cc;
-      rK[r] = live ? *reinterpret_cast<const uint4*>(K + tok(a, b, t0 + j, h) * 128 + c0)
-                   : make_uint4(0u, 0u, 0u, 0u);
-      if (PG) {   // the explicit write keys (hi, lo) of the record, tile [tok][ch] per 64 ch
-        const uint32_t off = (c0 >> 6) * 8192 + umma::sw128_offset(j, c0 & 63);
-        rWh[r] = *reinterpret_cast<const uint4*>(rec + rWF + off);
-        rWl[r] = *reinterpret_cast<const uint4*>(rec + rWF + 16384 + off);
-      }
-      rQ[r] = live ? *reinterpret_cast<const uint4*>(Q + tok(a, b, t0 + j, h) * 128 + c0)
-                   : make_uint4(0u, 0u, 0u, 0u);
-      rU[r] = rv[64 + j];
-      rEq[r] = rv[j];
-      rEk[r] = rv[192 + j];
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int e = tid + r * kBwdThreads, i = e >> 3, c0 = 8 * (e & 7);
-      rO[r] = i < Cc ? *reinterpret_cast<const uint4*>(dO + tok(a, b, t0 + i, h) * 128 + n0 + c0)
-                     : make_uint4(0u, 0u, 0u, 0u);
-    }
-    if (tid == 0) rG = rv[128];
-  };
-  fetch(NC - 1);
-  for (int c = NC - 1; c >= 0; --c) {
-    const size_t ri = (size_t)bh * NC + c;
-    const int t0 = 64 * c, Cc = min(64, a.T - t0);
-    __syncthreads();   // the previous chunk's readers of every buffer are done
-    // ---- dS_{c+1} for the local gradients
-    float* sv = g.w.dS + ri * 16384;
-    for (int e = tid; e < 128 * kNV / 4; e += kBwdThreads) {
-      const int r = e / (kNV / 4), n = 4 * (e % (kNV / 4));
-      *reinterpret_cast<float4*>(sv + r * 128 + n0 + n) =
-          *reinterpret_cast<const float4*>(sdS + r * cLDN + n);
-    }
-    // ---- operands from the registers: P and T (hi + lo), K and Q rows scaled, dO
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int e = tid + r * kBwdThreads, i = e >> 3, c0 = 8 * (e & 7);
-      float hh[8], ll[8];
-      unpack8(rPT[r][0], hh);
-      unpack8(rPT[r][1], ll);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) sP[i * cLD64T + c0 + q] = hh[q] + ll[q];
-      unpack8(rPT[r][2], hh);
-      unpack8(rPT[r][3], ll);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) sT[i * cLD64T + c0 + q] = hh[q] + ll[q];
-    }
-    if (PC) {   // the record's images (hi + lo); W'^T [c][j] -> W' [j][c]
-      const uint8_t* rec = g.w.rec + ri * g.w.recb;
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
-        const uint32_t off = (c0 >> 6) * 8192 + umma::sw128_offset(j, c0 & 63);
-        float qh[8], ql[8], wh[8], wl[8];
-        unpack8(*reinterpret_cast<const uint4*>(rec + rQPC + off), qh);
-        unpack8(*reinterpret_cast<const uint4*>(rec + rQPC + 16384 + off), ql);
-        unpack8(*reinterpret_cast<const uint4*>(rec + rWbPC + off), wh);
-        unpack8(*reinterpret_cast<const uint4*>(rec + rWbPC + 16384 + off), wl);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          sQg[j * cLDQ + c0 + q] = qh[q] + ql[q];
-          sWb[j * cLDW + c0 + q] = wh[q] + wl[q];
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int e = tid + r * kBwdThreads, cr = e >> 3, j0 = 8 * (e & 7);
-        const uint32_t off = umma::sw128_offset(cr, j0);
-        float hh[8], ll[8];
-        unpack8(*reinterpret_cast<const uint4*>(rec + rWpPC + off), hh);
-        unpack8(*reinterpret_cast<const uint4*>(rec + rWpPC + 16384 + off), ll);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) sKg[(j0 + q) * cLDQ + cr] = hh[q] + ll[q];
-      }
-      if (tid < 128) s_gam[tid] = reinterpret_cast<const float*>(rec + rVecF)[128 + tid];
-    }
-#pragma unroll
-    for (int r = 0; r < 4 && !PC; ++r) {
-      const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
-      float kf[8], qf[8], wf[8];
-      unpack8(rK[r], kf);
-      unpack8(rQ[r], qf);
-      if (PG) {
-        float wl[8];
-        unpack8(rWh[r], wf);
-        unpack8(rWl[r], wl);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) wf[q] += wl[q];
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) wf[q] = kf[q];
-      }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        sWb[j * cLDW + c0 + q] = rU[r] * wf[q];
-        sKg[j * cLDQ + c0 + q] = rEk[r] * kf[q];
-        sQg[j * cLDQ + c0 + q] = rEq[r] * qf[q];
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int e = tid + r * kBwdThreads, i = e >> 3, c0 = 8 * (e & 7);
-      float f[8];
-      unpack8(rO[r], f);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) sdO[i * cLDN + c0 + q] = f[q];
-    }
-    if (tid == 0) s_gamma = rG;
-    if (c > 0) fetch(c - 1);
-    __syncthreads();
-    // dE and dR: warp w takes row tile w & 3 and the 32 columns from 32 (w >> 2); the
-    // dS rows below are a row tile per warp
-    const int rt = 16 * (warp & 3), cq = 32 * (warp >> 2);
-    {
-      float d[4][4] = {};
-      mm3x<4, 8, true, false>(d, sP + rt, cLD64T, sdO + cq, cLDN, lane);
-      mm3x<4, 16, false, false>(d, sWb + rt * cLDW, cLDW, sdS + cq, cLDN, lane);
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          sdE[(rt + frag_row(lane, e)) * cLDN + cq + 8 * nt + frag_col(lane, e)] = d[nt][e];
-    }
-    __syncthreads();
-    // ---- dR = T^T dE, also dV (scalar decay: dR replaces dE once every warp has read it)
-    {
-      float d[4][4] = {};
-      mm3x<4, 8, true, false>(d, sT + rt, cLD64T, sdE + cq, cLDN, lane);
-      if (!PC) __syncthreads();
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = rt + frag_row(lane, e), n = cq + 8 * nt + frag_col(lane, e);
-          if (!PC) sdE[i * cLDN + n] = d[nt][e];
-          if (i < Cc) g.dv[tok(a, b, t0 + i, h) * 128 + n0 + n] = d[nt][e];
-        }
-    }
-    __syncthreads();
-    // ---- dS_c = gamma dS + (Gamma.Q^)^T dO - (Gamma.K^)^T dR (per-channel decay:
-    // (T Gamma.K)^T dE), warp: rows 16 warp .. + 16, 32 columns at a time
-#pragma unroll 1
-    for (int n32 = 0; n32 < kNV; n32 += 32) {
-      const float gam = s_gamma;
-      float d[4][4], m[4][4] = {};
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int row = 16 * warp + frag_row(lane, e);
-          d[nt][e] = (PC ? s_gam[row] : gam) * sdS[row * cLDN + n32 + 8 * nt + frag_col(lane, e)];
-        }
-      mm3x<4, 8, true, false>(d, sQg + 16 * warp, cLDQ, sdO + n32, cLDN, lane);
-      mm3x<4, 8, true, false>(m, sKg + 16 * warp, cLDQ, sdE + n32, cLDN, lane);
-      __syncwarp();
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          sdS[(16 * warp + frag_row(lane, e)) * cLDN + n32 + 8 * nt + frag_col(lane, e)] =
-              d[nt][e] - m[nt][e];
-    }
-  }
-  __syncthreads();
-  if (g.dS0) {
-    for (int e = tid; e < 128 * kNV; e += kBwdThreads) {
-      const int r = e / kNV, n = e % kNV;
-      g.dS0[((size_t)bh * 128 + r) * 128 + n0 + n] = sdS[r * cLDN + n];
-    }
-  }
-}
 
 // ================================================================= bwd_carry_tc
 // The reverse carry of the scalar-decay variants (GDN, KLA) on tcgen05: one CTA
@@ -507,7 +276,9 @@ constexpr uint32_t kcS = kcVec + 2048;  // dS hi | dS lo: [128 c][64 n] each (16
 constexpr uint32_t kcE = kcS + 32768;   // dE hi | dE lo [64][64] (8 KB each); then the dR exchange
 constexpr uint32_t kcR = kcE + 16384;   // dR' hi | lo; before it, the dE exchange
 constexpr uint32_t kcO2 = kcR + 16384;  // dO' hi | lo
+constexpr uint32_t kcW = kcO2 + 16384;  // PGDN: the record's write keys as [hi kb0 | lo kb0 | hi kb1 | lo kb1]
 constexpr uint32_t kCarryTcSmem = kcO2 + 16384 + 1024;
+constexpr uint32_t kCarryTcSmemPG = kcW + 32768 + 1024;
 constexpr uint32_t tcD1 = 0, tcD2 = 64, tcD3 = 192, tcD4 = 320, kCarryTcTmem = 512;
 constexpr uint32_t I_C1 = idesc_bf16(128, 64, 1, 1);
 constexpr uint32_t I_C2 = idesc_bf16(128, 128, 0, 1);
@@ -533,6 +304,9 @@ __device__ __forceinline__ void put_row32(uint8_t* base, uint32_t lo_off, int ro
   }
 }
 
+// PG (PGDN): W is explicit (the record's write keys, hi / lo), so G2 takes
+// [W_hi ; W_lo] in place of [K ; Q] and dE adds u . (hi.hi + hi.lo + lo.hi).
+template <bool PG>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_carry_tc_kernel(FwdArgs a, BwdArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -581,6 +355,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_carry_tc_kernel(FwdArgs a,
     for (int e = tid; e < 64; e += kBwdThreads) {   // vectors: sq, u, gamma at 128, sk at 192
       const float* rv = reinterpret_cast<const float*>(rec + rVecF);
       cpa16(sm + kcVec + (c & 1) * 1024 + 16 * e, rv + 4 * e);
+    }
+    for (int e = tid; PG && e < 2048; e += kBwdThreads) {   // PGDN write keys, rearranged per k-block
+      const uint32_t o = 16 * e, piece = o >> 13;
+      cpa16(sm + kcW + (piece & 1) * 16384 + (piece >> 1) * 8192 + (o & 8191), rec + rWF + o);
     }
     cpa_commit();
   };
@@ -636,9 +414,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_carry_tc_kernel(FwdArgs a,
       for (int ks = 0; ks < 4; ++ks)   // G1: K = 64 tokens
         mma_bf16(tmem + tcD1, desc_sw128(pb + ks * 2048, 8192, 1024), desc_sw128(ob + ks * 2048, 8192, 1024),
                  I_C1, ks > 0);
+      const uint32_t ab = PG ? smem_u32(sm + kcW) : kqb;   // [W_hi ; W_lo] or [K ; Q]
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)   // G2: K = 128 channels
-        mma_bf16(tmem + tcD2, desc_sw128(kqb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+        mma_bf16(tmem + tcD2, desc_sw128(ab + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
                  desc_sw128(sb + ks * 2048, 16384, 1024), I_C2, ks > 0);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)   // G4a: K = 64 tokens, A = Q^T (MN-major)
@@ -651,15 +430,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_carry_tc_kernel(FwdArgs a,
     __syncthreads();
     if (s_abort) break;
     tc_fence_after();
-    // ---- dE: lanes 64-127 hand D1's lo rows over; lanes 0-63 sum and write dE hi / lo
+    // ---- dE: lanes 64-127 hand D1's lo rows (PGDN: and u . W_lo dS_hi) over; lanes
+    //      0-63 sum and write dE hi / lo
     if (trow >= 64) {
-      float v[32];
+      float v[32], w[32];
       tmem_ld16(tl + tcD1 + 32 * hc, *reinterpret_cast<float(*)[16]>(v));
       tmem_ld16(tl + tcD1 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      if (PG) {
+        tmem_ld16(tl + tcD2 + 32 * hc, *reinterpret_cast<float(*)[16]>(w));
+        tmem_ld16(tl + tcD2 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(w + 16));
+      }
       tmem_ld_wait();
       const int i = trow - 64;
+      const float u = PG ? vec[64 + i] : 0.f;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) xch[i * 64 + ((32 * hc + e) ^ (i & 31))] = v[e];
+      for (int e = 0; e < 32; ++e) xch[i * 64 + ((32 * hc + e) ^ (i & 31))] = PG ? fmaf(u, w[e], v[e]) : v[e];
     }
     __syncthreads();
     if (trow < 64) {
@@ -2584,15 +2369,16 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
   if (pc) a.save_W = g.w.Wf;
   cudaError_t e = pc ? launch_kdn_split(a, DR_BF16, workspace, st) : launch_chunk_tc_split(a, workspace, st);
   if (e != cudaSuccess) return e;
-  const size_t c_smem = (size_t)kCarrySmemF * 4, s_smem = kStateSmem,
+  const size_t s_smem = kStateSmem,
                l_smem = kLocalSmem, p_smem = (size_t)kGainSmemF * 4,
                pm_smem = (size_t)kGainMapSmemF * 4;
-  if ((e = cudaFuncSetAttribute(bwd_carry_tc_kernel,
+  if ((e = cudaFuncSetAttribute(bwd_carry_tc_kernel<false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCarryTcSmem)) !=
           cudaSuccess ||
-      (e = cudaFuncSetAttribute(bwd_carry_kernel<true, false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c_smem)) !=
+      (e = cudaFuncSetAttribute(bwd_carry_tc_kernel<true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCarryTcSmemPG)) !=
           cudaSuccess ||
+
       (e = cudaFuncSetAttribute(bwd_carry_tc_pc_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCarryPcSmem)) !=
           cudaSuccess ||
@@ -2641,11 +2427,11 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
           cudaSuccess)
     return e;
   if (pg)
-    bwd_carry_kernel<true, false><<<fa.B * fa.H * 2, kBwdThreads, c_smem, st>>>(fa, g);
+    bwd_carry_tc_kernel<true><<<fa.B * fa.H * 2, kBwdThreads, kCarryTcSmemPG, st>>>(fa, g);
   else if (pc)
     bwd_carry_tc_pc_kernel<<<fa.B * fa.H * 2, kBwdThreads, kCarryPcSmem, st>>>(fa, g);
   else
-    bwd_carry_tc_kernel<<<fa.B * fa.H * 2, kBwdThreads, kCarryTcSmem, st>>>(fa, g);
+    bwd_carry_tc_kernel<false><<<fa.B * fa.H * 2, kBwdThreads, kCarryTcSmem, st>>>(fa, g);
   const int nsm = bwd_sm_count();
   if (nsm <= 0) return cudaErrorInvalidValue;
   bwd_state_kernel<<<(unsigned)(n < nsm ? n : nsm), kStateThreads, s_smem, st>>>(fa, g, n);
