@@ -1961,10 +1961,12 @@ __global__ void __launch_bounds__(128, 2) pgdn_gain_bwd_kernel(FwdArgs a, BwdArg
 // chunk's (A, B); gain_scan walks each row's maps backwards and leaves dp at
 // every chunk's end (and dL/dp_0); PHASE 1 (every chunk at once) runs the
 // chunk's tokens backwards from it and writes the gradients.
-constexpr int kKdnGainSmemF = 6 * 64 * 128;
+constexpr int kKdnGainSmemF = 6 * 64 * 128 + 4 * 128 * 4;
+constexpr int kGT = 512;                 // threads: four token parts of 16 per channel
+constexpr int kGW = kGT / 32;
 
 template <int PHASE>
-__global__ void __launch_bounds__(128, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
+__global__ void __launch_bounds__(kGT, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
   extern __shared__ __align__(16) float smf[];
   float* sK = smf;                  // k^ [t][c]
   float* sDW = sK + 64 * 128;       // dL/dw, then k^2 du
@@ -1972,165 +1974,210 @@ __global__ void __launch_bounds__(128, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs
   float* sA = sDK + 64 * 128;       // log-decay, then alpha
   float* sPh = sA + 64 * 128;       // omega, then p^
   float* sPo = sPh + 64 * 128;      // p (posterior)
+  float4* sMap = reinterpret_cast<float4*>(sPo + 64 * 128);   // [4 parts][128] part maps
   __shared__ float s_r[64], s_mr[64], s_cr[64], s_den[64], s_cc[64], s_iden[64], s_cd2[64];
-  const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int i = tid & 127, part = tid >> 7, t1 = 16 * part;   // channel, tokens t1 .. t1 + 15
   const int NC = (a.T + 63) / 64;
   const size_t ri = blockIdx.x;
   const int bh = (int)(ri / NC), c = (int)(ri % NC), b = bh / a.H, h = bh % a.H;
   const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
   const float mu = a.info_scale;
-  float dp = PHASE == 1 ? g.w.GE[ri * 128 + i] : 0.f;
+  const int t0 = 64 * c, Cc = min(64, a.T - t0);
+  if (tid < 64) {
+    s_r[tid] = tid < Cc ? a.r[tok(a, b, t0 + tid, h)] : 1.f;
+    s_mr[tid] = mu / s_r[tid];
+  }
+  for (int e = tid; e < 64 * 32; e += kGT) {
+    const int t = e >> 5, c4 = 4 * (e & 31);
+    const bool live = t < Cc;
+    const long o = tok(a, b, t0 + (live ? t : 0), h) * 128 + c4;
+    cpa16(sDW + t * 128 + c4, g.w.DW + ri * 8192 + t * 128 + c4, live ? 16 : 0);
+    if (PHASE == 1) cpa16(sDK + t * 128 + c4, g.dk + o, live ? 16 : 0);
+    cpa16(sA + t * 128 + c4, a.log_alpha + o, live ? 16 : 0);
+    cpa16(sPh + t * 128 + c4, a.omega + o, live ? 16 : 0);
+  }
+  for (int e = tid; e < 64 * 16; e += kGT) {   // raw keys
+    const int t = e >> 4, c0 = 8 * (e & 15);
+    float f[8];
+    if (t < Cc) {
+      unpack8(*reinterpret_cast<const uint4*>(K + tok(a, b, t0 + t, h) * 128 + c0), f);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) f[q] = 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) sK[t * 128 + c0 + q] = f[q];
+  }
+  cpa_wait_all();
+  __syncthreads();
+  for (int tt = 0; tt < 64 / kGW; ++tt) {   // key norms: warp w takes 4 tokens
+    const int t = (64 / kGW) * warp + tt;
+    float kk = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float x = sK[t * 128 + lane + 32 * m];
+      kk += x * x;
+    }
+    kk = warp_sum(kk);
+    if (lane == 0) s_cr[t] = a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f;
+  }
+  __syncthreads();
+  // the variance over the chunk from its chunk-start value: each part composes its
+  // tokens' maps of (n, d) (p = n / d; M = [[a^2, w], [u a^2, 1 + u w]], u = (mu / r) k^2),
+  // the chunk start through the earlier parts' maps gives its start, then it walks
+  const float p0 = c == 0 ? (a.aux0 ? a.aux0[(size_t)bh * 128 + i] : 1.f)
+                          : reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rP0PC)[i];
   {
-    const int t0 = 64 * c, Cc = min(64, a.T - t0);
-    if (i < 64) {
-      s_r[i] = i < Cc ? a.r[tok(a, b, t0 + i, h)] : 1.f;
-      s_mr[i] = mu / s_r[i];
+    float P0 = 1.f, P1 = 0.f, P2 = 0.f, P3 = 1.f;
+    for (int t = t1; t < t1 + 16 && t < Cc; ++t) {
+      const float kh = sK[t * 128 + i] * s_cr[t];
+      sK[t * 128 + i] = kh;
+      const float al = __expf(sA[t * 128 + i]), x = al * al, om = sPh[t * 128 + i];
+      sA[t * 128 + i] = al;
+      const float y = s_mr[t] * kh * kh;
+      const float q0 = fmaf(x, P0, om * P2), q1 = fmaf(x, P1, om * P3);
+      P2 = fmaf(y, q0, P2);
+      P3 = fmaf(y, q1, P3);
+      P0 = q0;
+      P1 = q1;
+      const float sc = __uint_as_float(0x7f000000u - (__float_as_uint(fmaxf(P3, P2)) & 0x7f800000u));
+      P0 *= sc;
+      P1 *= sc;
+      P2 *= sc;
+      P3 *= sc;
     }
-    for (int e = i; e < 64 * 32; e += 128) {
-      const int t = e >> 5, c4 = 4 * (e & 31);
-      const bool live = t < Cc;
-      const long o = tok(a, b, t0 + (live ? t : 0), h) * 128 + c4;
-      cpa16(sDW + t * 128 + c4, g.w.DW + ri * 8192 + t * 128 + c4, live ? 16 : 0);
-      if (PHASE == 1) cpa16(sDK + t * 128 + c4, g.dk + o, live ? 16 : 0);
-      cpa16(sA + t * 128 + c4, a.log_alpha + o, live ? 16 : 0);
-      cpa16(sPh + t * 128 + c4, a.omega + o, live ? 16 : 0);
-    }
-    for (int e = i; e < 64 * 16; e += 128) {   // raw keys
-      const int t = e >> 4, c0 = 8 * (e & 15);
-      float f[8];
-      if (t < Cc) {
-        unpack8(*reinterpret_cast<const uint4*>(K + tok(a, b, t0 + t, h) * 128 + c0), f);
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) f[q] = 0.f;
-      }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) sK[t * 128 + c0 + q] = f[q];
-    }
-    cpa_wait_all();
+    sMap[part * 128 + i] = make_float4(P0, P1, P2, P3);
     __syncthreads();
-    for (int tt = 0; tt < 16; ++tt) {   // key norms: warp w takes tokens 16 w .. + 15
-      const int t = 16 * warp + tt;
-      float kk = 0.f;
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float x = sK[t * 128 + lane + 32 * m];
-        kk += x * x;
-      }
-      kk = warp_sum(kk);
-      if (lane == 0) s_cr[t] = a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f;
+    float n = p0, d = 1.f;
+    for (int q = 0; q < part; ++q) {
+      const float4 Q = sMap[q * 128 + i];
+      const float n1 = fmaf(Q.x, n, Q.y * d), d1 = fmaf(Q.z, n, Q.w * d);
+      const float sc = __uint_as_float(0x7f000000u - (__float_as_uint(d1) & 0x7f800000u));
+      n = n1 * sc;
+      d = d1 * sc;
     }
-    __syncthreads();
-    // the variance over the chunk from its chunk-start value (thread i = channel i)
-    const float p0 = c == 0 ? (a.aux0 ? a.aux0[(size_t)bh * 128 + i] : 1.f)
-                            : reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rP0PC)[i];
-    {
-      float pv = p0;
-      for (int t = 0; t < Cc; ++t) {
-        const float kh = sK[t * 128 + i] * s_cr[t];
-        sK[t * 128 + i] = kh;
-        const float al = __expf(sA[t * 128 + i]);
-        const float ph = al * al * pv + sPh[t * 128 + i];
-        pv = __fdividef(ph, 1.f + s_mr[t] * kh * kh * ph);
-        sA[t * 128 + i] = al;
-        sPh[t * 128 + i] = ph;
-        sPo[t * 128 + i] = pv;
-      }
+    float pv = __fdividef(n, d);
+    for (int t = t1; t < t1 + 16 && t < Cc; ++t) {
+      const float kh = sK[t * 128 + i], al = sA[t * 128 + i];
+      const float ph = al * al * pv + sPh[t * 128 + i];
+      pv = __fdividef(ph, 1.f + s_mr[t] * kh * kh * ph);
+      sPh[t * 128 + i] = ph;
+      sPo[t * 128 + i] = pv;
     }
-    __syncthreads();
-    for (int tt = 0; tt < 16; ++tt) {   // den_t and c_t
-      const int t = 16 * warp + tt;
-      if (t >= Cc) break;
-      float z = 0.f, cc = 0.f;
+  }
+  __syncthreads();
+  for (int tt = 0; tt < 64 / kGW; ++tt) {   // den_t and c_t (warp w: 4 tokens)
+    const int t = (64 / kGW) * warp + tt;
+    if (t >= Cc) break;
+    float z = 0.f, cc = 0.f;
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int ch = lane + 32 * m;
-        const float kh = sK[t * 128 + ch], ph = sPh[t * 128 + ch];
-        z += ph * kh * kh;
-        cc += sDW[t * 128 + ch] * ph * kh;
-      }
-      z = warp_sum(z);
-      cc = warp_sum(cc);
-      if (lane == 0) {
-        const float den = s_r[t] + z;
-        s_den[t] = den;
-        s_cc[t] = cc;
-        s_iden[t] = 1.f / den;
-        s_cd2[t] = cc / (den * den);
-      }
+    for (int m = 0; m < 4; ++m) {
+      const int ch = lane + 32 * m;
+      const float kh = sK[t * 128 + ch], ph = sPh[t * 128 + ch];
+      z += ph * kh * kh;
+      cc += sDW[t * 128 + ch] * ph * kh;
     }
-    __syncthreads();
-    if (PHASE == 0) {   // the chunk's affine map dp_start = A dp_end + B, channel i
-      float A = 1.f, Bm = 0.f;
-      for (int t = Cc - 1; t >= 0; --t) {
-        const float kh = sK[t * 128 + i], ph = sPh[t * 128 + i], al = sA[t * 128 + i];
-        const float q1 = 1.f + s_mr[t] * kh * kh * ph;
-        const float a2 = al * al, f = a2 * __fdividef(1.f, q1 * q1);
-        const float x = sDW[t * 128 + i] * kh * s_iden[t] - s_cd2[t] * kh * kh;
-        A = f * A;
-        Bm = f * Bm + a2 * x;
-      }
-      g.w.GM[ri * 256 + i] = A;
-      g.w.GM[ri * 256 + 128 + i] = Bm;
-      return;
+    z = warp_sum(z);
+    cc = warp_sum(cc);
+    if (lane == 0) {
+      const float den = s_r[t] + z;
+      s_den[t] = den;
+      s_cc[t] = cc;
+      s_iden[t] = 1.f / den;
+      s_cd2[t] = cc / (den * den);
     }
-    // backwards over the chunk's tokens, per channel (the chain through dp)
-    for (int t = Cc - 1; t >= 0; --t) {
-      const float kh = sK[t * 128 + i], ph = sPh[t * 128 + i], al = sA[t * 128 + i];
-      const float dwv = sDW[t * 128 + i], iden = s_iden[t], cd2 = s_cd2[t], mr = s_mr[t];
-      const float q1 = 1.f + mr * kh * kh * ph;
-      const float iq2 = __fdividef(1.f, q1 * q1);
-      const float dph = dwv * kh * iden - cd2 * kh * kh + dp * iq2;
-      const float du = -dp * ph * ph * iq2;
-      sDK[t * 128 + i] += dwv * ph * iden - 2.f * cd2 * ph * kh + 2.f * mr * kh * du;
-      sDW[t * 128 + i] = kh * kh * du;
-      const float prev = t > 0 ? sPo[(t - 1) * 128 + i] : p0;
-      sA[t * 128 + i] = dph;                            // d omega
-      sPh[t * 128 + i] = 2.f * al * al * prev * dph;    // d log alpha through alpha^2 p
-      dp = al * al * dph;
+  }
+  __syncthreads();
+  // each part's affine map of the adjoint over its tokens, backwards: dp_start = A dp_end + B
+  float A = 1.f, Bm = 0.f;
+  for (int t = min(t1 + 15, Cc - 1); t >= t1; --t) {
+    const float kh = sK[t * 128 + i], ph = sPh[t * 128 + i], al = sA[t * 128 + i];
+    const float q1 = 1.f + s_mr[t] * kh * kh * ph;
+    const float a2 = al * al, f = a2 * __fdividef(1.f, q1 * q1);
+    const float x = sDW[t * 128 + i] * kh * s_iden[t] - s_cd2[t] * kh * kh;
+    A = f * A;
+    Bm = f * Bm + a2 * x;
+  }
+  __syncthreads();   // every part's map written over the forward maps' slots below
+  sMap[part * 128 + i] = make_float4(A, Bm, 0.f, 0.f);
+  __syncthreads();
+  if (PHASE == 0) {   // the chunk's map: part 0's of parts 1, 2, 3 in turn
+    if (part == 0) {
+      float Ac = 1.f, Bc = 0.f;
+      for (int q = 3; q >= 0; --q) {
+        const float4 M = sMap[q * 128 + i];
+        Bc = M.x * Bc + M.y;
+        Ac = M.x * Ac;
+      }
+      g.w.GM[ri * 256 + i] = Ac;
+      g.w.GM[ri * 256 + 128 + i] = Bc;
     }
-    __syncthreads();
-    {   // d omega out, d log alpha updated (coalesced; every load before the stores)
-      float4 la[16];
+    return;
+  }
+  // the adjoint at this part's end: the chunk end's value through the later parts' maps
+  float dp = g.w.GE[ri * 128 + i];
+  for (int q = 3; q > part; --q) {
+    const float4 M = sMap[q * 128 + i];
+    dp = M.x * dp + M.y;
+  }
+  // backwards over the part's tokens, per channel (the chain through dp)
+  for (int t = min(t1 + 15, Cc - 1); t >= t1; --t) {
+    const float kh = sK[t * 128 + i], ph = sPh[t * 128 + i], al = sA[t * 128 + i];
+    const float dwv = sDW[t * 128 + i], iden = s_iden[t], cd2 = s_cd2[t], mr = s_mr[t];
+    const float q1 = 1.f + mr * kh * kh * ph;
+    const float iq2 = __fdividef(1.f, q1 * q1);
+    const float dph = dwv * kh * iden - cd2 * kh * kh + dp * iq2;
+    const float du = -dp * ph * ph * iq2;
+    sDK[t * 128 + i] += dwv * ph * iden - 2.f * cd2 * ph * kh + 2.f * mr * kh * du;
+    sDW[t * 128 + i] = kh * kh * du;
+    const float prev = t > 0 ? sPo[(t - 1) * 128 + i] : p0;
+    sA[t * 128 + i] = dph;                            // d omega
+    sPh[t * 128 + i] = 2.f * al * al * prev * dph;    // d log alpha through alpha^2 p
+    dp = al * al * dph;
+  }
+  __syncthreads();
+  {   // d omega out, d log alpha updated (coalesced; every load before the stores)
+    constexpr int kR = 64 * 32 / kGT;
+    float4 la[kR];
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        const int e = i + 128 * r, t = e >> 5, c4 = 4 * (e & 31);
-        la[r] = t < Cc ? *reinterpret_cast<const float4*>(g.dla + tok(a, b, t0 + t, h) * 128 + c4)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        const int e = i + 128 * r, t = e >> 5, c4 = 4 * (e & 31);
-        if (t >= Cc) continue;
-        const long o = tok(a, b, t0 + t, h) * 128 + c4;
-        *reinterpret_cast<float4*>(g.domega + o) = *reinterpret_cast<const float4*>(sA + t * 128 + c4);
-        const float4 x = *reinterpret_cast<const float4*>(sPh + t * 128 + c4);
-        la[r].x += x.x; la[r].y += x.y; la[r].z += x.z; la[r].w += x.w;
-        *reinterpret_cast<float4*>(g.dla + o) = la[r];
-      }
+    for (int r = 0; r < kR; ++r) {
+      const int e = tid + kGT * r, t = e >> 5, c4 = 4 * (e & 31);
+      la[r] = t < Cc ? *reinterpret_cast<const float4*>(g.dla + tok(a, b, t0 + t, h) * 128 + c4)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    for (int tt = 0; tt < 16; ++tt) {   // d r and the key norm, warp w: tokens 16 w .. + 15
-      const int t = 16 * warp + tt;
-      if (t >= Cc) break;
-      float su = 0.f, dot = 0.f;
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int ch = lane + 32 * m;
-        su += sDW[t * 128 + ch];
-        dot += sK[t * 128 + ch] * sDK[t * 128 + ch];
-      }
-      su = warp_sum(su);
-      dot = warp_sum(dot);
-      const float rt = s_r[t], den = s_den[t];
-      if (lane == 0) g.dr[tok(a, b, t0 + t, h)] = -s_cc[t] / (den * den) - mu / (rt * rt) * su;
-      const float cr = s_cr[t];
-      float* dkrow = g.dk + tok(a, b, t0 + t, h) * 128;
+    for (int r = 0; r < kR; ++r) {
+      const int e = tid + kGT * r, t = e >> 5, c4 = 4 * (e & 31);
+      if (t >= Cc) continue;
+      const long o = tok(a, b, t0 + t, h) * 128 + c4;
+      *reinterpret_cast<float4*>(g.domega + o) = *reinterpret_cast<const float4*>(sA + t * 128 + c4);
+      const float4 x = *reinterpret_cast<const float4*>(sPh + t * 128 + c4);
+      la[r].x += x.x; la[r].y += x.y; la[r].z += x.z; la[r].w += x.w;
+      *reinterpret_cast<float4*>(g.dla + o) = la[r];
+    }
+  }
+  for (int tt = 0; tt < 64 / kGW; ++tt) {   // d r and the key norm, warp w: 4 tokens
+    const int t = (64 / kGW) * warp + tt;
+    if (t >= Cc) break;
+    float su = 0.f, dot = 0.f;
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int ch = lane + 32 * m;
-        const float v = sDK[t * 128 + ch];
-        dkrow[ch] = a.k_l2norm ? (v - sK[t * 128 + ch] * dot) * cr : v;
-      }
+    for (int m = 0; m < 4; ++m) {
+      const int ch = lane + 32 * m;
+      su += sDW[t * 128 + ch];
+      dot += sK[t * 128 + ch] * sDK[t * 128 + ch];
+    }
+    su = warp_sum(su);
+    dot = warp_sum(dot);
+    const float rt = s_r[t], den = s_den[t];
+    if (lane == 0) g.dr[tok(a, b, t0 + t, h)] = -s_cc[t] / (den * den) - mu / (rt * rt) * su;
+    const float cr = s_cr[t];
+    float* dkrow = g.dk + tok(a, b, t0 + t, h) * 128;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int ch = lane + 32 * m;
+      const float v = sDK[t * 128 + ch];
+      dkrow[ch] = a.k_l2norm ? (v - sK[t * 128 + ch] * dot) * cr : v;
     }
   }
 }
@@ -2440,9 +2487,9 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
     bwd_local_pc_kernel<DR_KDA><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
   } else if (fa.variant == DR_KDN) {
     bwd_local_pc_kernel<DR_KDN><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
-    kdn_gain_bwd_kernel<0><<<(unsigned)n, 128, kKdnGainSmemF * 4, st>>>(fa, g);
+    kdn_gain_bwd_kernel<0><<<(unsigned)n, kGT, kKdnGainSmemF * 4, st>>>(fa, g);
     gain_scan_kernel<<<fa.B * fa.H, 128, 0, st>>>(fa, g, 128);
-    kdn_gain_bwd_kernel<1><<<(unsigned)n, 128, kKdnGainSmemF * 4, st>>>(fa, g);
+    kdn_gain_bwd_kernel<1><<<(unsigned)n, kGT, kKdnGainSmemF * 4, st>>>(fa, g);
   } else if (fa.variant == DR_PKDA) {
     bwd_local_pc_kernel<DR_PKDA><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
     pgdn_gain_bwd_kernel<true, 0><<<(unsigned)n, 128, pm_smem, st>>>(fa, g);
