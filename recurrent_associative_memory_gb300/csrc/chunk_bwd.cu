@@ -1751,9 +1751,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ================================================================= pgdn_gain_bwd
-// One CTA per chunk, a thread per key channel.  The statistic A_t is recomputed
-// forward from its chunk-start value (the forward's record), then the tokens are
-// walked backwards (PDN notes Eq. (9)):
+// One CTA of 16 warps per chunk, four threads per key channel (16-token parts).  The
+// statistic A_t is recomputed forward from its chunk-start value (the forward's
+// record), then the tokens are walked backwards (PDN notes Eq. (9)):
 //   r = ln max(A, floor) - mu,  B = exp(-ln(x) r / (1 + |r|)),  w = eta B . k^
 //   d eta  = sum_i B k^ dw,   dr = -ln(x) B eta k^ dw / (1 + |r|)^2,
 //   dA_t = dA + [A > floor] dr / A,   d mu -= [A > floor] dr,
@@ -1771,140 +1771,173 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // gain_scan walks each row's maps backwards (dA at every chunk's end, dL/dA_0);
 // PHASE 1 (every chunk at once) runs the chunk backwards from it, writes the
 // gradients and the chunk's part of dL/dmu.
-constexpr int kGainSmemF = 4 * 64 * 128;
-constexpr int kGainMapSmemF = 3 * 64 * 128;   // PHASE 0 has no dL/dk^ buffer: two CTAs per SM
+constexpr int kGT = 512;                 // gain adjoints: four token parts of 16 per channel
+constexpr int kGW = kGT / 32;
+constexpr int kGainSmemF = 4 * 64 * 128 + 4 * 128 * 4 + 4 * 128;
+constexpr int kGainMapSmemF = kGainSmemF;
 
 template <bool PC, int PHASE>
-__global__ void __launch_bounds__(128, 2) pgdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
+__global__ void __launch_bounds__(kGT, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
   extern __shared__ __align__(16) float smf[];
   float* sK = smf;                  // k^ [t][i]
   float* sDW = sK + 64 * 128;       // dL/dw [t][i]
   float* sA = sDW + 64 * 128;       // A_t [t][i], then dA_t
   float* sDK = sA + 64 * 128;       // dL/dk^ [t][i]: the memory part, then the total (PHASE 1)
-  __shared__ float s_aP[64], s_bP[64], s_eta[64], s_cr[64], s_mu[4];
-  const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
+  float4* sMap = reinterpret_cast<float4*>(sDK + 64 * 128);   // [4 parts][128] part maps
+  float* sAs = reinterpret_cast<float*>(sMap + 4 * 128);      // [4 parts][128] A before each part
+  __shared__ float s_aP[64], s_bP[64], s_eta[64], s_cr[64], s_mu[kGW];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int i = tid & 127, part = tid >> 7, t1 = 16 * part;   // channel, tokens t1 .. t1 + 15
   const int NC = (a.T + 63) / 64;
   const size_t ri = blockIdx.x;
   const int bh = (int)(ri / NC), c = (int)(ri % NC), b = bh / a.H, h = bh % a.H;
   const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
   const float mu_h = a.mu[h];
-  float dA = PHASE == 1 ? g.w.GE[ri * 128 + i] : 0.f;
+  const int t0 = 64 * c, Cc = min(64, a.T - t0);
   float dmu = 0.f;
+  if (tid < 64) {
+    const bool live = tid < Cc;
+    const long ti = tok(a, b, t0 + (live ? tid : 0), h);
+    s_aP[tid] = live ? a.alphaP[ti] : 1.f;
+    s_bP[tid] = live ? a.betaP[ti] : 0.f;
+    s_eta[tid] = live ? a.eta[ti] : 0.f;
+    if (!PC) s_cr[tid] = live ? g.w.CR[ri * 64 + tid] : 0.f;
+  }
+  for (int e = tid; e < 64 * 32; e += kGT) {   // dL/dw and the memory part of dL/dk^
+    const int t = e >> 5, c4 = 4 * (e & 31);
+    const bool live = t < Cc;
+    cpa16(sDW + t * 128 + c4, g.w.DW + ri * 8192 + t * 128 + c4, live ? 16 : 0);
+    if (PHASE == 1)
+      cpa16(sDK + t * 128 + c4, g.dk + tok(a, b, t0 + (live ? t : 0), h) * 128 + c4, live ? 16 : 0);
+  }
+  cpa_wait_all();
+  __syncthreads();
+  for (int e = tid; e < 64 * 16; e += kGT) {   // k^ = k cr
+    const int t = e >> 4, c0 = 8 * (e & 15);
+    float f[8];
+    if (t < Cc) {
+      unpack8(*reinterpret_cast<const uint4*>(K + tok(a, b, t0 + t, h) * 128 + c0), f);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) f[q] = 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) sK[t * 128 + c0 + q] = PC ? f[q] : f[q] * s_cr[t];
+  }
+  __syncthreads();
+  if (PC) {   // key norms (warp w: 4 tokens), then k^ = k cr
+    for (int tt = 0; tt < 64 / kGW; ++tt) {
+      const int t = (64 / kGW) * warp + tt;
+      float kk = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float x = sK[t * 128 + lane + 32 * m];
+        kk += x * x;
+      }
+      kk = warp_sum(kk);
+      if (lane == 0) s_cr[t] = t < Cc ? (a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f) : 0.f;
+    }
+    __syncthreads();
+    for (int e = tid; e < 64 * 128; e += kGT) sK[e] *= s_cr[e >> 7];
+    __syncthreads();
+  }
+  // the statistic over the chunk from its chunk-start value: each part composes its
+  // tokens' affine maps A <- alphaP A + betaP k^2, the earlier parts' maps give its start
+  const float A0 =
+      PC ? (c == 0 ? (a.aux0 ? a.aux0[(size_t)bh * 128 + i] : 0.f)
+                   : reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rP0PC)[i])
+         : reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rAuxF)[256 + i];
   {
-    const int t0 = 64 * c, Cc = min(64, a.T - t0);
-    if (i < 64) {
-      const bool live = i < Cc;
-      const long ti = tok(a, b, t0 + (live ? i : 0), h);
-      s_aP[i] = live ? a.alphaP[ti] : 1.f;
-      s_bP[i] = live ? a.betaP[ti] : 0.f;
-      s_eta[i] = live ? a.eta[ti] : 0.f;
-      if (!PC) s_cr[i] = live ? g.w.CR[ri * 64 + i] : 0.f;
+    float Pm = 1.f, Pb = 0.f;
+    for (int t = t1; t < t1 + 16 && t < Cc; ++t) {
+      const float kv = sK[t * 128 + i];
+      Pm = s_aP[t] * Pm;
+      Pb = fmaf(s_aP[t], Pb, s_bP[t] * kv * kv);
     }
-    for (int e = i; e < 64 * 32; e += 128) {   // dL/dw and the memory part of dL/dk^
-      const int t = e >> 5, c4 = 4 * (e & 31);
-      const bool live = t < Cc;
-      cpa16(sDW + t * 128 + c4, g.w.DW + ri * 8192 + t * 128 + c4, live ? 16 : 0);
-      if (PHASE == 1)
-        cpa16(sDK + t * 128 + c4, g.dk + tok(a, b, t0 + (live ? t : 0), h) * 128 + c4, live ? 16 : 0);
-    }
-    cpa_wait_all();
+    sMap[part * 128 + i] = make_float4(Pm, Pb, 0.f, 0.f);
     __syncthreads();
-    for (int e = i; e < 64 * 16; e += 128) {   // k^ = k cr
-      const int t = e >> 4, c0 = 8 * (e & 15);
-      float f[8];
-      if (t < Cc) {
-        unpack8(*reinterpret_cast<const uint4*>(K + tok(a, b, t0 + t, h) * 128 + c0), f);
-      } else {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) f[q] = 0.f;
+    float A = A0;
+    for (int q = 0; q < part; ++q) {
+      const float4 M = sMap[q * 128 + i];
+      A = fmaf(M.x, A, M.y);
+    }
+    sAs[part * 128 + i] = A;
+    for (int t = t1; t < t1 + 16 && t < Cc; ++t) {
+      const float kv = sK[t * 128 + i];
+      A = s_aP[t] * A + s_bP[t] * kv * kv;
+      sA[t * 128 + i] = A;
+    }
+  }
+  // each part's affine map of the adjoint over its tokens, backwards:
+  // dA_start = M dA_end + N (token t: dA <- alphaP_t (dA + y_t), y_t = [A_t > floor] dr_t / A_t)
+  float M = 1.f, N = 0.f;
+  for (int t = min(t1 + 15, Cc - 1); t >= t1; --t) {
+    const float A = sA[t * 128 + i];
+    const float rr = logf(fmaxf(A, a.log_floor)) - mu_h;
+    const float den = 1.f + fabsf(rr);
+    const float Bv = expf(-a.ln_x * rr / den);
+    const float drr = -a.ln_x * Bv * (s_eta[t] * sK[t * 128 + i] * sDW[t * 128 + i]) / (den * den);
+    const float y = A > a.log_floor ? __fdividef(drr, A) : 0.f;
+    N = s_aP[t] * (N + y);
+    M = s_aP[t] * M;
+  }
+  __syncthreads();   // every part's forward map read
+  sMap[part * 128 + i] = make_float4(M, N, 0.f, 0.f);
+  __syncthreads();
+  if (PHASE == 0) {   // the chunk's map: the parts' maps composed from the last
+    if (part == 0) {
+      float Mc = 1.f, Nc = 0.f;
+      for (int q = 3; q >= 0; --q) {
+        const float4 Q = sMap[q * 128 + i];
+        Nc = Q.x * Nc + Q.y;
+        Mc = Q.x * Mc;
       }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) sK[t * 128 + c0 + q] = PC ? f[q] : f[q] * s_cr[t];
+      g.w.GM[ri * 256 + i] = Mc;
+      g.w.GM[ri * 256 + 128 + i] = Nc;
     }
-    __syncthreads();
-    if (PC) {   // key norms (warp w: tokens 16 w .. + 15), then k^ = k cr
-      for (int tt = 0; tt < 16; ++tt) {
-        const int t = 16 * warp + tt;
-        float kk = 0.f;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const float x = sK[t * 128 + lane + 32 * m];
-          kk += x * x;
-        }
-        kk = warp_sum(kk);
-        if (lane == 0) s_cr[t] = t < Cc ? (a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f) : 0.f;
-      }
-      __syncthreads();
-      for (int e = i; e < 64 * 128; e += 128) sK[e] *= s_cr[e >> 7];
-      __syncthreads();
-    }
-    // the statistic over the chunk from its chunk-start value
-    const float A0 =
-        PC ? (c == 0 ? (a.aux0 ? a.aux0[(size_t)bh * 128 + i] : 0.f)
-                     : reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rP0PC)[i])
-           : reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rAuxF)[256 + i];
-    {
-      float A = A0;
-      for (int t = 0; t < Cc; ++t) {
-        const float kv = sK[t * 128 + i];
-        A = s_aP[t] * A + s_bP[t] * kv * kv;
-        sA[t * 128 + i] = A;
-      }
-    }
-    if (PHASE == 0) {   // the chunk's affine map dA_start = M dA_end + N, channel i
-      float M = 1.f, N = 0.f;
-      for (int t = Cc - 1; t >= 0; --t) {
-        const float A = sA[t * 128 + i];
-        const float rr = logf(fmaxf(A, a.log_floor)) - mu_h;
-        const float den = 1.f + fabsf(rr);
-        const float Bv = expf(-a.ln_x * rr / den);
-        const float drr = -a.ln_x * Bv * (s_eta[t] * sK[t * 128 + i] * sDW[t * 128 + i]) / (den * den);
-        const float y = A > a.log_floor ? __fdividef(drr, A) : 0.f;
-        N = s_aP[t] * (N + y);
-        M = s_aP[t] * M;
-      }
-      g.w.GM[ri * 256 + i] = M;
-      g.w.GM[ri * 256 + 128 + i] = N;
-      return;
-    }
-    // backwards over the chunk's tokens: per channel only (the chain through dA);
-    // dA_t replaces A_t, and B k^ dw replaces dL/dw, for the sums over channels
-    for (int t = Cc - 1; t >= 0; --t) {
-      const float A = sA[t * 128 + i];
-      const float rr = logf(fmaxf(A, a.log_floor)) - mu_h;
-      const float den = 1.f + fabsf(rr);
-      const float Bv = expf(-a.ln_x * rr / den);
-      const float dwv = sDW[t * 128 + i], kv = sK[t * 128 + i], et = s_eta[t];
-      const float drr = -a.ln_x * Bv * (et * kv * dwv) / (den * den);
-      const bool above = A > a.log_floor;
-      const float dAt = dA + (above ? __fdividef(drr, A) : 0.f);
-      if (above) dmu -= drr;
-      sDK[t * 128 + i] += et * Bv * dwv + 2.f * s_bP[t] * kv * dAt;
-      sDW[t * 128 + i] = Bv * kv * dwv;
-      sA[t * 128 + i] = dAt;
-      dA = s_aP[t] * dAt;
-    }
-    __syncthreads();
-    // per token: d eta = sum B k^ dw, d alphaP = sum A_{t-1} dA_t, d betaP = sum k^2 dA_t,
-    // and the key norm (dk = (dk^ - k^ (k^ . dk^)) cr); warp w takes tokens 16 w .. + 15,
-    // a lane four channels, A_{t-1} recomputed from the chunk start on the way
+    return;
+  }
+  // the adjoint at this part's end: the chunk end's value through the later parts' maps
+  float dA = g.w.GE[ri * 128 + i];
+  for (int q = 3; q > part; --q) {
+    const float4 Q = sMap[q * 128 + i];
+    dA = Q.x * dA + Q.y;
+  }
+  // backwards over the part's tokens: per channel only (the chain through dA);
+  // dA_t replaces A_t, and B k^ dw replaces dL/dw, for the sums over channels
+  for (int t = min(t1 + 15, Cc - 1); t >= t1; --t) {
+    const float A = sA[t * 128 + i];
+    const float rr = logf(fmaxf(A, a.log_floor)) - mu_h;
+    const float den = 1.f + fabsf(rr);
+    const float Bv = expf(-a.ln_x * rr / den);
+    const float dwv = sDW[t * 128 + i], kv = sK[t * 128 + i], et = s_eta[t];
+    const float drr = -a.ln_x * Bv * (et * kv * dwv) / (den * den);
+    const bool above = A > a.log_floor;
+    const float dAt = dA + (above ? __fdividef(drr, A) : 0.f);
+    if (above) dmu -= drr;
+    sDK[t * 128 + i] += et * Bv * dwv + 2.f * s_bP[t] * kv * dAt;
+    sDW[t * 128 + i] = Bv * kv * dwv;
+    sA[t * 128 + i] = dAt;
+    dA = s_aP[t] * dAt;
+  }
+  __syncthreads();
+  // per token: d eta = sum B k^ dw, d alphaP = sum A_{t-1} dA_t, d betaP = sum k^2 dA_t,
+  // and the key norm (dk = (dk^ - k^ (k^ . dk^)) cr); warp w takes 4 tokens of part
+  // w / 4, a lane four channels, A_{t-1} recomputed from the part's start
+  {
+    const int tw = (64 / kGW) * warp, pw = tw >> 4;
     float Ap[4];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const int ch = lane + 32 * m;
-      Ap[m] = PC ? (c == 0 ? (a.aux0 ? a.aux0[(size_t)bh * 128 + ch] : 0.f)
-                           : reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rP0PC)[ch])
-                 : reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rAuxF)[256 + ch];
-    }
-    for (int t = 0; t < 16 * warp && t < Cc; ++t) {   // A up to this warp's first token
+    for (int m = 0; m < 4; ++m) Ap[m] = sAs[pw * 128 + lane + 32 * m];
+    for (int t = 16 * pw; t < tw && t < Cc; ++t) {
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const float kv = sK[t * 128 + lane + 32 * m];
         Ap[m] = s_aP[t] * Ap[m] + s_bP[t] * kv * kv;
       }
     }
-    for (int tt = 0; tt < 16; ++tt) {
-      const int t = 16 * warp + tt;
+    for (int tt = 0; tt < 64 / kGW; ++tt) {
+      const int t = tw + tt;
       if (t >= Cc) break;
       float se = 0.f, sa = 0.f, sb = 0.f, dot = 0.f;
 #pragma unroll
@@ -1940,14 +1973,19 @@ __global__ void __launch_bounds__(128, 2) pgdn_gain_bwd_kernel(FwdArgs a, BwdArg
   dmu = warp_sum(dmu);
   if (lane == 0) s_mu[warp] = dmu;
   __syncthreads();
-  if (i == 0) g.w.MU[ri] = s_mu[0] + s_mu[1] + s_mu[2] + s_mu[3];
+  if (tid == 0) {
+    float s = 0.f;
+    for (int w = 0; w < kGW; ++w) s += s_mu[w];
+    g.w.MU[ri] = s;
+  }
 }
 
 // ================================================================= kdn_gain_bwd
 // Diagonal KDN's write vector is the Kalman gain w = p^ . k^ / (r + sum_c p^ k^2)
 // with the predicted variance p^_t = alpha_t^2 p_{t-1} + omega_t and the posterior
 // p_t = p^_t / (1 + u_t p^_t), u_t = (mu / r_t) k^_t^2 (KDN notes Eq. (23) and
-// section 5).  One CTA per chunk, a thread per key channel: p^ and p are recomputed over the chunk from its chunk-start variance (the
+// section 5).  One CTA of 16 warps per chunk, four threads per key channel (16-token
+// parts, each composing its tokens' maps before it walks them): p^ and p are recomputed over the chunk from its chunk-start variance (the
 // forward's record), den_t = r_t + sum_c p^ k^2 and c_t = sum_c dw p^ k^ per token,
 // then the tokens are walked backwards with the variance adjoint dp (from dL/dp_T):
 //   dp^ = dw k^ / den - (c / den^2) k^2 + dp / q^2,  q = 1 + u p^,  du = -dp p^2 / q^2,
@@ -1962,8 +2000,6 @@ __global__ void __launch_bounds__(128, 2) pgdn_gain_bwd_kernel(FwdArgs a, BwdArg
 // every chunk's end (and dL/dp_0); PHASE 1 (every chunk at once) runs the
 // chunk's tokens backwards from it and writes the gradients.
 constexpr int kKdnGainSmemF = 6 * 64 * 128 + 4 * 128 * 4;
-constexpr int kGT = 512;                 // threads: four token parts of 16 per channel
-constexpr int kGW = kGT / 32;
 
 template <int PHASE>
 __global__ void __launch_bounds__(kGT, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
@@ -2217,7 +2253,7 @@ __global__ void gain_scan_kernel(FwdArgs a, BwdArgs g, int nch) {
 constexpr int kIkdnGainSmemF = 3 * 64 * 128;
 
 template <int PHASE>
-__global__ void __launch_bounds__(128, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
+__global__ void __launch_bounds__(kGT, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArgs g) {
   extern __shared__ __align__(16) float smf[];
   float* sK = smf;                  // k^ [t][c]
   float* sDW = sK + 64 * 128;       // dL/dw [t][c]
@@ -2239,14 +2275,14 @@ __global__ void __launch_bounds__(128, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArg
       s_r[i] = live ? a.r[ti] : 1.f;
       s_om[i] = live ? a.omega[ti] : 0.f;
     }
-    for (int e = i; e < 64 * 32; e += 128) {
+    for (int e = i; e < 64 * 32; e += kGT) {
       const int t = e >> 5, c4 = 4 * (e & 31);
       const bool live = t < Cc;
       const long o = tok(a, b, t0 + (live ? t : 0), h) * 128 + c4;
       cpa16(sDW + t * 128 + c4, g.w.DW + ri * 8192 + t * 128 + c4, live ? 16 : 0);
       cpa16(sA + t * 128 + c4, a.log_alpha + o, live ? 16 : 0);
     }
-    for (int e = i; e < 64 * 16; e += 128) {
+    for (int e = i; e < 64 * 16; e += kGT) {
       const int t = e >> 4, c0 = 8 * (e & 15);
       float f[8];
       if (t < Cc) {
@@ -2260,8 +2296,8 @@ __global__ void __launch_bounds__(128, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArg
     }
     cpa_wait_all();
     __syncthreads();
-    for (int tt = 0; tt < 16; ++tt) {   // per token: norm, s, abar, d beta (warp w: 16 w .. + 15)
-      const int t = 16 * warp + tt;
+    for (int tt = 0; tt < 64 / kGW; ++tt) {   // per token: norm, s, abar, d beta (warp w: 4 tokens)
+      const int t = (64 / kGW) * warp + tt;
       float kk = 0.f, a2 = 0.f;
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
@@ -2324,14 +2360,15 @@ __global__ void __launch_bounds__(128, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArg
     }
     __syncthreads();
     if (PHASE == 0) return;
-    float xk8[8][4], xl8[8][4];
+    constexpr int kTW = 64 / kGW;   // tokens per warp
+    float xk8[kTW][4], xl8[kTW][4];
 #pragma unroll
-    for (int tt = 0; tt < 16; ++tt) {   // per (token, channel), warp w: tokens 16 w .. + 15
-      const int t = 16 * warp + tt;
+    for (int tt = 0; tt < kTW; ++tt) {   // per (token, channel), warp w: tokens kTW w .. + kTW - 1
+      const int t = kTW * warp + tt;
       if (t >= Cc) continue;
-      if ((tt & 7) == 0) {   // the next 8 tokens' dk^ and d log alpha rows, before any store
+      if (tt == 0) {   // the warp's tokens' dk^ and d log alpha rows, before any store
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < kTW; ++u) {
           const int tu = t + u;
           const long ou = tok(a, b, t0 + (tu < Cc ? tu : 0), h) * 128;
 #pragma unroll
@@ -2356,9 +2393,9 @@ __global__ void __launch_bounds__(128, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArg
       for (int m = 0; m < 4; ++m) {
         const int ch = lane + 32 * m;
         const float kh = sK[t * 128 + ch];
-        dkh[m] = xk8[tt & 7][m] + (bhat / den) * sDW[t * 128 + ch] + 2.f * ds * kh;
+        dkh[m] = xk8[tt][m] + (bhat / den) * sDW[t * 128 + ch] + 2.f * ds * kh;
         dot += kh * dkh[m];
-        g.dla[tt_ * 128 + ch] = xl8[tt & 7][m] + fa * sA[t * 128 + ch];
+        g.dla[tt_ * 128 + ch] = xl8[tt][m] + fa * sA[t * 128 + ch];
       }
       dot = warp_sum(dot);
       const float cr = s_cr[t];
@@ -2492,22 +2529,22 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
     kdn_gain_bwd_kernel<1><<<(unsigned)n, kGT, kKdnGainSmemF * 4, st>>>(fa, g);
   } else if (fa.variant == DR_PKDA) {
     bwd_local_pc_kernel<DR_PKDA><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
-    pgdn_gain_bwd_kernel<true, 0><<<(unsigned)n, 128, pm_smem, st>>>(fa, g);
+    pgdn_gain_bwd_kernel<true, 0><<<(unsigned)n, kGT, pm_smem, st>>>(fa, g);
     gain_scan_kernel<<<fa.B * fa.H, 128, 0, st>>>(fa, g, 128);
-    pgdn_gain_bwd_kernel<true, 1><<<(unsigned)n, 128, p_smem, st>>>(fa, g);
+    pgdn_gain_bwd_kernel<true, 1><<<(unsigned)n, kGT, p_smem, st>>>(fa, g);
     pgdn_dmu_kernel<<<(fa.H + 127) / 128, 128, 0, st>>>(fa, g);
   } else if (fa.variant == DR_IKDN) {
     bwd_local_pc_kernel<DR_IKDN><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
-    ikdn_gain_bwd_kernel<0><<<(unsigned)n, 128, kIkdnGainSmemF * 4, st>>>(fa, g);
+    ikdn_gain_bwd_kernel<0><<<(unsigned)n, kGT, kIkdnGainSmemF * 4, st>>>(fa, g);
     gain_scan_kernel<<<fa.B * fa.H, 32, 0, st>>>(fa, g, 1);
-    ikdn_gain_bwd_kernel<1><<<(unsigned)n, 128, kIkdnGainSmemF * 4, st>>>(fa, g);
+    ikdn_gain_bwd_kernel<1><<<(unsigned)n, kGT, kIkdnGainSmemF * 4, st>>>(fa, g);
   } else if (fa.variant == DR_KLA) {
     bwd_local_kernel<DR_KLA><<<lgrid, kBwdThreads, l_smem, st>>>(fa, g, n);
   } else if (pg) {
     bwd_local_kernel<DR_PGDN><<<lgrid, kBwdThreads, l_smem, st>>>(fa, g, n);
-    pgdn_gain_bwd_kernel<false, 0><<<(unsigned)n, 128, pm_smem, st>>>(fa, g);
+    pgdn_gain_bwd_kernel<false, 0><<<(unsigned)n, kGT, pm_smem, st>>>(fa, g);
     gain_scan_kernel<<<fa.B * fa.H, 128, 0, st>>>(fa, g, 128);
-    pgdn_gain_bwd_kernel<false, 1><<<(unsigned)n, 128, p_smem, st>>>(fa, g);
+    pgdn_gain_bwd_kernel<false, 1><<<(unsigned)n, kGT, p_smem, st>>>(fa, g);
     pgdn_dmu_kernel<<<(fa.H + 127) / 128, 128, 0, st>>>(fa, g);
   } else {
     bwd_local_kernel<DR_GDN><<<lgrid, kBwdThreads, l_smem, st>>>(fa, g, n);
