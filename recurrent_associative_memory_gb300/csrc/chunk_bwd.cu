@@ -1472,8 +1472,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 constexpr int cKRS = 136;   // raw k, q rows (bf16): 272 bytes, 4 banks apart
 constexpr int kPcLocalSmem = (4 * 64 * cLDK + 2 * 64 * cLDM + 2 * 16 * cLDK) * 4 + 2 * 64 * cKRS * 2;
 
+constexpr int kLT = 512;   // bwd_local_pc: 16 warps
+constexpr int kLW = kLT / 32;
+
 template <int VARIANT>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kLT, 1)
     bwd_local_pc_kernel(FwdArgs a, BwdArgs g) {
   // every variant but KDA finishes its gain (and the key norm) in a gain kernel
   constexpr bool kGainK = VARIANT != DR_KDA;
@@ -1500,8 +1503,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   // ---- raw rows, w, log-decay, dP and dR E^T
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
+  for (int r = 0; r < 64 * 16 / kLT; ++r) {
+    const int e = tid + r * kLT, j = e >> 4, c0 = 8 * (e & 15);
     const bool live = j < Cc;
     const long o = tok(a, b, t0 + (live ? j : 0), h) * 128 + c0;
     *reinterpret_cast<uint4*>(sKr + j * cKRS + c0) =
@@ -1509,33 +1512,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     *reinterpret_cast<uint4*>(sQr + j * cKRS + c0) =
         live ? *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + o) : make_uint4(0u, 0u, 0u, 0u);
   }
-  for (int e = tid; e < 64 * 32; e += kBwdThreads) {
+  for (int e = tid; e < 64 * 32; e += kLT) {
     const int j = e >> 5, c4 = 4 * (e & 31);
     const bool live = j < Cc;
     cpa16(sW + j * cLDK + c4, g.w.Wf + (size_t)task * 8192 + j * 128 + c4);
     cpa16(sG + j * cLDK + c4, a.log_alpha + tok(a, b, t0 + (live ? j : 0), h) * 128 + c4, live ? 16 : 0);
   }
-  for (int e = tid; e < 64 * 16; e += kBwdThreads) {
+  for (int e = tid; e < 64 * 16; e += kLT) {
     const int i = e >> 4, c4 = 4 * (e & 15);
     cpa16(sMP + i * cLDM + c4, g.w.dP + (size_t)task * 4096 + i * 64 + c4);
     cpa16(sML + i * cLDM + c4, g.w.dL + (size_t)task * 4096 + i * 64 + c4);
   }
   if (tid < 64) s_eta[tid] = (!kGainK && tid < Cc) ? a.eta[tok(a, b, t0 + tid, h)] : 0.f;
-  for (int e = tid; e < 64 * 128; e += kBwdThreads) sDW[(e >> 7) * cLDK + (e & 127)] = 0.f;
+  for (int e = tid; e < 64 * 128; e += kLT) sDW[(e >> 7) * cLDK + (e & 127)] = 0.f;
   cpa_wait_all();
   __syncthreads();
-  {   // norms: four threads per row
-    const int j = tid >> 2, part = tid & 3;
+  {   // norms: eight threads per row
+    static_assert(kLT == 512, "eight threads per row");
+    const int j = tid >> 3, part = tid & 7;
     float kk = 0.f, qq = 0.f;
-    for (int c0 = 32 * part; c0 < 32 * part + 32; ++c0) {
+    for (int c0 = 16 * part; c0 < 16 * part + 16; ++c0) {
       const float x = bf(sKr[j * cKRS + c0]), y = bf(sQr[j * cKRS + c0]);
       kk += x * x;
       qq += y * y;
     }
-    kk += __shfl_xor_sync(0xffffffffu, kk, 1);
-    kk += __shfl_xor_sync(0xffffffffu, kk, 2);
-    qq += __shfl_xor_sync(0xffffffffu, qq, 1);
-    qq += __shfl_xor_sync(0xffffffffu, qq, 2);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      kk += __shfl_xor_sync(0xffffffffu, kk, o);
+      qq += __shfl_xor_sync(0xffffffffu, qq, o);
+    }
     if (part == 0) {
       s_cr[j] = a.k_l2norm ? 1.f / fmaxf(sqrtf(kk), 1e-30f) : 1.f;
       s_qn[j] = a.q_l2norm ? 1.f / fmaxf(sqrtf(qq), 1e-30f) : 1.f;
@@ -1548,7 +1553,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       sG[j * cLDK + tid] = gg;
     }
   }
-  for (int e = tid; e < 64 * 64; e += kBwdThreads) {
+  for (int e = tid; e < 64 * 64; e += kLT) {
     const int i = e >> 6, j = e & 63;
     sMP[i * cLDM + j] = (j <= i) ? sMP[i * cLDM + j] : 0.f;
     sML[i * cLDM + j] = (j < i) ? -sML[i * cLDM + j] : 0.f;
@@ -1558,7 +1563,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // ---- block rows I = 0..3
   for (int I = 0; I < 4; ++I) {
     const int nJ = 16 * (I + 1), m = 16 * I + 7;
-    for (int e = tid; e < nJ * 32; e += kBwdThreads) {   // w~ = w e^{g_m(I) - g}, rows j < 16 (I + 1)
+    for (int e = tid; e < nJ * 32; e += kLT) {   // w~ = w e^{g_m(I) - g}, rows j < 16 (I + 1)
       const int j = e >> 5, c4 = 4 * (e & 31);
       const float4 w4 = *reinterpret_cast<const float4*>(sW + j * cLDK + c4);
       const float4 g4 = *reinterpret_cast<const float4*>(sG + j * cLDK + c4);
@@ -1567,7 +1572,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           make_float4(w4.x * __expf(m4.x - g4.x), w4.y * __expf(m4.y - g4.y),
                       w4.z * __expf(m4.z - g4.z), w4.w * __expf(m4.w - g4.w));
     }
-    for (int e = tid; e < 16 * 32; e += kBwdThreads) {   // q~, k~ of the block's rows
+    for (int e = tid; e < 16 * 32; e += kLT) {   // q~, k~ of the block's rows
       const int r = e >> 5, c4 = 4 * (e & 31), i = 16 * I + r;
       const float4 g4 = *reinterpret_cast<const float4*>(sG + i * cLDK + c4);
       const float4 m4 = *reinterpret_cast<const float4*>(sG + m * cLDK + c4);
@@ -1586,30 +1591,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           make_float4(kf[0] * cr * f[0], kf[1] * cr * f[1], kf[2] * cr * f[2], kf[3] * cr * f[3]);
     }
     __syncthreads();
-    {   // dq^_P, dk^_L of the block's 16 rows (warp: columns 16 warp .. + 16)
-      float dq2[2][4] = {}, dk2[2][4] = {};
+    {   // dq^_P, dk^_L of the block's 16 rows (warp: columns kCW warp .. + kCW)
+      constexpr int kCW = 128 / kLW, kNT = kCW / 8;
+      float dq2[kNT][4] = {}, dk2[kNT][4] = {};
       for (int kk = 0; kk <= I; ++kk) {
-        mm3x<2, 2, false, false>(dq2, sMP + 16 * I * cLDM + 16 * kk, cLDM, sWt + 16 * kk * cLDK + 16 * warp,
-                                 cLDK, lane);
-        mm3x<2, 2, false, false>(dk2, sML + 16 * I * cLDM + 16 * kk, cLDM, sWt + 16 * kk * cLDK + 16 * warp,
-                                 cLDK, lane);
+        mm3x<kNT, 2, false, false>(dq2, sMP + 16 * I * cLDM + 16 * kk, cLDM,
+                                   sWt + 16 * kk * cLDK + kCW * warp, cLDK, lane);
+        mm3x<kNT, 2, false, false>(dk2, sML + 16 * I * cLDM + 16 * kk, cLDM,
+                                   sWt + 16 * kk * cLDK + kCW * warp, cLDK, lane);
       }
       // every raw X_Q / X_K value first (the stores below could alias them)
-      float xqa[2][4], xka[2][4];
+      float xqa[kNT][4], xka[kNT][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int i = 16 * I + frag_row(lane, e), cc = 16 * warp + 8 * nt + frag_col(lane, e);
+          const int i = 16 * I + frag_row(lane, e), cc = kCW * warp + 8 * nt + frag_col(lane, e);
           const long o = tok(a, b, t0 + (i < Cc ? i : 0), h) * 128 + cc;
           xqa[nt][e] = i < Cc ? g.dq[o] : 0.f;
           xka[nt][e] = i < Cc ? g.dk[o] : 0.f;
         }
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int i = 16 * I + frag_row(lane, e), cc = 16 * warp + 8 * nt + frag_col(lane, e);
+          const int i = 16 * I + frag_row(lane, e), cc = kCW * warp + 8 * nt + frag_col(lane, e);
           if (i < Cc) {
             const float gi = sG[i * cLDK + cc];
             const float sc = __expf(gi - sG[m * cLDK + cc]), eg = __expf(gi);
@@ -1624,7 +1630,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     }
     // dw of rows j < 16 (I + 1): M_P^T q~ + M_L^T k~ over the block's rows, times e^{g_m(I) - g_j}
-    for (int pp = warp; pp < 8 * (I + 1); pp += 8) {
+    for (int pp = warp; pp < 8 * (I + 1); pp += kLW) {
       const int mt = pp >> 3, nt0 = 2 * (pp & 7);
       float d2[2][4] = {};
       mm3x<2, 2, true, false>(d2, sMP + 16 * I * cLDM + 16 * mt, cLDM, sAq + 8 * nt0, cLDK, lane);
@@ -1643,8 +1649,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // ---- rows (eight threads per token, 16-byte pieces of the row side by side, two
   //      passes of 32 tokens): dw += e^{G - g} X_W, the column terms of dg, the write
   //      gain and the norms
-  for (int pass = 0; pass < 2; ++pass) {
-    const int j = 32 * pass + (tid >> 3), part = tid & 7;
+  for (int pass = 0; pass < 64 * 8 / kLT; ++pass) {
+    const int j = (kLT / 8) * pass + (tid >> 3), part = tid & 7;
     const bool live = j < Cc;
     const long o = tok(a, b, t0 + (live ? j : 0), h) * 128;
     const float* xw = g.w.XW + (size_t)task * 8192 + j * 128;
@@ -1743,7 +1749,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   }
   __syncthreads();
-  for (int e = tid; e < Cc * 32; e += kBwdThreads) {   // d log alpha out (coalesced)
+  for (int e = tid; e < Cc * 32; e += kLT) {   // d log alpha out (coalesced)
     const int j = e >> 5, c4 = 4 * (e & 31);
     *reinterpret_cast<float4*>(g.dla + tok(a, b, t0 + j, h) * 128 + c4) =
         *reinterpret_cast<const float4*>(sDW + j * cLDK + c4);
@@ -2521,20 +2527,20 @@ cudaError_t launch_chunk_bwd(const FwdArgs& fa, const void* d_out, const float* 
   bwd_state_kernel<<<(unsigned)(n < nsm ? n : nsm), kStateThreads, s_smem, st>>>(fa, g, n);
   const unsigned lgrid = (unsigned)(n < nsm ? n : nsm);
   if (fa.variant == DR_KDA) {
-    bwd_local_pc_kernel<DR_KDA><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
+    bwd_local_pc_kernel<DR_KDA><<<(unsigned)n, kLT, kPcLocalSmem, st>>>(fa, g);
   } else if (fa.variant == DR_KDN) {
-    bwd_local_pc_kernel<DR_KDN><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
+    bwd_local_pc_kernel<DR_KDN><<<(unsigned)n, kLT, kPcLocalSmem, st>>>(fa, g);
     kdn_gain_bwd_kernel<0><<<(unsigned)n, kGT, kKdnGainSmemF * 4, st>>>(fa, g);
     gain_scan_kernel<<<fa.B * fa.H, 128, 0, st>>>(fa, g, 128);
     kdn_gain_bwd_kernel<1><<<(unsigned)n, kGT, kKdnGainSmemF * 4, st>>>(fa, g);
   } else if (fa.variant == DR_PKDA) {
-    bwd_local_pc_kernel<DR_PKDA><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
+    bwd_local_pc_kernel<DR_PKDA><<<(unsigned)n, kLT, kPcLocalSmem, st>>>(fa, g);
     pgdn_gain_bwd_kernel<true, 0><<<(unsigned)n, kGT, pm_smem, st>>>(fa, g);
     gain_scan_kernel<<<fa.B * fa.H, 128, 0, st>>>(fa, g, 128);
     pgdn_gain_bwd_kernel<true, 1><<<(unsigned)n, kGT, p_smem, st>>>(fa, g);
     pgdn_dmu_kernel<<<(fa.H + 127) / 128, 128, 0, st>>>(fa, g);
   } else if (fa.variant == DR_IKDN) {
-    bwd_local_pc_kernel<DR_IKDN><<<(unsigned)n, kBwdThreads, kPcLocalSmem, st>>>(fa, g);
+    bwd_local_pc_kernel<DR_IKDN><<<(unsigned)n, kLT, kPcLocalSmem, st>>>(fa, g);
     ikdn_gain_bwd_kernel<0><<<(unsigned)n, kGT, kIkdnGainSmemF * 4, st>>>(fa, g);
     gain_scan_kernel<<<fa.B * fa.H, 32, 0, st>>>(fa, g, 1);
     ikdn_gain_bwd_kernel<1><<<(unsigned)n, kGT, kIkdnGainSmemF * 4, st>>>(fa, g);
