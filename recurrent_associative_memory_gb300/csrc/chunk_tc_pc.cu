@@ -406,12 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           a.aux[(long)bh * 128 + c] = end;
       }
       __syncthreads();
-    // every thread's hand-over store precedes the barrier; thread 0's fence and
-    // release store publish them at GPU scope (cumulative over the barrier)
-    if (chained && (kKdn || kPkda || kIkdn) && tid == 0 && ci + 1 < NC && ri + 1 != g_chain_withhold) {
-      __threadfence();
-      st_release_gpu(chain + ri + 1, 1u);
-    }
+      // every thread's hand-over store precedes the barrier; thread 0's release store
+      // publishes them at GPU scope (release semantics are cumulative over the barrier)
+      if (chained && tid == 0 && ci + 1 < NC && ri + 1 != g_chain_withhold)
+        st_release_gpu(chain + ri + 1, 1u);
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int o = (i0 + e) * 128 + c;
@@ -533,12 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncthreads();
-      // every thread's hand-over store precedes the barrier; thread 0's fence and
-      // release store publish them at GPU scope (cumulative over the barrier)
-      if (chained && (kKdn || kPkda || kIkdn) && tid == 0 && ci + 1 < NC && ri + 1 != g_chain_withhold) {
-        __threadfence();
+      // every thread's hand-over store precedes the barrier; thread 0's release store
+      // publishes them at GPU scope (release semantics are cumulative over the barrier)
+      if (chained && (kKdn || kPkda || kIkdn) && tid == 0 && ci + 1 < NC && ri + 1 != g_chain_withhold)
         st_release_gpu(chain + ri + 1, 1u);
-      }
     }
     if (kPkda) {   // the bound B(A) = exp(-ln(x) r / (1 + |r|)), r = log max(A, floor) - mu
                    // (PDN notes Eq. (9); fast log / exp), in place
