@@ -21,7 +21,7 @@
 //           sub-chunk, where it is bounded by the decay over 8 tokens.  bf16 hi/lo
 //           splits of both operands and three products keep fp32 accuracy.
 //   inverse T = (I + L)^-1: 16 x 16 diagonal blocks by substitution, the rest by
-//           recursive doubling (TF32x3 mma.sync: the blocks are below tcgen05's M).
+//           recursive doubling (bf16 hi/lo mma.sync: the blocks are below tcgen05's M).
 //   W'      W' = T (Gamma.K) on tcgen05 (Gamma.K = k^_i exp(g_i), hi/lo), read out
 //           transposed.
 //   record  T, W'^T, P, (Gamma.Q), Wbar = exp(g_C - g_j) w_j (bf16 hi/lo images),
@@ -861,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int blk = warp >> 1, nt = warp & 1;
       const int r0 = 32 * blk + 16, c0 = 32 * blk;
       float d[4] = {0.f, 0.f, 0.f, 0.f};
-      tile_mm3<2>(d, LT + r0 * LDL + c0, LDL, LT + c0 * LDL + c0 + 8 * nt, LDL, lane);
+      tile_mm3b<2>(d, LT + r0 * LDL + c0, LDL, LT + c0 * LDL + c0 + 8 * nt, LDL, lane);
       tile_store(XS + 16 * blk * LDX + 8 * nt, LDX, d, 1.f, lane);
     }
     __syncthreads();
@@ -869,14 +869,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int blk = warp >> 1, nt = warp & 1;
       const int r0 = 32 * blk + 16, c0 = 32 * blk;
       float d[4] = {0.f, 0.f, 0.f, 0.f};
-      tile_mm3<2>(d, LT + r0 * LDL + r0, LDL, XS + 16 * blk * LDX + 8 * nt, LDX, lane);
+      tile_mm3b<2>(d, LT + r0 * LDL + r0, LDL, XS + 16 * blk * LDX + 8 * nt, LDX, lane);
       tile_store(LT + r0 * LDL + c0 + 8 * nt, LDL, d, -1.f, lane);
     }
     __syncthreads();
     if (warp < 8) {
       const int mt = warp >> 2, nt = warp & 3;
       float d[4] = {0.f, 0.f, 0.f, 0.f};
-      tile_mm3<4>(d, LT + (32 + 16 * mt) * LDL, LDL, LT + 8 * nt, LDL, lane);
+      tile_mm3b<4>(d, LT + (32 + 16 * mt) * LDL, LDL, LT + 8 * nt, LDL, lane);
       tile_store(XS + 16 * mt * LDX + 8 * nt, LDX, d, 1.f, lane);
     }
     __syncthreads();
@@ -884,9 +884,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int mt = warp >> 2, nt = warp & 3;
       float d[4] = {0.f, 0.f, 0.f, 0.f};
       if (mt == 0)
-        tile_mm3<2>(d, LT + 32 * LDL + 32, LDL, XS + 8 * nt, LDX, lane);
+        tile_mm3b<2>(d, LT + 32 * LDL + 32, LDL, XS + 8 * nt, LDX, lane);
       else
-        tile_mm3<4>(d, LT + 48 * LDL + 32, LDL, XS + 8 * nt, LDX, lane);
+        tile_mm3b<4>(d, LT + 48 * LDL + 32, LDL, XS + 8 * nt, LDX, lane);
       tile_store(LT + (32 + 16 * mt) * LDL + 8 * nt, LDL, d, -1.f, lane);
     }
     __syncthreads();

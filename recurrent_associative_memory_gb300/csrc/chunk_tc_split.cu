@@ -13,7 +13,7 @@
 //   chunk_prep   one task per (b, h, chunk), 2 CTAs per SM, persistent.
 //                Gram [K; Q] W^T on tcgen05; gates, norms and write coefficients;
 //                L and P = lower((Q W^T) . e^{g_i - g_j}); T = (I + L)^-1 by
-//                16x16 forward substitution and TF32x3 recursive doubling;
+//                16x16 forward substitution and recursive doubling on bf16 hi/lo warp products;
 //                W' = T diag(e^g c) K on tcgen05.  Writes one record per chunk
 //                to the workspace: T, W' and P as bf16 hi/lo pairs, and the row
 //                vectors e^g qn, e^{g_C - g} c, gamma_C (PGDN adds its write keys
@@ -378,12 +378,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         }
       }
       named_bar(1, 256);
-      // level 1: T_10, T_32 ; level 2: the 32 x 32 lower-left block (TF32x3 mma.sync)
+      // level 1: T_10, T_32 ; level 2: the 32 x 32 lower-left block (bf16 hi/lo mma.sync)
       if (pwarp < 4) {
         const int blk = pwarp >> 1, nt = pwarp & 1;
         const int r0 = 32 * blk + 16, c0 = 32 * blk;
         float d[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_mm3<2>(d, LT + r0 * LDL + c0, LDL, LT + c0 * LDL + c0 + 8 * nt, LDL, lane);
+        tile_mm3b<2>(d, LT + r0 * LDL + c0, LDL, LT + c0 * LDL + c0 + 8 * nt, LDL, lane);
         tile_store(XS + 16 * blk * LDX + 8 * nt, LDX, d, 1.f, lane);
       }
       named_bar(1, 256);
@@ -391,14 +391,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         const int blk = pwarp >> 1, nt = pwarp & 1;
         const int r0 = 32 * blk + 16, c0 = 32 * blk;
         float d[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_mm3<2>(d, LT + r0 * LDL + r0, LDL, XS + 16 * blk * LDX + 8 * nt, LDX, lane);
+        tile_mm3b<2>(d, LT + r0 * LDL + r0, LDL, XS + 16 * blk * LDX + 8 * nt, LDX, lane);
         tile_store(LT + r0 * LDL + c0 + 8 * nt, LDL, d, -1.f, lane);
       }
       named_bar(1, 256);
       {
         const int mt = pwarp >> 2, nt = pwarp & 3;
         float d[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_mm3<4>(d, LT + (32 + 16 * mt) * LDL, LDL, LT + 8 * nt, LDL, lane);
+        tile_mm3b<4>(d, LT + (32 + 16 * mt) * LDL, LDL, LT + 8 * nt, LDL, lane);
         tile_store(XS + 16 * mt * LDX + 8 * nt, LDX, d, 1.f, lane);
       }
       named_bar(1, 256);
@@ -406,9 +406,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         const int mt = pwarp >> 2, nt = pwarp & 3;
         float d[4] = {0.f, 0.f, 0.f, 0.f};
         if (mt == 0)
-          tile_mm3<2>(d, LT + 32 * LDL + 32, LDL, XS + 8 * nt, LDX, lane);
+          tile_mm3b<2>(d, LT + 32 * LDL + 32, LDL, XS + 8 * nt, LDX, lane);
         else
-          tile_mm3<4>(d, LT + 48 * LDL + 32, LDL, XS + 8 * nt, LDX, lane);
+          tile_mm3b<4>(d, LT + 48 * LDL + 32, LDL, XS + 8 * nt, LDX, lane);
         tile_store(LT + (32 + 16 * mt) * LDL + 8 * nt, LDL, d, -1.f, lane);
       }
       named_bar(1, 256);

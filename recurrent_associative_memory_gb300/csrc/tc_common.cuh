@@ -99,6 +99,46 @@ static __device__ __forceinline__ void tile_mm3(float (&d)[4], const float* A, i
   for (int i = 0; i < 4; ++i) d[i] += dc[i];
 }
 
+// The same 16 x 8 tile product with each operand split into bf16 hi + lo and
+// m16n8k16 products (K = 16 per step, half the instructions of the TF32 form;
+// KSTEPS8 counts 8-wide steps and is even).  A lane's k slots (2t, 2t+1, 2t+8,
+// 2t+9) hold k0 + t + (0, 4, 8, 12) in A and B alike (a sum over k is order-free),
+// so it reads the addresses of two 8-wide steps.
+static __device__ __forceinline__ void bsplit2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(x0, x1);
+  lo = pack_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xFFFF0000u));
+}
+static __device__ __forceinline__ void mma_b16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32"
+      " {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+template <int KSTEPS8>
+static __device__ __forceinline__ void tile_mm3b(float (&d)[4], const float* A, int lda, const float* B,
+                                          int ldb, int lane) {
+  static_assert(KSTEPS8 % 2 == 0, "K must be a multiple of 16");
+  const int g = lane >> 2, t = lane & 3;
+  float dc[4] = {0.f, 0.f, 0.f, 0.f};   // correction terms, an independent accumulation chain
+#pragma unroll
+  for (int ks = 0; ks < KSTEPS8 / 2; ++ks) {
+    const int k0 = 16 * ks + t;
+    uint32_t ah[4], al[4], bh[2], bl[2];
+    bsplit2(A[g * lda + k0], A[g * lda + k0 + 4], ah[0], al[0]);
+    bsplit2(A[(g + 8) * lda + k0], A[(g + 8) * lda + k0 + 4], ah[1], al[1]);
+    bsplit2(A[g * lda + k0 + 8], A[g * lda + k0 + 12], ah[2], al[2]);
+    bsplit2(A[(g + 8) * lda + k0 + 8], A[(g + 8) * lda + k0 + 12], ah[3], al[3]);
+    bsplit2(B[k0 * ldb + g], B[(k0 + 4) * ldb + g], bh[0], bl[0]);
+    bsplit2(B[(k0 + 8) * ldb + g], B[(k0 + 12) * ldb + g], bh[1], bl[1]);
+    mma_b16816(dc, al, bh);
+    mma_b16816(dc, ah, bl);
+    mma_b16816(d, ah, bh);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] += dc[i];
+}
+
 // store a 16 x 8 fp32 fragment (scaled by s) at C[m0.., n0..]
 static __device__ __forceinline__ void tile_store(float* C, int ldc, const float (&d)[4], float s, int lane) {
   const int g = lane >> 2, t = lane & 3;
