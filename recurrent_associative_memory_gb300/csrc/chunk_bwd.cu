@@ -2245,7 +2245,8 @@ __global__ void gain_scan_kernel(FwdArgs a, BwdArgs g, int nch) {
 // abar_t = mean_c alpha_tc^2, w_t = beta_t k^_t, beta = b^ / (r + b^ s), s = ||k^||^2,
 // b_t = b^ / (1 + u b^), u = mu s / (dk r) (KDN notes Eq. (40)).  One CTA per chunk:
 // per token (in parallel) s, abar and d beta = k^ . dw; the
-// scalar chain over the chunk's tokens (thread 0; b^ recomputed from the chunk-start
+// scalar chain over the chunk's tokens (four lanes of warp 0, a 16-token part each
+// composing its tokens' maps before it walks; b^ recomputed from the chunk-start
 // variance of the record) with db (from dL/db_T):
 //   db^ = d beta r / den^2 + db / q^2,  q = 1 + u b^,  du = -db b^2 / q^2,  den = r + b^ s,
 //   d omega = db^,  db <- abar db^;
@@ -2272,7 +2273,6 @@ __global__ void __launch_bounds__(kGT, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArg
   const int bh = (int)(ri / NC), c = (int)(ri % NC), b = bh / a.H, h = bh % a.H;
   const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(a.k);
   const float mu = a.info_scale;
-  float db = PHASE == 1 ? g.w.GE[ri * 128] : 0.f;   // thread 0's chain
   {
     const int t0 = 64 * c, Cc = min(64, a.T - t0);
     if (i < 64) {
@@ -2333,35 +2333,81 @@ __global__ void __launch_bounds__(kGT, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArg
       }
     }
     __syncthreads();
-    if (i == 0) {   // the chunk's variances forward, then the chain backwards
-      float bv = c == 0 ? (a.aux0 ? a.aux0[bh] : 1.f)
-                        : reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rP0PC)[0];
-      for (int t = 0; t < Cc; ++t) {
+    if (warp == 0) {   // the chunk's variances forward, then the chain backwards, on
+                       // lanes 0-3 (a 16-token part each): every part composes its
+                       // tokens' maps, the earlier (later) parts' maps give its start
+      const int part = lane & 3, t1 = 16 * part, t2 = min(t1 + 16, Cc);
+      const float b0 = c == 0 ? (a.aux0 ? a.aux0[bh] : 1.f)
+                              : reinterpret_cast<const float*>(g.w.rec + ri * g.w.recb + rP0PC)[0];
+      // (n, d) -> [[ab, om], [u ab, 1 + u om]] (n, d), b = n / d, u = mu s / (dk r)
+      float P0 = 1.f, P1 = 0.f, P2 = 0.f, P3 = 1.f;
+      for (int t = t1; t < t2; ++t) {
+        const float x = s_ab[t], om = s_om[t], y = mu * s_s[t] / (128.f * s_r[t]);
+        const float q0 = fmaf(x, P0, om * P2), q1 = fmaf(x, P1, om * P3);
+        P2 = fmaf(y, q0, P2);
+        P3 = fmaf(y, q1, P3);
+        P0 = q0;
+        P1 = q1;
+        const float sc = __uint_as_float(0x7f000000u - (__float_as_uint(fmaxf(P3, P2)) & 0x7f800000u));
+        P0 *= sc;
+        P1 *= sc;
+        P2 *= sc;
+        P3 *= sc;
+      }
+      float n = b0, d = 1.f;
+      for (int q = 0; q < 3; ++q) {
+        const float Q0 = __shfl_sync(0xffffffffu, P0, q), Q1 = __shfl_sync(0xffffffffu, P1, q);
+        const float Q2 = __shfl_sync(0xffffffffu, P2, q), Q3 = __shfl_sync(0xffffffffu, P3, q);
+        if (q < part) {
+          const float n1 = fmaf(Q0, n, Q1 * d), d1 = fmaf(Q2, n, Q3 * d);
+          const float sc = __uint_as_float(0x7f000000u - (__float_as_uint(d1) & 0x7f800000u));
+          n = n1 * sc;
+          d = d1 * sc;
+        }
+      }
+      float bv = n / d;
+      for (int t = t1; t < t2 && lane < 4; ++t) {
         s_prev[t] = bv;
         const float bhat = s_ab[t] * bv + s_om[t];
         s_bh[t] = bhat;
         bv = bhat / (1.f + mu * s_s[t] / (128.f * s_r[t]) * bhat);
       }
-      if (PHASE == 0) {   // the chunk's affine map db_start = M db_end + N
-        float M = 1.f, N = 0.f;
-        for (int t = Cc - 1; t >= 0; --t) {
-          const float bhat = s_bh[t], rt = s_r[t], st = s_s[t];
-          const float den = rt + bhat * st, q1 = 1.f + mu * st / (128.f * rt) * bhat;
-          const float iq2 = 1.f / (q1 * q1);
-          N = s_ab[t] * (s_db[t] * rt / (den * den) + N * iq2);
-          M = s_ab[t] * iq2 * M;
-        }
-        g.w.GM[ri * 256] = M;
-        g.w.GM[ri * 256 + 128] = N;
-      }
-      for (int t = Cc - 1; PHASE == 1 && t >= 0; --t) {
+      // each part's affine map of the adjoint over its tokens, backwards
+      float M = 1.f, N = 0.f;
+      __syncwarp();
+      for (int t = t2 - 1; t >= t1; --t) {
         const float bhat = s_bh[t], rt = s_r[t], st = s_s[t];
         const float den = rt + bhat * st, q1 = 1.f + mu * st / (128.f * rt) * bhat;
         const float iq2 = 1.f / (q1 * q1);
-        const float dbh = s_db[t] * rt / (den * den) + db * iq2;
-        s_du[t] = -db * bhat * bhat * iq2;
-        s_dbh[t] = dbh;
-        db = s_ab[t] * dbh;
+        N = s_ab[t] * (s_db[t] * rt / (den * den) + N * iq2);
+        M = s_ab[t] * iq2 * M;
+      }
+      const float Ms[4] = {__shfl_sync(0xffffffffu, M, 0), __shfl_sync(0xffffffffu, M, 1),
+                           __shfl_sync(0xffffffffu, M, 2), __shfl_sync(0xffffffffu, M, 3)};
+      const float Ns[4] = {__shfl_sync(0xffffffffu, N, 0), __shfl_sync(0xffffffffu, N, 1),
+                           __shfl_sync(0xffffffffu, N, 2), __shfl_sync(0xffffffffu, N, 3)};
+      if (PHASE == 0) {   // the chunk's affine map db_start = M db_end + N
+        if (lane == 0) {
+          float Mc = 1.f, Nc = 0.f;
+          for (int q = 3; q >= 0; --q) {
+            Nc = Ms[q] * Nc + Ns[q];
+            Mc = Ms[q] * Mc;
+          }
+          g.w.GM[ri * 256] = Mc;
+          g.w.GM[ri * 256 + 128] = Nc;
+        }
+      } else if (lane < 4) {
+        float db = g.w.GE[ri * 128];   // the adjoint at the chunk end, then at this part's
+        for (int q = 3; q > part; --q) db = Ms[q] * db + Ns[q];
+        for (int t = t2 - 1; t >= t1; --t) {
+          const float bhat = s_bh[t], rt = s_r[t], st = s_s[t];
+          const float den = rt + bhat * st, q1 = 1.f + mu * st / (128.f * rt) * bhat;
+          const float iq2 = 1.f / (q1 * q1);
+          const float dbh = s_db[t] * rt / (den * den) + db * iq2;
+          s_du[t] = -db * bhat * bhat * iq2;
+          s_dbh[t] = dbh;
+          db = s_ab[t] * dbh;
+        }
       }
     }
     __syncthreads();
