@@ -1118,28 +1118,76 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
   int it = 0, nc = 0;
 
+  // L2 prefetch: this task's X_W, X_Q and X_K (read after its products) and the
+  // next task's raw rows and dP / dL, so those loads wait on L2 rather than HBM
+  auto prefetch = [&](long tk, bool now) {
+    if (tk >= n) return;
+    const int pbh = (int)(tk / NC), pc = (int)(tk % NC);
+    const int pb = pbh / a.H, ph = pbh % a.H, pt0 = 64 * pc, pCc = min(64, a.T - pt0);
+    const int j = tid & 63, part = tid >> 6;
+    if (j >= pCc) return;
+    const long o = tok(a, pb, pt0 + j, ph) * 128;
+    if (now) {
+      if (part == 0) l2_prefetch(g.dq + o, 512);
+      if (part == 1) l2_prefetch(g.dk + o, 512);
+      if (part == 2 && j < 16) l2_prefetch(g.w.XW + (size_t)tk * 8192 + 512 * j, 2048);
+    } else {
+      if (part == 0) l2_prefetch(K + o, 256);
+      if (part == 1) l2_prefetch(Qp + o, 256);
+      if (part == 2 && j < 8) l2_prefetch(g.w.dP + (size_t)tk * 4096 + 512 * j, 2048);
+      if (part == 3 && j < 8) l2_prefetch(g.w.dL + (size_t)tk * 4096 + 512 * j, 2048);
+      if (PG && part == 3 && j >= 8 && j < 24)
+        l2_prefetch(g.w.rec + (size_t)tk * g.w.recb + rWF + 2048 * (j - 8), 2048);
+    }
+  };
+  prefetch(blockIdx.x, false);
+
   for (long task = blockIdx.x; task < n; task += gridDim.x, ++it) {
     const int bh = (int)(task / NC), c = (int)(task % NC);
     const int b = bh / a.H, h = bh % a.H;
     const int t0 = 64 * c, Cc = min(64, a.T - t0);
-    // ---- raw rows, gates, PGDN's write-key images
+    prefetch(task, true);
+    prefetch(task + gridDim.x, false);
+    // ---- raw rows, gates, dP / dL (every load issued before the first shared-memory
+    //      store, which could otherwise alias them), PGDN's write-key images
+    float4 mp[4][2];   // dP / dL, used by the images below
+    {
+      uint4 rk[4], rq[4];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
-      const bool live = j < Cc;
-      const long o = tok(a, b, t0 + (live ? j : 0), h) * 128 + c0;
-      *reinterpret_cast<uint4*>(sKr + j * cKR + c0) =
-          live ? *reinterpret_cast<const uint4*>(K + o) : make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4*>(sQr + j * cKR + c0) =
-          live ? *reinterpret_cast<const uint4*>(Qp + o) : make_uint4(0u, 0u, 0u, 0u);
+      for (int r = 0; r < 4; ++r) {
+        const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
+        const bool live = j < Cc;
+        const long o = tok(a, b, t0 + (live ? j : 0), h) * 128 + c0;
+        rk[r] = live ? *reinterpret_cast<const uint4*>(K + o) : make_uint4(0u, 0u, 0u, 0u);
+        rq[r] = live ? *reinterpret_cast<const uint4*>(Qp + o) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int u = tid + r * kBwdThreads, row = u >> 3, j0 = 8 * (u & 7);
+        const float4* src = reinterpret_cast<const float4*>((row >= 64 ? g.w.dL : g.w.dP) +
+                                                            (size_t)task * 4096 + (row & 63) * 64 + j0);
+        mp[r][0] = src[0];
+        mp[r][1] = src[1];
+      }
+      float lg = 0.f, et = 0.f;
+      if (tid < Cc) {
+        lg = a.log_alpha[tok(a, b, t0 + tid, h)];
+        et = a.eta[tok(a, b, t0 + tid, h)];
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int e = tid + r * kBwdThreads, j = e >> 4, c0 = 8 * (e & 15);
+        *reinterpret_cast<uint4*>(sKr + j * cKR + c0) = rk[r];
+        *reinterpret_cast<uint4*>(sQr + j * cKR + c0) = rq[r];
+      }
+      if (tid < 64) {
+        s_g[tid] = lg;
+        s_eta[tid] = et;
+      }
     }
     if (PG) {
       const uint8_t* rw = g.w.rec + (size_t)task * g.w.recb + rWF;
       for (int e = tid; e < 32768 / 16; e += kBwdThreads) cpa16(sm + lW + 16 * e, rw + 16 * e);
-    }
-    if (tid < 64) {
-      s_g[tid] = (tid < Cc) ? a.log_alpha[tok(a, b, t0 + tid, h)] : 0.f;
-      s_eta[tid] = (tid < Cc) ? a.eta[tok(a, b, t0 + tid, h)] : 0.f;
     }
     __syncthreads();
     {   // norms: four threads per row
@@ -1214,9 +1262,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int u = tid + r * kBwdThreads, row = u >> 3, j0 = 8 * (u & 7);
       const bool isl = row >= 64;
       const int i = row & 63;
-      const float4* src = reinterpret_cast<const float4*>((isl ? g.w.dL : g.w.dP) +
-                                                          (size_t)task * 4096 + i * 64 + j0);
-      const float4 v0 = src[0], v1 = src[1];
+      const float4 v0 = mp[r][0], v1 = mp[r][1];
       const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
       const float gi = s_g[i];
       float x[8];

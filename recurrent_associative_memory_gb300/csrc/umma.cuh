@@ -108,6 +108,14 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Hint: bring `bytes` (a multiple of 16, from a 16-byte aligned address inside an
+// allocation) of global memory into L2 ahead of their loads.
+__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+
 // Contiguous bulk copy shared -> global, tracked by the issuing thread's bulk
 // async-groups (commit with bulk_commit, wait with bulk_wait_read / bulk_wait_all).
 __device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
