@@ -1118,26 +1118,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
   int it = 0, nc = 0;
 
-  // L2 prefetch: this task's X_W, X_Q and X_K (read after its products) and the
-  // next task's raw rows and dP / dL, so those loads wait on L2 rather than HBM
+  // L2 prefetch (one bulk hint per contiguous block): this task's X_W, read after its
+  // products, and the next task's dP / dL (and PGDN's write keys)
   auto prefetch = [&](long tk, bool now) {
-    if (tk >= n) return;
-    const int pbh = (int)(tk / NC), pc = (int)(tk % NC);
-    const int pb = pbh / a.H, ph = pbh % a.H, pt0 = 64 * pc, pCc = min(64, a.T - pt0);
-    const int j = tid & 63, part = tid >> 6;
-    if (j >= pCc) return;
-    const long o = tok(a, pb, pt0 + j, ph) * 128;
+    if (tk >= n || tid != 0) return;
     if (now) {
-      if (part == 0) l2_prefetch(g.dq + o, 512);
-      if (part == 1) l2_prefetch(g.dk + o, 512);
-      if (part == 2 && j < 16) l2_prefetch(g.w.XW + (size_t)tk * 8192 + 512 * j, 2048);
+      l2_prefetch(g.w.XW + (size_t)tk * 8192, 32768);
     } else {
-      if (part == 0) l2_prefetch(K + o, 256);
-      if (part == 1) l2_prefetch(Qp + o, 256);
-      if (part == 2 && j < 8) l2_prefetch(g.w.dP + (size_t)tk * 4096 + 512 * j, 2048);
-      if (part == 3 && j < 8) l2_prefetch(g.w.dL + (size_t)tk * 4096 + 512 * j, 2048);
-      if (PG && part == 3 && j >= 8 && j < 24)
-        l2_prefetch(g.w.rec + (size_t)tk * g.w.recb + rWF + 2048 * (j - 8), 2048);
+      l2_prefetch(g.w.dP + (size_t)tk * 4096, 16384);
+      l2_prefetch(g.w.dL + (size_t)tk * 4096, 16384);
+      if (PG) l2_prefetch(g.w.rec + (size_t)tk * g.w.recb + rWF, 32768);
     }
   };
   prefetch(blockIdx.x, false);
@@ -1320,6 +1310,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
     if (s_abort) break;
     tc_fence_after();
+    // X_Q (rows 0-63) and X_K (64-127) staged into the consumed IA images for G3:
+    // row-contiguous copies here, then each thread reads its own row (16-byte pieces
+    // XOR-swizzled by row, so a warp's 32 rows fall on distinct banks)
+    for (int u = tid; u < 128 * 32; u += kBwdThreads) {
+      const int r = u >> 5, ch = u & 31, i = r & 63;
+      const bool live = i < Cc;
+      const float* src = (r < 64 ? g.dq : g.dk) + tok(a, b, t0 + (live ? i : 0), h) * 128 + 4 * ch;
+      cpa16(sm + lA + r * 512 + ((ch ^ (r & 31)) << 4), src, live ? 16 : 0);
+    }
     // ---- G1: X_ij = M_P,ij (Q^W^T)_ij + M_L,ij (K^W^T)_ij (query rows first, then key rows)
     {
       float v[32];
@@ -1392,6 +1391,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       s_dbeta[j] = j < Cc ? dwk : 0.f;
       s_dGt[j] = s_ew[j] * xww;
     }
+    cpa_wait_all();
     __syncthreads();
     // ---- G3: rows of dq^ (TMEM rows 0-63) and dk^ (64-127); warp half hc takes 64 columns
     {
@@ -1399,7 +1399,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int i = trow & 63;
       const bool live = i < Cc;
       const float eg = __expf(s_g[i]);
-      float* orow = (isk ? g.dk : g.dq) + tok(a, b, t0 + (live ? i : 0), h) * 128 + 64 * hc;
+      float* xrow = reinterpret_cast<float*>(sm + lA + trow * 512);   // staged X_Q / X_K, out
+      auto xpiece = [&](int ch) { return reinterpret_cast<float4*>(xrow + 4 * (ch ^ (trow & 31))); };
       const uint16_t* rr = (isk ? sKr : sQr) + i * cKR + 64 * hc;
       const float sc = isk ? s_cr[i] : s_qn[i];
       const float bgain = (PG || !isk) ? 0.f : s_beta[i];
@@ -1411,8 +1412,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int p = 0; p < 2; ++p) {   // 32 columns: the raw row's loads first, then TMEM
         float4 x4[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          x4[e] = live ? *reinterpret_cast<const float4*>(orow + 32 * p + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int e = 0; e < 8; ++e) x4[e] = *xpiece(16 * hc + 8 * p + e);
         float v[32];
         tmem_ld16(tl + tG3 + 64 * hc + 32 * p, *reinterpret_cast<float(*)[16]>(v));
         tmem_ld16(tl + tG3 + 64 * hc + 32 * p + 16, *reinterpret_cast<float(*)[16]>(v + 16));
@@ -1446,7 +1446,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float xh = bf(rr[cc + f]) * sc;
             o4[f] = norm ? (d[cc + f] - xh * dot) * sc : d[cc + f];
           }
-          *reinterpret_cast<float4*>(orow + cc) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+          *xpiece(16 * hc + cc / 4) = make_float4(o4[0], o4[1], o4[2], o4[3]);
         }
         if (hc == 0) {
           const float x = s_xd[0][trow] + s_xd[1][trow];
@@ -1463,6 +1463,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    for (int u = tid; u < 128 * 32; u += kBwdThreads) {   // dq^, dk^ rows out (coalesced)
+      const int r = u >> 5, ch = u & 31, i = r & 63;
+      if (i < Cc)
+        *reinterpret_cast<float4*>((r < 64 ? g.dq : g.dk) + tok(a, b, t0 + i, h) * 128 + 4 * ch) =
+            *reinterpret_cast<const float4*>(sm + lA + r * 512 + ((ch ^ (r & 31)) << 4));
+    }
     // ---- d log alpha: reverse cumulative sum of dg, dG (+ gamma <dS, S_c>) on the last token
     if (warp == 0) {
       float x[2];
