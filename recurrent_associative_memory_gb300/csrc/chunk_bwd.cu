@@ -873,11 +873,6 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     s_abort = 0;
   }
   if (warp == 0) tmem_alloc(&tmem_base_s, kStateTmem);
-  for (int e = tid; e < 64 * 16; e += kStateThreads) {   // the dO rows' lo image: zero
-    const int r = e >> 4, c = e & 15;
-    *reinterpret_cast<uint4*>(sm + sAl + (c >> 3) * 16384 + r * 128 + (c & 7) * 16) =
-        make_uint4(0u, 0u, 0u, 0u);
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -894,7 +889,13 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     const float* Sc = g.w.S + (size_t)task * 16384;
     const float* Ec = g.w.E + (size_t)task * 8192;
     const float* dSc = g.w.dS + (size_t)task * 16384;
-    // ---- images: dO (bf16, copied as is), dR, S_c and E (hi / lo)
+    // ---- images: dO (bf16, copied as is; its lo rows zero, rewritten every task since
+    //      the previous task's outputs passed through them), dR, S_c and E (hi / lo)
+    for (int e = tid; e < 64 * 16; e += kStateThreads) {
+      const int r = e >> 4, cz = e & 15;
+      *reinterpret_cast<uint4*>(sm + sAl + (cz >> 3) * 16384 + r * 128 + (cz & 7) * 16) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
     for (int e = tid; e < 64 * 16; e += kStateThreads) {
       const int r = e >> 4, cc = e & 15;
       cpa16(sm + sAh + (cc >> 3) * 16384 + sw128_offset(r, 8 * (cc & 7)),
@@ -993,33 +994,46 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       mma_commit(&bars[1]);
       ++n2;
     }
-    // ---- D1, D2 out: warp (quadrant q, column quarter cq); lane = TMEM row
+    // ---- D1, D2 out: warp (quadrant q, column quarter cq); lane = TMEM row.  The rows
+    //      go out row-contiguously through shared memory: D1 through the [dO ; dR]
+    //      images (G1 and G2 have read them), D2 through the E images once G3 has
+    //      read those (16-byte pieces XOR-swizzled by row against bank conflicts)
     const int q = warp & 3, cq = warp >> 2, row = 32 * q + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
-    const int i = row & 63;
+    float z[16];
     {
-      float x[16], y[16], z[16];
+      float x[16], y[16];
       tmem_ld16(tl + tD1 + 32 * cq, x);
       tmem_ld16(tl + tD1 + 32 * cq + 16, y);
       tmem_ld16(tl + tD2 + 16 * cq, z);
       tmem_ld_wait();
-      if (i < Cc) {
-        float* dst = (row < 64 ? g.dq : g.dk) + tok(a, b, t0 + i, h) * 128 + 32 * cq;
+      uint8_t* st1 = sm + sAh + row * 512;
 #pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          *reinterpret_cast<float4*>(dst + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
-          *reinterpret_cast<float4*>(dst + 16 + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
-        }
+      for (int e = 0; e < 16; e += 4) {
+        const int ch = 8 * cq + e / 4;
+        *reinterpret_cast<float4*>(st1 + ((ch ^ (row & 31)) << 4)) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+        *reinterpret_cast<float4*>(st1 + (((ch + 4) ^ (row & 31)) << 4)) =
+            make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
       }
-      float* xd = (row < 64 ? g.w.dP : g.w.dL) + (size_t)task * 4096 + i * 64 + 16 * cq;
-#pragma unroll
-      for (int e = 0; e < 16; e += 4)
-        *reinterpret_cast<float4*>(xd + e) = make_float4(z[e], z[e + 1], z[e + 2], z[e + 3]);
+    }
+    __syncthreads();
+    for (int u = tid; u < 128 * 32; u += kStateThreads) {   // X_Q / X_K rows out
+      const int r = u >> 5, ch = u & 31, i = r & 63;
+      if (i < Cc)
+        *reinterpret_cast<float4*>((r < 64 ? g.dq : g.dk) + tok(a, b, t0 + i, h) * 128 + 4 * ch) =
+            *reinterpret_cast<const float4*>(sm + sAh + r * 512 + ((ch ^ (r & 31)) << 4));
     }
     if (!mbar_wait(&bars[1], it & 1, kWait)) s_abort = 1;
     __syncthreads();
     if (s_abort) break;
     tc_fence_after();
+    {
+      uint8_t* st2 = sm + sEh + row * 256;
+#pragma unroll
+      for (int e = 0; e < 16; e += 4)
+        *reinterpret_cast<float4*>(st2 + (((4 * cq + e / 4) ^ (row & 15)) << 4)) =
+            make_float4(z[e], z[e + 1], z[e + 2], z[e + 3]);
+    }
     {   // D3 = X_W^T: lane = state row n, column = token j -> X_W[j][n] (coalesced in n)
       float z[16];
       tmem_ld16(tl + tD3 + 16 * cq, z);
@@ -1027,6 +1041,12 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       float* xw = g.w.XW + (size_t)task * 8192 + row;
 #pragma unroll
       for (int e = 0; e < 16; ++e) xw[(16 * cq + e) * 128] = z[e];
+    }
+    __syncthreads();
+    for (int u = tid; u < 128 * 16; u += kStateThreads) {   // dO E^T / dR E^T rows out
+      const int r = u >> 4, ch = u & 15;
+      *reinterpret_cast<float4*>((r < 64 ? g.w.dP : g.w.dL) + (size_t)task * 4096 + (r & 63) * 64 + 4 * ch) =
+          *reinterpret_cast<const float4*>(sm + sEh + r * 256 + ((ch ^ (r & 15)) << 4));
     }
     tc_fence_before();
     __syncthreads();   // TMEM read and every image consumed before the next task
