@@ -95,9 +95,11 @@ inline int bwd_mode(int variant) {
 
 struct BwdWs {
   uint8_t* rec;   // [n] x kRecF
-  float* S;       // [n][128][128]  S_c
-  float* E;       // [n][64][128]   E
-  float* dS;      // [n][128][128]  dL/dS_{c+1}
+  // S, E and dS are stored as [32 column quads][rows][4] per chunk: the carries
+  // (one thread per row) write a warp's rows as one 512-byte piece
+  float* S;       // [n][32][128][4]  S_c
+  float* E;       // [n][32][64][4]   E
+  float* dS;      // [n][32][128][4]  dL/dS_{c+1}
   float* XW;      // [n][64][128]   E dS^T
   float* dP;      // [n][64][64]    dO E^T
   float* dL;      // [n][64][64]    dR E^T
@@ -381,9 +383,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_carry_tc_kernel(FwdArgs a,
     const int t0 = 64 * c, Cc = min(64, a.T - t0);
     // dL/dS_{c+1} for the local gradients; its hi / lo image for G2
     {
-      float* sv = g.w.dS + ri * 16384 + (size_t)trow * 128 + n0 + 32 * hc;
+      float* sv = g.w.dS + ri * 16384 + 4 * trow;
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(sv + e) = make_float4(ds[e], ds[e + 1], ds[e + 2], ds[e + 3]);
+      for (int e = 0; e < 32; e += 4)
+        *reinterpret_cast<float4*>(sv + (size_t)((n0 + 32 * hc + e) >> 2) * 512) =
+            make_float4(ds[e], ds[e + 1], ds[e + 2], ds[e + 3]);
       put_row32(sm + kcS, 16384, trow, 32 * hc, ds);
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -654,9 +658,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_carry_tc_pc_kernel(FwdArgs
     const size_t ri = (size_t)bh * NC + c;
     const int t0 = 64 * c, Cc = min(64, a.T - t0);
     {
-      float* sv = g.w.dS + ri * 16384 + (size_t)trow * 128 + n0 + 32 * hc;
+      float* sv = g.w.dS + ri * 16384 + 4 * trow;
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(sv + e) = make_float4(ds[e], ds[e + 1], ds[e + 2], ds[e + 3]);
+      for (int e = 0; e < 32; e += 4)
+        *reinterpret_cast<float4*>(sv + (size_t)((n0 + 32 * hc + e) >> 2) * 512) =
+            make_float4(ds[e], ds[e + 1], ds[e + 2], ds[e + 3]);
       put_row32(sm + kpS, 16384, trow, 32 * hc, ds);
     }
     asm volatile("cp.async.wait_group 1;" ::: "memory");   // this chunk's first group
@@ -857,6 +863,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   __shared__ uint64_t bars[2];
   __shared__ uint32_t tmem_base_s;
   __shared__ float s_red[kStateThreads / 32];
+  __shared__ float s_rowp[kStateThreads / 32][128];
   __shared__ volatile int s_abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NC = (a.T + 63) / 64;
@@ -901,29 +908,33 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       cpa16(sm + sAh + (cc >> 3) * 16384 + sw128_offset(r, 8 * (cc & 7)),
             dO + tok(a, b, t0 + min(r, Cc - 1), h) * 128 + 8 * cc, r < Cc ? 16 : 0);
     }
+    // S_c, E, dS in [column quad][row][4] order: element j of this thread is column
+    // quad warp + 16 (j >> 2) (k-block j >> 2, columns 4 warp ..) of row lane + 32 (j & 3)
     float4 sv[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      sv[j] = *reinterpret_cast<const float4*>(Sc + (16 * j + warp) * 128 + 4 * lane);
+      sv[j] = *reinterpret_cast<const float4*>(Sc + ((warp + 16 * (j >> 2)) * 128 + lane + 32 * (j & 3)) * 4);
     {
       float4 ev[4], rv[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
+        ev[j] = *reinterpret_cast<const float4*>(Ec + ((warp + 16 * (j >> 1)) * 64 + lane + 32 * (j & 1)) * 4);
         const int r = 16 * j + warp;
-        ev[j] = *reinterpret_cast<const float4*>(Ec + r * 128 + 4 * lane);
         rv[j] = r < Cc ? *reinterpret_cast<const float4*>(g.dv + tok(a, b, t0 + r, h) * 128 + 4 * lane)
                        : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int r = 16 * j + warp;
-        put4(sm + sEh + kb * 8192, sm + sEl + kb * 8192, sw128_offset(r, col), ev[j]);
+        put4(sm + sEh + (j >> 1) * 8192, sm + sEl + (j >> 1) * 8192, sw128_offset(lane + 32 * (j & 1), 4 * warp),
+             ev[j]);
         put4(sm + sAh + kb * 16384, sm + sAl + kb * 16384, sw128_offset(64 + r, col), rv[j]);
       }
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      put4(sm + sBh + kb * 16384, sm + sBl + kb * 16384, sw128_offset(16 * j + warp, col), sv[j]);
+      put4(sm + sBh + (j >> 2) * 16384, sm + sBl + (j >> 2) * 16384, sw128_offset(lane + 32 * (j & 3), 4 * warp),
+           sv[j]);
     cpa_wait_all();
     fence_proxy_async();
     __syncthreads();
@@ -949,18 +960,16 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     float4 dv[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      dv[j] = *reinterpret_cast<const float4*>(dSc + (16 * j + warp) * 128 + 4 * lane);
+      dv[j] = *reinterpret_cast<const float4*>(dSc + ((warp + 16 * (j >> 2)) * 128 + lane + 32 * (j & 3)) * 4);
     const float* rvec = reinterpret_cast<const float*>(g.w.rec + (size_t)task * g.w.recb + rVecF);
     float part = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float p = dv[j].x * sv[j].x + dv[j].y * sv[j].y + dv[j].z * sv[j].z + dv[j].w * sv[j].w;
-      if (pc) {
-        p = warp_sum(p);
-        if (lane == 0) g.w.SS[(size_t)task * 128 + 16 * j + warp] = rvec[128 + 16 * j + warp] * p;
-      } else {
-        part += p;
-      }
+    for (int j = 0; j < 4; ++j) {   // rows lane + 32 j: column quads warp and warp + 16
+      const float p = dv[j].x * sv[j].x + dv[j].y * sv[j].y + dv[j].z * sv[j].z + dv[j].w * sv[j].w +
+                      dv[j + 4].x * sv[j + 4].x + dv[j + 4].y * sv[j + 4].y + dv[j + 4].z * sv[j + 4].z +
+                      dv[j + 4].w * sv[j + 4].w;
+      if (pc) s_rowp[warp][lane + 32 * j] = p;
+      part += p;
     }
     if (!pc) {
       part = warp_sum(part);
@@ -974,10 +983,17 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       for (int w = 0; w < kStateThreads / 32; ++w) tsum += s_red[w];
       g.w.SS[task] = rvec[128] * tsum;
     }
+    if (pc && tid < 128) {   // gamma_c <dS, S_c>_c per state row: the 16 warps' parts
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < kStateThreads / 32; ++w) t += s_rowp[w][tid];
+      g.w.SS[(size_t)task * 128 + tid] = rvec[128 + tid] * t;
+    }
     // ---- dS's image over S_c's (G1 has read it), then G3
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      put4(sm + sBh + kb * 16384, sm + sBl + kb * 16384, sw128_offset(16 * j + warp, col), dv[j]);
+      put4(sm + sBh + (j >> 2) * 16384, sm + sBl + (j >> 2) * 16384, sw128_offset(lane + 32 * (j & 3), 4 * warp),
+           dv[j]);
     fence_proxy_async();
     __syncthreads();
     tc_fence_after();

@@ -977,11 +977,13 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
 
     for (int c = 0; c < NC; ++c) {
       const int slot = c & 1;
-      if (a.save_S) {   // backward: the state at this chunk's start
-        float* dst = a.save_S + (((size_t)bh * NCt + c0 + c) * 128 + srow) * 128 + half * 64 + 32 * hc;
+      if (a.save_S) {   // backward: the state at this chunk's start, as [32 column
+                        // quads][128 rows][4] (a warp's rows side by side: 512-byte stores)
+        float* dst = a.save_S + ((size_t)bh * NCt + c0 + c) * 16384 + 4 * srow;
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+          *reinterpret_cast<float4*>(dst + (size_t)((half * 64 + 32 * hc + j) >> 2) * 512) =
+              make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
       }
       float u_nxt = 0.f, g_nxt = 0.f;
       if (c + 1 < NC) {   // one chunk ahead; consumed next iteration
@@ -1024,12 +1026,13 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
             kv[e] += p.x; kv[e + 1] += p.y; kv[e + 2] += p.z; kv[e + 3] += p.w;
           }
         }
-        if (a.save_E) {   // backward: E(c), this thread's row and 16 columns
-          float* dst = a.save_E + (((size_t)bh * NCt + c0 + c) * 64 + erow) * 128 + half * 64 + 32 * hc +
-                       16 * keep;
+        if (a.save_E) {   // backward: E(c), this thread's row and 16 columns, as
+                          // [32 column quads][64 rows][4]
+          float* dst = a.save_E + ((size_t)bh * NCt + c0 + c) * 8192 + 4 * erow;
 #pragma unroll
           for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4*>(dst + e) = make_float4(kv[e], kv[e + 1], kv[e + 2], kv[e + 3]);
+            *reinterpret_cast<float4*>(dst + (size_t)((half * 64 + 32 * hc + 16 * keep + e) >> 2) * 256) =
+                make_float4(kv[e], kv[e + 1], kv[e + 2], kv[e + 3]);
         }
         uint8_t* Et = sm + cE;
 #pragma unroll
