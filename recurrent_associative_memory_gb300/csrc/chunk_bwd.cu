@@ -1897,6 +1897,12 @@ __global__ void __launch_bounds__(kGT, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArg
     s_eta[tid] = live ? a.eta[ti] : 0.f;
     if (!PC) s_cr[tid] = live ? g.w.CR[ri * 64 + tid] : 0.f;
   }
+  uint4 rk[64 * 16 / kGT];   // the raw keys, in flight with the copies below
+#pragma unroll
+  for (int r = 0; r < 64 * 16 / kGT; ++r) {
+    const int e = tid + r * kGT, t = e >> 4, c0 = 8 * (e & 15);
+    rk[r] = t < Cc ? *reinterpret_cast<const uint4*>(K + tok(a, b, t0 + t, h) * 128 + c0) : make_uint4(0u, 0u, 0u, 0u);
+  }
   for (int e = tid; e < 64 * 32; e += kGT) {   // dL/dw and the memory part of dL/dk^
     const int t = e >> 5, c4 = 4 * (e & 31);
     const bool live = t < Cc;
@@ -1906,15 +1912,11 @@ __global__ void __launch_bounds__(kGT, 1) pgdn_gain_bwd_kernel(FwdArgs a, BwdArg
   }
   cpa_wait_all();
   __syncthreads();
-  for (int e = tid; e < 64 * 16; e += kGT) {   // k^ = k cr
-    const int t = e >> 4, c0 = 8 * (e & 15);
-    float f[8];
-    if (t < Cc) {
-      unpack8(*reinterpret_cast<const uint4*>(K + tok(a, b, t0 + t, h) * 128 + c0), f);
-    } else {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) f[q] = 0.f;
-    }
+  for (int r = 0; r < 64 * 16 / kGT; ++r) {   // k^ = k cr
+    const int e = tid + r * kGT, t = e >> 4, c0 = 8 * (e & 15);
+    float f[8];
+    unpack8(rk[r], f);
 #pragma unroll
     for (int q = 0; q < 8; ++q) sK[t * 128 + c0 + q] = PC ? f[q] : f[q] * s_cr[t];
   }
@@ -2118,6 +2120,12 @@ __global__ void __launch_bounds__(kGT, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs
     s_r[tid] = tid < Cc ? a.r[tok(a, b, t0 + tid, h)] : 1.f;
     s_mr[tid] = mu / s_r[tid];
   }
+  uint4 rk[64 * 16 / kGT];   // the raw keys, in flight with the copies below
+#pragma unroll
+  for (int r = 0; r < 64 * 16 / kGT; ++r) {
+    const int e = tid + r * kGT, t = e >> 4, c0 = 8 * (e & 15);
+    rk[r] = t < Cc ? *reinterpret_cast<const uint4*>(K + tok(a, b, t0 + t, h) * 128 + c0) : make_uint4(0u, 0u, 0u, 0u);
+  }
   for (int e = tid; e < 64 * 32; e += kGT) {
     const int t = e >> 5, c4 = 4 * (e & 31);
     const bool live = t < Cc;
@@ -2127,15 +2135,11 @@ __global__ void __launch_bounds__(kGT, 1) kdn_gain_bwd_kernel(FwdArgs a, BwdArgs
     cpa16(sA + t * 128 + c4, a.log_alpha + o, live ? 16 : 0);
     cpa16(sPh + t * 128 + c4, a.omega + o, live ? 16 : 0);
   }
-  for (int e = tid; e < 64 * 16; e += kGT) {   // raw keys
-    const int t = e >> 4, c0 = 8 * (e & 15);
-    float f[8];
-    if (t < Cc) {
-      unpack8(*reinterpret_cast<const uint4*>(K + tok(a, b, t0 + t, h) * 128 + c0), f);
-    } else {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) f[q] = 0.f;
-    }
+  for (int r = 0; r < 64 * 16 / kGT; ++r) {
+    const int e = tid + r * kGT, t = e >> 4, c0 = 8 * (e & 15);
+    float f[8];
+    unpack8(rk[r], f);
 #pragma unroll
     for (int q = 0; q < 8; ++q) sK[t * 128 + c0 + q] = f[q];
   }
@@ -2369,6 +2373,12 @@ __global__ void __launch_bounds__(kGT, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArg
       s_r[i] = live ? a.r[ti] : 1.f;
       s_om[i] = live ? a.omega[ti] : 0.f;
     }
+    uint4 rk[64 * 16 / kGT];   // the raw keys, in flight with the copies below
+#pragma unroll
+    for (int r = 0; r < 64 * 16 / kGT; ++r) {
+      const int e = i + r * kGT, t = e >> 4, c0 = 8 * (e & 15);
+      rk[r] = t < Cc ? *reinterpret_cast<const uint4*>(K + tok(a, b, t0 + t, h) * 128 + c0) : make_uint4(0u, 0u, 0u, 0u);
+    }
     for (int e = i; e < 64 * 32; e += kGT) {
       const int t = e >> 5, c4 = 4 * (e & 31);
       const bool live = t < Cc;
@@ -2376,15 +2386,11 @@ __global__ void __launch_bounds__(kGT, 1) ikdn_gain_bwd_kernel(FwdArgs a, BwdArg
       cpa16(sDW + t * 128 + c4, g.w.DW + ri * 8192 + t * 128 + c4, live ? 16 : 0);
       cpa16(sA + t * 128 + c4, a.log_alpha + o, live ? 16 : 0);
     }
-    for (int e = i; e < 64 * 16; e += kGT) {
-      const int t = e >> 4, c0 = 8 * (e & 15);
-      float f[8];
-      if (t < Cc) {
-        unpack8(*reinterpret_cast<const uint4*>(K + tok(a, b, t0 + t, h) * 128 + c0), f);
-      } else {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) f[q] = 0.f;
-      }
+    for (int r = 0; r < 64 * 16 / kGT; ++r) {
+      const int e = i + r * kGT, t = e >> 4, c0 = 8 * (e & 15);
+      float f[8];
+      unpack8(rk[r], f);
 #pragma unroll
       for (int q = 0; q < 8; ++q) sK[t * 128 + c0 + q] = f[q];
     }
