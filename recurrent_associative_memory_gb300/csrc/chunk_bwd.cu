@@ -1688,32 +1688,41 @@ __global__ void __launch_bounds__(kLT, 1)
         mm3x<kNT, 2, false, false>(dk2, sML + 16 * I * cLDM + 16 * kk, cLDM,
                                    sWt + 16 * kk * cLDK + kCW * warp, cLDK, lane);
       }
-      // every raw X_Q / X_K value first (the stores below could alias them)
-      float xqa[kNT][4], xka[kNT][4];
+      // every raw X_Q / X_K value first (the stores below could alias them); a lane's
+      // fragment elements e and e + 1 are adjacent columns of one row: 8-byte accesses
+      float2 xqa[kNT][2], xka[kNT][2];
 #pragma unroll
       for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = 16 * I + frag_row(lane, e), cc = kCW * warp + 8 * nt + frag_col(lane, e);
+        for (int hh = 0; hh < 2; ++hh) {
+          const int i = 16 * I + frag_row(lane, 2 * hh), cc = kCW * warp + 8 * nt + frag_col(lane, 0);
           const long o = tok(a, b, t0 + (i < Cc ? i : 0), h) * 128 + cc;
-          xqa[nt][e] = i < Cc ? g.dq[o] : 0.f;
-          xka[nt][e] = i < Cc ? g.dk[o] : 0.f;
+          xqa[nt][hh] = i < Cc ? *reinterpret_cast<const float2*>(g.dq + o) : make_float2(0.f, 0.f);
+          xka[nt][hh] = i < Cc ? *reinterpret_cast<const float2*>(g.dk + o) : make_float2(0.f, 0.f);
         }
 #pragma unroll
       for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = 16 * I + frag_row(lane, e), cc = kCW * warp + 8 * nt + frag_col(lane, e);
+        for (int hh = 0; hh < 2; ++hh) {
+          const int i = 16 * I + frag_row(lane, 2 * hh), cc0 = kCW * warp + 8 * nt + frag_col(lane, 0);
           if (i < Cc) {
-            const float gi = sG[i * cLDK + cc];
-            const float sc = __expf(gi - sG[m * cLDK + cc]), eg = __expf(gi);
-            const float dqp = dq2[nt][e] * sc, dkl = dk2[nt][e] * sc;
-            const long o = tok(a, b, t0 + i, h) * 128 + cc;
-            const float xq = xqa[nt][e], xk = xka[nt][e];
-            const float qh = bf(sQr[i * cKRS + cc]) * s_qn[i], kh = bf(sKr[i * cKRS + cc]) * s_cr[i];
-            g.dq[o] = dqp + eg * xq;
-            g.dk[o] = dkl - eg * xk;
-            g.dla[o] = qh * dqp + kh * dkl + eg * (xq * qh - xk * kh);
+            float oq[2], ok[2], ol[2];
+#pragma unroll
+            for (int f = 0; f < 2; ++f) {
+              const int cc = cc0 + f;
+              const float gi = sG[i * cLDK + cc];
+              const float sc = __expf(gi - sG[m * cLDK + cc]), eg = __expf(gi);
+              const float dqp = dq2[nt][2 * hh + f] * sc, dkl = dk2[nt][2 * hh + f] * sc;
+              const float xq = f ? xqa[nt][hh].y : xqa[nt][hh].x, xk = f ? xka[nt][hh].y : xka[nt][hh].x;
+              const float qh = bf(sQr[i * cKRS + cc]) * s_qn[i], kh = bf(sKr[i * cKRS + cc]) * s_cr[i];
+              oq[f] = dqp + eg * xq;
+              ok[f] = dkl - eg * xk;
+              ol[f] = qh * dqp + kh * dkl + eg * (xq * qh - xk * kh);
+            }
+            const long o = tok(a, b, t0 + i, h) * 128 + cc0;
+            *reinterpret_cast<float2*>(g.dq + o) = make_float2(oq[0], oq[1]);
+            *reinterpret_cast<float2*>(g.dk + o) = make_float2(ok[0], ok[1]);
+            *reinterpret_cast<float2*>(g.dla + o) = make_float2(ol[0], ol[1]);
           }
         }
     }
