@@ -1706,7 +1706,7 @@ __global__ void __launch_bounds__(kLT, 1)
         for (int hh = 0; hh < 2; ++hh) {
           const int i = 16 * I + frag_row(lane, 2 * hh), cc0 = kCW * warp + 8 * nt + frag_col(lane, 0);
           if (i < Cc) {
-            float oq[2], ok[2], ol[2];
+            float oq[2], ok[2];
 #pragma unroll
             for (int f = 0; f < 2; ++f) {
               const int cc = cc0 + f;
@@ -1714,15 +1714,12 @@ __global__ void __launch_bounds__(kLT, 1)
               const float sc = __expf(gi - sG[m * cLDK + cc]), eg = __expf(gi);
               const float dqp = dq2[nt][2 * hh + f] * sc, dkl = dk2[nt][2 * hh + f] * sc;
               const float xq = f ? xqa[nt][hh].y : xqa[nt][hh].x, xk = f ? xka[nt][hh].y : xka[nt][hh].x;
-              const float qh = bf(sQr[i * cKRS + cc]) * s_qn[i], kh = bf(sKr[i * cKRS + cc]) * s_cr[i];
               oq[f] = dqp + eg * xq;
               ok[f] = dkl - eg * xk;
-              ol[f] = qh * dqp + kh * dkl + eg * (xq * qh - xk * kh);
             }
             const long o = tok(a, b, t0 + i, h) * 128 + cc0;
             *reinterpret_cast<float2*>(g.dq + o) = make_float2(oq[0], oq[1]);
             *reinterpret_cast<float2*>(g.dk + o) = make_float2(ok[0], ok[1]);
-            *reinterpret_cast<float2*>(g.dla + o) = make_float2(ol[0], ol[1]);
           }
         }
     }
@@ -1764,12 +1761,11 @@ __global__ void __launch_bounds__(kLT, 1)
       const float4 x4 = live ? *reinterpret_cast<const float4*>(xw + c0) : z4;
       const float4 k4v = live ? *reinterpret_cast<const float4*>(g.dk + o + c0) : z4;
       const float4 q4v = live ? *reinterpret_cast<const float4*>(g.dq + o + c0) : z4;
-      const float4 l4 = live ? *reinterpret_cast<const float4*>(g.dla + o + c0) : z4;
       const uint2 kr = *reinterpret_cast<const uint2*>(sKr + j * cKRS + c0);
       const uint2 qr = *reinterpret_cast<const uint2*>(sQr + j * cKRS + c0);
       const float gg[4] = {g4.x, g4.y, g4.z, g4.w}, gc[4] = {gC4.x, gC4.y, gC4.z, gC4.w};
       const float ww[4] = {w4.x, w4.y, w4.z, w4.w}, dg4[4] = {d4.x, d4.y, d4.z, d4.w};
-      const float xx[4] = {x4.x, x4.y, x4.z, x4.w}, ll[4] = {l4.x, l4.y, l4.z, l4.w};
+      const float xx[4] = {x4.x, x4.y, x4.z, x4.w};
       const float kk[4] = {k4v.x, k4v.y, k4v.z, k4v.w}, qq[4] = {q4v.x, q4v.y, q4v.z, q4v.w};
       const float kf[4] = {__uint_as_float(kr.x << 16), __uint_as_float(kr.x & 0xFFFF0000u),
                            __uint_as_float(kr.y << 16), __uint_as_float(kr.y & 0xFFFF0000u)};
@@ -1791,9 +1787,10 @@ __global__ void __launch_bounds__(kLT, 1)
           deta += kh[q] * dw;
         }
         dwo[e] = dw;
-        // the token's whole dg (the Gram's row terms and the state terms came from the
-        // block rows through d log alpha's array); kept here for the sums below
-        dgo[e] = live ? ll[e] - ww[e] * dg4[e] - ww[e] * ew * xx[e] : 0.f;
+        // the token's whole dg: the Gram's row terms and the state terms are
+        // q^ . dq^ + k^ . dk^ of the block rows' dq^, dk^ (the Gram part and e^g X_Q,
+        // -e^g X_K); kept here for the sums below
+        dgo[e] = live ? qh[q] * qq[e] + kh[q] * kk[e] - ww[e] * dg4[e] - ww[e] * ew * xx[e] : 0.f;
         dotk += dkh[q] * kh[q];
         dotq += dqh[q] * qh[q];
       }
