@@ -1580,6 +1580,7 @@ __global__ void __launch_bounds__(kLT, 1)
   uint16_t* sKr = reinterpret_cast<uint16_t*>(sDW + 64 * cLDK);   // raw k, q (bf16) [j][cKRS]
   uint16_t* sQr = sKr + 64 * cKRS;
   __shared__ float s_cr[64], s_qn[64], s_eta[64];
+  __shared__ float s_scan[4][128], s_scan2[4][128];   // channel scans: the parts' totals
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NC = (a.T + 63) / 64;
@@ -1634,17 +1635,28 @@ __global__ void __launch_bounds__(kLT, 1)
       s_qn[j] = a.q_l2norm ? 1.f / fmaxf(sqrtf(qq), 1e-30f) : 1.f;
     }
   }
-  if (tid < 128) {   // cumulative log-decay, channel tid
+  float gl[16];   // cumulative log-decay: four threads per channel, 16 tokens each
+  const int sch = tid & 127, spart = tid >> 7;
+  {
     float gg = 0.f;
-    for (int j = 0; j < 64; ++j) {
-      gg += sG[j * cLDK + tid];
-      sG[j * cLDK + tid] = gg;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      gg += sG[(16 * spart + q) * cLDK + sch];
+      gl[q] = gg;
     }
+    s_scan[spart][sch] = gg;
   }
   for (int e = tid; e < 64 * 64; e += kLT) {
     const int i = e >> 6, j = e & 63;
     sMP[i * cLDM + j] = (j <= i) ? sMP[i * cLDM + j] : 0.f;
     sML[i * cLDM + j] = (j < i) ? -sML[i * cLDM + j] : 0.f;
+  }
+  __syncthreads();
+  {
+    float off = 0.f;
+    for (int p = 0; p < spart; ++p) off += s_scan[p][sch];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) sG[(16 * spart + q) * cLDK + sch] = gl[q] + off;
   }
   __syncthreads();
 
@@ -1831,15 +1843,32 @@ __global__ void __launch_bounds__(kLT, 1)
     }
   }
   __syncthreads();
-  // ---- per channel: dG on the last token, then d log alpha = the reverse cumulative sum
-  if (tid < 128) {   // (the tokens' parts of dG_c were left in the w~ buffer by the rows)
-    const int cc = tid;
-    float dG = g.w.SS[(size_t)task * 128 + cc];
-    for (int j = 0; j < Cc; ++j) dG += sWt[j * cLDK + cc];
-    float acc = 0.f;
-    for (int j = Cc - 1; j >= 0; --j) {
-      acc += sDW[j * cLDK + cc] + (j == Cc - 1 ? dG : 0.f);
-      sDW[j * cLDK + cc] = acc;
+  // ---- per channel: dG on the last token, then d log alpha = the reverse cumulative
+  //      sum (four threads per channel, 16 tokens each; the tokens' parts of dG_c were
+  //      left in the w~ buffer by the rows)
+  {
+    float dg[16], acc = 0.f, dGp = 0.f;
+#pragma unroll
+    for (int q = 15; q >= 0; --q) {
+      const int j = 16 * spart + q;
+      if (j < Cc) {
+        acc += sDW[j * cLDK + sch];
+        dGp += sWt[j * cLDK + sch];
+      }
+      dg[q] = acc;
+    }
+    s_scan[spart][sch] = acc;
+    s_scan2[spart][sch] = dGp;
+    __syncthreads();
+    float off = g.w.SS[(size_t)task * 128 + sch];
+    for (int p = 0; p < 4; ++p) {
+      off += s_scan2[p][sch];
+      if (p > spart) off += s_scan[p][sch];
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int j = 16 * spart + q;
+      if (j < Cc) sDW[j * cLDK + sch] = dg[q] + off;
     }
   }
   __syncthreads();
