@@ -1590,16 +1590,17 @@ __global__ void __launch_bounds__(kLT, 1)
   const int t0 = 64 * c, Cc = min(64, a.T - t0);
   auto bf = [](uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); };
 
-  // ---- raw rows, w, log-decay, dP and dR E^T
+  // ---- raw rows (loaded ahead of the copies, stored after them: a store first could
+  //      alias the loads), w, log-decay, dP and dR E^T
+  constexpr int kRR = 64 * 16 / kLT;
+  uint4 rk[kRR], rq[kRR];
 #pragma unroll
-  for (int r = 0; r < 64 * 16 / kLT; ++r) {
+  for (int r = 0; r < kRR; ++r) {
     const int e = tid + r * kLT, j = e >> 4, c0 = 8 * (e & 15);
     const bool live = j < Cc;
     const long o = tok(a, b, t0 + (live ? j : 0), h) * 128 + c0;
-    *reinterpret_cast<uint4*>(sKr + j * cKRS + c0) =
-        live ? *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.k) + o) : make_uint4(0u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(sQr + j * cKRS + c0) =
-        live ? *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + o) : make_uint4(0u, 0u, 0u, 0u);
+    rk[r] = live ? *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.k) + o) : make_uint4(0u, 0u, 0u, 0u);
+    rq[r] = live ? *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + o) : make_uint4(0u, 0u, 0u, 0u);
   }
   for (int e = tid; e < 64 * 32; e += kLT) {
     const int j = e >> 5, c4 = 4 * (e & 31);
@@ -1614,6 +1615,12 @@ __global__ void __launch_bounds__(kLT, 1)
   }
   if (tid < 64) s_eta[tid] = (!kGainK && tid < Cc) ? a.eta[tok(a, b, t0 + tid, h)] : 0.f;
   for (int e = tid; e < 64 * 128; e += kLT) sDW[(e >> 7) * cLDK + (e & 127)] = 0.f;
+#pragma unroll
+  for (int r = 0; r < kRR; ++r) {
+    const int e = tid + r * kLT, j = e >> 4, c0 = 8 * (e & 15);
+    *reinterpret_cast<uint4*>(sKr + j * cKRS + c0) = rk[r];
+    *reinterpret_cast<uint4*>(sQr + j * cKRS + c0) = rq[r];
+  }
   cpa_wait_all();
   __syncthreads();
   {   // norms: eight threads per row
