@@ -786,7 +786,9 @@ enum {
   C_COUNT
 };
 
-template <int MODE>
+// SAVE: the backward's rerun, which also stores every chunk-start state and E (a
+// separate instantiation, so the forward's code carries none of it)
+template <int MODE, bool SAVE>
 __global__ void __launch_bounds__(kCarryThreads, 1)
     chunk_carry_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, FwdArgs a,
@@ -977,7 +979,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
 
     for (int c = 0; c < NC; ++c) {
       const int slot = c & 1;
-      if (a.save_S) {   // backward: the state at this chunk's start, as [32 column
+      if (SAVE) {   // backward: the state at this chunk's start, as [32 column
                         // quads][128 rows][4] (a warp's rows side by side: 512-byte stores)
         float* dst = a.save_S + ((size_t)bh * NCt + c0 + c) * 16384 + 4 * srow;
 #pragma unroll
@@ -1026,7 +1028,7 @@ __global__ void __launch_bounds__(kCarryThreads, 1)
             kv[e] += p.x; kv[e + 1] += p.y; kv[e + 2] += p.z; kv[e + 3] += p.w;
           }
         }
-        if (a.save_E) {   // backward: E(c), this thread's row and 16 columns, as
+        if (SAVE) {   // backward: E(c), this thread's row and 16 columns, as
                           // [32 column quads][64 rows][4]
           float* dst = a.save_E + ((size_t)bh * NCt + c0 + c) * 8192 + 4 * erow;
 #pragma unroll
@@ -1489,15 +1491,22 @@ cudaError_t launch_chunk_tc_split(const FwdArgs& a, void* workspace, cudaStream_
   DR_PREP(DR_GDN) else DR_PREP(DR_KLA) else DR_PREP(DR_PGDN) else return cudaErrorInvalidValue;
 #undef DR_PREP
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-#define DR_CARRY(M_)                                                                       \
+#define DR_CARRY1(M_, S_)                                                                  \
   {                                                                                        \
-    e = cudaFuncSetAttribute(chunk_carry_kernel<M_>,                                       \
+    e = cudaFuncSetAttribute(chunk_carry_kernel<M_, S_>,                                   \
                              cudaFuncAttributeMaxDynamicSharedMemorySize,                  \
                              (int)CarryMap<M_>::bytes);                                    \
     if (e != cudaSuccess) return e;                                                        \
-    chunk_carry_kernel<M_><<<a.B * a.H * 2, kCarryThreads, CarryMap<M_>::bytes, st>>>(     \
+    chunk_carry_kernel<M_, S_><<<a.B * a.H * 2, kCarryThreads, CarryMap<M_>::bytes, st>>>( \
         mq, mk, mv, a, ws);                                                                \
   }
+#define DR_CARRY(M_)                   \
+  if (a.save_S && a.save_E)            \
+    DR_CARRY1(M_, true)                \
+  else if (!a.save_S && !a.save_E)     \
+    DR_CARRY1(M_, false)               \
+  else                                 \
+    return cudaErrorInvalidValue;
   const int NC = (a.T + 63) / 64;
   int G, Ls;
   if (!a.save_S && seg_plan(nsm, (long)a.B * a.H, NC, &G, &Ls)) {
@@ -1511,15 +1520,15 @@ cudaError_t launch_chunk_tc_split(const FwdArgs& a, void* workspace, cudaStream_
     s3.seg_pass = 2;
 #define DR_CARRY_SEG(M_)                                                                   \
   {                                                                                        \
-    e = cudaFuncSetAttribute(chunk_carry_kernel<M_>,                                       \
+    e = cudaFuncSetAttribute(chunk_carry_kernel<M_, false>,                                \
                              cudaFuncAttributeMaxDynamicSharedMemorySize,                  \
                              (int)CarryMap<M_>::bytes);                                    \
     if (e != cudaSuccess) return e;                                                        \
-    chunk_carry_kernel<M_><<<a.B * a.H * (2 + 4 * (G - 2)), kCarryThreads,                 \
-                             CarryMap<M_>::bytes, st>>>(mq, mk, mv, s1, ws);               \
+    chunk_carry_kernel<M_, false><<<a.B * a.H * (2 + 4 * (G - 2)), kCarryThreads,          \
+                                    CarryMap<M_>::bytes, st>>>(mq, mk, mv, s1, ws);        \
     seg_compose_kernel<<<a.B * a.H * 4, 256, 0, st>>>(s1);                                 \
-    chunk_carry_kernel<M_><<<a.B * a.H * 2 * (G - 1), kCarryThreads,                       \
-                             CarryMap<M_>::bytes, st>>>(mq, mk, mv, s3, ws);               \
+    chunk_carry_kernel<M_, false><<<a.B * a.H * 2 * (G - 1), kCarryThreads,                \
+                                    CarryMap<M_>::bytes, st>>>(mq, mk, mv, s3, ws);        \
   }
     if (a.variant == DR_PGDN) DR_CARRY_SEG(1) else DR_CARRY_SEG(0)
 #undef DR_CARRY_SEG
