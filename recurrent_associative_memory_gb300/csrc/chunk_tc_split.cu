@@ -257,12 +257,21 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         // bounded map B(A) and the write keys w = eta B(A) . k^ (PDN notes Eq. (9)),
         // as bf16 hi/lo [64 tokens][128] tiles in the T region: the Gram's B operand
         // and the carry's dS operand (one bulk copy into the record)
-        if (ptid < 128) {
-          const int ch = ptid, kb = ch >> 6, col = ch & 63;
+        {   // two threads per channel: tokens 0-31 and 32-63 (the second runs the
+            // statistic's recurrence over the first half to its own start)
+          const int ch = ptid & 127, hf = ptid >> 7, kb = ch >> 6, col = ch & 63;
           const float mu_h = a.mu[(t / NC) % a.H];
           float A = reinterpret_cast<const float*>(rec + rAux)[256 + ch];
           uint8_t* Wt = sm + pT;
-          for (int i0 = 0; i0 < 64; i0 += 8) {
+          if (hf) {
+#pragma unroll 8
+            for (int i = 0; i < 32; ++i) {
+              const float kx = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                                   KQ + kb * 16384 + sw128_offset(i, col))) * vcr[i];
+              A = vaP[i] * A + vbP[i] * kx * kx;
+            }
+          }
+          for (int i0 = 32 * hf; i0 < 32 * hf + 32; i0 += 8) {
             float kv[8], Av[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
