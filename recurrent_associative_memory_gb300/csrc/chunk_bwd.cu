@@ -1119,6 +1119,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                            ~static_cast<uintptr_t>(1023));
   float* sD = reinterpret_cast<float*>(sm + lD);
   float* sX = reinterpret_cast<float*>(sm + lX);
+  float* sX2 = reinterpret_cast<float*>(sm + lW);   // scalar decay: after the products, IW is free
   uint16_t* sKr = reinterpret_cast<uint16_t*>(sm + lR);
   uint16_t* sQr = sKr + 64 * cKR;
   __shared__ uint64_t bar;
@@ -1362,14 +1363,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_ld16(tl + tG1 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(v + 16));
       tmem_ld_wait();
       const int i = trow & 63;
-      if (trow < 64) {
+      float m[32];   // this row's 32 IM entries, hi + lo, eight per 16-byte read
 #pragma unroll
-        for (int e = 0; e < 32; ++e) sX[i * 65 + 32 * hc + e] = hl(lM, 16384, trow, 32 * hc + e) * v[e];
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t o = lM + sw128_offset(trow, 32 * hc + 8 * q);
+        float mh[8], ml[8];
+        unpack8(*reinterpret_cast<const uint4*>(sm + o), mh);
+        unpack8(*reinterpret_cast<const uint4*>(sm + o + 16384), ml);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m[8 * q + e] = mh[e] + ml[e];
       }
-      __syncthreads();
-      if (trow >= 64) {
+      if (!PG) {   // query rows into sX, key rows into sX2 (the consumed IW images)
+        float* dst = (trow < 64 ? sX : sX2) + i * 65 + 32 * hc;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) sX[i * 65 + 32 * hc + e] += hl(lM, 16384, trow, 32 * hc + e) * v[e];
+        for (int e = 0; e < 32; ++e) dst[e] = m[e] * v[e];
+      } else {     // PGDN reads its IW images below: the halves meet in sX in turn
+        if (trow < 64) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sX[i * 65 + 32 * hc + e] = m[e] * v[e];
+        }
+        __syncthreads();
+        if (trow >= 64) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sX[i * 65 + 32 * hc + e] += m[e] * v[e];
+        }
       }
     }
     // ---- G2: dw_jc = (dw^T)_cj + e^{G-g_j} X_W,jc, transposed into sD (lane = channel);
@@ -1413,12 +1430,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
     if (tid < 64) {   // each Gram entry adds to dg of its row and takes from dg of its column
       float r = 0.f;
-      for (int j = 0; j < 64; ++j) r += sX[tid * 65 + j];
+      for (int j = 0; j < 64; ++j) r += PG ? sX[tid * 65 + j] : sX[tid * 65 + j] + sX2[tid * 65 + j];
       s_dgr[tid] = r;
     } else if (tid < 128) {
       const int j = tid - 64;
       float cs = 0.f;
-      for (int i = 0; i < 64; ++i) cs += sX[i * 65 + j];
+      for (int i = 0; i < 64; ++i) cs += PG ? sX[i * 65 + j] : sX[i * 65 + j] + sX2[i * 65 + j];
       s_dgx[j] = cs;
     } else if (tid < 192) {   // d beta_j and e^{G-g_j} X_W,j . w_j from the quadrants' parts
       const int j = tid - 128;
@@ -1454,13 +1471,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld16(tl + tG3 + 64 * hc + 32 * p + 16, *reinterpret_cast<float(*)[16]>(v + 16));
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < 8; ++e) {   // four columns: the raw row and dw as 8- and 16-byte reads
           const float xs[4] = {x4[e].x, x4[e].y, x4[e].z, x4[e].w};
+          const uint2 r2 = *reinterpret_cast<const uint2*>(rr + 32 * p + 4 * e);
+          const float xr[4] = {__uint_as_float(r2.x << 16), __uint_as_float(r2.x & 0xFFFF0000u),
+                               __uint_as_float(r2.y << 16), __uint_as_float(r2.y & 0xFFFF0000u)};
+          const float4 sd4 = isk ? *reinterpret_cast<const float4*>(sD + i * cLDK + 64 * hc + 32 * p + 4 * e)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float sdv[4] = {sd4.x, sd4.y, sd4.z, sd4.w};
 #pragma unroll
           for (int f = 0; f < 4; ++f) {
             const int cc = 32 * p + 4 * e + f;
-            const float xh = bf(rr[cc]) * sc;
-            const float val = isk ? v[4 * e + f] - eg * xs[f] + bgain * sD[i * cLDK + 64 * hc + cc] + ds2 * xh
+            const float xh = xr[f] * sc;
+            const float val = isk ? v[4 * e + f] - eg * xs[f] + bgain * sdv[f] + ds2 * xh
                                   : v[4 * e + f] + eg * xs[f];
             d[cc] = val;
             dot += val * xh;
@@ -1477,9 +1500,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int cc = 0; cc < 64; cc += 4) {
           float o4[4];
+          const uint2 r2 = *reinterpret_cast<const uint2*>(rr + cc);
+          const float xr[4] = {__uint_as_float(r2.x << 16), __uint_as_float(r2.x & 0xFFFF0000u),
+                               __uint_as_float(r2.y << 16), __uint_as_float(r2.y & 0xFFFF0000u)};
 #pragma unroll
           for (int f = 0; f < 4; ++f) {
-            const float xh = bf(rr[cc + f]) * sc;
+            const float xh = xr[f] * sc;
             o4[f] = norm ? (d[cc + f] - xh * dot) * sc : d[cc + f];
           }
           *xpiece(16 * hc + cc / 4) = make_float4(o4[0], o4[1], o4[2], o4[3]);
