@@ -1777,9 +1777,15 @@ __global__ void __launch_bounds__(kLT, 1)
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = 16 * mt + frag_row(lane, e), cc = 8 * (nt0 + nt) + frag_col(lane, e);
-          sDW[j * cLDK + cc] += d2[nt][e] * __expf(sG[m * cLDK + cc] - sG[j * cLDK + cc]);
+        for (int hh = 0; hh < 2; ++hh) {   // a lane's two adjacent columns as 8-byte accesses
+          const int j = 16 * mt + frag_row(lane, 2 * hh), cc = 8 * (nt0 + nt) + frag_col(lane, 0);
+          const float2 gm = *reinterpret_cast<const float2*>(sG + m * cLDK + cc);
+          const float2 gj = *reinterpret_cast<const float2*>(sG + j * cLDK + cc);
+          float2* dp = reinterpret_cast<float2*>(sDW + j * cLDK + cc);
+          float2 dv = *dp;
+          dv.x += d2[nt][2 * hh] * __expf(gm.x - gj.x);
+          dv.y += d2[nt][2 * hh + 1] * __expf(gm.y - gj.y);
+          *dp = dv;
         }
     }
     __syncthreads();
